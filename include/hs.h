@@ -1,0 +1,181 @@
+/*
+ * hs.h -- C ABI of the Hybrid HiSparse top-K resolver for sparse-MLA decode.
+ *
+ * Operations (each one cites the passage of the source pages that defines it):
+ *
+ *   hs_resolve_topk   the fused per-step top-K resolver.  "vLLM GLM 5.3 Optimizations: Hybrid
+ *                     HiSparse Offloading", section "Technical Implementation of Hybrid HiSparse",
+ *                     item 2 (Mixed residency): resident tokens are read in place, hot tokens are read
+ *                     and their LRU entry refreshed, a miss copies a single row from pinned host memory
+ *                     into an LRU slot; the same article in Japanese (news.ainew.jp), section
+ *                     "仕組み" (How it works), which adds that nothing on the decode path waits for a
+ *                     CPU decision, so the step stays CUDA-graph capturable.
+ *   hs_gather_rows    the single-stride gather by pool row id.  Japanese article, section "仕組み":
+ *                     whether a row sits in a resident page or in the hot buffer, the resolver hands
+ *                     back pool (HMA) row ids and they are gathered with one stride.
+ *   hs_offload_pages  the post-forward proactive copy.  English page, section "Key Architectural
+ *                     Details" (Proactive Copying, Lightweight Execution): completed prefix pages are
+ *                     copied to CPU memory while the GPU keeps serving them, all sparse-MLA layers in a
+ *                     single launch after the forward pass, ordered on the model's GPU stream.
+ *   hs_hot_reset      empties hot buffers (the buffer is leased empty for a new request: Japanese
+ *                     article, section "仕組み", "No residency" state).
+ *
+ * Conventions shared by every call
+ *   - The caller owns all memory (device buffers, pinned host pool, workspace) and all streams.
+ *     No call allocates device or pinned memory; hs_pool_create allocates only its small host struct.
+ *   - resolve / gather / offload / reset are asynchronous on the given stream: they validate what the
+ *     host can see, launch, and return.  They never synchronise the device.
+ *   - The return value reports host-checkable argument errors (HS_ERR_INVALID_ARG) and launch
+ *     failures (HS_ERR_CUDA).  Data errors found on the device are written to device status words
+ *     (out_stats for the resolver, an optional status word for gather/offload); they never trap.
+ *   - Stream ordering is the only synchronisation: gather after resolve on the same stream; reuse of a
+ *     GPU block after hs_offload_pages on the same stream; readers of host copies on another stream
+ *     wait for an event recorded after the offload.
+ *   - Layout: row id = gpu_block * page_size + offset (int32); the bytes of a row in layer l live at
+ *     gpu_layer_base[l] + (int64)row * row_bytes.  Host pool rows likewise with host blocks.
+ *   - Data-error precedence inside one (layer, request) unit, highest first:
+ *     HS_ERR_STEP_ORDER, HS_ERR_ID_RANGE, HS_ERR_TABLE_RANGE, HS_ERR_MISSING_ROW, HS_ERR_CAPACITY.
+ */
+#ifndef HS_H_
+#define HS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (ABI-identical to cudaStream_t / CUstream).  NULL = the legacy default stream. */
+typedef struct CUstream_st* hs_stream_t;
+
+typedef enum {
+  HS_OK = 0,
+  HS_ERR_INVALID_ARG = 1,  /* host-visible argument error; nothing was launched                  */
+  HS_ERR_ID_RANGE = 2,     /* a top-K id < -1, >= ctx_len[r], or on a page >= max_pages;
+                              gather: a row id outside [-1, num_gpu_blocks*page_size)            */
+  HS_ERR_MISSING_ROW = 3,  /* a miss on a placeholder page that has no host copy                  */
+  HS_ERR_CAPACITY = 4,     /* more misses than evictable hot slots this step                      */
+  HS_ERR_STEP_ORDER = 5,   /* step is older than a stamp already in the hot state                 */
+  HS_ERR_CUDA = 6,         /* a CUDA runtime call or launch failed                                */
+  HS_ERR_TIMEOUT = 7,      /* reserved: a bounded device wait gave up (no call waits today)       */
+  HS_ERR_TABLE_RANGE = 8   /* a block-table, host-block-table or hot-block entry that the step
+                              dereferences lies outside the pool; offload: a pair out of range    */
+} hs_status;
+
+/* Limits of this build.  Each launch's shared-memory footprint is also checked (see
+ * hs_resolve_smem_bytes); a shape that does not fit returns HS_ERR_INVALID_ARG. */
+#define HS_MAX_LAYERS 128
+#define HS_MAX_PAGE_SIZE 1024
+#define HS_MAX_CAPACITY 16384   /* hot rows per (layer, request) */
+#define HS_MAX_PLAN 16384       /* P * K ids per (layer, request) */
+
+typedef struct hs_pool hs_pool; /* opaque: geometry and the per-layer base pointers only */
+
+typedef struct {
+  int32_t num_layers;      /* sparse-MLA layers, 1..HS_MAX_LAYERS                                   */
+  int32_t page_size;       /* tokens per page (block), 1..HS_MAX_PAGE_SIZE                          */
+  int32_t row_bytes;       /* bytes of one KV row, > 0 and a multiple of 16 (656 for FP8 MLA rows)  */
+  int32_t num_gpu_blocks;  /* blocks per layer in the GPU pool; num_gpu_blocks*page_size < 2^31     */
+  int32_t num_host_blocks; /* blocks per layer in the pinned host pool (may be 0)                   */
+  /* [num_layers] device pointers, each to [num_gpu_blocks][page_size][row_bytes] bytes,
+   * 16-byte aligned.  Resident pages and leased hot blocks live in these same tensors. */
+  void* const* gpu_layer_base;
+  /* [num_layers] pinned (page-locked, device-mapped) host pointers, each to
+   * [num_host_blocks][page_size][row_bytes] bytes, 16-byte aligned.  May be NULL when
+   * num_host_blocks == 0. */
+  void* const* host_layer_base;
+} hs_pool_desc;
+
+/* Per-request LRU hot buffers.  The blocks are ordinary pool blocks leased by the caller and are
+ * shared by all layers (each layer's copy lives in that layer's tensor); the token/stamp state is
+ * per (layer, request) because each layer has its own top-K.  Slot v of request r is pool row
+ * hot_blocks[r][v / page_size] * page_size + v % page_size. */
+typedef struct {
+  int32_t capacity;          /* C rows per (layer, request): a multiple of page_size,
+                                page_size..HS_MAX_CAPACITY; the pages' default is 2*K            */
+  const int32_t* hot_blocks; /* device int32 [R][capacity/page_size]; every entry must be a pool
+                                block in [0, num_gpu_blocks), disjoint across requests and from
+                                every resident block (not checked for overlap)                   */
+  int32_t* slot_token;       /* device int32 [num_layers][R][capacity]; -1 = empty slot          */
+  int32_t* slot_stamp;       /* device int32 [num_layers][R][capacity]; last step that used the
+                                slot, -1 = never                                                  */
+} hs_hot_state;
+
+/* Validates the geometry and the pointers (device pointers must be device memory, host pointers
+ * pinned and device-mapped), copies the pointer arrays, and returns a handle in *out.  Needs a
+ * current CUDA device.  Returns HS_ERR_INVALID_ARG or HS_ERR_CUDA on failure (*out = NULL). */
+hs_status hs_pool_create(const hs_pool_desc* desc, hs_pool** out);
+void hs_pool_destroy(hs_pool* pool);
+
+/* Sets slot_token and slot_stamp of all num_layers x R x capacity slots to -1 (async). */
+hs_status hs_hot_reset(const hs_pool* pool, const hs_hot_state* hot, int32_t R, hs_stream_t stream);
+
+/* Bytes of caller-owned device workspace that hs_resolve_topk needs for this shape (the per-unit
+ * miss lists handed from the resolver kernel to the miss-copy kernel).  0 on a bad shape. */
+size_t hs_resolve_workspace_bytes(int32_t nl, int32_t R, int32_t P, int32_t K, int32_t capacity);
+
+/* Dynamic shared memory one resolver CTA needs for this shape, or 0 if the shape exceeds a limit. */
+size_t hs_resolve_smem_bytes(int32_t P, int32_t K, int32_t capacity);
+
+/* The fused top-K resolver for layers [layer_begin, layer_begin + nl) and R requests at decode
+ * step `step`.  One (layer, request) pair is one independent unit:
+ *   plan      the distinct non-padding ids of topk_ids[l][r][0..P)[0..K) in first-occurrence order
+ *             (position-major, then top-K order); all P query positions of a step share it;
+ *   resident  block_table[r][id/page_size] >= 0: row = that block * page_size + id % page_size,
+ *             read in place (wins over a stale hot copy);
+ *   hit       the id sits in a hot slot: row = the slot's pool row; its stamp becomes `step`;
+ *   miss      otherwise: the j-th miss in plan order takes the j-th smallest (stamp, slot) among
+ *             slots whose stamp is < step and that were not hit in this call; exactly one row is
+ *             copied from the pinned host pool (host_block_table[r][id/page_size]) into the slot,
+ *             whose token becomes id and stamp `step`.
+ * Arguments (all device pointers):
+ *   topk_ids         int32 [nl][R][P][K]; -1 = padding (row -1).
+ *   block_table      int32 [R][max_pages]; < 0 = placeholder page (not resident).
+ *   host_block_table int32 [R][max_pages]; < 0 = no host copy.
+ *   ctx_len          int32 [R]; ids must be < ctx_len[r].
+ *   out_rows         int32 [nl][R][P][K]; pool row per id (duplicates share the row; padding -1).
+ *   out_stats        int32 [nl][R][4] = {status, resident, hits, misses}, counted over the plan.
+ *   workspace        device scratch of >= hs_resolve_workspace_bytes(...) bytes, 16-byte aligned;
+ *                    its contents need no initialisation and are garbage after the call.
+ * A unit with a data error leaves its hot state and pool bytes unchanged, sets out_rows to -1 and
+ * out_stats to {code, 0, 0, 0}; other units proceed.  Calling again with the same ids and step
+ * returns the same rows with 0 misses (the replayable plan used by speculative decoding).
+ * Launches two kernels on `stream` (resolve, then the miss copy).  Concurrent calls that share hot
+ * state or workspace must be ordered by the caller. */
+hs_status hs_resolve_topk(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P,
+                          int32_t K, const int32_t* topk_ids, const int32_t* block_table,
+                          const int32_t* host_block_table, const int32_t* ctx_len, int32_t max_pages,
+                          const hs_hot_state* hot, int32_t step, int32_t* out_rows, int32_t* out_stats,
+                          void* workspace, size_t workspace_bytes, hs_stream_t stream);
+
+/* Single-stride gather: out[l][i] = row rows[l][i] of layer layer_begin + l, for l < nl, i < n.
+ *   rows        device int32 [nl][n]; -1 gives row_bytes zero bytes.
+ *   out         device [nl][n][row_bytes] bytes, 16-byte aligned.
+ *   out_status  optional device int32 (may be NULL): set to HS_ERR_ID_RANGE when a row id is
+ *               outside [-1, num_gpu_blocks*page_size) (that output row is zero-filled); never
+ *               written otherwise, so the caller zeroes it. */
+hs_status hs_gather_rows(const hs_pool* pool, int32_t layer_begin, int32_t nl, const int32_t* rows,
+                         int64_t n, void* out, int32_t* out_status, hs_stream_t stream);
+
+/* Post-forward proactive offload, one launch for all layers: for every pair i < n and every layer
+ * l, host page host_blocks[i] of layer l := GPU page gpu_blocks[i] of layer l (page_size*row_bytes
+ * bytes).  The GPU block may be reused by later work on the same stream as soon as this call
+ * returns; the host copy is complete when the stream reaches this point.
+ *   gpu_blocks, host_blocks  device int32 [n].
+ *   out_status  optional device int32: set to HS_ERR_TABLE_RANGE if a pair is out of range (that
+ *               pair is skipped). */
+hs_status hs_offload_pages(const hs_pool* pool, const int32_t* gpu_blocks, const int32_t* host_blocks,
+                           int32_t n, int32_t* out_status, hs_stream_t stream);
+
+/* Static description of a status code. */
+const char* hs_status_str(hs_status s);
+
+/* Number of kernels the library has launched since load (a host-side counter). */
+int64_t hs_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HS_H_ */
