@@ -1,0 +1,313 @@
+"""Hybrid HiSparse top-K resolver for sparse-MLA decode, GB300-native (sm_103a).
+
+Thin Python binding over the C ABI in include/hs.h (libhs.so, built in-tree by _build.py).  This
+module only marshals arguments: torch tensors are passed as raw pointers and the current torch
+CUDA stream as the launch stream.  Every step of the path runs in the library's CUDA kernels; there
+is no CPU fallback, and every call raises if the library is missing or returns an error.
+
+Operations (the passages that define them are cited in include/hs.h):
+  resolve_topk   fused per-step top-K resolver (resident / hot hit / one-row miss copy)
+  gather_rows    single-stride gather of resolved pool rows
+  offload_pages  post-forward proactive copy of completed pages, all layers in one launch
+  hot_reset      empty the hot buffers
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libhs.so")
+
+HS_OK = 0
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "ID_RANGE", 3: "MISSING_ROW", 4: "CAPACITY", 5: "STEP_ORDER",
+                6: "CUDA", 7: "TIMEOUT", 8: "TABLE_RANGE"}
+MAX_LAYERS = 128
+
+
+class HSError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(code, code)} ({status_str(code)})")
+        self.code = code
+
+
+class PoolDesc(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("page_size", ctypes.c_int32), ("row_bytes", ctypes.c_int32),
+                ("num_gpu_blocks", ctypes.c_int32), ("num_host_blocks", ctypes.c_int32),
+                ("gpu_layer_base", ctypes.POINTER(ctypes.c_void_p)),
+                ("host_layer_base", ctypes.POINTER(ctypes.c_void_p))]
+
+
+class HotStateC(ctypes.Structure):
+    _fields_ = [("capacity", ctypes.c_int32), ("hot_blocks", ctypes.c_void_p), ("slot_token", ctypes.c_void_p),
+                ("slot_stamp", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libhs.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with sparse_mla_kv_gb300._build.build() "
+                               "(there is no fallback implementation)")
+        L = ctypes.CDLL(LIB_PATH)
+        i32, i64, sz, p = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
+        L.hs_status_str.restype = ctypes.c_char_p
+        L.hs_status_str.argtypes = [i32]
+        L.hs_launch_count.restype = i64
+        L.hs_launch_count.argtypes = []
+        L.hs_pool_create.restype = i32
+        L.hs_pool_create.argtypes = [ctypes.POINTER(PoolDesc), ctypes.POINTER(p)]
+        L.hs_pool_destroy.restype = None
+        L.hs_pool_destroy.argtypes = [p]
+        L.hs_hot_reset.restype = i32
+        L.hs_hot_reset.argtypes = [p, ctypes.POINTER(HotStateC), i32, p]
+        L.hs_resolve_workspace_bytes.restype = sz
+        L.hs_resolve_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+        L.hs_resolve_smem_bytes.restype = sz
+        L.hs_resolve_smem_bytes.argtypes = [i32, i32, i32]
+        L.hs_resolve_topk.restype = i32
+        L.hs_resolve_topk.argtypes = [p, i32, i32, i32, i32, i32, p, p, p, p, i32, ctypes.POINTER(HotStateC), i32, p, p,
+                                      p, sz, p]
+        L.hs_gather_rows.restype = i32
+        L.hs_gather_rows.argtypes = [p, i32, i32, p, i64, p, p, p]
+        L.hs_offload_pages.restype = i32
+        L.hs_offload_pages.argtypes = [p, p, p, i32, p, p]
+        _lib = L
+    return _lib
+
+
+def status_str(code: int) -> str:
+    try:
+        return lib().hs_status_str(int(code)).decode()
+    except RuntimeError:
+        return STATUS_NAMES.get(code, str(code))
+
+
+def launch_count() -> int:
+    """Kernels the library has launched in this process."""
+    return int(lib().hs_launch_count())
+
+
+def _check(code: int, what: str) -> None:
+    if code != HS_OK:
+        raise HSError(code, what)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev_i32(t: torch.Tensor, name: str) -> ctypes.c_void_p:
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous int32 CUDA tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _opt(t: Optional[torch.Tensor], name: str) -> Optional[ctypes.c_void_p]:
+    return None if t is None else _dev_i32(t, name)
+
+
+class Pool:
+    """Geometry and base pointers of the paged KV pool: per layer one GPU tensor
+    [num_gpu_blocks, page_size, row_bytes] (resident pages and leased hot blocks share it) and one
+    pinned host tensor [num_host_blocks, page_size, row_bytes].  The tensors stay owned by the caller;
+    this object keeps references so they outlive the handle."""
+
+    def __init__(self, gpu_layers: Sequence[torch.Tensor], host_layers: Optional[Sequence[torch.Tensor]] = None):
+        if not gpu_layers or len(gpu_layers) > MAX_LAYERS:
+            raise ValueError("need 1..128 layers")
+        g0 = gpu_layers[0]
+        if g0.dim() != 3:
+            raise ValueError("GPU layer tensors must be [num_gpu_blocks, page_size, row_bytes]")
+        self.num_gpu_blocks, self.page_size, self.row_bytes = (int(x) for x in g0.shape)
+        self.num_layers = len(gpu_layers)
+        for t in gpu_layers:
+            if t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != tuple(g0.shape):
+                raise TypeError("GPU layer tensors must be contiguous uint8 CUDA tensors of one shape")
+        host_layers = list(host_layers or [])
+        self.num_host_blocks = int(host_layers[0].shape[0]) if host_layers else 0
+        if host_layers:
+            if len(host_layers) != self.num_layers:
+                raise ValueError("one host tensor per layer")
+            for t in host_layers:
+                if (t.dtype != torch.uint8 or t.is_cuda or not t.is_pinned() or not t.is_contiguous()
+                        or tuple(t.shape) != (self.num_host_blocks, self.page_size, self.row_bytes)):
+                    raise TypeError("host layer tensors must be contiguous pinned uint8 CPU tensors "
+                                    "[num_host_blocks, page_size, row_bytes]")
+        self.gpu_layers = list(gpu_layers)
+        self.host_layers = host_layers
+        gp = (ctypes.c_void_p * self.num_layers)(*[t.data_ptr() for t in gpu_layers])
+        hp = (ctypes.c_void_p * self.num_layers)(*[t.data_ptr() for t in host_layers]) if host_layers else None
+        desc = PoolDesc(self.num_layers, self.page_size, self.row_bytes, self.num_gpu_blocks, self.num_host_blocks,
+                        ctypes.cast(gp, ctypes.POINTER(ctypes.c_void_p)),
+                        ctypes.cast(hp, ctypes.POINTER(ctypes.c_void_p)) if hp is not None else None)
+        h = ctypes.c_void_p()
+        with torch.cuda.device(g0.device):
+            _check(lib().hs_pool_create(ctypes.byref(desc), ctypes.byref(h)), "hs_pool_create")
+        self.handle = h
+
+    def close(self) -> None:
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            lib().hs_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class HotState:
+    """Per-request hot buffers: leased block ids [R][C/page_size] (shared by all layers) and the
+    per-(layer, request) slot token/stamp arrays [num_layers][R][C] (-1 = empty / never used)."""
+
+    def __init__(self, capacity: int, hot_blocks: torch.Tensor, slot_token: torch.Tensor, slot_stamp: torch.Tensor):
+        self.capacity = int(capacity)
+        self.hot_blocks, self.slot_token, self.slot_stamp = hot_blocks, slot_token, slot_stamp
+        self.c = HotStateC(self.capacity, _dev_i32(hot_blocks, "hot_blocks"), _dev_i32(slot_token, "slot_token"),
+                           _dev_i32(slot_stamp, "slot_stamp"))
+
+    @classmethod
+    def allocate(cls, num_layers: int, hot_blocks: torch.Tensor, capacity: int) -> "HotState":
+        R = int(hot_blocks.shape[0])
+        dev = hot_blocks.device
+        tok = torch.empty((num_layers, R, capacity), dtype=torch.int32, device=dev)
+        st = torch.empty((num_layers, R, capacity), dtype=torch.int32, device=dev)
+        return cls(capacity, hot_blocks, tok, st)
+
+    @property
+    def R(self) -> int:
+        return int(self.hot_blocks.shape[0])
+
+
+def hot_reset(pool: Pool, hot: HotState, stream=None) -> None:
+    _check(lib().hs_hot_reset(pool.handle, ctypes.byref(hot.c), hot.R, _stream(stream)), "hs_hot_reset")
+
+
+def resolve_workspace_bytes(nl: int, R: int, P: int, K: int, capacity: int) -> int:
+    return int(lib().hs_resolve_workspace_bytes(nl, R, P, K, capacity))
+
+
+def resolve_smem_bytes(P: int, K: int, capacity: int) -> int:
+    return int(lib().hs_resolve_smem_bytes(P, K, capacity))
+
+
+def alloc_workspace(nl: int, R: int, P: int, K: int, capacity: int, device) -> torch.Tensor:
+    nbytes = resolve_workspace_bytes(nl, R, P, K, capacity)
+    return torch.empty(max(16, nbytes), dtype=torch.uint8, device=device)
+
+
+def resolve_topk(pool: Pool, topk: torch.Tensor, block_table: torch.Tensor, host_block_table: torch.Tensor,
+                 ctx_len: torch.Tensor, hot: HotState, step: int, *, layer_begin: int = 0,
+                 out_rows: Optional[torch.Tensor] = None, out_stats: Optional[torch.Tensor] = None,
+                 workspace: Optional[torch.Tensor] = None, stream=None):
+    """topk int32 [nl][R][P][K] -> (out_rows int32 [nl][R][P][K], out_stats int32 [nl][R][4])."""
+    if topk.dim() != 4:
+        raise ValueError("topk must be [nl][R][P][K]")
+    nl, R, P, K = (int(x) for x in topk.shape)
+    if block_table.dim() != 2 or block_table.shape[0] != R or tuple(host_block_table.shape) != tuple(block_table.shape):
+        raise ValueError("block tables must both be [R][max_pages]")
+    if hot.R != R:
+        raise ValueError("hot state has a different number of requests")
+    dev = topk.device
+    if out_rows is None:
+        out_rows = torch.empty_like(topk)
+    if out_stats is None:
+        out_stats = torch.empty((nl, R, 4), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(nl, R, P, K, hot.capacity, dev)
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda:
+        raise TypeError("workspace must be a uint8 CUDA tensor")
+    code = lib().hs_resolve_topk(pool.handle, layer_begin, nl, R, P, K, _dev_i32(topk, "topk"),
+                                 _dev_i32(block_table, "block_table"), _dev_i32(host_block_table, "host_block_table"),
+                                 _dev_i32(ctx_len, "ctx_len"), int(block_table.shape[1]), ctypes.byref(hot.c),
+                                 int(step), _dev_i32(out_rows, "out_rows"), _dev_i32(out_stats, "out_stats"),
+                                 ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream(stream))
+    _check(code, "hs_resolve_topk")
+    return out_rows, out_stats
+
+
+def gather_rows(pool: Pool, rows: torch.Tensor, *, layer_begin: int = 0, out: Optional[torch.Tensor] = None,
+                status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """rows int32 [nl][n] (or [n] for one layer) -> uint8 [nl][n][row_bytes] (or [n][row_bytes])."""
+    squeeze = rows.dim() == 1
+    r2 = rows.reshape(1, -1) if squeeze else rows.reshape(rows.shape[0], -1)
+    nl, n = int(r2.shape[0]), int(r2.shape[1])
+    if out is None:
+        out = torch.empty((nl, n, pool.row_bytes), dtype=torch.uint8, device=rows.device)
+    if out.dtype != torch.uint8 or not out.is_cuda or not out.is_contiguous() or out.numel() != nl * n * pool.row_bytes:
+        raise TypeError("out must be a contiguous uint8 CUDA tensor of nl*n*row_bytes bytes")
+    code = lib().hs_gather_rows(pool.handle, layer_begin, nl, _dev_i32(r2, "rows"), n, ctypes.c_void_p(out.data_ptr()),
+                                _opt(status, "status"), _stream(stream))
+    _check(code, "hs_gather_rows")
+    return out.reshape(n, pool.row_bytes) if squeeze else out
+
+
+def offload_pages(pool: Pool, gpu_blocks: torch.Tensor, host_blocks: torch.Tensor, *,
+                  status: Optional[torch.Tensor] = None, stream=None) -> None:
+    n = int(gpu_blocks.numel())
+    if int(host_blocks.numel()) != n:
+        raise ValueError("gpu_blocks and host_blocks differ in length")
+    if n == 0:
+        return
+    code = lib().hs_offload_pages(pool.handle, _dev_i32(gpu_blocks, "gpu_blocks"), _dev_i32(host_blocks, "host_blocks"),
+                                  n, _opt(status, "status"), _stream(stream))
+    _check(code, "hs_offload_pages")
+
+
+class PreparedStep:
+    """Pre-marshalled resolve / gather / offload calls over one fixed set of device buffers, for a
+    decode loop: per call only the top-K pointer and the step number change.  Still just the C ABI;
+    this only avoids rebuilding ctypes arguments every step."""
+
+    def __init__(self, pool: Pool, hot: HotState, block_table: torch.Tensor, host_block_table: torch.Tensor,
+                 ctx_len: torch.Tensor, out_rows: torch.Tensor, out_stats: torch.Tensor, workspace: torch.Tensor,
+                 gather_out: torch.Tensor, *, layer_begin: int = 0, gather_status: Optional[torch.Tensor] = None,
+                 stream=None):
+        nl, R, P, K = (int(x) for x in out_rows.shape)
+        self.shape = (nl, R, P, K)
+        self.pool, self.hot = pool, hot
+        self._keep = (block_table, host_block_table, ctx_len, out_rows, out_stats, workspace, gather_out, gather_status)
+        self.L = lib()
+        self.stream = _stream(stream)
+        self.lb = int(layer_begin)
+        self.max_pages = int(block_table.shape[1])
+        self.args_bt = (_dev_i32(block_table, "block_table"), _dev_i32(host_block_table, "host_block_table"),
+                        _dev_i32(ctx_len, "ctx_len"))
+        self.rows = _dev_i32(out_rows, "out_rows")
+        self.stats = _dev_i32(out_stats, "out_stats")
+        self.ws = ctypes.c_void_p(workspace.data_ptr())
+        self.ws_n = workspace.numel()
+        self.gout = ctypes.c_void_p(gather_out.data_ptr())
+        self.gstatus = _opt(gather_status, "gather_status")
+        self.n_per_layer = R * P * K
+        if gather_out.numel() != nl * self.n_per_layer * pool.row_bytes:
+            raise ValueError("gather_out must hold nl*R*P*K rows")
+
+    def resolve(self, topk: torch.Tensor, step: int) -> None:
+        nl, R, P, K = self.shape
+        if tuple(topk.shape) != self.shape:
+            raise ValueError("topk shape differs from the prepared shape")
+        _check(self.L.hs_resolve_topk(self.pool.handle, self.lb, nl, R, P, K, _dev_i32(topk, "topk"), *self.args_bt,
+                                      self.max_pages, ctypes.byref(self.hot.c), int(step), self.rows, self.stats,
+                                      self.ws, self.ws_n, self.stream), "hs_resolve_topk")
+
+    def gather(self) -> None:
+        _check(self.L.hs_gather_rows(self.pool.handle, self.lb, self.shape[0], self.rows, self.n_per_layer, self.gout,
+                                     self.gstatus, self.stream), "hs_gather_rows")
+
+    def offload(self, gpu_blocks: torch.Tensor, host_blocks: torch.Tensor, n: int) -> None:
+        if n:
+            _check(self.L.hs_offload_pages(self.pool.handle, _dev_i32(gpu_blocks, "gpu_blocks"),
+                                           _dev_i32(host_blocks, "host_blocks"), int(n), None, self.stream),
+                   "hs_offload_pages")

@@ -1,0 +1,219 @@
+// C ABI of the resolver library: argument validation, the pool handle, and kernel launches.
+// Every entry point is asynchronous on the caller's stream and allocates no device memory.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "hs_internal.cuh"
+
+struct hs_pool {
+  hs::PoolGeom g;
+  hs::LayerPtrs ptrs;
+  int device;
+};
+
+namespace hs {
+namespace {
+
+std::atomic<int64_t> g_launches{0};
+
+int sm_count(int dev) {
+  static std::atomic<int> cache[64];
+  if (dev < 0 || dev >= 64) return 0;
+  int v = cache[dev].load();
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return 0;
+  cache[dev].store(v);
+  return v;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+hs_status cuda_status(cudaError_t e) { return e == cudaSuccess ? HS_OK : HS_ERR_CUDA; }
+
+}  // namespace
+
+void count_launch(int k) { g_launches.fetch_add(k, std::memory_order_relaxed); }
+
+}  // namespace hs
+
+extern "C" {
+
+const char* hs_status_str(hs_status s) {
+  switch (s) {
+    case HS_OK: return "ok";
+    case HS_ERR_INVALID_ARG: return "invalid argument";
+    case HS_ERR_ID_RANGE: return "top-K id or row id out of range";
+    case HS_ERR_MISSING_ROW: return "miss on a placeholder page without a host copy";
+    case HS_ERR_CAPACITY: return "more misses than evictable hot slots";
+    case HS_ERR_STEP_ORDER: return "step older than the hot state";
+    case HS_ERR_CUDA: return "CUDA error";
+    case HS_ERR_TIMEOUT: return "device wait timed out";
+    case HS_ERR_TABLE_RANGE: return "table entry outside the pool";
+  }
+  return "unknown status";
+}
+
+int64_t hs_launch_count(void) { return hs::g_launches.load(); }
+
+hs_status hs_pool_create(const hs_pool_desc* d, hs_pool** out) {
+  if (!out) return HS_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!d) return HS_ERR_INVALID_ARG;
+  if (d->num_layers < 1 || d->num_layers > HS_MAX_LAYERS) return HS_ERR_INVALID_ARG;
+  if (d->page_size < 1 || d->page_size > HS_MAX_PAGE_SIZE) return HS_ERR_INVALID_ARG;
+  if (d->row_bytes <= 0 || d->row_bytes % 16 != 0) return HS_ERR_INVALID_ARG;
+  if ((int64_t)d->page_size * d->row_bytes >= (int64_t(1) << 31)) return HS_ERR_INVALID_ARG;
+  if (d->num_gpu_blocks < 1 || d->num_host_blocks < 0) return HS_ERR_INVALID_ARG;
+  if ((int64_t)d->num_gpu_blocks * d->page_size >= (int64_t(1) << 31)) return HS_ERR_INVALID_ARG;
+  if ((int64_t)d->num_host_blocks * d->page_size >= (int64_t(1) << 31)) return HS_ERR_INVALID_ARG;
+  if (!d->gpu_layer_base) return HS_ERR_INVALID_ARG;
+  if (d->num_host_blocks > 0 && !d->host_layer_base) return HS_ERR_INVALID_ARG;
+  for (int l = 0; l < d->num_layers; ++l) {
+    if (!d->gpu_layer_base[l] || !hs::aligned16(d->gpu_layer_base[l])) return HS_ERR_INVALID_ARG;
+    if (d->num_host_blocks > 0 && (!d->host_layer_base[l] || !hs::aligned16(d->host_layer_base[l])))
+      return HS_ERR_INVALID_ARG;
+  }
+  hs_pool* p = new (std::nothrow) hs_pool;
+  if (!p) return HS_ERR_INVALID_ARG;
+  std::memset(p, 0, sizeof(*p));
+  p->g = {d->num_layers, d->page_size, d->row_bytes, d->num_gpu_blocks, d->num_host_blocks};
+  if (cudaGetDevice(&p->device) != cudaSuccess) {
+    cudaGetLastError();
+    delete p;
+    return HS_ERR_CUDA;
+  }
+  for (int l = 0; l < d->num_layers; ++l) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, d->gpu_layer_base[l]) != cudaSuccess ||
+        (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)) {
+      cudaGetLastError();
+      delete p;
+      return HS_ERR_INVALID_ARG;
+    }
+    p->ptrs.gpu[l] = static_cast<uint8_t*>(d->gpu_layer_base[l]);
+    if (d->num_host_blocks > 0) {
+      void* dp = nullptr;
+      if (cudaHostGetDevicePointer(&dp, d->host_layer_base[l], 0) != cudaSuccess || !dp || !hs::aligned16(dp)) {
+        cudaGetLastError();
+        delete p;
+        return HS_ERR_INVALID_ARG;  // not pinned / not mapped into the device address space
+      }
+      p->ptrs.host[l] = static_cast<uint8_t*>(dp);
+    }
+  }
+  *out = p;
+  return HS_OK;
+}
+
+void hs_pool_destroy(hs_pool* p) { delete p; }
+
+hs_status hs_hot_reset(const hs_pool* pool, const hs_hot_state* hot, int32_t R, hs_stream_t stream) {
+  if (!pool || !hot || R < 0) return HS_ERR_INVALID_ARG;
+  if (hot->capacity < pool->g.page_size || hot->capacity > HS_MAX_CAPACITY || hot->capacity % pool->g.page_size)
+    return HS_ERR_INVALID_ARG;
+  const int64_t count = (int64_t)pool->g.num_layers * R * hot->capacity;
+  if (count == 0) return HS_OK;
+  if (!hot->slot_token || !hot->slot_stamp) return HS_ERR_INVALID_ARG;
+  const int sms = hs::sm_count(pool->device);
+  cudaError_t e = hs::launch_fill_i32(hot->slot_token, count, -1, sms, stream);
+  if (e == cudaSuccess) e = hs::launch_fill_i32(hot->slot_stamp, count, -1, sms, stream);
+  return hs::cuda_status(e);
+}
+
+size_t hs_resolve_workspace_bytes(int32_t nl, int32_t R, int32_t P, int32_t K, int32_t capacity) {
+  if (nl < 0 || R < 0 || P < 1 || K < 0 || capacity < 1) return 0;
+  const int64_t n = (int64_t)P * K;
+  if (n > HS_MAX_PLAN || capacity > HS_MAX_CAPACITY) return 0;
+  return hs::resolve_workspace_bytes((int64_t)nl * R, n, capacity);
+}
+
+size_t hs_resolve_smem_bytes(int32_t P, int32_t K, int32_t capacity) {
+  if (P < 1 || K < 0) return 0;
+  return hs::resolve_smem_plan((int64_t)P * K, capacity).total;
+}
+
+hs_status hs_resolve_topk(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P, int32_t K,
+                          const int32_t* topk_ids, const int32_t* block_table, const int32_t* host_block_table,
+                          const int32_t* ctx_len, int32_t max_pages, const hs_hot_state* hot, int32_t step,
+                          int32_t* out_rows, int32_t* out_stats, void* workspace, size_t workspace_bytes,
+                          hs_stream_t stream) {
+  if (!pool || !hot) return HS_ERR_INVALID_ARG;
+  const hs::PoolGeom& g = pool->g;
+  if (layer_begin < 0 || nl < 0 || (int64_t)layer_begin + nl > g.num_layers) return HS_ERR_INVALID_ARG;
+  if (R < 0 || P < 1 || K < 0 || step < 0 || max_pages < 1) return HS_ERR_INVALID_ARG;
+  const int64_t n = (int64_t)P * K;
+  const int32_t C = hot->capacity;
+  if (n > HS_MAX_PLAN || C < g.page_size || C > HS_MAX_CAPACITY || C % g.page_size) return HS_ERR_INVALID_ARG;
+  if ((int64_t)nl * R > INT32_MAX) return HS_ERR_INVALID_ARG;
+  if (nl == 0 || R == 0) return HS_OK;
+  if (!block_table || !host_block_table || !ctx_len || !hot->hot_blocks || !hot->slot_token || !hot->slot_stamp ||
+      !out_stats || !workspace)
+    return HS_ERR_INVALID_ARG;
+  if (n > 0 && (!topk_ids || !out_rows)) return HS_ERR_INVALID_ARG;
+  if (!hs::aligned16(workspace) || workspace_bytes < hs::resolve_workspace_bytes((int64_t)nl * R, n, C))
+    return HS_ERR_INVALID_ARG;
+  const hs::ResolveSmem sm = hs::resolve_smem_plan(n, C);
+  if (sm.total == 0 || sm.total > hs::resolve_smem_limit(pool->device)) return HS_ERR_INVALID_ARG;
+  const int sms = hs::sm_count(pool->device);
+  if (sms <= 0) return HS_ERR_CUDA;
+
+  hs::ResolveParams p{};
+  p.layer_begin = layer_begin;
+  p.nl = nl;
+  p.R = R;
+  p.n = (int32_t)n;
+  p.C = C;
+  p.S = g.page_size;
+  p.max_pages = max_pages;
+  p.step = step;
+  p.num_gpu_blocks = g.num_gpu_blocks;
+  p.num_host_blocks = g.num_host_blocks;
+  p.id_hash_bits = sm.id_hash_bits;
+  p.slot_hash_bits = sm.slot_hash_bits;
+  p.max_m = (int32_t)(n < C ? n : C);
+  p.topk = topk_ids;
+  p.bt = block_table;
+  p.hbt = host_block_table;
+  p.ctx_len = ctx_len;
+  p.hot_blocks = hot->hot_blocks;
+  p.slot_token = hot->slot_token;
+  p.slot_stamp = hot->slot_stamp;
+  p.out_rows = out_rows;
+  p.out_stats = out_stats;
+  const size_t count_bytes = (4 * (size_t)nl * R + 15) & ~size_t(15);
+  p.miss_count = static_cast<int32_t*>(workspace);
+  p.miss_list = reinterpret_cast<int2*>(static_cast<uint8_t*>(workspace) + count_bytes);
+
+  cudaError_t e = hs::launch_resolve(p, sm, stream);
+  if (e == cudaSuccess && p.max_m > 0) e = hs::launch_miss_copy(p, pool->ptrs, g.row_bytes, sms, stream);
+  return hs::cuda_status(e);
+}
+
+hs_status hs_gather_rows(const hs_pool* pool, int32_t layer_begin, int32_t nl, const int32_t* rows, int64_t n,
+                         void* out, int32_t* out_status, hs_stream_t stream) {
+  if (!pool) return HS_ERR_INVALID_ARG;
+  const hs::PoolGeom& g = pool->g;
+  if (layer_begin < 0 || nl < 0 || (int64_t)layer_begin + nl > g.num_layers || n < 0) return HS_ERR_INVALID_ARG;
+  if (nl == 0 || n == 0) return HS_OK;
+  if (!rows || !out || !hs::aligned16(out)) return HS_ERR_INVALID_ARG;
+  if (n > (INT64_MAX / 2) / g.row_bytes) return HS_ERR_INVALID_ARG;
+  const int sms = hs::sm_count(pool->device);
+  if (sms <= 0) return HS_ERR_CUDA;
+  return hs::cuda_status(hs::launch_gather(pool->ptrs, layer_begin, nl, rows, n, static_cast<uint8_t*>(out),
+                                           g.row_bytes, (int64_t)g.num_gpu_blocks * g.page_size, out_status, sms,
+                                           stream));
+}
+
+hs_status hs_offload_pages(const hs_pool* pool, const int32_t* gpu_blocks, const int32_t* host_blocks, int32_t n,
+                           int32_t* out_status, hs_stream_t stream) {
+  if (!pool || n < 0) return HS_ERR_INVALID_ARG;
+  if (n == 0) return HS_OK;
+  if (!gpu_blocks || !host_blocks || pool->g.num_host_blocks == 0) return HS_ERR_INVALID_ARG;
+  const int sms = hs::sm_count(pool->device);
+  if (sms <= 0) return HS_ERR_CUDA;
+  return hs::cuda_status(hs::launch_offload(pool->ptrs, pool->g, gpu_blocks, host_blocks, n, out_status, sms, stream));
+}
+
+}  // extern "C"

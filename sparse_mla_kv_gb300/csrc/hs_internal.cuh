@@ -1,0 +1,82 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "hs.h"
+
+namespace hs {
+
+// Per-layer base pointers, passed to kernels by value (kernel parameter space, no device
+// allocation).  host[] holds device-usable addresses of the pinned host pool.
+struct LayerPtrs {
+  uint8_t* gpu[HS_MAX_LAYERS];
+  uint8_t* host[HS_MAX_LAYERS];
+};
+
+struct PoolGeom {
+  int32_t num_layers, page_size, row_bytes, num_gpu_blocks, num_host_blocks;
+};
+
+// Resolver launch configuration.
+constexpr int kResolveThreads = 512;
+constexpr int kResolveWarps = kResolveThreads / 32;
+constexpr int kRadixBins = 256;
+// Miss-copy work item: this many consecutive misses of one unit.
+constexpr int kMissRowsPerItem = 8;
+
+// Error bits collected inside one resolver CTA; the reported code follows the precedence
+// STEP_ORDER > ID_RANGE > TABLE_RANGE > MISSING_ROW > CAPACITY.
+enum : uint32_t {
+  kErrStep = 1u,
+  kErrId = 2u,
+  kErrTable = 4u,
+  kErrMissing = 8u,
+  kErrCapacity = 16u,
+};
+
+struct ResolveParams {
+  int32_t layer_begin, nl, R, n /* P*K */, C, S, max_pages, step;
+  int32_t num_gpu_blocks, num_host_blocks;
+  int32_t id_hash_bits, slot_hash_bits;
+  int32_t max_m;  // miss-list capacity per unit = min(n, C)
+  const int32_t* topk;
+  const int32_t* bt;
+  const int32_t* hbt;
+  const int32_t* ctx_len;
+  const int32_t* hot_blocks;
+  int32_t* slot_token;
+  int32_t* slot_stamp;
+  int32_t* out_rows;
+  int32_t* out_stats;
+  int32_t* miss_count;  // workspace [nl*R]
+  int2* miss_list;      // workspace [nl*R][max_m] = (host row, pool row)
+};
+
+struct ResolveSmem {
+  // byte offsets into dynamic shared memory
+  size_t tok, stamp, ids, val, cls, idh, u /* slot hash, later radix buffers */, total;
+  int32_t id_hash_bits, slot_hash_bits;
+};
+
+// Shared-memory plan of one resolver CTA for (n = P*K ids, C slots); total = 0 if out of limits.
+ResolveSmem resolve_smem_plan(int64_t n, int64_t C);
+size_t resolve_workspace_bytes(int64_t units, int64_t n, int64_t C);
+// Largest dynamic shared memory a resolver CTA may use on device `dev` (0 on failure).
+size_t resolve_smem_limit(int dev);
+
+// Launchers (return cudaGetLastError() of the launch).
+cudaError_t launch_resolve(const ResolveParams& p, const ResolveSmem& sm, cudaStream_t s);
+cudaError_t launch_miss_copy(const ResolveParams& p, const LayerPtrs& ptrs, int32_t row_bytes, int sms,
+                             cudaStream_t s);
+cudaError_t launch_gather(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, const int32_t* rows, int64_t n,
+                          uint8_t* out, int32_t row_bytes, int64_t num_rows, int32_t* status, int sms,
+                          cudaStream_t s);
+cudaError_t launch_offload(const LayerPtrs& ptrs, const PoolGeom& g, const int32_t* gpu_blocks,
+                           const int32_t* host_blocks, int32_t n, int32_t* status, int sms, cudaStream_t s);
+cudaError_t launch_fill_i32(int32_t* a, int64_t count, int32_t value, int sms, cudaStream_t s);
+
+void count_launch(int k = 1);
+
+}  // namespace hs

@@ -1,0 +1,512 @@
+// Fused per-step top-K resolver and the miss-copy kernel.
+//
+// Source: "vLLM GLM 5.3 Optimizations: Hybrid HiSparse Offloading", section "Technical
+// Implementation of Hybrid HiSparse", item 2 (Mixed residency): resident tokens are read in place,
+// hot tokens are read and their LRU entry refreshed, a miss copies a single row from pinned host
+// memory into an LRU slot.  Japanese article (news.ainew.jp), section "仕組み" (How it works): the
+// block table mixes real blocks and null placeholders; the resolver hands back pool row ids; no
+// step waits for the CPU (CUDA-graph capturable).  Section "vLLM の他の部分との統合"
+// (Integration): speculative decoding uses one replayable per-step plan sharing the hot state.
+//
+// Design (sm_103a):
+//   resolve_kernel   one CTA (512 threads) per (layer, request) unit.  The unit's slot state is
+//                    staged in shared memory; two open-addressing hash tables (16-bit entries) map
+//                    token -> lowest slot and id -> first position; the plan, hit/miss
+//                    classification and the miss ranks come from block-wide scans; victims are the
+//                    candidates sorted by (stamp, slot) with a stable LSD radix sort (8-bit digits,
+//                    per-warp histograms, __match_any_sync ranking).  Misses go to a per-unit list in
+//                    the caller's workspace.  A unit with a data error writes nothing but -1 rows
+//                    and its status.
+//   miss_copy_kernel a persistent grid spreads every unit's misses over all SMs: each warp takes
+//                    batches of 32 (unit, 8-row) items, skips empty ones with one ballot, and copies
+//                    the rows as 16-byte zero-copy loads from the mapped pinned host pool.  Spreading
+//                    keeps enough loads in flight on the host link even when few units miss a lot.
+#include <atomic>
+#include <climits>
+
+#include "hs_internal.cuh"
+
+namespace hs {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr unsigned short kEmpty16 = 0xFFFF;
+enum : uint8_t { kNone = 0, kResident = 1, kHit = 2, kMiss = 3 };
+
+__device__ __forceinline__ uint32_t fib_hash(int32_t key, int bits) {
+  return ((uint32_t)key * 0x9E3779B1u) >> (32 - bits);
+}
+
+__device__ __forceinline__ void atomic_min_u16(unsigned short* a, unsigned short v) {
+  unsigned short cur = *(volatile unsigned short*)a;
+  while (v < cur) {
+    const unsigned short prev = atomicCAS(a, cur, v);
+    if (prev == cur) break;
+    cur = prev;
+  }
+}
+
+// Insert entry e (an index into keys[]) under key keys[e] == k; when the key is already present
+// keep the smallest entry (lowest slot / first position).
+__device__ __forceinline__ void hash_insert_min(unsigned short* tab, int bits, const int32_t* keys, int32_t k,
+                                                int e) {
+  const uint32_t mask = (1u << bits) - 1u;
+  uint32_t h = fib_hash(k, bits);
+  for (uint32_t it = 0; it <= mask; ++it, h = (h + 1u) & mask) {
+    unsigned short cur = *(volatile unsigned short*)&tab[h];
+    if (cur == kEmpty16) {
+      const unsigned short prev = atomicCAS(&tab[h], kEmpty16, (unsigned short)e);
+      if (prev == kEmpty16) return;
+      cur = prev;
+    }
+    if (keys[cur] == k) {
+      atomic_min_u16(&tab[h], (unsigned short)e);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ int hash_find(const unsigned short* tab, int bits, const int32_t* keys, int32_t k) {
+  const uint32_t mask = (1u << bits) - 1u;
+  uint32_t h = fib_hash(k, bits);
+  for (uint32_t it = 0; it <= mask; ++it, h = (h + 1u) & mask) {
+    const unsigned short cur = tab[h];
+    if (cur == kEmpty16) return -1;
+    if (keys[cur] == k) return cur;
+  }
+  return -1;
+}
+
+// Exclusive block-wide scan of two ints at once.  Contains __syncthreads: call uniformly.
+__device__ __forceinline__ void block_scan2(int a, int b, int& ea, int& eb, int& ta, int& tb, int* s_tmp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int ia = a, ib = b;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int xa = __shfl_up_sync(kFull, ia, o);
+    const int xb = __shfl_up_sync(kFull, ib, o);
+    if (lane >= o) { ia += xa; ib += xb; }
+  }
+  if (lane == 31) { s_tmp[warp] = ia; s_tmp[kResolveWarps + warp] = ib; }
+  __syncthreads();
+  if (warp == 0) {
+    int va = lane < kResolveWarps ? s_tmp[lane] : 0;
+    int vb = lane < kResolveWarps ? s_tmp[kResolveWarps + lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int xa = __shfl_up_sync(kFull, va, o);
+      const int xb = __shfl_up_sync(kFull, vb, o);
+      if (lane >= o) { va += xa; vb += xb; }
+    }
+    if (lane < kResolveWarps) { s_tmp[lane] = va; s_tmp[kResolveWarps + lane] = vb; }
+  }
+  __syncthreads();
+  ea = (warp ? s_tmp[warp - 1] : 0) + ia - a;
+  eb = (warp ? s_tmp[kResolveWarps + warp - 1] : 0) + ib - b;
+  ta = s_tmp[kResolveWarps - 1];
+  tb = s_tmp[2 * kResolveWarps - 1];
+  __syncthreads();
+}
+
+// Stable LSD radix sort of slot ids a[0..nc) by key stamp[slot] - lo over `passes` 8-bit digits.
+// Returns the buffer holding the result (a or b).  Call uniformly (contains __syncthreads).
+__device__ unsigned short* radix_sort_slots(unsigned short* a, unsigned short* b, int nc, const int32_t* s_stamp,
+                                            int lo, int passes, int* hist, int* s_tmp) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per_warp = (nc + kResolveWarps - 1) / kResolveWarps;
+  const int w0 = min(nc, warp * per_warp), w1 = min(nc, w0 + per_warp);
+  constexpr int kEntries = kRadixBins * kResolveWarps;
+  constexpr int kPerThread = kEntries / kResolveThreads;
+  static_assert(kEntries % kResolveThreads == 0, "histogram split");
+  for (int pass = 0; pass < passes; ++pass) {
+    const int shift = pass * 8;
+    for (int i = tid; i < kEntries; i += kResolveThreads) hist[i] = 0;
+    __syncthreads();
+    for (int e = w0 + lane; e < w1; e += 32) {
+      const uint32_t d = ((uint32_t)(s_stamp[a[e]] - lo) >> shift) & 0xFFu;
+      atomicAdd(&hist[d * kResolveWarps + warp], 1);
+    }
+    __syncthreads();
+    int loc[kPerThread];
+    int sum = 0;
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) { loc[k] = hist[tid * kPerThread + k]; sum += loc[k]; }
+    int base, dummy_e, total, dummy_t;
+    block_scan2(sum, 0, base, dummy_e, total, dummy_t, s_tmp);
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) { hist[tid * kPerThread + k] = base; base += loc[k]; }
+    __syncthreads();
+    for (int e0 = w0; e0 < w1; e0 += 32) {  // warp-uniform trip count
+      const int e = e0 + lane;
+      const bool valid = e < w1;
+      const unsigned short slot = valid ? a[e] : (unsigned short)0;
+      const uint32_t d = valid ? (((uint32_t)(s_stamp[slot] - lo) >> shift) & 0xFFu) : 0u;
+      const uint32_t key = valid ? d : (0x100u + (uint32_t)lane);
+      const uint32_t peers = __match_any_sync(kFull, key);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      int* ctr = &hist[d * kResolveWarps + warp];
+      if (valid) b[*ctr + rank] = slot;
+      __syncwarp();
+      if (valid && rank == 0) *ctr += __popc(peers);
+      __syncwarp();
+    }
+    __syncthreads();
+    unsigned short* t = a; a = b; b = t;
+  }
+  return a;
+}
+
+__global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const ResolveParams p, const ResolveSmem sm) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  int32_t* s_tok = reinterpret_cast<int32_t*>(smem + sm.tok);
+  int32_t* s_stamp = reinterpret_cast<int32_t*>(smem + sm.stamp);
+  int32_t* s_ids = reinterpret_cast<int32_t*>(smem + sm.ids);
+  int32_t* s_val = reinterpret_cast<int32_t*>(smem + sm.val);
+  uint8_t* s_cls = reinterpret_cast<uint8_t*>(smem + sm.cls);
+  unsigned short* s_idh = reinterpret_cast<unsigned short*>(smem + sm.idh);
+  unsigned short* s_slh = reinterpret_cast<unsigned short*>(smem + sm.u);
+  __shared__ uint32_t s_err;
+  __shared__ int s_cnt[3];
+  __shared__ int s_lo, s_hi;
+  __shared__ int s_tmp[2 * kResolveWarps];
+
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int unit = blockIdx.x;
+  const int lr = unit / p.R, r = unit - lr * p.R;
+  const int l = p.layer_begin + lr;
+  const int n = p.n, C = p.C, S = p.S, step = p.step;
+  const int64_t state_off = ((int64_t)l * p.R + r) * C;
+  const int32_t* ids_g = p.topk + (int64_t)unit * n;
+  const int32_t* bt = p.bt + (int64_t)r * p.max_pages;
+  const int32_t* hbt = p.hbt + (int64_t)r * p.max_pages;
+  const int32_t* hot = p.hot_blocks + (int64_t)r * (C / S);
+  int32_t* rows_g = p.out_rows + (int64_t)unit * n;
+  const int ctx = p.ctx_len[r];
+  const int HI = 1 << sm.id_hash_bits, HS = 1 << sm.slot_hash_bits;
+
+  // ---- phase 0: stage state and ids; checks that need no classification
+  if (tid == 0) {
+    s_err = 0u;
+    s_cnt[0] = s_cnt[1] = s_cnt[2] = 0;
+    s_lo = INT_MAX;
+    s_hi = INT_MIN;
+  }
+  for (int i = tid; i < HI; i += kResolveThreads) s_idh[i] = kEmpty16;
+  for (int i = tid; i < HS; i += kResolveThreads) s_slh[i] = kEmpty16;
+  uint32_t err = 0u;
+  for (int s = tid; s < C; s += kResolveThreads) {
+    const int t = p.slot_token[state_off + s];
+    const int st = p.slot_stamp[state_off + s];
+    s_tok[s] = t;
+    s_stamp[s] = st;
+    if (st > step) err |= kErrStep;
+  }
+  for (int i = tid; i < n; i += kResolveThreads) {
+    const int id = ids_g[i];
+    s_ids[i] = id;
+    if (id != -1 && (id < -1 || id >= ctx || id / S >= p.max_pages)) err |= kErrId;
+  }
+  for (int b = tid; b < C / S; b += kResolveThreads) {
+    const int hb = hot[b];
+    if (hb < 0 || hb >= p.num_gpu_blocks) err |= kErrTable;
+  }
+  if (err) atomicOr(&s_err, err);
+  __syncthreads();
+  const bool early = (s_err & (kErrStep | kErrId)) != 0u;
+
+  // ---- phase 1: hash tables (token -> lowest slot, id -> first position)
+  if (!early) {
+    for (int s = tid; s < C; s += kResolveThreads) {
+      const int t = s_tok[s];
+      if (t >= 0) hash_insert_min(s_slh, sm.slot_hash_bits, s_tok, t, s);
+    }
+    for (int i = tid; i < n; i += kResolveThreads) {
+      const int id = s_ids[i];
+      if (id >= 0) hash_insert_min(s_idh, sm.id_hash_bits, s_ids, id, i);
+    }
+  }
+  __syncthreads();
+
+  // ---- phase 2: classify each plan entry (first occurrences); hits get stamp = step in smem
+  int c_res = 0, c_hit = 0, c_miss = 0;
+  if (!early) {
+    for (int i = tid; i < n; i += kResolveThreads) {
+      const int id = s_ids[i];
+      uint8_t cls = kNone;
+      int val = 0;
+      if (id >= 0 && hash_find(s_idh, sm.id_hash_bits, s_ids, id) == i) {
+        const int page = id / S, off = id - page * S;
+        const int b = bt[page];
+        if (b >= 0) {
+          if (b >= p.num_gpu_blocks) err |= kErrTable;
+          else val = b * S + off;
+          cls = kResident;
+          ++c_res;
+        } else {
+          const int s = hash_find(s_slh, sm.slot_hash_bits, s_tok, id);
+          if (s >= 0) {
+            cls = kHit;
+            val = s;
+            s_stamp[s] = step;
+            ++c_hit;
+          } else {
+            const int h = hbt[page];
+            if (h < 0) err |= kErrMissing;
+            else if (h >= p.num_host_blocks) err |= kErrTable;
+            else val = h * S + off;
+            cls = kMiss;
+            ++c_miss;
+          }
+        }
+      }
+      s_cls[i] = cls;
+      s_val[i] = val;
+    }
+  }
+  c_res = __reduce_add_sync(kFull, c_res);
+  c_hit = __reduce_add_sync(kFull, c_hit);
+  c_miss = __reduce_add_sync(kFull, c_miss);
+  if (lane == 0 && (c_res | c_hit | c_miss)) {
+    atomicAdd(&s_cnt[0], c_res);
+    atomicAdd(&s_cnt[1], c_hit);
+    atomicAdd(&s_cnt[2], c_miss);
+  }
+  if (err) atomicOr(&s_err, err);
+  __syncthreads();
+
+  uint32_t e = s_err;
+  // per-thread contiguous chunks: positions [i0, i1) and slots [q0, q1)
+  const int ipt = (n + kResolveThreads - 1) / kResolveThreads;
+  const int i0 = min(n, tid * ipt), i1 = min(n, i0 + ipt);
+  const int spt = (C + kResolveThreads - 1) / kResolveThreads;
+  const int q0 = min(C, tid * spt), q1 = min(C, q0 + spt);
+  int miss_base = 0, cand_base = 0, tot_miss = 0, tot_cand = 0;
+  unsigned short* sorted = nullptr;
+
+  if (e == 0u) {
+    // ---- phase 3: miss ranks (plan order) and candidate positions (slot order); capacity
+    int my_miss = 0;
+    for (int i = i0; i < i1; ++i) my_miss += (s_cls[i] == kMiss);
+    int my_cand = 0, lo = INT_MAX, hi = INT_MIN;
+    for (int s = q0; s < q1; ++s) {
+      const int st = s_stamp[s];
+      if (st < step) { ++my_cand; lo = min(lo, st); hi = max(hi, st); }
+    }
+    lo = __reduce_min_sync(kFull, lo);
+    hi = __reduce_max_sync(kFull, hi);
+    if (lane == 0 && lo != INT_MAX) { atomicMin(&s_lo, lo); atomicMax(&s_hi, hi); }
+    block_scan2(my_miss, my_cand, miss_base, cand_base, tot_miss, tot_cand, s_tmp);
+    if (tot_miss > tot_cand) e = kErrCapacity;  // uniform: totals are block-wide
+    if (e == 0u && tot_miss > 0) {
+      // ---- phase 4: victims = candidates in ascending (stamp, slot)
+      unsigned short* buf_a = reinterpret_cast<unsigned short*>(smem + sm.u);
+      unsigned short* buf_b = buf_a + ((C + 7) & ~7);
+      int* hist = reinterpret_cast<int*>(buf_b + ((C + 7) & ~7));
+      __syncthreads();  // the slot hash (same memory) is dead from here on
+      int k = cand_base;
+      for (int s = q0; s < q1; ++s)
+        if (s_stamp[s] < step) buf_a[k++] = (unsigned short)s;
+      __syncthreads();
+      const int span = s_hi - s_lo;
+      const int bits = span > 0 ? 32 - __clz(span) : 0;
+      sorted = radix_sort_slots(buf_a, buf_b, tot_cand, s_stamp, s_lo, (bits + 7) / 8, hist, s_tmp);
+    }
+  }
+
+  if (e == 0u) {
+    // ---- phase 5: hits refresh their stamp; the j-th miss takes the j-th victim and one row
+    int j = miss_base;
+    for (int i = i0; i < i1; ++i) {
+      const uint8_t cls = s_cls[i];
+      if (cls == kMiss) {
+        const int v = sorted[j];
+        const int vb = v / S;
+        const int dst = hot[vb] * S + (v - vb * S);
+        p.miss_list[(int64_t)unit * p.max_m + j] = make_int2(s_val[i], dst);
+        p.slot_token[state_off + v] = s_ids[i];
+        p.slot_stamp[state_off + v] = step;
+        s_val[i] = dst;
+        ++j;
+      } else if (cls == kHit) {
+        const int v = s_val[i];
+        const int vb = v / S;
+        p.slot_stamp[state_off + v] = step;
+        s_val[i] = hot[vb] * S + (v - vb * S);
+      }
+    }
+    __syncthreads();
+    // ---- phase 6: emit rows (duplicates read their first occurrence's row)
+    for (int i = tid; i < n; i += kResolveThreads) {
+      const int id = s_ids[i];
+      int row = -1;
+      if (id >= 0) row = s_cls[i] != kNone ? s_val[i] : s_val[hash_find(s_idh, sm.id_hash_bits, s_ids, id)];
+      rows_g[i] = row;
+    }
+    if (tid == 0) {
+      int32_t* st = p.out_stats + (int64_t)unit * 4;
+      st[0] = HS_OK;
+      st[1] = s_cnt[0];
+      st[2] = s_cnt[1];
+      st[3] = s_cnt[2];
+      p.miss_count[unit] = tot_miss;
+    }
+  } else {
+    const int code = (e & kErrStep) ? HS_ERR_STEP_ORDER
+                   : (e & kErrId) ? HS_ERR_ID_RANGE
+                   : (e & kErrTable) ? HS_ERR_TABLE_RANGE
+                   : (e & kErrMissing) ? HS_ERR_MISSING_ROW
+                   : HS_ERR_CAPACITY;
+    for (int i = tid; i < n; i += kResolveThreads) rows_g[i] = -1;
+    if (tid == 0) {
+      int32_t* st = p.out_stats + (int64_t)unit * 4;
+      st[0] = code;
+      st[1] = st[2] = st[3] = 0;
+      p.miss_count[unit] = 0;
+    }
+  }
+}
+
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;
+
+template <int CPR>
+__global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(const ResolveParams p, const LayerPtrs ptrs,
+                                                                 int32_t row_bytes) {
+  const int cpr = CPR ? CPR : (row_bytes >> 4);
+  const int units = p.nl * p.R;
+  const int items_per_unit = (p.max_m + kMissRowsPerItem - 1) / kMissRowsPerItem;
+  const int64_t items = (int64_t)units * items_per_unit;
+  const int64_t batches = (items + 31) / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t bi = warp; bi < batches; bi += nwarps) {
+    // items are chunk-major, so the non-empty ones (low chunk numbers) come first
+    const int64_t item = bi * 32 + lane;
+    int unit = 0, chunk = 0, cnt = 0;
+    bool live = false;
+    if (item < items) {
+      chunk = (int)(item / units);
+      unit = (int)(item - (int64_t)chunk * units);
+      cnt = p.miss_count[unit];
+      live = chunk * kMissRowsPerItem < cnt;
+    }
+    uint32_t todo = __ballot_sync(kFull, live);
+    while (todo) {
+      const int src_lane = __ffs(todo) - 1;
+      todo &= todo - 1u;
+      const int u = __shfl_sync(kFull, unit, src_lane);
+      const int ch = __shfl_sync(kFull, chunk, src_lane);
+      const int c = __shfl_sync(kFull, cnt, src_lane);
+      const int r0 = ch * kMissRowsPerItem;
+      const int nrows = min(kMissRowsPerItem, c - r0);
+      const int l = p.layer_begin + u / p.R;
+      int2 ent = make_int2(0, 0);
+      if (lane < nrows) ent = p.miss_list[(int64_t)u * p.max_m + r0 + lane];
+      const uint8_t* host = ptrs.host[l];
+      uint8_t* pool = ptrs.gpu[l];
+      const int total = nrows * cpr;
+      for (int f0 = 0; f0 < total; f0 += 32 * kCopyUnroll) {
+        uint4 v[kCopyUnroll];
+        int64_t dst_off[kCopyUnroll];
+#pragma unroll
+        for (int k = 0; k < kCopyUnroll; ++k) {
+          const int f = f0 + k * 32 + lane;
+          const bool ok = f < total;
+          const int rr = ok ? f / cpr : 0;
+          const int cc = f - rr * cpr;
+          const int src = __shfl_sync(kFull, ent.x, rr);
+          const int dst = __shfl_sync(kFull, ent.y, rr);
+          dst_off[k] = -1;
+          if (ok) {
+            v[k] = __ldcg(reinterpret_cast<const uint4*>(host + (int64_t)src * row_bytes) + cc);
+            dst_off[k] = (int64_t)dst * row_bytes + (int64_t)cc * 16;
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kCopyUnroll; ++k)
+          if (dst_off[k] >= 0) *reinterpret_cast<uint4*>(pool + dst_off[k]) = v[k];
+      }
+    }
+  }
+}
+
+int ceil_log2(int64_t x) {
+  int b = 0;
+  while ((int64_t(1) << b) < x) ++b;
+  return b;
+}
+
+size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+}  // namespace
+
+ResolveSmem resolve_smem_plan(int64_t n, int64_t C) {
+  ResolveSmem sm{};
+  if (n < 0 || n > HS_MAX_PLAN || C < 1 || C > HS_MAX_CAPACITY) return sm;
+  sm.id_hash_bits = ceil_log2(2 * (n > 16 ? n : 16));
+  sm.slot_hash_bits = ceil_log2(2 * (C > 16 ? C : 16));
+  size_t off = 0;
+  sm.tok = off;   off = align16(off + 4 * (size_t)C);
+  sm.stamp = off; off = align16(off + 4 * (size_t)C);
+  sm.ids = off;   off = align16(off + 4 * (size_t)n);
+  sm.val = off;   off = align16(off + 4 * (size_t)n);
+  sm.cls = off;   off = align16(off + (size_t)n);
+  sm.idh = off;   off = align16(off + 2 * ((size_t)1 << sm.id_hash_bits));
+  sm.u = off;
+  const size_t slot_hash = 2 * ((size_t)1 << sm.slot_hash_bits);
+  const size_t cbuf = 2 * (size_t)((C + 7) & ~int64_t(7));
+  const size_t radix = 2 * cbuf + 4 * (size_t)kRadixBins * kResolveWarps;
+  off = align16(off + (slot_hash > radix ? slot_hash : radix));
+  sm.total = off;
+  return sm;
+}
+
+size_t resolve_workspace_bytes(int64_t units, int64_t n, int64_t C) {
+  const int64_t max_m = n < C ? n : C;
+  return align16(4 * (size_t)units) + 8 * (size_t)units * (size_t)max_m;
+}
+
+size_t resolve_smem_limit(int dev) {
+  // Dynamic shared memory one resolver CTA may use on this device (opt-in maximum minus the
+  // kernel's static shared memory).  Also raises the kernel's attribute to that limit, once.
+  static std::atomic<long long> limit[64];
+  if (dev < 0 || dev >= 64) return 0;
+  long long v = limit[dev].load();
+  if (v > 0) return (size_t)v;
+  int optin = 0;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+  cudaFuncAttributes fa{};
+  if (cudaFuncGetAttributes(&fa, resolve_kernel) != cudaSuccess) return 0;
+  const long long dyn = (long long)optin - (long long)fa.sharedSizeBytes;
+  if (dyn <= 0) return 0;
+  if (cudaFuncSetAttribute(resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) != cudaSuccess)
+    return 0;
+  limit[dev].store(dyn);
+  return (size_t)dyn;
+}
+
+cudaError_t launch_resolve(const ResolveParams& p, const ResolveSmem& sm, cudaStream_t s) {
+  resolve_kernel<<<p.nl * p.R, kResolveThreads, sm.total, s>>>(p, sm);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_miss_copy(const ResolveParams& p, const LayerPtrs& ptrs, int32_t row_bytes, int sms,
+                             cudaStream_t s) {
+  const int64_t units = (int64_t)p.nl * p.R;
+  const int64_t items = units * ((p.max_m + kMissRowsPerItem - 1) / kMissRowsPerItem);
+  const int64_t warps_needed = (items + 31) / 32;
+  int64_t blocks = (warps_needed + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
+  const int64_t cap = (int64_t)sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (row_bytes == 656)
+    miss_copy_kernel<41><<<(unsigned)blocks, kCopyThreads, 0, s>>>(p, ptrs, row_bytes);
+  else
+    miss_copy_kernel<0><<<(unsigned)blocks, kCopyThreads, 0, s>>>(p, ptrs, row_bytes);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace hs

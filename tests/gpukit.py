@@ -1,0 +1,141 @@
+"""Drive one synthetic workload through the CUDA library and the oracle side by side.
+
+Inputs come from synth (tables, top-K, closed-form row bytes); expected values come from the oracle
+(rows, stats, slot state, and pool bytes when `oracle_bytes`) and from the closed-form row contents
+(gathered bytes, hot-slot bytes).  Nothing expected is ever read back from the CUDA path."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import sparse_mla_kv_gb300 as hs
+from synth import content, device as sdev
+
+
+class Rig:
+    def __init__(self, w, *, oracle_bytes: bool = False, device: str = "cuda", check_hot_bytes: bool = True):
+        self.w = w
+        self.dev = torch.device(device)
+        self.oracle_bytes = oracle_bytes
+        self.check_hot_bytes = check_hot_bytes
+        L, R, C, S, B = w.L, w.R, w.C, w.S, w.B
+        self.gpu = [torch.empty((w.num_gpu_blocks, S, B), dtype=torch.uint8, device=self.dev) for _ in range(L)]
+        nhb = max(1, w.num_host_blocks)
+        self.host = [torch.zeros((nhb, S, B), dtype=torch.uint8).pin_memory() for _ in range(L)]
+        for l in range(L):
+            sdev.fill_gpu_pool(w, l, self.gpu[l])
+            if w.num_host_blocks:
+                sdev.fill_host_pool(w, l, self.host[l], self.dev)
+        self.pool = hs.Pool(self.gpu, self.host if w.num_host_blocks else None)
+        self.bt_np = w.block_table.copy()
+        self.hbt_np = w.host_block_table.copy()
+        self.bt = torch.from_numpy(self.bt_np).to(self.dev)
+        self.hbt = torch.from_numpy(self.hbt_np).to(self.dev)
+        self.hot_blocks = torch.from_numpy(w.hot_blocks.astype(np.int32)).to(self.dev)
+        self.hot = hs.HotState.allocate(L, self.hot_blocks, C)
+        hs.hot_reset(self.pool, self.hot)
+        self.ws = hs.alloc_workspace(L, R, w.P, w.K, C, self.dev)
+        self.o_tok = np.full((L, R, C), -1, np.int32)
+        self.o_stamp = np.full((L, R, C), -1, np.int32)
+        self.o_pools = self.o_hosts = None
+        if oracle_bytes:
+            self.o_pools = [np.zeros(w.num_gpu_blocks * S * B, np.uint8) for _ in range(L)]
+            self.o_hosts = [np.zeros(nhb * S * B, np.uint8) for _ in range(L)]
+            own_g, own_h = w.gpu_block_owner(), w.host_block_owner()
+            for l in range(L):
+                for blk in np.nonzero(own_g[:, 0] >= 0)[0]:
+                    r, p = own_g[blk]
+                    self.o_pools[l][blk * S * B:(blk + 1) * S * B] = content.page_np(
+                        w.content_seed, l, int(w.content_page[r, p]), S, B).reshape(-1)
+                for blk in np.nonzero(own_h[:, 0] >= 0)[0]:
+                    r, p = own_h[blk]
+                    self.o_hosts[l][blk * S * B:(blk + 1) * S * B] = content.page_np(
+                        w.content_seed, l, int(w.content_page[r, p]), S, B).reshape(-1)
+        torch.cuda.synchronize()
+
+    # ------------------------------------------------------------------ one step on both sides
+    def apply_edits(self, st) -> None:
+        w = self.w
+        for r, p, v in st.bt_edits:
+            self.bt_np[r, p] = v
+        for r, p, v in st.hbt_edits:
+            self.hbt_np[r, p] = v
+        if len(st.bt_edits):
+            self.bt.copy_(torch.from_numpy(self.bt_np))
+        if len(st.hbt_edits):
+            self.hbt.copy_(torch.from_numpy(self.hbt_np))
+        if len(st.fills):
+            blocks = st.fills[:, 0].astype(np.int64)
+            owners = st.fills[:, 1:].astype(np.int64)
+            for l in range(w.L):
+                sdev.fill_blocks(w, l, self.gpu[l], blocks, owners, self.dev)
+                if self.o_pools is not None:
+                    for b, (r, p) in zip(blocks, owners):
+                        self.o_pools[l][b * w.S * w.B:(b + 1) * w.S * w.B] = content.page_np(
+                            w.content_seed, l, int(w.content_page[r, p]), w.S, w.B).reshape(-1)
+
+    def step(self, st, *, check: bool = True):
+        w = self.w
+        self.apply_edits(st)
+        topk = torch.from_numpy(st.topk).to(self.dev)
+        ctx = torch.from_numpy(st.ctx_len.astype(np.int32)).to(self.dev)
+        rows, stats = hs.resolve_topk(self.pool, topk, self.bt, self.hbt, ctx, self.hot, st.index, workspace=self.ws)
+        out = hs.gather_rows(self.pool, rows.reshape(w.L, -1))
+        if len(st.off_gpu):
+            hs.offload_pages(self.pool, torch.from_numpy(st.off_gpu).to(self.dev),
+                             torch.from_numpy(st.off_host).to(self.dev))
+        torch.cuda.synchronize()
+        o_rows, o_stats = oracle.resolve(S=w.S, B=w.B, num_gpu_blocks=w.num_gpu_blocks,
+                                         num_host_blocks=w.num_host_blocks, topk=st.topk, block_table=self.bt_np,
+                                         host_block_table=self.hbt_np, ctx_len=st.ctx_len, max_pages=w.max_pages,
+                                         C=w.C, hot_blocks=w.hot_blocks, slot_token=self.o_tok,
+                                         slot_stamp=self.o_stamp, step=st.index, pools=self.o_pools,
+                                         hosts=self.o_hosts)
+        if len(st.off_gpu) and self.o_pools is not None:
+            oracle.offload(S=w.S, B=w.B, num_gpu_blocks=w.num_gpu_blocks, num_host_blocks=w.num_host_blocks,
+                           pools=self.o_pools, hosts=self.o_hosts, gpu_blocks=st.off_gpu, host_blocks=st.off_host)
+        if check:
+            self.compare(st, rows, stats, out, o_rows, o_stats)
+        return rows, stats, out, o_rows, o_stats
+
+    def compare(self, st, rows, stats, out, o_rows, o_stats) -> None:
+        w = self.w
+        g_rows = rows.cpu().numpy()
+        g_stats = stats.cpu().numpy()
+        assert np.array_equal(g_stats, o_stats), f"stats differ at step {st.index}"
+        assert np.array_equal(g_rows, o_rows), f"rows differ at step {st.index}"
+        assert np.array_equal(self.hot.slot_token.cpu().numpy(), self.o_tok), f"slot_token differs at step {st.index}"
+        assert np.array_equal(self.hot.slot_stamp.cpu().numpy(), self.o_stamp), f"slot_stamp differs at step {st.index}"
+        # gathered bytes == closed-form bytes of each logical token (zero for padding / failed units)
+        ids = torch.from_numpy(st.topk).to(self.dev)
+        ok = torch.from_numpy(o_stats[..., 0] == 0).to(self.dev)
+        for l in range(w.L):
+            idl = ids[l].reshape(w.R, -1).long()
+            idl = torch.where(ok[l][:, None], idl, torch.full_like(idl, -1))
+            r_idx = torch.arange(w.R, device=self.dev)[:, None].expand_as(idl).reshape(-1)
+            exp = sdev.expected_rows(w, l, r_idx, idl.reshape(-1))
+            assert torch.equal(out[l], exp), f"gathered bytes differ at step {st.index} layer {l}"
+        if self.o_pools is not None:
+            for l in range(w.L):
+                assert np.array_equal(self.gpu[l].cpu().numpy().reshape(-1), self.o_pools[l]), \
+                    f"pool bytes differ at step {st.index} layer {l}"
+                if w.num_host_blocks:
+                    assert np.array_equal(self.host[l].numpy().reshape(-1), self.o_hosts[l]), \
+                        f"host pool differs at step {st.index} layer {l}"
+        elif self.check_hot_bytes:
+            self.check_hot_rows()
+
+    def check_hot_rows(self) -> None:
+        """Every filled hot slot's pool row holds the closed-form bytes of its token."""
+        w = self.w
+        tok = self.hot.slot_token
+        for l in range(w.L):
+            t = tok[l].long()
+            r_idx = torch.arange(w.R, device=self.dev)[:, None].expand_as(t)
+            v = torch.arange(w.C, device=self.dev)[None, :].expand_as(t)
+            prow = self.hot_blocks.long()[r_idx, v // w.S] * w.S + v % w.S
+            m = t >= 0
+            got = self.gpu[l].reshape(-1, w.B)[prow[m]]
+            exp = sdev.expected_rows(w, l, r_idx[m], t[m])
+            assert torch.equal(got, exp), f"hot rows differ from their tokens' bytes (layer {l})"

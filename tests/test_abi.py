@@ -1,0 +1,101 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports every function that
+include/hs.h declares, and its host-side logic (argument checks that need no device, size queries,
+status strings) behaves as documented.  No compute call is made here."""
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+import sparse_mla_kv_gb300 as hs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hs.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(hs.LIB_PATH):
+        if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+            pytest.skip("no nvcc to build the library")
+        from sparse_mla_kv_gb300 import _build
+        _build.build()
+    return hs.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hs_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("hs_pool_create", "hs_pool_destroy", "hs_hot_reset", "hs_resolve_topk", "hs_gather_rows",
+                 "hs_offload_pages", "hs_status_str", "hs_resolve_workspace_bytes"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    nm = shutil.which("nm")
+    if nm:
+        out = subprocess.run([nm, "-D", "--defined-only", hs.LIB_PATH], capture_output=True, text=True).stdout
+        exported = set(re.findall(r"\b(hs_[a-z0-9_]+)\b", out))
+        assert set(declared_functions()) <= exported
+
+
+def test_status_strings(lib):
+    for code in (0, 1, 2, 3, 4, 5, 6, 7, 8):
+        s = hs.status_str(code)
+        assert s and s != "unknown status"
+    assert hs.status_str(99) == "unknown status"
+
+
+def test_size_queries(lib):
+    # miss-list workspace: 16-byte-aligned counts + (host row, pool row) per possible miss
+    assert hs.resolve_workspace_bytes(1, 64, 1, 2048, 4096) == 256 + 8 * 64 * 2048
+    assert hs.resolve_workspace_bytes(4, 256, 4, 2048, 4096) == 4096 + 8 * 1024 * 4096
+    assert hs.resolve_workspace_bytes(1, 3, 1, 5, 4) == 16 + 8 * 3 * 4
+    assert hs.resolve_workspace_bytes(1, 1, 0, 5, 4) == 0
+    # the benchmarked shapes fit in one CTA's shared memory; oversize plans report 0 or > 227 KB
+    for P, K, C in ((1, 256, 512), (1, 2048, 4096), (4, 2048, 4096)):
+        assert 0 < hs.resolve_smem_bytes(P, K, C) <= 227 * 1024
+    assert hs.resolve_smem_bytes(1, 16385, 4096) == 0
+    assert hs.resolve_smem_bytes(1, 16, 16385) == 0
+
+
+def test_pool_create_rejects_bad_descriptions_before_touching_a_device(lib):
+    L = lib
+    h = ctypes.c_void_p()
+    assert L.hs_pool_create(None, ctypes.byref(h)) == 1
+    buf = (ctypes.c_void_p * 1)(ctypes.c_void_p(16))
+    bad = [
+        hs.PoolDesc(0, 64, 656, 10, 0, ctypes.cast(buf, ctypes.POINTER(ctypes.c_void_p)), None),
+        hs.PoolDesc(1, 64, 650, 10, 0, ctypes.cast(buf, ctypes.POINTER(ctypes.c_void_p)), None),
+        hs.PoolDesc(1, 0, 656, 10, 0, ctypes.cast(buf, ctypes.POINTER(ctypes.c_void_p)), None),
+        hs.PoolDesc(1, 64, 656, 1 << 26, 0, ctypes.cast(buf, ctypes.POINTER(ctypes.c_void_p)), None),
+        hs.PoolDesc(1, 64, 656, 10, 5, ctypes.cast(buf, ctypes.POINTER(ctypes.c_void_p)), None),
+        hs.PoolDesc(1, 64, 656, 10, 0, None, None),
+        hs.PoolDesc(129, 64, 656, 10, 0, ctypes.cast(buf, ctypes.POINTER(ctypes.c_void_p)), None),
+    ]
+    for d in bad:
+        assert L.hs_pool_create(ctypes.byref(d), ctypes.byref(h)) == 1
+        assert not h.value
+    mis = (ctypes.c_void_p * 1)(ctypes.c_void_p(24))   # not 16-byte aligned
+    d = hs.PoolDesc(1, 64, 656, 10, 0, ctypes.cast(mis, ctypes.POINTER(ctypes.c_void_p)), None)
+    assert L.hs_pool_create(ctypes.byref(d), ctypes.byref(h)) == 1
+
+
+def test_calls_on_null_handles_are_rejected(lib):
+    L = lib
+    hot = hs.HotStateC(64, None, None, None)
+    assert L.hs_resolve_topk(None, 0, 1, 1, 1, 1, None, None, None, None, 1, ctypes.byref(hot), 0, None, None, None,
+                             0, None) == 1
+    assert L.hs_gather_rows(None, 0, 1, None, 1, None, None, None) == 1
+    assert L.hs_offload_pages(None, None, None, 1, None, None) == 1
+    assert L.hs_hot_reset(None, ctypes.byref(hot), 1, None) == 1
+    assert L.hs_launch_count() == 0

@@ -1,0 +1,277 @@
+"""GPU parity: the CUDA library (through its C ABI) against the oracle, bit for bit.
+
+Compared on every step: out_rows, out_stats, slot_token, slot_stamp (oracle), gathered bytes
+(closed-form row contents), and pool bytes (oracle with byte pools) or hot-slot bytes (closed form).
+Tolerance is zero everywhere: this is integer and byte work."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_mla_kv_gb300 as hs
+from synth import workloads
+from tests.casekit import Case
+from tests.test_bruteforce_vs_oracle import _ids, _random_case
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_mla_kv_gb300 import _build
+    _build.build()
+    hs.lib()
+
+
+def _rig(w, **kw):
+    from tests.gpukit import Rig
+    return Rig(w, **kw)
+
+
+def test_tiny_decode_all_bytes():
+    w = workloads.config1(seed=0, steps=8)
+    rig = _rig(w, oracle_bytes=True)
+    misses = 0
+    for st in w.iter_steps():
+        _, stats, _, _, _ = rig.step(st)
+        misses += int(stats[..., 3].sum())
+    assert misses > 0
+
+
+def test_tiny_decode_other_seeds_and_replay():
+    for seed in (1, 2):
+        w = workloads.config1(seed=seed, steps=6)
+        rig = _rig(w, oracle_bytes=True)
+        for st in w.iter_steps():
+            rows, stats, *_ = rig.step(st)
+            # replay the same step: same rows, no misses, state unchanged
+            tok = rig.hot.slot_token.clone()
+            rows2, stats2, *_ = rig.step(st)
+            assert torch.equal(rows, rows2)
+            assert int(stats2[..., 3].sum()) == 0
+            assert torch.equal(tok, rig.hot.slot_token)
+
+
+def _case_to_gpu(case, dev):
+    S, B = case.S, case.B
+    gpu = [torch.from_numpy(case.pools[0].reshape(case.ngb, S, B).copy()).to(dev)]
+    host = [torch.from_numpy(case.hosts[0].reshape(-1, S, B).copy()).pin_memory()]
+    pool = hs.Pool(gpu, host)
+    hot_blocks = torch.from_numpy(case.hot_blocks).to(dev)
+    hot = hs.HotState.allocate(1, hot_blocks, case.C)
+    hs.hot_reset(pool, hot)
+    return pool, gpu, host, hot
+
+
+def test_random_small_cases_vs_oracle():
+    """Random small shapes (page sizes 1/2/4, several positions, duplicates, padding, replays,
+    invalid ids, steps going backwards) through the library and the oracle with byte pools."""
+    rng = np.random.default_rng(777)
+    dev = torch.device("cuda")
+    seen = set()
+    for ci in range(150):
+        case, P, K = _random_case(rng)
+        pool, gpu, host, hot = _case_to_gpu(case, dev)
+        bt, hbt = torch.from_numpy(case.bt).to(dev), torch.from_numpy(case.hbt).to(dev)
+        ctx = torch.from_numpy(case.ctx).to(dev)
+        t = 0
+        for si in range(int(rng.integers(1, 10))):
+            u = rng.random()
+            t = t if u < 0.1 else (max(0, t - 2) if u < 0.13 else t + int(rng.integers(1, 3)))
+            ids = _ids(rng, case, P, K)
+            rows, stats = hs.resolve_topk(pool, torch.from_numpy(ids[None]).to(dev), bt, hbt, ctx, hot, t)
+            o_rows, o_stats = case.step(ids, t)
+            torch.cuda.synchronize()
+            seen.update(o_stats[0, :, 0].tolist())
+            msg = f"case {ci} step {si}"
+            assert np.array_equal(stats.cpu().numpy(), o_stats), msg
+            assert np.array_equal(rows.cpu().numpy(), o_rows), msg
+            assert np.array_equal(hot.slot_token.cpu().numpy(), case.tok), msg
+            assert np.array_equal(hot.slot_stamp.cpu().numpy(), case.stamp), msg
+            assert np.array_equal(gpu[0].cpu().numpy().reshape(-1), case.pools[0]), msg
+            g = hs.gather_rows(pool, rows.reshape(1, -1))
+            o_out, _ = case.gather(o_rows.reshape(1, -1))
+            assert np.array_equal(g.cpu().numpy(), o_out), msg
+        pool.close()
+    assert {0, 2, 5}.issubset(seen)
+
+
+def test_mixed_residency_decode_full_size():
+    """The 64-request, 131072-token, K=2048 mixed-residency batch (the benchmarked workload) for all
+    of its 64 steps."""
+    w = workloads.config2(seed=0, steps=64)
+    rig = _rig(w)
+    tot = np.zeros(3, np.int64)
+    for st in w.iter_steps():
+        _, stats, *_ = rig.step(st)
+        tot += stats[..., 1:].sum(axis=(0, 1)).cpu().numpy()
+    assert tot[1] > 0 and tot[2] > 0   # both hits and misses happened
+
+
+def test_cold_start_prefix_reuse_full_size():
+    """16 requests reusing a 1,048,576-token host-only prefix, empty hot buffers, 32 steps."""
+    w = workloads.config4(seed=0, steps=32)
+    rig = _rig(w)
+    for st in w.iter_steps():
+        _, stats, *_ = rig.step(st)
+    assert int(stats[..., 3].sum()) > 0
+
+
+def test_data_errors_are_isolated_per_unit():
+    w = workloads.config1(seed=3, steps=3)
+    rig = _rig(w, oracle_bytes=True)
+    steps = list(w.iter_steps())
+    rig.step(steps[0])
+    st = steps[1]
+    st.topk[0, 1, 0, 5] = 5000          # out of range for request 1
+    st.topk[0, 2, 0, 7] = -7            # invalid id for request 2
+    rows, stats, *_ = rig.step(st)
+    s = stats.cpu().numpy()[0]
+    assert s[1, 0] == 2 and s[2, 0] == 2 and s[0, 0] == 0 and s[3, 0] == 0
+    st2 = steps[2]
+    st2.index = 0   # older than the stamps of requests 0 and 3 (step 1); requests 1 and 2 failed at
+    rows, stats, *_ = rig.step(st2)   # step 1, so their newest stamp is still 0 and step 0 replays
+    assert stats.cpu().numpy()[0, :, 0].tolist() == [5, 0, 0, 5]
+
+
+def test_empty_and_degenerate_shapes():
+    dev = torch.device("cuda")
+    case = Case(R=2, S=4, B=16, C=8, max_pages=4, ctx=[16, 16], resident=True, host=True,
+                hot_blocks=[[0, 1], [2, 3]], num_gpu_blocks=6, num_host_blocks=8, bt=[[-1, -1, -1, 4], [-1, -1, -1, 5]],
+                hbt=[[0, 1, 2, 3], [4, 5, 6, 7]])
+    pool, gpu, host, hot = _case_to_gpu(case, dev)
+    bt, hbt = torch.from_numpy(case.bt).to(dev), torch.from_numpy(case.hbt).to(dev)
+    ctx = torch.from_numpy(case.ctx).to(dev)
+    # K = 0: an empty plan; stats OK with zero counts
+    rows, stats = hs.resolve_topk(pool, torch.zeros((1, 2, 1, 0), dtype=torch.int32, device=dev), bt, hbt, ctx, hot, 0)
+    assert stats.cpu().tolist() == [[[0, 0, 0, 0], [0, 0, 0, 0]]]
+    # all padding
+    ids = torch.full((1, 2, 2, 3), -1, dtype=torch.int32, device=dev)
+    rows, stats = hs.resolve_topk(pool, ids, bt, hbt, ctx, hot, 1)
+    assert (rows == -1).all() and stats.cpu().tolist() == [[[0, 0, 0, 0], [0, 0, 0, 0]]]
+    # zero requests / zero layers: no-op
+    hs.resolve_topk(pool, torch.zeros((0, 2, 1, 4), dtype=torch.int32, device=dev), bt, hbt, ctx, hot, 1)
+    out = hs.gather_rows(pool, torch.zeros((1, 0), dtype=torch.int32, device=dev))
+    assert out.numel() == 0
+    # every slot used in one step: capacity exactly C
+    ids = torch.tensor([[[[0, 1, 2, 3, 4, 5, 6, 7]], [[8, 9, 10, 11, 0, 1, 2, 3]]]], dtype=torch.int32, device=dev)
+    rows, stats = hs.resolve_topk(pool, ids, bt, hbt, ctx, hot, 2)
+    o_rows, o_stats = case.step(ids.cpu().numpy()[0], 2)
+    assert np.array_equal(stats.cpu().numpy(), o_stats) and np.array_equal(rows.cpu().numpy(), o_rows)
+    assert o_stats[0, :, 3].tolist() == [8, 8]
+    pool.close()
+
+
+def test_largest_shapes_and_shape_limits():
+    """P*K = 8192 ids with C = 4096 (the MTP3 shape) and C = 16384 with a short plan: parity on one
+    step; a plan that does not fit in shared memory is rejected on the host."""
+    dev = torch.device("cuda")
+    rng = np.random.default_rng(5)
+    for P, K, C in ((4, 2048, 4096), (1, 1024, 16384), (1, 4096, 8192)):
+        S, B, R, pages = 64, 32, 3, 512
+        ctx = pages * S
+        nb = C // S
+        ngb = R * nb + R * 16
+        perm = rng.permutation(ngb).astype(np.int32)
+        hot_blocks = perm[:R * nb].reshape(R, nb)
+        bt = np.full((R, pages), -1, np.int32)
+        bt[:, pages - 16:] = perm[R * nb:].reshape(R, 16)
+        hbt = rng.permutation(R * pages).astype(np.int32).reshape(R, pages)
+        case = Case(R=R, S=S, B=B, C=C, max_pages=pages, ctx=[ctx] * R, resident=True, host=True,
+                    hot_blocks=hot_blocks, num_gpu_blocks=ngb, num_host_blocks=R * pages, bt=bt, hbt=hbt)
+        pool, gpu, host, hot = _case_to_gpu(case, dev)
+        bt_t, hbt_t, ctx_t = (torch.from_numpy(x).to(dev) for x in (case.bt, case.hbt, case.ctx))
+        for t in range(3):
+            base = [rng.choice(ctx, K, replace=False) for _ in range(R)]
+            ids = np.stack([np.stack([np.where(rng.random(K) < 0.9, b, rng.integers(0, ctx, K)) for _ in range(P)])
+                            for b in base]).astype(np.int32)
+            rows, stats = hs.resolve_topk(pool, torch.from_numpy(ids[None]).to(dev), bt_t, hbt_t, ctx_t, hot, t)
+            o_rows, o_stats = case.step(ids, t)
+            torch.cuda.synchronize()
+            assert np.array_equal(stats.cpu().numpy(), o_stats), (P, K, C, t)
+            assert np.array_equal(rows.cpu().numpy(), o_rows), (P, K, C, t)
+            assert np.array_equal(hot.slot_token.cpu().numpy(), case.tok)
+            assert np.array_equal(hot.slot_stamp.cpu().numpy(), case.stamp)
+            assert np.array_equal(gpu[0].cpu().numpy().reshape(-1), case.pools[0])
+        pool.close()
+    assert hs.resolve_smem_bytes(8, 2048, 16384) == 0 or hs.resolve_smem_bytes(8, 2048, 16384) > 227 * 1024
+
+
+def test_gather_standalone_multilayer_and_status():
+    dev = torch.device("cuda")
+    L, S, B, ngb = 3, 8, 656, 40
+    gpu = [torch.randint(0, 256, (ngb, S, B), dtype=torch.uint8, device=dev) for _ in range(L)]
+    pool = hs.Pool(gpu, None)
+    rng = np.random.default_rng(1)
+    n = 5003  # ragged tail
+    rows = rng.integers(-1, ngb * S, size=(L, n)).astype(np.int32)
+    out = hs.gather_rows(pool, torch.from_numpy(rows).to(dev))
+    pools_np = [g.cpu().numpy().reshape(-1) for g in gpu]
+    o_out, st = oracle.gather(B=B, num_rows=ngb * S, pools=pools_np, rows=rows)
+    assert st == 0 and np.array_equal(out.cpu().numpy(), o_out)
+    bad = rows.copy()
+    bad[1, 17] = ngb * S
+    bad[2, 4000] = -9
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = hs.gather_rows(pool, torch.from_numpy(bad).to(dev), status=status)
+    o_out, st = oracle.gather(B=B, num_rows=ngb * S, pools=pools_np, rows=bad)
+    assert int(status.item()) == st == 2 and np.array_equal(out.cpu().numpy(), o_out)
+    # a layer window
+    out = hs.gather_rows(pool, torch.from_numpy(rows[:2]).to(dev), layer_begin=1)
+    o_out, _ = oracle.gather(B=B, num_rows=ngb * S, pools=pools_np, rows=rows[:2], layer_begin=1)
+    assert np.array_equal(out.cpu().numpy(), o_out)
+    pool.close()
+
+
+def test_offload_standalone_all_layers_one_launch():
+    dev = torch.device("cuda")
+    L, S, B, ngb, nhb = 4, 64, 656, 30, 50
+    gpu = [torch.randint(0, 256, (ngb, S, B), dtype=torch.uint8, device=dev) for _ in range(L)]
+    host = [torch.zeros((nhb, S, B), dtype=torch.uint8).pin_memory() for _ in range(L)]
+    pool = hs.Pool(gpu, host)
+    gb = np.array([3, 17, 0, 29, 8], np.int32)
+    hb = np.array([49, 0, 7, 21, 22], np.int32)
+    n0 = hs.launch_count()
+    hs.offload_pages(pool, torch.from_numpy(gb).to(dev), torch.from_numpy(hb).to(dev))
+    assert hs.launch_count() - n0 == 1
+    torch.cuda.synchronize()
+    pools_np = [g.cpu().numpy().reshape(-1) for g in gpu]
+    hosts_np = [np.zeros(nhb * S * B, np.uint8) for _ in range(L)]
+    oracle.offload(S=S, B=B, num_gpu_blocks=ngb, num_host_blocks=nhb, pools=pools_np, hosts=hosts_np, gpu_blocks=gb,
+                   host_blocks=hb)
+    for l in range(L):
+        assert np.array_equal(host[l].numpy().reshape(-1), hosts_np[l])
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    hs.offload_pages(pool, torch.tensor([ngb], dtype=torch.int32, device=dev),
+                     torch.tensor([0], dtype=torch.int32, device=dev), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 8
+    for l in range(L):
+        assert np.array_equal(host[l].numpy().reshape(-1), hosts_np[l])
+    pool.close()
+
+
+def test_host_argument_errors():
+    dev = torch.device("cuda")
+    gpu = [torch.zeros((4, 4, 16), dtype=torch.uint8, device=dev)]
+    with pytest.raises(TypeError):
+        hs.Pool(gpu, [torch.zeros((4, 4, 16), dtype=torch.uint8)])      # host memory not pinned
+    pool = hs.Pool(gpu, [torch.zeros((4, 4, 16), dtype=torch.uint8).pin_memory()])
+    hot = hs.HotState.allocate(1, torch.tensor([[0, 1]], dtype=torch.int32, device=dev), 8)
+    bt = torch.full((1, 4), -1, dtype=torch.int32, device=dev)
+    ctx = torch.tensor([16], dtype=torch.int32, device=dev)
+    ids = torch.zeros((1, 1, 1, 2), dtype=torch.int32, device=dev)
+    with pytest.raises(hs.HSError) as e:
+        hs.resolve_topk(pool, ids, bt, bt, ctx, hot, -1)             # negative step
+    assert e.value.code == 1
+    with pytest.raises(hs.HSError):
+        hs.resolve_topk(pool, ids, bt, bt, ctx, hot, 0, layer_begin=1)  # layer window outside the pool
+    small_ws = torch.empty(16, dtype=torch.uint8, device=dev)
+    with pytest.raises(hs.HSError):
+        hs.resolve_topk(pool, ids, bt, bt, ctx, hot, 0, workspace=small_ws)
+    bad_cap = hs.HotState.allocate(1, torch.tensor([[0, 1]], dtype=torch.int32, device=dev), 6)  # not a page multiple
+    with pytest.raises(hs.HSError):
+        hs.resolve_topk(pool, ids, bt, bt, ctx, bad_cap, 0)
+    pool.close()
