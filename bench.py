@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--soak-seconds", type=float, default=1.5)
+    ap.add_argument("--path", choices=["fused", "split"], default="fused",
+                    help="fused: hs_resolve_plan + hs_gather_planned (miss copies inside the gather); "
+                         "split: hs_resolve_topk (resolver + miss-copy kernel) + hs_gather_rows")
     return ap.parse_args()
 
 
@@ -228,7 +231,8 @@ def config_dict(w, args):
                         f"row {w.B} B, K={w.K}, P={w.P}, hot {w.C} rows/request",
             "layers": w.L, "requests": w.R, "ctx": int(w.ctx_len[0]), "page": w.S, "row_bytes": w.B, "K": w.K,
             "P": w.P, "hot_rows": w.C, "rows_per_step": w.rows_per_step, "seed": args.seed,
-            "index_dtype": "int32", "l2": "flushed (256 MB write) before every timed step, outside the timing"}
+            "index_dtype": "int32", "l2": "flushed (256 MB write) before every timed step, outside the timing",
+            "path": getattr(args, "path", "fused")}
 
 
 # ----------------------------------------------------------------------------- the GPU leg
@@ -281,10 +285,18 @@ def run_ours(args, ws, rank, local):
     h2d_gbs = 4 * (256 << 20) / (e0.elapsed_time(e1) * 1e-3) / 1e9
     del hbuf, dbuf
 
+    fused = args.path == "fused"
+
+    def phase1(i):
+        (prep.plan if fused else prep.resolve)(topk_all[i], steps[i].index)
+
+    def phase2():
+        (prep.gather_planned if fused else prep.gather)()
+
     # warm-up steps
     for i in range(W):
-        prep.resolve(topk_all[i], steps[i].index)
-        prep.gather()
+        phase1(i)
+        phase2()
     torch.cuda.synchronize()
     st_w = out_stats.cpu().numpy()
     assert (st_w[..., 0] == 0).all(), "warm-up step reported a data error"
@@ -295,12 +307,11 @@ def run_ours(args, ws, rank, local):
     t_end = time.time() + args.soak_seconds
     while time.time() < t_end:
         for _ in range(50):
-            prep.gather()
+            prep.gather()   # plain gather of the last rows: reads only
         torch.cuda.synchronize()
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    miss_total = 0
-    stats_acc = np.zeros(3, np.int64)
+    stats_all = torch.empty((K, L, R, 4), dtype=torch.int32, device=dev)
     barrier(dist)
     torch.cuda.synchronize()
     n_launch0 = hs.launch_count()
@@ -309,10 +320,11 @@ def run_ours(args, ws, rank, local):
         i = W + k
         flush.fill_(k & 0xFF)
         ev[k][0].record(stream)
-        prep.resolve(topk_all[i], steps[i].index)
+        phase1(i)
         ev[k][1].record(stream)
-        prep.gather()
+        phase2()
         ev[k][2].record(stream)
+        stats_all[k].copy_(out_stats, non_blocking=True)   # after the step's events: not timed
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     barrier(dist)
@@ -321,39 +333,47 @@ def run_ours(args, ws, rank, local):
     t_step = [ev[k][0].elapsed_time(ev[k][2]) * 1e-3 for k in range(K)]
     t_res = [ev[k][0].elapsed_time(ev[k][1]) * 1e-3 for k in range(K)]
     t_gat = [ev[k][1].elapsed_time(ev[k][2]) * 1e-3 for k in range(K)]
-    st_last = out_stats.cpu().numpy()
-    assert (st_last[..., 0] == 0).all(), "a timed step reported a data error"
+    st_all = stats_all.cpu().numpy()
+    assert (st_all[..., 0] == 0).all(), "a timed step reported a data error"
     sum_t = max_over_ranks(dist, float(sum(t_step)), dev)
-
-    # exact per-step work from the oracle-free stats of a replay is not needed: count misses by
-    # re-running the same steps' stats is costly, so take them from the warm-up + last step
-    hits_misses = st_last[..., 1:].sum(axis=(0, 1))
+    counts = st_all[..., 1:].sum(axis=(1, 2))           # [K][resident, hits, misses]
+    hits_misses = counts.sum(axis=0)
 
     rows_per_step = w.rows_per_step
     value = ws * rows_per_step * K / sum_t
     ms_per_step = 1e3 * sum_t / K
 
-    # roofline of the dominant kernel (gather): algorithmic bytes per launch / mean launch time
+    # roofline of the dominant kernel (the gather; fused path: the gather that also carries the miss
+    # copies): algorithmic HBM bytes per launch / mean launch time from the events around it.
+    # Per gathered row: 656 B out + 4 B row id (+ 4 B host source when fused) + 656 B row read from
+    # HBM -- or, for a miss in the fused path, 656 B read over the host link and 656 B into its slot.
     hbm_peak, peak_kind = measured_peaks()
     n_rows = L * R * P * Kk
-    gather_bytes = n_rows * (2 * B + 4)
+    m_mean = float(counts[:, 2].mean())
+    gather_bytes = n_rows * (2 * B + (8 if fused else 4))
     t_g = statistics.fmean(t_gat)
     achieved = gather_bytes / t_g / 1e9
-    tr = traffic_record("gather_kernel", "gather.cu")
-    roofline = {"bound": "hbm", "kernel": "gather_kernel", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak, "peak_kind": peak_kind,
-                "algorithmic_bytes_per_launch": gather_bytes,
-                "traffic": (tr["dram_bytes_per_launch"] * (n_rows / tr["rows"]) if tr else None)}
+    tr = traffic_record("gather_kernel_fused" if fused else "gather_kernel", "gather.cu")
+    roofline = {"bound": "hbm", "kernel": "gather_kernel<fused>" if fused else "gather_kernel",
+                "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                "peak_kind": peak_kind, "algorithmic_bytes_per_launch": gather_bytes,
+                "host_link_bytes_per_launch": (m_mean * B if fused else 0.0),
+                "traffic": (tr["dram_bytes_per_launch"] if tr else None)}
 
-    # whole-step roofline: max(HBM bytes / HBM peak, miss bytes / measured host-link bandwidth)
-    misses_last = int(st_last[..., 3].sum())
-    hbm_step = n_rows * (2 * B + 16) + L * R * 8 * C + misses_last * (B + 8)
-    h2d_step = misses_last * B
-    t_roof = max(hbm_step / (hbm_peak * 1e9), h2d_step / (h2d_gbs * 1e9))
-    step_roof = {"t_roof_us": t_roof * 1e6, "t_measured_us": 1e6 * statistics.fmean(t_step),
-                 "frac": t_roof / statistics.fmean(t_step), "hbm_bytes": hbm_step, "h2d_bytes": h2d_step,
-                 "h2d_gbs_measured": h2d_gbs, "basis": "misses of the last timed step",
-                 "resolve_us_mean": 1e6 * statistics.fmean(t_res), "gather_us_mean": 1e6 * t_g}
+    # whole-step roofline: max(HBM bytes / HBM peak, miss bytes / measured host-link bandwidth),
+    # step by step with each step's own miss count
+    roofs, meas = [], []
+    for k in range(K):
+        m = int(counts[k, 2])
+        hbm_step = n_rows * (2 * B + 16) + L * R * 8 * C + m * (B + 8)
+        roofs.append(max(hbm_step / (hbm_peak * 1e9), m * B / (h2d_gbs * 1e9)))
+        meas.append(t_step[k])
+    step_roof = {"t_roof_us": 1e6 * statistics.fmean(roofs), "t_measured_us": 1e6 * statistics.fmean(meas),
+                 "frac": sum(roofs) / sum(meas), "misses_per_step_mean": m_mean,
+                 "h2d_gbs_measured_bulk_copy": h2d_gbs, "path": args.path,
+                 "phase1_us_mean": 1e6 * statistics.fmean(t_res), "phase2_us_mean": 1e6 * t_g,
+                 "phase1": "hs_resolve_plan" if fused else "hs_resolve_topk (resolver + miss copy)",
+                 "phase2": "hs_gather_planned" if fused else "hs_gather_rows"}
 
     # end to end through the C ABI with host buffers: H2D of the step's top-K and contexts, D2H of
     # its rows and stats, inside the timed events (hot state reset, warm-up replayed first)
@@ -366,10 +386,16 @@ def run_ours(args, ws, rank, local):
         stats_host = torch.empty((L, R, 4), dtype=torch.int32, pin_memory=True)
         topk_dev = torch.empty((L, R, P, Kk), dtype=torch.int32, device=dev)
         prep2 = hs.PreparedStep(pool, hot, bt, hbt, ctx, out_rows, out_stats, ws_buf, gout, stream=stream)
+        def e2e_step(i):
+            if fused:
+                prep2.resolve_gather(topk_dev, steps[i].index)
+            else:
+                prep2.resolve(topk_dev, steps[i].index)
+                prep2.gather()
+
         for i in range(W):
             topk_dev.copy_(topk_host[i], non_blocking=True)
-            prep2.resolve(topk_dev, steps[i].index)
-            prep2.gather()
+            e2e_step(i)
         torch.cuda.synchronize()
         ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
         barrier(dist)
@@ -379,8 +405,7 @@ def run_ours(args, ws, rank, local):
             ev2[k][0].record(stream)
             topk_dev.copy_(topk_host[i], non_blocking=True)
             ctx.copy_(ctx_host, non_blocking=True)
-            prep2.resolve(topk_dev, steps[i].index)
-            prep2.gather()
+            e2e_step(i)
             rows_host.copy_(out_rows, non_blocking=True)
             stats_host.copy_(out_stats, non_blocking=True)
             ev2[k][1].record(stream)
@@ -408,9 +433,9 @@ def run_ours(args, ws, rank, local):
             "dtype": "u8", "data": "synthetic", "config": config_dict(w, args),
             "gathered_gbs": value * B / 1e9, "roofline": roofline, "step_roofline": step_roof,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
-            "wall_s_timed_region": wall, "last_step_counts": {"resident": int(hits_misses[0]),
-                                                               "hits": int(hits_misses[1]),
-                                                               "misses": int(hits_misses[2])},
+            "wall_s_timed_region": wall, "timed_counts": {"resident": int(hits_misses[0]),
+                                                          "hits": int(hits_misses[1]),
+                                                          "misses": int(hits_misses[2])},
         }
         print(json.dumps(line), flush=True)
     pool.close()

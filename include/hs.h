@@ -111,12 +111,14 @@ void hs_pool_destroy(hs_pool* pool);
 /* Sets slot_token and slot_stamp of all num_layers x R x capacity slots to -1 (async). */
 hs_status hs_hot_reset(const hs_pool* pool, const hs_hot_state* hot, int32_t R, hs_stream_t stream);
 
-/* Bytes of caller-owned device workspace that hs_resolve_topk needs for this shape (the per-unit
- * miss lists handed from the resolver kernel to the miss-copy kernel).  0 on a bad shape. */
+/* Bytes of caller-owned device workspace that hs_resolve_topk and hs_resolve_gather need for this
+ * shape (per-unit miss lists handed from the resolver kernel to the miss-copy kernel, or per-position
+ * host sources handed to the fused gather).  0 on a bad shape. */
 size_t hs_resolve_workspace_bytes(int32_t nl, int32_t R, int32_t P, int32_t K, int32_t capacity);
 
-/* Dynamic shared memory one resolver CTA needs for this shape, or 0 if the shape exceeds a limit. */
-size_t hs_resolve_smem_bytes(int32_t P, int32_t K, int32_t capacity);
+/* Dynamic shared memory one resolver CTA needs for this shape, or 0 if the shape exceeds a limit.
+ * Resolve calls reject shapes whose footprint exceeds the device's per-block opt-in maximum. */
+size_t hs_resolve_smem_bytes(int32_t P, int32_t K, int32_t capacity, int32_t page_size);
 
 /* The fused top-K resolver for layers [layer_begin, layer_begin + nl) and R requests at decode
  * step `step`.  One (layer, request) pair is one independent unit:
@@ -148,6 +150,41 @@ hs_status hs_resolve_topk(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
                           const int32_t* host_block_table, const int32_t* ctx_len, int32_t max_pages,
                           const hs_hot_state* hot, int32_t step, int32_t* out_rows, int32_t* out_stats,
                           void* workspace, size_t workspace_bytes, hs_stream_t stream);
+
+/* Resolve and gather in one call: the same results as hs_resolve_topk followed by
+ * hs_gather_rows(out_rows) over all nl*R*P*K positions -- out_rows, out_stats, hot state and pool bytes
+ * identical, and out[l][(r*P + p)*K + k] = the row of topk_ids[l][r][p][k].  The miss copy is fused
+ * into the gather: the resolver marks each miss position with its host row, and the gather reads
+ * those rows straight from the pinned host pool (storing the first occurrence of each into its hot
+ * slot) while resident and hit rows come from HBM in the same launch, so host-link and HBM traffic
+ * overlap instead of running back to back.  The consumer then reads hot rows as ordinary pool rows
+ * (Japanese article, section "仕組み": the sparse MLA kernel sees hot pages as normal pages).
+ * Equivalent to hs_resolve_plan followed by hs_gather_planned on the same stream.
+ *   out        device [nl][R*P*K][row_bytes] bytes, 16-byte aligned.
+ *   workspace  as for hs_resolve_topk (hs_resolve_workspace_bytes covers every resolve call). */
+hs_status hs_resolve_gather(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P,
+                            int32_t K, const int32_t* topk_ids, const int32_t* block_table,
+                            const int32_t* host_block_table, const int32_t* ctx_len, int32_t max_pages,
+                            const hs_hot_state* hot, int32_t step, int32_t* out_rows, int32_t* out_stats,
+                            void* out, void* workspace, size_t workspace_bytes, hs_stream_t stream);
+
+/* First half of hs_resolve_gather (one launch): everything hs_resolve_topk does except the miss
+ * copies.  Rows, stats and hot state are final; the victims' pool rows are NOT yet filled -- the
+ * per-position host sources wait in `workspace` for hs_gather_planned, which must follow on the same
+ * stream before anything reads those rows.  Same arguments as hs_resolve_topk. */
+hs_status hs_resolve_plan(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P,
+                          int32_t K, const int32_t* topk_ids, const int32_t* block_table,
+                          const int32_t* host_block_table, const int32_t* ctx_len, int32_t max_pages,
+                          const hs_hot_state* hot, int32_t step, int32_t* out_rows, int32_t* out_stats,
+                          void* workspace, size_t workspace_bytes, hs_stream_t stream);
+
+/* Second half of hs_resolve_gather (one launch): gathers all nl*R*P*K rows named by out_rows into
+ * `out`, taking miss rows from the pinned host pool as recorded by hs_resolve_plan in `workspace`
+ * and filling their hot slots.  nl, R, P, K, capacity, layer_begin, out_rows and workspace must be
+ * those of the preceding hs_resolve_plan call. */
+hs_status hs_gather_planned(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P,
+                            int32_t K, int32_t capacity, const int32_t* out_rows, const void* workspace,
+                            size_t workspace_bytes, void* out, hs_stream_t stream);
 
 /* Single-stride gather: out[l][i] = row rows[l][i] of layer layer_begin + l, for l < nl, i < n.
  *   rows        device int32 [nl][n]; -1 gives row_bytes zero bytes.

@@ -71,10 +71,17 @@ def lib():
         L.hs_resolve_workspace_bytes.restype = sz
         L.hs_resolve_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
         L.hs_resolve_smem_bytes.restype = sz
-        L.hs_resolve_smem_bytes.argtypes = [i32, i32, i32]
+        L.hs_resolve_smem_bytes.argtypes = [i32, i32, i32, i32]
         L.hs_resolve_topk.restype = i32
         L.hs_resolve_topk.argtypes = [p, i32, i32, i32, i32, i32, p, p, p, p, i32, ctypes.POINTER(HotStateC), i32, p, p,
                                       p, sz, p]
+        L.hs_resolve_gather.restype = i32
+        L.hs_resolve_gather.argtypes = [p, i32, i32, i32, i32, i32, p, p, p, p, i32, ctypes.POINTER(HotStateC), i32, p,
+                                        p, p, p, sz, p]
+        L.hs_resolve_plan.restype = i32
+        L.hs_resolve_plan.argtypes = L.hs_resolve_topk.argtypes
+        L.hs_gather_planned.restype = i32
+        L.hs_gather_planned.argtypes = [p, i32, i32, i32, i32, i32, i32, p, p, sz, p, p]
         L.hs_gather_rows.restype = i32
         L.hs_gather_rows.argtypes = [p, i32, i32, p, i64, p, p, p]
         L.hs_offload_pages.restype = i32
@@ -198,8 +205,8 @@ def resolve_workspace_bytes(nl: int, R: int, P: int, K: int, capacity: int) -> i
     return int(lib().hs_resolve_workspace_bytes(nl, R, P, K, capacity))
 
 
-def resolve_smem_bytes(P: int, K: int, capacity: int) -> int:
-    return int(lib().hs_resolve_smem_bytes(P, K, capacity))
+def resolve_smem_bytes(P: int, K: int, capacity: int, page_size: int = 64) -> int:
+    return int(lib().hs_resolve_smem_bytes(P, K, capacity, page_size))
 
 
 def alloc_workspace(nl: int, R: int, P: int, K: int, capacity: int, device) -> torch.Tensor:
@@ -235,6 +242,38 @@ def resolve_topk(pool: Pool, topk: torch.Tensor, block_table: torch.Tensor, host
                                  ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream(stream))
     _check(code, "hs_resolve_topk")
     return out_rows, out_stats
+
+
+def resolve_gather(pool: Pool, topk: torch.Tensor, block_table: torch.Tensor, host_block_table: torch.Tensor,
+                   ctx_len: torch.Tensor, hot: HotState, step: int, *, layer_begin: int = 0,
+                   out_rows: Optional[torch.Tensor] = None, out_stats: Optional[torch.Tensor] = None,
+                   out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Resolve and gather in one call (miss copies fused into the gather).
+    Returns (out_rows [nl][R][P][K], out_stats [nl][R][4], out uint8 [nl][R*P*K][row_bytes])."""
+    if topk.dim() != 4:
+        raise ValueError("topk must be [nl][R][P][K]")
+    nl, R, P, K = (int(x) for x in topk.shape)
+    if block_table.dim() != 2 or block_table.shape[0] != R or tuple(host_block_table.shape) != tuple(block_table.shape):
+        raise ValueError("block tables must both be [R][max_pages]")
+    if hot.R != R:
+        raise ValueError("hot state has a different number of requests")
+    dev = topk.device
+    out_rows = torch.empty_like(topk) if out_rows is None else out_rows
+    out_stats = torch.empty((nl, R, 4), dtype=torch.int32, device=dev) if out_stats is None else out_stats
+    workspace = alloc_workspace(nl, R, P, K, hot.capacity, dev) if workspace is None else workspace
+    if out is None:
+        out = torch.empty((nl, R * P * K, pool.row_bytes), dtype=torch.uint8, device=dev)
+    if out.dtype != torch.uint8 or not out.is_cuda or not out.is_contiguous() or out.numel() != nl * R * P * K * pool.row_bytes:
+        raise TypeError("out must be a contiguous uint8 CUDA tensor of nl*R*P*K*row_bytes bytes")
+    code = lib().hs_resolve_gather(pool.handle, layer_begin, nl, R, P, K, _dev_i32(topk, "topk"),
+                                   _dev_i32(block_table, "block_table"),
+                                   _dev_i32(host_block_table, "host_block_table"), _dev_i32(ctx_len, "ctx_len"),
+                                   int(block_table.shape[1]), ctypes.byref(hot.c), int(step),
+                                   _dev_i32(out_rows, "out_rows"), _dev_i32(out_stats, "out_stats"),
+                                   ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(workspace.data_ptr()),
+                                   workspace.numel(), _stream(stream))
+    _check(code, "hs_resolve_gather")
+    return out_rows, out_stats, out
 
 
 def gather_rows(pool: Pool, rows: torch.Tensor, *, layer_begin: int = 0, out: Optional[torch.Tensor] = None,
@@ -301,6 +340,27 @@ class PreparedStep:
         _check(self.L.hs_resolve_topk(self.pool.handle, self.lb, nl, R, P, K, _dev_i32(topk, "topk"), *self.args_bt,
                                       self.max_pages, ctypes.byref(self.hot.c), int(step), self.rows, self.stats,
                                       self.ws, self.ws_n, self.stream), "hs_resolve_topk")
+
+    def plan(self, topk: torch.Tensor, step: int) -> None:
+        nl, R, P, K = self.shape
+        if tuple(topk.shape) != self.shape:
+            raise ValueError("topk shape differs from the prepared shape")
+        _check(self.L.hs_resolve_plan(self.pool.handle, self.lb, nl, R, P, K, _dev_i32(topk, "topk"), *self.args_bt,
+                                      self.max_pages, ctypes.byref(self.hot.c), int(step), self.rows, self.stats,
+                                      self.ws, self.ws_n, self.stream), "hs_resolve_plan")
+
+    def gather_planned(self) -> None:
+        nl, R, P, K = self.shape
+        _check(self.L.hs_gather_planned(self.pool.handle, self.lb, nl, R, P, K, self.hot.capacity, self.rows, self.ws,
+                                        self.ws_n, self.gout, self.stream), "hs_gather_planned")
+
+    def resolve_gather(self, topk: torch.Tensor, step: int) -> None:
+        nl, R, P, K = self.shape
+        if tuple(topk.shape) != self.shape:
+            raise ValueError("topk shape differs from the prepared shape")
+        _check(self.L.hs_resolve_gather(self.pool.handle, self.lb, nl, R, P, K, _dev_i32(topk, "topk"), *self.args_bt,
+                                        self.max_pages, ctypes.byref(self.hot.c), int(step), self.rows, self.stats,
+                                        self.gout, self.ws, self.ws_n, self.stream), "hs_resolve_gather")
 
     def gather(self) -> None:
         _check(self.L.hs_gather_rows(self.pool.handle, self.lb, self.shape[0], self.rows, self.n_per_layer, self.gout,

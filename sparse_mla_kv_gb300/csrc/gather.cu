@@ -1,22 +1,32 @@
-// Single-stride gather of resolved pool rows.
+// Single-stride gather of resolved pool rows, and the fused gather that carries the miss copies.
 //
 // Source: Japanese article (news.ainew.jp), section "仕組み" (How it works): whether a row sits in a
 // resident page or in the hot buffer, the resolver hands back pool (HMA) row ids and the rows are
 // gathered with one stride; hot pages live in the same KV tensor, so the consumer sees them as
-// ordinary pages.
+// ordinary pages.  "vLLM GLM 5.3 Optimizations: Hybrid HiSparse Offloading", "Technical
+// Implementation of Hybrid HiSparse": a miss copies a single row from pinned host memory.
 //
-// Design: HBM-bound byte copy.  The output is a flat array of 16-byte chunks; consecutive threads
-// take consecutive chunks, so every warp stores 512 contiguous bytes and reads one or two source
-// rows contiguously.  blockIdx.y selects the layer; a grid-stride loop over the layer's chunks is
-// unrolled so each thread keeps several 16-byte loads in flight.  Row ids are re-read per chunk
-// (a broadcast within the warp, served by L1).
+// gather_kernel        HBM-bound byte copy.  The output is a flat array of 16-byte chunks;
+//                      consecutive threads take consecutive chunks, so a warp stores 512 contiguous
+//                      bytes and reads one or two source rows contiguously.  blockIdx.y selects the
+//                      layer; the grid is exactly one resident wave, and each thread keeps
+//                      kGatherUnroll loads in flight.
+// gather_fused_kernel  the same gather for the rows a resolve plan left in the pool (resident and
+//                      hit rows), run by 6 of every 8 warps, while the other 2 warps of each CTA copy
+//                      the plan's misses: one read of each host row over the host link, stored both
+//                      into its hot slot and into the output.  Host-link and HBM traffic overlap in
+//                      one launch, and HBM warps never wait on host latency.
+#include <climits>
+
 #include "hs_internal.cuh"
 
 namespace hs {
 namespace {
 
+constexpr unsigned kFull = 0xffffffffu;
 constexpr int kGatherThreads = 256;
-constexpr int kGatherUnroll = 4;
+constexpr int kGatherUnroll = 8;
+constexpr int kMissWarps = 2;  // per CTA of the fused gather
 
 template <int CPR>
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const LayerPtrs ptrs, int32_t layer_begin,
@@ -56,22 +66,163 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const LayerPtrs 
   if (bad && status) *status = HS_ERR_ID_RANGE;
 }
 
+template <int CPR>
+__global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
+    const LayerPtrs ptrs, int32_t layer_begin, int32_t R, int32_t n, int32_t max_m, const int32_t* __restrict__ rows,
+    const int32_t* __restrict__ miss_count, const int4* __restrict__ miss_list, const int32_t* __restrict__ msrc,
+    uint8_t* __restrict__ out, int32_t row_bytes, int64_t num_rows) {
+  const int cpr = CPR ? CPR : (row_bytes >> 4);
+  const int lr = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* __restrict__ pool = ptrs.gpu[layer_begin + lr];
+  const uint8_t* __restrict__ host = ptrs.host[layer_begin + lr];
+  const int64_t per_layer = (int64_t)R * n;
+  uint8_t* __restrict__ lout = out + (int64_t)lr * per_layer * row_bytes;
+
+  if (warp < kMissWarps) {
+    // ---- miss warps: items (request, group of kMissRowsPerItem misses) of this layer, numbered
+    // group-major so live items are the low numbers; lane j of miss-warp w tests item w + j * nmw.
+    constexpr int kU = CPR ? (kMissRowsPerItem * CPR + 31) / 32 : 4;
+    const int64_t mw = (int64_t)blockIdx.x * kMissWarps + warp;
+    const int64_t nmw = (int64_t)gridDim.x * kMissWarps;
+    const int items_per_unit = (max_m + kMissRowsPerItem - 1) / kMissRowsPerItem;
+    const int64_t items = (int64_t)R * items_per_unit;
+    for (int64_t base = mw; base < items; base += nmw * 32) {
+      const int64_t item = base + (int64_t)lane * nmw;
+      int r = 0, group = 0, cnt = 0;
+      bool live = false;
+      if (item < items) {
+        group = (int)(item / R);
+        r = (int)(item - (int64_t)group * R);
+        cnt = miss_count[lr * R + r];
+        live = group * kMissRowsPerItem < cnt;
+      }
+      uint32_t todo = __ballot_sync(kFull, live);
+      while (todo) {
+        const int src_lane = __ffs(todo) - 1;
+        todo &= todo - 1u;
+        const int rq = __shfl_sync(kFull, r, src_lane);
+        const int g = __shfl_sync(kFull, group, src_lane);
+        const int c = __shfl_sync(kFull, cnt, src_lane);
+        const int r0 = g * kMissRowsPerItem;
+        const int nrows = min(kMissRowsPerItem, c - r0);
+        int4 ent = make_int4(0, 0, 0, 0);
+        if (lane < nrows) ent = miss_list[((int64_t)lr * R + rq) * max_m + r0 + lane];
+        const int total = nrows * cpr;
+        for (int f0 = 0; f0 < total; f0 += 32 * kU) {
+          uint4 v[kU];
+          int64_t pool_off[kU], out_off[kU];
+#pragma unroll
+          for (int k = 0; k < kU; ++k) {
+            const int f = f0 + k * 32 + lane;
+            const bool ok = f < total;
+            const int rr = ok ? f / cpr : 0;
+            const int cc = f - rr * cpr;
+            const int src = __shfl_sync(kFull, ent.x, rr);
+            const int dst = __shfl_sync(kFull, ent.y, rr);
+            const int pos = __shfl_sync(kFull, ent.z, rr);
+            pool_off[k] = -1;
+            out_off[k] = 0;
+            if (ok) {
+              v[k] = __ldcg(reinterpret_cast<const uint4*>(host + (int64_t)src * row_bytes) + cc);
+              pool_off[k] = (int64_t)dst * row_bytes + (int64_t)cc * 16;
+              out_off[k] = (int64_t)pos * row_bytes + (int64_t)cc * 16;
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < kU; ++k) {
+            if (pool_off[k] >= 0) {
+              *reinterpret_cast<uint4*>(pool + pool_off[k]) = v[k];
+              *reinterpret_cast<uint4*>(lout + out_off[k]) = v[k];
+            }
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // ---- HBM warps: every position the miss warps do not own (resident rows, hit rows, padding,
+  // and repeated positions of a miss, which read the host row again); one source word per position
+  constexpr int kHbmThreads = kGatherThreads - kMissWarps * 32;
+  const int32_t* __restrict__ lmsrc = msrc + (int64_t)lr * per_layer;
+  uint4* __restrict__ lout4 = reinterpret_cast<uint4*>(lout);
+  const int64_t total = per_layer * cpr;
+  const int64_t stride = (int64_t)gridDim.x * kHbmThreads;
+  for (int64_t c0 = (int64_t)blockIdx.x * kHbmThreads + (threadIdx.x - kMissWarps * 32); c0 < total;
+       c0 += stride * kGatherUnroll) {
+    uint4 v[kGatherUnroll];
+    bool st[kGatherUnroll];
+#pragma unroll
+    for (int k = 0; k < kGatherUnroll; ++k) {
+      const int64_t c = c0 + k * stride;
+      v[k] = make_uint4(0u, 0u, 0u, 0u);
+      st[k] = false;
+      if (c < total) {
+        const int64_t i = c / cpr;
+        const int j = (int)(c - i * cpr);
+        const int ms = __ldg(lmsrc + i);
+        if (ms >= 0) {
+          if (ms < num_rows) v[k] = __ldg(reinterpret_cast<const uint4*>(pool + (int64_t)ms * row_bytes) + j);
+          st[k] = true;
+        } else if (ms == -1) {
+          st[k] = true;
+        } else if (ms != INT_MIN) {
+          v[k] = __ldcg(reinterpret_cast<const uint4*>(host + (int64_t)(-2 - ms) * row_bytes) + j);
+          st[k] = true;
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kGatherUnroll; ++k)
+      if (st[k]) lout4[c0 + k * stride] = v[k];
+  }
+}
+
+template <typename Kern>
+int resident_blocks(Kern kern, int* cache) {
+  if (*cache <= 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(cache, kern, kGatherThreads, 0) != cudaSuccess)
+    *cache = 2;
+  if (*cache <= 0) *cache = 1;
+  return *cache;
+}
+
+dim3 wave_grid(int sms, int occ, int64_t want, int nl) {
+  int64_t cap = ((int64_t)sms * occ) / (nl > 0 ? nl : 1);
+  if (cap < 1) cap = 1;
+  const int64_t gx = want < cap ? (want > 0 ? want : 1) : cap;
+  return dim3((unsigned)gx, (unsigned)nl);
+}
+
 }  // namespace
 
 cudaError_t launch_gather(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, const int32_t* rows, int64_t n,
                           uint8_t* out, int32_t row_bytes, int64_t num_rows, int32_t* status, int sms,
                           cudaStream_t s) {
-  const int64_t per_layer = n * (row_bytes >> 4);
-  const int64_t want = (per_layer + (int64_t)kGatherThreads * kGatherUnroll - 1) / ((int64_t)kGatherThreads * kGatherUnroll);
-  // persistent-style grid: about 8 resident CTAs of 256 threads per SM, split across the layers
-  int64_t cap = ((int64_t)sms * 8 + nl - 1) / nl;
-  if (cap < 1) cap = 1;
-  const int64_t gx = want < cap ? (want > 0 ? want : 1) : cap;
-  dim3 grid((unsigned)gx, (unsigned)nl);
-  if (row_bytes == 656)
-    gather_kernel<41><<<grid, kGatherThreads, 0, s>>>(ptrs, layer_begin, rows, n, out, row_bytes, num_rows, status);
-  else
-    gather_kernel<0><<<grid, kGatherThreads, 0, s>>>(ptrs, layer_begin, rows, n, out, row_bytes, num_rows, status);
+  static int occ[2] = {0, 0};
+  const bool k41 = row_bytes == 656;
+  auto kern = k41 ? gather_kernel<41> : gather_kernel<0>;
+  const int64_t want = (n * (row_bytes >> 4) + (int64_t)kGatherThreads * kGatherUnroll - 1) /
+                       ((int64_t)kGatherThreads * kGatherUnroll);
+  const dim3 grid = wave_grid(sms, resident_blocks(kern, &occ[k41 ? 0 : 1]), want, nl);
+  kern<<<grid, kGatherThreads, 0, s>>>(ptrs, layer_begin, rows, n, out, row_bytes, num_rows, status);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, int32_t R, int32_t n,
+                                int32_t max_m, const int32_t* rows, const int32_t* miss_count, const int4* miss_list,
+                                const int32_t* msrc, uint8_t* out, int32_t row_bytes, int64_t num_rows, int sms,
+                                cudaStream_t s) {
+  static int occ[2] = {0, 0};
+  const bool k41 = row_bytes == 656;
+  auto kern = k41 ? gather_fused_kernel<41> : gather_fused_kernel<0>;
+  const int64_t per_layer = (int64_t)R * n * (row_bytes >> 4);
+  const int64_t want = (per_layer + (int64_t)kGatherThreads * kGatherUnroll - 1) /
+                       ((int64_t)kGatherThreads * kGatherUnroll);
+  const dim3 grid = wave_grid(sms, resident_blocks(kern, &occ[k41 ? 0 : 1]), want, nl);
+  kern<<<grid, kGatherThreads, 0, s>>>(ptrs, layer_begin, R, n, max_m, rows, miss_count, miss_list, msrc, out,
+                                       row_bytes, num_rows);
   count_launch();
   return cudaGetLastError();
 }

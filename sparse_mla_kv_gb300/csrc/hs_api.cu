@@ -129,16 +129,22 @@ size_t hs_resolve_workspace_bytes(int32_t nl, int32_t R, int32_t P, int32_t K, i
   return hs::resolve_workspace_bytes((int64_t)nl * R, n, capacity);
 }
 
-size_t hs_resolve_smem_bytes(int32_t P, int32_t K, int32_t capacity) {
+size_t hs_resolve_smem_bytes(int32_t P, int32_t K, int32_t capacity, int32_t page_size) {
   if (P < 1 || K < 0) return 0;
-  return hs::resolve_smem_plan((int64_t)P * K, capacity).total;
+  return hs::resolve_smem_plan((int64_t)P * K, capacity, page_size).total;
 }
 
-hs_status hs_resolve_topk(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P, int32_t K,
+}  // extern "C"
+
+namespace {
+
+// Validates a resolve call and fills the launch parameters; shared by both resolve entry points.
+hs_status prepare_resolve(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P, int32_t K,
                           const int32_t* topk_ids, const int32_t* block_table, const int32_t* host_block_table,
                           const int32_t* ctx_len, int32_t max_pages, const hs_hot_state* hot, int32_t step,
                           int32_t* out_rows, int32_t* out_stats, void* workspace, size_t workspace_bytes,
-                          hs_stream_t stream) {
+                          hs::ResolveParams& p, hs::ResolveSmem& sm, int& sms, bool& nothing) {
+  nothing = false;
   if (!pool || !hot) return HS_ERR_INVALID_ARG;
   const hs::PoolGeom& g = pool->g;
   if (layer_begin < 0 || nl < 0 || (int64_t)layer_begin + nl > g.num_layers) return HS_ERR_INVALID_ARG;
@@ -147,19 +153,22 @@ hs_status hs_resolve_topk(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
   const int32_t C = hot->capacity;
   if (n > HS_MAX_PLAN || C < g.page_size || C > HS_MAX_CAPACITY || C % g.page_size) return HS_ERR_INVALID_ARG;
   if ((int64_t)nl * R > INT32_MAX) return HS_ERR_INVALID_ARG;
-  if (nl == 0 || R == 0) return HS_OK;
+  if (nl == 0 || R == 0) {
+    nothing = true;
+    return HS_OK;
+  }
   if (!block_table || !host_block_table || !ctx_len || !hot->hot_blocks || !hot->slot_token || !hot->slot_stamp ||
       !out_stats || !workspace)
     return HS_ERR_INVALID_ARG;
   if (n > 0 && (!topk_ids || !out_rows)) return HS_ERR_INVALID_ARG;
   if (!hs::aligned16(workspace) || workspace_bytes < hs::resolve_workspace_bytes((int64_t)nl * R, n, C))
     return HS_ERR_INVALID_ARG;
-  const hs::ResolveSmem sm = hs::resolve_smem_plan(n, C);
+  sm = hs::resolve_smem_plan(n, C, g.page_size);
   if (sm.total == 0 || sm.total > hs::resolve_smem_limit(pool->device)) return HS_ERR_INVALID_ARG;
-  const int sms = hs::sm_count(pool->device);
+  sms = hs::sm_count(pool->device);
   if (sms <= 0) return HS_ERR_CUDA;
 
-  hs::ResolveParams p{};
+  p = hs::ResolveParams{};
   p.layer_begin = layer_begin;
   p.nl = nl;
   p.R = R;
@@ -182,13 +191,89 @@ hs_status hs_resolve_topk(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
   p.slot_stamp = hot->slot_stamp;
   p.out_rows = out_rows;
   p.out_stats = out_stats;
-  const size_t count_bytes = (4 * (size_t)nl * R + 15) & ~size_t(15);
   p.miss_count = static_cast<int32_t*>(workspace);
-  p.miss_list = reinterpret_cast<int2*>(static_cast<uint8_t*>(workspace) + count_bytes);
+  p.miss_list = reinterpret_cast<int4*>(static_cast<uint8_t*>(workspace) + hs::ws_counts_bytes((int64_t)nl * R));
+  p.msrc = nullptr;
+  return HS_OK;
+}
 
+}  // namespace
+
+extern "C" {
+
+hs_status hs_resolve_topk(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P, int32_t K,
+                          const int32_t* topk_ids, const int32_t* block_table, const int32_t* host_block_table,
+                          const int32_t* ctx_len, int32_t max_pages, const hs_hot_state* hot, int32_t step,
+                          int32_t* out_rows, int32_t* out_stats, void* workspace, size_t workspace_bytes,
+                          hs_stream_t stream) {
+  hs::ResolveParams p;
+  hs::ResolveSmem sm;
+  int sms = 0;
+  bool nothing = false;
+  hs_status st = prepare_resolve(pool, layer_begin, nl, R, P, K, topk_ids, block_table, host_block_table, ctx_len,
+                                 max_pages, hot, step, out_rows, out_stats, workspace, workspace_bytes, p, sm, sms,
+                                 nothing);
+  if (st != HS_OK || nothing) return st;
   cudaError_t e = hs::launch_resolve(p, sm, stream);
-  if (e == cudaSuccess && p.max_m > 0) e = hs::launch_miss_copy(p, pool->ptrs, g.row_bytes, sms, stream);
+  if (e == cudaSuccess && p.max_m > 0) e = hs::launch_miss_copy(p, pool->ptrs, pool->g.row_bytes, sms, stream);
   return hs::cuda_status(e);
+}
+
+hs_status hs_resolve_plan(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P, int32_t K,
+                          const int32_t* topk_ids, const int32_t* block_table, const int32_t* host_block_table,
+                          const int32_t* ctx_len, int32_t max_pages, const hs_hot_state* hot, int32_t step,
+                          int32_t* out_rows, int32_t* out_stats, void* workspace, size_t workspace_bytes,
+                          hs_stream_t stream) {
+  hs::ResolveParams p;
+  hs::ResolveSmem sm;
+  int sms = 0;
+  bool nothing = false;
+  hs_status st = prepare_resolve(pool, layer_begin, nl, R, P, K, topk_ids, block_table, host_block_table, ctx_len,
+                                 max_pages, hot, step, out_rows, out_stats, workspace, workspace_bytes, p, sm, sms,
+                                 nothing);
+  if (st != HS_OK || nothing) return st;
+  p.msrc = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) +
+                                      hs::ws_msrc_offset((int64_t)nl * R, p.n, p.C));
+  return hs::cuda_status(hs::launch_resolve(p, sm, stream));
+}
+
+hs_status hs_gather_planned(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P, int32_t K,
+                            int32_t capacity, const int32_t* out_rows, const void* workspace, size_t workspace_bytes,
+                            void* out, hs_stream_t stream) {
+  if (!pool) return HS_ERR_INVALID_ARG;
+  const hs::PoolGeom& g = pool->g;
+  if (layer_begin < 0 || nl < 0 || (int64_t)layer_begin + nl > g.num_layers || R < 0 || P < 1 || K < 0)
+    return HS_ERR_INVALID_ARG;
+  const int64_t n = (int64_t)P * K;
+  if (n > HS_MAX_PLAN || (int64_t)nl * R > INT32_MAX || capacity < 1 || capacity > HS_MAX_CAPACITY)
+    return HS_ERR_INVALID_ARG;
+  if (nl == 0 || R == 0 || n == 0) return HS_OK;
+  const int64_t units = (int64_t)nl * R;
+  if (!out_rows || !workspace || !out || !hs::aligned16(out) || !hs::aligned16(workspace) ||
+      workspace_bytes < hs::resolve_workspace_bytes(units, n, capacity))
+    return HS_ERR_INVALID_ARG;
+  const int sms = hs::sm_count(pool->device);
+  if (sms <= 0) return HS_ERR_CUDA;
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  const int32_t max_m = (int32_t)(n < capacity ? n : capacity);
+  return hs::cuda_status(hs::launch_gather_fused(
+      pool->ptrs, layer_begin, nl, R, (int32_t)n, max_m, out_rows, reinterpret_cast<const int32_t*>(ws),
+      reinterpret_cast<const int4*>(ws + hs::ws_counts_bytes(units)),
+      reinterpret_cast<const int32_t*>(ws + hs::ws_msrc_offset(units, n, capacity)), static_cast<uint8_t*>(out),
+      g.row_bytes, (int64_t)g.num_gpu_blocks * g.page_size, sms, stream));
+}
+
+hs_status hs_resolve_gather(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P, int32_t K,
+                            const int32_t* topk_ids, const int32_t* block_table, const int32_t* host_block_table,
+                            const int32_t* ctx_len, int32_t max_pages, const hs_hot_state* hot, int32_t step,
+                            int32_t* out_rows, int32_t* out_stats, void* out, void* workspace,
+                            size_t workspace_bytes, hs_stream_t stream) {
+  if ((int64_t)P * K > 0 && nl > 0 && R > 0 && (!out || !hs::aligned16(out))) return HS_ERR_INVALID_ARG;
+  hs_status st = hs_resolve_plan(pool, layer_begin, nl, R, P, K, topk_ids, block_table, host_block_table, ctx_len,
+                                 max_pages, hot, step, out_rows, out_stats, workspace, workspace_bytes, stream);
+  if (st != HS_OK) return st;
+  return hs_gather_planned(pool, layer_begin, nl, R, P, K, hot->capacity, out_rows, workspace, workspace_bytes, out,
+                           stream);
 }
 
 hs_status hs_gather_rows(const hs_pool* pool, int32_t layer_begin, int32_t nl, const int32_t* rows, int64_t n,

@@ -20,11 +20,18 @@ struct PoolGeom {
 };
 
 // Resolver launch configuration.
-constexpr int kResolveThreads = 512;
+constexpr int kResolveThreads = 1024;
 constexpr int kResolveWarps = kResolveThreads / 32;
 constexpr int kRadixBins = 256;
+constexpr int kSortWarps = 8;  // warps that own chunks in the victim sort
 // Miss-copy work item: this many consecutive misses of one unit.
-constexpr int kMissRowsPerItem = 8;
+constexpr int kMissRowsPerItem = 4;
+// Workspace layout shared by the resolve entry points.
+inline size_t ws_counts_bytes(int64_t units) { return (4 * (size_t)units + 15) & ~size_t(15); }
+inline size_t ws_msrc_offset(int64_t units, int64_t n, int64_t C) {
+  const int64_t max_m = n < C ? n : C;
+  return ws_counts_bytes(units) + 16 * (size_t)units * (size_t)max_m;
+}
 
 // Error bits collected inside one resolver CTA; the reported code follows the precedence
 // STEP_ORDER > ID_RANGE > TABLE_RANGE > MISSING_ROW > CAPACITY.
@@ -51,17 +58,23 @@ struct ResolveParams {
   int32_t* out_rows;
   int32_t* out_stats;
   int32_t* miss_count;  // workspace [nl*R]
-  int2* miss_list;      // workspace [nl*R][max_m] = (host row, pool row)
+  int4* miss_list;      // workspace [nl*R][max_m] = (host row, pool row, position r*n+i, 0)
+  // Fused mode (non-null): per output position, the fused gather's source:
+  //   >= 0 pool row; -1 zero row (padding / failed unit); INT_MIN the first occurrence of a miss
+  //   (written by the gather's miss warps from the miss list); other values <= -2: host row
+  //   (-2 - value), a repeated position of a miss.
+  int32_t* msrc;
 };
 
 struct ResolveSmem {
   // byte offsets into dynamic shared memory
-  size_t tok, stamp, ids, val, cls, idh, u /* slot hash, later radix buffers */, total;
+  size_t tok, stamp, ids, val, cls, idh, hot, u /* slot hash, later radix buffers */, total;
   int32_t id_hash_bits, slot_hash_bits;
 };
 
-// Shared-memory plan of one resolver CTA for (n = P*K ids, C slots); total = 0 if out of limits.
-ResolveSmem resolve_smem_plan(int64_t n, int64_t C);
+// Shared-memory plan of one resolver CTA for (n = P*K ids, C slots, page size S); total = 0 if out
+// of limits.
+ResolveSmem resolve_smem_plan(int64_t n, int64_t C, int64_t S);
 size_t resolve_workspace_bytes(int64_t units, int64_t n, int64_t C);
 // Largest dynamic shared memory a resolver CTA may use on device `dev` (0 on failure).
 size_t resolve_smem_limit(int dev);
@@ -73,6 +86,13 @@ cudaError_t launch_miss_copy(const ResolveParams& p, const LayerPtrs& ptrs, int3
 cudaError_t launch_gather(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, const int32_t* rows, int64_t n,
                           uint8_t* out, int32_t row_bytes, int64_t num_rows, int32_t* status, int sms,
                           cudaStream_t s);
+// The fused gather: rows of layers [layer_begin, layer_begin+nl), R requests x n positions each; miss
+// rows come from the pinned host pool through the resolver's miss lists (dedicated warps) and are
+// also stored into their hot slots; msrc marks positions the miss warps own.
+cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, int32_t R, int32_t n,
+                                int32_t max_m, const int32_t* rows, const int32_t* miss_count, const int4* miss_list,
+                                const int32_t* msrc, uint8_t* out, int32_t row_bytes, int64_t num_rows, int sms,
+                                cudaStream_t s);
 cudaError_t launch_offload(const LayerPtrs& ptrs, const PoolGeom& g, const int32_t* gpu_blocks,
                            const int32_t* host_blocks, int32_t n, int32_t* status, int sms, cudaStream_t s);
 cudaError_t launch_fill_i32(int32_t* a, int64_t count, int32_t value, int sms, cudaStream_t s);

@@ -9,8 +9,8 @@
 // (Integration): speculative decoding uses one replayable per-step plan sharing the hot state.
 //
 // Design (sm_103a):
-//   resolve_kernel   one CTA (512 threads) per (layer, request) unit.  The unit's slot state is
-//                    staged in shared memory; two open-addressing hash tables (16-bit entries) map
+//   resolve_kernel   one CTA (1024 threads) per (layer, request) unit.  The unit's slot state is
+//                    staged in shared memory; two open-addressing hash tables (32-bit entries) map
 //                    token -> lowest slot and id -> first position; the plan, hit/miss
 //                    classification and the miss ranks come from block-wide scans; victims are the
 //                    candidates sorted by (stamp, slot) with a stable LSD radix sort (8-bit digits,
@@ -30,48 +30,37 @@ namespace hs {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr unsigned short kEmpty16 = 0xFFFF;
+constexpr int kEmpty = -1;
+constexpr int kBadHost = INT_MIN;
+constexpr int kGatherOwnedByMissWarps = INT_MIN;
 enum : uint8_t { kNone = 0, kResident = 1, kHit = 2, kMiss = 3 };
 
 __device__ __forceinline__ uint32_t fib_hash(int32_t key, int bits) {
   return ((uint32_t)key * 0x9E3779B1u) >> (32 - bits);
 }
 
-__device__ __forceinline__ void atomic_min_u16(unsigned short* a, unsigned short v) {
-  unsigned short cur = *(volatile unsigned short*)a;
-  while (v < cur) {
-    const unsigned short prev = atomicCAS(a, cur, v);
-    if (prev == cur) break;
-    cur = prev;
-  }
-}
-
-// Insert entry e (an index into keys[]) under key keys[e] == k; when the key is already present
-// keep the smallest entry (lowest slot / first position).
-__device__ __forceinline__ void hash_insert_min(unsigned short* tab, int bits, const int32_t* keys, int32_t k,
-                                                int e) {
+// Open addressing with linear probing; an entry is an index e into keys[] (the key is keys[e]).
+// Insert e under key k = keys[e]; when the key is already present keep the smallest entry (lowest
+// slot / first position).
+__device__ __forceinline__ void hash_insert_min(int* tab, int bits, const int32_t* keys, int32_t k, int e) {
   const uint32_t mask = (1u << bits) - 1u;
   uint32_t h = fib_hash(k, bits);
   for (uint32_t it = 0; it <= mask; ++it, h = (h + 1u) & mask) {
-    unsigned short cur = *(volatile unsigned short*)&tab[h];
-    if (cur == kEmpty16) {
-      const unsigned short prev = atomicCAS(&tab[h], kEmpty16, (unsigned short)e);
-      if (prev == kEmpty16) return;
-      cur = prev;
-    }
+    int cur = atomicCAS(&tab[h], kEmpty, e);
+    if (cur == kEmpty) return;
     if (keys[cur] == k) {
-      atomic_min_u16(&tab[h], (unsigned short)e);
+      atomicMin(&tab[h], e);
       return;
     }
   }
 }
 
-__device__ __forceinline__ int hash_find(const unsigned short* tab, int bits, const int32_t* keys, int32_t k) {
+__device__ __forceinline__ int hash_find(const int* tab, int bits, const int32_t* keys, int32_t k) {
   const uint32_t mask = (1u << bits) - 1u;
   uint32_t h = fib_hash(k, bits);
   for (uint32_t it = 0; it <= mask; ++it, h = (h + 1u) & mask) {
-    const unsigned short cur = tab[h];
-    if (cur == kEmpty16) return -1;
+    const int cur = tab[h];
+    if (cur == kEmpty) return -1;
     if (keys[cur] == k) return cur;
   }
   return -1;
@@ -109,13 +98,16 @@ __device__ __forceinline__ void block_scan2(int a, int b, int& ea, int& eb, int&
 }
 
 // Stable LSD radix sort of slot ids a[0..nc) by key stamp[slot] - lo over `passes` 8-bit digits.
-// Returns the buffer holding the result (a or b).  Call uniformly (contains __syncthreads).
+// kSortWarps warps own contiguous chunks (per-warp histograms keep the scatter stable); all threads
+// take part in the histogram scan.  Returns the buffer holding the result (a or b).  Call uniformly
+// (contains __syncthreads).
 __device__ unsigned short* radix_sort_slots(unsigned short* a, unsigned short* b, int nc, const int32_t* s_stamp,
                                             int lo, int passes, int* hist, int* s_tmp) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per_warp = (nc + kResolveWarps - 1) / kResolveWarps;
-  const int w0 = min(nc, warp * per_warp), w1 = min(nc, w0 + per_warp);
-  constexpr int kEntries = kRadixBins * kResolveWarps;
+  const int per_warp = (nc + kSortWarps - 1) / kSortWarps;
+  const int w0 = warp < kSortWarps ? min(nc, warp * per_warp) : nc;
+  const int w1 = warp < kSortWarps ? min(nc, w0 + per_warp) : nc;
+  constexpr int kEntries = kRadixBins * kSortWarps;
   constexpr int kPerThread = kEntries / kResolveThreads;
   static_assert(kEntries % kResolveThreads == 0, "histogram split");
   for (int pass = 0; pass < passes; ++pass) {
@@ -124,7 +116,7 @@ __device__ unsigned short* radix_sort_slots(unsigned short* a, unsigned short* b
     __syncthreads();
     for (int e = w0 + lane; e < w1; e += 32) {
       const uint32_t d = ((uint32_t)(s_stamp[a[e]] - lo) >> shift) & 0xFFu;
-      atomicAdd(&hist[d * kResolveWarps + warp], 1);
+      atomicAdd(&hist[d * kSortWarps + warp], 1);
     }
     __syncthreads();
     int loc[kPerThread];
@@ -144,7 +136,7 @@ __device__ unsigned short* radix_sort_slots(unsigned short* a, unsigned short* b
       const uint32_t key = valid ? d : (0x100u + (uint32_t)lane);
       const uint32_t peers = __match_any_sync(kFull, key);
       const int rank = __popc(peers & ((1u << lane) - 1u));
-      int* ctr = &hist[d * kResolveWarps + warp];
+      int* ctr = &hist[d * kSortWarps + warp];
       if (valid) b[*ctr + rank] = slot;
       __syncwarp();
       if (valid && rank == 0) *ctr += __popc(peers);
@@ -163,8 +155,9 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
   int32_t* s_ids = reinterpret_cast<int32_t*>(smem + sm.ids);
   int32_t* s_val = reinterpret_cast<int32_t*>(smem + sm.val);
   uint8_t* s_cls = reinterpret_cast<uint8_t*>(smem + sm.cls);
-  unsigned short* s_idh = reinterpret_cast<unsigned short*>(smem + sm.idh);
-  unsigned short* s_slh = reinterpret_cast<unsigned short*>(smem + sm.u);
+  int* s_idh = reinterpret_cast<int*>(smem + sm.idh);
+  int* s_slh = reinterpret_cast<int*>(smem + sm.u);
+  int32_t* s_hot = reinterpret_cast<int32_t*>(smem + sm.hot);
   __shared__ uint32_t s_err;
   __shared__ int s_cnt[3];
   __shared__ int s_lo, s_hi;
@@ -181,6 +174,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
   const int32_t* hbt = p.hbt + (int64_t)r * p.max_pages;
   const int32_t* hot = p.hot_blocks + (int64_t)r * (C / S);
   int32_t* rows_g = p.out_rows + (int64_t)unit * n;
+  int32_t* msrc_g = p.msrc ? p.msrc + (int64_t)unit * n : nullptr;
   const int ctx = p.ctx_len[r];
   const int HI = 1 << sm.id_hash_bits, HS = 1 << sm.slot_hash_bits;
 
@@ -191,24 +185,41 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
     s_lo = INT_MAX;
     s_hi = INT_MIN;
   }
-  for (int i = tid; i < HI; i += kResolveThreads) s_idh[i] = kEmpty16;
-  for (int i = tid; i < HS; i += kResolveThreads) s_slh[i] = kEmpty16;
+  for (int i = tid; i < HI; i += kResolveThreads) s_idh[i] = kEmpty;
+  for (int i = tid; i < HS; i += kResolveThreads) s_slh[i] = kEmpty;
   uint32_t err = 0u;
+  // ids, and their page's table entries fetched right away (independent of the hashing below) so
+  // that classification needs no global-memory round trip.  Combined entry in s_val:
+  //   e >= 0      resident block e;      e == -1   placeholder without a host copy;
+  //   e == kBadHost  placeholder whose host block is outside the pool;  else host block -2 - e.
+#pragma unroll 4
+  for (int i = tid; i < n; i += kResolveThreads) {
+    const int id = ids_g[i];
+    s_ids[i] = id;
+    int e = -1;
+    if (id != -1) {
+      if (id < -1 || id >= ctx || id / S >= p.max_pages) {
+        err |= kErrId;
+      } else {
+        const int page = id / S;
+        const int b = bt[page];
+        const int h = hbt[page];
+        e = b >= 0 ? b : (h < 0 ? -1 : (h >= p.num_host_blocks ? kBadHost : -2 - h));
+      }
+    }
+    s_val[i] = e;
+  }
+  for (int b = tid; b < C / S; b += kResolveThreads) {
+    const int hb = hot[b];
+    s_hot[b] = hb;
+    if (hb < 0 || hb >= p.num_gpu_blocks) err |= kErrTable;
+  }
   for (int s = tid; s < C; s += kResolveThreads) {
     const int t = p.slot_token[state_off + s];
     const int st = p.slot_stamp[state_off + s];
     s_tok[s] = t;
     s_stamp[s] = st;
     if (st > step) err |= kErrStep;
-  }
-  for (int i = tid; i < n; i += kResolveThreads) {
-    const int id = ids_g[i];
-    s_ids[i] = id;
-    if (id != -1 && (id < -1 || id >= ctx || id / S >= p.max_pages)) err |= kErrId;
-  }
-  for (int b = tid; b < C / S; b += kResolveThreads) {
-    const int hb = hot[b];
-    if (hb < 0 || hb >= p.num_gpu_blocks) err |= kErrTable;
   }
   if (err) atomicOr(&s_err, err);
   __syncthreads();
@@ -235,11 +246,11 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
       uint8_t cls = kNone;
       int val = 0;
       if (id >= 0 && hash_find(s_idh, sm.id_hash_bits, s_ids, id) == i) {
-        const int page = id / S, off = id - page * S;
-        const int b = bt[page];
-        if (b >= 0) {
-          if (b >= p.num_gpu_blocks) err |= kErrTable;
-          else val = b * S + off;
+        const int off = id % S;
+        const int e = s_val[i];
+        if (e >= 0) {
+          if (e >= p.num_gpu_blocks) err |= kErrTable;
+          else val = e * S + off;
           cls = kResident;
           ++c_res;
         } else {
@@ -250,10 +261,9 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
             s_stamp[s] = step;
             ++c_hit;
           } else {
-            const int h = hbt[page];
-            if (h < 0) err |= kErrMissing;
-            else if (h >= p.num_host_blocks) err |= kErrTable;
-            else val = h * S + off;
+            if (e == -1) err |= kErrMissing;
+            else if (e == kBadHost) err |= kErrTable;
+            else val = (-2 - e) * S + off;
             cls = kMiss;
             ++c_miss;
           }
@@ -321,8 +331,9 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
       if (cls == kMiss) {
         const int v = sorted[j];
         const int vb = v / S;
-        const int dst = hot[vb] * S + (v - vb * S);
-        p.miss_list[(int64_t)unit * p.max_m + j] = make_int2(s_val[i], dst);
+        const int dst = s_hot[vb] * S + (v - vb * S);
+        p.miss_list[(int64_t)unit * p.max_m + j] = make_int4(s_val[i], dst, r * n + i, 0);
+        if (msrc_g) msrc_g[i] = kGatherOwnedByMissWarps;
         p.slot_token[state_off + v] = s_ids[i];
         p.slot_stamp[state_off + v] = step;
         s_val[i] = dst;
@@ -331,7 +342,10 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
         const int v = s_val[i];
         const int vb = v / S;
         p.slot_stamp[state_off + v] = step;
-        s_val[i] = hot[vb] * S + (v - vb * S);
+        s_val[i] = s_hot[vb] * S + (v - vb * S);
+        if (msrc_g) msrc_g[i] = s_val[i];
+      } else if (msrc_g && cls == kResident) {
+        msrc_g[i] = s_val[i];
       }
     }
     __syncthreads();
@@ -339,7 +353,21 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
     for (int i = tid; i < n; i += kResolveThreads) {
       const int id = s_ids[i];
       int row = -1;
-      if (id >= 0) row = s_cls[i] != kNone ? s_val[i] : s_val[hash_find(s_idh, sm.id_hash_bits, s_ids, id)];
+      if (id >= 0) {
+        if (s_cls[i] != kNone) {
+          row = s_val[i];
+        } else {  // a repeated id: share the first occurrence's row (a miss: re-read its host row)
+          const int f = hash_find(s_idh, sm.id_hash_bits, s_ids, id);
+          row = s_val[f];
+          if (msrc_g) {
+            // a repeated position of a miss reads the host row again (the first occurrence's host
+            // row is re-derived from the host block table, which was valid for it)
+            msrc_g[i] = s_cls[f] == kMiss ? -2 - (hbt[id / S] * S + id % S) : row;
+          }
+        }
+      } else if (msrc_g) {
+        msrc_g[i] = -1;
+      }
       rows_g[i] = row;
     }
     if (tid == 0) {
@@ -356,7 +384,10 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
                    : (e & kErrTable) ? HS_ERR_TABLE_RANGE
                    : (e & kErrMissing) ? HS_ERR_MISSING_ROW
                    : HS_ERR_CAPACITY;
-    for (int i = tid; i < n; i += kResolveThreads) rows_g[i] = -1;
+    for (int i = tid; i < n; i += kResolveThreads) {
+      rows_g[i] = -1;
+      if (msrc_g) msrc_g[i] = -1;
+    }
     if (tid == 0) {
       int32_t* st = p.out_stats + (int64_t)unit * 4;
       st[0] = code;
@@ -367,22 +398,24 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
 }
 
 constexpr int kCopyThreads = 256;
-constexpr int kCopyUnroll = 4;
 
+// Copies the misses of every unit.  Items (unit, group of kMissRowsPerItem consecutive misses) are
+// numbered chunk-major (item = group * units + unit), so the live items are the low numbers; lane j of
+// warp w tests item w + j * nwarps, which spreads the live items over all warps of the grid.  A live
+// item's rows are copied with all its 16-byte loads issued before any store.
 template <int CPR>
 __global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(const ResolveParams p, const LayerPtrs ptrs,
                                                                  int32_t row_bytes) {
+  constexpr int kU = CPR ? (kMissRowsPerItem * CPR + 31) / 32 : 4;
   const int cpr = CPR ? CPR : (row_bytes >> 4);
   const int units = p.nl * p.R;
   const int items_per_unit = (p.max_m + kMissRowsPerItem - 1) / kMissRowsPerItem;
   const int64_t items = (int64_t)units * items_per_unit;
-  const int64_t batches = (items + 31) / 32;
   const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t bi = warp; bi < batches; bi += nwarps) {
-    // items are chunk-major, so the non-empty ones (low chunk numbers) come first
-    const int64_t item = bi * 32 + lane;
+  for (int64_t base = warp; base < items; base += nwarps * 32) {
+    const int64_t item = base + (int64_t)lane * nwarps;
     int unit = 0, chunk = 0, cnt = 0;
     bool live = false;
     if (item < items) {
@@ -401,16 +434,16 @@ __global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(const ResolvePa
       const int r0 = ch * kMissRowsPerItem;
       const int nrows = min(kMissRowsPerItem, c - r0);
       const int l = p.layer_begin + u / p.R;
-      int2 ent = make_int2(0, 0);
+      int4 ent = make_int4(0, 0, 0, 0);
       if (lane < nrows) ent = p.miss_list[(int64_t)u * p.max_m + r0 + lane];
       const uint8_t* host = ptrs.host[l];
       uint8_t* pool = ptrs.gpu[l];
       const int total = nrows * cpr;
-      for (int f0 = 0; f0 < total; f0 += 32 * kCopyUnroll) {
-        uint4 v[kCopyUnroll];
-        int64_t dst_off[kCopyUnroll];
+      for (int f0 = 0; f0 < total; f0 += 32 * kU) {
+        uint4 v[kU];
+        int64_t dst_off[kU];
 #pragma unroll
-        for (int k = 0; k < kCopyUnroll; ++k) {
+        for (int k = 0; k < kU; ++k) {
           const int f = f0 + k * 32 + lane;
           const bool ok = f < total;
           const int rr = ok ? f / cpr : 0;
@@ -424,7 +457,7 @@ __global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(const ResolvePa
           }
         }
 #pragma unroll
-        for (int k = 0; k < kCopyUnroll; ++k)
+        for (int k = 0; k < kU; ++k)
           if (dst_off[k] >= 0) *reinterpret_cast<uint4*>(pool + dst_off[k]) = v[k];
       }
     }
@@ -441,9 +474,9 @@ size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
 }  // namespace
 
-ResolveSmem resolve_smem_plan(int64_t n, int64_t C) {
+ResolveSmem resolve_smem_plan(int64_t n, int64_t C, int64_t S) {
   ResolveSmem sm{};
-  if (n < 0 || n > HS_MAX_PLAN || C < 1 || C > HS_MAX_CAPACITY) return sm;
+  if (n < 0 || n > HS_MAX_PLAN || C < 1 || C > HS_MAX_CAPACITY || S < 1 || C % S) return sm;
   sm.id_hash_bits = ceil_log2(2 * (n > 16 ? n : 16));
   sm.slot_hash_bits = ceil_log2(2 * (C > 16 ? C : 16));
   size_t off = 0;
@@ -452,19 +485,21 @@ ResolveSmem resolve_smem_plan(int64_t n, int64_t C) {
   sm.ids = off;   off = align16(off + 4 * (size_t)n);
   sm.val = off;   off = align16(off + 4 * (size_t)n);
   sm.cls = off;   off = align16(off + (size_t)n);
-  sm.idh = off;   off = align16(off + 2 * ((size_t)1 << sm.id_hash_bits));
+  sm.idh = off;   off = align16(off + 4 * ((size_t)1 << sm.id_hash_bits));
+  sm.hot = off;   off = align16(off + 4 * (size_t)(C / S));
   sm.u = off;
-  const size_t slot_hash = 2 * ((size_t)1 << sm.slot_hash_bits);
+  const size_t slot_hash = 4 * ((size_t)1 << sm.slot_hash_bits);
   const size_t cbuf = 2 * (size_t)((C + 7) & ~int64_t(7));
-  const size_t radix = 2 * cbuf + 4 * (size_t)kRadixBins * kResolveWarps;
+  const size_t radix = 2 * cbuf + 4 * (size_t)kRadixBins * kSortWarps;
   off = align16(off + (slot_hash > radix ? slot_hash : radix));
   sm.total = off;
   return sm;
 }
 
 size_t resolve_workspace_bytes(int64_t units, int64_t n, int64_t C) {
+  // [miss counts, 16-byte aligned] [miss lists: units x min(n, C) int4] [per-position sources: units x n]
   const int64_t max_m = n < C ? n : C;
-  return align16(4 * (size_t)units) + 8 * (size_t)units * (size_t)max_m;
+  return align16(4 * (size_t)units) + 16 * (size_t)units * (size_t)max_m + align16(4 * (size_t)units * (size_t)n);
 }
 
 size_t resolve_smem_limit(int dev) {
@@ -496,8 +531,8 @@ cudaError_t launch_miss_copy(const ResolveParams& p, const LayerPtrs& ptrs, int3
                              cudaStream_t s) {
   const int64_t units = (int64_t)p.nl * p.R;
   const int64_t items = units * ((p.max_m + kMissRowsPerItem - 1) / kMissRowsPerItem);
-  const int64_t warps_needed = (items + 31) / 32;
-  int64_t blocks = (warps_needed + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
+  // one warp per item at most, capped at a full resident grid
+  int64_t blocks = (items + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
   const int64_t cap = (int64_t)sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;

@@ -14,7 +14,10 @@ from synth import content, device as sdev
 
 
 class Rig:
-    def __init__(self, w, *, oracle_bytes: bool = False, device: str = "cuda", check_hot_bytes: bool = True):
+    def __init__(self, w, *, oracle_bytes: bool = False, device: str = "cuda", check_hot_bytes: bool = True,
+                 mode: str = "split"):
+        assert mode in ("split", "fused")
+        self.mode = mode
         self.w = w
         self.dev = torch.device(device)
         self.oracle_bytes = oracle_bytes
@@ -80,8 +83,13 @@ class Rig:
         self.apply_edits(st)
         topk = torch.from_numpy(st.topk).to(self.dev)
         ctx = torch.from_numpy(st.ctx_len.astype(np.int32)).to(self.dev)
-        rows, stats = hs.resolve_topk(self.pool, topk, self.bt, self.hbt, ctx, self.hot, st.index, workspace=self.ws)
-        out = hs.gather_rows(self.pool, rows.reshape(w.L, -1))
+        if self.mode == "fused":
+            rows, stats, out = hs.resolve_gather(self.pool, topk, self.bt, self.hbt, ctx, self.hot, st.index,
+                                                 workspace=self.ws)
+        else:
+            rows, stats = hs.resolve_topk(self.pool, topk, self.bt, self.hbt, ctx, self.hot, st.index,
+                                          workspace=self.ws)
+            out = hs.gather_rows(self.pool, rows.reshape(w.L, -1))
         if len(st.off_gpu):
             hs.offload_pages(self.pool, torch.from_numpy(st.off_gpu).to(self.dev),
                              torch.from_numpy(st.off_host).to(self.dev))

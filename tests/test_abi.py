@@ -56,16 +56,18 @@ def test_status_strings(lib):
 
 
 def test_size_queries(lib):
-    # miss-list workspace: 16-byte-aligned counts + (host row, pool row) per possible miss
-    assert hs.resolve_workspace_bytes(1, 64, 1, 2048, 4096) == 256 + 8 * 64 * 2048
-    assert hs.resolve_workspace_bytes(4, 256, 4, 2048, 4096) == 4096 + 8 * 1024 * 4096
-    assert hs.resolve_workspace_bytes(1, 3, 1, 5, 4) == 16 + 8 * 3 * 4
+    # workspace: 16-byte-aligned miss counts + (host row, pool row, position) per possible miss
+    # (min(P*K, C) per unit, 16 B each) + one host source per position (16-byte aligned)
+    assert hs.resolve_workspace_bytes(1, 64, 1, 2048, 4096) == 256 + 16 * 64 * 2048 + 4 * 64 * 2048
+    assert hs.resolve_workspace_bytes(4, 256, 4, 2048, 4096) == 4096 + 16 * 1024 * 4096 + 4 * 1024 * 8192
+    assert hs.resolve_workspace_bytes(1, 3, 1, 5, 4) == 16 + 16 * 3 * 4 + 64
     assert hs.resolve_workspace_bytes(1, 1, 0, 5, 4) == 0
     # the benchmarked shapes fit in one CTA's shared memory; oversize plans report 0 or > 227 KB
     for P, K, C in ((1, 256, 512), (1, 2048, 4096), (4, 2048, 4096)):
-        assert 0 < hs.resolve_smem_bytes(P, K, C) <= 227 * 1024
-    assert hs.resolve_smem_bytes(1, 16385, 4096) == 0
-    assert hs.resolve_smem_bytes(1, 16, 16385) == 0
+        assert 0 < hs.resolve_smem_bytes(P, K, C, 64) <= 227 * 1024
+    assert hs.resolve_smem_bytes(1, 16385, 4096, 64) == 0
+    assert hs.resolve_smem_bytes(1, 16, 16385, 1) == 0
+    assert hs.resolve_smem_bytes(1, 16, 100, 64) == 0          # capacity not a multiple of the page
 
 
 def test_pool_create_rejects_bad_descriptions_before_touching_a_device(lib):

@@ -30,9 +30,13 @@ def _rig(w, **kw):
     return Rig(w, **kw)
 
 
-def test_tiny_decode_all_bytes():
+MODES = ["split", "fused"]
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_tiny_decode_all_bytes(mode):
     w = workloads.config1(seed=0, steps=8)
-    rig = _rig(w, oracle_bytes=True)
+    rig = _rig(w, oracle_bytes=True, mode=mode)
     misses = 0
     for st in w.iter_steps():
         _, stats, _, _, _ = rig.step(st)
@@ -40,10 +44,11 @@ def test_tiny_decode_all_bytes():
     assert misses > 0
 
 
-def test_tiny_decode_other_seeds_and_replay():
+@pytest.mark.parametrize("mode", MODES)
+def test_tiny_decode_other_seeds_and_replay(mode):
     for seed in (1, 2):
         w = workloads.config1(seed=seed, steps=6)
-        rig = _rig(w, oracle_bytes=True)
+        rig = _rig(w, oracle_bytes=True, mode=mode)
         for st in w.iter_steps():
             rows, stats, *_ = rig.step(st)
             # replay the same step: same rows, no misses, state unchanged
@@ -65,7 +70,8 @@ def _case_to_gpu(case, dev):
     return pool, gpu, host, hot
 
 
-def test_random_small_cases_vs_oracle():
+@pytest.mark.parametrize("mode", MODES)
+def test_random_small_cases_vs_oracle(mode):
     """Random small shapes (page sizes 1/2/4, several positions, duplicates, padding, replays,
     invalid ids, steps going backwards) through the library and the oracle with byte pools."""
     rng = np.random.default_rng(777)
@@ -81,7 +87,11 @@ def test_random_small_cases_vs_oracle():
             u = rng.random()
             t = t if u < 0.1 else (max(0, t - 2) if u < 0.13 else t + int(rng.integers(1, 3)))
             ids = _ids(rng, case, P, K)
-            rows, stats = hs.resolve_topk(pool, torch.from_numpy(ids[None]).to(dev), bt, hbt, ctx, hot, t)
+            if mode == "fused":
+                rows, stats, g = hs.resolve_gather(pool, torch.from_numpy(ids[None]).to(dev), bt, hbt, ctx, hot, t)
+            else:
+                rows, stats = hs.resolve_topk(pool, torch.from_numpy(ids[None]).to(dev), bt, hbt, ctx, hot, t)
+                g = hs.gather_rows(pool, rows.reshape(1, -1))
             o_rows, o_stats = case.step(ids, t)
             torch.cuda.synchronize()
             seen.update(o_stats[0, :, 0].tolist())
@@ -91,18 +101,18 @@ def test_random_small_cases_vs_oracle():
             assert np.array_equal(hot.slot_token.cpu().numpy(), case.tok), msg
             assert np.array_equal(hot.slot_stamp.cpu().numpy(), case.stamp), msg
             assert np.array_equal(gpu[0].cpu().numpy().reshape(-1), case.pools[0]), msg
-            g = hs.gather_rows(pool, rows.reshape(1, -1))
             o_out, _ = case.gather(o_rows.reshape(1, -1))
             assert np.array_equal(g.cpu().numpy(), o_out), msg
         pool.close()
     assert {0, 2, 5}.issubset(seen)
 
 
-def test_mixed_residency_decode_full_size():
+@pytest.mark.parametrize("mode", MODES)
+def test_mixed_residency_decode_full_size(mode):
     """The 64-request, 131072-token, K=2048 mixed-residency batch (the benchmarked workload) for all
     of its 64 steps."""
     w = workloads.config2(seed=0, steps=64)
-    rig = _rig(w)
+    rig = _rig(w, mode=mode)
     tot = np.zeros(3, np.int64)
     for st in w.iter_steps():
         _, stats, *_ = rig.step(st)
@@ -110,18 +120,20 @@ def test_mixed_residency_decode_full_size():
     assert tot[1] > 0 and tot[2] > 0   # both hits and misses happened
 
 
-def test_cold_start_prefix_reuse_full_size():
+@pytest.mark.parametrize("mode", MODES)
+def test_cold_start_prefix_reuse_full_size(mode):
     """16 requests reusing a 1,048,576-token host-only prefix, empty hot buffers, 32 steps."""
     w = workloads.config4(seed=0, steps=32)
-    rig = _rig(w)
+    rig = _rig(w, mode=mode)
     for st in w.iter_steps():
         _, stats, *_ = rig.step(st)
     assert int(stats[..., 3].sum()) > 0
 
 
-def test_data_errors_are_isolated_per_unit():
+@pytest.mark.parametrize("mode", MODES)
+def test_data_errors_are_isolated_per_unit(mode):
     w = workloads.config1(seed=3, steps=3)
-    rig = _rig(w, oracle_bytes=True)
+    rig = _rig(w, oracle_bytes=True, mode=mode)
     steps = list(w.iter_steps())
     rig.step(steps[0])
     st = steps[1]
@@ -165,11 +177,11 @@ def test_empty_and_degenerate_shapes():
 
 
 def test_largest_shapes_and_shape_limits():
-    """P*K = 8192 ids with C = 4096 (the MTP3 shape) and C = 16384 with a short plan: parity on one
-    step; a plan that does not fit in shared memory is rejected on the host."""
+    """P*K = 8192 ids with C = 4096 (the MTP3 shape) and C = 8192 hot rows: parity over three steps;
+    a shape whose plan does not fit in one CTA's shared memory is rejected on the host."""
     dev = torch.device("cuda")
     rng = np.random.default_rng(5)
-    for P, K, C in ((4, 2048, 4096), (1, 1024, 16384), (1, 4096, 8192)):
+    for P, K, C in ((4, 2048, 4096), (1, 1024, 8192), (1, 4096, 8192)):
         S, B, R, pages = 64, 32, 3, 512
         ctx = pages * S
         nb = C // S
@@ -196,7 +208,18 @@ def test_largest_shapes_and_shape_limits():
             assert np.array_equal(hot.slot_stamp.cpu().numpy(), case.stamp)
             assert np.array_equal(gpu[0].cpu().numpy().reshape(-1), case.pools[0])
         pool.close()
-    assert hs.resolve_smem_bytes(8, 2048, 16384) == 0 or hs.resolve_smem_bytes(8, 2048, 16384) > 227 * 1024
+    big = hs.resolve_smem_bytes(1, 1024, 16384, 64)
+    assert big > 227 * 1024
+    S, C = 64, 16384
+    gpu = [torch.zeros((C // S + 1, S, 16), dtype=torch.uint8, device=dev)]
+    pool = hs.Pool(gpu, [torch.zeros((4, S, 16), dtype=torch.uint8).pin_memory()])
+    hot = hs.HotState.allocate(1, torch.arange(C // S, dtype=torch.int32, device=dev)[None], C)
+    bt = torch.full((1, 4), -1, dtype=torch.int32, device=dev)
+    with pytest.raises(hs.HSError) as e:
+        hs.resolve_topk(pool, torch.zeros((1, 1, 1, 1024), dtype=torch.int32, device=dev), bt, bt,
+                        torch.tensor([256], dtype=torch.int32, device=dev), hot, 0)
+    assert e.value.code == 1
+    pool.close()
 
 
 def test_gather_standalone_multilayer_and_status():
