@@ -205,6 +205,27 @@ hs_status hs_gather_rows(const hs_pool* pool, int32_t layer_begin, int32_t nl, c
 hs_status hs_offload_pages(const hs_pool* pool, const int32_t* gpu_blocks, const int32_t* host_blocks,
                            int32_t n, int32_t* out_status, hs_stream_t stream);
 
+/* hs_resolve_topk for callers that cannot allocate device memory (a plug-in inside an engine that has
+ * reserved nearly all device memory, a decode loop that must not let cudaMalloc synchronise the
+ * device, a C caller without a device allocator).  The pages have no counterpart: this is a library
+ * convenience.  Same arguments and results as hs_resolve_topk, minus the workspace: the scratch is a
+ * static __device__ array of HS_STATIC_SCRATCH_BYTES inside the library, held by every GPU that loads
+ * the library until the process exits.  No call allocates anything.
+ *   - Returns HS_ERR_INVALID_ARG when hs_resolve_workspace_bytes(nl, R, P, K, capacity) exceeds
+ *     HS_STATIC_SCRATCH_BYTES (about 340 units of the MTP3 shape P*K = 8192, C = 4096, or about 800
+ *     units of K = 2048, C = 4096).
+ *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress, with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the one array and it keeps the last call's contents (nothing in it needs to
+ *     start at zero).  Calls whose executions overlap on the GPU -- on different streams, or from
+ *     different threads without ordering -- race on it; order them on one stream. */
+#define HS_STATIC_SCRATCH_BYTES (32u << 20)
+hs_status hs_resolve_topk_noalloc(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P,
+                                  int32_t K, const int32_t* topk_ids, const int32_t* block_table,
+                                  const int32_t* host_block_table, const int32_t* ctx_len, int32_t max_pages,
+                                  const hs_hot_state* hot, int32_t step, int32_t* out_rows, int32_t* out_stats,
+                                  hs_stream_t stream);
+
 /* Static description of a status code. */
 const char* hs_status_str(hs_status s);
 
