@@ -6,6 +6,8 @@ the GPU (torch element-wise ops) and copied to pinned memory.  No resolver arith
 """
 from __future__ import annotations
 
+import weakref
+
 import numpy as np
 import torch
 
@@ -52,14 +54,45 @@ def fill_host_pool(w, layer: int, host: torch.Tensor, device) -> None:
     fill_blocks(w, layer, host, blocks[order], own[blocks[order]], device, chunk_blocks=2048)
 
 
+_CPT_CACHE = {}
+
+
 def expected_rows(w, layer: int, r_idx: torch.Tensor, ids: torch.Tensor) -> torch.Tensor:
     """Closed-form bytes of logical tokens ids (int64, device) of requests r_idx -> uint8 [n, B];
     ids == -1 gives zero rows."""
     dev = ids.device
-    cpt = torch.from_numpy(w.content_page.astype(np.int64)).to(dev)
+    key = (id(w), str(dev))
+    if key not in _CPT_CACHE:
+        _CPT_CACHE.clear()
+        _CPT_CACHE[key] = torch.from_numpy(w.content_page.astype(np.int64)).to(dev)
+    cpt = _CPT_CACHE[key]
     valid = ids >= 0
     safe = torch.where(valid, ids, torch.zeros_like(ids))
     cp = cpt[r_idx, safe // w.S]
     rows = content.rows_torch(w.content_seed, layer, cp, safe % w.S, w.B)
     rows[~valid] = 0
     return rows
+
+
+def _unregister(ptr: int) -> None:
+    try:
+        torch.cuda.cudart().cudaHostUnregister(ptr)
+    except Exception:
+        pass
+
+
+def pinned_empty(shape, dtype=torch.uint8) -> torch.Tensor:
+    """A page-locked, device-mapped host tensor of exactly this size.  torch's pinned allocator
+    rounds every request up to a power of two, which doubles tens-of-GB host pools; this registers
+    plain host memory instead (cudaHostRegister, portable | mapped)."""
+    itemsize = torch.empty((), dtype=dtype).element_size()
+    nbytes = int(np.prod(shape)) * itemsize
+    arr = np.empty(max(nbytes, 16), np.uint8)
+    try:
+        rc = torch.cuda.cudart().cudaHostRegister(arr.ctypes.data, arr.nbytes, 3)
+    except AttributeError:   # a torch without the binding: fall back to its pinned allocator
+        return torch.empty(shape, dtype=dtype, pin_memory=True)
+    if int(rc) != 0:
+        raise RuntimeError(f"cudaHostRegister failed ({int(rc)}) for {nbytes} bytes")
+    weakref.finalize(arr, _unregister, arr.ctypes.data)
+    return torch.from_numpy(arr[:nbytes]).view(dtype).reshape(shape)

@@ -82,14 +82,14 @@ class Workload:
     def gpu_block_owner(self) -> np.ndarray:
         """int64 [num_gpu_blocks][2] = (r, page) whose rows the block holds at start, (-1,-1) if none."""
         own = np.full((self.num_gpu_blocks, 2), -1, np.int64)
-        for r, p in self.gpu_resident_init:
-            own[self.block_table[r, p]] = (r, p)
+        rp = self.gpu_resident_init
+        own[self.block_table[rp[:, 0], rp[:, 1]]] = rp
         return own
 
     def host_block_owner(self) -> np.ndarray:
         own = np.full((self.num_host_blocks, 2), -1, np.int64)
-        for r, p in self.host_resident_init:
-            own[self.host_block_table[r, p]] = (r, p)
+        rp = self.host_resident_init
+        own[self.host_block_table[rp[:, 0], rp[:, 1]]] = rp
         return own
 
 
@@ -261,7 +261,177 @@ def config4(seed: int = 0, steps: int = 32, R: int = 16) -> Workload:
                     content_seed=seed, _gen=_fixed_ctx_gen("uniform", "uniform", 0.0))
 
 
-CONFIGS = {1: config1, 2: config2, 4: config4}
+# --------------------------------------------------------------------------- max batch with MTP3
+def _mtp_lists(rng, prev0, ctx, K, P, keep0, keep_pos, law="recency"):
+    """Position 0 keeps keep0 of its previous list (or draws K afresh); positions 1..P-1 keep
+    floor(keep_pos*K) of position 0 and draw the rest.  Returns int32 [P][K]."""
+    out = np.empty((P, K), np.int32)
+    p0 = next_topk(rng, prev0, ctx, K, keep0 if prev0 is not None else 0.0, law)
+    out[0] = p0
+    for q in range(1, P):
+        out[q] = next_topk(rng, p0, ctx, K, keep_pos, law)
+    return out
+
+
+def config5(seed: int = 0, steps: int = 128, R: int = 256, L: int = 4) -> Workload:
+    """Max-batch mixed load with speculative decode (MTP3): 4 layers, 256 requests, contexts
+    log-uniform in [8192, 1,048,576]; each non-tail page resident with a per-request probability
+    f ~ U[0,1] (tail always resident); P=4 positions per request share one plan, position 0 keeps 80%
+    of its previous list, positions 1..3 keep 90% of position 0; K=2048, hot 4096.  Each step appends
+    U{1..4} tokens (the accepted MTP length) and ends with one offload launch of the pages completed
+    in that step (all layers).  Host copies exist for the host-only pages; a page completed during the
+    run gets a fresh host block when it is offloaded."""
+    P, K, C, S, B = 4, 2048, 4096, 64, 656
+    lr = _layout_rng(5, seed)
+    ctx0 = np.floor(np.exp(lr.uniform(np.log(8192), np.log(1 << 20), size=R))).astype(np.int64)
+    frac = lr.uniform(0.0, 1.0, size=R)
+    grow = lr.integers(1, 5, size=(steps, R)).astype(np.int64)          # accepted tokens per step
+    ctx_final = ctx0 + grow.sum(axis=0)
+    max_pages = int(((ctx_final + S - 1) // S).max())
+    tail0 = (ctx0 - 1) // S
+    pages_final = (ctx_final + S - 1) // S
+    pidx = np.arange(max_pages)[None, :]
+    u = lr.random((R, max_pages))
+    resident = (pidx < tail0[:, None]) & (u < frac[:, None])
+    resident |= (pidx >= tail0[:, None]) & (pidx < pages_final[:, None])   # tail and future pages
+    bt, hot, ngb = _place(R, max_pages, resident, C // S, lr)
+    complete0 = pidx < (ctx0 // S)[:, None]
+    has_host = complete0 & ~resident
+    hbt, nhb_init = _host_place(R, max_pages, has_host, lr)
+    n_new = int((pages_final - ctx0 // S).sum()) + R
+    content = (np.arange(R)[:, None] * max_pages + pidx).astype(np.int64)
+    w = Workload("max-batch-mtp3", 5, seed, L, R, P, K, C, S, B, max_pages, ngb, nhb_init + n_new, bt, hbt, content,
+                 hot, ctx0.astype(np.int32), steps, _pairs(has_host), _pairs(resident), content_seed=seed,
+                 notes="GPU blocks of future tail pages are assigned and filled up front")
+    w._grow = grow
+    w._nhb_init = nhb_init
+
+    def gen(w: Workload, n: int) -> Iterator[Step]:
+        rngs = _rngs(w.cfg, w.seed, w.L * w.R)
+        prev = [None] * (w.L * w.R)
+        ctx = w.ctx_len.astype(np.int64).copy()
+        next_host = w._nhb_init
+        pending_hbt = np.zeros((0, 3), np.int32)
+        for s in range(n):
+            topk = np.empty((w.L, w.R, w.P, w.K), np.int32)
+            for l in range(w.L):
+                for r in range(w.R):
+                    uid = l * w.R + r
+                    lists = _mtp_lists(rngs[uid], prev[uid], int(ctx[r]), w.K, w.P, 0.8, 0.9)
+                    prev[uid] = lists[0]
+                    topk[l, r] = lists
+            g = w._grow[s % w._grow.shape[0]]
+            new_ctx = ctx + g
+            og, oh, src = [], [], []
+            for r in range(w.R):
+                for pg in range(int(ctx[r] // w.S), int(new_ctx[r] // w.S)):
+                    og.append(int(w.block_table[r, pg]))
+                    oh.append(next_host)
+                    src.append((r, pg))
+                    next_host += 1
+            st = Step(index=s, topk=topk, ctx_len=ctx.astype(np.int32), hbt_edits=pending_hbt,
+                      off_gpu=np.array(og, np.int32), off_host=np.array(oh, np.int32),
+                      off_src=np.array(src, np.int64).reshape(-1, 2))
+            pending_hbt = np.array([(r, pg, h) for (r, pg), h in zip(src, oh)], np.int32).reshape(-1, 3)
+            ctx = new_ctx
+            yield st
+    w._gen = gen
+    return w
+
+
+# --------------------------------------------------------------------------- multi-turn agentic
+def config3(seed: int = 0, turns: int = 13, decode_per_turn: int = 220, R: int = 32, L: int = 16,
+            first_turn: int = 74160, prompt_per_turn: int = 753, resident_frac: float = 0.4) -> Workload:
+    """Multi-turn agentic shape: 16 layers, 32 requests in lock-step, 13 turns (74,160-token first
+    turn, then +753 prompt tokens and 220 decode tokens per turn); K=2048, hot 4096, top-K locality
+    as in the mixed batch.  Residency stand-in: each request keeps its newest round(resident_frac *
+    final pages) pages on the GPU (tail included); when a new page needs a block, the oldest resident
+    page is released (its host copy already exists) and its block is reused for the new page, whose
+    rows the model would write (an untimed fill here).  Every completed page is offloaded (all layers,
+    one launch) after the step in which it completes, to a fresh host block; pages completed before
+    the first step have host copies from the start."""
+    K, C, S, B, P = 2048, 4096, 64, 656, 1
+    ctx_final = first_turn + (turns - 1) * (decode_per_turn + prompt_per_turn) + decode_per_turn
+    max_pages = (ctx_final + S - 1) // S
+    budget = int(round(resident_frac * max_pages))
+    lr = _layout_rng(3, seed)
+    ctx0 = first_turn
+    n0 = (ctx0 + S - 1) // S
+    resident = np.zeros((R, max_pages), bool)
+    resident[:, max(0, n0 - budget):n0] = True
+    bt, hot, ngb = _place(R, max_pages, resident, C // S, lr)
+    complete0 = np.zeros((R, max_pages), bool)
+    complete0[:, : ctx0 // S] = True
+    hbt, nhb_init = _host_place(R, max_pages, complete0, lr)
+    content = (np.arange(R)[:, None] * max_pages + np.arange(max_pages)[None, :]).astype(np.int64)
+    steps = turns * decode_per_turn
+    w = Workload("multi-turn-agentic", 3, seed, L, R, P, K, C, S, B, max_pages, ngb,
+                 nhb_init + R * (max_pages - ctx0 // S) + R, bt, hbt, content, hot, np.full(R, ctx0, np.int32),
+                 steps, _pairs(complete0), _pairs(resident), content_seed=seed,
+                 notes=f"resident budget {budget} pages per request")
+    w._budget = budget
+    w._nhb_init = nhb_init
+    w._turn = (decode_per_turn, prompt_per_turn)
+
+    def gen(w: Workload, n: int) -> Iterator[Step]:
+        rngs = _rngs(w.cfg, w.seed, w.L * w.R)
+        prev = [None] * (w.L * w.R)
+        bt = w.block_table.copy()
+        ctx = int(w.ctx_len[0])
+        res_pages = [sorted(np.nonzero(bt[r] >= 0)[0].tolist()) for r in range(w.R)]
+        next_host = w._nhb_init
+        pending_hbt = np.zeros((0, 3), np.int32)
+        dpt, ppt = w._turn
+        done_pages = int(w.ctx_len[0]) // w.S      # pages whose host copy exists or is queued
+        for s in range(n):
+            # tokens written before this step: one decoded token per step, plus the next turn's prompt
+            # at a turn boundary (except before the first step)
+            bt_edits, fills = [], []
+            if s > 0:
+                add = 1 + (ppt if s % dpt == 0 else 0)
+                new_ctx = ctx + add
+                for pg in range((ctx + w.S - 1) // w.S, (new_ctx + w.S - 1) // w.S):   # pages that start
+                    for r in range(w.R):
+                        if len(res_pages[r]) >= w._budget:
+                            old = res_pages[r].pop(0)
+                            blk = int(bt[r, old])
+                            bt[r, old] = -1
+                            bt_edits.append((r, old, -1))
+                        else:
+                            raise RuntimeError("no block to reuse")
+                        bt[r, pg] = blk
+                        res_pages[r].append(pg)
+                        bt_edits.append((r, pg, blk))
+                        fills.append((blk, r, pg))
+                ctx = new_ctx
+            topk = np.empty((w.L, w.R, 1, w.K), np.int32)
+            for l in range(w.L):
+                for r in range(w.R):
+                    uid = l * w.R + r
+                    ids = next_topk(rngs[uid], prev[uid], ctx, w.K, 0.8 if prev[uid] is not None else 0.0, "recency")
+                    prev[uid] = ids
+                    topk[l, r, 0] = ids
+            # pages completed by the tokens this step's context includes but the last offload did not
+            og, oh, src = [], [], []
+            for pg in range(done_pages, ctx // w.S):
+                for r in range(w.R):
+                    og.append(int(bt[r, pg]))
+                    oh.append(next_host)
+                    src.append((r, pg))
+                    next_host += 1
+            done_pages = ctx // w.S
+            st = Step(index=s, topk=topk, ctx_len=np.full(w.R, ctx, np.int32),
+                      bt_edits=np.array(bt_edits, np.int32).reshape(-1, 3),
+                      hbt_edits=pending_hbt, fills=np.array(fills, np.int64).reshape(-1, 3),
+                      off_gpu=np.array(og, np.int32), off_host=np.array(oh, np.int32),
+                      off_src=np.array(src, np.int64).reshape(-1, 2))
+            pending_hbt = np.array([(r, pg, h) for (r, pg), h in zip(src, oh)], np.int32).reshape(-1, 3)
+            yield st
+    w._gen = gen
+    return w
+
+
+CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
 
 
 def make(cfg: int, **kw) -> Workload:

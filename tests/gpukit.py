@@ -25,7 +25,10 @@ class Rig:
         L, R, C, S, B = w.L, w.R, w.C, w.S, w.B
         self.gpu = [torch.empty((w.num_gpu_blocks, S, B), dtype=torch.uint8, device=self.dev) for _ in range(L)]
         nhb = max(1, w.num_host_blocks)
-        self.host = [torch.zeros((nhb, S, B), dtype=torch.uint8).pin_memory() for _ in range(L)]
+        self.host = [sdev.pinned_empty((nhb, S, B)) for _ in range(L)]
+        if oracle_bytes:
+            for h in self.host:
+                h.zero_()
         for l in range(L):
             sdev.fill_gpu_pool(w, l, self.gpu[l])
             if w.num_host_blocks:
@@ -105,7 +108,16 @@ class Rig:
                            pools=self.o_pools, hosts=self.o_hosts, gpu_blocks=st.off_gpu, host_blocks=st.off_host)
         if check:
             self.compare(st, rows, stats, out, o_rows, o_stats)
+            self.check_offload(st)
         return rows, stats, out, o_rows, o_stats
+
+    def check_offload(self, st) -> None:
+        """Every page offloaded after this step holds, in every layer, the closed-form rows of its page."""
+        w = self.w
+        for (r, pg), h in zip(st.off_src, st.off_host):
+            for l in range(w.L):
+                exp = content.page_np(w.content_seed, l, int(w.content_page[r, pg]), w.S, w.B)
+                assert np.array_equal(self.host[l][int(h)].numpy(), exp), f"offloaded page ({r},{pg}) layer {l}"
 
     def compare(self, st, rows, stats, out, o_rows, o_stats) -> None:
         w = self.w
@@ -122,8 +134,10 @@ class Rig:
             idl = ids[l].reshape(w.R, -1).long()
             idl = torch.where(ok[l][:, None], idl, torch.full_like(idl, -1))
             r_idx = torch.arange(w.R, device=self.dev)[:, None].expand_as(idl).reshape(-1)
-            exp = sdev.expected_rows(w, l, r_idx, idl.reshape(-1))
-            assert torch.equal(out[l], exp), f"gathered bytes differ at step {st.index} layer {l}"
+            flat = idl.reshape(-1)
+            for c0 in range(0, flat.numel(), 1 << 18):
+                exp = sdev.expected_rows(w, l, r_idx[c0:c0 + (1 << 18)], flat[c0:c0 + (1 << 18)])
+                assert torch.equal(out[l][c0:c0 + (1 << 18)], exp), f"gathered bytes differ at step {st.index} layer {l}"
         if self.o_pools is not None:
             for l in range(w.L):
                 assert np.array_equal(self.gpu[l].cpu().numpy().reshape(-1), self.o_pools[l]), \
@@ -144,6 +158,9 @@ class Rig:
             v = torch.arange(w.C, device=self.dev)[None, :].expand_as(t)
             prow = self.hot_blocks.long()[r_idx, v // w.S] * w.S + v % w.S
             m = t >= 0
-            got = self.gpu[l].reshape(-1, w.B)[prow[m]]
-            exp = sdev.expected_rows(w, l, r_idx[m], t[m])
-            assert torch.equal(got, exp), f"hot rows differ from their tokens' bytes (layer {l})"
+            rows_m, r_m, t_m = prow[m], r_idx[m], t[m]
+            for c0 in range(0, rows_m.numel(), 1 << 18):
+                sl = slice(c0, c0 + (1 << 18))
+                got = self.gpu[l].reshape(-1, w.B)[rows_m[sl]]
+                exp = sdev.expected_rows(w, l, r_m[sl], t_m[sl])
+                assert torch.equal(got, exp), f"hot rows differ from their tokens' bytes (layer {l})"

@@ -130,6 +130,51 @@ def test_cold_start_prefix_reuse_full_size(mode):
     assert int(stats[..., 3].sum()) > 0
 
 
+def test_max_batch_mtp3_full_size():
+    """4 layers x 256 requests, contexts log-uniform to 1,048,576 tokens, per-page residency, P=4 query
+    positions sharing one plan per step, contexts growing by the accepted MTP length, and one offload
+    launch of the completed pages (all layers) after every step -- the full-size configuration,
+    fused path, first 6 steps."""
+    w = workloads.config5(seed=0, steps=6)
+    rig = _rig(w, mode="fused")
+    offloaded = 0
+    for st in w.iter_steps(6):
+        _, stats, *_ = rig.step(st)
+        offloaded += len(st.off_gpu)
+    assert offloaded > 0
+
+
+def test_max_batch_mtp3_split_path_64_requests():
+    w = workloads.config5(seed=1, steps=4, R=64)
+    rig = _rig(w, mode="split")
+    for st in w.iter_steps(4):
+        rig.step(st)
+
+
+def test_multi_turn_agentic_full_geometry():
+    """16 layers x 32 requests at the first turn's 74,160-token context with a 40% resident budget:
+    24 steps cover the first completed page (offloaded for all 16 layers in one launch) and the
+    release of each request's oldest resident page whose block is reused for the new page."""
+    w = workloads.config3(seed=0)
+    rig = _rig(w, mode="fused")
+    saw_edit = saw_off = False
+    for st in w.iter_steps(24):
+        rig.step(st)
+        saw_edit |= len(st.bt_edits) > 0
+        saw_off |= len(st.off_gpu) > 0
+    assert saw_edit and saw_off
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_multi_turn_agentic_turn_boundaries(mode):
+    """Same geometry with 6 decode steps per turn, so two turn boundaries (753 prompt tokens: a dozen
+    pages complete and start at once) fall inside 14 steps."""
+    w = workloads.config3(seed=2, decode_per_turn=6, L=4)
+    rig = _rig(w, mode=mode)
+    for st in w.iter_steps(14):
+        rig.step(st)
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_data_errors_are_isolated_per_unit(mode):
     w = workloads.config1(seed=3, steps=3)
