@@ -318,7 +318,9 @@ class PreparedStep:
         self.pool, self.hot = pool, hot
         self._keep = (block_table, host_block_table, ctx_len, out_rows, out_stats, workspace, gather_out, gather_status)
         self.L = lib()
-        self.stream = _stream(stream)
+        # stream=None: launch on whatever torch stream is current at each call (so the calls can be
+        # captured into a CUDA graph); otherwise always on the given stream
+        self._fixed_stream = None if stream is None else _stream(stream)
         self.lb = int(layer_begin)
         self.max_pages = int(block_table.shape[1])
         self.args_bt = (_dev_i32(block_table, "block_table"), _dev_i32(host_block_table, "host_block_table"),
@@ -332,6 +334,10 @@ class PreparedStep:
         self.n_per_layer = R * P * K
         if gather_out.numel() != nl * self.n_per_layer * pool.row_bytes:
             raise ValueError("gather_out must hold nl*R*P*K rows")
+
+    @property
+    def stream(self) -> ctypes.c_void_p:
+        return self._fixed_stream if self._fixed_stream is not None else _stream(None)
 
     def resolve(self, topk: torch.Tensor, step: int) -> None:
         nl, R, P, K = self.shape

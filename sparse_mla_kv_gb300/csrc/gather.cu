@@ -179,6 +179,9 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
   }
 }
 
+int g_occ_plain[2] = {0, 0};
+int g_occ_fused[2] = {0, 0};
+
 template <typename Kern>
 int resident_blocks(Kern kern, int* cache) {
   if (*cache <= 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(cache, kern, kGatherThreads, 0) != cudaSuccess)
@@ -196,10 +199,17 @@ dim3 wave_grid(int sms, int occ, int64_t want, int nl) {
 
 }  // namespace
 
+void warm_gather_launch_configs() {
+  resident_blocks(gather_kernel<41>, &g_occ_plain[0]);
+  resident_blocks(gather_kernel<0>, &g_occ_plain[1]);
+  resident_blocks(gather_fused_kernel<41>, &g_occ_fused[0]);
+  resident_blocks(gather_fused_kernel<0>, &g_occ_fused[1]);
+}
+
 cudaError_t launch_gather(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, const int32_t* rows, int64_t n,
                           uint8_t* out, int32_t row_bytes, int64_t num_rows, int32_t* status, int sms,
                           cudaStream_t s) {
-  static int occ[2] = {0, 0};
+  int* occ = g_occ_plain;
   const bool k41 = row_bytes == 656;
   auto kern = k41 ? gather_kernel<41> : gather_kernel<0>;
   const int64_t want = (n * (row_bytes >> 4) + (int64_t)kGatherThreads * kGatherUnroll - 1) /
@@ -214,7 +224,7 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
                                 int32_t max_m, const int32_t* rows, const int32_t* miss_count, const int4* miss_list,
                                 const int32_t* msrc, uint8_t* out, int32_t row_bytes, int64_t num_rows, int sms,
                                 cudaStream_t s) {
-  static int occ[2] = {0, 0};
+  int* occ = g_occ_fused;
   const bool k41 = row_bytes == 656;
   auto kern = k41 ? gather_fused_kernel<41> : gather_fused_kernel<0>;
   const int64_t per_layer = (int64_t)R * n * (row_bytes >> 4);

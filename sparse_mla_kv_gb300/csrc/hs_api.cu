@@ -103,6 +103,13 @@ hs_status hs_pool_create(const hs_pool_desc* d, hs_pool** out) {
       p->ptrs.host[l] = static_cast<uint8_t*>(dp);
     }
   }
+  // settle the lazily computed launch configuration now, once, outside any later stream work
+  if (hs::sm_count(p->device) <= 0 || hs::resolve_smem_limit(p->device) == 0) {
+    cudaGetLastError();
+    delete p;
+    return HS_ERR_CUDA;
+  }
+  hs::warm_gather_launch_configs();
   *out = p;
   return HS_OK;
 }
@@ -163,8 +170,10 @@ hs_status prepare_resolve(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
   if (n > 0 && (!topk_ids || !out_rows)) return HS_ERR_INVALID_ARG;
   if (!hs::aligned16(workspace) || workspace_bytes < hs::resolve_workspace_bytes((int64_t)nl * R, n, C))
     return HS_ERR_INVALID_ARG;
+  const size_t smem_limit = hs::resolve_smem_limit(pool->device);
   sm = hs::resolve_smem_plan(n, C, g.page_size);
-  if (sm.total == 0 || sm.total > hs::resolve_smem_limit(pool->device)) return HS_ERR_INVALID_ARG;
+  if (sm.total == 0 || sm.total > smem_limit) return HS_ERR_INVALID_ARG;
+  sm = hs::resolve_smem_plan_staged(n, C, g.page_size, max_pages, smem_limit);
   sms = hs::sm_count(pool->device);
   if (sms <= 0) return HS_ERR_CUDA;
 

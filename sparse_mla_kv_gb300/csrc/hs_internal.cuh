@@ -70,11 +70,17 @@ struct ResolveSmem {
   // byte offsets into dynamic shared memory
   size_t tok, stamp, ids, val, cls, idh, hot, u /* slot hash, later radix buffers */, total;
   int32_t id_hash_bits, slot_hash_bits;
+  size_t tbl;         // staged block-table + host-table rows (when tbl_pages > 0)
+  int32_t tbl_pages;
 };
 
 // Shared-memory plan of one resolver CTA for (n = P*K ids, C slots, page size S); total = 0 if out
 // of limits.
 ResolveSmem resolve_smem_plan(int64_t n, int64_t C, int64_t S);
+// The same plan plus the request's two table rows staged in shared memory when max_pages is at most
+// kMaxStagedPages and the total stays within `limit`.
+constexpr int64_t kMaxStagedPages = 8192;
+ResolveSmem resolve_smem_plan_staged(int64_t n, int64_t C, int64_t S, int64_t max_pages, size_t limit);
 size_t resolve_workspace_bytes(int64_t units, int64_t n, int64_t C);
 // Largest dynamic shared memory a resolver CTA may use on device `dev` (0 on failure).
 size_t resolve_smem_limit(int dev);
@@ -98,5 +104,8 @@ cudaError_t launch_offload(const LayerPtrs& ptrs, const PoolGeom& g, const int32
 cudaError_t launch_fill_i32(int32_t* a, int64_t count, int32_t value, int sms, cudaStream_t s);
 
 void count_launch(int k = 1);
+// Per-device launch configuration (occupancy, shared-memory limits) is computed once, at pool
+// creation, so that no later call needs a CUDA attribute query.
+void warm_gather_launch_configs();
 
 }  // namespace hs

@@ -148,6 +148,8 @@ __device__ unsigned short* radix_sort_slots(unsigned short* a, unsigned short* b
   return a;
 }
 
+// kS: the page size when it is a compile-time constant (64 in the pages' FP8 MLA setup), else 0.
+template <int kS>
 __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const ResolveParams p, const ResolveSmem sm) {
   extern __shared__ __align__(16) unsigned char smem[];
   int32_t* s_tok = reinterpret_cast<int32_t*>(smem + sm.tok);
@@ -158,6 +160,10 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
   int* s_idh = reinterpret_cast<int*>(smem + sm.idh);
   int* s_slh = reinterpret_cast<int*>(smem + sm.u);
   int32_t* s_hot = reinterpret_cast<int32_t*>(smem + sm.hot);
+  // the request's block-table and host-table rows, staged when they are small (sm.tbl_pages > 0)
+  const bool staged = sm.tbl_pages > 0;
+  int32_t* s_bt = reinterpret_cast<int32_t*>(smem + sm.tbl);
+  int32_t* s_hbt = s_bt + sm.tbl_pages;
   __shared__ uint32_t s_err;
   __shared__ int s_cnt[3];
   __shared__ int s_lo, s_hi;
@@ -167,7 +173,8 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
   const int unit = blockIdx.x;
   const int lr = unit / p.R, r = unit - lr * p.R;
   const int l = p.layer_begin + lr;
-  const int n = p.n, C = p.C, S = p.S, step = p.step;
+  const int n = p.n, C = p.C, step = p.step;
+  const int S = kS ? kS : p.S;
   const int64_t state_off = ((int64_t)l * p.R + r) * C;
   const int32_t* ids_g = p.topk + (int64_t)unit * n;
   const int32_t* bt = p.bt + (int64_t)r * p.max_pages;
@@ -192,16 +199,22 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
   // that classification needs no global-memory round trip.  Combined entry in s_val:
   //   e >= 0      resident block e;      e == -1   placeholder without a host copy;
   //   e == kBadHost  placeholder whose host block is outside the pool;  else host block -2 - e.
+  if (staged) {
+    for (int j = tid; j < sm.tbl_pages; j += kResolveThreads) {
+      s_bt[j] = bt[j];
+      s_hbt[j] = hbt[j];
+    }
+  }
 #pragma unroll 4
   for (int i = tid; i < n; i += kResolveThreads) {
     const int id = ids_g[i];
     s_ids[i] = id;
     int e = -1;
     if (id != -1) {
-      if (id < -1 || id >= ctx || id / S >= p.max_pages) {
+      if (id < -1 || id >= ctx || (unsigned)id / S >= (unsigned)p.max_pages) {
         err |= kErrId;
-      } else {
-        const int page = id / S;
+      } else if (!staged) {
+        const int page = (unsigned)id / S;
         const int b = bt[page];
         const int h = hbt[page];
         e = b >= 0 ? b : (h < 0 ? -1 : (h >= p.num_host_blocks ? kBadHost : -2 - h));
@@ -233,7 +246,15 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
     }
     for (int i = tid; i < n; i += kResolveThreads) {
       const int id = s_ids[i];
-      if (id >= 0) hash_insert_min(s_idh, sm.id_hash_bits, s_ids, id, i);
+      if (id >= 0) {
+        hash_insert_min(s_idh, sm.id_hash_bits, s_ids, id, i);
+        if (staged) {
+          const int page = (unsigned)id / S;
+          const int b = s_bt[page];
+          const int h = s_hbt[page];
+          s_val[i] = b >= 0 ? b : (h < 0 ? -1 : (h >= p.num_host_blocks ? kBadHost : -2 - h));
+        }
+      }
     }
   }
   __syncthreads();
@@ -246,7 +267,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
       uint8_t cls = kNone;
       int val = 0;
       if (id >= 0 && hash_find(s_idh, sm.id_hash_bits, s_ids, id) == i) {
-        const int off = id % S;
+        const int off = (unsigned)id % S;
         const int e = s_val[i];
         if (e >= 0) {
           if (e >= p.num_gpu_blocks) err |= kErrTable;
@@ -330,7 +351,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
       const uint8_t cls = s_cls[i];
       if (cls == kMiss) {
         const int v = sorted[j];
-        const int vb = v / S;
+        const int vb = (unsigned)v / S;
         const int dst = s_hot[vb] * S + (v - vb * S);
         p.miss_list[(int64_t)unit * p.max_m + j] = make_int4(s_val[i], dst, r * n + i, 0);
         if (msrc_g) msrc_g[i] = kGatherOwnedByMissWarps;
@@ -340,7 +361,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
         ++j;
       } else if (cls == kHit) {
         const int v = s_val[i];
-        const int vb = v / S;
+        const int vb = (unsigned)v / S;
         p.slot_stamp[state_off + v] = step;
         s_val[i] = s_hot[vb] * S + (v - vb * S);
         if (msrc_g) msrc_g[i] = s_val[i];
@@ -362,7 +383,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
           if (msrc_g) {
             // a repeated position of a miss reads the host row again (the first occurrence's host
             // row is re-derived from the host block table, which was valid for it)
-            msrc_g[i] = s_cls[f] == kMiss ? -2 - (hbt[id / S] * S + id % S) : row;
+            msrc_g[i] = s_cls[f] == kMiss ? -2 - (hbt[(unsigned)id / S] * S + (unsigned)id % S) : row;
           }
         }
       } else if (msrc_g) {
@@ -496,6 +517,18 @@ ResolveSmem resolve_smem_plan(int64_t n, int64_t C, int64_t S) {
   return sm;
 }
 
+ResolveSmem resolve_smem_plan_staged(int64_t n, int64_t C, int64_t S, int64_t max_pages, size_t limit) {
+  ResolveSmem sm = resolve_smem_plan(n, C, S);
+  if (sm.total == 0) return sm;
+  const size_t tbl = align16(8 * (size_t)max_pages);
+  if (max_pages <= kMaxStagedPages && sm.total + tbl <= limit) {
+    sm.tbl = sm.total;
+    sm.tbl_pages = (int32_t)max_pages;
+    sm.total += tbl;
+  }
+  return sm;
+}
+
 size_t resolve_workspace_bytes(int64_t units, int64_t n, int64_t C) {
   // [miss counts, 16-byte aligned] [miss lists: units x min(n, C) int4] [per-position sources: units x n]
   const int64_t max_m = n < C ? n : C;
@@ -511,18 +544,25 @@ size_t resolve_smem_limit(int dev) {
   if (v > 0) return (size_t)v;
   int optin = 0;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
-  cudaFuncAttributes fa{};
-  if (cudaFuncGetAttributes(&fa, resolve_kernel) != cudaSuccess) return 0;
-  const long long dyn = (long long)optin - (long long)fa.sharedSizeBytes;
+  cudaFuncAttributes fa{}, fb{};
+  if (cudaFuncGetAttributes(&fa, resolve_kernel<64>) != cudaSuccess) return 0;
+  if (cudaFuncGetAttributes(&fb, resolve_kernel<0>) != cudaSuccess) return 0;
+  const size_t st = fa.sharedSizeBytes > fb.sharedSizeBytes ? fa.sharedSizeBytes : fb.sharedSizeBytes;
+  const long long dyn = (long long)optin - (long long)st;
   if (dyn <= 0) return 0;
-  if (cudaFuncSetAttribute(resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) != cudaSuccess)
+  if (cudaFuncSetAttribute(resolve_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) != cudaSuccess)
+    return 0;
+  if (cudaFuncSetAttribute(resolve_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) != cudaSuccess)
     return 0;
   limit[dev].store(dyn);
   return (size_t)dyn;
 }
 
 cudaError_t launch_resolve(const ResolveParams& p, const ResolveSmem& sm, cudaStream_t s) {
-  resolve_kernel<<<p.nl * p.R, kResolveThreads, sm.total, s>>>(p, sm);
+  if (p.S == 64)
+    resolve_kernel<64><<<p.nl * p.R, kResolveThreads, sm.total, s>>>(p, sm);
+  else
+    resolve_kernel<0><<<p.nl * p.R, kResolveThreads, sm.total, s>>>(p, sm);
   count_launch();
   return cudaGetLastError();
 }

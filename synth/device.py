@@ -54,18 +54,15 @@ def fill_host_pool(w, layer: int, host: torch.Tensor, device) -> None:
     fill_blocks(w, layer, host, blocks[order], own[blocks[order]], device, chunk_blocks=2048)
 
 
-_CPT_CACHE = {}
-
-
 def expected_rows(w, layer: int, r_idx: torch.Tensor, ids: torch.Tensor) -> torch.Tensor:
     """Closed-form bytes of logical tokens ids (int64, device) of requests r_idx -> uint8 [n, B];
     ids == -1 gives zero rows."""
     dev = ids.device
-    key = (id(w), str(dev))
-    if key not in _CPT_CACHE:
-        _CPT_CACHE.clear()
-        _CPT_CACHE[key] = torch.from_numpy(w.content_page.astype(np.int64)).to(dev)
-    cpt = _CPT_CACHE[key]
+    cached = getattr(w, "_content_page_dev", None)   # a device copy kept on the workload itself
+    if cached is None or cached.device != dev:
+        cached = torch.from_numpy(w.content_page.astype(np.int64)).to(dev)
+        w._content_page_dev = cached
+    cpt = cached
     valid = ids >= 0
     safe = torch.where(valid, ids, torch.zeros_like(ids))
     cp = cpt[r_idx, safe // w.S]

@@ -15,9 +15,11 @@ from synth import content, device as sdev
 
 class Rig:
     def __init__(self, w, *, oracle_bytes: bool = False, device: str = "cuda", check_hot_bytes: bool = True,
-                 mode: str = "split"):
+                 mode: str = "split", graph: bool = False):
         assert mode in ("split", "fused")
         self.mode = mode
+        self.graph = graph
+        self.prep = None
         self.w = w
         self.dev = torch.device(device)
         self.oracle_bytes = oracle_bytes
@@ -86,14 +88,16 @@ class Rig:
         self.apply_edits(st)
         topk = torch.from_numpy(st.topk).to(self.dev)
         ctx = torch.from_numpy(st.ctx_len.astype(np.int32)).to(self.dev)
-        if self.mode == "fused":
+        if self.graph:
+            rows, stats, out = self._graph_step(st, topk, ctx)
+        elif self.mode == "fused":
             rows, stats, out = hs.resolve_gather(self.pool, topk, self.bt, self.hbt, ctx, self.hot, st.index,
                                                  workspace=self.ws)
         else:
             rows, stats = hs.resolve_topk(self.pool, topk, self.bt, self.hbt, ctx, self.hot, st.index,
                                           workspace=self.ws)
             out = hs.gather_rows(self.pool, rows.reshape(w.L, -1))
-        if len(st.off_gpu):
+        if len(st.off_gpu) and not self.graph:
             hs.offload_pages(self.pool, torch.from_numpy(st.off_gpu).to(self.dev),
                              torch.from_numpy(st.off_host).to(self.dev))
         torch.cuda.synchronize()
@@ -118,6 +122,33 @@ class Rig:
             for l in range(w.L):
                 exp = content.page_np(w.content_seed, l, int(w.content_page[r, pg]), w.S, w.B)
                 assert np.array_equal(self.host[l][int(h)].numpy(), exp), f"offloaded page ({r},{pg}) layer {l}"
+
+    def _graph_step(self, st, topk, ctx):
+        """The whole step (resolve + gather, and the step's offload) captured into one CUDA graph, then
+        replayed once."""
+        w = self.w
+        if self.prep is None:
+            self.ctx_dev = torch.empty(w.R, dtype=torch.int32, device=self.dev)
+            self.g_rows = torch.empty((w.L, w.R, w.P, w.K), dtype=torch.int32, device=self.dev)
+            self.g_stats = torch.empty((w.L, w.R, 4), dtype=torch.int32, device=self.dev)
+            self.g_out = torch.empty((w.L, w.R * w.P * w.K, w.B), dtype=torch.uint8, device=self.dev)
+            self.prep = hs.PreparedStep(self.pool, self.hot, self.bt, self.hbt, self.ctx_dev, self.g_rows,
+                                        self.g_stats, self.ws, self.g_out)
+        self.ctx_dev.copy_(ctx)
+        gb = torch.from_numpy(st.off_gpu).to(self.dev)
+        hb = torch.from_numpy(st.off_host).to(self.dev)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            if self.mode == "fused":
+                self.prep.resolve_gather(topk, st.index)
+            else:
+                self.prep.resolve(topk, st.index)
+                self.prep.gather()
+            self.prep.offload(gb, hb, len(st.off_gpu))
+        g.replay()
+        torch.cuda.synchronize()
+        return self.g_rows, self.g_stats, self.g_out.reshape(w.L, -1, w.B)
 
     def compare(self, st, rows, stats, out, o_rows, o_stats) -> None:
         w = self.w

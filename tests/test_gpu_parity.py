@@ -130,6 +130,21 @@ def test_cold_start_prefix_reuse_full_size(mode):
     assert int(stats[..., 3].sum()) > 0
 
 
+@pytest.mark.parametrize("mode", MODES)
+def test_whole_step_captured_in_a_cuda_graph(mode):
+    """Each decode step -- resolve + gather and the step's single offload launch -- captured into one
+    CUDA graph and replayed (no host decision anywhere on the path): results identical to the oracle.
+    Uses the agentic workload with compressed turns so steps with offloads and table edits occur."""
+    w = workloads.config3(seed=4, decode_per_turn=6, L=2, R=8)
+    rig = _rig(w, mode=mode, graph=True)
+    for st in w.iter_steps(13):
+        rig.step(st)
+    w1 = workloads.config1(seed=6, steps=6)
+    rig1 = _rig(w1, mode=mode, graph=True, oracle_bytes=True)
+    for st in w1.iter_steps():
+        rig1.step(st)
+
+
 def test_max_batch_mtp3_full_size():
     """4 layers x 256 requests, contexts log-uniform to 1,048,576 tokens, per-page residency, P=4 query
     positions sharing one plan per step, contexts growing by the accepted MTP length, and one offload
