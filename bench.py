@@ -6,9 +6,11 @@ Default workload: the mixed-residency decode batch -- 1 sparse-MLA layer, 64 req
 page 64, 656-byte rows, K=2048, hot buffer 4096 rows per request; each step keeps 80% of the previous
 top-K and draws the rest with probability proportional to recency^-0.7.  Synthetic, seeded.
 
-One step = hs_resolve_topk (resolver + miss copy) + hs_gather_rows over the step's batch (+ one
-hs_offload_pages launch when pages complete; this workload's contexts are fixed, so none do).
-L2 is flushed (a 256 MB write) before every timed step, outside the timed events.
+One step = the fused path (hs_resolve_plan + hs_gather_planned: the resolver, then one gather that
+also carries the miss copies) or, with --path split, hs_resolve_topk + hs_gather_rows, over the
+step's batch (+ one hs_offload_pages launch when pages complete; this workload's contexts are fixed,
+so none do).  L2 is flushed (a 256 MB write) before every timed step, outside the timed events, and
+the host waits for each step before enqueueing the next.
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on the host cores instead.
 """
@@ -47,6 +49,19 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--soak-seconds", type=float, default=1.5)
+    ap.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi during the timed steps")
+    ap.add_argument("--passes", type=int, default=2, choices=[1, 2],
+                    help="2: an untimed pass over the warm-up and timed steps precedes the timed pass")
+    ap.add_argument("--no-prefault", action="store_true",
+                    help="skip the one bulk read of the pinned host pool through the GPU before timing")
+    ap.add_argument("--run-ahead", action="store_true",
+                    help="enqueue all timed steps without waiting for each (default: wait for each step's end "
+                         "before enqueueing the next; the L2 flush queued ahead of each step keeps the GPU busy "
+                         "while the step is enqueued)")
+    ap.add_argument("--timing", choices=["graph", "eager"], default="eager",
+                    help="eager: the step's C-ABI calls, each timed step enqueued behind a 256 MB L2 flush so the "
+                         "GPU is busy while the host enqueues it; graph: replays of CUDA graphs captured from those "
+                         "calls, one pair per step")
     ap.add_argument("--path", choices=["fused", "split"], default="fused",
                     help="fused: hs_resolve_plan + hs_gather_planned (miss copies inside the gather); "
                          "split: hs_resolve_topk (resolver + miss-copy kernel) + hs_gather_rows")
@@ -232,7 +247,8 @@ def config_dict(w, args):
             "layers": w.L, "requests": w.R, "ctx": int(w.ctx_len[0]), "page": w.S, "row_bytes": w.B, "K": w.K,
             "P": w.P, "hot_rows": w.C, "rows_per_step": w.rows_per_step, "seed": args.seed,
             "index_dtype": "int32", "l2": "flushed (256 MB write) before every timed step, outside the timing",
-            "path": getattr(args, "path", "fused")}
+            "path": getattr(args, "path", "fused"), "timing": getattr(args, "timing", "eager"),
+            "warmup_passes": getattr(args, "passes", 2)}
 
 
 # ----------------------------------------------------------------------------- the GPU leg
@@ -251,7 +267,7 @@ def run_ours(args, ws, rank, local):
     w, steps = make_workload(args.config, args.seed, W + K)
     L, R, P, Kk, C, S, B = w.L, w.R, w.P, w.K, w.C, w.S, w.B
     gpu = [torch.empty((w.num_gpu_blocks, S, B), dtype=torch.uint8, device=dev) for _ in range(L)]
-    host = [torch.empty((max(1, w.num_host_blocks), S, B), dtype=torch.uint8, pin_memory=True) for _ in range(L)]
+    host = [sdev.pinned_empty((max(1, w.num_host_blocks), S, B)) for _ in range(L)]
     for l in range(L):
         sdev.fill_gpu_pool(w, l, gpu[l])
         sdev.fill_host_pool(w, l, host[l], dev)
@@ -268,7 +284,7 @@ def run_ours(args, ws, rank, local):
     gout = torch.empty((L, R * P * Kk, B), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    prep = hs.PreparedStep(pool, hot, bt, hbt, ctx, out_rows, out_stats, ws_buf, gout, stream=stream)
+    prep = hs.PreparedStep(pool, hot, bt, hbt, ctx, out_rows, out_stats, ws_buf, gout)
 
     # host-link bandwidth (bulk pinned copies), for the step roofline's H2D term
     hbuf = torch.empty(256 << 20, dtype=torch.uint8, pin_memory=True)
@@ -287,29 +303,63 @@ def run_ours(args, ws, rank, local):
 
     fused = args.path == "fused"
 
+    # One bulk DMA read of the whole pinned host pool through the GPU before anything is timed: the
+    # first GPU accesses to freshly pinned host pages are slow (their GPU mappings are set up on
+    # first use), which a long-running server pays once, not per step.
+    if not args.no_prefault:
+        scratch = torch.empty(64 << 20, dtype=torch.uint8, device=dev)
+        for h in host:
+            flat = h.view(-1)
+            for o in range(0, flat.numel(), scratch.numel()):
+                n_ = min(scratch.numel(), flat.numel() - o)
+                scratch[:n_].copy_(flat[o:o + n_], non_blocking=True)
+        torch.cuda.synchronize()
+        del scratch
+
     def phase1(i):
         (prep.plan if fused else prep.resolve)(topk_all[i], steps[i].index)
 
     def phase2():
         (prep.gather_planned if fused else prep.gather)()
 
-    # warm-up steps
-    for i in range(W):
-        phase1(i)
-        phase2()
-    torch.cuda.synchronize()
-    st_w = out_stats.cpu().numpy()
-    assert (st_w[..., 0] == 0).all(), "warm-up step reported a data error"
+    # warm-up: one untimed pass over the warm-up AND the timed steps, then the hot state is reset and
+    # the warm-up steps replayed, so the timed steps start from exactly the state they would have had.
+    # The timed steps' host rows have then been read through the GPU once, as in a long-running
+    # server; right after another process unpins a large amount of host memory, the first GPU reads
+    # of pinned pages can stall for milliseconds for a few seconds (--passes 1 skips the first pass).
+    for p_ in range(args.passes):
+        if p_:
+            hs.hot_reset(pool, hot)
+        for i in range(W + (K if p_ + 1 < args.passes else 0)):
+            phase1(i)
+            phase2()
+        torch.cuda.synchronize()
+        st_w = out_stats.cpu().numpy()
+        assert (st_w[..., 0] == 0).all(), "warm-up step reported a data error"
 
-    # clock soak: repeated gathers of the last warm-up step (read-only for the hot state) so the clocks
-    # settle and the sampler sees the GPU under this load before and during the timed steps
-    sampler = ClockSampler(local) if rank == 0 else None
+    # clock soak: the last warm-up step's phase 2 again and again (it rewrites the same bytes, so the
+    # workload state does not change), each after an L2 flush, so the HBM and the host link carry this
+    # step's traffic while the clocks settle and the sampler sees the GPU under load
+    sampler = ClockSampler(local) if rank == 0 and not args.no_clocks else None
     t_end = time.time() + args.soak_seconds
     while time.time() < t_end:
-        for _ in range(50):
-            prep.gather()   # plain gather of the last rows: reads only
+        for _ in range(20):
+            flush.fill_(1)
+            phase2()
         torch.cuda.synchronize()
 
+    # --timing graph: each timed step is two CUDA graphs (phase 1 and phase 2), captured up front
+    graphs, kernels_per_step = [], 0
+    if args.timing == "graph":
+        for k in range(K):
+            gp, gg = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            n0 = hs.launch_count()
+            with torch.cuda.graph(gp):
+                phase1(W + k)
+            with torch.cuda.graph(gg):
+                phase2()
+            kernels_per_step = hs.launch_count() - n0
+            graphs.append((gp, gg))
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     stats_all = torch.empty((K, L, R, 4), dtype=torch.int32, device=dev)
     barrier(dist)
@@ -320,15 +370,18 @@ def run_ours(args, ws, rank, local):
         i = W + k
         flush.fill_(k & 0xFF)
         ev[k][0].record(stream)
-        phase1(i)
+        graphs[k][0].replay() if graphs else phase1(i)
         ev[k][1].record(stream)
-        phase2()
+        graphs[k][1].replay() if graphs else phase2()
         ev[k][2].record(stream)
         stats_all[k].copy_(out_stats, non_blocking=True)   # after the step's events: not timed
+        if not args.run_ahead:
+            ev[k][2].synchronize()
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     barrier(dist)
-    launches = hs.launch_count() - n_launch0
+    # our kernels inside the timed region: counted at capture for graph replays, live otherwise
+    launches = K * kernels_per_step if graphs else hs.launch_count() - n_launch0
     clocks = sampler.stop() if sampler else None
     t_step = [ev[k][0].elapsed_time(ev[k][2]) * 1e-3 for k in range(K)]
     t_res = [ev[k][0].elapsed_time(ev[k][1]) * 1e-3 for k in range(K)]
@@ -372,6 +425,9 @@ def run_ours(args, ws, rank, local):
                  "frac": sum(roofs) / sum(meas), "misses_per_step_mean": m_mean,
                  "h2d_gbs_measured_bulk_copy": h2d_gbs, "path": args.path,
                  "phase1_us_mean": 1e6 * statistics.fmean(t_res), "phase2_us_mean": 1e6 * t_g,
+                 "phase1_us_median": 1e6 * statistics.median(t_res), "phase2_us_median": 1e6 * statistics.median(t_gat),
+                 "phase2_us_max": 1e6 * max(t_gat), "step_us_median": 1e6 * statistics.median(t_step),
+                 "phase2_us_all": [round(1e6 * x, 1) for x in t_gat],
                  "phase1": "hs_resolve_plan" if fused else "hs_resolve_topk (resolver + miss copy)",
                  "phase2": "hs_gather_planned" if fused else "hs_gather_rows"}
 

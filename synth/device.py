@@ -32,12 +32,15 @@ def fill_blocks(w, layer: int, dst: torch.Tensor, blocks: np.ndarray, owners: np
         if dst.is_cuda:
             dst[torch.from_numpy(b.astype(np.int64)).to(dst.device)] = rows
         else:
-            host = rows.cpu()
-            bi = torch.from_numpy(b.astype(np.int64))
-            if len(b) and (np.diff(b) == 1).all():
-                dst[int(b[0]):int(b[0]) + len(b)].copy_(host)
-            else:
-                dst[bi] = host
+            # pinned host pool: written by DMA straight from the device, one copy per run of
+            # consecutive blocks (in a serving system the host pool is written by the GPU too --
+            # offloads and prefill -- never by CPU stores)
+            cuts = np.nonzero(np.diff(b) != 1)[0] + 1
+            starts = np.concatenate([[0], cuts])
+            ends = np.concatenate([cuts, [len(b)]])
+            for a, e in zip(starts, ends):
+                dst[int(b[a]):int(b[a]) + int(e - a)].copy_(rows[a:e])
+            torch.cuda.synchronize(rows.device)
 
 
 def fill_gpu_pool(w, layer: int, pool: torch.Tensor) -> None:
