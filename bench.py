@@ -86,6 +86,13 @@ def dist_init(ws):
     return None
 
 
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank serves its own independent batch of requests (the path shards by request: every
+    (layer, request) unit, table row, hot buffer and output slice is independent), so ranks draw
+    different requests from the same generator: weak scaling, no data-path collective."""
+    return seed + 1000003 * rank
+
+
 def barrier(dist):
     if dist is not None:
         dist.barrier()
@@ -264,7 +271,7 @@ def run_ours(args, ws, rank, local):
     from synth import device as sdev
 
     W, K = args.warmup, args.steps
-    w, steps = make_workload(args.config, args.seed, W + K)
+    w, steps = make_workload(args.config, rank_seed(args.seed, rank), W + K)
     L, R, P, Kk, C, S, B = w.L, w.R, w.P, w.K, w.C, w.S, w.B
     gpu = [torch.empty((w.num_gpu_blocks, S, B), dtype=torch.uint8, device=dev) for _ in range(L)]
     host = [sdev.pinned_empty((max(1, w.num_host_blocks), S, B)) for _ in range(L)]
