@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
     const LayerPtrs ptrs, int32_t layer_begin, int32_t R, int32_t n, int32_t max_m, const int32_t* __restrict__ rows,
     const int32_t* __restrict__ miss_count, const int4* __restrict__ miss_list, const int32_t* __restrict__ msrc,
     uint8_t* __restrict__ out, int32_t row_bytes, int64_t num_rows) {
+  pdl_wait_prerequisites();   // the resolve plan (rows, sources, miss lists) must be complete and visible
   const int cpr = CPR ? CPR : (row_bytes >> 4);
   const int lr = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -231,8 +232,9 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
   const int64_t want = (per_layer + (int64_t)kGatherThreads * kGatherUnroll - 1) /
                        ((int64_t)kGatherThreads * kGatherUnroll);
   const dim3 grid = wave_grid(sms, resident_blocks(kern, &occ[k41 ? 0 : 1]), want, nl);
-  kern<<<grid, kGatherThreads, 0, s>>>(ptrs, layer_begin, R, n, max_m, rows, miss_count, miss_list, msrc, out,
-                                       row_bytes, num_rows);
+  cudaError_t e = launch_dependent(kern, grid, dim3(kGatherThreads), 0, s, ptrs, layer_begin, R, n, max_m, rows,
+                                   miss_count, miss_list, msrc, out, row_bytes, num_rows);
+  if (e != cudaSuccess) return e;
   count_launch();
   return cudaGetLastError();
 }

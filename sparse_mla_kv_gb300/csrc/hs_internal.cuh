@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "hs.h"
 
 namespace hs {
@@ -104,6 +106,29 @@ cudaError_t launch_offload(const LayerPtrs& ptrs, const PoolGeom& g, const int32
 cudaError_t launch_fill_i32(int32_t* a, int64_t count, int32_t value, int sms, cudaStream_t s);
 
 void count_launch(int k = 1);
+
+// Programmatic dependent launch.  A kernel that follows another of this library's kernels on the
+// same stream is launched with programmatic stream serialization: its CTAs may be placed as soon as
+// the previous kernel has started (and signalled), and wait in hardware for the previous grid to
+// complete and its memory to be visible before reading anything it wrote.
+__device__ __forceinline__ void pdl_allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 // Per-device launch configuration (occupancy, shared-memory limits) is computed once, at pool
 // creation, so that no later call needs a CUDA attribute query.
 void warm_gather_launch_configs();

@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
   __shared__ int s_tmp[2 * kResolveWarps];
 
   const int tid = threadIdx.x, lane = tid & 31;
+  pdl_allow_dependents();   // the following gather / miss-copy kernel may place its CTAs now
   const int unit = blockIdx.x;
   const int lr = unit / p.R, r = unit - lr * p.R;
   const int l = p.layer_begin + lr;
@@ -428,6 +429,7 @@ template <int CPR>
 __global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(const ResolveParams p, const LayerPtrs ptrs,
                                                                  int32_t row_bytes) {
   constexpr int kU = CPR ? (kMissRowsPerItem * CPR + 31) / 32 : 4;
+  pdl_wait_prerequisites();   // the resolver's miss lists must be complete and visible
   const int cpr = CPR ? CPR : (row_bytes >> 4);
   const int units = p.nl * p.R;
   const int items_per_unit = (p.max_m + kMissRowsPerItem - 1) / kMissRowsPerItem;
@@ -576,10 +578,9 @@ cudaError_t launch_miss_copy(const ResolveParams& p, const LayerPtrs& ptrs, int3
   const int64_t cap = (int64_t)sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  if (row_bytes == 656)
-    miss_copy_kernel<41><<<(unsigned)blocks, kCopyThreads, 0, s>>>(p, ptrs, row_bytes);
-  else
-    miss_copy_kernel<0><<<(unsigned)blocks, kCopyThreads, 0, s>>>(p, ptrs, row_bytes);
+  cudaError_t e = launch_dependent(row_bytes == 656 ? miss_copy_kernel<41> : miss_copy_kernel<0>,
+                                   dim3((unsigned)blocks), dim3(kCopyThreads), 0, s, p, ptrs, row_bytes);
+  if (e != cudaSuccess) return e;
   count_launch();
   return cudaGetLastError();
 }
