@@ -12,7 +12,7 @@
 //                      layer; the grid is exactly one resident wave, and each thread keeps
 //                      kGatherUnroll loads in flight.
 // gather_fused_kernel  the same gather for the rows a resolve plan left in the pool (resident and
-//                      hit rows), run by 6 of every 8 warps, while the other 2 warps of each CTA copy
+//                      hit rows), run by 7 of every 8 warps, while the other warp of each CTA copies
 //                      the plan's misses: one read of each host row over the host link, stored both
 //                      into its hot slot and into the output.  Host-link and HBM traffic overlap in
 //                      one launch, and HBM warps never wait on host latency.
@@ -26,7 +26,7 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kGatherThreads = 256;
 constexpr int kGatherUnroll = 8;
-constexpr int kMissWarps = 2;  // per CTA of the fused gather
+constexpr int kMissWarps = 1;  // per CTA of the fused gather (one is enough to keep the host link busy)
 
 template <int CPR>
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const LayerPtrs ptrs, int32_t layer_begin,
