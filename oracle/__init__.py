@@ -59,10 +59,10 @@ def load_library(path: str):
     L = ctypes.CDLL(path)
     i32, i64, p = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
     L.hso_resolve_unit.restype = i32
-    L.hso_resolve_unit.argtypes = [i32, i32, i32, i32, p, p, i32, p, p, p, i32, i32, i32, p, p, p, i32, p, p]
+    L.hso_resolve_unit.argtypes = [i32, i32, i32, i32, i32, p, p, i32, p, p, p, i32, i32, i32, p, p, p, i32, p, p]
     L.hso_resolve.restype = None
-    L.hso_resolve.argtypes = [i32, i32, i32, i32, p, p, i32, i32, i32, i32, p, p, p, p, i32, i32, p, p, p, i32,
-                              p, p, i32]
+    L.hso_resolve.argtypes = [i32, i32, i32, i32, p, p, i32, i32, i32, i32, i32, p, p, p, p, i32, i32, p, p, p,
+                              i32, p, p, i32]
     L.hso_gather.restype = i32
     L.hso_gather.argtypes = [i32, i64, p, i32, i32, p, i64, p, i32]
     L.hso_offload.restype = i32
@@ -95,22 +95,26 @@ def default_threads() -> int:
 def resolve(*, S: int, B: int, num_gpu_blocks: int, num_host_blocks: int, topk: np.ndarray, block_table,
             host_block_table, ctx_len, max_pages: int, C: int, hot_blocks, slot_token: np.ndarray,
             slot_stamp: np.ndarray, step: int, layer_begin: int = 0, pools=None, hosts=None,
-            threads: Optional[int] = None):
-    """Resolve all units of topk [nl][R][P][K] at `step`.
+            threads: Optional[int] = None, layers_per_index: int = 1):
+    """Resolve all units of topk [ng][R][P][K] at `step`: ng index groups of G = layers_per_index
+    consecutive layers from layer `layer_begin` (a multiple of G; G = 1: one group per layer).
 
-    slot_token/slot_stamp int32 [num_layers][R][C] are updated in place; pools/hosts (per-layer
-    uint8 arrays [blocks*S*B]) get the miss copies when given.  Returns (out_rows, out_stats)."""
+    slot_token/slot_stamp int32 [num_layers/G][R][C] are updated in place; pools/hosts (per-layer
+    uint8 arrays [blocks*S*B], all layers) get the miss copies when given.  Returns (out_rows,
+    out_stats)."""
+    G = max(1, int(layers_per_index))
+    assert layer_begin % G == 0
     topk = _c32(topk)
-    nl, R = topk.shape[0], topk.shape[1]
+    nl, R = topk.shape[0] * G, topk.shape[1]
     n = int(np.prod(topk.shape[2:]))
     assert slot_token.dtype == np.int32 and slot_token.flags.c_contiguous
     assert slot_stamp.dtype == np.int32 and slot_stamp.flags.c_contiguous
     bt, hbt, cl, hb = _c32(block_table), _c32(host_block_table), _c32(ctx_len), _c32(hot_blocks)
     out_rows = np.empty(topk.shape, np.int32)
-    out_stats = np.empty((nl, R, 4), np.int32)
+    out_stats = np.empty((nl // G, R, 4), np.int32)
     pp, _k1 = _ptr_array(pools)
     hp, _k2 = _ptr_array(hosts)
-    lib().hso_resolve(S, B, num_gpu_blocks, num_host_blocks, pp, hp, layer_begin, nl, R, n, _ptr(topk), _ptr(bt),
+    lib().hso_resolve(S, B, num_gpu_blocks, num_host_blocks, pp, hp, G, layer_begin, nl, R, n, _ptr(topk), _ptr(bt),
                       _ptr(hbt), _ptr(cl), max_pages, C, _ptr(hb), _ptr(slot_token), _ptr(slot_stamp), step,
                       _ptr(out_rows), _ptr(out_stats), threads or default_threads())
     return out_rows, out_stats

@@ -13,10 +13,14 @@ OK, ID_RANGE, MISSING_ROW, CAPACITY, STEP_ORDER, TABLE_RANGE = 0, 2, 3, 4, 5, 8
 
 
 def resolve_unit(*, S, num_gpu_blocks, num_host_blocks, ids, bt, hbt, ctx_len, max_pages, C, hot_blocks_r,
-                 slots, step, pool=None, host=None):
+                 slots, step, pool=None, host=None, group_pools=None, group_hosts=None):
     """ids: flat list (positions then top-K); bt/hbt: lists over pages; slots: list of C [token, stamp]
-    (mutated on success); pool/host: dict row -> bytes (pool mutated on success).
+    (mutated on success); pool/host: dict row -> bytes (pool mutated on success).  Under IndexShare
+    (several layers read one indexer's top-K and share these slots) group_pools/group_hosts list one
+    such dict per layer of the group, and every miss is copied in each of them.
     Returns (rows list, [status, resident, hits, misses])."""
+    if pool is not None:
+        group_pools, group_hosts = [pool], [host]
     errors = set()
     if any(st > step for _, st in slots):
         errors.add(STEP_ORDER)
@@ -88,8 +92,8 @@ def resolve_unit(*, S, num_gpu_blocks, num_host_blocks, ids, bt, hbt, ctx_len, m
         slots[best][0] = x
         slots[best][1] = step
         row_of[x] = slot_row(best)
-        if pool is not None:
-            pool[row_of[x]] = host[kind[x][1]]
+        for lp, lh in zip(group_pools or [], group_hosts or []):
+            lp[row_of[x]] = lh[kind[x][1]]
     rows = [row_of[x] if x >= 0 else -1 for x in ids]
     counts = [sum(1 for x in plan if kind[x][0] == k) for k in ("res", "hit", "miss")]
     return rows, [OK] + counts

@@ -17,11 +17,16 @@
  *     all sparse-MLA layers are copied in a single launch after the forward pass.
  *   - "vLLM の他の部分との統合" (Integration): speculative decoding works through a per-step
  *     replayable resolver plan that shares the request's hot state.
+ *   - "必要な時にスパーシティを活用する" (Using sparsity when it is needed): under GLM 5.3's IndexShare
+ *     one indexer layer serves four sparse-MLA layers, so those layers select the same top-K.  Read
+ *     here as: an index group of G consecutive layers has one top-K list and one LRU state per
+ *     request; its decisions are made once, and each miss copies the token's row of every layer of
+ *     the group (G = 1 is the plain per-layer case).
  * The LRU details the pages leave open are fixed as: hits are refreshed before victims are chosen;
  * victims are the smallest (last-used step, slot) among slots not used in this step; misses take
  * them in plan order (first occurrence, position-major then top-K order).
  *
- * Each unit (layer, request) is processed by hso_resolve_unit, one plain pass per step of the
+ * Each unit (index group, request) is processed by hso_resolve_unit, one plain pass per step of the
  * method; library qsort is the only primitive.  Units are independent, so hso_resolve runs them on
  * an OpenMP loop (the order of independent units does not change any result).
  */
@@ -67,12 +72,12 @@ static int64_t hot_row(const int32_t* hot_blocks_r, int32_t S, int32_t slot) {
 
 /*
  * One unit.  ids: [n] (n = P*K, position-major).  bt/hbt: this request's rows of the tables.
- * tok/stamp: this unit's C slots (updated in place unless an error is found).  pool/host: this
- * layer's byte arrays, or NULL to skip byte work.  out_rows: [n]; out_stats: [4].
- * Returns the status (also written to out_stats[0]).
+ * tok/stamp: this unit's C slots (updated in place unless an error is found).  pools/hosts: the
+ * byte arrays of the G layers of this unit's index group, or NULL to skip byte work.
+ * out_rows: [n]; out_stats: [4].  Returns the status (also written to out_stats[0]).
  */
-int32_t hso_resolve_unit(int32_t S, int32_t B, int32_t num_gpu_blocks, int32_t num_host_blocks,
-                         uint8_t* pool, const uint8_t* host, int32_t n, const int32_t* ids,
+int32_t hso_resolve_unit(int32_t S, int32_t B, int32_t num_gpu_blocks, int32_t num_host_blocks, int32_t G,
+                         uint8_t* const* pools, uint8_t* const* hosts, int32_t n, const int32_t* ids,
                          const int32_t* bt, const int32_t* hbt, int32_t ctx_len, int32_t max_pages,
                          int32_t C, const int32_t* hot_blocks_r, int32_t* tok, int32_t* stamp,
                          int32_t step, int32_t* out_rows, int32_t* out_stats) {
@@ -182,8 +187,13 @@ int32_t hso_resolve_unit(int32_t S, int32_t B, int32_t num_gpu_blocks, int32_t n
       tok[v] = ids[i];
       stamp[v] = step;
       row[i] = hot_row(hot_blocks_r, S, v);
-      if (pool && host)
-        memcpy(pool + row[i] * (int64_t)B, host + src[i] * (int64_t)B, (size_t)B);
+      if (pools && hosts) {
+        for (int32_t g = 0; g < G; g++) {  /* the same row of every layer of the index group */
+          uint8_t* pool = pools[g];
+          const uint8_t* host = hosts[g];
+          memcpy(pool + row[i] * (int64_t)B, host + src[i] * (int64_t)B, (size_t)B);
+        }
+      }
     }
     /* Step 7: emit a row for every position (duplicates share their first occurrence's row). */
     for (i = 0; i < n; i++)
@@ -197,27 +207,28 @@ int32_t hso_resolve_unit(int32_t S, int32_t B, int32_t num_gpu_blocks, int32_t n
 }
 
 /*
- * All units of one call: layers [layer_begin, layer_begin+nl) x R requests.
- * topk/out_rows: [nl][R][n]; out_stats: [nl][R][4]; tok/stamp: [num_layers][R][C];
+ * All units of one call: layers [layer_begin, layer_begin+nl) x R requests, in index groups of G
+ * consecutive layers (layer_begin and nl multiples of G).  With ng = nl/G:
+ * topk/out_rows: [ng][R][n]; out_stats: [ng][R][4]; tok/stamp: [num_layers/G][R][C];
  * bt/hbt: [R][max_pages]; hot_blocks: [R][C/S]; pools/hosts: [num_layers] byte arrays or NULL.
  */
 void hso_resolve(int32_t S, int32_t B, int32_t num_gpu_blocks, int32_t num_host_blocks,
-                 uint8_t** pools, uint8_t** hosts, int32_t layer_begin, int32_t nl, int32_t R,
+                 uint8_t** pools, uint8_t** hosts, int32_t G, int32_t layer_begin, int32_t nl, int32_t R,
                  int32_t n, const int32_t* topk, const int32_t* bt, const int32_t* hbt,
                  const int32_t* ctx_len, int32_t max_pages, int32_t C, const int32_t* hot_blocks,
                  int32_t* tok, int32_t* stamp, int32_t step, int32_t* out_rows, int32_t* out_stats,
                  int32_t threads) {
   int64_t u;
-  int64_t units = (int64_t)nl * R;
+  int64_t units = (int64_t)(nl / G) * R;
 #pragma omp parallel for schedule(dynamic, 1) num_threads(threads > 0 ? threads : 1)
   for (u = 0; u < units; u++) {
-    int32_t lr = (int32_t)(u / R), r = (int32_t)(u % R);
-    int32_t l = layer_begin + lr;
-    hso_resolve_unit(S, B, num_gpu_blocks, num_host_blocks, pools ? pools[l] : NULL,
-                     hosts ? hosts[l] : NULL, n, topk + u * n, bt + (int64_t)r * max_pages,
+    int32_t gr = (int32_t)(u / R), r = (int32_t)(u % R);
+    int32_t grp = layer_begin / G + gr;   /* index group; its layers are grp*G .. grp*G + G-1 */
+    hso_resolve_unit(S, B, num_gpu_blocks, num_host_blocks, G, pools ? pools + (int64_t)grp * G : NULL,
+                     hosts ? hosts + (int64_t)grp * G : NULL, n, topk + u * n, bt + (int64_t)r * max_pages,
                      hbt + (int64_t)r * max_pages, ctx_len[r], max_pages, C,
-                     hot_blocks + (int64_t)r * (C / S), tok + ((int64_t)l * R + r) * C,
-                     stamp + ((int64_t)l * R + r) * C, step, out_rows + u * n, out_stats + u * 4);
+                     hot_blocks + (int64_t)r * (C / S), tok + ((int64_t)grp * R + r) * C,
+                     stamp + ((int64_t)grp * R + r) * C, step, out_rows + u * n, out_stats + u * 4);
   }
 }
 

@@ -100,3 +100,58 @@ def test_bruteforce_agrees_with_oracle():
                 assert got[row * B:(row + 1) * B].tobytes() == pool[row], f"case {ci} pool row {row}"
     # the random mix reaches success and every data-error class
     assert {0, 2, 3, 5}.issubset(statuses), statuses
+
+
+def test_bruteforce_agrees_with_oracle_index_share():
+    """IndexShare: G consecutive layers read one top-K list and share one hot state per request; the
+    brute force keeps one slot list per (group, request) and copies every miss into each layer."""
+    import oracle
+
+    rng = np.random.default_rng(20240601)
+    for ci in range(max(1, N_CASES // 10)):
+        case0, P, K = _random_case(rng)
+        G = int(rng.choice([2, 4]))
+        ng_total = int(rng.integers(1, 3))
+        L = G * ng_total
+        case = Case(R=case0.R, S=case0.S, B=case0.B, C=case0.C, max_pages=case0.max_pages, ctx=case0.ctx,
+                    resident=True, host=True, hot_blocks=case0.hot_blocks, num_gpu_blocks=case0.ngb,
+                    num_host_blocks=case0.nhb, bt=case0.bt, hbt=case0.hbt, L=L, seed=case0.seed)
+        case.tok = np.full((ng_total, case.R, case.C), -1, np.int32)
+        case.stamp = np.full((ng_total, case.R, case.C), -1, np.int32)
+        B, S = case.B, case.S
+        g0 = int(rng.integers(0, ng_total))            # first group of the calls
+        ng = int(rng.integers(1, ng_total - g0 + 1))
+        slots = [[[[-1, -1] for _ in range(case.C)] for _ in range(case.R)] for _ in range(ng_total)]
+        pools = [{row: case.pools[l][row * B:(row + 1) * B].tobytes() for row in range(case.ngb * S)}
+                 for l in range(L)]
+        hosts = [{row: case.hosts[l][row * B:(row + 1) * B].tobytes() for row in range(case.nhb * S)}
+                 for l in range(L)]
+        t = 0
+        for si in range(int(rng.integers(1, 8))):
+            t += int(rng.integers(0, 3))
+            ids = np.stack([_ids(rng, case, P, K) for _ in range(ng)])
+            rows, stats = oracle.resolve(S=S, B=B, num_gpu_blocks=case.ngb, num_host_blocks=case.nhb, topk=ids,
+                                         block_table=case.bt, host_block_table=case.hbt, ctx_len=case.ctx,
+                                         max_pages=case.max_pages, C=case.C, hot_blocks=case.hot_blocks,
+                                         slot_token=case.tok, slot_stamp=case.stamp, step=t, layer_begin=g0 * G,
+                                         pools=case.pools, hosts=case.hosts, threads=2, layers_per_index=G)
+            for gi in range(ng):
+                grp = g0 + gi
+                for r in range(case.R):
+                    b_rows, b_stats = bruteforce.resolve_unit(
+                        S=S, num_gpu_blocks=case.ngb, num_host_blocks=case.nhb, ids=ids[gi, r].reshape(-1).tolist(),
+                        bt=case.bt[r].tolist(), hbt=case.hbt[r].tolist(), ctx_len=int(case.ctx[r]),
+                        max_pages=case.max_pages, C=case.C, hot_blocks_r=case.hot_blocks[r].tolist(),
+                        slots=slots[grp][r], step=t, group_pools=pools[grp * G:(grp + 1) * G],
+                        group_hosts=hosts[grp * G:(grp + 1) * G])
+                    msg = f"case {ci} step {si} group {grp} request {r}"
+                    assert rows[gi, r].reshape(-1).tolist() == b_rows, msg
+                    assert stats[gi, r].tolist() == b_stats, msg
+            for grp in range(ng_total):
+                for r in range(case.R):
+                    assert case.tok[grp, r].tolist() == [s[0] for s in slots[grp][r]], f"case {ci} tokens"
+                    assert case.stamp[grp, r].tolist() == [s[1] for s in slots[grp][r]], f"case {ci} stamps"
+            for l in range(L):
+                got = case.pools[l]
+                for row in range(case.ngb * S):
+                    assert got[row * B:(row + 1) * B].tobytes() == pools[l][row], f"case {ci} layer {l} row {row}"

@@ -32,6 +32,8 @@ MUTANTS = [
     ("gather_wrong_stride", r"pools\[layer_begin \+ l\] \+ \(int64_t\)r \* B", "pools[layer_begin + l] + (int64_t)r * (B - 16)"),
     ("offload_one_layer", r"for \(int32_t l = 0; l < num_layers; l\+\+\)", "for (int32_t l = 0; l < 1; l++)"),
     ("stats_hits_misses_swapped", r"out_stats\[2\] = nhit; out_stats\[3\] = nmiss;", "out_stats[2] = nmiss; out_stats[3] = nhit;"),
+    ("index_share_copies_one_layer", r"for \(int32_t g = 0; g < G; g\+\+\)", "for (int32_t g = 0; g < 1; g++)"),
+    ("index_share_group_offset_dropped", r"int32_t grp = layer_begin / G \+ gr;", "int32_t grp = gr;"),
 ]
 
 PIN_FUNCS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]

@@ -338,3 +338,61 @@ def test_gather_zero_rows_and_range():
     assert (out[0, 0] == pools[0][7 * B:8 * B]).all() and (out[0, 1] == 0).all()
     out, st = oracle.gather(B=B, num_rows=ngb * S, pools=pools, rows=np.array([[8, -3]], np.int32))
     assert st == 2 and (out == 0).all()
+
+
+@pytest.mark.parametrize("G,layer_begin,nl", [(4, 4, 4), (2, 2, 4), (4, 0, 8)])
+def test_index_share_equals_layers_given_the_same_topk(G, layer_begin, nl):
+    """IndexShare (one indexer per group of G layers): a group resolved once with one shared state
+    must give what G independent layers give when each is handed the group's top-K -- the same rows
+    and stats for every layer, per-layer states equal to the group's, and every layer's pool holding
+    its own copy of each miss row.  Layers outside [layer_begin, layer_begin + nl) stay untouched."""
+    L, R, S, B, C, K, pages = 8, 3, 4, 16, 8, 4, 12
+    rng = np.random.default_rng(100 + G + layer_begin)
+    nb = C // S
+    hot = np.arange(R * nb, dtype=np.int32).reshape(R, nb)
+    res = rng.random((R, pages)) < 0.3
+    res[:, -1] = True
+    bt = np.full((R, pages), -1, np.int32)
+    bt[res] = R * nb + np.arange(int(res.sum()), dtype=np.int32)
+    hbt = np.arange(R * pages, dtype=np.int32).reshape(R, pages)
+    geo = dict(R=R, S=S, B=B, C=C, max_pages=pages, ctx=[pages * S] * R, resident=True, host=True, hot_blocks=hot,
+               num_gpu_blocks=R * nb + int(res.sum()), num_host_blocks=R * pages, bt=bt, hbt=hbt, L=L, seed=5)
+    per_layer, shared = Case(**geo), Case(**geo)
+    shared.tok = np.full((L // G, R, C), -1, np.int32)
+    shared.stamp = np.full((L // G, R, C), -1, np.int32)
+    untouched = [p.copy() for p in per_layer.pools]
+    kw = dict(S=S, B=B, num_gpu_blocks=geo["num_gpu_blocks"], num_host_blocks=R * pages, block_table=bt,
+              host_block_table=hbt, ctx_len=per_layer.ctx, max_pages=pages, C=C, hot_blocks=hot,
+              layer_begin=layer_begin, threads=2)
+    misses = 0
+    for t in range(10):
+        ids = rng.integers(-1, pages * S, size=(nl // G, R, 1, K)).astype(np.int32)
+        if t == 6:
+            ids[0, 1, 0, 0] = pages * S           # one failing unit: ID_RANGE, no mutation there
+        s_rows, s_stats = oracle.resolve(topk=ids, slot_token=shared.tok, slot_stamp=shared.stamp, step=t,
+                                         pools=shared.pools, hosts=shared.hosts, layers_per_index=G, **kw)
+        p_rows, p_stats = oracle.resolve(topk=np.repeat(ids, G, axis=0), slot_token=per_layer.tok,
+                                         slot_stamp=per_layer.stamp, step=t, pools=per_layer.pools,
+                                         hosts=per_layer.hosts, **kw)
+        assert np.array_equal(p_rows, np.repeat(s_rows, G, axis=0)), t
+        assert np.array_equal(p_stats, np.repeat(s_stats, G, axis=0)), t
+        if t == 6:
+            assert s_stats[0, 1, 0] == 2
+        misses += int(s_stats[..., 3].sum())
+        for l in range(L):
+            assert np.array_equal(per_layer.tok[l], shared.tok[l // G]), (t, l)
+            assert np.array_equal(per_layer.stamp[l], shared.stamp[l // G]), (t, l)
+            assert np.array_equal(per_layer.pools[l], shared.pools[l]), (t, l)
+    assert misses > 0
+    for l in list(range(layer_begin)) + list(range(layer_begin + nl, L)):
+        assert np.array_equal(shared.pools[l], untouched[l]), l
+        assert (shared.tok[l // G] == -1).all()
+    # every filled slot of every layer of a called group holds its token's closed-form bytes
+    for l in range(layer_begin, layer_begin + nl):
+        for r in range(R):
+            for v in range(C):
+                tok = int(shared.tok[l // G, r, v])
+                if tok >= 0:
+                    row = shared.hot_row(r, v)
+                    assert np.array_equal(shared.pools[l][row * B:(row + 1) * B],
+                                          shared.expected_row_bytes(l, r, tok)), (l, r, v)
