@@ -89,17 +89,28 @@ typedef struct {
 
 /* Per-request LRU hot buffers.  The blocks are ordinary pool blocks leased by the caller and are
  * shared by all layers (each layer's copy lives in that layer's tensor); the token/stamp state is
- * per (layer, request) because each layer has its own top-K.  Slot v of request r is pool row
- * hot_blocks[r][v / page_size] * page_size + v % page_size. */
+ * per (index group, request): an index group is the set of consecutive layers that read one top-K
+ * list.  Slot v of request r is pool row hot_blocks[r][v / page_size] * page_size + v % page_size.
+ *
+ * layers_per_index (G) selects the grouping:
+ *   0 or 1  every layer has its own top-K list and its own state (G = 1);
+ *   G > 1   IndexShare: one indexer serves G consecutive sparse-MLA layers (Japanese article
+ *           (news.ainew.jp), section "必要な時にスパーシティを活用する" (Using sparsity when it is
+ *           needed): GLM 5.3 places one indexer layer per four sparse-MLA layers).  The layers of
+ *           a group see the same ids, tables and step, so their LRU decisions are identical: the
+ *           resolver runs once per (group, request), and each miss copies the token's row of every
+ *           layer of the group into that layer's tensor (same slot, same pool row).
+ * num_layers must be a multiple of G; groups are layers [g*G, (g+1)*G). */
 typedef struct {
-  int32_t capacity;          /* C rows per (layer, request): a multiple of page_size,
+  int32_t capacity;          /* C rows per (group, request): a multiple of page_size,
                                 page_size..HS_MAX_CAPACITY; the pages' default is 2*K            */
   const int32_t* hot_blocks; /* device int32 [R][capacity/page_size]; every entry must be a pool
                                 block in [0, num_gpu_blocks), disjoint across requests and from
                                 every resident block (not checked for overlap)                   */
-  int32_t* slot_token;       /* device int32 [num_layers][R][capacity]; -1 = empty slot          */
-  int32_t* slot_stamp;       /* device int32 [num_layers][R][capacity]; last step that used the
+  int32_t* slot_token;       /* device int32 [num_layers/G][R][capacity]; -1 = empty slot        */
+  int32_t* slot_stamp;       /* device int32 [num_layers/G][R][capacity]; last step that used the
                                 slot, -1 = never                                                  */
+  int32_t layers_per_index;  /* G, 0..HS_MAX_LAYERS (0 reads as 1)                                */
 } hs_hot_state;
 
 /* Validates the geometry and the pointers (device pointers must be device memory, host pointers
@@ -108,12 +119,14 @@ typedef struct {
 hs_status hs_pool_create(const hs_pool_desc* desc, hs_pool** out);
 void hs_pool_destroy(hs_pool* pool);
 
-/* Sets slot_token and slot_stamp of all num_layers x R x capacity slots to -1 (async). */
+/* Sets slot_token and slot_stamp of all (num_layers/G) x R x capacity slots to -1 (async). */
 hs_status hs_hot_reset(const hs_pool* pool, const hs_hot_state* hot, int32_t R, hs_stream_t stream);
 
 /* Bytes of caller-owned device workspace that hs_resolve_topk and hs_resolve_gather need for this
  * shape (per-unit miss lists handed from the resolver kernel to the miss-copy kernel, or per-position
- * host sources handed to the fused gather).  0 on a bad shape. */
+ * host sources handed to the fused gather).  nl counts resolver units per request: layers when
+ * G = 1, index groups (layers / G) under IndexShare; passing the layer count there over-sizes the
+ * workspace, which is harmless.  0 on a bad shape. */
 size_t hs_resolve_workspace_bytes(int32_t nl, int32_t R, int32_t P, int32_t K, int32_t capacity);
 
 /* Dynamic shared memory one resolver CTA needs for this shape, or 0 if the shape exceeds a limit.
@@ -121,39 +134,43 @@ size_t hs_resolve_workspace_bytes(int32_t nl, int32_t R, int32_t P, int32_t K, i
 size_t hs_resolve_smem_bytes(int32_t P, int32_t K, int32_t capacity, int32_t page_size);
 
 /* The fused top-K resolver for layers [layer_begin, layer_begin + nl) and R requests at decode
- * step `step`.  One (layer, request) pair is one independent unit:
- *   plan      the distinct non-padding ids of topk_ids[l][r][0..P)[0..K) in first-occurrence order
+ * step `step`.  One (index group, request) pair is one independent unit (with G = 1 a group is one
+ * layer); g below indexes the call's groups, g < nl/G:
+ *   plan      the distinct non-padding ids of topk_ids[g][r][0..P)[0..K) in first-occurrence order
  *             (position-major, then top-K order); all P query positions of a step share it;
  *   resident  block_table[r][id/page_size] >= 0: row = that block * page_size + id % page_size,
  *             read in place (wins over a stale hot copy);
  *   hit       the id sits in a hot slot: row = the slot's pool row; its stamp becomes `step`;
  *   miss      otherwise: the j-th miss in plan order takes the j-th smallest (stamp, slot) among
- *             slots whose stamp is < step and that were not hit in this call; exactly one row is
- *             copied from the pinned host pool (host_block_table[r][id/page_size]) into the slot,
- *             whose token becomes id and stamp `step`.
+ *             slots whose stamp is < step and that were not hit in this call; exactly one row per
+ *             layer of the group is copied from the pinned host pool
+ *             (host_block_table[r][id/page_size]) into the slot, whose token becomes id and stamp
+ *             `step`.
+ * layer_begin and nl must be multiples of G = hot->layers_per_index.
  * Arguments (all device pointers):
- *   topk_ids         int32 [nl][R][P][K]; -1 = padding (row -1).
+ *   topk_ids         int32 [nl/G][R][P][K]; -1 = padding (row -1).
  *   block_table      int32 [R][max_pages]; < 0 = placeholder page (not resident).
  *   host_block_table int32 [R][max_pages]; < 0 = no host copy.
  *   ctx_len          int32 [R]; ids must be < ctx_len[r].
- *   out_rows         int32 [nl][R][P][K]; pool row per id (duplicates share the row; padding -1).
- *   out_stats        int32 [nl][R][4] = {status, resident, hits, misses}, counted over the plan.
+ *   out_rows         int32 [nl/G][R][P][K]; pool row per id (duplicates share the row; padding -1);
+ *                    the same row id serves every layer of the group.
+ *   out_stats        int32 [nl/G][R][4] = {status, resident, hits, misses}, counted over the plan.
  *   workspace        device scratch of >= hs_resolve_workspace_bytes(...) bytes, 16-byte aligned;
  *                    its contents need no initialisation and are garbage after the call.
  * A unit with a data error leaves its hot state and pool bytes unchanged, sets out_rows to -1 and
  * out_stats to {code, 0, 0, 0}; other units proceed.  Calling again with the same ids and step
  * returns the same rows with 0 misses (the replayable plan used by speculative decoding).
- * Launches two kernels on `stream` (resolve, then the miss copy).  Concurrent calls that share hot
- * state or workspace must be ordered by the caller. */
+ * Launches two kernels on `stream` (resolve, then the miss copy of every layer).  Concurrent calls
+ * that share hot state or workspace must be ordered by the caller. */
 hs_status hs_resolve_topk(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P,
                           int32_t K, const int32_t* topk_ids, const int32_t* block_table,
                           const int32_t* host_block_table, const int32_t* ctx_len, int32_t max_pages,
                           const hs_hot_state* hot, int32_t step, int32_t* out_rows, int32_t* out_stats,
                           void* workspace, size_t workspace_bytes, hs_stream_t stream);
 
-/* Resolve and gather in one call: the same results as hs_resolve_topk followed by
- * hs_gather_rows(out_rows) over all nl*R*P*K positions -- out_rows, out_stats, hot state and pool bytes
- * identical, and out[l][(r*P + p)*K + k] = the row of topk_ids[l][r][p][k].  The miss copy is fused
+/* Resolve and gather in one call: the same results as hs_resolve_topk followed by a gather of
+ * out_rows for every layer -- out_rows, out_stats, hot state and pool bytes identical, and
+ * out[l][(r*P + p)*K + k] = layer layer_begin + l's row of topk_ids[l/G][r][p][k], for l < nl.  The miss copy is fused
  * into the gather: the resolver marks each miss position with its host row, and the gather reads
  * those rows straight from the pinned host pool (storing the first occurrence of each into its hot
  * slot) while resident and hit rows come from HBM in the same launch, so host-link and HBM traffic
@@ -180,10 +197,11 @@ hs_status hs_resolve_plan(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
 
 /* Second half of hs_resolve_gather (one launch): gathers all nl*R*P*K rows named by out_rows into
  * `out`, taking miss rows from the pinned host pool as recorded by hs_resolve_plan in `workspace`
- * and filling their hot slots.  nl, R, P, K, capacity, layer_begin, out_rows and workspace must be
- * those of the preceding hs_resolve_plan call. */
+ * and filling their hot slots in every layer.  nl, R, P, K, layer_begin, hot (only its capacity and
+ * layers_per_index are read), out_rows and workspace must be those of the preceding hs_resolve_plan
+ * call. */
 hs_status hs_gather_planned(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P,
-                            int32_t K, int32_t capacity, const int32_t* out_rows, const void* workspace,
+                            int32_t K, const hs_hot_state* hot, const int32_t* out_rows, const void* workspace,
                             size_t workspace_bytes, void* out, hs_stream_t stream);
 
 /* Single-stride gather: out[l][i] = row rows[l][i] of layer layer_begin + l, for l < nl, i < n.

@@ -43,7 +43,7 @@ class PoolDesc(ctypes.Structure):
 
 class HotStateC(ctypes.Structure):
     _fields_ = [("capacity", ctypes.c_int32), ("hot_blocks", ctypes.c_void_p), ("slot_token", ctypes.c_void_p),
-                ("slot_stamp", ctypes.c_void_p)]
+                ("slot_stamp", ctypes.c_void_p), ("layers_per_index", ctypes.c_int32)]
 
 
 _lib = None
@@ -81,7 +81,7 @@ def lib():
         L.hs_resolve_plan.restype = i32
         L.hs_resolve_plan.argtypes = L.hs_resolve_topk.argtypes
         L.hs_gather_planned.restype = i32
-        L.hs_gather_planned.argtypes = [p, i32, i32, i32, i32, i32, i32, p, p, sz, p, p]
+        L.hs_gather_planned.argtypes = [p, i32, i32, i32, i32, i32, ctypes.POINTER(HotStateC), p, p, sz, p, p]
         L.hs_gather_rows.restype = i32
         L.hs_gather_rows.argtypes = [p, i32, i32, p, i64, p, p, p]
         L.hs_offload_pages.restype = i32
@@ -176,21 +176,29 @@ class Pool:
 
 class HotState:
     """Per-request hot buffers: leased block ids [R][C/page_size] (shared by all layers) and the
-    per-(layer, request) slot token/stamp arrays [num_layers][R][C] (-1 = empty / never used)."""
+    per-(index group, request) slot token/stamp arrays [num_layers/G][R][C] (-1 = empty / never used).
+    G = layers_per_index: 1 when every layer has its own top-K; G > 1 under IndexShare, where G
+    consecutive layers read one indexer's top-K and share one state."""
 
-    def __init__(self, capacity: int, hot_blocks: torch.Tensor, slot_token: torch.Tensor, slot_stamp: torch.Tensor):
+    def __init__(self, capacity: int, hot_blocks: torch.Tensor, slot_token: torch.Tensor, slot_stamp: torch.Tensor,
+                 layers_per_index: int = 1):
         self.capacity = int(capacity)
+        self.G = max(1, int(layers_per_index))
         self.hot_blocks, self.slot_token, self.slot_stamp = hot_blocks, slot_token, slot_stamp
         self.c = HotStateC(self.capacity, _dev_i32(hot_blocks, "hot_blocks"), _dev_i32(slot_token, "slot_token"),
-                           _dev_i32(slot_stamp, "slot_stamp"))
+                           _dev_i32(slot_stamp, "slot_stamp"), self.G)
 
     @classmethod
-    def allocate(cls, num_layers: int, hot_blocks: torch.Tensor, capacity: int) -> "HotState":
+    def allocate(cls, num_layers: int, hot_blocks: torch.Tensor, capacity: int,
+                 layers_per_index: int = 1) -> "HotState":
+        G = max(1, int(layers_per_index))
+        if num_layers % G:
+            raise ValueError("num_layers must be a multiple of layers_per_index")
         R = int(hot_blocks.shape[0])
         dev = hot_blocks.device
-        tok = torch.empty((num_layers, R, capacity), dtype=torch.int32, device=dev)
-        st = torch.empty((num_layers, R, capacity), dtype=torch.int32, device=dev)
-        return cls(capacity, hot_blocks, tok, st)
+        tok = torch.empty((num_layers // G, R, capacity), dtype=torch.int32, device=dev)
+        st = torch.empty((num_layers // G, R, capacity), dtype=torch.int32, device=dev)
+        return cls(capacity, hot_blocks, tok, st, G)
 
     @property
     def R(self) -> int:
@@ -218,10 +226,12 @@ def resolve_topk(pool: Pool, topk: torch.Tensor, block_table: torch.Tensor, host
                  ctx_len: torch.Tensor, hot: HotState, step: int, *, layer_begin: int = 0,
                  out_rows: Optional[torch.Tensor] = None, out_stats: Optional[torch.Tensor] = None,
                  workspace: Optional[torch.Tensor] = None, stream=None):
-    """topk int32 [nl][R][P][K] -> (out_rows int32 [nl][R][P][K], out_stats int32 [nl][R][4])."""
+    """topk int32 [ng][R][P][K] -> (out_rows int32 [ng][R][P][K], out_stats int32 [ng][R][4]), for the
+    ng index groups of G = hot.G layers starting at layer_begin (ng = layers when G = 1)."""
     if topk.dim() != 4:
-        raise ValueError("topk must be [nl][R][P][K]")
-    nl, R, P, K = (int(x) for x in topk.shape)
+        raise ValueError("topk must be [ng][R][P][K]")
+    ng, R, P, K = (int(x) for x in topk.shape)
+    nl = ng * hot.G
     if block_table.dim() != 2 or block_table.shape[0] != R or tuple(host_block_table.shape) != tuple(block_table.shape):
         raise ValueError("block tables must both be [R][max_pages]")
     if hot.R != R:
@@ -230,9 +240,9 @@ def resolve_topk(pool: Pool, topk: torch.Tensor, block_table: torch.Tensor, host
     if out_rows is None:
         out_rows = torch.empty_like(topk)
     if out_stats is None:
-        out_stats = torch.empty((nl, R, 4), dtype=torch.int32, device=dev)
+        out_stats = torch.empty((ng, R, 4), dtype=torch.int32, device=dev)
     if workspace is None:
-        workspace = alloc_workspace(nl, R, P, K, hot.capacity, dev)
+        workspace = alloc_workspace(ng, R, P, K, hot.capacity, dev)
     if workspace.dtype != torch.uint8 or not workspace.is_cuda:
         raise TypeError("workspace must be a uint8 CUDA tensor")
     code = lib().hs_resolve_topk(pool.handle, layer_begin, nl, R, P, K, _dev_i32(topk, "topk"),
@@ -248,19 +258,21 @@ def resolve_gather(pool: Pool, topk: torch.Tensor, block_table: torch.Tensor, ho
                    ctx_len: torch.Tensor, hot: HotState, step: int, *, layer_begin: int = 0,
                    out_rows: Optional[torch.Tensor] = None, out_stats: Optional[torch.Tensor] = None,
                    out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None):
-    """Resolve and gather in one call (miss copies fused into the gather).
-    Returns (out_rows [nl][R][P][K], out_stats [nl][R][4], out uint8 [nl][R*P*K][row_bytes])."""
+    """Resolve and gather in one call (miss copies fused into the gather).  topk [ng][R][P][K] for ng
+    index groups of G = hot.G layers (nl = ng * G layers).
+    Returns (out_rows [ng][R][P][K], out_stats [ng][R][4], out uint8 [nl][R*P*K][row_bytes])."""
     if topk.dim() != 4:
-        raise ValueError("topk must be [nl][R][P][K]")
-    nl, R, P, K = (int(x) for x in topk.shape)
+        raise ValueError("topk must be [ng][R][P][K]")
+    ng, R, P, K = (int(x) for x in topk.shape)
+    nl = ng * hot.G
     if block_table.dim() != 2 or block_table.shape[0] != R or tuple(host_block_table.shape) != tuple(block_table.shape):
         raise ValueError("block tables must both be [R][max_pages]")
     if hot.R != R:
         raise ValueError("hot state has a different number of requests")
     dev = topk.device
     out_rows = torch.empty_like(topk) if out_rows is None else out_rows
-    out_stats = torch.empty((nl, R, 4), dtype=torch.int32, device=dev) if out_stats is None else out_stats
-    workspace = alloc_workspace(nl, R, P, K, hot.capacity, dev) if workspace is None else workspace
+    out_stats = torch.empty((ng, R, 4), dtype=torch.int32, device=dev) if out_stats is None else out_stats
+    workspace = alloc_workspace(ng, R, P, K, hot.capacity, dev) if workspace is None else workspace
     if out is None:
         out = torch.empty((nl, R * P * K, pool.row_bytes), dtype=torch.uint8, device=dev)
     if out.dtype != torch.uint8 or not out.is_cuda or not out.is_contiguous() or out.numel() != nl * R * P * K * pool.row_bytes:
@@ -313,8 +325,10 @@ class PreparedStep:
                  ctx_len: torch.Tensor, out_rows: torch.Tensor, out_stats: torch.Tensor, workspace: torch.Tensor,
                  gather_out: torch.Tensor, *, layer_begin: int = 0, gather_status: Optional[torch.Tensor] = None,
                  stream=None):
-        nl, R, P, K = (int(x) for x in out_rows.shape)
-        self.shape = (nl, R, P, K)
+        ng, R, P, K = (int(x) for x in out_rows.shape)
+        self.shape = (ng, R, P, K)
+        self.G = hot.G
+        self.nl = nl = ng * hot.G
         self.pool, self.hot = pool, hot
         self._keep = (block_table, host_block_table, ctx_len, out_rows, out_stats, workspace, gather_out, gather_status)
         self.L = lib()
@@ -340,7 +354,7 @@ class PreparedStep:
         return self._fixed_stream if self._fixed_stream is not None else _stream(None)
 
     def resolve(self, topk: torch.Tensor, step: int) -> None:
-        nl, R, P, K = self.shape
+        nl, (_, R, P, K) = self.nl, self.shape
         if tuple(topk.shape) != self.shape:
             raise ValueError("topk shape differs from the prepared shape")
         _check(self.L.hs_resolve_topk(self.pool.handle, self.lb, nl, R, P, K, _dev_i32(topk, "topk"), *self.args_bt,
@@ -348,7 +362,7 @@ class PreparedStep:
                                       self.ws, self.ws_n, self.stream), "hs_resolve_topk")
 
     def plan(self, topk: torch.Tensor, step: int) -> None:
-        nl, R, P, K = self.shape
+        nl, (_, R, P, K) = self.nl, self.shape
         if tuple(topk.shape) != self.shape:
             raise ValueError("topk shape differs from the prepared shape")
         _check(self.L.hs_resolve_plan(self.pool.handle, self.lb, nl, R, P, K, _dev_i32(topk, "topk"), *self.args_bt,
@@ -356,12 +370,12 @@ class PreparedStep:
                                       self.ws, self.ws_n, self.stream), "hs_resolve_plan")
 
     def gather_planned(self) -> None:
-        nl, R, P, K = self.shape
-        _check(self.L.hs_gather_planned(self.pool.handle, self.lb, nl, R, P, K, self.hot.capacity, self.rows, self.ws,
-                                        self.ws_n, self.gout, self.stream), "hs_gather_planned")
+        nl, (_, R, P, K) = self.nl, self.shape
+        _check(self.L.hs_gather_planned(self.pool.handle, self.lb, nl, R, P, K, ctypes.byref(self.hot.c), self.rows,
+                                        self.ws, self.ws_n, self.gout, self.stream), "hs_gather_planned")
 
     def resolve_gather(self, topk: torch.Tensor, step: int) -> None:
-        nl, R, P, K = self.shape
+        nl, (_, R, P, K) = self.nl, self.shape
         if tuple(topk.shape) != self.shape:
             raise ValueError("topk shape differs from the prepared shape")
         _check(self.L.hs_resolve_gather(self.pool.handle, self.lb, nl, R, P, K, _dev_i32(topk, "topk"), *self.args_bt,
@@ -369,8 +383,17 @@ class PreparedStep:
                                         self.gout, self.ws, self.ws_n, self.stream), "hs_resolve_gather")
 
     def gather(self) -> None:
-        _check(self.L.hs_gather_rows(self.pool.handle, self.lb, self.shape[0], self.rows, self.n_per_layer, self.gout,
-                                     self.gstatus, self.stream), "hs_gather_rows")
+        if self.G == 1:
+            _check(self.L.hs_gather_rows(self.pool.handle, self.lb, self.nl, self.rows, self.n_per_layer, self.gout,
+                                         self.gstatus, self.stream), "hs_gather_rows")
+            return
+        # IndexShare: every layer of a group gathers the group's rows (one launch per layer)
+        n, B = self.n_per_layer, self.pool.row_bytes
+        for l in range(self.nl):
+            _check(self.L.hs_gather_rows(self.pool.handle, self.lb + l, 1,
+                                         ctypes.c_void_p(self.rows.value + 4 * n * (l // self.G)), n,
+                                         ctypes.c_void_p(self.gout.value + n * B * l), self.gstatus, self.stream),
+                   "hs_gather_rows")
 
     def offload(self, gpu_blocks: torch.Tensor, host_blocks: torch.Tensor, n: int) -> None:
         if n:

@@ -15,7 +15,9 @@
 //                      hit rows), run by 7 of every 8 warps, while the other warp of each CTA copies
 //                      the plan's misses: one read of each host row over the host link, stored both
 //                      into its hot slot and into the output.  Host-link and HBM traffic overlap in
-//                      one launch, and HBM warps never wait on host latency.
+//                      one launch, and HBM warps never wait on host latency.  Under IndexShare
+//                      the G layers of an index group read the same plan (rows, sources, miss
+//                      list); each layer's CTAs copy the misses into that layer's tensor.
 #include <climits>
 
 #include "hs_internal.cuh"
@@ -68,12 +70,13 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const LayerPtrs 
 
 template <int CPR>
 __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
-    const LayerPtrs ptrs, int32_t layer_begin, int32_t R, int32_t n, int32_t max_m, const int32_t* __restrict__ rows,
-    const int32_t* __restrict__ miss_count, const int4* __restrict__ miss_list, const int32_t* __restrict__ msrc,
-    uint8_t* __restrict__ out, int32_t row_bytes, int64_t num_rows) {
+    const LayerPtrs ptrs, int32_t layer_begin, int32_t group, int32_t R, int32_t n, int32_t max_m,
+    const int32_t* __restrict__ rows, const int32_t* __restrict__ miss_count, const int4* __restrict__ miss_list,
+    const int32_t* __restrict__ msrc, uint8_t* __restrict__ out, int32_t row_bytes, int64_t num_rows) {
   pdl_wait_prerequisites();   // the resolve plan (rows, sources, miss lists) must be complete and visible
   const int cpr = CPR ? CPR : (row_bytes >> 4);
   const int lr = blockIdx.y;
+  const int pu = lr / group;  // the index group (plan) this layer reads
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* __restrict__ pool = ptrs.gpu[layer_begin + lr];
   const uint8_t* __restrict__ host = ptrs.host[layer_begin + lr];
@@ -81,8 +84,8 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
   uint8_t* __restrict__ lout = out + (int64_t)lr * per_layer * row_bytes;
 
   if (warp < kMissWarps) {
-    // ---- miss warps: items (request, group of kMissRowsPerItem misses) of this layer, numbered
-    // group-major so live items are the low numbers; lane j of miss-warp w tests item w + j * nmw.
+    // ---- miss warps: items (request, chunk of kMissRowsPerItem misses) of this layer, numbered
+    // chunk-major so live items are the low numbers; lane j of miss-warp w tests item w + j * nmw.
     constexpr int kU = CPR ? (kMissRowsPerItem * CPR + 31) / 32 : 4;
     const int64_t mw = (int64_t)blockIdx.x * kMissWarps + warp;
     const int64_t nmw = (int64_t)gridDim.x * kMissWarps;
@@ -90,25 +93,25 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
     const int64_t items = (int64_t)R * items_per_unit;
     for (int64_t base = mw; base < items; base += nmw * 32) {
       const int64_t item = base + (int64_t)lane * nmw;
-      int r = 0, group = 0, cnt = 0;
+      int r = 0, chunk = 0, cnt = 0;
       bool live = false;
       if (item < items) {
-        group = (int)(item / R);
-        r = (int)(item - (int64_t)group * R);
-        cnt = miss_count[lr * R + r];
-        live = group * kMissRowsPerItem < cnt;
+        chunk = (int)(item / R);
+        r = (int)(item - (int64_t)chunk * R);
+        cnt = miss_count[pu * R + r];
+        live = chunk * kMissRowsPerItem < cnt;
       }
       uint32_t todo = __ballot_sync(kFull, live);
       while (todo) {
         const int src_lane = __ffs(todo) - 1;
         todo &= todo - 1u;
         const int rq = __shfl_sync(kFull, r, src_lane);
-        const int g = __shfl_sync(kFull, group, src_lane);
+        const int ch = __shfl_sync(kFull, chunk, src_lane);
         const int c = __shfl_sync(kFull, cnt, src_lane);
-        const int r0 = g * kMissRowsPerItem;
+        const int r0 = ch * kMissRowsPerItem;
         const int nrows = min(kMissRowsPerItem, c - r0);
         int4 ent = make_int4(0, 0, 0, 0);
-        if (lane < nrows) ent = miss_list[((int64_t)lr * R + rq) * max_m + r0 + lane];
+        if (lane < nrows) ent = miss_list[((int64_t)pu * R + rq) * max_m + r0 + lane];
         const int total = nrows * cpr;
         for (int f0 = 0; f0 < total; f0 += 32 * kU) {
           uint4 v[kU];
@@ -146,7 +149,7 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
   // ---- HBM warps: every position the miss warps do not own (resident rows, hit rows, padding,
   // and repeated positions of a miss, which read the host row again); one source word per position
   constexpr int kHbmThreads = kGatherThreads - kMissWarps * 32;
-  const int32_t* __restrict__ lmsrc = msrc + (int64_t)lr * per_layer;
+  const int32_t* __restrict__ lmsrc = msrc + (int64_t)pu * per_layer;
   uint4* __restrict__ lout4 = reinterpret_cast<uint4*>(lout);
   const int64_t total = per_layer * cpr;
   const int64_t stride = (int64_t)gridDim.x * kHbmThreads;
@@ -221,10 +224,10 @@ cudaError_t launch_gather(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, int32_t R, int32_t n,
-                                int32_t max_m, const int32_t* rows, const int32_t* miss_count, const int4* miss_list,
-                                const int32_t* msrc, uint8_t* out, int32_t row_bytes, int64_t num_rows, int sms,
-                                cudaStream_t s) {
+cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, int32_t group, int32_t R,
+                                int32_t n, int32_t max_m, const int32_t* rows, const int32_t* miss_count,
+                                const int4* miss_list, const int32_t* msrc, uint8_t* out, int32_t row_bytes,
+                                int64_t num_rows, int sms, cudaStream_t s) {
   int* occ = g_occ_fused;
   const bool k41 = row_bytes == 656;
   auto kern = k41 ? gather_fused_kernel<41> : gather_fused_kernel<0>;
@@ -232,8 +235,8 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
   const int64_t want = (per_layer + (int64_t)kGatherThreads * kGatherUnroll - 1) /
                        ((int64_t)kGatherThreads * kGatherUnroll);
   const dim3 grid = wave_grid(sms, resident_blocks(kern, &occ[k41 ? 0 : 1]), want, nl);
-  cudaError_t e = launch_dependent(kern, grid, dim3(kGatherThreads), 0, s, ptrs, layer_begin, R, n, max_m, rows,
-                                   miss_count, miss_list, msrc, out, row_bytes, num_rows);
+  cudaError_t e = launch_dependent(kern, grid, dim3(kGatherThreads), 0, s, ptrs, layer_begin, group, R, n, max_m,
+                                   rows, miss_count, miss_list, msrc, out, row_bytes, num_rows);
   if (e != cudaSuccess) return e;
   count_launch();
   return cudaGetLastError();

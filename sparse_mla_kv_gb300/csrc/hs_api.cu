@@ -30,6 +30,13 @@ int sm_count(int dev) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Layers per index group (IndexShare) of a hot state; 0 if the value does not fit the pool.
+int32_t layers_per_index(const hs_hot_state* hot, const hs::PoolGeom& g) {
+  const int32_t G = hot->layers_per_index <= 1 ? 1 : hot->layers_per_index;
+  if (hot->layers_per_index < 0 || G > HS_MAX_LAYERS || g.num_layers % G) return 0;
+  return G;
+}
+
 hs_status cuda_status(cudaError_t e) { return e == cudaSuccess ? HS_OK : HS_ERR_CUDA; }
 
 }  // namespace
@@ -120,7 +127,9 @@ hs_status hs_hot_reset(const hs_pool* pool, const hs_hot_state* hot, int32_t R, 
   if (!pool || !hot || R < 0) return HS_ERR_INVALID_ARG;
   if (hot->capacity < pool->g.page_size || hot->capacity > HS_MAX_CAPACITY || hot->capacity % pool->g.page_size)
     return HS_ERR_INVALID_ARG;
-  const int64_t count = (int64_t)pool->g.num_layers * R * hot->capacity;
+  const int32_t G = hs::layers_per_index(hot, pool->g);
+  if (G == 0) return HS_ERR_INVALID_ARG;
+  const int64_t count = (int64_t)(pool->g.num_layers / G) * R * hot->capacity;
   if (count == 0) return HS_OK;
   if (!hot->slot_token || !hot->slot_stamp) return HS_ERR_INVALID_ARG;
   const int sms = hs::sm_count(pool->device);
@@ -159,7 +168,10 @@ hs_status prepare_resolve(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
   const int64_t n = (int64_t)P * K;
   const int32_t C = hot->capacity;
   if (n > HS_MAX_PLAN || C < g.page_size || C > HS_MAX_CAPACITY || C % g.page_size) return HS_ERR_INVALID_ARG;
-  if ((int64_t)nl * R > INT32_MAX) return HS_ERR_INVALID_ARG;
+  const int32_t G = hs::layers_per_index(hot, g);
+  if (G == 0 || layer_begin % G || nl % G) return HS_ERR_INVALID_ARG;
+  const int32_t ng = nl / G;  // index groups in this call: the resolver's units are (group, request)
+  if ((int64_t)ng * R > INT32_MAX) return HS_ERR_INVALID_ARG;
   if (nl == 0 || R == 0) {
     nothing = true;
     return HS_OK;
@@ -168,7 +180,7 @@ hs_status prepare_resolve(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
       !out_stats || !workspace)
     return HS_ERR_INVALID_ARG;
   if (n > 0 && (!topk_ids || !out_rows)) return HS_ERR_INVALID_ARG;
-  if (!hs::aligned16(workspace) || workspace_bytes < hs::resolve_workspace_bytes((int64_t)nl * R, n, C))
+  if (!hs::aligned16(workspace) || workspace_bytes < hs::resolve_workspace_bytes((int64_t)ng * R, n, C))
     return HS_ERR_INVALID_ARG;
   const size_t smem_limit = hs::resolve_smem_limit(pool->device);
   sm = hs::resolve_smem_plan(n, C, g.page_size);
@@ -178,8 +190,9 @@ hs_status prepare_resolve(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
   if (sms <= 0) return HS_ERR_CUDA;
 
   p = hs::ResolveParams{};
-  p.layer_begin = layer_begin;
-  p.nl = nl;
+  p.layer_begin = layer_begin / G;
+  p.nl = ng;
+  p.group = G;
   p.R = R;
   p.n = (int32_t)n;
   p.C = C;
@@ -189,7 +202,6 @@ hs_status prepare_resolve(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
   p.num_gpu_blocks = g.num_gpu_blocks;
   p.num_host_blocks = g.num_host_blocks;
   p.id_hash_bits = sm.id_hash_bits;
-  p.slot_hash_bits = sm.slot_hash_bits;
   p.max_m = (int32_t)(n < C ? n : C);
   p.topk = topk_ids;
   p.bt = block_table;
@@ -201,7 +213,7 @@ hs_status prepare_resolve(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
   p.out_rows = out_rows;
   p.out_stats = out_stats;
   p.miss_count = static_cast<int32_t*>(workspace);
-  p.miss_list = reinterpret_cast<int4*>(static_cast<uint8_t*>(workspace) + hs::ws_counts_bytes((int64_t)nl * R));
+  p.miss_list = reinterpret_cast<int4*>(static_cast<uint8_t*>(workspace) + hs::ws_counts_bytes((int64_t)ng * R));
   p.msrc = nullptr;
   return HS_OK;
 }
@@ -242,22 +254,25 @@ hs_status hs_resolve_plan(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
                                  nothing);
   if (st != HS_OK || nothing) return st;
   p.msrc = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) +
-                                      hs::ws_msrc_offset((int64_t)nl * R, p.n, p.C));
+                                      hs::ws_msrc_offset((int64_t)p.nl * R, p.n, p.C));
   return hs::cuda_status(hs::launch_resolve(p, sm, stream));
 }
 
 hs_status hs_gather_planned(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P, int32_t K,
-                            int32_t capacity, const int32_t* out_rows, const void* workspace, size_t workspace_bytes,
-                            void* out, hs_stream_t stream) {
-  if (!pool) return HS_ERR_INVALID_ARG;
+                            const hs_hot_state* hot, const int32_t* out_rows, const void* workspace,
+                            size_t workspace_bytes, void* out, hs_stream_t stream) {
+  if (!pool || !hot) return HS_ERR_INVALID_ARG;
   const hs::PoolGeom& g = pool->g;
   if (layer_begin < 0 || nl < 0 || (int64_t)layer_begin + nl > g.num_layers || R < 0 || P < 1 || K < 0)
     return HS_ERR_INVALID_ARG;
   const int64_t n = (int64_t)P * K;
+  const int32_t capacity = hot->capacity;
+  const int32_t G = hs::layers_per_index(hot, g);
+  if (G == 0 || layer_begin % G || nl % G) return HS_ERR_INVALID_ARG;
   if (n > HS_MAX_PLAN || (int64_t)nl * R > INT32_MAX || capacity < 1 || capacity > HS_MAX_CAPACITY)
     return HS_ERR_INVALID_ARG;
   if (nl == 0 || R == 0 || n == 0) return HS_OK;
-  const int64_t units = (int64_t)nl * R;
+  const int64_t units = (int64_t)(nl / G) * R;
   if (!out_rows || !workspace || !out || !hs::aligned16(out) || !hs::aligned16(workspace) ||
       workspace_bytes < hs::resolve_workspace_bytes(units, n, capacity))
     return HS_ERR_INVALID_ARG;
@@ -266,7 +281,7 @@ hs_status hs_gather_planned(const hs_pool* pool, int32_t layer_begin, int32_t nl
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
   const int32_t max_m = (int32_t)(n < capacity ? n : capacity);
   return hs::cuda_status(hs::launch_gather_fused(
-      pool->ptrs, layer_begin, nl, R, (int32_t)n, max_m, out_rows, reinterpret_cast<const int32_t*>(ws),
+      pool->ptrs, layer_begin, nl, G, R, (int32_t)n, max_m, out_rows, reinterpret_cast<const int32_t*>(ws),
       reinterpret_cast<const int4*>(ws + hs::ws_counts_bytes(units)),
       reinterpret_cast<const int32_t*>(ws + hs::ws_msrc_offset(units, n, capacity)), static_cast<uint8_t*>(out),
       g.row_bytes, (int64_t)g.num_gpu_blocks * g.page_size, sms, stream));
@@ -281,8 +296,7 @@ hs_status hs_resolve_gather(const hs_pool* pool, int32_t layer_begin, int32_t nl
   hs_status st = hs_resolve_plan(pool, layer_begin, nl, R, P, K, topk_ids, block_table, host_block_table, ctx_len,
                                  max_pages, hot, step, out_rows, out_stats, workspace, workspace_bytes, stream);
   if (st != HS_OK) return st;
-  return hs_gather_planned(pool, layer_begin, nl, R, P, K, hot->capacity, out_rows, workspace, workspace_bytes, out,
-                           stream);
+  return hs_gather_planned(pool, layer_begin, nl, R, P, K, hot, out_rows, workspace, workspace_bytes, out, stream);
 }
 
 hs_status hs_gather_rows(const hs_pool* pool, int32_t layer_begin, int32_t nl, const int32_t* rows, int64_t n,

@@ -45,10 +45,12 @@ enum : uint32_t {
   kErrCapacity = 16u,
 };
 
+// A resolver unit is (index group, request); `group` = G layers share one top-K list and one hot
+// state.  layer_begin and nl count groups: the group's layers are [g*G, (g+1)*G).
 struct ResolveParams {
-  int32_t layer_begin, nl, R, n /* P*K */, C, S, max_pages, step;
+  int32_t layer_begin, nl, group, R, n /* P*K */, C, S, max_pages, step;
   int32_t num_gpu_blocks, num_host_blocks;
-  int32_t id_hash_bits, slot_hash_bits;
+  int32_t id_hash_bits;
   int32_t max_m;  // miss-list capacity per unit = min(n, C)
   const int32_t* topk;
   const int32_t* bt;
@@ -59,7 +61,7 @@ struct ResolveParams {
   int32_t* slot_stamp;
   int32_t* out_rows;
   int32_t* out_stats;
-  int32_t* miss_count;  // workspace [nl*R]
+  int32_t* miss_count;  // workspace [nl*R] (units)
   int4* miss_list;      // workspace [nl*R][max_m] = (host row, pool row, position r*n+i, 0)
   // Fused mode (non-null): per output position, the fused gather's source:
   //   >= 0 pool row; -1 zero row (padding / failed unit); INT_MIN the first occurrence of a miss
@@ -70,17 +72,18 @@ struct ResolveParams {
 
 struct ResolveSmem {
   // byte offsets into dynamic shared memory
-  size_t tok, stamp, ids, val, cls, idh, hot, u /* slot hash, later radix buffers */, total;
-  int32_t id_hash_bits, slot_hash_bits;
+  size_t stamp, ids, val, cls, slot, hot, idh /* id hash, later radix buffers */, total;
+  int32_t id_hash_bits;
+  int32_t id_hash_wide;  // 1: 64-bit (id, position) entries; 0: 32-bit position entries
   size_t tbl;         // staged block-table + host-table rows (when tbl_pages > 0)
   int32_t tbl_pages;
 };
 
 // Shared-memory plan of one resolver CTA for (n = P*K ids, C slots, page size S); total = 0 if out
-// of limits.
-ResolveSmem resolve_smem_plan(int64_t n, int64_t C, int64_t S);
-// The same plan plus the request's two table rows staged in shared memory when max_pages is at most
-// kMaxStagedPages and the total stays within `limit`.
+// of limits.  The narrow plan is the smallest footprint.
+ResolveSmem resolve_smem_plan(int64_t n, int64_t C, int64_t S, bool wide = false);
+// The plan to launch: the wide id table and the request's two table rows staged in shared memory
+// (when max_pages is at most kMaxStagedPages) as far as they fit within `limit`.
 constexpr int64_t kMaxStagedPages = 8192;
 ResolveSmem resolve_smem_plan_staged(int64_t n, int64_t C, int64_t S, int64_t max_pages, size_t limit);
 size_t resolve_workspace_bytes(int64_t units, int64_t n, int64_t C);
@@ -96,10 +99,12 @@ cudaError_t launch_gather(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl
                           cudaStream_t s);
 // The fused gather: rows of layers [layer_begin, layer_begin+nl), R requests x n positions each; miss
 // rows come from the pinned host pool through the resolver's miss lists (dedicated warps) and are
-// also stored into their hot slots; msrc marks positions the miss warps own.
-cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, int32_t R, int32_t n,
-                                int32_t max_m, const int32_t* rows, const int32_t* miss_count, const int4* miss_list,
-                                const int32_t* msrc, uint8_t* out, int32_t row_bytes, int64_t num_rows, int sms,
+// also stored into their hot slots; msrc marks positions the miss warps own.  Layer layer_begin + l
+// reads the plan of unit group (l / group); layer_begin is a multiple of group.
+cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, int32_t group, int32_t R,
+                                int32_t n, int32_t max_m, const int32_t* rows, const int32_t* miss_count,
+                                const int4* miss_list, const int32_t* msrc, uint8_t* out, int32_t row_bytes,
+                                int64_t num_rows, int sms,
                                 cudaStream_t s);
 cudaError_t launch_offload(const LayerPtrs& ptrs, const PoolGeom& g, const int32_t* gpu_blocks,
                            const int32_t* host_blocks, int32_t n, int32_t* status, int sms, cudaStream_t s);

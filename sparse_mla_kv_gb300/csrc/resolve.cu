@@ -9,18 +9,27 @@
 // (Integration): speculative decoding uses one replayable per-step plan sharing the hot state.
 //
 // Design (sm_103a):
-//   resolve_kernel   one CTA (1024 threads) per (layer, request) unit.  The unit's slot state is
-//                    staged in shared memory; two open-addressing hash tables (32-bit entries) map
-//                    token -> lowest slot and id -> first position; the plan, hit/miss
-//                    classification and the miss ranks come from block-wide scans; victims are the
-//                    candidates sorted by (stamp, slot) with a stable LSD radix sort (8-bit digits,
-//                    per-warp histograms, __match_any_sync ranking).  Misses go to a per-unit list in
-//                    the caller's workspace.  A unit with a data error writes nothing but -1 rows
-//                    and its status.
+//   resolve_kernel   one CTA (1024 threads) per (index group, request) unit.  The unit's slot stamps,
+//                    ids and their pages' table entries are staged in shared memory; an
+//                    open-addressing hash table (32-bit entries) maps id -> first position, and each
+//                    slot's token is looked up in it once, so that every plan entry learns the lowest
+//                    slot holding its token (an atomicMin) without a second table over the slots.
+//                    The plan, hit/miss classification and the miss ranks come from block-wide scans;
+//                    victims are the candidates sorted by (stamp, slot) with a stable LSD radix sort
+//                    (8-bit digits, per-warp histograms, __match_any_sync ranking) whose buffers reuse
+//                    the hash table's memory.  Misses go to a per-unit list in the caller's
+//                    workspace.  A unit with a data error writes nothing but -1 rows and its status.
+//                    The footprint, 4*C + 13*P*K bytes plus the hash table, fits the pages' MTP sizing
+//                    (num_spec + 2) * K = 10240 slots with P*K = 8192 ids in one CTA.
 //   miss_copy_kernel a persistent grid spreads every unit's misses over all SMs: each warp takes
-//                    batches of 32 (unit, 8-row) items, skips empty ones with one ballot, and copies
-//                    the rows as 16-byte zero-copy loads from the mapped pinned host pool.  Spreading
-//                    keeps enough loads in flight on the host link even when few units miss a lot.
+//                    batches of 32 (unit, 4-row) items, skips empty ones with one ballot, and copies
+//                    the rows as 16-byte zero-copy loads from the mapped pinned host pool, once for
+//                    each layer of the unit's index group.  Spreading keeps enough loads in flight on
+//                    the host link even when few units miss a lot.
+//
+// IndexShare (one indexer per group of G sparse-MLA layers): the group's layers resolve the same ids
+// against the same tables at the same step, so one unit per (group, request) decides for all of
+// them, and only the byte copies are repeated per layer.
 #include <atomic>
 #include <climits>
 
@@ -33,7 +42,10 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kEmpty = -1;
 constexpr int kBadHost = INT_MIN;
 constexpr int kGatherOwnedByMissWarps = INT_MIN;
-enum : uint8_t { kNone = 0, kResident = 1, kHit = 2, kMiss = 3 };
+constexpr int kNoSlot = INT_MAX;
+constexpr int kTokRegs = 4;  // slot tokens per thread held in registers between phases 0 and 1b
+// kNone: padding; kDup: a repeated id (s_val holds its first occurrence's position)
+enum : uint8_t { kNone = 0, kResident = 1, kHit = 2, kMiss = 3, kDup = 4 };
 
 __device__ __forceinline__ uint32_t fib_hash(int32_t key, int bits) {
   return ((uint32_t)key * 0x9E3779B1u) >> (32 - bits);
@@ -65,6 +77,58 @@ __device__ __forceinline__ int hash_find(const int* tab, int bits, const int32_t
   }
   return -1;
 }
+
+// The id -> first position table.  Narrow: 32-bit entries holding a position (the key is read from
+// the ids array: two dependent shared-memory reads per probe).  Wide: 64-bit entries packing
+// (id << 32 | position), one read per probe; since the id is the high half, atomicMin on an entry
+// keeps the smallest position of that id.  Wide is used when its shared memory fits.
+template <bool kWide>
+struct IdHash;
+
+template <>
+struct IdHash<false> {
+  int* tab;
+  int bits;
+  const int32_t* keys;
+  __device__ void clear() {
+    for (int i = threadIdx.x; i < (1 << bits); i += kResolveThreads) tab[i] = kEmpty;
+  }
+  __device__ void insert_min(int32_t k, int e) { hash_insert_min(tab, bits, keys, k, e); }
+  __device__ int find(int32_t k) const { return hash_find(tab, bits, keys, k); }
+};
+
+template <>
+struct IdHash<true> {
+  unsigned long long* tab;
+  int bits;
+  static constexpr unsigned long long kVoid = ~0ull;
+  __device__ void clear() {
+    for (int i = threadIdx.x; i < (1 << bits); i += kResolveThreads) tab[i] = kVoid;
+  }
+  __device__ void insert_min(int32_t k, int e) {
+    const uint32_t mask = (1u << bits) - 1u;
+    const unsigned long long packed = ((unsigned long long)(uint32_t)k << 32) | (uint32_t)e;
+    uint32_t h = fib_hash(k, bits);
+    for (uint32_t it = 0; it <= mask; ++it, h = (h + 1u) & mask) {
+      const unsigned long long cur = atomicCAS(&tab[h], kVoid, packed);
+      if (cur == kVoid) return;
+      if ((uint32_t)(cur >> 32) == (uint32_t)k) {
+        atomicMin(&tab[h], packed);
+        return;
+      }
+    }
+  }
+  __device__ int find(int32_t k) const {
+    const uint32_t mask = (1u << bits) - 1u;
+    uint32_t h = fib_hash(k, bits);
+    for (uint32_t it = 0; it <= mask; ++it, h = (h + 1u) & mask) {
+      const unsigned long long cur = tab[h];
+      if (cur == kVoid) return -1;
+      if ((uint32_t)(cur >> 32) == (uint32_t)k) return (int)(uint32_t)cur;
+    }
+    return -1;
+  }
+};
 
 // Exclusive block-wide scan of two ints at once.  Contains __syncthreads: call uniformly.
 __device__ __forceinline__ void block_scan2(int a, int b, int& ea, int& eb, int& ta, int& tb, int* s_tmp) {
@@ -149,16 +213,16 @@ __device__ unsigned short* radix_sort_slots(unsigned short* a, unsigned short* b
 }
 
 // kS: the page size when it is a compile-time constant (64 in the pages' FP8 MLA setup), else 0.
-template <int kS>
+// kWide: the id table's entry width (see IdHash).
+template <int kS, bool kWide>
 __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const ResolveParams p, const ResolveSmem sm) {
   extern __shared__ __align__(16) unsigned char smem[];
-  int32_t* s_tok = reinterpret_cast<int32_t*>(smem + sm.tok);
   int32_t* s_stamp = reinterpret_cast<int32_t*>(smem + sm.stamp);
   int32_t* s_ids = reinterpret_cast<int32_t*>(smem + sm.ids);
   int32_t* s_val = reinterpret_cast<int32_t*>(smem + sm.val);
   uint8_t* s_cls = reinterpret_cast<uint8_t*>(smem + sm.cls);
-  int* s_idh = reinterpret_cast<int*>(smem + sm.idh);
-  int* s_slh = reinterpret_cast<int*>(smem + sm.u);
+  int32_t* s_slot = reinterpret_cast<int32_t*>(smem + sm.slot);  // lowest slot holding position i's id
+
   int32_t* s_hot = reinterpret_cast<int32_t*>(smem + sm.hot);
   // the request's block-table and host-table rows, staged when they are small (sm.tbl_pages > 0)
   const bool staged = sm.tbl_pages > 0;
@@ -173,10 +237,10 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
   pdl_allow_dependents();   // the following gather / miss-copy kernel may place its CTAs now
   const int unit = blockIdx.x;
   const int lr = unit / p.R, r = unit - lr * p.R;
-  const int l = p.layer_begin + lr;
+  const int grp = p.layer_begin + lr;  // index group (a layer when no layers share an indexer)
   const int n = p.n, C = p.C, step = p.step;
   const int S = kS ? kS : p.S;
-  const int64_t state_off = ((int64_t)l * p.R + r) * C;
+  const int64_t state_off = ((int64_t)grp * p.R + r) * C;
   const int32_t* ids_g = p.topk + (int64_t)unit * n;
   const int32_t* bt = p.bt + (int64_t)r * p.max_pages;
   const int32_t* hbt = p.hbt + (int64_t)r * p.max_pages;
@@ -184,7 +248,12 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
   int32_t* rows_g = p.out_rows + (int64_t)unit * n;
   int32_t* msrc_g = p.msrc ? p.msrc + (int64_t)unit * n : nullptr;
   const int ctx = p.ctx_len[r];
-  const int HI = 1 << sm.id_hash_bits, HS = 1 << sm.slot_hash_bits;
+  IdHash<kWide> idh;
+  if constexpr (kWide) {
+    idh = IdHash<kWide>{reinterpret_cast<unsigned long long*>(smem + sm.idh), sm.id_hash_bits};
+  } else {
+    idh = IdHash<kWide>{reinterpret_cast<int*>(smem + sm.idh), sm.id_hash_bits, s_ids};
+  }
 
   // ---- phase 0: stage state and ids; checks that need no classification
   if (tid == 0) {
@@ -193,8 +262,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
     s_lo = INT_MAX;
     s_hi = INT_MIN;
   }
-  for (int i = tid; i < HI; i += kResolveThreads) s_idh[i] = kEmpty;
-  for (int i = tid; i < HS; i += kResolveThreads) s_slh[i] = kEmpty;
+  idh.clear();
   uint32_t err = 0u;
   // ids, and their page's table entries fetched right away (independent of the hashing below) so
   // that classification needs no global-memory round trip.  Combined entry in s_val:
@@ -222,16 +290,23 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
       }
     }
     s_val[i] = e;
+    s_slot[i] = kNoSlot;
   }
   for (int b = tid; b < C / S; b += kResolveThreads) {
     const int hb = hot[b];
     s_hot[b] = hb;
     if (hb < 0 || hb >= p.num_gpu_blocks) err |= kErrTable;
   }
+  // slot tokens: the first kTokRegs * kResolveThreads are loaded now (their latency overlaps the
+  // loads above) and held in registers until phase 1b; any further ones are read there
+  int tokr[kTokRegs];
+#pragma unroll
+  for (int k = 0; k < kTokRegs; ++k) {
+    const int s = tid + k * kResolveThreads;
+    tokr[k] = s < C ? p.slot_token[state_off + s] : -1;
+  }
   for (int s = tid; s < C; s += kResolveThreads) {
-    const int t = p.slot_token[state_off + s];
     const int st = p.slot_stamp[state_off + s];
-    s_tok[s] = t;
     s_stamp[s] = st;
     if (st > step) err |= kErrStep;
   }
@@ -239,16 +314,12 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
   __syncthreads();
   const bool early = (s_err & (kErrStep | kErrId)) != 0u;
 
-  // ---- phase 1: hash tables (token -> lowest slot, id -> first position)
+  // ---- phase 1: hash table id -> first position
   if (!early) {
-    for (int s = tid; s < C; s += kResolveThreads) {
-      const int t = s_tok[s];
-      if (t >= 0) hash_insert_min(s_slh, sm.slot_hash_bits, s_tok, t, s);
-    }
     for (int i = tid; i < n; i += kResolveThreads) {
       const int id = s_ids[i];
       if (id >= 0) {
-        hash_insert_min(s_idh, sm.id_hash_bits, s_ids, id, i);
+        idh.insert_min(id, i);
         if (staged) {
           const int page = (unsigned)id / S;
           const int b = s_bt[page];
@@ -260,14 +331,40 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
   }
   __syncthreads();
 
-  // ---- phase 2: classify each plan entry (first occurrences); hits get stamp = step in smem
+  // ---- phase 1b: each slot's token, looked up among the ids: the plan entry of that id learns the
+  // lowest slot holding it
+  if (!early) {
+#pragma unroll
+    for (int k = 0; k < kTokRegs; ++k) {
+      const int t = tokr[k];
+      if (t >= 0) {
+        const int f = idh.find(t);
+        if (f >= 0) atomicMin(&s_slot[f], tid + k * kResolveThreads);
+      }
+    }
+    for (int s = tid + kTokRegs * kResolveThreads; s < C; s += kResolveThreads) {
+      const int t = p.slot_token[state_off + s];
+      if (t >= 0) {
+        const int f = idh.find(t);
+        if (f >= 0) atomicMin(&s_slot[f], s);
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- phase 2: classify each plan entry (first occurrences); hits get stamp = step in smem;
+  // repeated ids record their first occurrence
   int c_res = 0, c_hit = 0, c_miss = 0;
   if (!early) {
     for (int i = tid; i < n; i += kResolveThreads) {
       const int id = s_ids[i];
       uint8_t cls = kNone;
       int val = 0;
-      if (id >= 0 && hash_find(s_idh, sm.id_hash_bits, s_ids, id) == i) {
+      const int f = id >= 0 ? idh.find(id) : -1;
+      if (f >= 0 && f != i) {
+        cls = kDup;
+        val = f;
+      } else if (f == i) {
         const int off = (unsigned)id % S;
         const int e = s_val[i];
         if (e >= 0) {
@@ -276,8 +373,8 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
           cls = kResident;
           ++c_res;
         } else {
-          const int s = hash_find(s_slh, sm.slot_hash_bits, s_tok, id);
-          if (s >= 0) {
+          const int s = s_slot[i];
+          if (s != kNoSlot) {
             cls = kHit;
             val = s;
             s_stamp[s] = step;
@@ -331,10 +428,10 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
     if (tot_miss > tot_cand) e = kErrCapacity;  // uniform: totals are block-wide
     if (e == 0u && tot_miss > 0) {
       // ---- phase 4: victims = candidates in ascending (stamp, slot)
-      unsigned short* buf_a = reinterpret_cast<unsigned short*>(smem + sm.u);
+      unsigned short* buf_a = reinterpret_cast<unsigned short*>(smem + sm.idh);
       unsigned short* buf_b = buf_a + ((C + 7) & ~7);
       int* hist = reinterpret_cast<int*>(buf_b + ((C + 7) & ~7));
-      __syncthreads();  // the slot hash (same memory) is dead from here on
+      __syncthreads();  // the id hash (same memory) is dead from here on
       int k = cand_base;
       for (int s = q0; s < q1; ++s)
         if (s_stamp[s] < step) buf_a[k++] = (unsigned short)s;
@@ -376,10 +473,10 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
       const int id = s_ids[i];
       int row = -1;
       if (id >= 0) {
-        if (s_cls[i] != kNone) {
+        if (s_cls[i] != kDup) {
           row = s_val[i];
         } else {  // a repeated id: share the first occurrence's row (a miss: re-read its host row)
-          const int f = hash_find(s_idh, sm.id_hash_bits, s_ids, id);
+          const int f = s_val[i];
           row = s_val[f];
           if (msrc_g) {
             // a repeated position of a miss reads the host row again (the first occurrence's host
@@ -456,32 +553,34 @@ __global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(const ResolvePa
       const int c = __shfl_sync(kFull, cnt, src_lane);
       const int r0 = ch * kMissRowsPerItem;
       const int nrows = min(kMissRowsPerItem, c - r0);
-      const int l = p.layer_begin + u / p.R;
+      const int l0 = (p.layer_begin + u / p.R) * p.group;
       int4 ent = make_int4(0, 0, 0, 0);
       if (lane < nrows) ent = p.miss_list[(int64_t)u * p.max_m + r0 + lane];
-      const uint8_t* host = ptrs.host[l];
-      uint8_t* pool = ptrs.gpu[l];
       const int total = nrows * cpr;
-      for (int f0 = 0; f0 < total; f0 += 32 * kU) {
-        uint4 v[kU];
-        int64_t dst_off[kU];
+      for (int l = l0; l < l0 + p.group; ++l) {  // every layer of the unit's index group
+        const uint8_t* host = ptrs.host[l];
+        uint8_t* pool = ptrs.gpu[l];
+        for (int f0 = 0; f0 < total; f0 += 32 * kU) {
+          uint4 v[kU];
+          int64_t dst_off[kU];
 #pragma unroll
-        for (int k = 0; k < kU; ++k) {
-          const int f = f0 + k * 32 + lane;
-          const bool ok = f < total;
-          const int rr = ok ? f / cpr : 0;
-          const int cc = f - rr * cpr;
-          const int src = __shfl_sync(kFull, ent.x, rr);
-          const int dst = __shfl_sync(kFull, ent.y, rr);
-          dst_off[k] = -1;
-          if (ok) {
-            v[k] = __ldcg(reinterpret_cast<const uint4*>(host + (int64_t)src * row_bytes) + cc);
-            dst_off[k] = (int64_t)dst * row_bytes + (int64_t)cc * 16;
+          for (int k = 0; k < kU; ++k) {
+            const int f = f0 + k * 32 + lane;
+            const bool ok = f < total;
+            const int rr = ok ? f / cpr : 0;
+            const int cc = f - rr * cpr;
+            const int src = __shfl_sync(kFull, ent.x, rr);
+            const int dst = __shfl_sync(kFull, ent.y, rr);
+            dst_off[k] = -1;
+            if (ok) {
+              v[k] = __ldcg(reinterpret_cast<const uint4*>(host + (int64_t)src * row_bytes) + cc);
+              dst_off[k] = (int64_t)dst * row_bytes + (int64_t)cc * 16;
+            }
           }
-        }
 #pragma unroll
-        for (int k = 0; k < kU; ++k)
-          if (dst_off[k] >= 0) *reinterpret_cast<uint4*>(pool + dst_off[k]) = v[k];
+          for (int k = 0; k < kU; ++k)
+            if (dst_off[k] >= 0) *reinterpret_cast<uint4*>(pool + dst_off[k]) = v[k];
+        }
       }
     }
   }
@@ -497,38 +596,43 @@ size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
 }  // namespace
 
-ResolveSmem resolve_smem_plan(int64_t n, int64_t C, int64_t S) {
+ResolveSmem resolve_smem_plan(int64_t n, int64_t C, int64_t S, bool wide) {
   ResolveSmem sm{};
   if (n < 0 || n > HS_MAX_PLAN || C < 1 || C > HS_MAX_CAPACITY || S < 1 || C % S) return sm;
   sm.id_hash_bits = ceil_log2(2 * (n > 16 ? n : 16));
-  sm.slot_hash_bits = ceil_log2(2 * (C > 16 ? C : 16));
+  sm.id_hash_wide = wide ? 1 : 0;
   size_t off = 0;
-  sm.tok = off;   off = align16(off + 4 * (size_t)C);
   sm.stamp = off; off = align16(off + 4 * (size_t)C);
   sm.ids = off;   off = align16(off + 4 * (size_t)n);
   sm.val = off;   off = align16(off + 4 * (size_t)n);
   sm.cls = off;   off = align16(off + (size_t)n);
-  sm.idh = off;   off = align16(off + 4 * ((size_t)1 << sm.id_hash_bits));
+  sm.slot = off;  off = align16(off + 4 * (size_t)n);
   sm.hot = off;   off = align16(off + 4 * (size_t)(C / S));
-  sm.u = off;
-  const size_t slot_hash = 4 * ((size_t)1 << sm.slot_hash_bits);
+  sm.idh = off;   // the id hash, later the victim sort's buffers
+  const size_t id_hash = (wide ? 8 : 4) * ((size_t)1 << sm.id_hash_bits);
   const size_t cbuf = 2 * (size_t)((C + 7) & ~int64_t(7));
   const size_t radix = 2 * cbuf + 4 * (size_t)kRadixBins * kSortWarps;
-  off = align16(off + (slot_hash > radix ? slot_hash : radix));
+  off = align16(off + (id_hash > radix ? id_hash : radix));
   sm.total = off;
   return sm;
 }
 
 ResolveSmem resolve_smem_plan_staged(int64_t n, int64_t C, int64_t S, int64_t max_pages, size_t limit) {
-  ResolveSmem sm = resolve_smem_plan(n, C, S);
-  if (sm.total == 0) return sm;
+  // preference: wide id table with staged table rows, narrow with staged rows, wide, narrow
   const size_t tbl = align16(8 * (size_t)max_pages);
-  if (max_pages <= kMaxStagedPages && sm.total + tbl <= limit) {
-    sm.tbl = sm.total;
-    sm.tbl_pages = (int32_t)max_pages;
-    sm.total += tbl;
+  for (int k = 0; k < 4; ++k) {
+    const bool wide = (k % 2) == 0, staged = k < 2;
+    if (staged && max_pages > kMaxStagedPages) continue;
+    ResolveSmem sm = resolve_smem_plan(n, C, S, wide);
+    if (sm.total == 0) return sm;
+    if (staged) {
+      sm.tbl = sm.total;
+      sm.tbl_pages = (int32_t)max_pages;
+      sm.total += tbl;
+    }
+    if (sm.total <= limit) return sm;
   }
-  return sm;
+  return resolve_smem_plan(n, C, S, false);
 }
 
 size_t resolve_workspace_bytes(int64_t units, int64_t n, int64_t C) {
@@ -539,32 +643,38 @@ size_t resolve_workspace_bytes(int64_t units, int64_t n, int64_t C) {
 
 size_t resolve_smem_limit(int dev) {
   // Dynamic shared memory one resolver CTA may use on this device (opt-in maximum minus the
-  // kernel's static shared memory).  Also raises the kernel's attribute to that limit, once.
+  // kernel's static shared memory).  Also raises the kernels' attribute to that limit, once.
   static std::atomic<long long> limit[64];
   if (dev < 0 || dev >= 64) return 0;
   long long v = limit[dev].load();
   if (v > 0) return (size_t)v;
   int optin = 0;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
-  cudaFuncAttributes fa{}, fb{};
-  if (cudaFuncGetAttributes(&fa, resolve_kernel<64>) != cudaSuccess) return 0;
-  if (cudaFuncGetAttributes(&fb, resolve_kernel<0>) != cudaSuccess) return 0;
-  const size_t st = fa.sharedSizeBytes > fb.sharedSizeBytes ? fa.sharedSizeBytes : fb.sharedSizeBytes;
+  const void* kernels[4] = {(const void*)resolve_kernel<64, true>, (const void*)resolve_kernel<64, false>,
+                            (const void*)resolve_kernel<0, true>, (const void*)resolve_kernel<0, false>};
+  size_t st = 0;
+  for (const void* k : kernels) {
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, k) != cudaSuccess) return 0;
+    if (fa.sharedSizeBytes > st) st = fa.sharedSizeBytes;
+  }
   const long long dyn = (long long)optin - (long long)st;
   if (dyn <= 0) return 0;
-  if (cudaFuncSetAttribute(resolve_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) != cudaSuccess)
-    return 0;
-  if (cudaFuncSetAttribute(resolve_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) != cudaSuccess)
-    return 0;
+  for (const void* k : kernels)
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) != cudaSuccess) return 0;
   limit[dev].store(dyn);
   return (size_t)dyn;
 }
 
 cudaError_t launch_resolve(const ResolveParams& p, const ResolveSmem& sm, cudaStream_t s) {
-  if (p.S == 64)
-    resolve_kernel<64><<<p.nl * p.R, kResolveThreads, sm.total, s>>>(p, sm);
-  else
-    resolve_kernel<0><<<p.nl * p.R, kResolveThreads, sm.total, s>>>(p, sm);
+  const dim3 grid(p.nl * p.R), block(kResolveThreads);
+  if (p.S == 64) {
+    if (sm.id_hash_wide) resolve_kernel<64, true><<<grid, block, sm.total, s>>>(p, sm);
+    else resolve_kernel<64, false><<<grid, block, sm.total, s>>>(p, sm);
+  } else {
+    if (sm.id_hash_wide) resolve_kernel<0, true><<<grid, block, sm.total, s>>>(p, sm);
+    else resolve_kernel<0, false><<<grid, block, sm.total, s>>>(p, sm);
+  }
   count_launch();
   return cudaGetLastError();
 }

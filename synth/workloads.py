@@ -30,7 +30,7 @@ SEED_TAG = 0x48535041  # "HSPA"
 @dataclass
 class Step:
     index: int
-    topk: np.ndarray                 # int32 [L][R][P][K]
+    topk: np.ndarray                 # int32 [L/G][R][P][K] (one list per index group of G layers)
     ctx_len: np.ndarray              # int32 [R]
     # table edits applied before this step's resolve: arrays of (r, page, value)
     bt_edits: np.ndarray = field(default_factory=lambda: np.zeros((0, 3), np.int32))
@@ -67,6 +67,7 @@ class Workload:
     host_resident_init: np.ndarray  # int64 [n][2] (r, page) whose host copy exists at start
     gpu_resident_init: np.ndarray   # int64 [n][2] (r, page) resident at start
     content_seed: int = 0
+    G: int = 1                      # layers per indexer (IndexShare); top-K lists are per group
     _gen: object = None             # step generator factory
     notes: str = ""
 
@@ -273,15 +274,19 @@ def _mtp_lists(rng, prev0, ctx, K, P, keep0, keep_pos, law="recency"):
     return out
 
 
-def config5(seed: int = 0, steps: int = 128, R: int = 256, L: int = 4) -> Workload:
+def config5(seed: int = 0, steps: int = 128, R: int = 256, L: int = 4, layers_per_index: int = 1,
+            capacity: int = 4096) -> Workload:
     """Max-batch mixed load with speculative decode (MTP3): 4 layers, 256 requests, contexts
     log-uniform in [8192, 1,048,576]; each non-tail page resident with a per-request probability
     f ~ U[0,1] (tail always resident); P=4 positions per request share one plan, position 0 keeps 80%
     of its previous list, positions 1..3 keep 90% of position 0; K=2048, hot 4096.  Each step appends
     U{1..4} tokens (the accepted MTP length) and ends with one offload launch of the pages completed
     in that step (all layers).  Host copies exist for the host-only pages; a page completed during the
-    run gets a fresh host block when it is offloaded."""
-    P, K, C, S, B = 4, 2048, 4096, 64, 656
+    run gets a fresh host block when it is offloaded.  layers_per_index = G > 1 draws one top-K per
+    index group of G layers (IndexShare) instead of one per layer.  capacity sets the hot rows per
+    request: 4096 = 2K by default; (num_spec + 2) * K = 10240 is the pages' MTP sizing."""
+    P, K, C, S, B = 4, 2048, capacity, 64, 656
+    assert L % layers_per_index == 0
     lr = _layout_rng(5, seed)
     ctx0 = np.floor(np.exp(lr.uniform(np.log(8192), np.log(1 << 20), size=R))).astype(np.int64)
     frac = lr.uniform(0.0, 1.0, size=R)
@@ -302,19 +307,20 @@ def config5(seed: int = 0, steps: int = 128, R: int = 256, L: int = 4) -> Worklo
     content = (np.arange(R)[:, None] * max_pages + pidx).astype(np.int64)
     w = Workload("max-batch-mtp3", 5, seed, L, R, P, K, C, S, B, max_pages, ngb, nhb_init + n_new, bt, hbt, content,
                  hot, ctx0.astype(np.int32), steps, _pairs(has_host), _pairs(resident), content_seed=seed,
-                 notes="GPU blocks of future tail pages are assigned and filled up front")
+                 G=layers_per_index, notes="GPU blocks of future tail pages are assigned and filled up front")
     w._grow = grow
     w._nhb_init = nhb_init
 
     def gen(w: Workload, n: int) -> Iterator[Step]:
-        rngs = _rngs(w.cfg, w.seed, w.L * w.R)
-        prev = [None] * (w.L * w.R)
+        ng = w.L // w.G
+        rngs = _rngs(w.cfg, w.seed, ng * w.R)
+        prev = [None] * (ng * w.R)
         ctx = w.ctx_len.astype(np.int64).copy()
         next_host = w._nhb_init
         pending_hbt = np.zeros((0, 3), np.int32)
         for s in range(n):
-            topk = np.empty((w.L, w.R, w.P, w.K), np.int32)
-            for l in range(w.L):
+            topk = np.empty((ng, w.R, w.P, w.K), np.int32)
+            for l in range(ng):
                 for r in range(w.R):
                     uid = l * w.R + r
                     lists = _mtp_lists(rngs[uid], prev[uid], int(ctx[r]), w.K, w.P, 0.8, 0.9)
@@ -341,7 +347,8 @@ def config5(seed: int = 0, steps: int = 128, R: int = 256, L: int = 4) -> Worklo
 
 # --------------------------------------------------------------------------- multi-turn agentic
 def config3(seed: int = 0, turns: int = 13, decode_per_turn: int = 220, R: int = 32, L: int = 16,
-            first_turn: int = 74160, prompt_per_turn: int = 753, resident_frac: float = 0.4) -> Workload:
+            first_turn: int = 74160, prompt_per_turn: int = 753, resident_frac: float = 0.4,
+            layers_per_index: int = 1) -> Workload:
     """Multi-turn agentic shape: 16 layers, 32 requests in lock-step, 13 turns (74,160-token first
     turn, then +753 prompt tokens and 220 decode tokens per turn); K=2048, hot 4096, top-K locality
     as in the mixed batch.  Residency stand-in: each request keeps its newest round(resident_frac *
@@ -349,8 +356,10 @@ def config3(seed: int = 0, turns: int = 13, decode_per_turn: int = 220, R: int =
     page is released (its host copy already exists) and its block is reused for the new page, whose
     rows the model would write (an untimed fill here).  Every completed page is offloaded (all layers,
     one launch) after the step in which it completes, to a fresh host block; pages completed before
-    the first step have host copies from the start."""
+    the first step have host copies from the start.  layers_per_index = G > 1 draws one top-K per
+    index group of G layers (IndexShare: one indexer per four sparse-MLA layers in GLM 5.3)."""
     K, C, S, B, P = 2048, 4096, 64, 656, 1
+    assert L % layers_per_index == 0
     ctx_final = first_turn + (turns - 1) * (decode_per_turn + prompt_per_turn) + decode_per_turn
     max_pages = (ctx_final + S - 1) // S
     budget = int(round(resident_frac * max_pages))
@@ -367,15 +376,16 @@ def config3(seed: int = 0, turns: int = 13, decode_per_turn: int = 220, R: int =
     steps = turns * decode_per_turn
     w = Workload("multi-turn-agentic", 3, seed, L, R, P, K, C, S, B, max_pages, ngb,
                  nhb_init + R * (max_pages - ctx0 // S) + R, bt, hbt, content, hot, np.full(R, ctx0, np.int32),
-                 steps, _pairs(complete0), _pairs(resident), content_seed=seed,
+                 steps, _pairs(complete0), _pairs(resident), content_seed=seed, G=layers_per_index,
                  notes=f"resident budget {budget} pages per request")
     w._budget = budget
     w._nhb_init = nhb_init
     w._turn = (decode_per_turn, prompt_per_turn)
 
     def gen(w: Workload, n: int) -> Iterator[Step]:
-        rngs = _rngs(w.cfg, w.seed, w.L * w.R)
-        prev = [None] * (w.L * w.R)
+        ng = w.L // w.G
+        rngs = _rngs(w.cfg, w.seed, ng * w.R)
+        prev = [None] * (ng * w.R)
         bt = w.block_table.copy()
         ctx = int(w.ctx_len[0])
         res_pages = [sorted(np.nonzero(bt[r] >= 0)[0].tolist()) for r in range(w.R)]
@@ -404,8 +414,8 @@ def config3(seed: int = 0, turns: int = 13, decode_per_turn: int = 220, R: int =
                         bt_edits.append((r, pg, blk))
                         fills.append((blk, r, pg))
                 ctx = new_ctx
-            topk = np.empty((w.L, w.R, 1, w.K), np.int32)
-            for l in range(w.L):
+            topk = np.empty((ng, w.R, 1, w.K), np.int32)
+            for l in range(ng):
                 for r in range(w.R):
                     uid = l * w.R + r
                     ids = next_topk(rngs[uid], prev[uid], ctx, w.K, 0.8 if prev[uid] is not None else 0.0, "recency")

@@ -41,11 +41,12 @@ class Rig:
         self.bt = torch.from_numpy(self.bt_np).to(self.dev)
         self.hbt = torch.from_numpy(self.hbt_np).to(self.dev)
         self.hot_blocks = torch.from_numpy(w.hot_blocks.astype(np.int32)).to(self.dev)
-        self.hot = hs.HotState.allocate(L, self.hot_blocks, C)
+        self.G = G = w.G
+        self.hot = hs.HotState.allocate(L, self.hot_blocks, C, layers_per_index=G)
         hs.hot_reset(self.pool, self.hot)
-        self.ws = hs.alloc_workspace(L, R, w.P, w.K, C, self.dev)
-        self.o_tok = np.full((L, R, C), -1, np.int32)
-        self.o_stamp = np.full((L, R, C), -1, np.int32)
+        self.ws = hs.alloc_workspace(L // G, R, w.P, w.K, C, self.dev)
+        self.o_tok = np.full((L // G, R, C), -1, np.int32)
+        self.o_stamp = np.full((L // G, R, C), -1, np.int32)
         self.o_pools = self.o_hosts = None
         if oracle_bytes:
             self.o_pools = [np.zeros(w.num_gpu_blocks * S * B, np.uint8) for _ in range(L)]
@@ -96,7 +97,12 @@ class Rig:
         else:
             rows, stats = hs.resolve_topk(self.pool, topk, self.bt, self.hbt, ctx, self.hot, st.index,
                                           workspace=self.ws)
-            out = hs.gather_rows(self.pool, rows.reshape(w.L, -1))
+            if self.G == 1:
+                out = hs.gather_rows(self.pool, rows.reshape(w.L, -1))
+            else:   # each layer of an index group gathers the group's rows
+                out = torch.empty((w.L, w.R * w.P * w.K, w.B), dtype=torch.uint8, device=self.dev)
+                for l in range(w.L):
+                    hs.gather_rows(self.pool, rows[l // self.G].reshape(-1), layer_begin=l, out=out[l])
         if len(st.off_gpu) and not self.graph:
             hs.offload_pages(self.pool, torch.from_numpy(st.off_gpu).to(self.dev),
                              torch.from_numpy(st.off_host).to(self.dev))
@@ -106,7 +112,7 @@ class Rig:
                                          host_block_table=self.hbt_np, ctx_len=st.ctx_len, max_pages=w.max_pages,
                                          C=w.C, hot_blocks=w.hot_blocks, slot_token=self.o_tok,
                                          slot_stamp=self.o_stamp, step=st.index, pools=self.o_pools,
-                                         hosts=self.o_hosts)
+                                         hosts=self.o_hosts, layers_per_index=self.G)
         if len(st.off_gpu) and self.o_pools is not None:
             oracle.offload(S=w.S, B=w.B, num_gpu_blocks=w.num_gpu_blocks, num_host_blocks=w.num_host_blocks,
                            pools=self.o_pools, hosts=self.o_hosts, gpu_blocks=st.off_gpu, host_blocks=st.off_host)
@@ -129,8 +135,8 @@ class Rig:
         w = self.w
         if self.prep is None:
             self.ctx_dev = torch.empty(w.R, dtype=torch.int32, device=self.dev)
-            self.g_rows = torch.empty((w.L, w.R, w.P, w.K), dtype=torch.int32, device=self.dev)
-            self.g_stats = torch.empty((w.L, w.R, 4), dtype=torch.int32, device=self.dev)
+            self.g_rows = torch.empty((w.L // self.G, w.R, w.P, w.K), dtype=torch.int32, device=self.dev)
+            self.g_stats = torch.empty((w.L // self.G, w.R, 4), dtype=torch.int32, device=self.dev)
             self.g_out = torch.empty((w.L, w.R * w.P * w.K, w.B), dtype=torch.uint8, device=self.dev)
             self.prep = hs.PreparedStep(self.pool, self.hot, self.bt, self.hbt, self.ctx_dev, self.g_rows,
                                         self.g_stats, self.ws, self.g_out)
@@ -162,8 +168,8 @@ class Rig:
         ids = torch.from_numpy(st.topk).to(self.dev)
         ok = torch.from_numpy(o_stats[..., 0] == 0).to(self.dev)
         for l in range(w.L):
-            idl = ids[l].reshape(w.R, -1).long()
-            idl = torch.where(ok[l][:, None], idl, torch.full_like(idl, -1))
+            idl = ids[l // self.G].reshape(w.R, -1).long()
+            idl = torch.where(ok[l // self.G][:, None], idl, torch.full_like(idl, -1))
             r_idx = torch.arange(w.R, device=self.dev)[:, None].expand_as(idl).reshape(-1)
             flat = idl.reshape(-1)
             for c0 in range(0, flat.numel(), 1 << 18):
@@ -184,7 +190,7 @@ class Rig:
         w = self.w
         tok = self.hot.slot_token
         for l in range(w.L):
-            t = tok[l].long()
+            t = tok[l // self.G].long()
             r_idx = torch.arange(w.R, device=self.dev)[:, None].expand_as(t)
             v = torch.arange(w.C, device=self.dev)[None, :].expand_as(t)
             prow = self.hot_blocks.long()[r_idx, v // w.S] * w.S + v % w.S

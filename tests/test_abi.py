@@ -62,9 +62,11 @@ def test_size_queries(lib):
     assert hs.resolve_workspace_bytes(4, 256, 4, 2048, 4096) == 4096 + 16 * 1024 * 4096 + 4 * 1024 * 8192
     assert hs.resolve_workspace_bytes(1, 3, 1, 5, 4) == 16 + 16 * 3 * 4 + 64
     assert hs.resolve_workspace_bytes(1, 1, 0, 5, 4) == 0
-    # the benchmarked shapes fit in one CTA's shared memory; oversize plans report 0 or > 227 KB
-    for P, K, C in ((1, 256, 512), (1, 2048, 4096), (4, 2048, 4096)):
+    # the benchmarked shapes and the MTP3 sizing (num_spec + 2) * K = 10240 fit in one CTA's shared
+    # memory; oversize plans report 0 or > 227 KB
+    for P, K, C in ((1, 256, 512), (1, 2048, 4096), (4, 2048, 4096), (4, 2048, 10240), (1, 1024, 16384)):
         assert 0 < hs.resolve_smem_bytes(P, K, C, 64) <= 227 * 1024
+    assert hs.resolve_smem_bytes(1, 8192, 16384, 64) > 227 * 1024
     assert hs.resolve_smem_bytes(1, 16385, 4096, 64) == 0
     assert hs.resolve_smem_bytes(1, 16, 16385, 1) == 0
     assert hs.resolve_smem_bytes(1, 16, 100, 64) == 0          # capacity not a multiple of the page

@@ -107,6 +107,98 @@ def test_random_small_cases_vs_oracle(mode):
     assert {0, 2, 5}.issubset(seen)
 
 
+def _group_case_to_gpu(case, dev, G):
+    S, B = case.S, case.B
+    gpu = [torch.from_numpy(p.reshape(case.ngb, S, B).copy()).to(dev) for p in case.pools]
+    host = [torch.from_numpy(h.reshape(-1, S, B).copy()).pin_memory() for h in case.hosts]
+    pool = hs.Pool(gpu, host)
+    hot = hs.HotState.allocate(case.L, torch.from_numpy(case.hot_blocks).to(dev), case.C, layers_per_index=G)
+    hs.hot_reset(pool, hot)
+    return pool, gpu, host, hot
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_index_share_random_small_cases_vs_oracle(mode):
+    """IndexShare: G in {2, 4} layers read one top-K list and share one hot state per request; calls
+    cover a window of index groups.  Rows, stats, the group states, every layer's pool bytes and the
+    gathered bytes of every layer equal the oracle's."""
+    rng = np.random.default_rng(4242)
+    dev = torch.device("cuda")
+    for ci in range(60):
+        case0, P, K = _random_case(rng)
+        G = int(rng.choice([2, 4]))
+        ng_total = int(rng.integers(1, 3))
+        case = Case(R=case0.R, S=case0.S, B=case0.B, C=case0.C, max_pages=case0.max_pages, ctx=case0.ctx,
+                    resident=True, host=True, hot_blocks=case0.hot_blocks, num_gpu_blocks=case0.ngb,
+                    num_host_blocks=case0.nhb, bt=case0.bt, hbt=case0.hbt, L=G * ng_total, seed=case0.seed)
+        case.tok = np.full((ng_total, case.R, case.C), -1, np.int32)
+        case.stamp = np.full((ng_total, case.R, case.C), -1, np.int32)
+        pool, gpu, host, hot = _group_case_to_gpu(case, dev, G)
+        bt, hbt = torch.from_numpy(case.bt).to(dev), torch.from_numpy(case.hbt).to(dev)
+        ctx = torch.from_numpy(case.ctx).to(dev)
+        g0 = int(rng.integers(0, ng_total))
+        ng = int(rng.integers(1, ng_total - g0 + 1))
+        lb = g0 * G
+        t = 0
+        for si in range(int(rng.integers(1, 8))):
+            t += int(rng.integers(0, 3))
+            ids = np.stack([_ids(rng, case, P, K) for _ in range(ng)])
+            ids_d = torch.from_numpy(ids).to(dev)
+            if mode == "fused":
+                rows, stats, g = hs.resolve_gather(pool, ids_d, bt, hbt, ctx, hot, t, layer_begin=lb)
+            else:
+                rows, stats = hs.resolve_topk(pool, ids_d, bt, hbt, ctx, hot, t, layer_begin=lb)
+                g = torch.stack([hs.gather_rows(pool, rows[l // G].reshape(-1), layer_begin=lb + l)
+                                 for l in range(ng * G)])
+            o_rows, o_stats = oracle.resolve(
+                S=case.S, B=case.B, num_gpu_blocks=case.ngb, num_host_blocks=case.nhb, topk=ids,
+                block_table=case.bt, host_block_table=case.hbt, ctx_len=case.ctx, max_pages=case.max_pages,
+                C=case.C, hot_blocks=case.hot_blocks, slot_token=case.tok, slot_stamp=case.stamp, step=t,
+                layer_begin=lb, pools=case.pools, hosts=case.hosts, threads=2, layers_per_index=G)
+            torch.cuda.synchronize()
+            msg = f"case {ci} step {si} G={G}"
+            assert np.array_equal(stats.cpu().numpy(), o_stats), msg
+            assert np.array_equal(rows.cpu().numpy(), o_rows), msg
+            assert np.array_equal(hot.slot_token.cpu().numpy(), case.tok), msg
+            assert np.array_equal(hot.slot_stamp.cpu().numpy(), case.stamp), msg
+            for l in range(case.L):
+                assert np.array_equal(gpu[l].cpu().numpy().reshape(-1), case.pools[l]), f"{msg} layer {l}"
+            o_out, _ = case.gather(np.repeat(o_rows.reshape(ng, -1), G, axis=0), layer_begin=lb)
+            assert np.array_equal(g.cpu().numpy().reshape(o_out.shape), o_out), msg
+        pool.close()
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_index_share_multi_turn_agentic(mode):
+    """IndexShare on the agentic shape: 8 layers in 2 index groups of 4 (one indexer per four
+    sparse-MLA layers), 32 requests at 74,160+ tokens, compressed turns so that turn boundaries,
+    block reuse and all-layer offloads fall inside 14 steps."""
+    w = workloads.config3(seed=5, decode_per_turn=6, L=8, layers_per_index=4)
+    rig = _rig(w, mode=mode)
+    misses = 0
+    for st in w.iter_steps(14):
+        _, stats, *_ = rig.step(st)
+        misses += int(stats[..., 3].sum())
+    assert misses > 0
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_index_share_graph_capture(mode):
+    """IndexShare steps captured into CUDA graphs (resolve, the per-layer or fused gather, offload)."""
+    w = workloads.config3(seed=6, decode_per_turn=6, L=4, R=8, layers_per_index=2)
+    rig = _rig(w, mode=mode, graph=True)
+    for st in w.iter_steps(13):
+        rig.step(st)
+
+
+def test_index_share_mtp3_64_requests():
+    """IndexShare with MTP3 plans: 4 layers in one index group, 64 requests, P=4 positions."""
+    w = workloads.config5(seed=2, steps=3, R=64, layers_per_index=4)
+    rig = _rig(w, mode="fused")
+    for st in w.iter_steps(3):
+        rig.step(st)
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_mixed_residency_decode_full_size(mode):
     """The 64-request, 131072-token, K=2048 mixed-residency batch (the benchmarked workload) for all
@@ -157,6 +249,25 @@ def test_max_batch_mtp3_full_size():
         _, stats, *_ = rig.step(st)
         offloaded += len(st.off_gpu)
     assert offloaded > 0
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_mtp3_hot_sizing_and_verify_replays(mode):
+    """The pages' MTP hot-buffer sizing, (num_spec + 2) * K = 10240 rows per request with P = 4 positions
+    sharing one plan, 64 requests.  Every step is resolved a second time with the same ids (a verify
+    iteration replaying the plan): identical rows, no miss, hot state unchanged."""
+    w = workloads.config5(seed=3, steps=4, R=64, capacity=10240)
+    rig = _rig(w, mode=mode)
+    for st in w.iter_steps(4):
+        rows, stats, *_ = rig.step(st)
+        rows, stats = rows.clone(), stats.clone()
+        tok, stamp = rig.hot.slot_token.clone(), rig.hot.slot_stamp.clone()
+        rows2, stats2, *_ = rig.step(st)
+        assert torch.equal(rows, rows2)
+        assert int(stats2[..., 3].sum()) == 0
+        assert torch.equal(stats[..., 1].add(stats[..., 3]).add(stats[..., 2]),
+                           stats2[..., 1].add(stats2[..., 2]))
+        assert torch.equal(tok, rig.hot.slot_token) and torch.equal(stamp, rig.hot.slot_stamp)
 
 
 def test_max_batch_mtp3_split_path_64_requests():
@@ -237,11 +348,12 @@ def test_empty_and_degenerate_shapes():
 
 
 def test_largest_shapes_and_shape_limits():
-    """P*K = 8192 ids with C = 4096 (the MTP3 shape) and C = 8192 hot rows: parity over three steps;
-    a shape whose plan does not fit in one CTA's shared memory is rejected on the host."""
+    """P*K = 8192 ids with C = 4096 (the MTP3 shape) and with C = 10240 (the pages' MTP sizing
+    (num_spec + 2) * K), C = 8192 and the largest capacity C = 16384: parity over three steps; a shape
+    whose plan does not fit in one CTA's shared memory is rejected on the host."""
     dev = torch.device("cuda")
     rng = np.random.default_rng(5)
-    for P, K, C in ((4, 2048, 4096), (1, 1024, 8192), (1, 4096, 8192)):
+    for P, K, C in ((4, 2048, 4096), (4, 2048, 10240), (1, 1024, 8192), (1, 4096, 8192), (1, 1024, 16384)):
         S, B, R, pages = 64, 32, 3, 512
         ctx = pages * S
         nb = C // S
@@ -268,7 +380,7 @@ def test_largest_shapes_and_shape_limits():
             assert np.array_equal(hot.slot_stamp.cpu().numpy(), case.stamp)
             assert np.array_equal(gpu[0].cpu().numpy().reshape(-1), case.pools[0])
         pool.close()
-    big = hs.resolve_smem_bytes(1, 1024, 16384, 64)
+    big = hs.resolve_smem_bytes(1, 8192, 16384, 64)
     assert big > 227 * 1024
     S, C = 64, 16384
     gpu = [torch.zeros((C // S + 1, S, 16), dtype=torch.uint8, device=dev)]
@@ -276,7 +388,7 @@ def test_largest_shapes_and_shape_limits():
     hot = hs.HotState.allocate(1, torch.arange(C // S, dtype=torch.int32, device=dev)[None], C)
     bt = torch.full((1, 4), -1, dtype=torch.int32, device=dev)
     with pytest.raises(hs.HSError) as e:
-        hs.resolve_topk(pool, torch.zeros((1, 1, 1, 1024), dtype=torch.int32, device=dev), bt, bt,
+        hs.resolve_topk(pool, torch.zeros((1, 1, 1, 8192), dtype=torch.int32, device=dev), bt, bt,
                         torch.tensor([256], dtype=torch.int32, device=dev), hot, 0)
     assert e.value.code == 1
     pool.close()
