@@ -27,8 +27,7 @@ def resolve_unit(*, S, num_gpu_blocks, num_host_blocks, ids, bt, hbt, ctx_len, m
     for x in ids:
         if x != -1 and (x < -1 or x >= ctx_len or x // S >= max_pages):
             errors.add(ID_RANGE)
-    if any(b < 0 or b >= num_gpu_blocks for b in hot_blocks_r):
-        errors.add(TABLE_RANGE)
+    hot_ok = all(0 <= b < num_gpu_blocks for b in hot_blocks_r)
 
     def slot_row(v):
         return hot_blocks_r[v // S] * S + v % S
@@ -61,6 +60,8 @@ def resolve_unit(*, S, num_gpu_blocks, num_host_blocks, ids, bt, hbt, ctx_len, m
                 kind[x] = ("miss", hbt[page] * S + off)
         hit_slots = [kind[x][1] for x in plan if kind[x][0] == "hit"]
         n_miss = sum(1 for x in plan if kind[x][0] == "miss")
+        if not hot_ok and (hit_slots or n_miss):      # only hits and misses touch the hot blocks
+            errors.add(TABLE_RANGE)
         eligible = [v for v in range(C) if slots[v][1] < step and v not in hit_slots]
         if n_miss > len(eligible):
             errors.add(CAPACITY)

@@ -82,7 +82,7 @@ int32_t hso_resolve_unit(int32_t S, int32_t B, int32_t num_gpu_blocks, int32_t n
                          int32_t C, const int32_t* hot_blocks_r, int32_t* tok, int32_t* stamp,
                          int32_t step, int32_t* out_rows, int32_t* out_stats) {
   int32_t i, j, s;
-  int err_step = 0, err_id = 0, err_table = 0, err_missing = 0, err_capacity = 0;
+  int err_step = 0, err_id = 0, err_table = 0, err_missing = 0, err_capacity = 0, hot_bad = 0;
 
   /* Step 1: validate what needs no classification. */
   for (s = 0; s < C; s++)
@@ -92,8 +92,9 @@ int32_t hso_resolve_unit(int32_t S, int32_t B, int32_t num_gpu_blocks, int32_t n
     if (id == -1) continue;
     if (id < -1 || id >= ctx_len || id / S >= max_pages) err_id = 1;
   }
+  /* hot blocks are dereferenced only by hits and misses; checked after classification */
   for (j = 0; j < C / S; j++)
-    if (hot_blocks_r[j] < 0 || hot_blocks_r[j] >= num_gpu_blocks) err_table = 1;
+    if (hot_blocks_r[j] < 0 || hot_blocks_r[j] >= num_gpu_blocks) hot_bad = 1;
 
   pair_t* by_id = (pair_t*)malloc(sizeof(pair_t) * (size_t)(n > 0 ? n : 1));
   pair_t* by_tok = (pair_t*)malloc(sizeof(pair_t) * (size_t)(C > 0 ? C : 1));
@@ -153,6 +154,9 @@ int32_t hso_resolve_unit(int32_t S, int32_t B, int32_t num_gpu_blocks, int32_t n
         }
       }
     }
+
+    /* A unit with a hit or a miss reads or writes its hot blocks: they must lie in the pool. */
+    if (hot_bad && nhit + nmiss > 0) err_table = 1;
 
     /* Step 4: capacity -- evictable slots are those not used in this step (stamp < step) and
      * not hit now. */

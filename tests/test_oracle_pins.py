@@ -275,6 +275,24 @@ def test_error_codes_and_precedence_leave_state_untouched():
     assert stats[0, 0, 0] == 4
 
 
+def test_fully_resident_unit_needs_no_hot_buffer():
+    """Full residency (Japanese article, "仕組み": all sparse-MLA KV on the GPU) reads every id in place,
+    so a request that holds no hot blocks (entries -1) resolves normally; as soon as one of its ids is a
+    hit or a miss, the unusable hot blocks give HS_ERR_TABLE_RANGE and nothing changes."""
+    S, C, pages, B = 4, 8, 6, 16
+    bt = np.array([[0, 1, 2, -1, -1, 3]], np.int32)
+    hbt = np.array([[-1, -1, -1, 0, 1, -1]], np.int32)
+    c = Case(R=1, S=S, B=B, C=C, max_pages=pages, ctx=[pages * S], resident=True, host=True,
+             hot_blocks=[[-1, -1]], num_gpu_blocks=4, num_host_blocks=2, bt=bt, hbt=hbt)
+    rows, stats = c.step(np.array([[[0, 5, 9, 21, 5]]], np.int32), 0)
+    assert stats[0, 0].tolist() == [0, 4, 0, 0]
+    assert rows.reshape(-1).tolist() == [0, 5, 9, 3 * S + 1, 5]
+    pool = c.pools[0].copy()
+    rows, stats = c.step(np.array([[[0, 13]]], np.int32), 1)          # 13 sits on a host-only page
+    assert stats[0, 0].tolist() == [8, 0, 0, 0] and (rows == -1).all()
+    assert (c.tok == -1).all() and (c.stamp == -1).all() and (c.pools[0] == pool).all()
+
+
 def test_tiny_decode_bytes_and_invariants():
     """Tiny-decode workload, 8 steps, with byte pools: every gathered row equals the closed-form row
     of its logical token; resident bytes never change; only victim rows change, one per miss; no
