@@ -104,9 +104,11 @@ typedef struct {
 typedef struct {
   int32_t capacity;          /* C rows per (group, request): a multiple of page_size,
                                 page_size..HS_MAX_CAPACITY; the pages' default is 2*K            */
-  const int32_t* hot_blocks; /* device int32 [R][capacity/page_size]; every entry must be a pool
-                                block in [0, num_gpu_blocks), disjoint across requests and from
-                                every resident block (not checked for overlap)                   */
+  const int32_t* hot_blocks; /* device int32 [R][capacity/page_size]; pool blocks in
+                                [0, num_gpu_blocks), disjoint across requests and from every
+                                resident block (not checked for overlap).  A request whose ids are
+                                all resident needs none (entries may be -1); a unit with a hit or a
+                                miss and an entry outside the pool gets HS_ERR_TABLE_RANGE        */
   int32_t* slot_token;       /* device int32 [num_layers/G][R][capacity]; -1 = empty slot        */
   int32_t* slot_stamp;       /* device int32 [num_layers/G][R][capacity]; last step that used the
                                 slot, -1 = never                                                  */
@@ -121,6 +123,13 @@ void hs_pool_destroy(hs_pool* pool);
 
 /* Sets slot_token and slot_stamp of all (num_layers/G) x R x capacity slots to -1 (async). */
 hs_status hs_hot_reset(const hs_pool* pool, const hs_hot_state* hot, int32_t R, hs_stream_t stream);
+
+/* Sets slot_token and slot_stamp to -1 for the listed requests only, in every index group (async):
+ * the requests that just leased a hot buffer (hs_res_take_resets in hs_residency.h) start with empty
+ * slots, while the other requests keep theirs.
+ *   requests  device int32 [n]; entries outside [0, R) are skipped. */
+hs_status hs_hot_reset_requests(const hs_pool* pool, const hs_hot_state* hot, int32_t R, const int32_t* requests,
+                                int32_t n, hs_stream_t stream);
 
 /* Bytes of caller-owned device workspace that hs_resolve_topk and hs_resolve_gather need for this
  * shape (per-unit miss lists handed from the resolver kernel to the miss-copy kernel, or per-position

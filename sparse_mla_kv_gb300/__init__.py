@@ -68,6 +68,8 @@ def lib():
         L.hs_pool_destroy.argtypes = [p]
         L.hs_hot_reset.restype = i32
         L.hs_hot_reset.argtypes = [p, ctypes.POINTER(HotStateC), i32, p]
+        L.hs_hot_reset_requests.restype = i32
+        L.hs_hot_reset_requests.argtypes = [p, ctypes.POINTER(HotStateC), i32, p, i32, p]
         L.hs_resolve_workspace_bytes.restype = sz
         L.hs_resolve_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
         L.hs_resolve_smem_bytes.restype = sz
@@ -207,6 +209,14 @@ class HotState:
 
 def hot_reset(pool: Pool, hot: HotState, stream=None) -> None:
     _check(lib().hs_hot_reset(pool.handle, ctypes.byref(hot.c), hot.R, _stream(stream)), "hs_hot_reset")
+
+
+def hot_reset_requests(pool: Pool, hot: HotState, requests: torch.Tensor, stream=None) -> None:
+    """Empty the hot slots of the listed requests (device int32 [n]) in every index group."""
+    n = int(requests.numel())
+    if n:
+        _check(lib().hs_hot_reset_requests(pool.handle, ctypes.byref(hot.c), hot.R, _dev_i32(requests, "requests"),
+                                           n, _stream(stream)), "hs_hot_reset_requests")
 
 
 def resolve_workspace_bytes(nl: int, R: int, P: int, K: int, capacity: int) -> int:

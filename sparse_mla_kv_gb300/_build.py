@@ -26,12 +26,12 @@ def _stale(out: str, deps) -> bool:
 
 def build(force: bool = False, verbose: bool = False, extra: tuple = ()) -> str:
     os.makedirs(BUILD, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    headers = sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [os.path.join(ROOT, "include", "hs.h")]
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
+    headers = sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(ROOT, "include", "*.h")))
     objs = []
     jobs = []
     for s in srcs:
-        o = os.path.join(BUILD, os.path.basename(s)[:-3] + ".o")
+        o = os.path.join(BUILD, os.path.basename(s).replace(".", "_") + ".o")
         objs.append(o)
         if force or _stale(o, [s] + headers):
             jobs.append([NVCC, *ARCH, *FLAGS, *extra, "-c", s, "-o", o])

@@ -138,6 +138,21 @@ hs_status hs_hot_reset(const hs_pool* pool, const hs_hot_state* hot, int32_t R, 
   return hs::cuda_status(e);
 }
 
+hs_status hs_hot_reset_requests(const hs_pool* pool, const hs_hot_state* hot, int32_t R, const int32_t* requests,
+                                int32_t n, hs_stream_t stream) {
+  if (!pool || !hot || R < 0 || n < 0) return HS_ERR_INVALID_ARG;
+  if (hot->capacity < pool->g.page_size || hot->capacity > HS_MAX_CAPACITY || hot->capacity % pool->g.page_size)
+    return HS_ERR_INVALID_ARG;
+  const int32_t G = hs::layers_per_index(hot, pool->g);
+  if (G == 0) return HS_ERR_INVALID_ARG;
+  if (n == 0 || R == 0) return HS_OK;
+  if (!requests || !hot->slot_token || !hot->slot_stamp) return HS_ERR_INVALID_ARG;
+  const int sms = hs::sm_count(pool->device);
+  if (sms <= 0) return HS_ERR_CUDA;
+  return hs::cuda_status(hs::launch_reset_requests(hot->slot_token, hot->slot_stamp, pool->g.num_layers / G, R,
+                                                   hot->capacity, requests, n, sms, stream));
+}
+
 size_t hs_resolve_workspace_bytes(int32_t nl, int32_t R, int32_t P, int32_t K, int32_t capacity) {
   if (nl < 0 || R < 0 || P < 1 || K < 0 || capacity < 1) return 0;
   const int64_t n = (int64_t)P * K;

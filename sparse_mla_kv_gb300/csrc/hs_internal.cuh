@@ -43,6 +43,7 @@ enum : uint32_t {
   kErrTable = 4u,
   kErrMissing = 8u,
   kErrCapacity = 16u,
+  kErrHot = 32u,  // a hot-block entry outside the pool: TABLE_RANGE only if the unit has a hit or a miss
 };
 
 // A resolver unit is (index group, request); `group` = G layers share one top-K list and one hot
@@ -109,6 +110,8 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
 cudaError_t launch_offload(const LayerPtrs& ptrs, const PoolGeom& g, const int32_t* gpu_blocks,
                            const int32_t* host_blocks, int32_t n, int32_t* status, int sms, cudaStream_t s);
 cudaError_t launch_fill_i32(int32_t* a, int64_t count, int32_t value, int sms, cudaStream_t s);
+cudaError_t launch_reset_requests(int32_t* tok, int32_t* stamp, int32_t groups, int32_t R, int32_t C,
+                                  const int32_t* requests, int32_t n, int sms, cudaStream_t s);
 
 void count_launch(int k = 1);
 

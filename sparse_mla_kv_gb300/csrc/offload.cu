@@ -62,6 +62,23 @@ __global__ void fill_i32_kernel(int32_t* __restrict__ a, int64_t count, int32_t 
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += stride) a[i] = value;
 }
 
+// Empties the slots of the listed requests in every group: element k of the flat range
+// [groups][n][C] is slot k % C of request requests[(k / C) % n] in group k / (n * C).
+__global__ void reset_requests_kernel(int32_t* __restrict__ tok, int32_t* __restrict__ stamp, int32_t groups,
+                                      int32_t R, int32_t C, const int32_t* __restrict__ requests, int32_t n) {
+  const int64_t total = (int64_t)groups * n * C;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < total; k += stride) {
+    const int64_t s = k % C, gi = k / C;
+    const int32_t r = __ldg(requests + gi % n);
+    const int64_t g = gi / n;
+    if (r < 0 || r >= R) continue;
+    const int64_t o = (g * R + r) * C + s;
+    tok[o] = -1;
+    stamp[o] = -1;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_offload(const LayerPtrs& ptrs, const PoolGeom& g, const int32_t* gpu_blocks,
@@ -76,6 +93,17 @@ cudaError_t launch_offload(const LayerPtrs& ptrs, const PoolGeom& g, const int32
   dim3 grid((unsigned)gx, (unsigned)g.num_layers);
   offload_kernel<<<grid, kOffloadThreads, 0, s>>>(ptrs, page_chunks, g.num_gpu_blocks, g.num_host_blocks, gpu_blocks,
                                                   host_blocks, n, status);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reset_requests(int32_t* tok, int32_t* stamp, int32_t groups, int32_t R, int32_t C,
+                                  const int32_t* requests, int32_t n, int sms, cudaStream_t s) {
+  const int64_t total = (int64_t)groups * n * C;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+  if (blocks < 1) blocks = 1;
+  reset_requests_kernel<<<(unsigned)blocks, 256, 0, s>>>(tok, stamp, groups, R, C, requests, n);
   count_launch();
   return cudaGetLastError();
 }

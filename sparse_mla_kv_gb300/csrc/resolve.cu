@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
   for (int b = tid; b < C / S; b += kResolveThreads) {
     const int hb = hot[b];
     s_hot[b] = hb;
-    if (hb < 0 || hb >= p.num_gpu_blocks) err |= kErrTable;
+    if (hb < 0 || hb >= p.num_gpu_blocks) err |= kErrHot;
   }
   // slot tokens: the first kTokRegs * kResolveThreads are loaded now (their latency overlaps the
   // loads above) and held in registers until phase 1b; any further ones are read there
@@ -404,6 +404,10 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
   __syncthreads();
 
   uint32_t e = s_err;
+  if (e & kErrHot) {  // hot blocks matter only to a unit that hits or misses (uniform: block totals)
+    e &= ~kErrHot;
+    if (s_cnt[1] + s_cnt[2] > 0) e |= kErrTable;
+  }
   // per-thread contiguous chunks: positions [i0, i1) and slots [q0, q1)
   const int ipt = (n + kResolveThreads - 1) / kResolveThreads;
   const int i0 = min(n, tid * ipt), i1 = min(n, i0 + ipt);

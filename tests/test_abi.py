@@ -1,5 +1,5 @@
 """The C ABI without a GPU: the library builds for sm_103a, loads, exports every function that
-include/hs.h declares, and its host-side logic (argument checks that need no device, size queries,
+the headers in include/ declare, and its host-side logic (argument checks that need no device, size queries,
 status strings) behaves as documented.  No compute call is made here."""
 import ctypes
 import os
@@ -12,7 +12,8 @@ import pytest
 import sparse_mla_kv_gb300 as hs
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "hs.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+                 if f.endswith(".h"))
 
 
 @pytest.fixture(scope="module")
@@ -26,7 +27,7 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(hs_[a-z0-9_]+)\s*\(", text)))
 
@@ -34,7 +35,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ("hs_pool_create", "hs_pool_destroy", "hs_hot_reset", "hs_resolve_topk", "hs_gather_rows",
-                 "hs_offload_pages", "hs_status_str", "hs_resolve_workspace_bytes"):
+                 "hs_offload_pages", "hs_status_str", "hs_resolve_workspace_bytes", "hs_hot_reset_requests",
+                 "hs_res_create", "hs_res_admit", "hs_res_append", "hs_res_collect", "hs_res_tables"):
         assert must in names
 
 

@@ -1,0 +1,73 @@
+"""Parity of the native residency manager (libhs.so, host code) with its oracle: the same random
+operation sequences through both, compared after every operation -- return values and error codes,
+the exported tables, free block counts, the offload queue, hot-buffer resets and fills.  Host-only
+calls: runs without a GPU."""
+import numpy as np
+import pytest
+
+import oracle.residency as ores
+from tests.test_residency_pins import apply_op, check_invariants, random_ops
+
+
+@pytest.fixture(scope="module")
+def native():
+    from sparse_mla_kv_gb300 import _build
+    _build.build()
+    from sparse_mla_kv_gb300.residency import Residency
+    return Residency
+
+
+def _same_tables(o, n):
+    ob, oh, ohot, octx = o.tables()
+    nb, nh, nhot, nctx = n.tables()
+    assert np.array_equal(np.array(ob, np.int32), nb)
+    assert np.array_equal(np.array(oh, np.int32), nh)
+    assert np.array_equal(np.array(ohot, np.int32).reshape(nhot.shape), nhot)
+    assert np.array_equal(np.array(octx, np.int32), nctx)
+
+
+@pytest.mark.parametrize("seed", range(200))
+def test_native_manager_equals_oracle_on_random_sequences(native, seed):
+    (G, H, S, R, max_pages, Hc), ops = random_ops(1000 + seed, 150)
+    o = ores.Residency(G, H, S, R, max_pages, Hc)
+    n = native(G, H, S, R, max_pages, Hc)
+    rng = np.random.default_rng(seed)
+    for i, op in enumerate(ops):
+        ro, rn = apply_op(o, op), apply_op(n, op)
+        assert ro == rn, (i, op, ro, rn)
+        _same_tables(o, n)
+        assert o.free_gpu_blocks() == n.free_gpu_blocks(), (i, op)
+        if rng.random() < 0.3:
+            assert o.take_resets() == n.take_resets(), (i, op)
+            assert o.take_fills() == n.take_fills(), (i, op)
+        check_invariants(o, G)
+    assert o.collect() == n.collect()
+    n.close()
+
+
+def test_native_manager_on_a_pressure_scenario(native):
+    """Four requests decoding in lock-step over a pool that holds about half of their pages, with
+    the indexer touching a sliding set of pages: both sides agree on every release, lease and copy."""
+    G, H, S, R, P, Hc = 96, 4096, 4, 4, 64, 4
+    o = ores.Residency(G, H, S, R, P, Hc)
+    n = native(G, H, S, R, P, Hc)
+    rng = np.random.default_rng(3)
+    for r in range(R):
+        for m in (o, n):
+            m.admit(r, 20 * S + 1)
+        assert o.collect() == n.collect()
+    for step in range(60):
+        for r in range(R):
+            for m in (o, n):
+                m.append(r, 1)
+            ids = rng.integers(0, o.reqs[r].ctx, 8).tolist()
+            for m in (o, n):
+                m.touch(r, ids, step)
+        assert o.take_fills() == n.take_fills()
+        assert o.take_resets() == n.take_resets()
+        assert o.collect() == n.collect()
+        _same_tables(o, n)
+        check_invariants(o, G)
+    released = sum(1 for r in range(R) for p in range(P) if o.reqs[r].bt[p] < 0 and o.reqs[r].hbt[p] >= 0)
+    assert released > 0
+    n.close()
