@@ -8,9 +8,13 @@ top-K and draws the rest with probability proportional to recency^-0.7.  Synthet
 
 One step = the fused path (hs_resolve_plan + hs_gather_planned: the resolver, then one gather that
 also carries the miss copies) or, with --path split, hs_resolve_topk + hs_gather_rows, over the
-step's batch (+ one hs_offload_pages launch when pages complete; this workload's contexts are fixed,
-so none do).  L2 is flushed (a 256 MB write) before every timed step, outside the timed events, and
-the host waits for each step before enqueueing the next.
+step's batch, then one hs_offload_pages launch for the pages the step completes (all layers).  The
+default workload's contexts are fixed, so its steps complete no page; --config 3 (multi-turn agentic,
+contexts growing, block reuse) and --config 5 (MTP3 max batch) offload every step, and take
+--layers-per-index (IndexShare) and, for 5, --capacity (the (num_spec + 2) * K hot sizing).  Table
+edits and the model's page writes of a step are applied before its timed events.  L2 is flushed (a
+256 MB write) before every timed step, outside the timed events, and the host waits for each step
+before enqueueing the next.
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on the host cores instead.
 """
@@ -43,7 +47,13 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 4])
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--requests", type=int, default=None, help="requests per rank (configs 2-5)")
+    ap.add_argument("--layers", type=int, default=None, help="sparse-MLA layers (configs 3, 5)")
+    ap.add_argument("--layers-per-index", type=int, default=1,
+                    help="IndexShare: layers that read one indexer's top-K and share one hot state (configs 3, 5)")
+    ap.add_argument("--capacity", type=int, default=None, help="hot rows per request (config 5)")
+    ap.add_argument("--decode-per-turn", type=int, default=None, help="decode steps per turn (config 3)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -58,10 +68,6 @@ def parse():
                     help="enqueue all timed steps without waiting for each (default: wait for each step's end "
                          "before enqueueing the next; the L2 flush queued ahead of each step keeps the GPU busy "
                          "while the step is enqueued)")
-    ap.add_argument("--timing", choices=["graph", "eager"], default="eager",
-                    help="eager: the step's C-ABI calls, each timed step enqueued behind a 256 MB L2 flush so the "
-                         "GPU is busy while the host enqueues it; graph: replays of CUDA graphs captured from those "
-                         "calls, one pair per step")
     ap.add_argument("--path", choices=["fused", "split"], default="fused",
                     help="fused: hs_resolve_plan + hs_gather_planned (miss copies inside the gather); "
                          "split: hs_resolve_topk (resolver + miss-copy kernel) + hs_gather_rows")
@@ -107,12 +113,46 @@ def max_over_ranks(dist, x: float, device) -> float:
 
 
 # ----------------------------------------------------------------------------- workload
-def make_workload(cfg: int, seed: int, n_steps: int):
+def make_workload(args, seed: int, n_steps: int):
     from synth import workloads
-    w = workloads.make(cfg, seed=seed)
+    kw = {}
+    if args.requests is not None and args.config != 1:
+        kw["R"] = args.requests
+    if args.config in (3, 5):
+        if args.layers is not None:
+            kw["L"] = args.layers
+        kw["layers_per_index"] = args.layers_per_index
+    if args.config == 5 and args.capacity is not None:
+        kw["capacity"] = args.capacity
+    if args.config == 3 and args.decode_per_turn is not None:
+        kw["decode_per_turn"] = args.decode_per_turn
+    w = workloads.make(args.config, seed=seed, **kw)
     w.steps = max(w.steps, n_steps)
     steps = list(w.iter_steps(n_steps))
     return w, steps
+
+
+class Tables:
+    """The step's tables as the resolver sees them: the initial block tables edited step by step
+    (page release and block reuse, new host copies), the step's contexts, and its offload pairs.
+    restore() goes back to the state before the first step, so that passes replay identically."""
+
+    def __init__(self, w, steps):
+        self.w, self.steps = w, steps
+        self.restore()
+
+    def restore(self):
+        self.bt = self.w.block_table.copy()
+        self.hbt = self.w.host_block_table.copy()
+
+    def edit(self, i) -> bool:
+        """Apply step i's table edits; True if a table changed."""
+        st = self.steps[i]
+        for r, p_, v in st.bt_edits:
+            self.bt[r, p_] = v
+        for r, p_, v in st.hbt_edits:
+            self.hbt[r, p_] = v
+        return bool(len(st.bt_edits) or len(st.hbt_edits))
 
 
 def measured_peaks():
@@ -179,28 +219,41 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- the CPU oracle leg
+def oracle_step(o, w, tb, st, pools, hosts, tok, stamp, threads):
+    """One step through the oracle: resolve with miss copies, gather, and the step's offload."""
+    S, B = w.S, w.B
+    rows, _ = o.resolve(S=S, B=B, num_gpu_blocks=w.num_gpu_blocks, num_host_blocks=w.num_host_blocks, topk=st.topk,
+                        block_table=tb.bt, host_block_table=tb.hbt, ctx_len=st.ctx_len, max_pages=w.max_pages,
+                        C=w.C, hot_blocks=w.hot_blocks, slot_token=tok, slot_stamp=stamp, step=st.index,
+                        pools=pools, hosts=hosts, threads=threads, layers_per_index=w.G)
+    o.gather(B=B, num_rows=w.num_gpu_blocks * S, pools=pools,
+             rows=np.repeat(rows.reshape(w.L // w.G, -1), w.G, axis=0), threads=threads)
+    if len(st.off_gpu):
+        o.offload(S=S, B=B, num_gpu_blocks=w.num_gpu_blocks, num_host_blocks=w.num_host_blocks, pools=pools,
+                  hosts=hosts, gpu_blocks=st.off_gpu, host_blocks=st.off_host)
+
+
 def oracle_run(w, steps, seconds: float, threads=None):
-    """Time the oracle (resolve with byte pools + gather) over the workload's steps, restarting from
-    an empty hot state until `seconds` have passed.  Pools hold a constant byte pattern (the bytes do
-    not change the work).  Returns (rows/s, steps timed, threads)."""
+    """Time the oracle (resolve with byte pools + gather + offload) over the workload's steps,
+    restarting from an empty hot state and the initial tables until `seconds` have passed.  Pools hold
+    a constant byte pattern (the bytes do not change the work).  Returns (rows/s, steps timed,
+    threads)."""
     import oracle
     threads = threads or oracle.default_threads()
     S, B = w.S, w.B
     pools = [np.full(w.num_gpu_blocks * S * B, 7, np.uint8) for _ in range(w.L)]
     hosts = [np.full(max(1, w.num_host_blocks) * S * B, 9, np.uint8) for _ in range(w.L)]
+    tb = Tables(w, steps)
     done = 0
     t_total = 0.0
     while t_total < seconds:
-        tok = np.full((w.L, w.R, w.C), -1, np.int32)
-        stamp = np.full((w.L, w.R, w.C), -1, np.int32)
-        for st in steps:
+        tb.restore()
+        tok = np.full((w.L // w.G, w.R, w.C), -1, np.int32)
+        stamp = np.full((w.L // w.G, w.R, w.C), -1, np.int32)
+        for i, st in enumerate(steps):
+            tb.edit(i)
             t0 = time.perf_counter()
-            rows, stats = oracle.resolve(S=S, B=B, num_gpu_blocks=w.num_gpu_blocks, num_host_blocks=w.num_host_blocks,
-                                         topk=st.topk, block_table=w.block_table, host_block_table=w.host_block_table,
-                                         ctx_len=st.ctx_len, max_pages=w.max_pages, C=w.C, hot_blocks=w.hot_blocks,
-                                         slot_token=tok, slot_stamp=stamp, step=st.index, pools=pools, hosts=hosts,
-                                         threads=threads)
-            oracle.gather(B=B, num_rows=w.num_gpu_blocks * S, pools=pools, rows=rows.reshape(w.L, -1), threads=threads)
+            oracle_step(oracle, w, tb, st, pools, hosts, tok, stamp, threads)
             t_total += time.perf_counter() - t0
             done += 1
             if t_total >= seconds:
@@ -213,22 +266,19 @@ def run_reference(args, ws, rank):
         return 0
     import oracle
     oracle.build()
-    w, steps = make_workload(args.config, args.seed, args.warmup + args.steps)
+    w, steps = make_workload(args, args.seed, args.warmup + args.steps)
     threads = oracle.default_threads()
-    o = oracle
     S, B = w.S, w.B
     pools = [np.full(w.num_gpu_blocks * S * B, 7, np.uint8) for _ in range(w.L)]
     hosts = [np.full(max(1, w.num_host_blocks) * S * B, 9, np.uint8) for _ in range(w.L)]
-    tok = np.full((w.L, w.R, w.C), -1, np.int32)
-    stamp = np.full((w.L, w.R, w.C), -1, np.int32)
+    tok = np.full((w.L // w.G, w.R, w.C), -1, np.int32)
+    stamp = np.full((w.L // w.G, w.R, w.C), -1, np.int32)
+    tb = Tables(w, steps)
     t_timed = 0.0
     for i, st in enumerate(steps):   # warm-up steps untimed, then exactly `steps` timed steps
+        tb.edit(i)
         t0 = time.perf_counter()
-        rows, _ = o.resolve(S=S, B=B, num_gpu_blocks=w.num_gpu_blocks, num_host_blocks=w.num_host_blocks, topk=st.topk,
-                            block_table=w.block_table, host_block_table=w.host_block_table, ctx_len=st.ctx_len,
-                            max_pages=w.max_pages, C=w.C, hot_blocks=w.hot_blocks, slot_token=tok, slot_stamp=stamp,
-                            step=st.index, pools=pools, hosts=hosts, threads=threads)
-        o.gather(B=B, num_rows=w.num_gpu_blocks * S, pools=pools, rows=rows.reshape(w.L, -1), threads=threads)
+        oracle_step(oracle, w, tb, st, pools, hosts, tok, stamp, threads)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             t_timed += dt
@@ -240,7 +290,7 @@ def run_reference(args, ws, rank):
         "config": config_dict(w, args),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"{args.steps} timed steps of the workload (after {args.warmup} warm-up), "
-                                   "resolve with miss copies + gather, host cores"},
+                                   "resolve with miss copies + gather + offload, host cores"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -248,13 +298,17 @@ def run_reference(args, ws, rank):
 
 
 def config_dict(w, args):
-    names = {1: "tiny decode", 2: "mixed-residency decode batch", 4: "no-residency cold start (prefix reuse)"}
-    return {"workload": f"{names[w.cfg]}: {w.L} layer(s), {w.R} requests, ctx {int(w.ctx_len[0])}, page {w.S}, "
-                        f"row {w.B} B, K={w.K}, P={w.P}, hot {w.C} rows/request",
-            "layers": w.L, "requests": w.R, "ctx": int(w.ctx_len[0]), "page": w.S, "row_bytes": w.B, "K": w.K,
-            "P": w.P, "hot_rows": w.C, "rows_per_step": w.rows_per_step, "seed": args.seed,
-            "index_dtype": "int32", "l2": "flushed (256 MB write) before every timed step, outside the timing",
-            "path": getattr(args, "path", "fused"), "timing": getattr(args, "timing", "eager"),
+    names = {1: "tiny decode", 2: "mixed-residency decode batch", 3: "multi-turn agentic decode",
+             4: "no-residency cold start (prefix reuse)", 5: "max batch with MTP3"}
+    share = f", IndexShare {w.G} layers per indexer" if w.G > 1 else ""
+    return {"workload": f"{names[w.cfg]}: {w.L} layer(s){share}, {w.R} requests, ctx {int(w.ctx_len[0])}, "
+                        f"page {w.S}, row {w.B} B, K={w.K}, P={w.P}, hot {w.C} rows/request",
+            "layers": w.L, "layers_per_index": w.G, "requests": w.R, "ctx": int(w.ctx_len[0]), "page": w.S,
+            "row_bytes": w.B, "K": w.K, "P": w.P, "hot_rows": w.C, "rows_per_step": w.rows_per_step,
+            "seed": args.seed, "index_dtype": "int32",
+            "offload": "one hs_offload_pages launch per step for the pages it completes (all layers), timed",
+            "l2": "flushed (256 MB write) before every timed step, outside the timing",
+            "path": getattr(args, "path", "fused"), "timing": "eager C-ABI calls, CUDA events on the launch stream",
             "warmup_passes": getattr(args, "passes", 2)}
 
 
@@ -271,41 +325,51 @@ def run_ours(args, ws, rank, local):
     from synth import device as sdev
 
     W, K = args.warmup, args.steps
-    w, steps = make_workload(args.config, rank_seed(args.seed, rank), W + K)
-    L, R, P, Kk, C, S, B = w.L, w.R, w.P, w.K, w.C, w.S, w.B
+    w, steps = make_workload(args, rank_seed(args.seed, rank), W + K)
+    L, G, R, P, Kk, C, S, B = w.L, w.G, w.R, w.P, w.K, w.C, w.S, w.B
+    NG = L // G   # resolver units per request: index groups
     gpu = [torch.empty((w.num_gpu_blocks, S, B), dtype=torch.uint8, device=dev) for _ in range(L)]
     host = [sdev.pinned_empty((max(1, w.num_host_blocks), S, B)) for _ in range(L)]
     for l in range(L):
         sdev.fill_gpu_pool(w, l, gpu[l])
         sdev.fill_host_pool(w, l, host[l], dev)
     pool = hs.Pool(gpu, host)
-    bt = torch.from_numpy(w.block_table).to(dev)
-    hbt = torch.from_numpy(w.host_block_table).to(dev)
+    tb = Tables(w, steps)
+    bt = torch.from_numpy(tb.bt).to(dev)
+    hbt = torch.from_numpy(tb.hbt).to(dev)
     ctx = torch.from_numpy(w.ctx_len.astype(np.int32)).to(dev)
-    hot = hs.HotState.allocate(L, torch.from_numpy(w.hot_blocks).to(dev), C)
+    hot = hs.HotState.allocate(L, torch.from_numpy(w.hot_blocks).to(dev), C, layers_per_index=G)
     hs.hot_reset(pool, hot)
     topk_all = torch.from_numpy(np.stack([st.topk for st in steps])).to(dev)   # inputs resident in HBM
-    out_rows = torch.empty((L, R, P, Kk), dtype=torch.int32, device=dev)
-    out_stats = torch.empty((L, R, 4), dtype=torch.int32, device=dev)
-    ws_buf = hs.alloc_workspace(L, R, P, Kk, C, dev)
+    ctx_all = torch.from_numpy(np.stack([st.ctx_len.astype(np.int32) for st in steps])).to(dev)
+    off_g = [torch.from_numpy(st.off_gpu.astype(np.int32)).to(dev) for st in steps]
+    off_h = [torch.from_numpy(st.off_host.astype(np.int32)).to(dev) for st in steps]
+    out_rows = torch.empty((NG, R, P, Kk), dtype=torch.int32, device=dev)
+    out_stats = torch.empty((NG, R, 4), dtype=torch.int32, device=dev)
+    ws_buf = hs.alloc_workspace(NG, R, P, Kk, C, dev)
     gout = torch.empty((L, R * P * Kk, B), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     prep = hs.PreparedStep(pool, hot, bt, hbt, ctx, out_rows, out_stats, ws_buf, gout)
 
-    # host-link bandwidth (bulk pinned copies), for the step roofline's H2D term
+    # host-link bandwidth (bulk pinned copies, both directions), for the step roofline
     hbuf = torch.empty(256 << 20, dtype=torch.uint8, pin_memory=True)
     dbuf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    for _ in range(2):
-        dbuf.copy_(hbuf, non_blocking=True)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(4):
-        dbuf.copy_(hbuf, non_blocking=True)
-    e1.record()
-    e1.synchronize()
-    h2d_gbs = 4 * (256 << 20) / (e0.elapsed_time(e1) * 1e-3) / 1e9
+
+    def copy_rate(dst, src):
+        for _ in range(2):
+            dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(4):
+            dst.copy_(src, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        return 4 * (256 << 20) / (e0.elapsed_time(e1) * 1e-3) / 1e9
+
+    h2d_gbs = copy_rate(dbuf, hbuf)
+    d2h_gbs = copy_rate(hbuf, dbuf)
     del hbuf, dbuf
 
     fused = args.path == "fused"
@@ -323,28 +387,56 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize()
         del scratch
 
+    def restore():
+        """Back to the state before the first step: tables, contexts and empty hot buffers."""
+        tb.restore()
+        bt.copy_(torch.from_numpy(tb.bt))
+        hbt.copy_(torch.from_numpy(tb.hbt))
+        hs.hot_reset(pool, hot)
+
+    def before(i, upload_tables=True):
+        """Step i's inputs that come from outside the hot path, applied before its timed events:
+        table edits (released pages, reused blocks, new host copies), the model's writes of the pages
+        that start, and the step's contexts."""
+        st = steps[i]
+        changed = tb.edit(i)
+        if changed and upload_tables:
+            bt.copy_(torch.from_numpy(tb.bt))
+            hbt.copy_(torch.from_numpy(tb.hbt))
+        if len(st.fills):
+            blocks = st.fills[:, 0].astype(np.int64)
+            owners = st.fills[:, 1:].astype(np.int64)
+            for l in range(L):
+                sdev.fill_blocks(w, l, gpu[l], blocks, owners, dev)
+        ctx.copy_(ctx_all[i])
+        return changed
+
     def phase1(i):
         (prep.plan if fused else prep.resolve)(topk_all[i], steps[i].index)
 
     def phase2():
         (prep.gather_planned if fused else prep.gather)()
 
-    # warm-up: one untimed pass over the warm-up AND the timed steps, then the hot state is reset and
+    def phase3(i):
+        prep.offload(off_g[i], off_h[i], len(steps[i].off_gpu))
+
+    # warm-up: one untimed pass over the warm-up AND the timed steps, then the state is restored and
     # the warm-up steps replayed, so the timed steps start from exactly the state they would have had.
     # The timed steps' host rows have then been read through the GPU once, as in a long-running
     # server; right after another process unpins a large amount of host memory, the first GPU reads
     # of pinned pages can stall for milliseconds for a few seconds (--passes 1 skips the first pass).
     for p_ in range(args.passes):
-        if p_:
-            hs.hot_reset(pool, hot)
+        restore()
         for i in range(W + (K if p_ + 1 < args.passes else 0)):
+            before(i)
             phase1(i)
             phase2()
+            phase3(i)
         torch.cuda.synchronize()
         st_w = out_stats.cpu().numpy()
         assert (st_w[..., 0] == 0).all(), "warm-up step reported a data error"
 
-    # clock soak: the last warm-up step's phase 2 again and again (it rewrites the same bytes, so the
+    # clock soak: the last warm-up step's gather again and again (it rewrites the same bytes, so the
     # workload state does not change), each after an L2 flush, so the HBM and the host link carry this
     # step's traffic while the clocks settle and the sampler sees the GPU under load
     sampler = ClockSampler(local) if rank == 0 and not args.no_clocks else None
@@ -355,34 +447,26 @@ def run_ours(args, ws, rank, local):
             phase2()
         torch.cuda.synchronize()
 
-    # --timing graph: each timed step is two CUDA graphs (phase 1 and phase 2), captured up front
-    graphs, kernels_per_step = [], 0
-    if args.timing == "graph":
-        for k in range(K):
-            gp, gg = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-            n0 = hs.launch_count()
-            with torch.cuda.graph(gp):
-                phase1(W + k)
-            with torch.cuda.graph(gg):
-                phase2()
-            kernels_per_step = hs.launch_count() - n0
-            graphs.append((gp, gg))
-    stats_all = torch.empty((K, L, R, 4), dtype=torch.int32, device=dev)
+    stats_all = torch.empty((K, NG, R, 4), dtype=torch.int32, device=dev)
 
     def timed_pass(split: bool):
         """The K timed steps, each behind an L2 flush and bracketed by CUDA events on the launch
         stream.  split=False: events around the whole step only, so the gather launch overlaps the
-        resolver's tail (programmatic dependent launch); split=True: one more event between the two
-        calls, which times each separately at the cost of that overlap."""
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        resolver's tail (programmatic dependent launch); split=True: events between the calls too,
+        which time each separately at the cost of that overlap."""
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
         for k in range(K):
             i = W + k
+            before(i)
             flush.fill_(k & 0xFF)
             ev[k][0].record(stream)
-            graphs[k][0].replay() if graphs else phase1(i)
+            phase1(i)
             if split:
                 ev[k][1].record(stream)
-            graphs[k][1].replay() if graphs else phase2()
+            phase2()
+            if split:
+                ev[k][3].record(stream)
+            phase3(i)
             ev[k][2].record(stream)
             stats_all[k].copy_(out_stats, non_blocking=True)   # after the step's events: not timed
             if not args.run_ahead:
@@ -390,6 +474,12 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize()
         return ev
 
+    restore()
+    for i in range(W):
+        before(i)
+        phase1(i)
+        phase2()
+        phase3(i)
     barrier(dist)
     torch.cuda.synchronize()
     n_launch0 = hs.launch_count()
@@ -397,25 +487,29 @@ def run_ours(args, ws, rank, local):
     ev = timed_pass(split=False)
     wall = time.perf_counter() - wall0
     barrier(dist)
-    # our kernels inside the timed region: counted at capture for graph replays, live otherwise
-    launches = K * kernels_per_step if graphs else hs.launch_count() - n_launch0
+    # our kernels inside the timed region (the model's page writes are torch's, not ours)
+    launches = hs.launch_count() - n_launch0
     clocks = sampler.stop() if sampler else None
     t_step = [ev[k][0].elapsed_time(ev[k][2]) * 1e-3 for k in range(K)]
     st_all = stats_all.cpu().numpy()
     assert (st_all[..., 0] == 0).all(), "a timed step reported a data error"
 
-    # second pass over the same steps for the per-call split (roofline of the gather): the hot state
-    # is reset and the warm-up steps replayed, so each timed step starts from the same state again
-    hs.hot_reset(pool, hot)
+    # second pass over the same steps for the per-call split (roofline of the gather): the state is
+    # restored and the warm-up steps replayed, so each timed step starts from the same state again
+    restore()
     for i in range(W):
+        before(i)
         phase1(i)
         phase2()
+        phase3(i)
     torch.cuda.synchronize()
     ev_s = timed_pass(split=True)
     assert np.array_equal(stats_all.cpu().numpy(), st_all), "the split pass resolved differently"
     t_res = [ev_s[k][0].elapsed_time(ev_s[k][1]) * 1e-3 for k in range(K)]
-    t_gat = [ev_s[k][1].elapsed_time(ev_s[k][2]) * 1e-3 for k in range(K)]
+    t_gat = [ev_s[k][1].elapsed_time(ev_s[k][3]) * 1e-3 for k in range(K)]
+    t_off = [ev_s[k][3].elapsed_time(ev_s[k][2]) * 1e-3 for k in range(K)]
     t_step_split = [ev_s[k][0].elapsed_time(ev_s[k][2]) * 1e-3 for k in range(K)]
+
     sum_t = max_over_ranks(dist, float(sum(t_step)), dev)
     counts = st_all[..., 1:].sum(axis=(1, 2))           # [K][resident, hits, misses]
     hits_misses = counts.sum(axis=0)
@@ -428,6 +522,7 @@ def run_ours(args, ws, rank, local):
     # copies): algorithmic HBM bytes per launch / mean launch time from the events around it.
     # Per gathered row: 656 B out + 4 B row id (+ 4 B host source when fused) + 656 B row read from
     # HBM -- or, for a miss in the fused path, 656 B read over the host link and 656 B into its slot.
+    # Under IndexShare every layer of a group gathers, and copies, the group's rows.
     hbm_peak, peak_kind = measured_peaks()
     n_rows = L * R * P * Kk
     m_mean = float(counts[:, 2].mean())
@@ -435,7 +530,7 @@ def run_ours(args, ws, rank, local):
     t_g = statistics.fmean(t_gat)
     achieved = gather_bytes / t_g / 1e9
     tr = traffic_record("gather_kernel_fused" if fused else "gather_kernel", "gather.cu")
-    link_bytes = m_mean * B if fused else 0.0
+    link_bytes = m_mean * G * B if fused else 0.0
     roofline = {"bound": "hbm", "kernel": "gather_kernel<fused>" if fused else "gather_kernel",
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "peak_kind": peak_kind, "algorithmic_bytes_per_launch": gather_bytes,
@@ -445,69 +540,91 @@ def run_ours(args, ws, rank, local):
                 # bulk pinned-copy rate
                 "host_link_achieved_gbs": link_bytes / t_g / 1e9,
                 "host_link_peak_gbs": h2d_gbs, "host_link_frac": link_bytes / t_g / 1e9 / h2d_gbs,
-                "traffic": (tr["dram_bytes_per_launch"] if tr else None)}
+                "traffic": (tr["dram_bytes_per_launch"] if tr and tr.get("rows") == n_rows else None)}
 
-    # whole-step roofline: max(HBM bytes / HBM peak, miss bytes / measured host-link bandwidth),
-    # step by step with each step's own miss count
+    # whole-step roofline: max(HBM bytes / HBM peak, miss bytes / H2D rate, offload bytes / D2H rate),
+    # step by step with each step's own miss and offload counts
     roofs, meas = [], []
+    page_bytes = S * B
     for k in range(K):
-        m = int(counts[k, 2])
-        hbm_step = n_rows * (2 * B + 16) + L * R * 8 * C + m * (B + 8)
-        roofs.append(max(hbm_step / (hbm_peak * 1e9), m * B / (h2d_gbs * 1e9)))
+        m = int(counts[k, 2]) * G
+        n_off = len(steps[W + k].off_gpu) * L
+        hbm_step = n_rows * (2 * B + 16) + NG * R * 8 * C + m * (B + 8) + n_off * page_bytes
+        roofs.append(max(hbm_step / (hbm_peak * 1e9), m * B / (h2d_gbs * 1e9), n_off * page_bytes / (d2h_gbs * 1e9)))
         meas.append(t_step[k])
     step_roof = {"t_roof_us": 1e6 * statistics.fmean(roofs), "t_measured_us": 1e6 * statistics.fmean(meas),
                  "frac": sum(roofs) / sum(meas), "misses_per_step_mean": m_mean,
-                 "h2d_gbs_measured_bulk_copy": h2d_gbs, "path": args.path,
+                 "offloaded_pages_per_step_mean": statistics.fmean(len(steps[W + k].off_gpu) for k in range(K)),
+                 "h2d_gbs_measured_bulk_copy": h2d_gbs, "d2h_gbs_measured_bulk_copy": d2h_gbs, "path": args.path,
                  "step_us_median": 1e6 * statistics.median(t_step),
-                 "split_pass": "phase times from a second pass over the same steps with an event between the "
-                               "two calls (that event stops the gather launch from overlapping the resolver)",
+                 "split_pass": "phase times from a second pass over the same steps with events between the "
+                               "calls (they stop the gather launch from overlapping the resolver)",
                  "phase1_us_mean": 1e6 * statistics.fmean(t_res), "phase2_us_mean": 1e6 * t_g,
+                 "phase3_offload_us_mean": 1e6 * statistics.fmean(t_off),
                  "phase1_us_median": 1e6 * statistics.median(t_res), "phase2_us_median": 1e6 * statistics.median(t_gat),
                  "phase2_us_max": 1e6 * max(t_gat), "split_step_us_median": 1e6 * statistics.median(t_step_split),
                  "phase2_us_all": [round(1e6 * x, 1) for x in t_gat],
                  "phase1": "hs_resolve_plan" if fused else "hs_resolve_topk (resolver + miss copy)",
-                 "phase2": "hs_gather_planned" if fused else "hs_gather_rows"}
+                 "phase2": "hs_gather_planned" if fused else "hs_gather_rows",
+                 "phase3": "hs_offload_pages"}
 
-    # end to end through the C ABI with host buffers: H2D of the step's top-K and contexts, D2H of
-    # its rows and stats, inside the timed events (hot state reset, warm-up replayed first)
+    # end to end through the C ABI with host buffers: H2D of the step's top-K, contexts and (when the
+    # step edits them) block tables, D2H of its rows and stats, inside the timed events
     e2e = None
     if not args.no_e2e:
-        hs.hot_reset(pool, hot)
         topk_host = torch.from_numpy(np.stack([st.topk for st in steps])).pin_memory()
-        ctx_host = torch.from_numpy(w.ctx_len.astype(np.int32)).pin_memory()
-        rows_host = torch.empty((L, R, P, Kk), dtype=torch.int32, pin_memory=True)
-        stats_host = torch.empty((L, R, 4), dtype=torch.int32, pin_memory=True)
-        topk_dev = torch.empty((L, R, P, Kk), dtype=torch.int32, device=dev)
+        ctx_host = torch.from_numpy(np.stack([st.ctx_len.astype(np.int32) for st in steps])).pin_memory()
+        bt_host = torch.empty(tuple(bt.shape), dtype=torch.int32, pin_memory=True)
+        hbt_host = torch.empty(tuple(hbt.shape), dtype=torch.int32, pin_memory=True)
+        rows_host = torch.empty((NG, R, P, Kk), dtype=torch.int32, pin_memory=True)
+        stats_host = torch.empty((NG, R, 4), dtype=torch.int32, pin_memory=True)
+        topk_dev = torch.empty((NG, R, P, Kk), dtype=torch.int32, device=dev)
         prep2 = hs.PreparedStep(pool, hot, bt, hbt, ctx, out_rows, out_stats, ws_buf, gout, stream=stream)
+
         def e2e_step(i):
             if fused:
                 prep2.resolve_gather(topk_dev, steps[i].index)
             else:
                 prep2.resolve(topk_dev, steps[i].index)
                 prep2.gather()
+            prep2.offload(off_g[i], off_h[i], len(steps[i].off_gpu))
 
+        restore()
         for i in range(W):
+            before(i)
             topk_dev.copy_(topk_host[i], non_blocking=True)
             e2e_step(i)
         torch.cuda.synchronize()
         ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        h2d_bytes = []
         barrier(dist)
         for k in range(K):
             i = W + k
+            changed = before(i, upload_tables=False)
+            if changed:
+                bt_host.copy_(torch.from_numpy(tb.bt))
+                hbt_host.copy_(torch.from_numpy(tb.hbt))
             flush.fill_(k & 0xFF)
             ev2[k][0].record(stream)
             topk_dev.copy_(topk_host[i], non_blocking=True)
-            ctx.copy_(ctx_host, non_blocking=True)
+            ctx.copy_(ctx_host[i], non_blocking=True)
+            nb = topk_host[i].numel() * 4 + ctx_host[i].numel() * 4
+            if changed:
+                bt.copy_(bt_host, non_blocking=True)
+                hbt.copy_(hbt_host, non_blocking=True)
+                nb += 2 * bt_host.numel() * 4
+            h2d_bytes.append(nb)
             e2e_step(i)
             rows_host.copy_(out_rows, non_blocking=True)
             stats_host.copy_(out_stats, non_blocking=True)
             ev2[k][1].record(stream)
+            ev2[k][1].synchronize()
+            assert (stats_host.numpy()[..., 0] == 0).all()
         torch.cuda.synchronize()
         barrier(dist)
-        assert (stats_host.numpy()[..., 0] == 0).all()
         t2 = max_over_ranks(dist, float(sum(ev2[k][0].elapsed_time(ev2[k][1]) * 1e-3 for k in range(K))), dev)
         e2e = {"value": ws * rows_per_step * K / t2, "unit": UNIT,
-               "h2d_bytes_per_step": int(topk_host[0].numel() * 4 + ctx_host.numel() * 4),
+               "h2d_bytes_per_step": int(statistics.fmean(h2d_bytes)),
                "d2h_bytes_per_step": int(rows_host.numel() * 4 + stats_host.numel() * 4)}
 
     cpu = None
@@ -517,7 +634,7 @@ def run_ours(args, ws, rank, local):
         v, n_done, thr = oracle_run(w, steps, args.cpu_seconds)
         cpu = {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
                "sample": f"{n_done} steps of this workload (restarting from an empty hot state), resolve with "
-                         f"miss copies + gather, about {args.cpu_seconds:.0f} s of host time"}
+                         f"miss copies + gather + offload, about {args.cpu_seconds:.0f} s of host time"}
 
     if rank == 0:
         line = {

@@ -6,8 +6,6 @@ the GPU (torch element-wise ops) and copied to pinned memory.  No resolver arith
 """
 from __future__ import annotations
 
-import weakref
-
 import numpy as np
 import torch
 
@@ -74,25 +72,8 @@ def expected_rows(w, layer: int, r_idx: torch.Tensor, ids: torch.Tensor) -> torc
     return rows
 
 
-def _unregister(ptr: int) -> None:
-    try:
-        torch.cuda.cudart().cudaHostUnregister(ptr)
-    except Exception:
-        pass
-
-
 def pinned_empty(shape, dtype=torch.uint8) -> torch.Tensor:
-    """A page-locked, device-mapped host tensor of exactly this size.  torch's pinned allocator
-    rounds every request up to a power of two, which doubles tens-of-GB host pools; this registers
-    plain host memory instead (cudaHostRegister, portable | mapped)."""
-    itemsize = torch.empty((), dtype=dtype).element_size()
-    nbytes = int(np.prod(shape)) * itemsize
-    arr = np.empty(max(nbytes, 16), np.uint8)
-    try:
-        rc = torch.cuda.cudart().cudaHostRegister(arr.ctypes.data, arr.nbytes, 3)
-    except AttributeError:   # a torch without the binding: fall back to its pinned allocator
-        return torch.empty(shape, dtype=dtype, pin_memory=True)
-    if int(rc) != 0:
-        raise RuntimeError(f"cudaHostRegister failed ({int(rc)}) for {nbytes} bytes")
-    weakref.finalize(arr, _unregister, arr.ctypes.data)
-    return torch.from_numpy(arr[:nbytes]).view(dtype).reshape(shape)
+    """A page-locked, device-mapped host tensor of exactly this size, huge-page backed (the library's
+    host-pool allocator)."""
+    from sparse_mla_kv_gb300.hostmem import pinned_host_pool
+    return pinned_host_pool(shape, dtype)
