@@ -552,6 +552,16 @@ def run_ours(args, ws, rank, local):
         hbm_step = n_rows * (2 * B + 16) + NG * R * 8 * C + m * (B + 8) + n_off * page_bytes
         roofs.append(max(hbm_step / (hbm_peak * 1e9), m * B / (h2d_gbs * 1e9), n_off * page_bytes / (d2h_gbs * 1e9)))
         meas.append(t_step[k])
+    # the post-forward offload (a9): its launches in the split pass, bytes moved over the link / time
+    off_k = [k for k in range(K) if len(steps[W + k].off_gpu)]
+    offload = None
+    if off_k:
+        off_bytes = sum(len(steps[W + k].off_gpu) * L * page_bytes for k in off_k)
+        off_time = sum(t_off[k] for k in off_k)
+        offload = {"launches": len(off_k), "pages_x_layers": sum(len(steps[W + k].off_gpu) * L for k in off_k),
+                   "bytes": off_bytes, "achieved_gbs": off_bytes / off_time / 1e9, "d2h_peak_gbs": d2h_gbs,
+                   "frac": off_bytes / off_time / 1e9 / d2h_gbs, "bound": "host link (D2H)",
+                   "timing": "split pass, events around the hs_offload_pages launch"}
     step_roof = {"t_roof_us": 1e6 * statistics.fmean(roofs), "t_measured_us": 1e6 * statistics.fmean(meas),
                  "frac": sum(roofs) / sum(meas), "misses_per_step_mean": m_mean,
                  "offloaded_pages_per_step_mean": statistics.fmean(len(steps[W + k].off_gpu) for k in range(K)),
@@ -566,7 +576,7 @@ def run_ours(args, ws, rank, local):
                  "phase2_us_all": [round(1e6 * x, 1) for x in t_gat],
                  "phase1": "hs_resolve_plan" if fused else "hs_resolve_topk (resolver + miss copy)",
                  "phase2": "hs_gather_planned" if fused else "hs_gather_rows",
-                 "phase3": "hs_offload_pages"}
+                 "phase3": "hs_offload_pages", "offload": offload}
 
     # end to end through the C ABI with host buffers: H2D of the step's top-K, contexts and (when the
     # step edits them) block tables, D2H of its rows and stats, inside the timed events
