@@ -43,7 +43,17 @@ constexpr int kEmpty = -1;
 constexpr int kBadHost = INT_MIN;
 constexpr int kGatherOwnedByMissWarps = INT_MIN;
 constexpr int kNoSlot = INT_MAX;
-constexpr int kTokRegs = 4;  // slot tokens per thread held in registers between phases 0 and 1b
+constexpr int kTokRegs = 4;  // slot tokens and stamps per thread loaded first and held in registers
+constexpr int kIdRegs = 2;   // ids per thread loaded first
+constexpr int kTblRegs = 2;  // staged block-table / host-table entries per thread loaded first
+
+// A load issued where it is written: the asm statement (with a memory clobber) keeps the compiler from
+// sinking it to the value's first use, so a thread's independent loads are all in flight together.
+__device__ __forceinline__ int ld_early(const int32_t* ptr) {
+  int v;
+  asm volatile("ld.global.s32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
 // kNone: padding; kDup: a repeated id (s_val holds its first occurrence's position)
 enum : uint8_t { kNone = 0, kResident = 1, kHit = 2, kMiss = 3, kDup = 4 };
 
@@ -255,58 +265,100 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
     idh = IdHash<kWide>{reinterpret_cast<int*>(smem + sm.idh), sm.id_hash_bits, s_ids};
   }
 
-  // ---- phase 0: stage state and ids; checks that need no classification
+  // ---- phase 0: every independent load of the unit is issued first (their latencies overlap), then
+  // staged in shared memory; checks that need no classification.  With the wide id table the ids are
+  // inserted as they are staged (an entry carries its key, so no other position must be staged first).
   if (tid == 0) {
     s_err = 0u;
     s_cnt[0] = s_cnt[1] = s_cnt[2] = 0;
     s_lo = INT_MAX;
     s_hi = INT_MIN;
   }
+  const int32_t* tok_g = p.slot_token + state_off;
+  const int32_t* stamp_g = p.slot_stamp + state_off;
+  int idr[kIdRegs], tokr[kTokRegs], str[kTokRegs], btr[kTblRegs], hbtr[kTblRegs];
+#pragma unroll
+  for (int k = 0; k < kIdRegs; ++k) {
+    const int i = tid + k * kResolveThreads;
+    idr[k] = i < n ? ld_early(ids_g + i) : -1;
+  }
+#pragma unroll
+  for (int k = 0; k < kTokRegs; ++k) {
+    const int s = tid + k * kResolveThreads;
+    tokr[k] = s < C ? ld_early(tok_g + s) : -1;
+    str[k] = s < C ? ld_early(stamp_g + s) : -1;
+  }
+#pragma unroll
+  for (int k = 0; k < kTblRegs; ++k) {
+    const int j = tid + k * kResolveThreads;
+    btr[k] = (staged && j < sm.tbl_pages) ? ld_early(bt + j) : -1;
+    hbtr[k] = (staged && j < sm.tbl_pages) ? ld_early(hbt + j) : -1;
+  }
+  const int hotr = tid < C / S ? ld_early(hot + tid) : 0;
   idh.clear();
+  __syncthreads();  // the status words are reset and the table empty before any thread uses them
   uint32_t err = 0u;
-  // ids, and their page's table entries fetched right away (independent of the hashing below) so
-  // that classification needs no global-memory round trip.  Combined entry in s_val:
+  // ids, and (unstaged tables) their page's table entries.  Combined entry in s_val:
   //   e >= 0      resident block e;      e == -1   placeholder without a host copy;
   //   e == kBadHost  placeholder whose host block is outside the pool;  else host block -2 - e.
-  if (staged) {
-    for (int j = tid; j < sm.tbl_pages; j += kResolveThreads) {
-      s_bt[j] = bt[j];
-      s_hbt[j] = hbt[j];
-    }
-  }
-#pragma unroll 4
-  for (int i = tid; i < n; i += kResolveThreads) {
-    const int id = ids_g[i];
+  auto stage_id = [&](int i, int id) {
     s_ids[i] = id;
     int e = -1;
     if (id != -1) {
       if (id < -1 || id >= ctx || (unsigned)id / S >= (unsigned)p.max_pages) {
         err |= kErrId;
-      } else if (!staged) {
-        const int page = (unsigned)id / S;
-        const int b = bt[page];
-        const int h = hbt[page];
-        e = b >= 0 ? b : (h < 0 ? -1 : (h >= p.num_host_blocks ? kBadHost : -2 - h));
+      } else {
+        if constexpr (kWide) idh.insert_min(id, i);
+        if (!staged) {
+          const int page = (unsigned)id / S;
+          const int b = bt[page];
+          const int h = hbt[page];
+          e = b >= 0 ? b : (h < 0 ? -1 : (h >= p.num_host_blocks ? kBadHost : -2 - h));
+        }
       }
     }
     s_val[i] = e;
     s_slot[i] = kNoSlot;
+  };
+#pragma unroll
+  for (int k = 0; k < kIdRegs; ++k) {
+    const int i = tid + k * kResolveThreads;
+    if (i < n) stage_id(i, idr[k]);
   }
-  for (int b = tid; b < C / S; b += kResolveThreads) {
+  for (int i = tid + kIdRegs * kResolveThreads; i < n; i += kResolveThreads) stage_id(i, ids_g[i]);
+  if (staged) {
+#pragma unroll
+    for (int k = 0; k < kTblRegs; ++k) {
+      const int j = tid + k * kResolveThreads;
+      if (j < sm.tbl_pages) {
+        s_bt[j] = btr[k];
+        s_hbt[j] = hbtr[k];
+      }
+    }
+    for (int j = tid + kTblRegs * kResolveThreads; j < sm.tbl_pages; j += kResolveThreads) {
+      s_bt[j] = bt[j];
+      s_hbt[j] = hbt[j];
+    }
+  }
+  if (tid < C / S) {
+    s_hot[tid] = hotr;
+    if (hotr < 0 || hotr >= p.num_gpu_blocks) err |= kErrHot;
+  }
+  for (int b = tid + kResolveThreads; b < C / S; b += kResolveThreads) {
     const int hb = hot[b];
     s_hot[b] = hb;
     if (hb < 0 || hb >= p.num_gpu_blocks) err |= kErrHot;
   }
-  // slot tokens: the first kTokRegs * kResolveThreads are loaded now (their latency overlaps the
-  // loads above) and held in registers until phase 1b; any further ones are read there
-  int tokr[kTokRegs];
 #pragma unroll
   for (int k = 0; k < kTokRegs; ++k) {
     const int s = tid + k * kResolveThreads;
-    tokr[k] = s < C ? p.slot_token[state_off + s] : -1;
+    if (s < C) {
+      s_stamp[s] = str[k];
+      if (str[k] > step) err |= kErrStep;
+    }
   }
-  for (int s = tid; s < C; s += kResolveThreads) {
-    const int st = p.slot_stamp[state_off + s];
+  for (int s = tid + kTokRegs * kResolveThreads; s < C; s += kResolveThreads) {
+    const int st = stamp_g[s];
     s_stamp[s] = st;
     if (st > step) err |= kErrStep;
   }
@@ -314,22 +366,16 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
   __syncthreads();
   const bool early = (s_err & (kErrStep | kErrId)) != 0u;
 
-  // ---- phase 1: hash table id -> first position
-  if (!early) {
-    for (int i = tid; i < n; i += kResolveThreads) {
-      const int id = s_ids[i];
-      if (id >= 0) {
-        idh.insert_min(id, i);
-        if (staged) {
-          const int page = (unsigned)id / S;
-          const int b = s_bt[page];
-          const int h = s_hbt[page];
-          s_val[i] = b >= 0 ? b : (h < 0 ? -1 : (h >= p.num_host_blocks ? kBadHost : -2 - h));
-        }
+  // ---- phase 1 (narrow id table only): inserts, once every id is staged (a probe reads other keys)
+  if constexpr (!kWide) {
+    if (!early) {
+      for (int i = tid; i < n; i += kResolveThreads) {
+        const int id = s_ids[i];
+        if (id >= 0) idh.insert_min(id, i);
       }
     }
+    __syncthreads();
   }
-  __syncthreads();
 
   // ---- phase 1b: each slot's token, looked up among the ids: the plan entry of that id learns the
   // lowest slot holding it
@@ -343,10 +389,21 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
       }
     }
     for (int s = tid + kTokRegs * kResolveThreads; s < C; s += kResolveThreads) {
-      const int t = p.slot_token[state_off + s];
+      const int t = tok_g[s];
       if (t >= 0) {
         const int f = idh.find(t);
         if (f >= 0) atomicMin(&s_slot[f], s);
+      }
+    }
+    if (staged) {  // each id's table entry, from the staged rows
+      for (int i = tid; i < n; i += kResolveThreads) {
+        const int id = s_ids[i];
+        if (id >= 0) {
+          const int page = (unsigned)id / S;
+          const int b = s_bt[page];
+          const int h = s_hbt[page];
+          s_val[i] = b >= 0 ? b : (h < 0 ? -1 : (h >= p.num_host_blocks ? kBadHost : -2 - h));
+        }
       }
     }
   }
