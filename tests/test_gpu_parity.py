@@ -394,6 +394,27 @@ def test_largest_shapes_and_shape_limits():
     pool.close()
 
 
+def test_hot_reset_of_listed_requests_only():
+    """hs_hot_reset_requests empties the slots of the listed requests in every index group and leaves
+    the others (and entries outside [0, R)) alone."""
+    dev = torch.device("cuda")
+    S, C, R, L, G = 4, 8, 5, 4, 2
+    gpu = [torch.zeros((64, S, 16), dtype=torch.uint8, device=dev) for _ in range(L)]
+    pool = hs.Pool(gpu)
+    hot = hs.HotState.allocate(L, torch.arange(R * (C // S), dtype=torch.int32, device=dev).reshape(R, -1), C,
+                               layers_per_index=G)
+    tok = torch.arange(L // G * R * C, dtype=torch.int32, device=dev).reshape(L // G, R, C)
+    hot.slot_token.copy_(tok)
+    hot.slot_stamp.copy_(tok + 7)
+    hs.hot_reset_requests(pool, hot, torch.tensor([3, 0, 9, -1], dtype=torch.int32, device=dev))
+    torch.cuda.synchronize()
+    exp_t, exp_s = tok.clone(), tok + 7
+    exp_t[:, [0, 3]] = -1
+    exp_s[:, [0, 3]] = -1
+    assert torch.equal(hot.slot_token, exp_t) and torch.equal(hot.slot_stamp, exp_s)
+    pool.close()
+
+
 def test_gather_standalone_multilayer_and_status():
     dev = torch.device("cuda")
     L, S, B, ngb = 3, 8, 656, 40
