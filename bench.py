@@ -344,8 +344,11 @@ def run_ours(args, ws, rank, local):
     ctx_all = torch.from_numpy(np.stack([st.ctx_len.astype(np.int32) for st in steps])).to(dev)
     off_g = [torch.from_numpy(st.off_gpu.astype(np.int32)).to(dev) for st in steps]
     off_h = [torch.from_numpy(st.off_host.astype(np.int32)).to(dev) for st in steps]
-    out_rows = torch.empty((NG, R, P, Kk), dtype=torch.int32, device=dev)
-    out_stats = torch.empty((NG, R, 4), dtype=torch.int32, device=dev)
+    # the step's results in one device buffer (rows, then stats), so a caller reads them back in one copy
+    n_rows_dev = NG * R * P * Kk
+    res_dev = torch.empty(n_rows_dev + NG * R * 4, dtype=torch.int32, device=dev)
+    out_rows = res_dev[:n_rows_dev].view(NG, R, P, Kk)
+    out_stats = res_dev[n_rows_dev:].view(NG, R, 4)
     ws_buf = hs.alloc_workspace(NG, R, P, Kk, C, dev)
     gout = torch.empty((L, R * P * Kk, B), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -578,18 +581,22 @@ def run_ours(args, ws, rank, local):
                  "phase2": "hs_gather_planned" if fused else "hs_gather_rows",
                  "phase3": "hs_offload_pages", "offload": offload}
 
-    # end to end through the C ABI with host buffers: H2D of the step's top-K, contexts and (when the
-    # step edits them) block tables, D2H of its rows and stats, inside the timed events
+    # end to end through the C ABI with host buffers: H2D of the step's top-K and contexts (one packed
+    # copy) and (when the step edits them) block tables, D2H of its rows and stats (one packed copy),
+    # inside the timed events
     e2e = None
     if not args.no_e2e:
-        topk_host = torch.from_numpy(np.stack([st.topk for st in steps])).pin_memory()
-        ctx_host = torch.from_numpy(np.stack([st.ctx_len.astype(np.int32) for st in steps])).pin_memory()
+        # per step, top-K ids then contexts, packed in one pinned buffer and one device buffer
+        inp_host = torch.from_numpy(np.stack([np.concatenate([st.topk.reshape(-1), st.ctx_len.astype(np.int32)])
+                                              for st in steps])).pin_memory()
+        inp_dev = torch.empty(n_rows_dev + R, dtype=torch.int32, device=dev)
+        topk_dev = inp_dev[:n_rows_dev].view(NG, R, P, Kk)
+        ctx_e2e = inp_dev[n_rows_dev:]
         bt_host = torch.empty(tuple(bt.shape), dtype=torch.int32, pin_memory=True)
         hbt_host = torch.empty(tuple(hbt.shape), dtype=torch.int32, pin_memory=True)
-        rows_host = torch.empty((NG, R, P, Kk), dtype=torch.int32, pin_memory=True)
-        stats_host = torch.empty((NG, R, 4), dtype=torch.int32, pin_memory=True)
-        topk_dev = torch.empty((NG, R, P, Kk), dtype=torch.int32, device=dev)
-        prep2 = hs.PreparedStep(pool, hot, bt, hbt, ctx, out_rows, out_stats, ws_buf, gout, stream=stream)
+        res_host = torch.empty(res_dev.numel(), dtype=torch.int32, pin_memory=True)
+        stats_host = res_host[n_rows_dev:].view(NG, R, 4)
+        prep2 = hs.PreparedStep(pool, hot, bt, hbt, ctx_e2e, out_rows, out_stats, ws_buf, gout, stream=stream)
 
         def e2e_step(i):
             if fused:
@@ -602,7 +609,7 @@ def run_ours(args, ws, rank, local):
         restore()
         for i in range(W):
             before(i)
-            topk_dev.copy_(topk_host[i], non_blocking=True)
+            inp_dev.copy_(inp_host[i], non_blocking=True)
             e2e_step(i)
         torch.cuda.synchronize()
         ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
@@ -616,17 +623,15 @@ def run_ours(args, ws, rank, local):
                 hbt_host.copy_(torch.from_numpy(tb.hbt))
             flush.fill_(k & 0xFF)
             ev2[k][0].record(stream)
-            topk_dev.copy_(topk_host[i], non_blocking=True)
-            ctx.copy_(ctx_host[i], non_blocking=True)
-            nb = topk_host[i].numel() * 4 + ctx_host[i].numel() * 4
+            inp_dev.copy_(inp_host[i], non_blocking=True)
+            nb = inp_host[i].numel() * 4
             if changed:
                 bt.copy_(bt_host, non_blocking=True)
                 hbt.copy_(hbt_host, non_blocking=True)
                 nb += 2 * bt_host.numel() * 4
             h2d_bytes.append(nb)
             e2e_step(i)
-            rows_host.copy_(out_rows, non_blocking=True)
-            stats_host.copy_(out_stats, non_blocking=True)
+            res_host.copy_(res_dev, non_blocking=True)
             ev2[k][1].record(stream)
             ev2[k][1].synchronize()
             assert (stats_host.numpy()[..., 0] == 0).all()
@@ -635,7 +640,8 @@ def run_ours(args, ws, rank, local):
         t2 = max_over_ranks(dist, float(sum(ev2[k][0].elapsed_time(ev2[k][1]) * 1e-3 for k in range(K))), dev)
         e2e = {"value": ws * rows_per_step * K / t2, "unit": UNIT,
                "h2d_bytes_per_step": int(statistics.fmean(h2d_bytes)),
-               "d2h_bytes_per_step": int(rows_host.numel() * 4 + stats_host.numel() * 4)}
+               "d2h_bytes_per_step": int(res_host.numel() * 4),
+               "copies": "per step one H2D of top-K + contexts, one D2H of rows + stats (packed buffers)"}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
