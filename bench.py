@@ -68,6 +68,9 @@ def parse():
                     help="enqueue all timed steps without waiting for each (default: wait for each step's end "
                          "before enqueueing the next; the L2 flush queued ahead of each step keeps the GPU busy "
                          "while the step is enqueued)")
+    ap.add_argument("--residency", action="store_true",
+                    help="time the host-side residency manager (native and its oracle) on a decode loop under "
+                         "KV pressure instead of the GPU path; host only")
     ap.add_argument("--path", choices=["fused", "split"], default="fused",
                     help="fused: hs_resolve_plan + hs_gather_planned (miss copies inside the gather); "
                          "split: hs_resolve_topk (resolver + miss-copy kernel) + hs_gather_rows")
@@ -670,9 +673,75 @@ def run_ours(args, ws, rank, local):
     return 0
 
 
+def run_residency(args):
+    """The residency manager's own step: R requests decode under KV pressure (the pool holds about 60%
+    of what they grow to); each step appends each request's tokens, touches the pages of its top-K,
+    collects the offload queue and takes the tables, fills and resets.  Timed through the native
+    manager and through its oracle on the same operations."""
+    import oracle.residency as ores
+    from sparse_mla_kv_gb300 import _build
+    _build.build()
+    from sparse_mla_kv_gb300.residency import Residency
+    from synth import workloads
+    R, S, K, C, max_pages = args.requests or 64, 64, 2048, 4096, 1024
+    ctx0, grow = 48 * S, 16
+    G = int(0.6 * R * (ctx0 // S + args.steps * grow // S + C // S))
+    rng = np.random.default_rng(args.seed)
+    prev = [None] * R
+    ops = []
+    ctx = [ctx0] * R
+    for t in range(args.warmup + args.steps):
+        step = []
+        for r in range(R):
+            ctx[r] += int(rng.integers(1, 2 * grow))
+            ids = workloads.next_topk(rng, prev[r], ctx[r], K, 0.8 if prev[r] is not None else 0.0, "recency")
+            prev[r] = ids
+            step.append((r, ctx[r], ids))
+        ops.append(step)
+
+    def drive(m):
+        for r in range(R):
+            m.admit(r, ctx0)
+        m.collect()
+        m.take_fills()
+        last = [ctx0] * R
+        times = []
+        for t, step in enumerate(ops):
+            t0 = time.perf_counter()
+            for r, c, ids in step:
+                m.append(r, c - last[r])
+                last[r] = c
+            m.take_fills()
+            m.tables()
+            m.take_resets()
+            m.touch_all(np.stack([ids for _, _, ids in step]), t)
+            m.collect()
+            if t >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        return times
+
+    t_native = drive(Residency(G, 1 << 20, S, R, max_pages, C // S))
+    t_oracle = drive(ores.Residency(G, 1 << 20, S, R, max_pages, C // S))
+    v = len(t_native) / sum(t_native)
+    vo = len(t_oracle) / sum(t_oracle)
+    print(json.dumps({
+        "metric": "residency manager decode steps/s (host)", "value": v, "unit": "steps/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / v, "higher_is_better": True,
+        "dtype": "int32", "data": "synthetic",
+        "config": {"workload": f"{R} requests decoding under KV pressure, K={K} top-K touches, page {S}, "
+                               f"hot {C} rows, GPU pool {G} blocks (about 60% of the demand)",
+                   "requests": R, "K": K, "gpu_blocks": G},
+        "cpu_baseline": {"value": vo, "unit": "steps/s", "cores": 1, "kind": "oracle",
+                         "sample": "the same operations through oracle/residency.py"},
+        "speedup_vs_oracle": v / vo}), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     ws, rank, local = dist_env()
+    if args.residency:
+        return run_residency(args) if rank == 0 else 0
     if args.impl == "reference":
         return run_reference(args, ws, rank)
     return run_ours(args, ws, rank, local)

@@ -77,6 +77,11 @@ hs_status hs_res_append(hs_residency* m, int32_t r, int32_t n_tokens);
  * their pages' last use becomes `step`.  Ids outside [0, ctx_len) are ignored. */
 hs_status hs_res_touch(hs_residency* m, int32_t r, const int32_t* ids, int64_t n, int32_t step);
 
+/* hs_res_touch for every active request at once: ids is a host array [max_requests][n_per_request]
+ * (row r holds request r's ids; entries outside [0, ctx_len) -- e.g. -1 padding -- are ignored, and the
+ * rows of inactive requests are skipped).  One call per decode step instead of one per request. */
+hs_status hs_res_touch_all(hs_residency* m, const int32_t* ids, int32_t n_per_request, int32_t step);
+
 /* Request r leaves: its GPU blocks (pages and hot buffer) return to the pool, its host references are
  * dropped, and its queued offloads and fills are discarded. */
 hs_status hs_res_finish(hs_residency* m, int32_t r);

@@ -29,7 +29,8 @@ Readings where the pages are silent (the same in the native manager):
     coldest page of any other request, ascending (last use, request, page);
   - a request leases its hot buffer (capacity / page_size blocks, taken one by one through the same
     allocation) when it first has a placeholder page: at admission with a host-only prefix, or when
-    its first page is released; it returns the buffer when it finishes;
+    its first page is released; it returns the buffer when it finishes.  A lease that cannot be
+    completed returns the blocks it took and is tried again at the request's next release;
   - host blocks are reference-counted (a prefix may be shared by several requests) and return to
     the free pool at zero;
   - when no block can be found the call fails with CAPACITY: a failed admission leaves the request
@@ -116,10 +117,19 @@ class Residency:
     def _lease_hot(self, q: int) -> None:
         x = self.reqs[q]
         x.hot = []
-        if q not in self.resets:
+        added = q not in self.resets
+        if added:
             self.resets.append(q)
-        for _ in range(self.Hc):
-            x.hot.append(self._alloc_gpu(q))
+        try:
+            for _ in range(self.Hc):
+                x.hot.append(self._alloc_gpu(q))
+        except ResidencyError:        # a lease is all or nothing: the next release tries again
+            for b in x.hot:
+                self._free_gpu_block(b)
+            x.hot = None
+            if added:
+                self.resets.remove(q)
+            raise
 
     def _alloc_gpu(self, r: int) -> int:
         while not self.free_gpu:
@@ -204,6 +214,12 @@ class Residency:
             if 0 <= t < x.ctx:
                 x.lu[t // self.S] = step
 
+    def touch_all(self, ids, step: int) -> None:
+        """touch() for every active request: ids [max_requests][n], row r for request r."""
+        for r, x in enumerate(self.reqs):
+            if x is not None:
+                self.touch(r, ids[r], step)
+
     def collect(self):
         """Queued offloads (gpu block, host block) in queue order; the queue is emptied (the caller
         enqueues them in the post-forward offload launch)."""
@@ -256,7 +272,7 @@ class Residency:
             if x is None:
                 continue
             bt[r], hbt[r], ctx[r] = list(x.bt), list(x.hbt), x.ctx
-            if x.hot is not None and len(x.hot) == self.Hc:
+            if x.hot is not None:
                 hot[r] = list(x.hot)
         return bt, hbt, hot, ctx
 

@@ -43,6 +43,7 @@ struct Fill {
 
 struct hs_residency {
   int32_t S, max_pages, Hc;
+  int32_t S_shift;  // log2(S) when S is a power of two, else -1
   std::priority_queue<int32_t, std::vector<int32_t>, std::greater<int32_t>> free_gpu;
   std::priority_queue<int32_t, std::vector<int32_t>, std::greater<int32_t>> free_host;  // lazy
   std::vector<int32_t> host_ref, host_held;
@@ -177,6 +178,23 @@ struct hs_residency {
     fills.erase(std::remove_if(fills.begin(), fills.end(), [r](const Fill& f) { return f.r == r; }), fills.end());
   }
 
+  int32_t page_of(int32_t t) const { return S_shift >= 0 ? (t >> S_shift) : t / S; }
+
+  void touch(int32_t r, const int32_t* ids, int64_t n, int32_t step) {
+    Request& x = req[r];
+    for (int64_t i = 0; i < n; ++i) {
+      const int32_t t = ids[i];
+      if (t < 0 || t >= x.ctx) continue;
+      const int32_t p = page_of(t);
+      if (x.lu[p] == step) continue;
+      if (x.in_set[p]) {
+        x.releasable.erase({x.lu[p], p});
+        x.releasable.insert({step, p});
+      }
+      x.lu[p] = step;
+    }
+  }
+
   void init_request(int32_t r, int32_t ctx) {
     Request& x = req[r];
     x = Request{};
@@ -203,6 +221,9 @@ hs_status hs_res_create(int32_t num_gpu_blocks, int32_t num_host_blocks, int32_t
   if (!m) return HS_ERR_INVALID_ARG;
   try {
     m->S = page_size;
+    m->S_shift = -1;
+    for (int32_t k = 0; k < 31; ++k)
+      if ((int32_t(1) << k) == page_size) m->S_shift = k;
     m->max_pages = max_pages;
     m->Hc = hot_blocks_per_request;
     std::vector<int32_t> g(num_gpu_blocks), h(num_host_blocks);
@@ -293,18 +314,14 @@ hs_status hs_res_append(hs_residency* m, int32_t r, int32_t n_tokens) {
 hs_status hs_res_touch(hs_residency* m, int32_t r, const int32_t* ids, int64_t n, int32_t step) {
   if (!m || r < 0 || r >= (int32_t)m->req.size() || !m->req[r].active || n < 0) return HS_ERR_INVALID_ARG;
   if (n > 0 && !ids) return HS_ERR_INVALID_ARG;
-  Request& x = m->req[r];
-  for (int64_t i = 0; i < n; ++i) {
-    const int32_t t = ids[i];
-    if (t < 0 || t >= x.ctx) continue;
-    const int32_t p = t / m->S;
-    if (x.lu[p] == step) continue;
-    if (x.in_set[p]) {
-      x.releasable.erase({x.lu[p], p});
-      x.releasable.insert({step, p});
-    }
-    x.lu[p] = step;
-  }
+  m->touch(r, ids, n, step);
+  return HS_OK;
+}
+
+hs_status hs_res_touch_all(hs_residency* m, const int32_t* ids, int32_t n_per_request, int32_t step) {
+  if (!m || n_per_request < 0 || (n_per_request > 0 && !ids)) return HS_ERR_INVALID_ARG;
+  for (int32_t r = 0; r < (int32_t)m->req.size(); ++r)
+    if (m->req[r].active) m->touch(r, ids + (int64_t)r * n_per_request, n_per_request, step);
   return HS_OK;
 }
 

@@ -28,6 +28,8 @@ def _lib():
         L.hs_res_append.argtypes = [p, i32, i32]
         L.hs_res_touch.restype = i32
         L.hs_res_touch.argtypes = [p, i32, P32, i64, i32]
+        L.hs_res_touch_all.restype = i32
+        L.hs_res_touch_all.argtypes = [p, P32, i32, i32]
         L.hs_res_finish.restype = i32
         L.hs_res_finish.argtypes = [p, i32]
         L.hs_res_hold_host.restype = i32
@@ -93,6 +95,15 @@ class Residency:
     def touch(self, r: int, ids, step: int) -> None:
         arr, ptr = _i32(ids)
         _check(_lib().hs_res_touch(self.h, r, ptr, arr.size, step), "hs_res_touch")
+
+    def touch_all(self, ids, step: int) -> None:
+        """ids [max_requests][n]: every active request's selected ids in one call (rows of inactive
+        requests are ignored)."""
+        arr = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+        if arr.ndim != 2 or arr.shape[0] != self.R:
+            raise ValueError("ids must be [max_requests][n]")
+        _check(_lib().hs_res_touch_all(self.h, arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), arr.shape[1],
+                                       step), "hs_res_touch_all")
 
     def finish(self, r: int) -> None:
         _check(_lib().hs_res_finish(self.h, r), "hs_res_finish")

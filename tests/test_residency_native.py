@@ -60,9 +60,14 @@ def test_native_manager_on_a_pressure_scenario(native):
         for r in range(R):
             for m in (o, n):
                 m.append(r, 1)
-            ids = rng.integers(0, o.reqs[r].ctx, 8).tolist()
+        ids = np.stack([rng.integers(-1, o.reqs[r].ctx + 3, 8) for r in range(R)]).astype(np.int32)
+        if step % 2:
             for m in (o, n):
-                m.touch(r, ids, step)
+                m.touch_all(ids, step)
+        else:
+            for r in range(R):
+                for m in (o, n):
+                    m.touch(r, ids[r].tolist(), step)
         assert o.take_fills() == n.take_fills()
         assert o.take_resets() == n.take_resets()
         assert o.collect() == n.collect()
