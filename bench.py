@@ -646,7 +646,7 @@ def run_ours(args, ws, rank, local):
                "d2h_bytes_per_step": int(res_host.numel() * 4),
                "copies": "per step one H2D of top-K + contexts, one D2H of rows + stats (packed buffers)"}
 
-    cpu = None
+    cpu = cpu1 = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
@@ -654,6 +654,9 @@ def run_ours(args, ws, rank, local):
         cpu = {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
                "sample": f"{n_done} steps of this workload (restarting from an empty hot state), resolve with "
                          f"miss copies + gather + offload, about {args.cpu_seconds:.0f} s of host time"}
+        v1, n1, _ = oracle_run(w, steps, args.cpu_seconds / 4, threads=1)
+        cpu1 = {"value": v1, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"{n1} steps, one host thread, about {args.cpu_seconds / 4:.0f} s"}
 
     if rank == 0:
         line = {
@@ -661,7 +664,8 @@ def run_ours(args, ws, rank, local):
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "u8", "data": "synthetic", "config": config_dict(w, args),
             "gathered_gbs": value * B / 1e9, "roofline": roofline, "step_roofline": step_roof,
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
+            "cpu_baseline": cpu, "cpu_baseline_1thread": cpu1, "e2e": e2e, "gpu_launches": int(launches),
+            "clocks": clocks,
             "wall_s_timed_region": wall, "timed_counts": {"resident": int(hits_misses[0]),
                                                           "hits": int(hits_misses[1]),
                                                           "misses": int(hits_misses[2])},
