@@ -232,9 +232,14 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
   const bool k41 = row_bytes == 656;
   auto kern = k41 ? gather_fused_kernel<41> : gather_fused_kernel<0>;
   const int64_t per_layer = (int64_t)R * n * (row_bytes >> 4);
-  const int64_t want = (per_layer + (int64_t)kGatherThreads * kGatherUnroll - 1) /
-                       ((int64_t)kGatherThreads * kGatherUnroll);
-  const dim3 grid = wave_grid(sms, resident_blocks(kern, &occ[k41 ? 0 : 1]), want, nl);
+  const int64_t want_hbm = (per_layer + (int64_t)kGatherThreads * kGatherUnroll - 1) /
+                           ((int64_t)kGatherThreads * kGatherUnroll);
+  // one miss warp per CTA: enough CTAs that each can take one item (kMissRowsPerItem misses) of the most
+  // a layer can have, so a small batch does not queue its host round trips on a few warps
+  const int64_t want_miss = ((int64_t)R * ((max_m + kMissRowsPerItem - 1) / kMissRowsPerItem) + kMissWarps - 1) /
+                            kMissWarps;
+  const dim3 grid = wave_grid(sms, resident_blocks(kern, &occ[k41 ? 0 : 1]), want_hbm > want_miss ? want_hbm : want_miss,
+                              nl);
   cudaError_t e = launch_dependent(kern, grid, dim3(kGatherThreads), 0, s, ptrs, layer_begin, group, R, n, max_m,
                                    rows, miss_count, miss_list, msrc, out, row_bytes, num_rows);
   if (e != cudaSuccess) return e;
