@@ -54,6 +54,8 @@ def parse():
                     help="IndexShare: layers that read one indexer's top-K and share one hot state (configs 3, 5)")
     ap.add_argument("--capacity", type=int, default=None, help="hot rows per request (config 5)")
     ap.add_argument("--decode-per-turn", type=int, default=None, help="decode steps per turn (config 3)")
+    ap.add_argument("--full-residency", action="store_true",
+                    help="config 2 with every page resident (no KV pressure: no hit, no miss)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -129,6 +131,8 @@ def make_workload(args, seed: int, n_steps: int):
         kw["capacity"] = args.capacity
     if args.config == 3 and args.decode_per_turn is not None:
         kw["decode_per_turn"] = args.decode_per_turn
+    if args.config == 2 and args.full_residency:
+        kw["resident_tokens"] = 131072
     w = workloads.make(args.config, seed=seed, **kw)
     w.steps = max(w.steps, n_steps)
     steps = list(w.iter_steps(n_steps))
@@ -304,6 +308,8 @@ def config_dict(w, args):
     names = {1: "tiny decode", 2: "mixed-residency decode batch", 3: "multi-turn agentic decode",
              4: "no-residency cold start (prefix reuse)", 5: "max batch with MTP3"}
     share = f", IndexShare {w.G} layers per indexer" if w.G > 1 else ""
+    if w.cfg == 2 and getattr(args, "full_residency", False):
+        share += ", full residency"
     return {"workload": f"{names[w.cfg]}: {w.L} layer(s){share}, {w.R} requests, ctx {int(w.ctx_len[0])}, "
                         f"page {w.S}, row {w.B} B, K={w.K}, P={w.P}, hot {w.C} rows/request",
             "layers": w.L, "layers_per_index": w.G, "requests": w.R, "ctx": int(w.ctx_len[0]), "page": w.S,

@@ -377,6 +377,55 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
     __syncthreads();
   }
 
+  // ---- phase 1a: each id's table entry (from the staged rows when staged), and whether the unit reads
+  // any page that is not resident (or a table entry outside the pool): one barrier with an OR decides
+  // for the whole unit.
+  bool other = false;
+  if (!early) {
+    for (int i = tid; i < n; i += kResolveThreads) {
+      const int id = s_ids[i];
+      if (id >= 0) {
+        int e = s_val[i];
+        if (staged) {
+          const int page = (unsigned)id / S;
+          const int b = s_bt[page];
+          const int h = s_hbt[page];
+          e = b >= 0 ? b : (h < 0 ? -1 : (h >= p.num_host_blocks ? kBadHost : -2 - h));
+          s_val[i] = e;
+        }
+        other |= (e < 0 || e >= p.num_gpu_blocks);
+      }
+    }
+  }
+  const bool fully_resident = !__syncthreads_or(other) && !early;
+
+  if (fully_resident) {
+    // Full residency (Japanese article, "仕組み"): every id is read in place, nothing is hit or copied,
+    // and the hot state is not touched -- the same results as the phases below, without them.
+    int c = 0;
+    for (int i = tid; i < n; i += kResolveThreads) {
+      const int id = s_ids[i];
+      int row = -1;
+      if (id >= 0) {
+        row = s_val[i] * S + (int)((unsigned)id % S);
+        c += idh.find(id) == i;  // distinct ids: first occurrences
+      }
+      rows_g[i] = row;
+      if (msrc_g) msrc_g[i] = row;
+    }
+    c = __reduce_add_sync(kFull, c);
+    if (lane == 0 && c) atomicAdd(&s_cnt[0], c);
+    __syncthreads();
+    if (tid == 0) {
+      int32_t* st = p.out_stats + (int64_t)unit * 4;
+      st[0] = HS_OK;
+      st[1] = s_cnt[0];
+      st[2] = st[3] = 0;
+      p.miss_count[unit] = 0;
+    }
+    return;
+  }
+
   // ---- phase 1b: each slot's token, looked up among the ids: the plan entry of that id learns the
   // lowest slot holding it
   if (!early) {
@@ -393,17 +442,6 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
       if (t >= 0) {
         const int f = idh.find(t);
         if (f >= 0) atomicMin(&s_slot[f], s);
-      }
-    }
-    if (staged) {  // each id's table entry, from the staged rows
-      for (int i = tid; i < n; i += kResolveThreads) {
-        const int id = s_ids[i];
-        if (id >= 0) {
-          const int page = (unsigned)id / S;
-          const int b = s_bt[page];
-          const int h = s_hbt[page];
-          s_val[i] = b >= 0 ? b : (h < 0 ? -1 : (h >= p.num_host_blocks ? kBadHost : -2 - h));
-        }
       }
     }
   }

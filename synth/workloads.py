@@ -221,15 +221,16 @@ def config1(seed: int = 0, steps: int = 8) -> Workload:
                     content_seed=seed, _gen=_fixed_ctx_gen("uniform", "uniform", 0.5))
 
 
-def config2(seed: int = 0, steps: int = 64, R: int = 64) -> Workload:
+def config2(seed: int = 0, steps: int = 64, R: int = 64, resident_tokens: int = 16384) -> Workload:
     """Mixed-residency decode batch: 1 layer, 64 requests, ctx 131072; tail 16384 tokens resident,
-    rest host-only, full host copy; K=2048, hot 4096; keep 80%, recency^-0.7 draws."""
+    rest host-only, full host copy; K=2048, hot 4096; keep 80%, recency^-0.7 draws.
+    resident_tokens = 131072 gives the same batch with full residency (no KV pressure)."""
     L, P, K, C, S, B = 1, 1, 2048, 4096, 64, 656
     ctx = 131072
     max_pages = ctx // S
     lr = _layout_rng(2, seed)
     resident = np.zeros((R, max_pages), bool)
-    resident[:, max_pages - 16384 // S:] = True
+    resident[:, max_pages - resident_tokens // S:] = True
     bt, hot, ngb = _place(R, max_pages, resident, C // S, lr)
     has_host = np.ones((R, max_pages), bool)
     hbt, nhb = _host_place(R, max_pages, has_host, lr)

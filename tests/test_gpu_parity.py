@@ -213,6 +213,19 @@ def test_mixed_residency_decode_full_size(mode):
 
 
 @pytest.mark.parametrize("mode", MODES)
+def test_full_residency_batch(mode):
+    """The mixed batch with every page resident (no KV pressure): every id is read in place, there is
+    no hit and no miss, and the hot state stays empty -- the resolver's full-residency path."""
+    w = workloads.config2(seed=1, steps=4, R=16, resident_tokens=131072)
+    rig = _rig(w, mode=mode)
+    for st in w.iter_steps():
+        _, stats, *_ = rig.step(st)
+        s = stats.cpu().numpy()
+        assert (s[..., 0] == 0).all() and (s[..., 2:] == 0).all() and (s[..., 1] > 0).all()
+    assert (rig.hot.slot_token.cpu().numpy() == -1).all()
+
+
+@pytest.mark.parametrize("mode", MODES)
 def test_cold_start_prefix_reuse_full_size(mode):
     """16 requests reusing a 1,048,576-token host-only prefix, empty hot buffers, 32 steps."""
     w = workloads.config4(seed=0, steps=32)
