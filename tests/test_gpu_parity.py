@@ -407,6 +407,35 @@ def test_largest_shapes_and_shape_limits():
     pool.close()
 
 
+@pytest.mark.parametrize("mode", MODES)
+def test_snapshot_restore_continues_identically(mode):
+    """Checkpoint/resume: the hot state and pool bytes copied out mid-run and copied back give the same
+    continuation (rows, stats, state, gathered bytes), with a fresh workspace full of garbage -- the
+    library keeps nothing between calls and needs nothing from the workspace's previous contents."""
+    w = workloads.config1(seed=5, steps=8)
+    rig = _rig(w, mode=mode, oracle_bytes=True)
+    steps = list(w.iter_steps())
+    for st in steps[:4]:
+        rig.step(st)
+    snap = (rig.hot.slot_token.clone(), rig.hot.slot_stamp.clone(), [g.clone() for g in rig.gpu],
+            rig.o_tok.copy(), rig.o_stamp.copy(), [p.copy() for p in rig.o_pools])
+    first = []
+    for st in steps[4:]:
+        rows, stats, out, *_ = rig.step(st)
+        first.append((rows.clone(), stats.clone(), out.clone()))
+    rig.hot.slot_token.copy_(snap[0])
+    rig.hot.slot_stamp.copy_(snap[1])
+    for g, s_ in zip(rig.gpu, snap[2]):
+        g.copy_(s_)
+    rig.o_tok[...], rig.o_stamp[...] = snap[3], snap[4]
+    for dst, src in zip(rig.o_pools, snap[5]):
+        dst[...] = src
+    rig.ws.fill_(0xA5)
+    for st, (r0, s0, o0) in zip(steps[4:], first):
+        rows, stats, out, *_ = rig.step(st)
+        assert torch.equal(rows, r0) and torch.equal(stats, s0) and torch.equal(out, o0)
+
+
 def test_hot_reset_of_listed_requests_only():
     """hs_hot_reset_requests empties the slots of the listed requests in every index group and leaves
     the others (and entries outside [0, R)) alone."""

@@ -414,3 +414,28 @@ def test_index_share_equals_layers_given_the_same_topk(G, layer_begin, nl):
                     row = shared.hot_row(r, v)
                     assert np.array_equal(shared.pools[l][row * B:(row + 1) * B],
                                           shared.expected_row_bytes(l, r, tok)), (l, r, v)
+
+
+def test_snapshot_and_restore_continue_identically():
+    """Invariant: the resolver's state is the slot tokens, stamps and pool bytes, nothing hidden -- a
+    snapshot taken mid-run and restored into a fresh case continues exactly like the original."""
+    w = workloads.config1(seed=4, steps=8)
+    geo = dict(R=w.R, S=w.S, B=w.B, C=w.C, max_pages=w.max_pages, ctx=w.ctx_len, resident=True, host=True,
+               hot_blocks=w.hot_blocks, num_gpu_blocks=w.num_gpu_blocks, num_host_blocks=w.num_host_blocks,
+               bt=w.block_table, hbt=w.host_block_table, seed=w.content_seed, content_page=w.content_page)
+    a = Case(**geo)
+    steps = list(w.iter_steps())
+    for st in steps[:4]:
+        a.step(st.topk, st.index)
+    snap = (a.tok.copy(), a.stamp.copy(), [p.copy() for p in a.pools])
+    out_a = [a.step(st.topk, st.index) for st in steps[4:]]
+    b = Case(**geo)
+    b.tok[...], b.stamp[...] = snap[0], snap[1]
+    for dst, src in zip(b.pools, snap[2]):
+        dst[...] = src
+    out_b = [b.step(st.topk, st.index) for st in steps[4:]]
+    for (ra, sa), (rb, sb) in zip(out_a, out_b):
+        assert np.array_equal(ra, rb) and np.array_equal(sa, sb)
+    assert np.array_equal(a.tok, b.tok) and np.array_equal(a.stamp, b.stamp)
+    assert all(np.array_equal(x, y) for x, y in zip(a.pools, b.pools))
+    assert sum(int(s[..., 3].sum()) for _, s in out_a) > 0
