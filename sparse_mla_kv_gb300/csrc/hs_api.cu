@@ -203,6 +203,7 @@ hs_status prepare_resolve(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
   sm = hs::resolve_smem_plan_staged(n, C, g.page_size, max_pages, smem_limit);
   sms = hs::sm_count(pool->device);
   if (sms <= 0) return HS_ERR_CUDA;
+  sm.threads = hs::resolve_threads(sm, (int64_t)ng * R, n, sms, pool->device);
 
   p = hs::ResolveParams{};
   p.layer_begin = layer_begin / G;

@@ -76,6 +76,7 @@ struct ResolveSmem {
   size_t stamp, ids, val, cls, slot, hot, idh /* id hash, later radix buffers */, total;
   int32_t id_hash_bits;
   int32_t id_hash_wide;  // 1: 64-bit (id, position) entries; 0: 32-bit position entries
+  int32_t threads;       // threads per resolver CTA (1024, or 512: two units per SM)
   size_t tbl;         // staged block-table + host-table rows (when tbl_pages > 0)
   int32_t tbl_pages;
 };
@@ -90,6 +91,9 @@ ResolveSmem resolve_smem_plan_staged(int64_t n, int64_t C, int64_t S, int64_t ma
 size_t resolve_workspace_bytes(int64_t units, int64_t n, int64_t C);
 // Largest dynamic shared memory a resolver CTA may use on device `dev` (0 on failure).
 size_t resolve_smem_limit(int dev);
+// Threads per resolver CTA for this plan: 512 when two CTAs fit in an SM and the units outnumber the
+// SMs or a unit is small, else 1024.  resolve_smem_limit(dev) must have been called.
+int resolve_threads(const ResolveSmem& sm, int64_t units, int64_t n, int sms, int dev);
 
 // Launchers (return cudaGetLastError() of the launch).
 cudaError_t launch_resolve(const ResolveParams& p, const ResolveSmem& sm, cudaStream_t s);

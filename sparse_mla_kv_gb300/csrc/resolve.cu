@@ -101,7 +101,7 @@ struct IdHash<false> {
   int bits;
   const int32_t* keys;
   __device__ void clear() {
-    for (int i = threadIdx.x; i < (1 << bits); i += kResolveThreads) tab[i] = kEmpty;
+    for (int i = threadIdx.x; i < (1 << bits); i += blockDim.x) tab[i] = kEmpty;
   }
   __device__ void insert_min(int32_t k, int e) { hash_insert_min(tab, bits, keys, k, e); }
   __device__ int find(int32_t k) const { return hash_find(tab, bits, keys, k); }
@@ -113,7 +113,7 @@ struct IdHash<true> {
   int bits;
   static constexpr unsigned long long kVoid = ~0ull;
   __device__ void clear() {
-    for (int i = threadIdx.x; i < (1 << bits); i += kResolveThreads) tab[i] = kVoid;
+    for (int i = threadIdx.x; i < (1 << bits); i += blockDim.x) tab[i] = kVoid;
   }
   __device__ void insert_min(int32_t k, int e) {
     const uint32_t mask = (1u << bits) - 1u;
@@ -140,7 +140,8 @@ struct IdHash<true> {
   }
 };
 
-// Exclusive block-wide scan of two ints at once.  Contains __syncthreads: call uniformly.
+// Exclusive block-wide scan of two ints at once over kW warps.  Contains __syncthreads: call uniformly.
+template <int kW>
 __device__ __forceinline__ void block_scan2(int a, int b, int& ea, int& eb, int& ta, int& tb, int* s_tmp) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int ia = a, ib = b;
@@ -150,24 +151,24 @@ __device__ __forceinline__ void block_scan2(int a, int b, int& ea, int& eb, int&
     const int xb = __shfl_up_sync(kFull, ib, o);
     if (lane >= o) { ia += xa; ib += xb; }
   }
-  if (lane == 31) { s_tmp[warp] = ia; s_tmp[kResolveWarps + warp] = ib; }
+  if (lane == 31) { s_tmp[warp] = ia; s_tmp[kW + warp] = ib; }
   __syncthreads();
   if (warp == 0) {
-    int va = lane < kResolveWarps ? s_tmp[lane] : 0;
-    int vb = lane < kResolveWarps ? s_tmp[kResolveWarps + lane] : 0;
+    int va = lane < kW ? s_tmp[lane] : 0;
+    int vb = lane < kW ? s_tmp[kW + lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int xa = __shfl_up_sync(kFull, va, o);
       const int xb = __shfl_up_sync(kFull, vb, o);
       if (lane >= o) { va += xa; vb += xb; }
     }
-    if (lane < kResolveWarps) { s_tmp[lane] = va; s_tmp[kResolveWarps + lane] = vb; }
+    if (lane < kW) { s_tmp[lane] = va; s_tmp[kW + lane] = vb; }
   }
   __syncthreads();
   ea = (warp ? s_tmp[warp - 1] : 0) + ia - a;
-  eb = (warp ? s_tmp[kResolveWarps + warp - 1] : 0) + ib - b;
-  ta = s_tmp[kResolveWarps - 1];
-  tb = s_tmp[2 * kResolveWarps - 1];
+  eb = (warp ? s_tmp[kW + warp - 1] : 0) + ib - b;
+  ta = s_tmp[kW - 1];
+  tb = s_tmp[2 * kW - 1];
   __syncthreads();
 }
 
@@ -175,6 +176,7 @@ __device__ __forceinline__ void block_scan2(int a, int b, int& ea, int& eb, int&
 // kSortWarps warps own contiguous chunks (per-warp histograms keep the scatter stable); all threads
 // take part in the histogram scan.  Returns the buffer holding the result (a or b).  Call uniformly
 // (contains __syncthreads).
+template <int kT>
 __device__ unsigned short* radix_sort_slots(unsigned short* a, unsigned short* b, int nc, const int32_t* s_stamp,
                                             int lo, int passes, int* hist, int* s_tmp) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -182,11 +184,11 @@ __device__ unsigned short* radix_sort_slots(unsigned short* a, unsigned short* b
   const int w0 = warp < kSortWarps ? min(nc, warp * per_warp) : nc;
   const int w1 = warp < kSortWarps ? min(nc, w0 + per_warp) : nc;
   constexpr int kEntries = kRadixBins * kSortWarps;
-  constexpr int kPerThread = kEntries / kResolveThreads;
-  static_assert(kEntries % kResolveThreads == 0, "histogram split");
+  constexpr int kPerThread = kEntries / kT;
+  static_assert(kEntries % kT == 0, "histogram split");
   for (int pass = 0; pass < passes; ++pass) {
     const int shift = pass * 8;
-    for (int i = tid; i < kEntries; i += kResolveThreads) hist[i] = 0;
+    for (int i = tid; i < kEntries; i += kT) hist[i] = 0;
     __syncthreads();
     for (int e = w0 + lane; e < w1; e += 32) {
       const uint32_t d = ((uint32_t)(s_stamp[a[e]] - lo) >> shift) & 0xFFu;
@@ -198,7 +200,7 @@ __device__ unsigned short* radix_sort_slots(unsigned short* a, unsigned short* b
 #pragma unroll
     for (int k = 0; k < kPerThread; ++k) { loc[k] = hist[tid * kPerThread + k]; sum += loc[k]; }
     int base, dummy_e, total, dummy_t;
-    block_scan2(sum, 0, base, dummy_e, total, dummy_t, s_tmp);
+    block_scan2<kT / 32>(sum, 0, base, dummy_e, total, dummy_t, s_tmp);
 #pragma unroll
     for (int k = 0; k < kPerThread; ++k) { hist[tid * kPerThread + k] = base; base += loc[k]; }
     __syncthreads();
@@ -223,9 +225,10 @@ __device__ unsigned short* radix_sort_slots(unsigned short* a, unsigned short* b
 }
 
 // kS: the page size when it is a compile-time constant (64 in the pages' FP8 MLA setup), else 0.
-// kWide: the id table's entry width (see IdHash).
-template <int kS, bool kWide>
-__global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const ResolveParams p, const ResolveSmem sm) {
+// kWide: the id table's entry width (see IdHash).  kT: threads per CTA -- 1024, or 512 so that two
+// units share an SM when there are more units than SMs or a unit is small.  Results do not depend on it.
+template <int kS, bool kWide, int kT>
+__global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const ResolveParams p, const ResolveSmem sm) {
   extern __shared__ __align__(16) unsigned char smem[];
   int32_t* s_stamp = reinterpret_cast<int32_t*>(smem + sm.stamp);
   int32_t* s_ids = reinterpret_cast<int32_t*>(smem + sm.ids);
@@ -241,7 +244,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
   __shared__ uint32_t s_err;
   __shared__ int s_cnt[3];
   __shared__ int s_lo, s_hi;
-  __shared__ int s_tmp[2 * kResolveWarps];
+  __shared__ int s_tmp[2 * (kT / 32)];
 
   const int tid = threadIdx.x, lane = tid & 31;
   pdl_allow_dependents();   // the following gather / miss-copy kernel may place its CTAs now
@@ -279,18 +282,18 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
   int idr[kIdRegs], tokr[kTokRegs], str[kTokRegs], btr[kTblRegs], hbtr[kTblRegs];
 #pragma unroll
   for (int k = 0; k < kIdRegs; ++k) {
-    const int i = tid + k * kResolveThreads;
+    const int i = tid + k * kT;
     idr[k] = i < n ? ld_early(ids_g + i) : -1;
   }
 #pragma unroll
   for (int k = 0; k < kTokRegs; ++k) {
-    const int s = tid + k * kResolveThreads;
+    const int s = tid + k * kT;
     tokr[k] = s < C ? ld_early(tok_g + s) : -1;
     str[k] = s < C ? ld_early(stamp_g + s) : -1;
   }
 #pragma unroll
   for (int k = 0; k < kTblRegs; ++k) {
-    const int j = tid + k * kResolveThreads;
+    const int j = tid + k * kT;
     btr[k] = (staged && j < sm.tbl_pages) ? ld_early(bt + j) : -1;
     hbtr[k] = (staged && j < sm.tbl_pages) ? ld_early(hbt + j) : -1;
   }
@@ -322,20 +325,20 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
   };
 #pragma unroll
   for (int k = 0; k < kIdRegs; ++k) {
-    const int i = tid + k * kResolveThreads;
+    const int i = tid + k * kT;
     if (i < n) stage_id(i, idr[k]);
   }
-  for (int i = tid + kIdRegs * kResolveThreads; i < n; i += kResolveThreads) stage_id(i, ids_g[i]);
+  for (int i = tid + kIdRegs * kT; i < n; i += kT) stage_id(i, ids_g[i]);
   if (staged) {
 #pragma unroll
     for (int k = 0; k < kTblRegs; ++k) {
-      const int j = tid + k * kResolveThreads;
+      const int j = tid + k * kT;
       if (j < sm.tbl_pages) {
         s_bt[j] = btr[k];
         s_hbt[j] = hbtr[k];
       }
     }
-    for (int j = tid + kTblRegs * kResolveThreads; j < sm.tbl_pages; j += kResolveThreads) {
+    for (int j = tid + kTblRegs * kT; j < sm.tbl_pages; j += kT) {
       s_bt[j] = bt[j];
       s_hbt[j] = hbt[j];
     }
@@ -344,20 +347,20 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
     s_hot[tid] = hotr;
     if (hotr < 0 || hotr >= p.num_gpu_blocks) err |= kErrHot;
   }
-  for (int b = tid + kResolveThreads; b < C / S; b += kResolveThreads) {
+  for (int b = tid + kT; b < C / S; b += kT) {
     const int hb = hot[b];
     s_hot[b] = hb;
     if (hb < 0 || hb >= p.num_gpu_blocks) err |= kErrHot;
   }
 #pragma unroll
   for (int k = 0; k < kTokRegs; ++k) {
-    const int s = tid + k * kResolveThreads;
+    const int s = tid + k * kT;
     if (s < C) {
       s_stamp[s] = str[k];
       if (str[k] > step) err |= kErrStep;
     }
   }
-  for (int s = tid + kTokRegs * kResolveThreads; s < C; s += kResolveThreads) {
+  for (int s = tid + kTokRegs * kT; s < C; s += kT) {
     const int st = stamp_g[s];
     s_stamp[s] = st;
     if (st > step) err |= kErrStep;
@@ -369,7 +372,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
   // ---- phase 1 (narrow id table only): inserts, once every id is staged (a probe reads other keys)
   if constexpr (!kWide) {
     if (!early) {
-      for (int i = tid; i < n; i += kResolveThreads) {
+      for (int i = tid; i < n; i += kT) {
         const int id = s_ids[i];
         if (id >= 0) idh.insert_min(id, i);
       }
@@ -382,7 +385,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
   // for the whole unit.
   bool other = false;
   if (!early) {
-    for (int i = tid; i < n; i += kResolveThreads) {
+    for (int i = tid; i < n; i += kT) {
       const int id = s_ids[i];
       if (id >= 0) {
         int e = s_val[i];
@@ -403,7 +406,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
     // Full residency (Japanese article, "仕組み"): every id is read in place, nothing is hit or copied,
     // and the hot state is not touched -- the same results as the phases below, without them.
     int c = 0;
-    for (int i = tid; i < n; i += kResolveThreads) {
+    for (int i = tid; i < n; i += kT) {
       const int id = s_ids[i];
       int row = -1;
       if (id >= 0) {
@@ -434,10 +437,10 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
       const int t = tokr[k];
       if (t >= 0) {
         const int f = idh.find(t);
-        if (f >= 0) atomicMin(&s_slot[f], tid + k * kResolveThreads);
+        if (f >= 0) atomicMin(&s_slot[f], tid + k * kT);
       }
     }
-    for (int s = tid + kTokRegs * kResolveThreads; s < C; s += kResolveThreads) {
+    for (int s = tid + kTokRegs * kT; s < C; s += kT) {
       const int t = tok_g[s];
       if (t >= 0) {
         const int f = idh.find(t);
@@ -451,7 +454,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
   // repeated ids record their first occurrence
   int c_res = 0, c_hit = 0, c_miss = 0;
   if (!early) {
-    for (int i = tid; i < n; i += kResolveThreads) {
+    for (int i = tid; i < n; i += kT) {
       const int id = s_ids[i];
       uint8_t cls = kNone;
       int val = 0;
@@ -504,9 +507,9 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
     if (s_cnt[1] + s_cnt[2] > 0) e |= kErrTable;
   }
   // per-thread contiguous chunks: positions [i0, i1) and slots [q0, q1)
-  const int ipt = (n + kResolveThreads - 1) / kResolveThreads;
+  const int ipt = (n + kT - 1) / kT;
   const int i0 = min(n, tid * ipt), i1 = min(n, i0 + ipt);
-  const int spt = (C + kResolveThreads - 1) / kResolveThreads;
+  const int spt = (C + kT - 1) / kT;
   const int q0 = min(C, tid * spt), q1 = min(C, q0 + spt);
   int miss_base = 0, cand_base = 0, tot_miss = 0, tot_cand = 0;
   unsigned short* sorted = nullptr;
@@ -523,7 +526,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
     lo = __reduce_min_sync(kFull, lo);
     hi = __reduce_max_sync(kFull, hi);
     if (lane == 0 && lo != INT_MAX) { atomicMin(&s_lo, lo); atomicMax(&s_hi, hi); }
-    block_scan2(my_miss, my_cand, miss_base, cand_base, tot_miss, tot_cand, s_tmp);
+    block_scan2<kT / 32>(my_miss, my_cand, miss_base, cand_base, tot_miss, tot_cand, s_tmp);
     if (tot_miss > tot_cand) e = kErrCapacity;  // uniform: totals are block-wide
     if (e == 0u && tot_miss > 0) {
       // ---- phase 4: victims = candidates in ascending (stamp, slot)
@@ -537,7 +540,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
       __syncthreads();
       const int span = s_hi - s_lo;
       const int bits = span > 0 ? 32 - __clz(span) : 0;
-      sorted = radix_sort_slots(buf_a, buf_b, tot_cand, s_stamp, s_lo, (bits + 7) / 8, hist, s_tmp);
+      sorted = radix_sort_slots<kT>(buf_a, buf_b, tot_cand, s_stamp, s_lo, (bits + 7) / 8, hist, s_tmp);
     }
   }
 
@@ -568,7 +571,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
     }
     __syncthreads();
     // ---- phase 6: emit rows (duplicates read their first occurrence's row)
-    for (int i = tid; i < n; i += kResolveThreads) {
+    for (int i = tid; i < n; i += kT) {
       const int id = s_ids[i];
       int row = -1;
       if (id >= 0) {
@@ -602,7 +605,7 @@ __global__ void __launch_bounds__(kResolveThreads, 1) resolve_kernel(const Resol
                    : (e & kErrTable) ? HS_ERR_TABLE_RANGE
                    : (e & kErrMissing) ? HS_ERR_MISSING_ROW
                    : HS_ERR_CAPACITY;
-    for (int i = tid; i < n; i += kResolveThreads) {
+    for (int i = tid; i < n; i += kT) {
       rows_g[i] = -1;
       if (msrc_g) msrc_g[i] = -1;
     }
@@ -740,42 +743,63 @@ size_t resolve_workspace_bytes(int64_t units, int64_t n, int64_t C) {
   return align16(4 * (size_t)units) + 16 * (size_t)units * (size_t)max_m + align16(4 * (size_t)units * (size_t)n);
 }
 
+namespace {
+
+// every resolver instantiation, in the order (page size 64?, wide table?, 512 threads?) -> index
+const void* resolver_kernels[8] = {
+    (const void*)resolve_kernel<0, false, 1024>, (const void*)resolve_kernel<0, false, 512>,
+    (const void*)resolve_kernel<0, true, 1024>,  (const void*)resolve_kernel<0, true, 512>,
+    (const void*)resolve_kernel<64, false, 1024>, (const void*)resolve_kernel<64, false, 512>,
+    (const void*)resolve_kernel<64, true, 1024>,  (const void*)resolve_kernel<64, true, 512>};
+
+std::atomic<long long> g_smem_limit[64];
+std::atomic<long long> g_smem_per_sm[64];
+std::atomic<int> g_static_smem{0};
+
+}  // namespace
+
 size_t resolve_smem_limit(int dev) {
   // Dynamic shared memory one resolver CTA may use on this device (opt-in maximum minus the
-  // kernel's static shared memory).  Also raises the kernels' attribute to that limit, once.
-  static std::atomic<long long> limit[64];
+  // kernels' static shared memory).  Also raises the kernels' attribute to that limit, once.
   if (dev < 0 || dev >= 64) return 0;
-  long long v = limit[dev].load();
+  long long v = g_smem_limit[dev].load();
   if (v > 0) return (size_t)v;
-  int optin = 0;
+  int optin = 0, per_sm = 0;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
-  const void* kernels[4] = {(const void*)resolve_kernel<64, true>, (const void*)resolve_kernel<64, false>,
-                            (const void*)resolve_kernel<0, true>, (const void*)resolve_kernel<0, false>};
+  if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) return 0;
   size_t st = 0;
-  for (const void* k : kernels) {
+  for (const void* k : resolver_kernels) {
     cudaFuncAttributes fa{};
     if (cudaFuncGetAttributes(&fa, k) != cudaSuccess) return 0;
     if (fa.sharedSizeBytes > st) st = fa.sharedSizeBytes;
   }
   const long long dyn = (long long)optin - (long long)st;
   if (dyn <= 0) return 0;
-  for (const void* k : kernels)
+  for (const void* k : resolver_kernels)
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) != cudaSuccess) return 0;
-  limit[dev].store(dyn);
+  g_static_smem.store((int)st);
+  g_smem_per_sm[dev].store(per_sm);
+  g_smem_limit[dev].store(dyn);
   return (size_t)dyn;
 }
 
+int resolve_threads(const ResolveSmem& sm, int64_t units, int64_t n, int sms, int dev) {
+  // 512 threads when two CTAs fit in one SM's shared memory (with the 1 KB the hardware reserves per
+  // CTA) and either the units outnumber the SMs or a unit is small; 1024 otherwise
+  if (dev < 0 || dev >= 64) return kResolveThreads;
+  const long long per_sm = g_smem_per_sm[dev].load();
+  const long long need = 2 * ((long long)sm.total + g_static_smem.load() + 1024);
+  if (per_sm <= 0 || need > per_sm) return kResolveThreads;
+  return (units > sms || n <= 1024) ? kResolveThreads / 2 : kResolveThreads;
+}
+
 cudaError_t launch_resolve(const ResolveParams& p, const ResolveSmem& sm, cudaStream_t s) {
-  const dim3 grid(p.nl * p.R), block(kResolveThreads);
-  if (p.S == 64) {
-    if (sm.id_hash_wide) resolve_kernel<64, true><<<grid, block, sm.total, s>>>(p, sm);
-    else resolve_kernel<64, false><<<grid, block, sm.total, s>>>(p, sm);
-  } else {
-    if (sm.id_hash_wide) resolve_kernel<0, true><<<grid, block, sm.total, s>>>(p, sm);
-    else resolve_kernel<0, false><<<grid, block, sm.total, s>>>(p, sm);
-  }
+  const int idx = (p.S == 64 ? 4 : 0) + (sm.id_hash_wide ? 2 : 0) + (sm.threads == kResolveThreads / 2 ? 1 : 0);
+  const dim3 grid(p.nl * p.R), block(sm.threads == kResolveThreads / 2 ? kResolveThreads / 2 : kResolveThreads);
+  void* args[] = {(void*)&p, (void*)&sm};
+  cudaError_t e = cudaLaunchKernel(resolver_kernels[idx], grid, block, args, sm.total, s);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_miss_copy(const ResolveParams& p, const LayerPtrs& ptrs, int32_t row_bytes, int sms,
