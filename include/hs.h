@@ -63,7 +63,7 @@ typedef enum {
                               dereferences lies outside the pool; offload: a pair out of range    */
 } hs_status;
 
-/* Limits of this build.  Each launch's shared-memory footprint is also checked (see
+/* Compile-time limits of the library.  Each launch's shared-memory footprint is also checked (see
  * hs_resolve_smem_bytes); a shape that does not fit returns HS_ERR_INVALID_ARG. */
 #define HS_MAX_LAYERS 128
 #define HS_MAX_PAGE_SIZE 1024
