@@ -73,6 +73,9 @@ def parse():
     ap.add_argument("--residency", action="store_true",
                     help="time the host-side residency manager (native and its oracle) on a decode loop under "
                          "KV pressure instead of the GPU path; host only")
+    ap.add_argument("--miss-order", choices=["auto", "on", "off"], default="auto",
+                    help="miss layout handed to the copy warps: auto (the library's default: host-address order "
+                         "for host pools of 16 GiB or more), on (always address order), off (per-unit lists)")
     ap.add_argument("--path", choices=["fused", "split"], default="fused",
                     help="fused: hs_resolve_plan + hs_gather_planned (miss copies inside the gather); "
                          "split: hs_resolve_topk (resolver + miss-copy kernel) + hs_gather_rows")
@@ -343,6 +346,7 @@ def run_ours(args, ws, rank, local):
         sdev.fill_gpu_pool(w, l, gpu[l])
         sdev.fill_host_pool(w, l, host[l], dev)
     pool = hs.Pool(gpu, host)
+    pool.set_miss_order({"auto": hs.MISS_ORDER_AUTO, "on": hs.MISS_ORDER_ON, "off": hs.MISS_ORDER_OFF}[args.miss_order])
     tb = Tables(w, steps)
     bt = torch.from_numpy(tb.bt).to(dev)
     hbt = torch.from_numpy(tb.hbt).to(dev)
@@ -359,6 +363,8 @@ def run_ours(args, ws, rank, local):
     out_rows = res_dev[:n_rows_dev].view(NG, R, P, Kk)
     out_stats = res_dev[n_rows_dev:].view(NG, R, 4)
     ws_buf = hs.alloc_workspace(NG, R, P, Kk, C, dev)
+    miss_order = ("host-address buckets" if hs.miss_order_used(pool, hot, L, R, P, Kk, ws_buf.numel())
+                  else "per-unit lists")
     gout = torch.empty((L, R * P * Kk, B), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -668,7 +674,7 @@ def run_ours(args, ws, rank, local):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": W,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "u8", "data": "synthetic", "config": config_dict(w, args),
+            "dtype": "u8", "data": "synthetic", "config": dict(config_dict(w, args), miss_order=miss_order),
             "gathered_gbs": value * B / 1e9, "roofline": roofline, "step_roofline": step_roof,
             "cpu_baseline": cpu, "cpu_baseline_1thread": cpu1, "e2e": e2e, "gpu_launches": int(launches),
             "clocks": clocks,

@@ -131,12 +131,45 @@ hs_status hs_hot_reset(const hs_pool* pool, const hs_hot_state* hot, int32_t R, 
 hs_status hs_hot_reset_requests(const hs_pool* pool, const hs_hot_state* hot, int32_t R, const int32_t* requests,
                                 int32_t n, hs_stream_t stream);
 
-/* Bytes of caller-owned device workspace that hs_resolve_topk and hs_resolve_gather need for this
- * shape (per-unit miss lists handed from the resolver kernel to the miss-copy kernel, or per-position
- * host sources handed to the fused gather).  nl counts resolver units per request: layers when
- * G = 1, index groups (layers / G) under IndexShare; passing the layer count there over-sizes the
- * workspace, which is harmless.  0 on a bad shape. */
+/* Bytes of caller-owned device workspace for hs_resolve_topk and hs_resolve_gather with this shape
+ * (per-unit miss lists handed from the resolver kernel to the miss-copy kernel, per-position host
+ * sources handed to the fused gather), including the room the address-ordered miss layout needs
+ * (hs_pool_set_miss_order).  nl counts resolver units per request: layers when G = 1, index groups
+ * (layers / G) under IndexShare; passing the layer count there over-sizes the workspace, which is
+ * harmless.  0 on a bad shape. */
 size_t hs_resolve_workspace_bytes(int32_t nl, int32_t R, int32_t P, int32_t K, int32_t capacity);
+
+/* The smallest workspace resolve calls accept for this shape: the same without the ordered layout's
+ * room (calls given less than hs_resolve_workspace_bytes use per-unit miss lists).  0 on a bad shape. */
+size_t hs_resolve_workspace_bytes_min(int32_t nl, int32_t R, int32_t P, int32_t K, int32_t capacity);
+
+/* How resolve calls hand a step's misses to the kernels that copy them.  Results are identical in
+ * every mode; only the order of the host reads differs.
+ *   HS_MISS_ORDER_AUTO (default)  address-ordered when the host pools of the call's layers hold at
+ *                                 least 16 GiB together and the workspace has room for it;
+ *   HS_MISS_ORDER_OFF             per-unit lists, copied unit by unit;
+ *   HS_MISS_ORDER_ON              address-ordered whenever the workspace has room for it.
+ * Address-ordered: the resolver files each index group's misses into 256 buckets by host row range,
+ * and the copy warps take them bucket by bucket, so that the host rows in flight at any moment lie in
+ * a few neighbouring ranges of the pool.  The pages copy single rows from pinned host memory
+ * ("vLLM GLM 5.3 Optimizations: Hybrid HiSparse Offloading", "Technical Implementation of Hybrid
+ * HiSparse") and say nothing of their order; this is the library's choice.  Zero-copy reads spread
+ * over tens of GB of host memory are bound by the device's address translation for host memory, not
+ * by the link, and the same rows read in address order arrive several times faster.  It costs one
+ * more small kernel per resolve call and workspace of 2 x R x min(P*K, capacity) x 16 bytes per index
+ * group.  A plan and its hs_gather_planned must see the same mode and workspace size.  Set it
+ * between calls, not while another thread is calling with the same pool.  HS_ERR_INVALID_ARG for an
+ * unknown mode. */
+#define HS_MISS_ORDER_AUTO 0
+#define HS_MISS_ORDER_OFF 1
+#define HS_MISS_ORDER_ON 2
+hs_status hs_pool_set_miss_order(hs_pool* pool, int32_t mode);
+
+/* 1 if a resolve call on layers [layer_begin, layer_begin + nl) with this shape, hot state and
+ * workspace size uses the address-ordered miss layout, 0 if it uses per-unit lists, -1 on bad
+ * arguments. */
+int32_t hs_resolve_miss_order(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P, int32_t K,
+                              const hs_hot_state* hot, size_t workspace_bytes);
 
 /* Dynamic shared memory one resolver CTA needs for this shape, or 0 if the shape exceeds a limit.
  * Resolve calls reject shapes whose footprint exceeds the device's per-block opt-in maximum. */
@@ -164,12 +197,14 @@ size_t hs_resolve_smem_bytes(int32_t P, int32_t K, int32_t capacity, int32_t pag
  *   out_rows         int32 [nl/G][R][P][K]; pool row per id (duplicates share the row; padding -1);
  *                    the same row id serves every layer of the group.
  *   out_stats        int32 [nl/G][R][4] = {status, resident, hits, misses}, counted over the plan.
- *   workspace        device scratch of >= hs_resolve_workspace_bytes(...) bytes, 16-byte aligned;
- *                    its contents need no initialisation and are garbage after the call.
+ *   workspace        device scratch of >= hs_resolve_workspace_bytes_min(...) bytes (with
+ *                    hs_resolve_workspace_bytes(...) the ordered miss layout is available), 16-byte
+ *                    aligned; its contents need no initialisation and are garbage after the call.
  * A unit with a data error leaves its hot state and pool bytes unchanged, sets out_rows to -1 and
  * out_stats to {code, 0, 0, 0}; other units proceed.  Calling again with the same ids and step
  * returns the same rows with 0 misses (the replayable plan used by speculative decoding).
- * Launches two kernels on `stream` (resolve, then the miss copy of every layer).  Concurrent calls
+ * Launches two kernels on `stream` (resolve, then the miss copy of every layer), and one more small
+ * kernel before them with the ordered miss layout.  Concurrent calls
  * that share hot state or workspace must be ordered by the caller. */
 hs_status hs_resolve_topk(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P,
                           int32_t K, const int32_t* topk_ids, const int32_t* block_table,
@@ -180,10 +215,11 @@ hs_status hs_resolve_topk(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
 /* Resolve and gather in one call: the same results as hs_resolve_topk followed by a gather of
  * out_rows for every layer -- out_rows, out_stats, hot state and pool bytes identical, and
  * out[l][(r*P + p)*K + k] = layer layer_begin + l's row of topk_ids[l/G][r][p][k], for l < nl.  The miss copy is fused
- * into the gather: the resolver marks each miss position with its host row, and the gather reads
- * those rows straight from the pinned host pool (storing the first occurrence of each into its hot
- * slot) while resident and hit rows come from HBM in the same launch, so host-link and HBM traffic
- * overlap instead of running back to back.  The consumer then reads hot rows as ordinary pool rows
+ * into the gather: the resolver lists each missed id once with its host row and links the id's
+ * repeated positions (other query positions of a multi-position plan), and the gather reads each
+ * such row once from the pinned host pool and stores it into its hot slot and into every position
+ * of the id, while resident and hit rows come from HBM in the same launch, so host-link and HBM
+ * traffic overlap instead of running back to back.  The consumer then reads hot rows as ordinary pool rows
  * (Japanese article, section "仕組み": the sparse MLA kernel sees hot pages as normal pages).
  * Equivalent to hs_resolve_plan followed by hs_gather_planned on the same stream.
  *   out        device [nl][R*P*K][row_bytes] bytes, 16-byte aligned.
@@ -238,9 +274,9 @@ hs_status hs_offload_pages(const hs_pool* pool, const int32_t* gpu_blocks, const
  * convenience.  Same arguments and results as hs_resolve_topk, minus the workspace: the scratch is a
  * static __device__ array of HS_STATIC_SCRATCH_BYTES inside the library, held by every GPU that loads
  * the library until the process exits.  No call allocates anything.
- *   - Returns HS_ERR_INVALID_ARG when hs_resolve_workspace_bytes(nl, R, P, K, capacity) exceeds
+ *   - Returns HS_ERR_INVALID_ARG when hs_resolve_workspace_bytes_min(nl, R, P, K, capacity) exceeds
  *     HS_STATIC_SCRATCH_BYTES (about 340 units of the MTP3 shape P*K = 8192, C = 4096, or about 800
- *     units of K = 2048, C = 4096).
+ *     units of K = 2048, C = 4096).  The ordered miss layout is used only where it fits too.
  *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress, with
  *     that device current); make that first call before any stream capture.
  *   - Every call shares the one array and it keeps the last call's contents (nothing in it needs to

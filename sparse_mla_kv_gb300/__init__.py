@@ -23,6 +23,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libhs.so")
 
 HS_OK = 0
+MISS_ORDER_AUTO, MISS_ORDER_OFF, MISS_ORDER_ON = 0, 1, 2
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "ID_RANGE", 3: "MISSING_ROW", 4: "CAPACITY", 5: "STEP_ORDER",
                 6: "CUDA", 7: "TIMEOUT", 8: "TABLE_RANGE"}
 MAX_LAYERS = 128
@@ -72,6 +73,12 @@ def lib():
         L.hs_hot_reset_requests.argtypes = [p, ctypes.POINTER(HotStateC), i32, p, i32, p]
         L.hs_resolve_workspace_bytes.restype = sz
         L.hs_resolve_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+        L.hs_resolve_workspace_bytes_min.restype = sz
+        L.hs_resolve_workspace_bytes_min.argtypes = [i32, i32, i32, i32, i32]
+        L.hs_pool_set_miss_order.restype = i32
+        L.hs_pool_set_miss_order.argtypes = [p, i32]
+        L.hs_resolve_miss_order.restype = i32
+        L.hs_resolve_miss_order.argtypes = [p, i32, i32, i32, i32, i32, ctypes.POINTER(HotStateC), sz]
         L.hs_resolve_smem_bytes.restype = sz
         L.hs_resolve_smem_bytes.argtypes = [i32, i32, i32, i32]
         L.hs_resolve_topk.restype = i32
@@ -164,6 +171,10 @@ class Pool:
             _check(lib().hs_pool_create(ctypes.byref(desc), ctypes.byref(h)), "hs_pool_create")
         self.handle = h
 
+    def set_miss_order(self, mode: int) -> None:
+        """MISS_ORDER_AUTO (default), MISS_ORDER_OFF or MISS_ORDER_ON: see hs_pool_set_miss_order."""
+        _check(lib().hs_pool_set_miss_order(self.handle, int(mode)), "hs_pool_set_miss_order")
+
     def close(self) -> None:
         if getattr(self, "handle", None) is not None and self.handle.value:
             lib().hs_pool_destroy(self.handle)
@@ -221,6 +232,20 @@ def hot_reset_requests(pool: Pool, hot: HotState, requests: torch.Tensor, stream
 
 def resolve_workspace_bytes(nl: int, R: int, P: int, K: int, capacity: int) -> int:
     return int(lib().hs_resolve_workspace_bytes(nl, R, P, K, capacity))
+
+
+def resolve_workspace_bytes_min(nl: int, R: int, P: int, K: int, capacity: int) -> int:
+    return int(lib().hs_resolve_workspace_bytes_min(nl, R, P, K, capacity))
+
+
+def miss_order_used(pool: Pool, hot: HotState, nl: int, R: int, P: int, K: int, workspace_bytes: int,
+                    layer_begin: int = 0) -> bool:
+    """Whether a resolve call of this shape files its misses in host address order."""
+    v = int(lib().hs_resolve_miss_order(pool.handle, layer_begin, nl, R, P, K, ctypes.byref(hot.c),
+                                        int(workspace_bytes)))
+    if v < 0:
+        raise ValueError("bad arguments to hs_resolve_miss_order")
+    return bool(v)
 
 
 def resolve_smem_bytes(P: int, K: int, capacity: int, page_size: int = 64) -> int:

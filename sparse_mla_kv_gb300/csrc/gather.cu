@@ -13,13 +13,12 @@
 //                      kGatherUnroll loads in flight.
 // gather_fused_kernel  the same gather for the rows a resolve plan left in the pool (resident and
 //                      hit rows), run by 7 of every 8 warps, while the other warp of each CTA copies
-//                      the plan's misses: one read of each host row over the host link, stored both
-//                      into its hot slot and into the output.  Host-link and HBM traffic overlap in
+//                      the plan's misses: one read of each host row over the host link, stored into
+//                      its hot slot and into every output position of its id.  Host-link and HBM traffic overlap in
 //                      one launch, and HBM warps never wait on host latency.  Under IndexShare
 //                      the G layers of an index group read the same plan (rows, sources, miss
-//                      list); each layer's CTAs copy the misses into that layer's tensor.
-#include <climits>
-
+//                      list); each layer's CTAs copy the misses into that layer's tensor.  With the
+//                      ordered miss layout the miss warps take the misses in host-row-range order.
 #include "hs_internal.cuh"
 
 namespace hs {
@@ -68,11 +67,79 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const LayerPtrs 
   if (bad && status) *status = HS_ERR_ID_RANGE;
 }
 
+constexpr int kRepeatRegs = 3;  // repeat positions per entry followed before the stores (P - 1 for MTP3)
+
+// Copies the rows of up to kMissRowsPerItem miss entries (lane j < nrows holds entry j) from the
+// host pool into their hot slots, their output positions and the output positions of their repeats
+// (the chain that starts at the entry's fourth field and continues through lmsrc, the plan's
+// per-position sources).  The host loads are issued first; the first kRepeatRegs links of each chain
+// are read while they are in flight, then everything is stored.  n: positions per request.
+template <int CPR>
+__device__ __forceinline__ void copy_miss_item(const uint8_t* __restrict__ host, uint8_t* __restrict__ pool,
+                                               uint8_t* __restrict__ lout, const int32_t* __restrict__ lmsrc,
+                                               int n, int4 ent, int nrows, int row_bytes) {
+  constexpr int kU = CPR ? (kMissRowsPerItem * CPR + 31) / 32 : 4;
+  const int cpr = CPR ? CPR : (row_bytes >> 4);
+  const int lane = threadIdx.x & 31;
+  const int total = nrows * cpr;
+  const int rq = lane < nrows ? ent.z / n : 0;  // the entry's request
+  for (int f0 = 0; f0 < total; f0 += 32 * kU) {
+    uint4 v[kU];
+#pragma unroll
+    for (int k = 0; k < kU; ++k) {
+      const int f = f0 + k * 32 + lane;
+      const int rr = f < total ? f / cpr : 0;
+      const int src = __shfl_sync(kFull, ent.x, rr);
+      if (f < total) v[k] = __ldcg(reinterpret_cast<const uint4*>(host + (int64_t)src * row_bytes) + (f - rr * cpr));
+    }
+    int d = lane < nrows ? ent.w : -1;
+    int rep[kRepeatRegs];
+#pragma unroll
+    for (int t = 0; t < kRepeatRegs; ++t) {
+      rep[t] = d;
+      if (d >= 0) d = -3 - __ldcg(lmsrc + (int64_t)rq * n + d);
+    }
+#pragma unroll
+    for (int k = 0; k < kU; ++k) {
+      const int f = f0 + k * 32 + lane;
+      const bool ok = f < total;
+      const int rr = ok ? f / cpr : 0;
+      const int64_t cc16 = (int64_t)(f - rr * cpr) * 16;
+      const int dst = __shfl_sync(kFull, ent.y, rr);
+      const int pos = __shfl_sync(kFull, ent.z, rr);
+      const int q = __shfl_sync(kFull, rq, rr);
+      int rp[kRepeatRegs];
+#pragma unroll
+      for (int t = 0; t < kRepeatRegs; ++t) rp[t] = __shfl_sync(kFull, rep[t], rr);
+      if (ok) {
+        *reinterpret_cast<uint4*>(pool + (int64_t)dst * row_bytes + cc16) = v[k];
+        *reinterpret_cast<uint4*>(lout + (int64_t)pos * row_bytes + cc16) = v[k];
+#pragma unroll
+        for (int t = 0; t < kRepeatRegs; ++t)
+          if (rp[t] >= 0) *reinterpret_cast<uint4*>(lout + ((int64_t)q * n + rp[t]) * row_bytes + cc16) = v[k];
+      }
+    }
+    while (__any_sync(kFull, d >= 0)) {  // longer chains: one link per round
+#pragma unroll
+      for (int k = 0; k < kU; ++k) {
+        const int f = f0 + k * 32 + lane;
+        const int rr = f < total ? f / cpr : 0;
+        const int q = __shfl_sync(kFull, rq, rr);
+        const int dd = __shfl_sync(kFull, d, rr);
+        if (f < total && dd >= 0)
+          *reinterpret_cast<uint4*>(lout + ((int64_t)q * n + dd) * row_bytes + (int64_t)(f - rr * cpr) * 16) = v[k];
+      }
+      if (d >= 0) d = -3 - __ldcg(lmsrc + (int64_t)rq * n + d);
+    }
+  }
+}
+
 template <int CPR>
 __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
     const LayerPtrs ptrs, int32_t layer_begin, int32_t group, int32_t R, int32_t n, int32_t max_m,
     const int32_t* __restrict__ rows, const int32_t* __restrict__ miss_count, const int4* __restrict__ miss_list,
-    const int32_t* __restrict__ msrc, uint8_t* __restrict__ out, int32_t row_bytes, int64_t num_rows) {
+    const MissOrder ord, const int32_t* __restrict__ msrc, uint8_t* __restrict__ out, int32_t row_bytes,
+    int64_t num_rows) {
   pdl_wait_prerequisites();   // the resolve plan (rows, sources, miss lists) must be complete and visible
   const int cpr = CPR ? CPR : (row_bytes >> 4);
   const int lr = blockIdx.y;
@@ -82,13 +149,31 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
   const uint8_t* __restrict__ host = ptrs.host[layer_begin + lr];
   const int64_t per_layer = (int64_t)R * n;
   uint8_t* __restrict__ lout = out + (int64_t)lr * per_layer * row_bytes;
+  const int32_t* __restrict__ lmsrc = msrc + (int64_t)pu * per_layer;
 
   if (warp < kMissWarps) {
-    // ---- miss warps: items (request, chunk of kMissRowsPerItem misses) of this layer, numbered
-    // chunk-major so live items are the low numbers; lane j of miss-warp w tests item w + j * nmw.
-    constexpr int kU = CPR ? (kMissRowsPerItem * CPR + 31) / 32 : 4;
     const int64_t mw = (int64_t)blockIdx.x * kMissWarps + warp;
     const int64_t nmw = (int64_t)gridDim.x * kMissWarps;
+    if (ord.cnt) {
+      // ---- ordered layout: the layer's miss warps take its group's items in bucket order (warp w:
+      // items w, w + nmw, ...), so the host rows in flight lie in neighbouring ranges
+      __shared__ MissItems mi;
+      mi.load(ord, pu);
+      const int4* bk = ord.buckets + (int64_t)pu * kMissBuckets * ord.cap;
+      const int4* ovl = ord.overflow + (int64_t)pu * ord.per_group;
+      for (int32_t i = (int32_t)mw; i < mi.items; i += (int32_t)nmw) {
+        int64_t start;
+        bool in_ov;
+        int nrows;
+        mi.locate(ord, i, start, in_ov, nrows);
+        int4 ent = make_int4(0, 0, 0, 0);
+        if (lane < nrows) ent = (in_ov ? ovl : bk)[start + lane];
+        copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes);
+      }
+      return;
+    }
+    // ---- miss warps: items (request, chunk of kMissRowsPerItem misses) of this layer, numbered
+    // chunk-major so live items are the low numbers; lane j of miss-warp w tests item w + j * nmw.
     const int items_per_unit = (max_m + kMissRowsPerItem - 1) / kMissRowsPerItem;
     const int64_t items = (int64_t)R * items_per_unit;
     for (int64_t base = mw; base < items; base += nmw * 32) {
@@ -112,44 +197,15 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
         const int nrows = min(kMissRowsPerItem, c - r0);
         int4 ent = make_int4(0, 0, 0, 0);
         if (lane < nrows) ent = miss_list[((int64_t)pu * R + rq) * max_m + r0 + lane];
-        const int total = nrows * cpr;
-        for (int f0 = 0; f0 < total; f0 += 32 * kU) {
-          uint4 v[kU];
-          int64_t pool_off[kU], out_off[kU];
-#pragma unroll
-          for (int k = 0; k < kU; ++k) {
-            const int f = f0 + k * 32 + lane;
-            const bool ok = f < total;
-            const int rr = ok ? f / cpr : 0;
-            const int cc = f - rr * cpr;
-            const int src = __shfl_sync(kFull, ent.x, rr);
-            const int dst = __shfl_sync(kFull, ent.y, rr);
-            const int pos = __shfl_sync(kFull, ent.z, rr);
-            pool_off[k] = -1;
-            out_off[k] = 0;
-            if (ok) {
-              v[k] = __ldcg(reinterpret_cast<const uint4*>(host + (int64_t)src * row_bytes) + cc);
-              pool_off[k] = (int64_t)dst * row_bytes + (int64_t)cc * 16;
-              out_off[k] = (int64_t)pos * row_bytes + (int64_t)cc * 16;
-            }
-          }
-#pragma unroll
-          for (int k = 0; k < kU; ++k) {
-            if (pool_off[k] >= 0) {
-              *reinterpret_cast<uint4*>(pool + pool_off[k]) = v[k];
-              *reinterpret_cast<uint4*>(lout + out_off[k]) = v[k];
-            }
-          }
-        }
+        copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes);
       }
     }
     return;
   }
 
-  // ---- HBM warps: every position the miss warps do not own (resident rows, hit rows, padding,
-  // and repeated positions of a miss, which read the host row again); one source word per position
+  // ---- HBM warps: every position the miss warps do not own (resident rows, hit rows, padding);
+  // one source word per position
   constexpr int kHbmThreads = kGatherThreads - kMissWarps * 32;
-  const int32_t* __restrict__ lmsrc = msrc + (int64_t)pu * per_layer;
   uint4* __restrict__ lout4 = reinterpret_cast<uint4*>(lout);
   const int64_t total = per_layer * cpr;
   const int64_t stride = (int64_t)gridDim.x * kHbmThreads;
@@ -171,10 +227,7 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
           st[k] = true;
         } else if (ms == -1) {
           st[k] = true;
-        } else if (ms != INT_MIN) {
-          v[k] = __ldcg(reinterpret_cast<const uint4*>(host + (int64_t)(-2 - ms) * row_bytes) + j);
-          st[k] = true;
-        }
+        }  // <= -2: a missed id's position, stored by the miss warps
       }
     }
 #pragma unroll
@@ -226,8 +279,8 @@ cudaError_t launch_gather(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl
 
 cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, int32_t group, int32_t R,
                                 int32_t n, int32_t max_m, const int32_t* rows, const int32_t* miss_count,
-                                const int4* miss_list, const int32_t* msrc, uint8_t* out, int32_t row_bytes,
-                                int64_t num_rows, int sms, cudaStream_t s) {
+                                const int4* miss_list, const MissOrder& ord, const int32_t* msrc, uint8_t* out,
+                                int32_t row_bytes, int64_t num_rows, int sms, cudaStream_t s) {
   int* occ = g_occ_fused;
   const bool k41 = row_bytes == 656;
   auto kern = k41 ? gather_fused_kernel<41> : gather_fused_kernel<0>;
@@ -240,8 +293,18 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
                             kMissWarps;
   const dim3 grid = wave_grid(sms, resident_blocks(kern, &occ[k41 ? 0 : 1]), want_hbm > want_miss ? want_hbm : want_miss,
                               nl);
-  cudaError_t e = launch_dependent(kern, grid, dim3(kGatherThreads), 0, s, ptrs, layer_begin, group, R, n, max_m,
-                                   rows, miss_count, miss_list, msrc, out, row_bytes, num_rows);
+  // With the ordered layout (large host pools) the gather is not launched early: CTAs placed while
+  // the resolver still runs made the whole gather's host reads slower there (measured: agentic
+  // decode over a 29 GB pool, 684 us per step against 333 us with the launch held back).
+  cudaError_t e;
+  if (ord.cnt) {
+    kern<<<grid, kGatherThreads, 0, s>>>(ptrs, layer_begin, group, R, n, max_m, rows, miss_count, miss_list, ord, msrc,
+                                         out, row_bytes, num_rows);
+    e = cudaGetLastError();
+  } else {
+    e = launch_dependent(kern, grid, dim3(kGatherThreads), 0, s, ptrs, layer_begin, group, R, n, max_m, rows,
+                         miss_count, miss_list, ord, msrc, out, row_bytes, num_rows);
+  }
   if (e != cudaSuccess) return e;
   count_launch();
   return cudaGetLastError();

@@ -11,6 +11,7 @@ struct hs_pool {
   hs::PoolGeom g;
   hs::LayerPtrs ptrs;
   int device;
+  int32_t miss_order;  // HS_MISS_ORDER_*
 };
 
 namespace hs {
@@ -38,6 +39,26 @@ int32_t layers_per_index(const hs_hot_state* hot, const hs::PoolGeom& g) {
 }
 
 hs_status cuda_status(cudaError_t e) { return e == cudaSuccess ? HS_OK : HS_ERR_CUDA; }
+
+// Whether a resolve call on nl layers (ng = nl / G index groups) files its misses in address order.
+// Both halves of a planned call decide it alike.
+bool use_miss_order(const hs_pool* pool, int32_t nl, int64_t ng, int32_t R, int64_t n, int32_t C,
+                    size_t workspace_bytes) {
+  const PoolGeom& g = pool->g;
+  if (pool->miss_order == HS_MISS_ORDER_OFF || g.num_host_blocks == 0 || n == 0 || ng * R == 0) return false;
+  const int64_t max_m = n < C ? n : C;
+  if (2 * (int64_t)R * max_m > INT32_MAX) return false;
+  if (workspace_bytes < resolve_workspace_bytes_ordered(ng, R, n, C)) return false;
+  const int64_t host_bytes = (int64_t)g.num_host_blocks * g.page_size * g.row_bytes * nl;
+  return pool->miss_order == HS_MISS_ORDER_ON || host_bytes >= kMissOrderAutoBytes;
+}
+
+// The ordered layout's pointers within `workspace`, or cnt = nullptr for per-unit lists.
+MissOrder call_miss_order(const hs_pool* pool, int32_t nl, int64_t ng, int32_t R, int64_t n, int32_t C,
+                          void* workspace, size_t workspace_bytes) {
+  if (!use_miss_order(pool, nl, ng, R, n, C, workspace_bytes)) return MissOrder{};
+  return miss_order_layout(workspace, ng, R, n, C, (int64_t)pool->g.num_host_blocks * pool->g.page_size);
+}
 
 }  // namespace
 
@@ -123,6 +144,12 @@ hs_status hs_pool_create(const hs_pool_desc* d, hs_pool** out) {
 
 void hs_pool_destroy(hs_pool* p) { delete p; }
 
+hs_status hs_pool_set_miss_order(hs_pool* pool, int32_t mode) {
+  if (!pool || mode < HS_MISS_ORDER_AUTO || mode > HS_MISS_ORDER_ON) return HS_ERR_INVALID_ARG;
+  pool->miss_order = mode;
+  return HS_OK;
+}
+
 hs_status hs_hot_reset(const hs_pool* pool, const hs_hot_state* hot, int32_t R, hs_stream_t stream) {
   if (!pool || !hot || R < 0) return HS_ERR_INVALID_ARG;
   if (hot->capacity < pool->g.page_size || hot->capacity > HS_MAX_CAPACITY || hot->capacity % pool->g.page_size)
@@ -153,11 +180,26 @@ hs_status hs_hot_reset_requests(const hs_pool* pool, const hs_hot_state* hot, in
                                                    hot->capacity, requests, n, sms, stream));
 }
 
-size_t hs_resolve_workspace_bytes(int32_t nl, int32_t R, int32_t P, int32_t K, int32_t capacity) {
+size_t hs_resolve_workspace_bytes_min(int32_t nl, int32_t R, int32_t P, int32_t K, int32_t capacity) {
   if (nl < 0 || R < 0 || P < 1 || K < 0 || capacity < 1) return 0;
   const int64_t n = (int64_t)P * K;
   if (n > HS_MAX_PLAN || capacity > HS_MAX_CAPACITY) return 0;
   return hs::resolve_workspace_bytes((int64_t)nl * R, n, capacity);
+}
+
+size_t hs_resolve_workspace_bytes(int32_t nl, int32_t R, int32_t P, int32_t K, int32_t capacity) {
+  if (hs_resolve_workspace_bytes_min(nl, R, P, K, capacity) == 0) return 0;
+  return hs::resolve_workspace_bytes_ordered(nl, R, (int64_t)P * K, capacity);
+}
+
+int32_t hs_resolve_miss_order(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P, int32_t K,
+                              const hs_hot_state* hot, size_t workspace_bytes) {
+  if (!pool || !hot || layer_begin < 0 || nl < 0 || (int64_t)layer_begin + nl > pool->g.num_layers || R < 0 ||
+      P < 1 || K < 0 || hot->capacity < 1 || hot->capacity > HS_MAX_CAPACITY || (int64_t)P * K > HS_MAX_PLAN)
+    return -1;
+  const int32_t G = hs::layers_per_index(hot, pool->g);
+  if (G == 0 || layer_begin % G || nl % G) return -1;
+  return hs::use_miss_order(pool, nl, nl / G, R, (int64_t)P * K, hot->capacity, workspace_bytes) ? 1 : 0;
 }
 
 size_t hs_resolve_smem_bytes(int32_t P, int32_t K, int32_t capacity, int32_t page_size) {
@@ -230,6 +272,7 @@ hs_status prepare_resolve(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
   p.out_stats = out_stats;
   p.miss_count = static_cast<int32_t*>(workspace);
   p.miss_list = reinterpret_cast<int4*>(static_cast<uint8_t*>(workspace) + hs::ws_counts_bytes((int64_t)ng * R));
+  p.ord = hs::call_miss_order(pool, nl, ng, R, n, C, workspace, workspace_bytes);
   p.msrc = nullptr;
   return HS_OK;
 }
@@ -296,9 +339,11 @@ hs_status hs_gather_planned(const hs_pool* pool, int32_t layer_begin, int32_t nl
   if (sms <= 0) return HS_ERR_CUDA;
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
   const int32_t max_m = (int32_t)(n < capacity ? n : capacity);
+  const hs::MissOrder ord =
+      hs::call_miss_order(pool, nl, nl / G, R, n, capacity, const_cast<void*>(workspace), workspace_bytes);
   return hs::cuda_status(hs::launch_gather_fused(
       pool->ptrs, layer_begin, nl, G, R, (int32_t)n, max_m, out_rows, reinterpret_cast<const int32_t*>(ws),
-      reinterpret_cast<const int4*>(ws + hs::ws_counts_bytes(units)),
+      reinterpret_cast<const int4*>(ws + hs::ws_counts_bytes(units)), ord,
       reinterpret_cast<const int32_t*>(ws + hs::ws_msrc_offset(units, n, capacity)), static_cast<uint8_t*>(out),
       g.row_bytes, (int64_t)g.num_gpu_blocks * g.page_size, sms, stream));
 }

@@ -26,14 +26,52 @@ constexpr int kResolveThreads = 1024;
 constexpr int kResolveWarps = kResolveThreads / 32;
 constexpr int kRadixBins = 256;
 constexpr int kSortWarps = 8;  // warps that own chunks in the victim sort
-// Miss-copy work item: this many consecutive misses of one unit.
+// Miss-copy work item: this many consecutive misses of one unit (or of one bucket, below).
 constexpr int kMissRowsPerItem = 4;
+
+// Address-ordered miss layout.  Misses scattered over tens of GB of pinned host memory are limited
+// by the device's address translation for host memory, not by the link: a step whose in-flight
+// reads span the whole pool misses the translation caches on nearly every row.  In this layout the
+// resolver files each miss of an index group into one of kMissBuckets buckets by host row range
+// (bucket = host row >> shift), and the copy warps take consecutive items in bucket order, so the
+// rows in flight at any moment lie in a few neighbouring ranges.  Results do not depend on it: every
+// miss writes its own hot slot and output row.
+constexpr int kMissBuckets = 256;
+constexpr int kBucketsPerLane = kMissBuckets / 32;
+struct MissOrder {
+  int32_t* cnt;       // [groups][kMissBuckets + 1]: entries filed per bucket, then the overflow count;
+                      // zeroed before the resolver runs.  nullptr: per-unit lists instead.
+  int4* buckets;      // [groups][kMissBuckets][cap]
+  int4* overflow;     // [groups][per_group]: misses whose bucket was full (in no particular order)
+  int32_t shift;      // bucket of host row h: h >> shift
+  int32_t cap;        // entries per bucket
+  int32_t per_group;  // misses an index group can have: R * max_m
+};
+// Bucket capacity: twice the even share, so that only strongly skewed steps overflow.
+inline int32_t miss_bucket_cap(int64_t per_group) {
+  return (int32_t)((2 * per_group + kMissBuckets - 1) / kMissBuckets);
+}
+// Smallest shift that maps every host row below num_host_rows into the buckets.
+inline int32_t miss_bucket_shift(int64_t num_host_rows) {
+  int32_t s = 0;
+  while (num_host_rows > 0 && ((num_host_rows - 1) >> s) >= kMissBuckets) ++s;
+  return s;
+}
+// Host pools at least this large (over the layers of a call) use the ordered layout by default.
+constexpr int64_t kMissOrderAutoBytes = int64_t(16) << 30;
 // Workspace layout shared by the resolve entry points.
 inline size_t ws_counts_bytes(int64_t units) { return (4 * (size_t)units + 15) & ~size_t(15); }
 inline size_t ws_msrc_offset(int64_t units, int64_t n, int64_t C) {
   const int64_t max_m = n < C ? n : C;
   return ws_counts_bytes(units) + 16 * (size_t)units * (size_t)max_m;
 }
+// The ordered layout's extra areas follow the per-unit layout (resolve_workspace_bytes): bucket
+// counters, then the buckets; its overflow lists reuse the per-unit miss lists (group g's at unit
+// (g, 0)).  resolve_workspace_bytes_ordered is the whole size with them.
+inline size_t ws_order_cnt_bytes(int64_t groups) { return (4 * (size_t)groups * (kMissBuckets + 1) + 15) & ~size_t(15); }
+size_t resolve_workspace_bytes_ordered(int64_t groups, int64_t R, int64_t n, int64_t C);
+// The ordered layout for a call, or cnt = nullptr when the per-unit layout is used.
+MissOrder miss_order_layout(void* workspace, int64_t groups, int64_t R, int64_t n, int64_t C, int64_t num_host_rows);
 
 // Error bits collected inside one resolver CTA; the reported code follows the precedence
 // STEP_ORDER > ID_RANGE > TABLE_RANGE > MISSING_ROW > CAPACITY.
@@ -63,11 +101,13 @@ struct ResolveParams {
   int32_t* out_rows;
   int32_t* out_stats;
   int32_t* miss_count;  // workspace [nl*R] (units)
-  int4* miss_list;      // workspace [nl*R][max_m] = (host row, pool row, position r*n+i, 0)
+  int4* miss_list;      // workspace [nl*R][max_m] = (host row, pool row, position r*n+i, first repeat)
+  MissOrder ord;        // ord.cnt != nullptr: misses are filed by host row range instead
   // Fused mode (non-null): per output position, the fused gather's source:
-  //   >= 0 pool row; -1 zero row (padding / failed unit); INT_MIN the first occurrence of a miss
-  //   (written by the gather's miss warps from the miss list); other values <= -2: host row
-  //   (-2 - value), a repeated position of a miss.
+  //   >= 0 pool row; -1 zero row (padding / failed unit); <= -2 written by the miss warps: INT_MIN the
+  //   first occurrence of a missed id, -3 - next a repeated position of it (next: the unit-local
+  //   position of the following repeat, -1 after the last).  A miss entry's fourth field is its first
+  //   repeat (-1: none), so the repeats form a chain that starts at the entry.
   int32_t* msrc;
 };
 
@@ -96,6 +136,8 @@ size_t resolve_smem_limit(int dev);
 int resolve_threads(const ResolveSmem& sm, int64_t units, int64_t n, int sms, int dev);
 
 // Launchers (return cudaGetLastError() of the launch).
+// With the ordered layout (p.ord.cnt set) launch_resolve first clears its counters with a small
+// kernel, on which the resolver depends programmatically.
 cudaError_t launch_resolve(const ResolveParams& p, const ResolveSmem& sm, cudaStream_t s);
 cudaError_t launch_miss_copy(const ResolveParams& p, const LayerPtrs& ptrs, int32_t row_bytes, int sms,
                              cudaStream_t s);
@@ -108,9 +150,8 @@ cudaError_t launch_gather(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl
 // reads the plan of unit group (l / group); layer_begin is a multiple of group.
 cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, int32_t group, int32_t R,
                                 int32_t n, int32_t max_m, const int32_t* rows, const int32_t* miss_count,
-                                const int4* miss_list, const int32_t* msrc, uint8_t* out, int32_t row_bytes,
-                                int64_t num_rows, int sms,
-                                cudaStream_t s);
+                                const int4* miss_list, const MissOrder& ord, const int32_t* msrc, uint8_t* out,
+                                int32_t row_bytes, int64_t num_rows, int sms, cudaStream_t s);
 cudaError_t launch_offload(const LayerPtrs& ptrs, const PoolGeom& g, const int32_t* gpu_blocks,
                            const int32_t* host_blocks, int32_t n, int32_t* status, int sms, cudaStream_t s);
 cudaError_t launch_fill_i32(int32_t* a, int64_t count, int32_t value, int sms, cudaStream_t s);
@@ -118,6 +159,74 @@ cudaError_t launch_reset_requests(int32_t* tok, int32_t* stamp, int32_t groups, 
                                   const int32_t* requests, int32_t n, int sms, cudaStream_t s);
 
 void count_launch(int k = 1);
+
+// The item index of an index group's ordered misses, kept in shared memory (one per CTA): item i
+// (up to kMissRowsPerItem consecutive entries of one bucket, or of the overflow list) -> its first
+// entry and its row count.  load() is called by one whole warp; the others read after a barrier.
+struct MissItems {
+  int32_t cnt[kMissBuckets];       // entries in each bucket (at most cap)
+  int32_t pref[kMissBuckets + 1];  // items before each bucket; pref[kMissBuckets]: all bucket items
+  int32_t overflow;                // overflow entries
+  int32_t items;                   // bucket items plus overflow items
+
+  __device__ __forceinline__ void load(const MissOrder& o, int g) {
+    const int lane = threadIdx.x & 31;
+    const int32_t* c = o.cnt + (int64_t)g * (kMissBuckets + 1);
+    int32_t v[kBucketsPerLane];
+    int32_t sum = 0;
+#pragma unroll
+    for (int k = 0; k < kBucketsPerLane; ++k) {
+      const int32_t x = __ldcg(c + lane * kBucketsPerLane + k);
+      v[k] = x < o.cap ? x : o.cap;
+      sum += (v[k] + kMissRowsPerItem - 1) / kMissRowsPerItem;
+    }
+    int32_t incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int32_t x = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += x;
+    }
+    int32_t base = incl - sum;
+#pragma unroll
+    for (int k = 0; k < kBucketsPerLane; ++k) {
+      cnt[lane * kBucketsPerLane + k] = v[k];
+      pref[lane * kBucketsPerLane + k] = base;
+      base += (v[k] + kMissRowsPerItem - 1) / kMissRowsPerItem;
+    }
+    if (lane == 31) {
+      pref[kMissBuckets] = incl;
+      const int32_t ov = __ldcg(c + kMissBuckets);
+      overflow = ov < o.per_group ? ov : o.per_group;
+      items = incl + (overflow + kMissRowsPerItem - 1) / kMissRowsPerItem;
+    }
+    __syncwarp();
+  }
+  // Item i < items: its first entry (relative to the group's buckets, or to its overflow list when
+  // in_overflow) and its row count.
+  __device__ __forceinline__ void locate(const MissOrder& o, int32_t i, int64_t& start, bool& in_overflow,
+                                         int& nrows) const {
+    const int32_t nb = pref[kMissBuckets];
+    int32_t first, count;
+    if (i >= nb) {
+      first = (i - nb) * kMissRowsPerItem;
+      count = overflow - first;
+      start = first;
+      in_overflow = true;
+    } else {
+      int lo = 0, hi = kMissBuckets - 1;  // the last bucket b with pref[b] <= i (it has items)
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pref[mid] <= i) lo = mid;
+        else hi = mid - 1;
+      }
+      first = (i - pref[lo]) * kMissRowsPerItem;
+      count = cnt[lo] - first;
+      start = (int64_t)lo * o.cap + first;
+      in_overflow = false;
+    }
+    nrows = count < kMissRowsPerItem ? count : kMissRowsPerItem;
+  }
+};
 
 // Programmatic dependent launch.  A kernel that follows another of this library's kernels on the
 // same stream is launched with programmatic stream serialization: its CTAs may be placed as soon as

@@ -55,7 +55,7 @@ extern "C" hs_status hs_resolve_topk_noalloc(const hs_pool* pool, int32_t layer_
   // Shapes whose scratch would exceed the built-in array are refused before anything else (units are
   // index groups: nl / G of them per request).
   const int32_t G = hot->layers_per_index > 1 ? hot->layers_per_index : 1;
-  const size_t need = hs_resolve_workspace_bytes(nl / G, R, P, K, hot->capacity);
+  const size_t need = hs_resolve_workspace_bytes_min(nl / G, R, P, K, hot->capacity);
   if (need > (size_t)HS_STATIC_SCRATCH_BYTES) return HS_ERR_INVALID_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {

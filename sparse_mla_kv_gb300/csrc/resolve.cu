@@ -18,7 +18,10 @@
 //                    victims are the candidates sorted by (stamp, slot) with a stable LSD radix sort
 //                    (8-bit digits, per-warp histograms, __match_any_sync ranking) whose buffers reuse
 //                    the hash table's memory.  Misses go to a per-unit list in the caller's
-//                    workspace.  A unit with a data error writes nothing but -1 rows and its status.
+//                    workspace (or, for large host pools, filed by host row range: the ordered
+//                    layout).  For the fused gather, the repeated positions of a missed id are
+//                    chained so that the row read once serves all of them.  A unit with a data error
+//                    writes nothing but -1 rows and its status.
 //                    The footprint, 4*C + 13*P*K bytes plus the hash table, fits the pages' MTP sizing
 //                    (num_spec + 2) * K = 10240 slots with P*K = 8192 ids in one CTA.
 //   miss_copy_kernel a persistent grid spreads every unit's misses over all SMs: each warp takes
@@ -426,6 +429,9 @@ __global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const
       st[2] = st[3] = 0;
       p.miss_count[unit] = 0;
     }
+    // ordered layout: no unit of the grid ends before the counters' clearing kernel has, so the
+    // kernels after this one never see a counter of an earlier step
+    if (p.ord.cnt) pdl_wait_prerequisites();
     return;
   }
 
@@ -544,6 +550,47 @@ __global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const
     }
   }
 
+  // ---- phase 4b (ordered miss layout): the unit counts its misses per host row range, reserves
+  // that many entries in each of its group's buckets (one global atomic per bucket it uses), and
+  // phase 5 files each miss at the next reserved entry of its bucket (the overflow list once a
+  // bucket is full).  s_bk reuses the victim sort's histogram memory.
+  const bool ordered = p.ord.cnt != nullptr && e == 0u && tot_miss > 0;  // uniform
+  int* s_bk = reinterpret_cast<int*>(smem + sm.idh) + ((C + 7) & ~7);    // after the two slot buffers
+  int32_t* ord_cnt = ordered ? p.ord.cnt + (int64_t)lr * (kMissBuckets + 1) : nullptr;
+  // ---- phase 4c (fused plans with misses): the repeated positions of a missed id are chained, so that
+  // the gather's miss warps store the row they read once into every position of the id.  s_slot (dead
+  // since phase 2) becomes the chain heads: s_slot[f] = the last-linked repeat of first occurrence f;
+  // a repeat's per-position source holds the link to the next one, -3 - next (-2 ends the chain).
+  const bool chains = msrc_g != nullptr && e == 0u && tot_miss > 0;  // uniform
+  if (chains) {
+    for (int i = tid; i < n; i += kT) s_slot[i] = -1;
+    __syncthreads();
+    for (int i = tid; i < n; i += kT) {
+      if (s_cls[i] == kDup) {
+        const int f = s_val[i];
+        if (s_cls[f] == kMiss) msrc_g[i] = -3 - atomicExch(&s_slot[f], i);
+      }
+    }
+    __syncthreads();
+  }
+
+  // every unit of an ordered launch waits for the counters' clearing kernel (launched just before
+  // this one): those that file misses need the counters zero, and none may end before it has
+  if (p.ord.cnt) pdl_wait_prerequisites();
+  if (ordered) {
+    __syncthreads();  // the sort's histogram is dead
+    for (int b = tid; b < kMissBuckets; b += kT) s_bk[b] = 0;
+    __syncthreads();
+    for (int i = i0; i < i1; ++i)
+      if (s_cls[i] == kMiss) atomicAdd(&s_bk[min(kMissBuckets - 1, (int)((uint32_t)s_val[i] >> p.ord.shift))], 1);
+    __syncthreads();
+    for (int b = tid; b < kMissBuckets; b += kT) {
+      const int c = s_bk[b];
+      s_bk[b] = c ? atomicAdd(ord_cnt + b, c) : 0;
+    }
+    __syncthreads();
+  }
+
   if (e == 0u) {
     // ---- phase 5: hits refresh their stamp; the j-th miss takes the j-th victim and one row
     int j = miss_base;
@@ -553,7 +600,19 @@ __global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const
         const int v = sorted[j];
         const int vb = (unsigned)v / S;
         const int dst = s_hot[vb] * S + (v - vb * S);
-        p.miss_list[(int64_t)unit * p.max_m + j] = make_int4(s_val[i], dst, r * n + i, 0);
+        const int4 ent = make_int4(s_val[i], dst, r * n + i, chains ? s_slot[i] : -1);
+        if (ordered) {
+          const int b = min(kMissBuckets - 1, (int)((uint32_t)s_val[i] >> p.ord.shift));
+          const int q = atomicAdd(&s_bk[b], 1);
+          if (q < p.ord.cap) {
+            p.ord.buckets[((int64_t)lr * kMissBuckets + b) * p.ord.cap + q] = ent;
+          } else {
+            const int o = atomicAdd(ord_cnt + kMissBuckets, 1);
+            if (o < p.ord.per_group) p.ord.overflow[(int64_t)lr * p.ord.per_group + o] = ent;
+          }
+        } else {
+          p.miss_list[(int64_t)unit * p.max_m + j] = ent;
+        }
         if (msrc_g) msrc_g[i] = kGatherOwnedByMissWarps;
         p.slot_token[state_off + v] = s_ids[i];
         p.slot_stamp[state_off + v] = step;
@@ -577,14 +636,10 @@ __global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const
       if (id >= 0) {
         if (s_cls[i] != kDup) {
           row = s_val[i];
-        } else {  // a repeated id: share the first occurrence's row (a miss: re-read its host row)
+        } else {  // a repeated id: share the first occurrence's row
           const int f = s_val[i];
           row = s_val[f];
-          if (msrc_g) {
-            // a repeated position of a miss reads the host row again (the first occurrence's host
-            // row is re-derived from the host block table, which was valid for it)
-            msrc_g[i] = s_cls[f] == kMiss ? -2 - (hbt[(unsigned)id / S] * S + (unsigned)id % S) : row;
-          }
+          if (msrc_g && s_cls[f] != kMiss) msrc_g[i] = row;  // a miss's repeats are chained (phase 4c)
         }
       } else if (msrc_g) {
         msrc_g[i] = -1;
@@ -620,20 +675,79 @@ __global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const
 
 constexpr int kCopyThreads = 256;
 
-// Copies the misses of every unit.  Items (unit, group of kMissRowsPerItem consecutive misses) are
-// numbered chunk-major (item = group * units + unit), so the live items are the low numbers; lane j of
-// warp w tests item w + j * nwarps, which spreads the live items over all warps of the grid.  A live
-// item's rows are copied with all its 16-byte loads issued before any store.
+// Copies the rows of up to kMissRowsPerItem entries (lane j < nrows holds entry j) from the host pool
+// into their hot slots, in every layer [l0, l0 + group), all of a layer's 16-byte loads before its
+// stores.
+template <int CPR>
+__device__ __forceinline__ void copy_miss_rows(const LayerPtrs& ptrs, int l0, int group, int4 ent, int nrows,
+                                               int row_bytes) {
+  constexpr int kU = CPR ? (kMissRowsPerItem * CPR + 31) / 32 : 4;
+  const int cpr = CPR ? CPR : (row_bytes >> 4);
+  const int lane = threadIdx.x & 31;
+  const int total = nrows * cpr;
+  for (int l = l0; l < l0 + group; ++l) {
+    const uint8_t* host = ptrs.host[l];
+    uint8_t* pool = ptrs.gpu[l];
+    for (int f0 = 0; f0 < total; f0 += 32 * kU) {
+      uint4 v[kU];
+      int64_t dst_off[kU];
+#pragma unroll
+      for (int k = 0; k < kU; ++k) {
+        const int f = f0 + k * 32 + lane;
+        const bool ok = f < total;
+        const int rr = ok ? f / cpr : 0;
+        const int cc = f - rr * cpr;
+        const int src = __shfl_sync(kFull, ent.x, rr);
+        const int dst = __shfl_sync(kFull, ent.y, rr);
+        dst_off[k] = -1;
+        if (ok) {
+          v[k] = __ldcg(reinterpret_cast<const uint4*>(host + (int64_t)src * row_bytes) + cc);
+          dst_off[k] = (int64_t)dst * row_bytes + (int64_t)cc * 16;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kU; ++k)
+        if (dst_off[k] >= 0) *reinterpret_cast<uint4*>(pool + dst_off[k]) = v[k];
+    }
+  }
+}
+
+// Copies the misses of every unit.  Per-unit lists: items (unit, group of kMissRowsPerItem
+// consecutive misses) are numbered chunk-major (item = group * units + unit), so the live items are
+// the low numbers; lane j of warp w tests item w + j * nwarps, which spreads the live items over all
+// warps of the grid.  Ordered layout: blockIdx.y is the index group, and the warps of its CTAs take
+// its items in bucket order (warp w: items w, w + nwarps, ...), so the rows in flight lie in
+// neighbouring host ranges.  A live item's rows are copied with all its 16-byte loads issued before
+// any store.
 template <int CPR>
 __global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(const ResolveParams p, const LayerPtrs ptrs,
                                                                  int32_t row_bytes) {
-  constexpr int kU = CPR ? (kMissRowsPerItem * CPR + 31) / 32 : 4;
   pdl_wait_prerequisites();   // the resolver's miss lists must be complete and visible
-  const int cpr = CPR ? CPR : (row_bytes >> 4);
+  const int lane = threadIdx.x & 31;
+  if (p.ord.cnt) {
+    const int g = blockIdx.y;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    __shared__ MissItems mi;
+    if (threadIdx.x < 32) mi.load(p.ord, g);
+    __syncthreads();
+    const int4* bk = p.ord.buckets + (int64_t)g * kMissBuckets * p.ord.cap;
+    const int4* ov = p.ord.overflow + (int64_t)g * p.ord.per_group;
+    const int l0 = (p.layer_begin + g) * p.group;
+    for (int32_t i = (int32_t)warp; i < mi.items; i += (int32_t)nwarps) {
+      int64_t start;
+      bool in_ov;
+      int nrows;
+      mi.locate(p.ord, i, start, in_ov, nrows);
+      int4 ent = make_int4(0, 0, 0, 0);
+      if (lane < nrows) ent = (in_ov ? ov : bk)[start + lane];
+      copy_miss_rows<CPR>(ptrs, l0, p.group, ent, nrows, row_bytes);
+    }
+    return;
+  }
   const int units = p.nl * p.R;
   const int items_per_unit = (p.max_m + kMissRowsPerItem - 1) / kMissRowsPerItem;
   const int64_t items = (int64_t)units * items_per_unit;
-  const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   for (int64_t base = warp; base < items; base += nwarps * 32) {
@@ -655,37 +769,18 @@ __global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(const ResolvePa
       const int c = __shfl_sync(kFull, cnt, src_lane);
       const int r0 = ch * kMissRowsPerItem;
       const int nrows = min(kMissRowsPerItem, c - r0);
-      const int l0 = (p.layer_begin + u / p.R) * p.group;
       int4 ent = make_int4(0, 0, 0, 0);
       if (lane < nrows) ent = p.miss_list[(int64_t)u * p.max_m + r0 + lane];
-      const int total = nrows * cpr;
-      for (int l = l0; l < l0 + p.group; ++l) {  // every layer of the unit's index group
-        const uint8_t* host = ptrs.host[l];
-        uint8_t* pool = ptrs.gpu[l];
-        for (int f0 = 0; f0 < total; f0 += 32 * kU) {
-          uint4 v[kU];
-          int64_t dst_off[kU];
-#pragma unroll
-          for (int k = 0; k < kU; ++k) {
-            const int f = f0 + k * 32 + lane;
-            const bool ok = f < total;
-            const int rr = ok ? f / cpr : 0;
-            const int cc = f - rr * cpr;
-            const int src = __shfl_sync(kFull, ent.x, rr);
-            const int dst = __shfl_sync(kFull, ent.y, rr);
-            dst_off[k] = -1;
-            if (ok) {
-              v[k] = __ldcg(reinterpret_cast<const uint4*>(host + (int64_t)src * row_bytes) + cc);
-              dst_off[k] = (int64_t)dst * row_bytes + (int64_t)cc * 16;
-            }
-          }
-#pragma unroll
-          for (int k = 0; k < kU; ++k)
-            if (dst_off[k] >= 0) *reinterpret_cast<uint4*>(pool + dst_off[k]) = v[k];
-        }
-      }
+      copy_miss_rows<CPR>(ptrs, (p.layer_begin + u / p.R) * p.group, p.group, ent, nrows, row_bytes);
     }
   }
+}
+
+// Zeroes the ordered layout's counters; the resolver launched after it waits for it only where it
+// first touches them.
+__global__ void order_clear_kernel(int32_t* __restrict__ cnt, int32_t count) {
+  pdl_allow_dependents();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < count; i += gridDim.x * blockDim.x) cnt[i] = 0;
 }
 
 int ceil_log2(int64_t x) {
@@ -743,6 +838,28 @@ size_t resolve_workspace_bytes(int64_t units, int64_t n, int64_t C) {
   return align16(4 * (size_t)units) + 16 * (size_t)units * (size_t)max_m + align16(4 * (size_t)units * (size_t)n);
 }
 
+size_t resolve_workspace_bytes_ordered(int64_t groups, int64_t R, int64_t n, int64_t C) {
+  const int64_t max_m = n < C ? n : C;
+  return resolve_workspace_bytes(groups * R, n, C) + ws_order_cnt_bytes(groups) +
+         16 * (size_t)groups * kMissBuckets * (size_t)miss_bucket_cap(R * max_m);
+}
+
+MissOrder miss_order_layout(void* workspace, int64_t groups, int64_t R, int64_t n, int64_t C, int64_t num_host_rows) {
+  MissOrder o{};
+  const int64_t max_m = n < C ? n : C;
+  const int64_t per_group = R * max_m;
+  if (!workspace || per_group <= 0 || 2 * per_group > INT32_MAX) return o;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t base = resolve_workspace_bytes(groups * R, n, C);
+  o.cnt = reinterpret_cast<int32_t*>(ws + base);
+  o.buckets = reinterpret_cast<int4*>(ws + base + ws_order_cnt_bytes(groups));
+  o.overflow = reinterpret_cast<int4*>(ws + ws_counts_bytes(groups * R));
+  o.shift = miss_bucket_shift(num_host_rows);
+  o.cap = miss_bucket_cap(per_group);
+  o.per_group = (int32_t)per_group;
+  return o;
+}
+
 namespace {
 
 // every resolver instantiation, in the order (page size 64?, wide table?, 512 threads?) -> index
@@ -797,7 +914,27 @@ cudaError_t launch_resolve(const ResolveParams& p, const ResolveSmem& sm, cudaSt
   const int idx = (p.S == 64 ? 4 : 0) + (sm.id_hash_wide ? 2 : 0) + (sm.threads == kResolveThreads / 2 ? 1 : 0);
   const dim3 grid(p.nl * p.R), block(sm.threads == kResolveThreads / 2 ? kResolveThreads / 2 : kResolveThreads);
   void* args[] = {(void*)&p, (void*)&sm};
-  cudaError_t e = cudaLaunchKernel(resolver_kernels[idx], grid, block, args, sm.total, s);
+  if (!p.ord.cnt) {
+    cudaError_t e = cudaLaunchKernel(resolver_kernels[idx], grid, block, args, sm.total, s);
+    count_launch();
+    return e;
+  }
+  const int count = p.nl * (kMissBuckets + 1);
+  order_clear_kernel<<<(count + 255) / 256, 256, 0, s>>>(p.ord.cnt, count);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = sm.total;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelExC(&cfg, resolver_kernels[idx], args);
   count_launch();
   return e;
 }
@@ -806,13 +943,22 @@ cudaError_t launch_miss_copy(const ResolveParams& p, const LayerPtrs& ptrs, int3
                              cudaStream_t s) {
   const int64_t units = (int64_t)p.nl * p.R;
   const int64_t items = units * ((p.max_m + kMissRowsPerItem - 1) / kMissRowsPerItem);
-  // one warp per item at most, capped at a full resident grid
+  // one warp per item at most, capped at a full resident grid (split over the index groups when
+  // the ordered layout gives each group its own CTAs)
   int64_t blocks = (items + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
-  const int64_t cap = (int64_t)sms * 8;
+  const int64_t cap = p.ord.cnt ? ((int64_t)sms * 8 + p.nl - 1) / p.nl : (int64_t)sms * 8;
+  if (p.ord.cnt) blocks = (blocks + p.nl - 1) / p.nl;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  cudaError_t e = launch_dependent(row_bytes == 656 ? miss_copy_kernel<41> : miss_copy_kernel<0>,
-                                   dim3((unsigned)blocks), dim3(kCopyThreads), 0, s, p, ptrs, row_bytes);
+  const dim3 grid((unsigned)blocks, p.ord.cnt ? (unsigned)p.nl : 1u);
+  auto kern = row_bytes == 656 ? miss_copy_kernel<41> : miss_copy_kernel<0>;
+  cudaError_t e;
+  if (p.ord.cnt) {  // large host pools: no early launch (as for the fused gather)
+    kern<<<grid, kCopyThreads, 0, s>>>(p, ptrs, row_bytes);
+    e = cudaGetLastError();
+  } else {
+    e = launch_dependent(kern, grid, dim3(kCopyThreads), 0, s, p, ptrs, row_bytes);
+  }
   if (e != cudaSuccess) return e;
   count_launch();
   return cudaGetLastError();

@@ -16,8 +16,12 @@ from synth import content, device as sdev
 class Rig:
     def __init__(self, w, *, oracle_bytes: bool = False, device: str = "cuda", check_hot_bytes: bool = True,
                  mode: str = "split", graph: bool = False):
-        assert mode in ("split", "fused")
-        self.mode = mode
+        # "split" / "fused": the library's default miss layout for the pool (ordered only for large host
+        # pools); a "+order" suffix forces the address-ordered layout on any pool
+        base, _, opt = mode.partition("+")
+        assert base in ("split", "fused") and opt in ("", "order")
+        self.mode = base
+        self.force_order = opt == "order"
         self.graph = graph
         self.prep = None
         self.w = w
@@ -36,6 +40,8 @@ class Rig:
             if w.num_host_blocks:
                 sdev.fill_host_pool(w, l, self.host[l], self.dev)
         self.pool = hs.Pool(self.gpu, self.host if w.num_host_blocks else None)
+        if self.force_order:
+            self.pool.set_miss_order(hs.MISS_ORDER_ON)
         self.bt_np = w.block_table.copy()
         self.hbt_np = w.host_block_table.copy()
         self.bt = torch.from_numpy(self.bt_np).to(self.dev)
@@ -45,6 +51,8 @@ class Rig:
         self.hot = hs.HotState.allocate(L, self.hot_blocks, C, layers_per_index=G)
         hs.hot_reset(self.pool, self.hot)
         self.ws = hs.alloc_workspace(L // G, R, w.P, w.K, C, self.dev)
+        self.ordered = hs.miss_order_used(self.pool, self.hot, L, R, w.P, w.K, self.ws.numel())
+        assert self.ordered or not (self.force_order and w.num_host_blocks)
         self.o_tok = np.full((L // G, R, C), -1, np.int32)
         self.o_stamp = np.full((L // G, R, C), -1, np.int32)
         self.o_pools = self.o_hosts = None

@@ -57,12 +57,24 @@ def test_status_strings(lib):
     assert hs.status_str(99) == "unknown status"
 
 
+def _ordered_extra(ng, R, P, K, C):
+    # bucket counters (256 + 1 per index group, 16-byte aligned) and 256 buckets per group of twice
+    # the even share of the group's R * min(P*K, C) possible misses, 16 B per entry
+    per_group = R * min(P * K, C)
+    cap = -(-2 * per_group // 256)
+    return -(-4 * ng * 257 // 16) * 16 + 16 * ng * 256 * cap
+
+
 def test_size_queries(lib):
     # workspace: 16-byte-aligned miss counts + (host row, pool row, position) per possible miss
     # (min(P*K, C) per unit, 16 B each) + one host source per position (16-byte aligned)
-    assert hs.resolve_workspace_bytes(1, 64, 1, 2048, 4096) == 256 + 16 * 64 * 2048 + 4 * 64 * 2048
-    assert hs.resolve_workspace_bytes(4, 256, 4, 2048, 4096) == 4096 + 16 * 1024 * 4096 + 4 * 1024 * 8192
-    assert hs.resolve_workspace_bytes(1, 3, 1, 5, 4) == 16 + 16 * 3 * 4 + 64
+    assert hs.resolve_workspace_bytes_min(1, 64, 1, 2048, 4096) == 256 + 16 * 64 * 2048 + 4 * 64 * 2048
+    assert hs.resolve_workspace_bytes_min(4, 256, 4, 2048, 4096) == 4096 + 16 * 1024 * 4096 + 4 * 1024 * 8192
+    assert hs.resolve_workspace_bytes_min(1, 3, 1, 5, 4) == 16 + 16 * 3 * 4 + 64
+    assert hs.resolve_workspace_bytes_min(1, 1, 0, 5, 4) == 0
+    # the full size adds the address-ordered miss layout's room
+    for shape in ((1, 64, 1, 2048, 4096), (4, 256, 4, 2048, 4096), (1, 3, 1, 5, 4), (16, 32, 1, 2048, 4096)):
+        assert hs.resolve_workspace_bytes(*shape) == hs.resolve_workspace_bytes_min(*shape) + _ordered_extra(*shape)
     assert hs.resolve_workspace_bytes(1, 1, 0, 5, 4) == 0
     # the benchmarked shapes and the MTP3 sizing (num_spec + 2) * K = 10240 fit in one CTA's shared
     # memory; oversize plans report 0 or > 227 KB

@@ -31,9 +31,21 @@ def _rig(w, **kw):
 
 
 MODES = ["split", "fused"]
+# the same, plus both paths with the address-ordered miss layout forced on (small pools default to
+# per-unit lists)
+MODES_ORDER = MODES + ["split+order", "fused+order"]
 
 
-@pytest.mark.parametrize("mode", MODES)
+def _base(mode):
+    return mode.partition("+")[0]
+
+
+def _set_order(pool, mode):
+    if mode.endswith("+order"):
+        pool.set_miss_order(hs.MISS_ORDER_ON)
+
+
+@pytest.mark.parametrize("mode", MODES_ORDER)
 def test_tiny_decode_all_bytes(mode):
     w = workloads.config1(seed=0, steps=8)
     rig = _rig(w, oracle_bytes=True, mode=mode)
@@ -70,7 +82,7 @@ def _case_to_gpu(case, dev):
     return pool, gpu, host, hot
 
 
-@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mode", MODES_ORDER)
 def test_random_small_cases_vs_oracle(mode):
     """Random small shapes (page sizes 1/2/4, several positions, duplicates, padding, replays,
     invalid ids, steps going backwards) through the library and the oracle with byte pools."""
@@ -80,6 +92,7 @@ def test_random_small_cases_vs_oracle(mode):
     for ci in range(150):
         case, P, K = _random_case(rng)
         pool, gpu, host, hot = _case_to_gpu(case, dev)
+        _set_order(pool, mode)
         bt, hbt = torch.from_numpy(case.bt).to(dev), torch.from_numpy(case.hbt).to(dev)
         ctx = torch.from_numpy(case.ctx).to(dev)
         t = 0
@@ -87,7 +100,7 @@ def test_random_small_cases_vs_oracle(mode):
             u = rng.random()
             t = t if u < 0.1 else (max(0, t - 2) if u < 0.13 else t + int(rng.integers(1, 3)))
             ids = _ids(rng, case, P, K)
-            if mode == "fused":
+            if _base(mode) == "fused":
                 rows, stats, g = hs.resolve_gather(pool, torch.from_numpy(ids[None]).to(dev), bt, hbt, ctx, hot, t)
             else:
                 rows, stats = hs.resolve_topk(pool, torch.from_numpy(ids[None]).to(dev), bt, hbt, ctx, hot, t)
@@ -117,7 +130,7 @@ def _group_case_to_gpu(case, dev, G):
     return pool, gpu, host, hot
 
 
-@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mode", MODES_ORDER)
 def test_index_share_random_small_cases_vs_oracle(mode):
     """IndexShare: G in {2, 4} layers read one top-K list and share one hot state per request; calls
     cover a window of index groups.  Rows, stats, the group states, every layer's pool bytes and the
@@ -134,6 +147,7 @@ def test_index_share_random_small_cases_vs_oracle(mode):
         case.tok = np.full((ng_total, case.R, case.C), -1, np.int32)
         case.stamp = np.full((ng_total, case.R, case.C), -1, np.int32)
         pool, gpu, host, hot = _group_case_to_gpu(case, dev, G)
+        _set_order(pool, mode)
         bt, hbt = torch.from_numpy(case.bt).to(dev), torch.from_numpy(case.hbt).to(dev)
         ctx = torch.from_numpy(case.ctx).to(dev)
         g0 = int(rng.integers(0, ng_total))
@@ -144,7 +158,7 @@ def test_index_share_random_small_cases_vs_oracle(mode):
             t += int(rng.integers(0, 3))
             ids = np.stack([_ids(rng, case, P, K) for _ in range(ng)])
             ids_d = torch.from_numpy(ids).to(dev)
-            if mode == "fused":
+            if _base(mode) == "fused":
                 rows, stats, g = hs.resolve_gather(pool, ids_d, bt, hbt, ctx, hot, t, layer_begin=lb)
             else:
                 rows, stats = hs.resolve_topk(pool, ids_d, bt, hbt, ctx, hot, t, layer_begin=lb)
@@ -182,7 +196,7 @@ def test_index_share_multi_turn_agentic(mode):
     assert misses > 0
 
 
-@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mode", MODES_ORDER)
 def test_index_share_graph_capture(mode):
     """IndexShare steps captured into CUDA graphs (resolve, the per-layer or fused gather, offload)."""
     w = workloads.config3(seed=6, decode_per_turn=6, L=4, R=8, layers_per_index=2)
@@ -191,10 +205,11 @@ def test_index_share_graph_capture(mode):
         rig.step(st)
 
 
-def test_index_share_mtp3_64_requests():
+@pytest.mark.parametrize("mode", ["fused", "split+order", "fused+order"])
+def test_index_share_mtp3_64_requests(mode):
     """IndexShare with MTP3 plans: 4 layers in one index group, 64 requests, P=4 positions."""
     w = workloads.config5(seed=2, steps=3, R=64, layers_per_index=4)
-    rig = _rig(w, mode="fused")
+    rig = _rig(w, mode=mode)
     for st in w.iter_steps(3):
         rig.step(st)
 
@@ -225,7 +240,7 @@ def test_full_residency_batch(mode):
     assert (rig.hot.slot_token.cpu().numpy() == -1).all()
 
 
-@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mode", MODES_ORDER)
 def test_cold_start_prefix_reuse_full_size(mode):
     """16 requests reusing a 1,048,576-token host-only prefix, empty hot buffers, 32 steps."""
     w = workloads.config4(seed=0, steps=32)
@@ -235,7 +250,7 @@ def test_cold_start_prefix_reuse_full_size(mode):
     assert int(stats[..., 3].sum()) > 0
 
 
-@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mode", MODES_ORDER)
 def test_whole_step_captured_in_a_cuda_graph(mode):
     """Each decode step -- resolve + gather and the step's single offload launch -- captured into one
     CUDA graph and replayed (no host decision anywhere on the path): results identical to the oracle.
@@ -257,6 +272,7 @@ def test_max_batch_mtp3_full_size():
     fused path, first 6 steps."""
     w = workloads.config5(seed=0, steps=6)
     rig = _rig(w, mode="fused")
+    assert rig.ordered   # a host pool of tens of GB: misses are filed in address order by default
     offloaded = 0
     for st in w.iter_steps(6):
         _, stats, *_ = rig.step(st)
@@ -264,7 +280,7 @@ def test_max_batch_mtp3_full_size():
     assert offloaded > 0
 
 
-@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mode", MODES_ORDER)
 def test_mtp3_hot_sizing_and_verify_replays(mode):
     """The pages' MTP hot-buffer sizing, (num_spec + 2) * K = 10240 rows per request with P = 4 positions
     sharing one plan, 64 requests.  Every step is resolved a second time with the same ids (a verify
@@ -283,9 +299,10 @@ def test_mtp3_hot_sizing_and_verify_replays(mode):
         assert torch.equal(tok, rig.hot.slot_token) and torch.equal(stamp, rig.hot.slot_stamp)
 
 
-def test_max_batch_mtp3_split_path_64_requests():
+@pytest.mark.parametrize("mode", ["split", "split+order"])
+def test_max_batch_mtp3_split_path_64_requests(mode):
     w = workloads.config5(seed=1, steps=4, R=64)
-    rig = _rig(w, mode="split")
+    rig = _rig(w, mode=mode)
     for st in w.iter_steps(4):
         rig.step(st)
 
@@ -304,7 +321,7 @@ def test_multi_turn_agentic_full_geometry():
     assert saw_edit and saw_off
 
 
-@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mode", MODES_ORDER)
 def test_multi_turn_agentic_turn_boundaries(mode):
     """Same geometry with 6 decode steps per turn, so two turn boundaries (753 prompt tokens: a dozen
     pages complete and start at once) fall inside 14 steps."""
@@ -314,7 +331,7 @@ def test_multi_turn_agentic_turn_boundaries(mode):
         rig.step(st)
 
 
-@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mode", MODES_ORDER)
 def test_data_errors_are_isolated_per_unit(mode):
     w = workloads.config1(seed=3, steps=3)
     rig = _rig(w, oracle_bytes=True, mode=mode)
@@ -407,7 +424,7 @@ def test_largest_shapes_and_shape_limits():
     pool.close()
 
 
-@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mode", MODES_ORDER)
 def test_snapshot_restore_continues_identically(mode):
     """Checkpoint/resume: the hot state and pool bytes copied out mid-run and copied back give the same
     continuation (rows, stats, state, gathered bytes), with a fresh workspace full of garbage -- the
@@ -434,6 +451,34 @@ def test_snapshot_restore_continues_identically(mode):
     for st, (r0, s0, o0) in zip(steps[4:], first):
         rows, stats, out, *_ = rig.step(st)
         assert torch.equal(rows, r0) and torch.equal(stats, s0) and torch.equal(out, o0)
+
+
+def test_miss_order_decision():
+    """hs_resolve_miss_order: the default (AUTO) keeps per-unit lists for a small host pool; ON files
+    misses in address order when the workspace has room for it (hs_resolve_workspace_bytes) and not
+    with the minimal workspace; OFF never; an unknown mode is refused."""
+    dev = torch.device("cuda")
+    S, C, R, P, K = 4, 8, 3, 1, 8
+    gpu = [torch.zeros((32, S, 16), dtype=torch.uint8, device=dev) for _ in range(2)]
+    host = [torch.zeros((16, S, 16), dtype=torch.uint8).pin_memory() for _ in range(2)]
+    pool = hs.Pool(gpu, host)
+    hot = hs.HotState.allocate(2, torch.zeros((R, C // S), dtype=torch.int32, device=dev), C)
+    full, small = hs.resolve_workspace_bytes(2, R, P, K, C), hs.resolve_workspace_bytes_min(2, R, P, K, C)
+    assert full > small
+    assert not hs.miss_order_used(pool, hot, 2, R, P, K, full)
+    pool.set_miss_order(hs.MISS_ORDER_ON)
+    assert hs.miss_order_used(pool, hot, 2, R, P, K, full)
+    assert hs.miss_order_used(pool, hot, 1, R, P, K, full, layer_begin=1)
+    assert not hs.miss_order_used(pool, hot, 2, R, P, K, small)
+    pool.set_miss_order(hs.MISS_ORDER_OFF)
+    assert not hs.miss_order_used(pool, hot, 2, R, P, K, full)
+    with pytest.raises(hs.HSError):
+        pool.set_miss_order(7)
+    no_host = hs.Pool(gpu)
+    no_host.set_miss_order(hs.MISS_ORDER_ON)
+    assert not hs.miss_order_used(no_host, hot, 2, R, P, K, full)
+    pool.close()
+    no_host.close()
 
 
 def test_hot_reset_of_listed_requests_only():

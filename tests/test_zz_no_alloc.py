@@ -63,7 +63,7 @@ def test_noalloc_matches_workspace_entry_point_twice(lib, cfg):
     bt = torch.from_numpy(w.block_table).to(dev)
     hbt = torch.from_numpy(w.host_block_table).to(dev)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    assert hs.resolve_workspace_bytes(w.L, w.R, w.P, w.K, w.C) <= HS_STATIC_SCRATCH_BYTES
+    assert hs.resolve_workspace_bytes_min(w.L, w.R, w.P, w.K, w.C) <= HS_STATIC_SCRATCH_BYTES
     for st in w.iter_steps():   # two calls in a row
         topk = torch.from_numpy(st.topk).to(dev)
         ctx = torch.from_numpy(st.ctx_len).to(dev)
@@ -95,7 +95,7 @@ def test_noalloc_refuses_shapes_beyond_its_scratch(lib):
     pool = hs.Pool(gpu, None)
     hot = hs.HotState.allocate(1, torch.arange(C // S, dtype=torch.int32, device=dev)[None], C)
     R, P, K = 400, 4, 2048     # 400 units x 96 KB of scratch > the built-in 32 MiB
-    assert hs.resolve_workspace_bytes(1, R, P, K, C) > HS_STATIC_SCRATCH_BYTES
+    assert hs.resolve_workspace_bytes_min(1, R, P, K, C) > HS_STATIC_SCRATCH_BYTES
     dummy = torch.zeros(16, dtype=torch.int32, device=dev)
     d = ctypes.c_void_p(dummy.data_ptr())
     code = lib.hs_resolve_topk_noalloc(pool.handle, 0, 1, R, P, K, d, d, d, d, 1, ctypes.byref(hot.c), 0, d, d,
