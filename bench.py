@@ -60,7 +60,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--soak-seconds", type=float, default=1.5)
+    ap.add_argument("--soak-seconds", type=float, default=None,
+                    help="seconds of repeated gathers before the timed steps (default 1.5; 5 for host pools of "
+                         "16 GiB or more, whose first seconds of reads after pinning run unevenly)")
     ap.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi during the timed steps")
     ap.add_argument("--passes", type=int, default=2, choices=[1, 2],
                     help="2: an untimed pass over the warm-up and timed steps precedes the timed pass")
@@ -458,7 +460,9 @@ def run_ours(args, ws, rank, local):
     # workload state does not change), each after an L2 flush, so the HBM and the host link carry this
     # step's traffic while the clocks settle and the sampler sees the GPU under load
     sampler = ClockSampler(local) if rank == 0 and not args.no_clocks else None
-    t_end = time.time() + args.soak_seconds
+    host_pool_bytes = L * max(1, w.num_host_blocks) * S * B
+    soak = args.soak_seconds if args.soak_seconds is not None else (5.0 if host_pool_bytes >= 16 << 30 else 1.5)
+    t_end = time.time() + soak
     while time.time() < t_end:
         for _ in range(20):
             flush.fill_(1)
