@@ -60,6 +60,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--settle-seconds", type=float, default=60.0,
+                    help="upper bound on the untimed passes over the timed steps that run until two in a row agree "
+                         "within 5%% (at least two passes)")
     ap.add_argument("--soak-seconds", type=float, default=None,
                     help="seconds of repeated gathers before the timed steps (default 1.5; 5 for host pools of "
                          "16 GiB or more, whose first seconds of reads after pinning run unevenly)")
@@ -372,25 +375,28 @@ def run_ours(args, ws, rank, local):
     stream = torch.cuda.current_stream()
     prep = hs.PreparedStep(pool, hot, bt, hbt, ctx, out_rows, out_stats, ws_buf, gout)
 
-    # host-link bandwidth (bulk pinned copies, both directions), for the step roofline
-    hbuf = torch.empty(256 << 20, dtype=torch.uint8, pin_memory=True)
-    dbuf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    # host-link bandwidth (bulk pinned copies, both directions) for the step roofline: measured after the
+    # timed passes, the best of several trials, so that a host whose first reads of fresh pinned memory
+    # are slow does not lower the peak
+    def link_peaks():
+        hbuf = torch.empty(256 << 20, dtype=torch.uint8, pin_memory=True)
+        dbuf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
-    def copy_rate(dst, src):
-        for _ in range(2):
-            dst.copy_(src, non_blocking=True)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(4):
-            dst.copy_(src, non_blocking=True)
-        e1.record()
-        e1.synchronize()
-        return 4 * (256 << 20) / (e0.elapsed_time(e1) * 1e-3) / 1e9
+        def copy_rate(dst, src):
+            best = 0.0
+            for _ in range(5):
+                dst.copy_(src, non_blocking=True)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(4):
+                    dst.copy_(src, non_blocking=True)
+                e1.record()
+                e1.synchronize()
+                best = max(best, 4 * (256 << 20) / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+            return best
 
-    h2d_gbs = copy_rate(dbuf, hbuf)
-    d2h_gbs = copy_rate(hbuf, dbuf)
-    del hbuf, dbuf
+        return copy_rate(dbuf, hbuf), copy_rate(hbuf, dbuf)
 
     fused = args.path == "fused"
 
@@ -496,12 +502,30 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize()
         return ev
 
-    restore()
-    for i in range(W):
-        before(i)
-        phase1(i)
-        phase2()
-        phase3(i)
+    def replay_warmup():
+        restore()
+        for i in range(W):
+            before(i)
+            phase1(i)
+            phase2()
+            phase3(i)
+        torch.cuda.synchronize()
+
+    # settle: untimed passes over the timed steps until two in a row agree within 5% (at most
+    # --settle-seconds).  On host pools of tens of GB the first seconds after pinning read unevenly
+    # on some machines; a long-running server sees the settled rate.
+    settle_medians = []
+    t_settle = time.time()
+    while True:
+        replay_warmup()
+        ev_u = timed_pass(split=False)
+        settle_medians.append(statistics.median(ev_u[k][0].elapsed_time(ev_u[k][2]) for k in range(K)))
+        if len(settle_medians) >= 2 and abs(settle_medians[-1] - settle_medians[-2]) <= 0.05 * settle_medians[-2]:
+            break
+        if time.time() - t_settle > args.settle_seconds:
+            break
+
+    replay_warmup()
     barrier(dist)
     torch.cuda.synchronize()
     n_launch0 = hs.launch_count()
@@ -531,6 +555,7 @@ def run_ours(args, ws, rank, local):
     t_gat = [ev_s[k][1].elapsed_time(ev_s[k][3]) * 1e-3 for k in range(K)]
     t_off = [ev_s[k][3].elapsed_time(ev_s[k][2]) * 1e-3 for k in range(K)]
     t_step_split = [ev_s[k][0].elapsed_time(ev_s[k][2]) * 1e-3 for k in range(K)]
+    h2d_gbs, d2h_gbs = link_peaks()
 
     sum_t = max_over_ranks(dist, float(sum(t_step)), dev)
     counts = st_all[..., 1:].sum(axis=(1, 2))           # [K][resident, hits, misses]
@@ -678,7 +703,10 @@ def run_ours(args, ws, rank, local):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": W,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "u8", "data": "synthetic", "config": dict(config_dict(w, args), miss_order=miss_order),
+            "dtype": "u8", "data": "synthetic",
+            "config": dict(config_dict(w, args), miss_order=miss_order,
+                           settle_passes=len(settle_medians),
+                           settle_step_us_medians=[round(1e3 * m, 1) for m in settle_medians]),
             "gathered_gbs": value * B / 1e9, "roofline": roofline, "step_roofline": step_roof,
             "cpu_baseline": cpu, "cpu_baseline_1thread": cpu1, "e2e": e2e, "gpu_launches": int(launches),
             "clocks": clocks,
