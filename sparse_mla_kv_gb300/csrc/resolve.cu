@@ -247,6 +247,7 @@ __global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const
   __shared__ uint32_t s_err;
   __shared__ int s_cnt[3];
   __shared__ int s_lo, s_hi;
+  __shared__ int s_any_dup;  // some plan entry repeats an earlier id
   __shared__ int s_tmp[2 * (kT / 32)];
 
   const int tid = threadIdx.x, lane = tid & 31;
@@ -279,6 +280,7 @@ __global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const
     s_cnt[0] = s_cnt[1] = s_cnt[2] = 0;
     s_lo = INT_MAX;
     s_hi = INT_MIN;
+    s_any_dup = 0;
   }
   const int32_t* tok_g = p.slot_token + state_off;
   const int32_t* stamp_g = p.slot_stamp + state_off;
@@ -468,6 +470,7 @@ __global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const
       if (f >= 0 && f != i) {
         cls = kDup;
         val = f;
+        s_any_dup = 1;
       } else if (f == i) {
         const int off = (unsigned)id % S;
         const int e = s_val[i];
@@ -561,7 +564,7 @@ __global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const
   // the gather's miss warps store the row they read once into every position of the id.  s_slot (dead
   // since phase 2) becomes the chain heads: s_slot[f] = the last-linked repeat of first occurrence f;
   // a repeat's per-position source holds the link to the next one, -3 - next (-2 ends the chain).
-  const bool chains = msrc_g != nullptr && e == 0u && tot_miss > 0;  // uniform
+  const bool chains = msrc_g != nullptr && e == 0u && tot_miss > 0 && s_any_dup;  // uniform
   if (chains) {
     for (int i = tid; i < n; i += kT) s_slot[i] = -1;
     __syncthreads();
