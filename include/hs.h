@@ -230,8 +230,8 @@ hs_status hs_resolve_gather(const hs_pool* pool, int32_t layer_begin, int32_t nl
                             const hs_hot_state* hot, int32_t step, int32_t* out_rows, int32_t* out_stats,
                             void* out, void* workspace, size_t workspace_bytes, hs_stream_t stream);
 
-/* First half of hs_resolve_gather (one launch): everything hs_resolve_topk does except the miss
- * copies.  Rows, stats and hot state are final; the victims' pool rows are NOT yet filled -- the
+/* First half of hs_resolve_gather (one launch; two with the ordered miss layout, whose counters a
+ * small kernel clears first): everything hs_resolve_topk does except the miss copies.  Rows, stats and hot state are final; the victims' pool rows are NOT yet filled -- the
  * per-position host sources wait in `workspace` for hs_gather_planned, which must follow on the same
  * stream before anything reads those rows.  Same arguments as hs_resolve_topk. */
 hs_status hs_resolve_plan(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P,
@@ -243,8 +243,8 @@ hs_status hs_resolve_plan(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
 /* Second half of hs_resolve_gather (one launch): gathers all nl*R*P*K rows named by out_rows into
  * `out`, taking miss rows from the pinned host pool as recorded by hs_resolve_plan in `workspace`
  * and filling their hot slots in every layer.  nl, R, P, K, layer_begin, hot (only its capacity and
- * layers_per_index are read), out_rows and workspace must be those of the preceding hs_resolve_plan
- * call. */
+ * layers_per_index are read), out_rows, workspace and workspace_bytes must be those of the preceding
+ * hs_resolve_plan call, and the pool's miss order (hs_pool_set_miss_order) must not change in between. */
 hs_status hs_gather_planned(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P,
                             int32_t K, const hs_hot_state* hot, const int32_t* out_rows, const void* workspace,
                             size_t workspace_bytes, void* out, hs_stream_t stream);
