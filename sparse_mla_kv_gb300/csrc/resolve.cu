@@ -28,7 +28,11 @@
 //                    batches of 32 (unit, 4-row) items, skips empty ones with one ballot, and copies
 //                    the rows as 16-byte zero-copy loads from the mapped pinned host pool, once for
 //                    each layer of the unit's index group.  Spreading keeps enough loads in flight on
-//                    the host link even when few units miss a lot.
+//                    the host link even when few units miss a lot.  With the ordered layout each
+//                    index group gets its own CTAs, whose warps take the group's 4-entry items in
+//                    bucket (host row range) order.
+//   order_clear_kernel zeroes the ordered layout's bucket counters before the resolver, which is its
+//                    programmatic dependent and waits for it only where it first needs them.
 //
 // IndexShare (one indexer per group of G sparse-MLA layers): the group's layers resolve the same ids
 // against the same tables at the same step, so one unit per (group, request) decides for all of
