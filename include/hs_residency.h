@@ -34,10 +34,11 @@
  *     not admitted, a failed append leaves the context unchanged (blocks taken for its new pages are
  *     returned); releases made before the failure stay (each leaves a valid state).
  *
- * Typical decode step: hs_res_append for each request's new tokens; hs_res_take_fills (the model
- * writes those blocks); hs_res_tables and hs_res_take_resets (copied to the device: tables, and
- * hs_hot_reset_requests for the listed requests); the resolver and gather; hs_res_touch with the
- * step's top-K; after the forward pass hs_res_collect and one hs_offload_pages launch with the pairs.
+ * Typical decode step: hs_res_append_all (or hs_res_append per request) for the new tokens;
+ * hs_res_take_fills (the model writes those blocks); hs_res_tables and hs_res_take_resets (copied to the
+ * device: tables, and hs_hot_reset_requests for the listed requests); the resolver and gather;
+ * hs_res_touch_all (or hs_res_touch per request) with the step's top-K; after the forward pass
+ * hs_res_collect and one hs_offload_pages launch with the pairs.
  *
  * Not thread-safe: one caller at a time per manager.
  */
@@ -72,6 +73,13 @@ hs_status hs_res_admit(hs_residency* m, int32_t r, int32_t ctx_len, const int32_
 /* n_tokens >= 0 tokens appended to active request r: each page that starts gets a GPU block (a fill),
  * each page that completes gets a host block and a queued offload. */
 hs_status hs_res_append(hs_residency* m, int32_t r, int32_t n_tokens);
+
+/* hs_res_append for every request r with n_tokens[r] != 0, in request order (n_tokens is a host array
+ * [max_requests]; zero entries, e.g. of inactive requests, are skipped).  One call per decode step
+ * instead of one per request.  Stops at the first failing request and returns its status: the
+ * requests before it keep their appends, it is left as a failed hs_res_append leaves it, and the
+ * requests after it are not appended. */
+hs_status hs_res_append_all(hs_residency* m, const int32_t* n_tokens);
 
 /* The indexer selected ids[0..n) of request r at decode step `step` (non-decreasing across calls):
  * their pages' last use becomes `step`.  Ids outside [0, ctx_len) are ignored. */

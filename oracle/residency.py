@@ -206,6 +206,13 @@ class Residency:
         for p in range(old // self.S, new // self.S):
             self._complete(r, p)
 
+    def append_all(self, n_tokens) -> None:
+        """append() for every request with a non-zero entry of n_tokens [max_requests], in request order;
+        the first failure stops the call (earlier appends stay)."""
+        for r, n in enumerate(n_tokens):
+            if int(n) != 0:
+                self.append(r, int(n))
+
     def touch(self, r: int, ids, step: int) -> None:
         """The pages of the indexer's selected ids were used at `step` (non-decreasing)."""
         self._check_req(r, True)

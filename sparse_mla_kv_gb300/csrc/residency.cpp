@@ -2,15 +2,16 @@
 //
 // Data structures: the free GPU blocks and the free host blocks are min-heaps (lowest id first; a
 // host entry is valid only while its block has no reference, so stale entries are skipped lazily).
-// Each request keeps, besides its page tables, the ordered set of its releasable pages keyed by
+// Each request keeps, besides its page tables, its releasable pages in a doubly-linked list sorted by
 // (last use, page); a page's membership is recomputed whenever one of its conditions changes, so
-// choosing a victim costs one set lookup per request.
+// choosing a victim reads one list head per request.  A touch moves pages to the newest step, which
+// sorts after every other key: they are unlinked and appended in page order, O(1) each (a page
+// entering the list for another reason is placed by a walk from the tail, where recent keys are).
 #include <algorithm>
 #include <cstdint>
 #include <functional>
 #include <new>
 #include <queue>
-#include <set>
 #include <utility>
 #include <vector>
 
@@ -25,10 +26,29 @@ struct Request {
   int32_t ctx = 0;
   std::vector<int32_t> bt, hbt, lu;
   std::vector<char> pending;       // offload queued, not yet collected
-  std::vector<char> in_set;        // page is in `releasable`
+  std::vector<char> in_set;        // page is in the releasable list
   bool leased = false;             // hot buffer leased (possibly in progress)
   std::vector<int32_t> hot;
-  std::set<std::pair<int32_t, int32_t>> releasable;  // (last use, page)
+  // releasable pages, ascending (last use, page): head = the coldest; -1 ends the list
+  std::vector<int32_t> nxt, prv;
+  int32_t head = -1, tail = -1;
+
+  bool before(int32_t a, int32_t b) const { return lu[a] < lu[b] || (lu[a] == lu[b] && a < b); }
+  void unlink(int32_t p) {
+    const int32_t a = prv[p], b = nxt[p];
+    (a >= 0 ? nxt[a] : head) = b;
+    (b >= 0 ? prv[b] : tail) = a;
+  }
+  // links p at its place, searching from the tail (its key must not be in the list yet)
+  void link_sorted(int32_t p) {
+    int32_t q = tail;
+    while (q >= 0 && before(p, q)) q = prv[q];
+    const int32_t b = q >= 0 ? nxt[q] : head;
+    prv[p] = q;
+    nxt[p] = b;
+    (q >= 0 ? nxt[q] : head) = p;
+    (b >= 0 ? prv[b] : tail) = p;
+  }
 };
 
 struct QueuedCopy {
@@ -49,6 +69,7 @@ struct hs_residency {
   std::vector<int32_t> host_ref, host_held;
   int32_t host_free_count = 0;
   std::vector<Request> req;
+  std::vector<int32_t> moved;  // touch's scratch (kept between calls)
   std::vector<QueuedCopy> queue;
   std::vector<int32_t> resets;
   std::vector<Fill> fills;
@@ -85,8 +106,8 @@ struct hs_residency {
     if (p < 0 || p >= max_pages) return;
     const bool want = releasable_now(x, p);
     if (want == (bool)x.in_set[p]) return;
-    if (want) x.releasable.insert({x.lu[p], p});
-    else x.releasable.erase({x.lu[p], p});
+    if (want) x.link_sorted(p);
+    else x.unlink(p);
     x.in_set[p] = want;
   }
   void set_ctx(Request& x, int32_t ctx) {
@@ -98,22 +119,22 @@ struct hs_residency {
   // ------------------------------------------------------------------ allocation under pressure
   bool pick_cold(int32_t r, int32_t* q_out, int32_t* p_out) const {
     const Request& own = req[r];
-    if (!own.releasable.empty()) {
+    if (own.head >= 0) {
       *q_out = r;
-      *p_out = own.releasable.begin()->second;
+      *p_out = own.head;
       return true;
     }
     bool found = false;
     int32_t best_lu = 0, best_q = 0, best_p = 0;
     for (int32_t q = 0; q < (int32_t)req.size(); ++q) {
       const Request& x = req[q];
-      if (q == r || !x.active || x.releasable.empty()) continue;
-      const auto& e = *x.releasable.begin();
-      if (!found || e.first < best_lu) {  // ties on last use: the lower request index (scanned first)
+      if (q == r || !x.active || x.head < 0) continue;
+      const int32_t lu = x.lu[x.head];
+      if (!found || lu < best_lu) {  // ties on last use: the lower request index (scanned first)
         found = true;
-        best_lu = e.first;
+        best_lu = lu;
         best_q = q;
-        best_p = e.second;
+        best_p = x.head;
       }
     }
     *q_out = best_q;
@@ -180,19 +201,26 @@ struct hs_residency {
 
   int32_t page_of(int32_t t) const { return S_shift >= 0 ? (t >> S_shift) : t / S; }
 
+  // The pages of ids[0..n) were used at `step` (not older than any last use).  A releasable page whose
+  // last use changes is unlinked, and all of them are linked again in page order: with the new key
+  // (step, page) each lands at the tail, behind any page touched earlier in this step with a lower id.
   void touch(int32_t r, const int32_t* ids, int64_t n, int32_t step) {
     Request& x = req[r];
+    moved.clear();
     for (int64_t i = 0; i < n; ++i) {
       const int32_t t = ids[i];
       if (t < 0 || t >= x.ctx) continue;
       const int32_t p = page_of(t);
       if (x.lu[p] == step) continue;
       if (x.in_set[p]) {
-        x.releasable.erase({x.lu[p], p});
-        x.releasable.insert({step, p});
+        x.unlink(p);
+        moved.push_back(p);
       }
       x.lu[p] = step;
     }
+    std::sort(moved.begin(), moved.end());
+    for (const int32_t p : moved) x.link_sorted(p);
+    moved.clear();
   }
 
   void init_request(int32_t r, int32_t ctx) {
@@ -205,6 +233,9 @@ struct hs_residency {
     x.lu.assign(max_pages, -1);
     x.pending.assign(max_pages, 0);
     x.in_set.assign(max_pages, 0);
+    x.nxt.assign(max_pages, -1);
+    x.prv.assign(max_pages, -1);
+    x.head = x.tail = -1;
   }
 };
 
@@ -308,6 +339,16 @@ hs_status hs_res_append(hs_residency* m, int32_t r, int32_t n_tokens) {
   }
   m->set_ctx(x, (int32_t)nw);
   for (int32_t p = (int32_t)(old / S); p < (int32_t)(nw / S); ++p) m->complete(r, p);
+  return HS_OK;
+}
+
+hs_status hs_res_append_all(hs_residency* m, const int32_t* n_tokens) {
+  if (!m || !n_tokens) return HS_ERR_INVALID_ARG;
+  for (int32_t r = 0; r < (int32_t)m->req.size(); ++r) {
+    if (n_tokens[r] == 0) continue;
+    const hs_status st = hs_res_append(m, r, n_tokens[r]);
+    if (st != HS_OK) return st;
+  }
   return HS_OK;
 }
 

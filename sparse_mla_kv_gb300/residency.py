@@ -26,6 +26,8 @@ def _lib():
         L.hs_res_admit.argtypes = [p, i32, i32, P32, i32]
         L.hs_res_append.restype = i32
         L.hs_res_append.argtypes = [p, i32, i32]
+        L.hs_res_append_all.restype = i32
+        L.hs_res_append_all.argtypes = [p, P32]
         L.hs_res_touch.restype = i32
         L.hs_res_touch.argtypes = [p, i32, P32, i64, i32]
         L.hs_res_touch_all.restype = i32
@@ -92,6 +94,15 @@ class Residency:
     def append(self, r: int, n: int) -> None:
         _check(_lib().hs_res_append(self.h, r, n), "hs_res_append")
 
+    def append_all(self, n_tokens) -> None:
+        """n_tokens [max_requests]: append() for every request with a non-zero entry, in request order,
+        in one call."""
+        arr = np.ascontiguousarray(np.asarray(n_tokens, dtype=np.int32).reshape(-1))
+        if arr.size != self.R:
+            raise ValueError("n_tokens must have max_requests entries")
+        _check(_lib().hs_res_append_all(self.h, arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))),
+               "hs_res_append_all")
+
     def touch(self, r: int, ids, step: int) -> None:
         arr, ptr = _i32(ids)
         _check(_lib().hs_res_touch(self.h, r, ptr, arr.size, step), "hs_res_touch")
@@ -153,12 +164,22 @@ class Residency:
         _check(_lib().hs_res_take_fills(self.h, bp, rp, pp, b.size, ctypes.byref(n)), "hs_res_take_fills")
         return [(int(b[i]), int(r[i]), int(p[i])) for i in range(n.value)]
 
-    def tables(self):
-        """(block_table [R][max_pages], host_block_table [R][max_pages], hot_blocks [R][Hc], ctx_len [R])."""
-        bt = np.empty((self.R, self.max_pages), np.int32)
-        hbt = np.empty((self.R, self.max_pages), np.int32)
-        hot = np.empty((self.R, max(1, self.Hc)), np.int32)
-        ctx = np.empty(self.R, np.int32)
+    def tables(self, out=None):
+        """(block_table [R][max_pages], host_block_table [R][max_pages], hot_blocks [R][Hc], ctx_len [R]).
+        out: a tuple returned by an earlier call, refilled in place (no new arrays; e.g. pinned buffers
+        that are then copied to the device)."""
+        if out is None:
+            bt = np.empty((self.R, self.max_pages), np.int32)
+            hbt = np.empty((self.R, self.max_pages), np.int32)
+            hot = np.empty((self.R, max(1, self.Hc)), np.int32)
+            ctx = np.empty(self.R, np.int32)
+        else:
+            bt, hbt, hot, ctx = out
+            hot = hot.base if hot.base is not None and hot.shape[1] != max(1, self.Hc) else hot
+            for a, shape in ((bt, (self.R, self.max_pages)), (hbt, (self.R, self.max_pages)),
+                             (hot, (self.R, max(1, self.Hc))), (ctx, (self.R,))):
+                if a.dtype != np.int32 or a.shape != shape or not a.flags.c_contiguous:
+                    raise ValueError("out must be the arrays of an earlier tables() call")
         P = ctypes.POINTER(ctypes.c_int32)
         _check(_lib().hs_res_tables(self.h, bt.ctypes.data_as(P), hbt.ctypes.data_as(P), hot.ctypes.data_as(P),
                                     ctx.ctypes.data_as(P)), "hs_res_tables")
