@@ -216,9 +216,16 @@ def random_ops(seed: int, n_ops: int):
             pref = [int(x) for x in rng.integers(0, H, npref)]
             ops.append(("admit", r, ctx, pref))
         elif u < 0.55:
-            ops.append(("append", r, int(rng.integers(0, 2 * S + 1))))
+            if rng.random() < 0.15:   # every request at once (zero for some; inactive ones fail the call)
+                counts = [int(x) if rng.random() < 0.7 else 0 for x in rng.integers(0, 2 * S + 1, R)]
+                ops.append(("append_all", counts))
+            else:
+                ops.append(("append", r, int(rng.integers(0, 2 * S + 1))))
         elif u < 0.75:
-            ops.append(("touch", r, [int(x) for x in rng.integers(-1, max_pages * S, 4)], step))
+            if rng.random() < 0.3:
+                ops.append(("touch_all", [[int(x) for x in rng.integers(-1, max_pages * S, 4)] for _ in range(R)], step))
+            else:
+                ops.append(("touch", r, [int(x) for x in rng.integers(-1, max_pages * S, 4)], step))
             step += int(rng.integers(0, 2))
         elif u < 0.90:
             ops.append(("collect",))
@@ -240,6 +247,10 @@ def apply_op(m, op):
             return m.append(op[1], op[2])
         if kind == "touch":
             return m.touch(op[1], op[2], op[3])
+        if kind == "append_all":
+            return m.append_all(op[1])
+        if kind == "touch_all":
+            return m.touch_all(np.array(op[1], np.int32), op[2])
         if kind == "collect":
             return m.collect()
         if kind == "hold":
