@@ -69,7 +69,8 @@ struct hs_residency {
   std::vector<int32_t> host_ref, host_held;
   int32_t host_free_count = 0;
   std::vector<Request> req;
-  std::vector<int32_t> moved;  // touch's scratch (kept between calls)
+  std::vector<int32_t> moved;   // touch's scratch (kept between calls)
+  std::vector<uint64_t> seen;   // touch's page bits
   std::vector<QueuedCopy> queue;
   std::vector<int32_t> resets;
   std::vector<Fill> fills;
@@ -207,18 +208,43 @@ struct hs_residency {
   void touch(int32_t r, const int32_t* ids, int64_t n, int32_t step) {
     Request& x = req[r];
     moved.clear();
-    for (int64_t i = 0; i < n; ++i) {
-      const int32_t t = ids[i];
-      if (t < 0 || t >= x.ctx) continue;
-      const int32_t p = page_of(t);
-      if (x.lu[p] == step) continue;
-      if (x.in_set[p]) {
-        x.unlink(p);
-        moved.push_back(p);
-      }
-      x.lu[p] = step;
+    // pass 1: the pages of the valid ids, as bits, in four interleaved bitmaps (the ids of one request
+    // fall on few words, and four independent read-modify-write chains run about 3x faster than one);
+    // pass 2: each page once, in page order
+    const uint32_t ctx = (uint32_t)x.ctx;  // one unsigned compare rejects negative ids too
+    const int32_t words = (max_pages + 63) / 64;
+    const size_t stride = (size_t)words + 1;  // word `words` of each bitmap absorbs the invalid ids
+    seen.assign(4 * stride, 0);
+    uint64_t* const bm = seen.data();
+    const uint32_t sink = (uint32_t)words * 64;
+    auto page = [&](uint32_t t) -> uint32_t {
+      return t < ctx ? (S_shift >= 0 ? t >> S_shift : t / (uint32_t)S) : sink;
+    };
+    int64_t i = 0;
+    for (; i + 4 <= n; i += 4) {
+      const uint32_t p0 = page((uint32_t)ids[i]), p1 = page((uint32_t)ids[i + 1]);
+      const uint32_t p2 = page((uint32_t)ids[i + 2]), p3 = page((uint32_t)ids[i + 3]);
+      bm[p0 >> 6] |= uint64_t(1) << (p0 & 63);
+      bm[stride + (p1 >> 6)] |= uint64_t(1) << (p1 & 63);
+      bm[2 * stride + (p2 >> 6)] |= uint64_t(1) << (p2 & 63);
+      bm[3 * stride + (p3 >> 6)] |= uint64_t(1) << (p3 & 63);
     }
-    std::sort(moved.begin(), moved.end());
+    for (; i < n; ++i) {
+      const uint32_t p0 = page((uint32_t)ids[i]);
+      bm[p0 >> 6] |= uint64_t(1) << (p0 & 63);
+    }
+    int32_t* lu = x.lu.data();
+    for (int32_t w = 0; w < words; ++w) {
+      for (uint64_t b = bm[w] | bm[stride + w] | bm[2 * stride + w] | bm[3 * stride + w]; b; b &= b - 1) {
+        const int32_t p = w * 64 + __builtin_ctzll(b);
+        if (lu[p] == step) continue;
+        if (x.in_set[p]) {
+          x.unlink(p);
+          moved.push_back(p);
+        }
+        lu[p] = step;
+      }
+    }
     for (const int32_t p : moved) x.link_sorted(p);
     moved.clear();
   }
