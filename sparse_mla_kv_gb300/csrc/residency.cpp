@@ -482,14 +482,20 @@ hs_status hs_res_tables(const hs_residency* m, int32_t* block_table, int32_t* ho
                         int32_t* ctx_len) {
   if (!m) return HS_ERR_INVALID_ARG;
   const int64_t P = m->max_pages, H = m->Hc;
-  for (int64_t r = 0; r < (int64_t)m->req.size(); ++r) {
+  for (int64_t r = 0; r < (int64_t)m->req.size(); ++r) {  // whole rows: plain copies or fills
     const Request& x = m->req[r];
-    for (int64_t p = 0; p < P; ++p) {
-      if (block_table) block_table[r * P + p] = x.active ? x.bt[p] : -1;
-      if (host_block_table) host_block_table[r * P + p] = x.active ? x.hbt[p] : -1;
+    if (block_table) {
+      if (x.active) std::copy(x.bt.begin(), x.bt.end(), block_table + r * P);
+      else std::fill(block_table + r * P, block_table + (r + 1) * P, -1);
     }
-    for (int64_t k = 0; k < H; ++k)
-      if (hot_blocks) hot_blocks[r * H + k] = (x.active && x.leased && (int64_t)x.hot.size() == H) ? x.hot[k] : -1;
+    if (host_block_table) {
+      if (x.active) std::copy(x.hbt.begin(), x.hbt.end(), host_block_table + r * P);
+      else std::fill(host_block_table + r * P, host_block_table + (r + 1) * P, -1);
+    }
+    if (hot_blocks) {
+      if (x.active && x.leased && (int64_t)x.hot.size() == H) std::copy(x.hot.begin(), x.hot.end(), hot_blocks + r * H);
+      else std::fill(hot_blocks + r * H, hot_blocks + (r + 1) * H, -1);
+    }
     if (ctx_len) ctx_len[r] = x.active ? x.ctx : 0;
   }
   return HS_OK;

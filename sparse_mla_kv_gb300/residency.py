@@ -137,6 +137,8 @@ class Residency:
 
     def collect(self) -> List[Tuple[int, int]]:
         n_q = self.counts()[0]
+        if n_q == 0:
+            return []
         g, gp = _i32(np.zeros(max(1, n_q)))
         hb, hp = _i32(np.zeros(max(1, n_q)))
         n = ctypes.c_int32()
@@ -150,6 +152,8 @@ class Residency:
 
     def take_resets(self) -> List[int]:
         n_r = self.counts()[1]
+        if n_r == 0:
+            return []
         a, ap = _i32(np.zeros(max(1, n_r)))
         n = ctypes.c_int32()
         _check(_lib().hs_res_take_resets(self.h, ap, a.size, ctypes.byref(n)), "hs_res_take_resets")
@@ -157,6 +161,8 @@ class Residency:
 
     def take_fills(self) -> List[Tuple[int, int, int]]:
         n_f = self.counts()[2]
+        if n_f == 0:
+            return []
         b, bp = _i32(np.zeros(max(1, n_f)))
         r, rp = _i32(np.zeros(max(1, n_f)))
         p, pp = _i32(np.zeros(max(1, n_f)))
