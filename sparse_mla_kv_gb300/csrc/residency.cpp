@@ -200,8 +200,6 @@ struct hs_residency {
     fills.erase(std::remove_if(fills.begin(), fills.end(), [r](const Fill& f) { return f.r == r; }), fills.end());
   }
 
-  int32_t page_of(int32_t t) const { return S_shift >= 0 ? (t >> S_shift) : t / S; }
-
   // The pages of ids[0..n) were used at `step` (not older than any last use).  A releasable page whose
   // last use changes is unlinked, and all of them are linked again in page order: with the new key
   // (step, page) each lands at the tail, behind any page touched earlier in this step with a lower id.
