@@ -1,5 +1,6 @@
-"""bench.py's reference arm (the oracle timed on the host cores) on CPU: one JSON line with the keys the
-benchmark contract names, and a rank-1 process of a two-rank launch exits without work."""
+"""bench.py's host legs on CPU: the reference arm (the oracle timed on the host cores) prints one JSON line
+with the keys the benchmark contract names, a rank-1 process of a two-rank launch exits without work, and the
+residency-manager leg times the native manager and its oracle."""
 import json
 import os
 import subprocess
@@ -38,3 +39,14 @@ def test_reference_arm_other_ranks_exit_without_work():
              env={"RANK": "1", "LOCAL_RANK": "1", "WORLD_SIZE": "2", "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": "29555"})
     assert p.returncode == 0, p.stderr[-2000:]
     assert not [l for l in p.stdout.splitlines() if l.startswith("{")]
+
+
+def test_residency_leg_times_native_and_oracle():
+    p = _run(["--residency", "--steps", "3", "--warmup", "1", "--requests", "8"])
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["unit"] == "steps/s" and d["value"] > 0 and d["steps"] == 3 and d["warmup"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] > 0
+    assert d["config"]["requests"] == 8
