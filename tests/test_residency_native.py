@@ -76,3 +76,42 @@ def test_native_manager_on_a_pressure_scenario(native):
     released = sum(1 for r in range(R) for p in range(P) if o.reqs[r].bt[p] < 0 and o.reqs[r].hbt[p] >= 0)
     assert released > 0
     n.close()
+
+
+def test_native_manager_on_a_larger_decode_loop(native):
+    """16 requests with growing contexts over a pool of about 60% of their demand, 512 top-K ids each per
+    step (batched appends and touches, as a serving loop calls them): the native manager and the oracle
+    agree on every export after every step, and pages are released and leased along the way."""
+    from synth import workloads
+    R, S, K, Hc, P = 16, 16, 512, 8, 256
+    rng = np.random.default_rng(21)
+    ctx = [40 * S] * R
+    G = int(0.6 * R * (ctx[0] // S + 30 + Hc))
+    o = ores.Residency(G, 1 << 16, S, R, P, Hc)
+    n = native(G, 1 << 16, S, R, P, Hc)
+    for r in range(R):
+        for m in (o, n):
+            m.admit(r, ctx[r])
+    assert o.collect() == n.collect()
+    assert o.take_fills() == n.take_fills()
+    prev = [None] * R
+    for step in range(30):
+        grow = rng.integers(1, 2 * S, R).astype(np.int32)
+        for m in (o, n):
+            m.append_all(grow)
+        ids = np.empty((R, K), np.int32)
+        for r in range(R):
+            ctx[r] += int(grow[r])
+            ids[r] = workloads.next_topk(rng, prev[r], ctx[r], K, 0.8 if prev[r] is not None else 0.0, "recency")
+            prev[r] = ids[r]
+        assert o.take_fills() == n.take_fills()
+        assert o.take_resets() == n.take_resets()
+        for m in (o, n):
+            m.touch_all(ids, step)
+        assert o.collect() == n.collect()
+        _same_tables(o, n)
+        assert o.free_gpu_blocks() == n.free_gpu_blocks()
+        check_invariants(o, G)
+    released = sum(1 for r in range(R) for p in range(P) if o.reqs[r].bt[p] < 0 and o.reqs[r].hbt[p] >= 0)
+    assert released > 0
+    n.close()
