@@ -198,7 +198,7 @@ __device__ unsigned short* radix_sort_slots(unsigned short* a, unsigned short* b
     for (int i = tid; i < kEntries; i += kT) hist[i] = 0;
     __syncthreads();
     for (int e = w0 + lane; e < w1; e += 32) {
-      const uint32_t d = ((uint32_t)(s_stamp[a[e]] - lo) >> shift) & 0xFFu;
+      const uint32_t d = (((uint32_t)s_stamp[a[e]] - (uint32_t)lo) >> shift) & 0xFFu;
       atomicAdd(&hist[d * kSortWarps + warp], 1);
     }
     __syncthreads();
@@ -215,7 +215,7 @@ __device__ unsigned short* radix_sort_slots(unsigned short* a, unsigned short* b
       const int e = e0 + lane;
       const bool valid = e < w1;
       const unsigned short slot = valid ? a[e] : (unsigned short)0;
-      const uint32_t d = valid ? (((uint32_t)(s_stamp[slot] - lo) >> shift) & 0xFFu) : 0u;
+      const uint32_t d = valid ? ((((uint32_t)s_stamp[slot] - (uint32_t)lo) >> shift) & 0xFFu) : 0u;
       const uint32_t key = valid ? d : (0x100u + (uint32_t)lane);
       const uint32_t peers = __match_any_sync(kFull, key);
       const int rank = __popc(peers & ((1u << lane) - 1u));
@@ -551,8 +551,10 @@ __global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const
       for (int s = q0; s < q1; ++s)
         if (s_stamp[s] < step) buf_a[k++] = (unsigned short)s;
       __syncthreads();
-      const int span = s_hi - s_lo;
-      const int bits = span > 0 ? 32 - __clz(span) : 0;
+      // the span of the candidates' stamps, in unsigned arithmetic: any two int32 stamps differ by less
+      // than 2^32, so keys stamp - lo are exact as uint32 (up to four 8-bit passes)
+      const uint32_t span = (uint32_t)s_hi - (uint32_t)s_lo;
+      const int bits = span ? 32 - __clz((int)span) : 0;
       sorted = radix_sort_slots<kT>(buf_a, buf_b, tot_cand, s_stamp, s_lo, (bits + 7) / 8, hist, s_tmp);
     }
   }
