@@ -274,11 +274,17 @@ hs_status hs_offload_pages(const hs_pool* pool, const int32_t* gpu_blocks, const
  * convenience.  Same arguments and results as hs_resolve_topk, minus the workspace: the scratch is a
  * static __device__ array of HS_STATIC_SCRATCH_BYTES inside the library, held by every GPU that loads
  * the library until the process exits.  No call allocates anything.
- *   - Returns HS_ERR_INVALID_ARG when hs_resolve_workspace_bytes_min(nl, R, P, K, capacity) exceeds
- *     HS_STATIC_SCRATCH_BYTES (about 340 units of the MTP3 shape P*K = 8192, C = 4096, or about 800
- *     units of K = 2048, C = 4096).  The ordered miss layout is used only where it fits too.
- *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress, with
- *     that device current); make that first call before any stream capture.
+ *   - Returns HS_ERR_INVALID_ARG when hs_resolve_workspace_bytes_min(nl / G, R, P, K, capacity)
+ *     exceeds HS_STATIC_SCRATCH_BYTES, with G = hot->layers_per_index (the resolver's units are
+ *     index groups; G = 1 without IndexShare): about 340 units of the MTP3 shape P*K = 8192,
+ *     C = 4096, or about 800 units of K = 2048, C = 4096.  The ordered miss layout is used only where
+ *     it fits too.
+ *   - Returns HS_ERR_INVALID_ARG when the current device is not the pool's device.
+ *   - The first call in each CUDA context looks up the array's device address (cudaGetSymbolAddress,
+ *     with the pool's device current) and caches it for that context; make that first call before
+ *     any stream capture.  A context created anew (after cudaDeviceReset, or after the primary
+ *     context was released) is a new context: its first call looks the address up again, so it too
+ *     should come before any capture.
  *   - Every call shares the one array and it keeps the last call's contents (nothing in it needs to
  *     start at zero).  Calls whose executions overlap on the GPU -- on different streams, or from
  *     different threads without ordering -- race on it; order them on one stream. */

@@ -64,6 +64,8 @@ MissOrder call_miss_order(const hs_pool* pool, int32_t nl, int64_t ng, int32_t R
 
 void count_launch(int k) { g_launches.fetch_add(k, std::memory_order_relaxed); }
 
+int pool_device(const hs_pool* pool) { return pool ? pool->device : -1; }
+
 }  // namespace hs
 
 extern "C" {

@@ -159,6 +159,8 @@ cudaError_t launch_reset_requests(int32_t* tok, int32_t* stamp, int32_t groups, 
                                   const int32_t* requests, int32_t n, int sms, cudaStream_t s);
 
 void count_launch(int k = 1);
+// The device a pool was created on (its device pointers belong to it).
+int pool_device(const hs_pool* pool);
 
 // The item index of an index group's ordered misses, kept in shared memory (one per CTA): item i
 // (up to kMissRowsPerItem consecutive entries of one bucket, or of the overflow list) -> its first

@@ -11,35 +11,79 @@
 // Every GPU that loads this library's code holds that array until the process exits.
 //
 // In host code the array's name is only a host-side stand-in, not a device address; the device
-// address comes from cudaGetSymbolAddress, taken once per device with that device current, and is
-// then passed to the kernels like any caller workspace.
+// address comes from cudaGetSymbolAddress, taken with the pool's device current, and is then passed
+// to the kernels like any caller workspace.  The address belongs to the CUDA context that loaded the
+// module: it is cached per context, keyed on the context's unique id (a context created after
+// cudaDeviceReset has a new id, so its address is looked up again).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
 
-#include "hs.h"
+#include "hs_internal.cuh"
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_resolve_scratch[HS_STATIC_SCRATCH_BYTES];
 
-std::mutex g_scratch_mu;
-void* g_scratch_addr[64] = {};
+// The driver's context queries, reached through the runtime so that the library does not link the
+// driver library directly.
+typedef CUresult(CUDAAPI* CtxGetCurrentFn)(CUcontext*);
+typedef CUresult(CUDAAPI* CtxGetIdFn)(CUcontext, unsigned long long*);
 
-// Device address of g_resolve_scratch on device `dev` (which must be current), set up on first use.
+struct ScratchCache {
+  unsigned long long ctx_id = 0;  // 0: nothing cached (context ids start at 1)
+  void* addr = nullptr;
+};
+
+std::mutex g_scratch_mu;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+bool g_ctx_fns_tried = false;
+ScratchCache g_scratch[64];
+
+// The unique id of the current context (0 if it cannot be read).  Caller holds g_scratch_mu.
+unsigned long long current_ctx_id() {
+  if (!g_ctx_fns_tried) {
+    g_ctx_fns_tried = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f);
+    cudaGetLastError();
+  }
+  if (!g_ctx_get_current || !g_ctx_get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of g_resolve_scratch in the current context of device `dev` (which must be
+// current).  Looked up on the first call in each context.
 hs_status scratch_address(int dev, void** out) {
   if (dev < 0 || dev >= 64) return HS_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  const unsigned long long id = current_ctx_id();
+  ScratchCache& c = g_scratch[dev];
+  if (id == 0 || c.ctx_id != id || !c.addr) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_resolve_scratch);
     if (e != cudaSuccess || p == nullptr) {
       cudaGetLastError();
+      c = ScratchCache{};
       return HS_ERR_CUDA;
     }
-    g_scratch_addr[dev] = p;
+    c.addr = p;
+    c.ctx_id = id;  // id 0 (context id unreadable): looked up again on every call
   }
-  *out = g_scratch_addr[dev];
+  *out = c.addr;
   return HS_OK;
 }
 
@@ -62,6 +106,8 @@ extern "C" hs_status hs_resolve_topk_noalloc(const hs_pool* pool, int32_t layer_
     cudaGetLastError();
     return HS_ERR_CUDA;
   }
+  // the scratch must live on the pool's GPU: its array is looked up in the current device's context
+  if (dev != hs::pool_device(pool)) return HS_ERR_INVALID_ARG;
   void* scratch = nullptr;
   const hs_status st = scratch_address(dev, &scratch);
   if (st != HS_OK) return st;

@@ -5,7 +5,8 @@ nearly all device memory for its KV cache, a decode loop that must not let cudaM
 the device, or a C caller with no device allocator.  This entry point takes no workspace; its scratch
 is a fixed-size array compiled into the library.  The test calls it through the C ABI (ctypes on
 libhs.so) and checks, on two calls in a row, that its rows, stats, hot state and pool bytes equal
-those of hs_resolve_topk given a caller-allocated workspace (tolerance 0: integer and byte work).
+those of hs_resolve_topk given a caller-allocated workspace (tolerance 0: integer and byte work),
+with and without IndexShare (several layers reading one top-K list, whose units are index groups).
 This file is collected last on purpose, so a run that stops at the first failure has already run
 every other test; it also passes on its own in a fresh process.
 """
@@ -83,6 +84,81 @@ def test_noalloc_matches_workspace_entry_point_twice(lib, cfg):
         assert torch.equal(hot_a.slot_token, hot_b.slot_token)
         assert torch.equal(hot_a.slot_stamp, hot_b.slot_stamp)
         assert torch.equal(gpu_a[0], gpu_b[0])
+    pool_a.close()
+    pool_b.close()
+
+
+def _group_inputs(rng, R, ctx, K, ng, prev=None):
+    """[ng][R][1][K] distinct ids per (group, request); half of each list kept from prev."""
+    out = np.empty((ng, R, 1, K), np.int32)
+    for g in range(ng):
+        for r in range(R):
+            if prev is None:
+                out[g, r, 0] = rng.choice(ctx, size=K, replace=False)
+            else:
+                keep = rng.choice(prev[g, r, 0], size=K // 2, replace=False)
+                rest = np.setdiff1d(np.arange(ctx), keep)
+                out[g, r, 0] = rng.permutation(np.concatenate([keep, rng.choice(rest, size=K - K // 2, replace=False)]))
+    return out
+
+
+@pytest.mark.parametrize("G,R", [(2, 16), (4, 256)])
+def test_noalloc_index_share_matches_workspace_entry_point_twice(lib, G, R):
+    """IndexShare (G layers per index group): the scratch bound counts index groups, so a shape with
+    4 layers x 256 requests (1024 per-layer units, beyond the built-in array) is accepted with G = 4
+    (256 units); rows, stats, hot state and the pool bytes of every layer equal those of
+    hs_resolve_topk given a caller workspace, on two calls in a row."""
+    import sparse_mla_kv_gb300 as hs
+    dev = torch.device("cuda")
+    rng = np.random.default_rng(G * 1000 + R)
+    L, S, B, K, C, P = 4, 64, 16, 2048, 4096, 1
+    pages, tail = 128, 16
+    ctx = pages * S
+    ng = L // G
+    assert hs.resolve_workspace_bytes_min(ng, R, P, K, C) <= HS_STATIC_SCRATCH_BYTES
+    if R == 256:   # the per-layer count alone would not fit
+        assert hs.resolve_workspace_bytes_min(L, R, P, K, C) > HS_STATIC_SCRATCH_BYTES
+    n_res = R * tail
+    perm = rng.permutation(n_res + R * (C // S)).astype(np.int32)
+    bt = np.full((R, pages), -1, np.int32)
+    bt[:, pages - tail:] = perm[:n_res].reshape(R, tail)
+    hot_blocks = perm[n_res:].reshape(R, C // S)
+    hbt = rng.permutation(R * pages).astype(np.int32).reshape(R, pages)
+    ngb = n_res + R * (C // S)
+    host = [torch.randint(0, 256, (R * pages, S, B), dtype=torch.uint8).pin_memory() for _ in range(L)]
+    base = [torch.randint(0, 256, (ngb, S, B), dtype=torch.uint8, device=dev) for _ in range(L)]
+    sides = []
+    for _ in range(2):
+        gpu = [b.clone() for b in base]
+        pool = hs.Pool(gpu, host)
+        hot = hs.HotState.allocate(L, torch.from_numpy(hot_blocks).to(dev), C, layers_per_index=G)
+        hs.hot_reset(pool, hot)
+        sides.append((pool, gpu, hot))
+    (pool_a, gpu_a, hot_a), (pool_b, gpu_b, hot_b) = sides
+    bt_d, hbt_d = torch.from_numpy(bt).to(dev), torch.from_numpy(hbt).to(dev)
+    ctx_d = torch.full((R,), ctx, dtype=torch.int32, device=dev)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    ids = None
+    for step in (5, 6):   # two calls in a row
+        ids = _group_inputs(rng, R, ctx, K, ng, ids)
+        topk = torch.from_numpy(ids).to(dev)
+        rows_a, stats_a = hs.resolve_topk(pool_a, topk, bt_d, hbt_d, ctx_d, hot_a, step)
+        rows_b = torch.empty_like(topk)
+        stats_b = torch.empty((ng, R, 4), dtype=torch.int32, device=dev)
+        code = lib.hs_resolve_topk_noalloc(pool_b.handle, 0, L, R, P, K, ctypes.c_void_p(topk.data_ptr()),
+                                           ctypes.c_void_p(bt_d.data_ptr()), ctypes.c_void_p(hbt_d.data_ptr()),
+                                           ctypes.c_void_p(ctx_d.data_ptr()), pages, ctypes.byref(hot_b.c), step,
+                                           ctypes.c_void_p(rows_b.data_ptr()), ctypes.c_void_p(stats_b.data_ptr()),
+                                           stream)
+        assert code == 0, hs.status_str(code)
+        torch.cuda.synchronize()
+        assert (stats_a[..., 0] == 0).all() and int(stats_a[..., 3].sum()) > 0
+        assert torch.equal(stats_a, stats_b)
+        assert torch.equal(rows_a, rows_b)
+        assert torch.equal(hot_a.slot_token, hot_b.slot_token)
+        assert torch.equal(hot_a.slot_stamp, hot_b.slot_stamp)
+        for l in range(L):
+            assert torch.equal(gpu_a[l], gpu_b[l]), f"layer {l}"
     pool_a.close()
     pool_b.close()
 
