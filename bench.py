@@ -1,22 +1,27 @@
 #!/usr/bin/env python3
-"""Benchmark of the Hybrid HiSparse decode hot path (resolve + gather, + offload when pages complete).
+"""Benchmark of the Hybrid HiSparse decode hot path (resolve + gather, + offload of completed pages).
 
-Default workload: the mixed-residency decode batch -- 1 sparse-MLA layer, 64 requests, context
-131,072 tokens each (tail 16,384 tokens resident, older pages host-only with a full pinned host copy),
-page 64, 656-byte rows, K=2048, hot buffer 4096 rows per request; each step keeps 80% of the previous
-top-K and draws the rest with probability proportional to recency^-0.7.  Synthetic, seeded.
+Default workload: the max batch with speculative decode (MTP3) at full size -- 4 sparse-MLA layers,
+256 requests with contexts log-uniform in [8192, 1,048,576] tokens, each non-tail page resident with
+a per-request probability f ~ U[0, 1] (the tail always resident, host copies of the host-only pages:
+about 80 GB of GPU pool and 80 GB of pinned host pool), page 64, 656-byte rows, K = 2048, P = 4 query
+positions sharing one plan (90% overlap), hot buffer 4096 rows per request; each step appends 1-4
+tokens per request and ends with one offload launch of the pages it completed (all layers).
+8,388,608 resolved rows per step.  Synthetic, seeded.  --config 1..4 select the other workloads
+(tiny decode, the mixed-residency batch, multi-turn agentic decode, cold start with prefix reuse).
 
 One step = the fused path (hs_resolve_plan + hs_gather_planned: the resolver, then one gather that
 also carries the miss copies) or, with --path split, hs_resolve_topk + hs_gather_rows, over the
-step's batch, then one hs_offload_pages launch for the pages the step completes (all layers).  The
-default workload's contexts are fixed, so its steps complete no page; --config 3 (multi-turn agentic,
-contexts growing, block reuse) and --config 5 (MTP3 max batch) offload every step, and take
---layers-per-index (IndexShare) and, for 5, --capacity (the (num_spec + 2) * K hot sizing).  Table
+step's batch, then one hs_offload_pages launch for the pages the step completes (all layers).  Table
 edits and the model's page writes of a step are applied before its timed events.  L2 is flushed (a
 256 MB write) before every timed step, outside the timed events, and the host waits for each step
-before enqueueing the next.
+before enqueueing the next.  With --timing graph (or both) each timed step is also captured as one
+CUDA graph and replayed once.
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on the host cores instead.
+The oracle legs (the reference arm and the cpu_baseline of the GPU line) run on the first requests
+of the same workload, as many as keep the oracle's byte pools within a few GB (all of them for
+configs 1, 2 and 4), with their block ids renumbered densely; rows/s adds over independent requests.
 """
 from __future__ import annotations
 
@@ -44,10 +49,10 @@ L2_FLUSH_BYTES = 256 << 20
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--requests", type=int, default=None, help="requests per rank (configs 2-5)")
     ap.add_argument("--layers", type=int, default=None, help="sparse-MLA layers (configs 3, 5)")
     ap.add_argument("--layers-per-index", type=int, default=1,
@@ -78,9 +83,22 @@ def parse():
     ap.add_argument("--residency", action="store_true",
                     help="time the host-side residency manager (native and its oracle) on a decode loop under "
                          "KV pressure instead of the GPU path; host only")
+    ap.add_argument("--link-probe", action="store_true",
+                    help="measure the miss path's host-link rate against the span of host memory it reads "
+                         "(one layer, all-miss steps) instead of a workload")
+    ap.add_argument("--probe-pool-gb", type=float, default=72.0, help="pinned host pool of the link probe")
+    ap.add_argument("--probe-windows-gb", type=float, nargs="+", default=[1, 4, 10, 20, 40, 72],
+                    help="spans of the host pool the link probe's misses read")
     ap.add_argument("--miss-order", choices=["auto", "on", "off"], default="auto",
                     help="miss layout handed to the copy warps: auto (the library's default: host-address order "
                          "for host pools of 16 GiB or more), on (always address order), off (per-unit lists)")
+    ap.add_argument("--timing", choices=["auto", "eager", "graph", "both"], default="auto",
+                    help="eager: the C-ABI calls of each timed step bracketed by events; graph: each timed step "
+                         "captured as one CUDA graph and replayed once, the replay bracketed by events; both: "
+                         "eager is the headline and the graph replay is reported beside it; auto: both for host "
+                         "pools under 16 GiB, eager alone above")
+    ap.add_argument("--oracle-pool-gb", type=float, default=8.0,
+                    help="the oracle legs run on the first requests whose byte pools fit in this many GB")
     ap.add_argument("--path", choices=["fused", "split"], default="fused",
                     help="fused: hs_resolve_plan + hs_gather_planned (miss copies inside the gather); "
                          "split: hs_resolve_topk (resolver + miss-copy kernel) + hs_gather_rows")
@@ -170,6 +188,75 @@ class Tables:
         return bool(len(st.bt_edits) or len(st.hbt_edits))
 
 
+def subset_workload(w, steps, n_req: int):
+    """The first n_req requests of a workload and of its steps, with the GPU and host blocks they use
+    renumbered densely (0, 1, ... in their original order), so that byte pools for them stay small.
+    Requests are independent units: their rows, hits, misses, copies and offloads are the same as in
+    the whole batch, only at other block addresses.  Returns (workload, steps)."""
+    import dataclasses
+    from synth.workloads import Step
+    if n_req >= w.R:
+        return w, steps
+    n = n_req
+    g_used = [w.block_table[:n][w.block_table[:n] >= 0].ravel(), w.hot_blocks[:n].ravel()]
+    h_used = [w.host_block_table[:n][w.host_block_table[:n] >= 0].ravel()]
+    for st in steps:
+        e = st.bt_edits[st.bt_edits[:, 0] < n]
+        g_used.append(e[e[:, 2] >= 0, 2])
+        e = st.hbt_edits[st.hbt_edits[:, 0] < n]
+        h_used.append(e[e[:, 2] >= 0, 2])
+        m = st.off_src[:, 0] < n if len(st.off_src) else np.zeros(0, bool)
+        g_used.append(st.off_gpu[m])
+        h_used.append(st.off_host[m])
+        g_used.append(st.fills[st.fills[:, 1] < n, 0])
+    gu = np.unique(np.concatenate([np.asarray(x, np.int64) for x in g_used]))
+    hu = np.unique(np.concatenate([np.asarray(x, np.int64) for x in h_used]))
+    gmap = np.full(w.num_gpu_blocks, -1, np.int64)
+    gmap[gu] = np.arange(len(gu))
+    hmap = np.full(max(1, w.num_host_blocks), -1, np.int64)
+    hmap[hu] = np.arange(len(hu))
+
+    def remap(a, m):
+        a = np.asarray(a)
+        out = a.astype(np.int64).copy()
+        ok = a >= 0
+        out[ok] = m[a[ok]]
+        return out.astype(a.dtype)
+
+    def remap_edits(e, m):
+        e = e[e[:, 0] < n].copy()
+        e[:, 2] = remap(e[:, 2], m)
+        return e
+
+    bt = remap(w.block_table[:n], gmap)
+    hbt = remap(w.host_block_table[:n], hmap)
+    keep_g = w.gpu_resident_init[w.gpu_resident_init[:, 0] < n]
+    keep_h = w.host_resident_init[w.host_resident_init[:, 0] < n]
+    sub = dataclasses.replace(w, R=n, block_table=bt, host_block_table=hbt, content_page=w.content_page[:n],
+                              hot_blocks=remap(w.hot_blocks[:n], gmap), ctx_len=w.ctx_len[:n],
+                              num_gpu_blocks=max(1, len(gu)), num_host_blocks=len(hu),
+                              host_resident_init=keep_h, gpu_resident_init=keep_g)
+    out = []
+    for st in steps:
+        m = st.off_src[:, 0] < n if len(st.off_src) else np.zeros(0, bool)
+        fills = st.fills[st.fills[:, 1] < n].copy()
+        fills[:, 0] = remap(fills[:, 0], gmap)
+        out.append(Step(index=st.index, topk=np.ascontiguousarray(st.topk[:, :n]), ctx_len=st.ctx_len[:n].copy(),
+                        bt_edits=remap_edits(st.bt_edits, gmap), hbt_edits=remap_edits(st.hbt_edits, hmap),
+                        fills=fills, off_gpu=remap(st.off_gpu[m], gmap).astype(np.int32),
+                        off_host=remap(st.off_host[m], hmap).astype(np.int32), off_src=st.off_src[m]))
+    return sub, out
+
+
+def oracle_requests(w, steps, pool_gb: float) -> int:
+    """How many leading requests the oracle legs take: all of them when their byte pools (GPU mirror
+    and host pool, every layer) fit in pool_gb, else proportionally fewer (at least one)."""
+    total = w.L * (w.num_gpu_blocks + max(1, w.num_host_blocks)) * w.S * w.B
+    if total <= pool_gb * 1e9:
+        return w.R
+    return max(1, min(w.R, int(w.R * pool_gb * 1e9 / total)))
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -179,15 +266,27 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_record(kernel: str, src: str):
-    """dram bytes per launch from a committed ncu summary, if taken on the current kernel source."""
+def traffic_record(kernel: str, src: str, rows: int):
+    """DRAM bytes per launch of `kernel` from a committed ncu summary, if it was taken on the current
+    kernel source: as captured when the capture processed `rows` rows, else scaled by rows when the
+    summary says its traffic grows in proportion to the rows (a smaller case of the same workload)."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
-        d = json.load(open(p))[kernel]
+        recs = json.load(open(p))[kernel]
     except Exception:
         return None
     sha = hashlib.sha256(open(os.path.join(ROOT, "sparse_mla_kv_gb300", "csrc", src), "rb").read()).hexdigest()
-    return d if d.get("source_sha256") == sha else None
+    recs = recs if isinstance(recs, list) else [recs]
+    for d in recs:
+        if d.get("source_sha256") != sha:
+            continue
+        if d.get("rows") == rows:
+            return dict(d, source=d.get("capture", "ncu"))
+    for d in recs:
+        if d.get("source_sha256") == sha and d.get("scales_with_rows") and d.get("rows"):
+            return dict(d, dram_bytes_per_launch=d["dram_bytes_per_launch"] * rows / d["rows"],
+                        source=f"{d.get('capture', 'ncu')}, scaled by rows ({d['rows']} -> {rows})")
+    return None
 
 
 class ClockSampler:
@@ -281,7 +380,9 @@ def run_reference(args, ws, rank):
         return 0
     import oracle
     oracle.build()
-    w, steps = make_workload(args, args.seed, args.warmup + args.steps)
+    w_full, steps_full = make_workload(args, args.seed, args.warmup + args.steps)
+    n_req = oracle_requests(w_full, steps_full, args.oracle_pool_gb)
+    w, steps = subset_workload(w_full, steps_full, n_req)
     threads = oracle.default_threads()
     S, B = w.S, w.B
     pools = [np.full(w.num_gpu_blocks * S * B, 7, np.uint8) for _ in range(w.L)]
@@ -298,13 +399,15 @@ def run_reference(args, ws, rank):
         if i >= args.warmup:
             t_timed += dt
     value = args.steps * w.rows_per_step / t_timed
+    part = "" if n_req == w_full.R else (f", on its first {n_req} of {w_full.R} requests (block ids renumbered; "
+                                          f"{w.rows_per_step} of {w_full.rows_per_step} rows per step)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_timed / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": config_dict(w, args),
+        "config": config_dict(w_full, args),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"{args.steps} timed steps of the workload (after {args.warmup} warm-up), "
+                         "sample": f"{args.steps} timed steps of the workload (after {args.warmup} warm-up){part}; "
                                    "resolve with miss copies + gather + offload, host cores"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -555,6 +658,45 @@ def run_ours(args, ws, rank, local):
     t_gat = [ev_s[k][1].elapsed_time(ev_s[k][3]) * 1e-3 for k in range(K)]
     t_off = [ev_s[k][3].elapsed_time(ev_s[k][2]) * 1e-3 for k in range(K)]
     t_step_split = [ev_s[k][0].elapsed_time(ev_s[k][2]) * 1e-3 for k in range(K)]
+
+    # graph pass: the same timed steps, each captured as one CUDA graph (untimed; its kernels and
+    # arguments fixed at capture, the tables read at replay) and replayed once behind an L2 flush, the
+    # replay bracketed by events.  The host enqueues one graph instead of the step's C-ABI calls.
+    timing = args.timing
+    if timing == "auto":
+        timing = "both" if host_pool_bytes < (16 << 30) else "eager"
+    graph = None
+    if timing in ("graph", "both"):
+        replay_warmup()
+        n0 = hs.launch_count()
+        graphs = []
+        for k in range(K):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                phase1(W + k)
+                phase2()
+                phase3(W + k)
+            graphs.append(g)
+        nodes = hs.launch_count() - n0
+        stats_g = torch.empty_like(stats_all)
+        ev_g = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        for k in range(K):
+            before(W + k)
+            flush.fill_(k & 0xFF)
+            ev_g[k][0].record(stream)
+            graphs[k].replay()
+            ev_g[k][1].record(stream)
+            stats_g[k].copy_(out_stats, non_blocking=True)
+            ev_g[k][1].synchronize()
+        torch.cuda.synchronize()
+        assert np.array_equal(stats_g.cpu().numpy(), st_all), "the graph replays resolved differently"
+        t_graph = [ev_g[k][0].elapsed_time(ev_g[k][1]) * 1e-3 for k in range(K)]
+        sum_g = max_over_ranks(dist, float(sum(t_graph)), dev)
+        graph = {"value": ws * w.rows_per_step * K / sum_g, "unit": UNIT, "ms_per_step": 1e3 * sum_g / K,
+                 "step_us_median": 1e6 * statistics.median(t_graph), "kernels_per_step": nodes / K,
+                 "timing": "each timed step captured as one CUDA graph, replayed once behind an L2 flush; "
+                           "events around the replay"}
+        del graphs
     h2d_gbs, d2h_gbs = link_peaks()
 
     sum_t = max_over_ranks(dist, float(sum(t_step)), dev)
@@ -564,6 +706,13 @@ def run_ours(args, ws, rank, local):
     rows_per_step = w.rows_per_step
     value = ws * rows_per_step * K / sum_t
     ms_per_step = 1e3 * sum_t / K
+    headline_timing = "eager C-ABI calls, CUDA events on the launch stream"
+    t_head = t_step
+    if timing == "graph":
+        t_head = t_graph
+        value, ms_per_step = graph["value"], graph["ms_per_step"]
+        launches = int(round(graph["kernels_per_step"] * K))
+        headline_timing = graph["timing"]
 
     # roofline of the dominant kernel (the gather; fused path: the gather that also carries the miss
     # copies): algorithmic HBM bytes per launch / mean launch time from the events around it.
@@ -575,19 +724,28 @@ def run_ours(args, ws, rank, local):
     m_mean = float(counts[:, 2].mean())
     gather_bytes = n_rows * (2 * B + (8 if fused else 4))
     t_g = statistics.fmean(t_gat)
-    achieved = gather_bytes / t_g / 1e9
-    tr = traffic_record("gather_kernel_fused" if fused else "gather_kernel", "gather.cu")
+    tr = traffic_record("gather_kernel_fused" if fused else "gather_kernel", "gather.cu", n_rows)
+    # The fused gather moves its miss rows over the host link while it streams the other rows from HBM:
+    # its roof is the slower of the two, each against its own peak -- HBM against the measured copy
+    # peak, the host link against this run's bulk pinned host-to-device copy rate (MEASURED_PEAKS
+    # holds no link figure)
     link_bytes = m_mean * G * B if fused else 0.0
-    roofline = {"bound": "hbm", "kernel": "gather_kernel<fused>" if fused else "gather_kernel",
-                "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                "peak_kind": peak_kind, "algorithmic_bytes_per_launch": gather_bytes,
+    t_hbm_roof = gather_bytes / (hbm_peak * 1e9)
+    t_link_roof = link_bytes / (h2d_gbs * 1e9)
+    hbm_part = {"achieved": gather_bytes / t_g / 1e9, "peak": hbm_peak, "unit": "GB/s", "frac": t_hbm_roof / t_g,
+                "peak_kind": peak_kind, "algorithmic_bytes_per_launch": gather_bytes}
+    link_part = {"achieved": link_bytes / t_g / 1e9, "peak": h2d_gbs, "unit": "GB/s", "frac": t_link_roof / t_g,
+                 "peak_kind": "measured in this run: bulk pinned host-to-device cudaMemcpyAsync, 256 MB, best of 5",
+                 "algorithmic_bytes_per_launch": link_bytes}
+    bound = "host_link" if t_link_roof > t_hbm_roof else "hbm"
+    main = link_part if bound == "host_link" else hbm_part
+    roofline = {"bound": bound, "kernel": "gather_kernel<fused>" if fused else "gather_kernel",
+                "achieved": main["achieved"], "peak": main["peak"], "unit": "GB/s", "frac": main["frac"],
+                "peak_kind": main["peak_kind"], "algorithmic_bytes_per_launch": main["algorithmic_bytes_per_launch"],
                 "timing": "mean launch time from the split pass (events between the calls)",
-                "host_link_bytes_per_launch": link_bytes,
-                # the fused gather's miss rows come over the host link: its rate against this run's
-                # bulk pinned-copy rate
-                "host_link_achieved_gbs": link_bytes / t_g / 1e9,
-                "host_link_peak_gbs": h2d_gbs, "host_link_frac": link_bytes / t_g / 1e9 / h2d_gbs,
-                "traffic": (tr["dram_bytes_per_launch"] if tr and tr.get("rows") == n_rows else None)}
+                "components": {"hbm": hbm_part, "host_link": link_part},
+                "traffic": tr["dram_bytes_per_launch"] if tr else None,
+                "traffic_source": tr.get("source") if tr else None}
 
     # whole-step roofline: max(HBM bytes / HBM peak, miss bytes / H2D rate, offload bytes / D2H rate),
     # step by step with each step's own miss and offload counts
@@ -598,7 +756,7 @@ def run_ours(args, ws, rank, local):
         n_off = len(steps[W + k].off_gpu) * L
         hbm_step = n_rows * (2 * B + 16) + NG * R * 8 * C + m * (B + 8) + n_off * page_bytes
         roofs.append(max(hbm_step / (hbm_peak * 1e9), m * B / (h2d_gbs * 1e9), n_off * page_bytes / (d2h_gbs * 1e9)))
-        meas.append(t_step[k])
+        meas.append(t_head[k])
     # the post-forward offload (a9): its launches in the split pass, bytes moved over the link / time
     off_k = [k for k in range(K) if len(steps[W + k].off_gpu)]
     offload = None
@@ -613,7 +771,7 @@ def run_ours(args, ws, rank, local):
                  "frac": sum(roofs) / sum(meas), "misses_per_step_mean": m_mean,
                  "offloaded_pages_per_step_mean": statistics.fmean(len(steps[W + k].off_gpu) for k in range(K)),
                  "h2d_gbs_measured_bulk_copy": h2d_gbs, "d2h_gbs_measured_bulk_copy": d2h_gbs, "path": args.path,
-                 "step_us_median": 1e6 * statistics.median(t_step),
+                 "step_us_median": 1e6 * statistics.median(t_head),
                  "split_pass": "phase times from a second pass over the same steps with events between the "
                                "calls (they stop the gather launch from overlapping the resolver)",
                  "phase1_us_mean": 1e6 * statistics.fmean(t_res), "phase2_us_mean": 1e6 * t_g,
@@ -621,6 +779,7 @@ def run_ours(args, ws, rank, local):
                  "phase1_us_median": 1e6 * statistics.median(t_res), "phase2_us_median": 1e6 * statistics.median(t_gat),
                  "phase2_us_max": 1e6 * max(t_gat), "split_step_us_median": 1e6 * statistics.median(t_step_split),
                  "phase2_us_all": [round(1e6 * x, 1) for x in t_gat],
+                 "step_us_all": [round(1e6 * x, 1) for x in t_head],
                  "phase1": "hs_resolve_plan" if fused else "hs_resolve_topk (resolver + miss copy)",
                  "phase2": "hs_gather_planned" if fused else "hs_gather_rows",
                  "phase3": "hs_offload_pages", "offload": offload}
@@ -691,24 +850,30 @@ def run_ours(args, ws, rank, local):
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
-        v, n_done, thr = oracle_run(w, steps, args.cpu_seconds)
+        n_req = oracle_requests(w, steps, args.oracle_pool_gb)
+        w_o, steps_o = subset_workload(w, steps, n_req)
+        part = "" if n_req == w.R else (f" on its first {n_req} of {w.R} requests (block ids renumbered; "
+                                        f"{w_o.rows_per_step} rows per step)")
+        v, n_done, thr = oracle_run(w_o, steps_o, args.cpu_seconds)
         cpu = {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
-               "sample": f"{n_done} steps of this workload (restarting from an empty hot state), resolve with "
-                         f"miss copies + gather + offload, about {args.cpu_seconds:.0f} s of host time"}
-        v1, n1, _ = oracle_run(w, steps, args.cpu_seconds / 4, threads=1)
+               "sample": f"{n_done} steps of this workload{part}, restarting from an empty hot state after its "
+                         f"{len(steps_o)} steps; resolve with miss copies + gather + offload, about "
+                         f"{args.cpu_seconds:.0f} s of host time"}
+        v1, n1, _ = oracle_run(w_o, steps_o, args.cpu_seconds / 4, threads=1)
         cpu1 = {"value": v1, "unit": UNIT, "cores": 1, "kind": "oracle",
-                "sample": f"{n1} steps, one host thread, about {args.cpu_seconds / 4:.0f} s"}
+                "sample": f"{n1} steps{part}, one host thread, about {args.cpu_seconds / 4:.0f} s"}
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": W,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "u8", "data": "synthetic",
-            "config": dict(config_dict(w, args), miss_order=miss_order,
+            "config": dict(config_dict(w, args), miss_order=miss_order, timing=headline_timing,
                            settle_passes=len(settle_medians),
                            settle_step_us_medians=[round(1e3 * m, 1) for m in settle_medians]),
             "gathered_gbs": value * B / 1e9, "roofline": roofline, "step_roofline": step_roof,
             "cpu_baseline": cpu, "cpu_baseline_1thread": cpu1, "e2e": e2e, "gpu_launches": int(launches),
+            "graph_replay": graph,
             "clocks": clocks,
             "wall_s_timed_region": wall, "timed_counts": {"resident": int(hits_misses[0]),
                                                           "hits": int(hits_misses[1]),
@@ -797,11 +962,133 @@ def run_residency(args):
     return 0
 
 
+def run_link_probe(args):
+    """Rate of the library's miss path against the span of pinned host memory its misses touch.
+
+    One layer, 64 requests, K = 2048, hot buffers of 4096 rows, 656-byte rows, page 64.  The requests
+    share one host prefix that fills a window of the pinned host pool (their host tables point at the
+    same host blocks, in a seeded permutation); each request's last page is resident.  The pool has
+    --probe-pool-gb of pinned, device-mapped, huge-page host memory, written by DMA from the device;
+    only the window is read.  Every step empties the hot buffers first (untimed), so each of the step's
+    R x K uniform top-K ids on a host page is a miss.  Per (window, miss order) the same steps are timed
+    three ways with events: hs_resolve_topk (resolver + miss-copy kernel), hs_resolve_plan (the
+    resolver alone) and hs_resolve_plan + hs_gather_planned (the fused gather, which carries the
+    misses).  The miss copy's time is the first minus the second, step by step.  Host pools and the
+    order of the reads, not the bytes, change between the rows of the table."""
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    from sparse_mla_kv_gb300 import _build
+    _build.build()
+    import sparse_mla_kv_gb300 as hs
+    from sparse_mla_kv_gb300.hostmem import pinned_host_pool
+    S, B, K, C, R = 64, 656, 2048, 4096, args.requests or 64
+    page = S * B
+    pool_bytes = int(args.probe_pool_gb * 1e9) // page * page
+    nhb = pool_bytes // page
+    windows = sorted({min(nhb, int(g * 1e9) // page) for g in args.probe_windows_gb})
+    host = pinned_host_pool((nhb, S, B))
+    # written by DMA from the device (host memory last written by CPU stores reads slowly through the GPU)
+    dbuf = torch.arange(1 << 30, dtype=torch.int64, device=dev).to(torch.uint8)
+    flat = host.view(-1)
+    for o in range(0, flat.numel(), dbuf.numel()):
+        n_ = min(dbuf.numel(), flat.numel() - o)
+        flat[o:o + n_].copy_(dbuf[:n_], non_blocking=True)
+    torch.cuda.synchronize()
+    del dbuf
+    ngb = R * (C // S) + R
+    gpu = torch.zeros((ngb, S, B), dtype=torch.uint8, device=dev)
+    pool = hs.Pool([gpu], [host])
+    hot_blocks = torch.arange(R * (C // S), dtype=torch.int32, device=dev).reshape(R, C // S)
+    hot = hs.HotState.allocate(1, hot_blocks, C)
+    ws_buf = hs.alloc_workspace(1, R, 1, K, C, dev)
+    out_rows = torch.empty((1, R, 1, K), dtype=torch.int32, device=dev)
+    out_stats = torch.empty((1, R, 4), dtype=torch.int32, device=dev)
+    gout = torch.empty((1, R * K, B), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    rng = np.random.default_rng(args.seed)
+    n_steps = args.warmup + args.steps
+    table = []
+    for wb in windows:
+        max_pages = wb + 1
+        ctx_n = max_pages * S
+        hrow = rng.permutation(wb).astype(np.int32)
+        bt = torch.full((R, max_pages), -1, dtype=torch.int32, device=dev)
+        bt[:, wb] = torch.arange(R * (C // S), R * (C // S) + R, dtype=torch.int32, device=dev)
+        hbt = torch.full((R, max_pages), -1, dtype=torch.int32, device=dev)
+        hbt[:, :wb] = torch.from_numpy(hrow).to(dev)[None, :]
+        ctx = torch.full((R,), ctx_n, dtype=torch.int32, device=dev)
+        topk = []
+        for _ in range(n_steps):
+            ids = np.empty((R, K), np.int32)
+            for r in range(R):
+                c = rng.integers(0, wb * S, size=3 * K)
+                _, first = np.unique(c, return_index=True)
+                ids[r] = c[np.sort(first)][:K]
+            topk.append(torch.from_numpy(ids.reshape(1, R, 1, K)).to(dev))
+        prep = hs.PreparedStep(pool, hot, bt, hbt, ctx, out_rows, out_stats, ws_buf, gout)
+        for order, mode in (("per-unit lists", hs.MISS_ORDER_OFF), ("host-address buckets", hs.MISS_ORDER_ON)):
+            pool.set_miss_order(mode)
+
+            def timed(call):
+                ts = []
+                for i in range(n_steps):
+                    hs.hot_reset(pool, hot)
+                    flush.fill_(i & 0xFF)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    call(i)
+                    e1.record(stream)
+                    e1.synchronize()
+                    if i >= args.warmup:
+                        ts.append(e0.elapsed_time(e1) * 1e3)
+                return ts
+
+            def split(i):
+                prep.resolve(topk[i], 1)
+
+            def plan(i):
+                prep.plan(topk[i], 1)
+
+            def fused(i):
+                prep.plan(topk[i], 1)
+                prep.gather_planned()
+
+            med = []
+            t0 = time.time()
+            while True:   # settle: until two passes agree within 5% (reads of fresh pinned memory start slow)
+                med.append(statistics.median(timed(split)))
+                if len(med) >= 2 and abs(med[-1] - med[-2]) <= 0.05 * med[-2]:
+                    break
+                if time.time() - t0 > args.settle_seconds:
+                    break
+            t_split = timed(split)
+            t_plan = timed(plan)
+            t_fused = timed(fused)
+            misses = int(out_stats[..., 3].sum())
+            t_copy = statistics.median(a - b for a, b in zip(t_split, t_plan))
+            t_fg = statistics.median(a - b for a, b in zip(t_fused, t_plan))
+            table.append({"window_gb": round(wb * page / 1e9, 2), "miss_order": order, "misses_per_step": misses,
+                          "resolver_us": round(statistics.median(t_plan), 1),
+                          "miss_copy_us": round(t_copy, 1), "miss_copy_gbs": round(misses * B / t_copy / 1e3, 1),
+                          "fused_gather_us": round(t_fg, 1), "fused_gather_miss_gbs": round(misses * B / t_fg / 1e3, 1),
+                          "settle_passes": len(med)})
+            print(json.dumps(table[-1]), file=sys.stderr, flush=True)
+    pool.close()
+    print(json.dumps({"metric": "miss-path host-link rate vs span of host memory read", "unit": "GB/s",
+                      "pool_gb": round(pool_bytes / 1e9, 2), "requests": R, "K": K, "row_bytes": B,
+                      "steps": args.steps, "warmup": args.warmup, "table": table,
+                      "how": run_link_probe.__doc__.split("\n\n")[1].replace("\n", " ").strip()}), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     ws, rank, local = dist_env()
     if args.residency:
         return run_residency(args) if rank == 0 else 0
+    if args.link_probe:
+        return run_link_probe(args) if rank == 0 else 0
     if args.impl == "reference":
         return run_reference(args, ws, rank)
     return run_ours(args, ws, rank, local)
