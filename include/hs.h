@@ -301,6 +301,18 @@ const char* hs_status_str(hs_status s);
 /* Number of kernels the library has launched since load (a host-side counter). */
 int64_t hs_launch_count(void);
 
+/* Bounds-checked build of the library (compiled with HS_CHECKED=1; sparse_mla_kv_gb300/libhs_checked.so)
+ * only -- a debugging aid with no counterpart in the pages.  In that build every address a kernel
+ * derives from data it read (a table entry, a slot index, a miss-list entry, a repeat-chain link, an
+ * output position) is checked against the extent of its buffer before the access, and a violation
+ * skips the access and is recorded.  Synchronises the current device, then returns the site of the
+ * first violation recorded since the previous call and clears it:
+ *   0 none; 1 table page; 2 hot-state slot; 3 miss-list index; 4 GPU pool row; 5 host pool row;
+ *   6 output position; 7 repeat-chain link; -2 the device or the record could not be read.
+ * Returns -1 in the normal build, which compiles these checks away (its data errors are reported
+ * through the status words described above). */
+int32_t hs_check_status(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -20,7 +20,9 @@ from typing import Optional, Sequence
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libhs.so")
+# HS_LIB_VARIANT=checked loads the bounds-checked build (libhs_checked.so, see hs_check_status)
+LIB_VARIANT = os.environ.get("HS_LIB_VARIANT", "")
+LIB_PATH = os.path.join(_HERE, f"libhs_{LIB_VARIANT}.so" if LIB_VARIANT else "libhs.so")
 
 HS_OK = 0
 MISS_ORDER_AUTO, MISS_ORDER_OFF, MISS_ORDER_ON = 0, 1, 2
@@ -55,14 +57,16 @@ def lib():
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: build it with sparse_mla_kv_gb300._build.build() "
-                               "(there is no fallback implementation)")
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with sparse_mla_kv_gb300._build.build("
+                               f"variant={LIB_VARIANT!r}) (there is no fallback implementation)")
         L = ctypes.CDLL(LIB_PATH)
         i32, i64, sz, p = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
         L.hs_status_str.restype = ctypes.c_char_p
         L.hs_status_str.argtypes = [i32]
         L.hs_launch_count.restype = i64
         L.hs_launch_count.argtypes = []
+        L.hs_check_status.restype = i32
+        L.hs_check_status.argtypes = []
         L.hs_pool_create.restype = i32
         L.hs_pool_create.argtypes = [ctypes.POINTER(PoolDesc), ctypes.POINTER(p)]
         L.hs_pool_destroy.restype = None
@@ -104,6 +108,12 @@ def status_str(code: int) -> str:
         return lib().hs_status_str(int(code)).decode()
     except RuntimeError:
         return STATUS_NAMES.get(code, str(code))
+
+
+def check_status() -> int:
+    """Bounds-checked build: the first bounds violation recorded since the last call (0 = none); -1 in
+    the normal build.  Synchronises the device."""
+    return int(lib().hs_check_status())
 
 
 def launch_count() -> int:

@@ -24,6 +24,8 @@
 namespace hs {
 namespace {
 
+HS_CHECK_WORD
+
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kGatherThreads = 256;
 constexpr int kGatherUnroll = 8;
@@ -77,12 +79,22 @@ constexpr int kRepeatRegs = 3;  // repeat positions per entry followed before th
 template <int CPR>
 __device__ __forceinline__ void copy_miss_item(const uint8_t* __restrict__ host, uint8_t* __restrict__ pool,
                                                uint8_t* __restrict__ lout, const int32_t* __restrict__ lmsrc,
-                                               int n, int4 ent, int nrows, int row_bytes) {
+                                               int n, int4 ent, int nrows, int row_bytes, int64_t per_layer,
+                                               int64_t gpu_rows, int64_t host_rows) {
   constexpr int kU = CPR ? (kMissRowsPerItem * CPR + 31) / 32 : 4;
   const int cpr = CPR ? CPR : (row_bytes >> 4);
   const int lane = threadIdx.x & 31;
   const int total = nrows * cpr;
-  const int rq = lane < nrows ? ent.z / n : 0;  // the entry's request
+  // checked build: an entry whose host row, pool row or output position lies outside its buffer is
+  // skipped (lanes past nrows hold no entry)
+  const int ok = lane >= nrows || (HS_CHECK(ent.x >= 0 && ent.x < host_rows, kChkHostRow) &&
+                                   HS_CHECK(ent.y >= 0 && ent.y < gpu_rows, kChkPoolRow) &&
+                                   HS_CHECK(ent.z >= 0 && ent.z < per_layer, kChkOutPos));
+  (void)ok;
+  (void)per_layer;
+  (void)gpu_rows;
+  (void)host_rows;
+  const int rq = lane < nrows && ok ? ent.z / n : 0;  // the entry's request
   for (int f0 = 0; f0 < total; f0 += 32 * kU) {
     uint4 v[kU];
 #pragma unroll
@@ -90,20 +102,23 @@ __device__ __forceinline__ void copy_miss_item(const uint8_t* __restrict__ host,
       const int f = f0 + k * 32 + lane;
       const int rr = f < total ? f / cpr : 0;
       const int src = __shfl_sync(kFull, ent.x, rr);
-      if (f < total) v[k] = __ldcg(reinterpret_cast<const uint4*>(host + (int64_t)src * row_bytes) + (f - rr * cpr));
+      const bool row_ok = HS_CHECKED ? __shfl_sync(kFull, ok, rr) != 0 : true;
+      if (f < total && row_ok)
+        v[k] = __ldcg(reinterpret_cast<const uint4*>(host + (int64_t)src * row_bytes) + (f - rr * cpr));
     }
-    int d = lane < nrows ? ent.w : -1;
+    int d = lane < nrows && ok ? ent.w : -1;
     int rep[kRepeatRegs];
 #pragma unroll
     for (int t = 0; t < kRepeatRegs; ++t) {
+      if (d >= 0 && !HS_CHECK(d < n, kChkChain)) d = -1;
       rep[t] = d;
       if (d >= 0) d = -3 - __ldcg(lmsrc + (int64_t)rq * n + d);
     }
 #pragma unroll
     for (int k = 0; k < kU; ++k) {
       const int f = f0 + k * 32 + lane;
-      const bool ok = f < total;
-      const int rr = ok ? f / cpr : 0;
+      const bool in = f < total;
+      const int rr = in ? f / cpr : 0;
       const int64_t cc16 = (int64_t)(f - rr * cpr) * 16;
       const int dst = __shfl_sync(kFull, ent.y, rr);
       const int pos = __shfl_sync(kFull, ent.z, rr);
@@ -111,7 +126,8 @@ __device__ __forceinline__ void copy_miss_item(const uint8_t* __restrict__ host,
       int rp[kRepeatRegs];
 #pragma unroll
       for (int t = 0; t < kRepeatRegs; ++t) rp[t] = __shfl_sync(kFull, rep[t], rr);
-      if (ok) {
+      const bool row_ok = HS_CHECKED ? __shfl_sync(kFull, ok, rr) != 0 : true;
+      if (in && row_ok) {
         *reinterpret_cast<uint4*>(pool + (int64_t)dst * row_bytes + cc16) = v[k];
         *reinterpret_cast<uint4*>(lout + (int64_t)pos * row_bytes + cc16) = v[k];
 #pragma unroll
@@ -119,6 +135,7 @@ __device__ __forceinline__ void copy_miss_item(const uint8_t* __restrict__ host,
           if (rp[t] >= 0) *reinterpret_cast<uint4*>(lout + ((int64_t)q * n + rp[t]) * row_bytes + cc16) = v[k];
       }
     }
+    if (d >= 0 && !HS_CHECK(d < n, kChkChain)) d = -1;
     while (__any_sync(kFull, d >= 0)) {  // longer chains: one link per round
 #pragma unroll
       for (int k = 0; k < kU; ++k) {
@@ -130,6 +147,7 @@ __device__ __forceinline__ void copy_miss_item(const uint8_t* __restrict__ host,
           *reinterpret_cast<uint4*>(lout + ((int64_t)q * n + dd) * row_bytes + (int64_t)(f - rr * cpr) * 16) = v[k];
       }
       if (d >= 0) d = -3 - __ldcg(lmsrc + (int64_t)rq * n + d);
+      if (d >= 0 && !HS_CHECK(d < n, kChkChain)) d = -1;
     }
   }
 }
@@ -139,7 +157,7 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
     const LayerPtrs ptrs, int32_t layer_begin, int32_t group, int32_t R, int32_t n, int32_t max_m,
     const int32_t* __restrict__ rows, const int32_t* __restrict__ miss_count, const int4* __restrict__ miss_list,
     const MissOrder ord, const int32_t* __restrict__ msrc, uint8_t* __restrict__ out, int32_t row_bytes,
-    int64_t num_rows) {
+    int64_t num_rows, int64_t num_host_rows) {
   pdl_wait_prerequisites();   // the resolve plan (rows, sources, miss lists) must be complete and visible
   const int cpr = CPR ? CPR : (row_bytes >> 4);
   const int lr = blockIdx.y;
@@ -168,7 +186,7 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
         mi.locate(ord, i, start, in_ov, nrows);
         int4 ent = make_int4(0, 0, 0, 0);
         if (lane < nrows) ent = (in_ov ? ovl : bk)[start + lane];
-        copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes);
+        copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
       }
       return;
     }
@@ -197,7 +215,7 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
         const int nrows = min(kMissRowsPerItem, c - r0);
         int4 ent = make_int4(0, 0, 0, 0);
         if (lane < nrows) ent = miss_list[((int64_t)pu * R + rq) * max_m + r0 + lane];
-        copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes);
+        copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
       }
     }
     return;
@@ -256,6 +274,20 @@ dim3 wave_grid(int sms, int occ, int64_t want, int nl) {
 
 }  // namespace
 
+uint32_t check_take_gather() {
+#if HS_CHECKED
+  unsigned v = 0u, z = 0u;
+  if (cudaMemcpyFromSymbol(&v, hs_check_word_, sizeof(v)) != cudaSuccess ||
+      cudaMemcpyToSymbol(hs_check_word_, &z, sizeof(z)) != cudaSuccess) {
+    cudaGetLastError();
+    return 0xFFFFFFFFu;
+  }
+  return v;
+#else
+  return 0u;
+#endif
+}
+
 void warm_gather_launch_configs() {
   resident_blocks(gather_kernel<41>, &g_occ_plain[0]);
   resident_blocks(gather_kernel<0>, &g_occ_plain[1]);
@@ -280,7 +312,7 @@ cudaError_t launch_gather(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl
 cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, int32_t group, int32_t R,
                                 int32_t n, int32_t max_m, const int32_t* rows, const int32_t* miss_count,
                                 const int4* miss_list, const MissOrder& ord, const int32_t* msrc, uint8_t* out,
-                                int32_t row_bytes, int64_t num_rows, int sms, cudaStream_t s) {
+                                int32_t row_bytes, int64_t num_rows, int64_t num_host_rows, int sms, cudaStream_t s) {
   int* occ = g_occ_fused;
   const bool k41 = row_bytes == 656;
   auto kern = k41 ? gather_fused_kernel<41> : gather_fused_kernel<0>;
@@ -299,11 +331,11 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
   cudaError_t e;
   if (ord.cnt) {
     kern<<<grid, kGatherThreads, 0, s>>>(ptrs, layer_begin, group, R, n, max_m, rows, miss_count, miss_list, ord, msrc,
-                                         out, row_bytes, num_rows);
+                                         out, row_bytes, num_rows, num_host_rows);
     e = cudaGetLastError();
   } else {
     e = launch_dependent(kern, grid, dim3(kGatherThreads), 0, s, ptrs, layer_begin, group, R, n, max_m, rows,
-                         miss_count, miss_list, ord, msrc, out, row_bytes, num_rows);
+                         miss_count, miss_list, ord, msrc, out, row_bytes, num_rows, num_host_rows);
   }
   if (e != cudaSuccess) return e;
   count_launch();

@@ -87,6 +87,21 @@ const char* hs_status_str(hs_status s) {
 
 int64_t hs_launch_count(void) { return hs::g_launches.load(); }
 
+int32_t hs_check_status(void) {
+#if HS_CHECKED
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return -2;
+  }
+  const uint32_t a = hs::check_take_resolve();
+  const uint32_t b = hs::check_take_gather();
+  if (a == 0xFFFFFFFFu || b == 0xFFFFFFFFu) return -2;
+  return (int32_t)(a ? a : b);
+#else
+  return -1;
+#endif
+}
+
 hs_status hs_pool_create(const hs_pool_desc* d, hs_pool** out) {
   if (!out) return HS_ERR_INVALID_ARG;
   *out = nullptr;
@@ -153,6 +168,7 @@ hs_status hs_pool_set_miss_order(hs_pool* pool, int32_t mode) {
 }
 
 hs_status hs_hot_reset(const hs_pool* pool, const hs_hot_state* hot, int32_t R, hs_stream_t stream) {
+  HS_RANGE("hs_hot_reset");
   if (!pool || !hot || R < 0) return HS_ERR_INVALID_ARG;
   if (hot->capacity < pool->g.page_size || hot->capacity > HS_MAX_CAPACITY || hot->capacity % pool->g.page_size)
     return HS_ERR_INVALID_ARG;
@@ -169,6 +185,7 @@ hs_status hs_hot_reset(const hs_pool* pool, const hs_hot_state* hot, int32_t R, 
 
 hs_status hs_hot_reset_requests(const hs_pool* pool, const hs_hot_state* hot, int32_t R, const int32_t* requests,
                                 int32_t n, hs_stream_t stream) {
+  HS_RANGE("hs_hot_reset_requests");
   if (!pool || !hot || R < 0 || n < 0) return HS_ERR_INVALID_ARG;
   if (hot->capacity < pool->g.page_size || hot->capacity > HS_MAX_CAPACITY || hot->capacity % pool->g.page_size)
     return HS_ERR_INVALID_ARG;
@@ -288,6 +305,7 @@ hs_status hs_resolve_topk(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
                           const int32_t* ctx_len, int32_t max_pages, const hs_hot_state* hot, int32_t step,
                           int32_t* out_rows, int32_t* out_stats, void* workspace, size_t workspace_bytes,
                           hs_stream_t stream) {
+  HS_RANGE("hs_resolve_topk");
   hs::ResolveParams p;
   hs::ResolveSmem sm;
   int sms = 0;
@@ -306,6 +324,7 @@ hs_status hs_resolve_plan(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
                           const int32_t* ctx_len, int32_t max_pages, const hs_hot_state* hot, int32_t step,
                           int32_t* out_rows, int32_t* out_stats, void* workspace, size_t workspace_bytes,
                           hs_stream_t stream) {
+  HS_RANGE("hs_resolve_plan");
   hs::ResolveParams p;
   hs::ResolveSmem sm;
   int sms = 0;
@@ -322,6 +341,7 @@ hs_status hs_resolve_plan(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
 hs_status hs_gather_planned(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P, int32_t K,
                             const hs_hot_state* hot, const int32_t* out_rows, const void* workspace,
                             size_t workspace_bytes, void* out, hs_stream_t stream) {
+  HS_RANGE("hs_gather_planned");
   if (!pool || !hot) return HS_ERR_INVALID_ARG;
   const hs::PoolGeom& g = pool->g;
   if (layer_begin < 0 || nl < 0 || (int64_t)layer_begin + nl > g.num_layers || R < 0 || P < 1 || K < 0)
@@ -347,7 +367,7 @@ hs_status hs_gather_planned(const hs_pool* pool, int32_t layer_begin, int32_t nl
       pool->ptrs, layer_begin, nl, G, R, (int32_t)n, max_m, out_rows, reinterpret_cast<const int32_t*>(ws),
       reinterpret_cast<const int4*>(ws + hs::ws_counts_bytes(units)), ord,
       reinterpret_cast<const int32_t*>(ws + hs::ws_msrc_offset(units, n, capacity)), static_cast<uint8_t*>(out),
-      g.row_bytes, (int64_t)g.num_gpu_blocks * g.page_size, sms, stream));
+      g.row_bytes, (int64_t)g.num_gpu_blocks * g.page_size, (int64_t)g.num_host_blocks * g.page_size, sms, stream));
 }
 
 hs_status hs_resolve_gather(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P, int32_t K,
@@ -355,6 +375,7 @@ hs_status hs_resolve_gather(const hs_pool* pool, int32_t layer_begin, int32_t nl
                             const int32_t* ctx_len, int32_t max_pages, const hs_hot_state* hot, int32_t step,
                             int32_t* out_rows, int32_t* out_stats, void* out, void* workspace,
                             size_t workspace_bytes, hs_stream_t stream) {
+  HS_RANGE("hs_resolve_gather");
   if ((int64_t)P * K > 0 && nl > 0 && R > 0 && (!out || !hs::aligned16(out))) return HS_ERR_INVALID_ARG;
   hs_status st = hs_resolve_plan(pool, layer_begin, nl, R, P, K, topk_ids, block_table, host_block_table, ctx_len,
                                  max_pages, hot, step, out_rows, out_stats, workspace, workspace_bytes, stream);
@@ -364,6 +385,7 @@ hs_status hs_resolve_gather(const hs_pool* pool, int32_t layer_begin, int32_t nl
 
 hs_status hs_gather_rows(const hs_pool* pool, int32_t layer_begin, int32_t nl, const int32_t* rows, int64_t n,
                          void* out, int32_t* out_status, hs_stream_t stream) {
+  HS_RANGE("hs_gather_rows");
   if (!pool) return HS_ERR_INVALID_ARG;
   const hs::PoolGeom& g = pool->g;
   if (layer_begin < 0 || nl < 0 || (int64_t)layer_begin + nl > g.num_layers || n < 0) return HS_ERR_INVALID_ARG;
@@ -379,6 +401,7 @@ hs_status hs_gather_rows(const hs_pool* pool, int32_t layer_begin, int32_t nl, c
 
 hs_status hs_offload_pages(const hs_pool* pool, const int32_t* gpu_blocks, const int32_t* host_blocks, int32_t n,
                            int32_t* out_status, hs_stream_t stream) {
+  HS_RANGE("hs_offload_pages");
   if (!pool || n < 0) return HS_ERR_INVALID_ARG;
   if (n == 0) return HS_OK;
   if (!gpu_blocks || !host_blocks || pool->g.num_host_blocks == 0) return HS_ERR_INVALID_ARG;

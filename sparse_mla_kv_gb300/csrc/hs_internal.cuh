@@ -8,7 +8,71 @@
 
 #include "hs.h"
 
+// NVTX ranges: every entry point that launches work opens one range named after itself in the "hs"
+// domain, so that a timeline of a decode step attributes its time to resolve, gather and offload.
+// Header-only NVTX (v3): with no tool attached a range costs a load and a branch.  HS_NVTX=0 builds
+// without them.
+#ifndef HS_NVTX
+#define HS_NVTX 1
+#endif
+#if HS_NVTX
+#include <nvtx3/nvToolsExt.h>
 namespace hs {
+inline nvtxDomainHandle_t nvtx_domain() {
+  static const nvtxDomainHandle_t d = nvtxDomainCreateA("hs");
+  return d;
+}
+struct NvtxRange {
+  explicit NvtxRange(const char* name) {
+    nvtxEventAttributes_t a{};
+    a.version = NVTX_VERSION;
+    a.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+    a.messageType = NVTX_MESSAGE_TYPE_ASCII;
+    a.message.ascii = name;
+    nvtxDomainRangePushEx(nvtx_domain(), &a);
+  }
+  ~NvtxRange() { nvtxDomainRangePop(nvtx_domain()); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+}  // namespace hs
+#define HS_RANGE(name) const ::hs::NvtxRange hs_nvtx_range_(name)
+#else
+#define HS_RANGE(name) ((void)0)
+#endif
+
+// Bounds-checked build.  Compiled with HS_CHECKED=1, every address a kernel computes from data it read
+// (a table entry, a slot index, a miss-list entry, a chain link, an output position) is checked
+// against the extent of the buffer it points into before the access; a violation skips the access and
+// records the site of the first failing check in a device word of the kernel's file, which
+// hs_check_status reads and clears.  The normal build (HS_CHECKED=0) compiles the checks away and keeps
+// the data checks the ABI documents (status words).
+#ifndef HS_CHECKED
+#define HS_CHECKED 0
+#endif
+#if HS_CHECKED
+#define HS_CHECK_WORD static __device__ unsigned int hs_check_word_ = 0u;
+#define HS_CHECK(cond, site) ((cond) ? true : (atomicCAS(&hs_check_word_, 0u, (unsigned)(site)), false))
+#else
+#define HS_CHECK_WORD
+#define HS_CHECK(cond, site) true
+#endif
+
+namespace hs {
+
+// Sites of the bounds-checked build's checks (the value hs_check_status returns).
+enum CheckSite : uint32_t {
+  kChkTablePage = 1,  // resolver: a page index outside the request's table row
+  kChkStateSlot = 2,  // resolver: a slot index outside the unit's hot state
+  kChkMissList = 3,   // resolver: a miss-list index outside the unit's list
+  kChkPoolRow = 4,    // a GPU pool row outside the pool (miss destination)
+  kChkHostRow = 5,    // a host pool row outside the pinned pool (miss source)
+  kChkOutPos = 6,     // an output position outside the call's output
+  kChkChain = 7,      // a repeat-chain link outside the unit's positions
+};
+// Reads and clears the check word of each kernel file (0 in the normal build).
+uint32_t check_take_resolve();
+uint32_t check_take_gather();
 
 // Per-layer base pointers, passed to kernels by value (kernel parameter space, no device
 // allocation).  host[] holds device-usable addresses of the pinned host pool.
@@ -151,7 +215,7 @@ cudaError_t launch_gather(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl
 cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, int32_t group, int32_t R,
                                 int32_t n, int32_t max_m, const int32_t* rows, const int32_t* miss_count,
                                 const int4* miss_list, const MissOrder& ord, const int32_t* msrc, uint8_t* out,
-                                int32_t row_bytes, int64_t num_rows, int sms, cudaStream_t s);
+                                int32_t row_bytes, int64_t num_rows, int64_t num_host_rows, int sms, cudaStream_t s);
 cudaError_t launch_offload(const LayerPtrs& ptrs, const PoolGeom& g, const int32_t* gpu_blocks,
                            const int32_t* host_blocks, int32_t n, int32_t* status, int sms, cudaStream_t s);
 cudaError_t launch_fill_i32(int32_t* a, int64_t count, int32_t value, int sms, cudaStream_t s);

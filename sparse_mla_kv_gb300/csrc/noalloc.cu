@@ -95,6 +95,7 @@ extern "C" hs_status hs_resolve_topk_noalloc(const hs_pool* pool, int32_t layer_
                                              const int32_t* ctx_len, int32_t max_pages, const hs_hot_state* hot,
                                              int32_t step, int32_t* out_rows, int32_t* out_stats,
                                              hs_stream_t stream) {
+  HS_RANGE("hs_resolve_topk_noalloc");
   if (!pool || !hot) return HS_ERR_INVALID_ARG;
   // Shapes whose scratch would exceed the built-in array are refused before anything else (units are
   // index groups: nl / G of them per request).

@@ -45,6 +45,8 @@
 namespace hs {
 namespace {
 
+HS_CHECK_WORD
+
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kEmpty = -1;
 constexpr int kBadHost = INT_MIN;
@@ -321,8 +323,8 @@ __global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const
         err |= kErrId;
       } else {
         if constexpr (kWide) idh.insert_min(id, i);
-        if (!staged) {
-          const int page = (unsigned)id / S;
+        const int page = (unsigned)id / S;
+        if (!staged && HS_CHECK((unsigned)page < (unsigned)p.max_pages, kChkTablePage)) {
           const int b = bt[page];
           const int h = hbt[page];
           e = b >= 0 ? b : (h < 0 ? -1 : (h >= p.num_host_blocks ? kBadHost : -2 - h));
@@ -398,8 +400,8 @@ __global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const
       const int id = s_ids[i];
       if (id >= 0) {
         int e = s_val[i];
-        if (staged) {
-          const int page = (unsigned)id / S;
+        const int page = (unsigned)id / S;
+        if (staged && HS_CHECK((unsigned)page < (unsigned)sm.tbl_pages, kChkTablePage)) {
           const int b = s_bt[page];
           const int h = s_hbt[page];
           e = b >= 0 ? b : (h < 0 ? -1 : (h >= p.num_host_blocks ? kBadHost : -2 - h));
@@ -607,8 +609,17 @@ __global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const
       const uint8_t cls = s_cls[i];
       if (cls == kMiss) {
         const int v = sorted[j];
+        if (!HS_CHECK((unsigned)v < (unsigned)C, kChkStateSlot) ||
+            !HS_CHECK(ordered || (unsigned)j < (unsigned)p.max_m, kChkMissList)) {
+          ++j;
+          continue;
+        }
         const int vb = (unsigned)v / S;
         const int dst = s_hot[vb] * S + (v - vb * S);
+        if (!HS_CHECK((unsigned)dst < (unsigned)p.num_gpu_blocks * (unsigned)S, kChkPoolRow)) {
+          ++j;
+          continue;
+        }
         const int4 ent = make_int4(s_val[i], dst, r * n + i, chains ? s_slot[i] : -1);
         if (ordered) {
           const int b = min(kMissBuckets - 1, (int)((uint32_t)s_val[i] >> p.ord.shift));
@@ -629,6 +640,7 @@ __global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const
         ++j;
       } else if (cls == kHit) {
         const int v = s_val[i];
+        if (!HS_CHECK((unsigned)v < (unsigned)C, kChkStateSlot)) continue;
         const int vb = (unsigned)v / S;
         p.slot_stamp[state_off + v] = step;
         s_val[i] = s_hot[vb] * S + (v - vb * S);
@@ -689,11 +701,15 @@ constexpr int kCopyThreads = 256;
 // stores.
 template <int CPR>
 __device__ __forceinline__ void copy_miss_rows(const LayerPtrs& ptrs, int l0, int group, int4 ent, int nrows,
-                                               int row_bytes) {
+                                               int row_bytes, int gpu_rows, int host_rows) {
   constexpr int kU = CPR ? (kMissRowsPerItem * CPR + 31) / 32 : 4;
   const int cpr = CPR ? CPR : (row_bytes >> 4);
   const int lane = threadIdx.x & 31;
   const int total = nrows * cpr;
+  // checked build: a lane whose entry points outside either pool has its row skipped
+  const int ok = lane >= nrows || (HS_CHECK((unsigned)ent.x < (unsigned)host_rows, kChkHostRow) &&
+                                   HS_CHECK((unsigned)ent.y < (unsigned)gpu_rows, kChkPoolRow));
+  (void)ok;
   for (int l = l0; l < l0 + group; ++l) {
     const uint8_t* host = ptrs.host[l];
     uint8_t* pool = ptrs.gpu[l];
@@ -703,13 +719,14 @@ __device__ __forceinline__ void copy_miss_rows(const LayerPtrs& ptrs, int l0, in
 #pragma unroll
       for (int k = 0; k < kU; ++k) {
         const int f = f0 + k * 32 + lane;
-        const bool ok = f < total;
-        const int rr = ok ? f / cpr : 0;
+        const bool ok_f = f < total;
+        const int rr = ok_f ? f / cpr : 0;
         const int cc = f - rr * cpr;
         const int src = __shfl_sync(kFull, ent.x, rr);
         const int dst = __shfl_sync(kFull, ent.y, rr);
+        const bool row_ok = HS_CHECKED ? __shfl_sync(kFull, ok, rr) != 0 : true;
         dst_off[k] = -1;
-        if (ok) {
+        if (ok_f && row_ok) {
           v[k] = __ldcg(reinterpret_cast<const uint4*>(host + (int64_t)src * row_bytes) + cc);
           dst_off[k] = (int64_t)dst * row_bytes + (int64_t)cc * 16;
         }
@@ -750,7 +767,7 @@ __global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(const ResolvePa
       mi.locate(p.ord, i, start, in_ov, nrows);
       int4 ent = make_int4(0, 0, 0, 0);
       if (lane < nrows) ent = (in_ov ? ov : bk)[start + lane];
-      copy_miss_rows<CPR>(ptrs, l0, p.group, ent, nrows, row_bytes);
+      copy_miss_rows<CPR>(ptrs, l0, p.group, ent, nrows, row_bytes, p.num_gpu_blocks * p.S, p.num_host_blocks * p.S);
     }
     return;
   }
@@ -780,7 +797,8 @@ __global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(const ResolvePa
       const int nrows = min(kMissRowsPerItem, c - r0);
       int4 ent = make_int4(0, 0, 0, 0);
       if (lane < nrows) ent = p.miss_list[(int64_t)u * p.max_m + r0 + lane];
-      copy_miss_rows<CPR>(ptrs, (p.layer_begin + u / p.R) * p.group, p.group, ent, nrows, row_bytes);
+      copy_miss_rows<CPR>(ptrs, (p.layer_begin + u / p.R) * p.group, p.group, ent, nrows, row_bytes,
+                          p.num_gpu_blocks * p.S, p.num_host_blocks * p.S);
     }
   }
 }
@@ -801,6 +819,20 @@ int ceil_log2(int64_t x) {
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
 }  // namespace
+
+uint32_t check_take_resolve() {
+#if HS_CHECKED
+  unsigned v = 0u, z = 0u;
+  if (cudaMemcpyFromSymbol(&v, hs_check_word_, sizeof(v)) != cudaSuccess ||
+      cudaMemcpyToSymbol(hs_check_word_, &z, sizeof(z)) != cudaSuccess) {
+    cudaGetLastError();
+    return 0xFFFFFFFFu;
+  }
+  return v;
+#else
+  return 0u;
+#endif
+}
 
 ResolveSmem resolve_smem_plan(int64_t n, int64_t C, int64_t S, bool wide) {
   ResolveSmem sm{};

@@ -121,3 +121,15 @@ def test_calls_on_null_handles_are_rejected(lib):
     assert L.hs_resolve_workspace_bytes_min(1, 1, 0, 5, 4) == 0
     assert L.hs_resolve_workspace_bytes_min(1, 1, 1, 16385, 4) == 0   # plan beyond HS_MAX_PLAN
     assert L.hs_launch_count() == 0
+    assert L.hs_check_status() == -1   # the normal build has no bounds checks to report (no CUDA call)
+
+
+def test_checked_build_exports_every_declared_symbol(lib):
+    """The bounds-checked variant (HS_CHECKED=1) builds for sm_103a and exports the same boundary."""
+    from sparse_mla_kv_gb300 import _build
+    path = _build.build(variant="checked")
+    nm = shutil.which("nm")
+    if not nm:
+        pytest.skip("no nm")
+    out = subprocess.run([nm, "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    assert set(declared_functions()) <= set(re.findall(r"\b(hs_[a-z0-9_]+)\b", out))
