@@ -83,6 +83,10 @@ def parse():
     ap.add_argument("--residency", action="store_true",
                     help="time the host-side residency manager (native and its oracle) on a decode loop under "
                          "KV pressure instead of the GPU path; host only")
+    ap.add_argument("--gather-ab", action="store_true",
+                    help="after the timed passes, time the plain gather (hs_gather_rows) of the last step's "
+                         "resolved rows with 16-byte loads and with bulk copies (hs_pool_set_gather_copy), "
+                         "alternating, in this process")
     ap.add_argument("--link-probe", action="store_true",
                     help="measure the miss path's host-link rate against the span of host memory it reads "
                          "(one layer, all-miss steps) instead of a workload")
@@ -697,6 +701,34 @@ def run_ours(args, ws, rank, local):
                  "timing": "each timed step captured as one CUDA graph, replayed once behind an L2 flush; "
                            "events around the replay"}
         del graphs
+    gather_ab = None
+    if args.gather_ab:
+        # the plain gather of the last timed step's rows, every layer of each index group reading its
+        # group's rows, with each copy mode in turn; the pool's misses are filled by then (stream order)
+        rows_l = out_rows.reshape(NG, -1)
+        reps = max(5, K)
+        t_ab = {hs.GATHER_COPY_LOADS: [], hs.GATHER_COPY_BULK: []}
+        for rep in range(reps + 1):
+            for mode in (hs.GATHER_COPY_LOADS, hs.GATHER_COPY_BULK):
+                pool.set_gather_copy(mode)
+                flush.fill_(rep & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for l in range(L):
+                    hs.gather_rows(pool, rows_l[l // G], layer_begin=l, out=gout[l])
+                e1.record(stream)
+                e1.synchronize()
+                if rep:   # the first round is a warm-up
+                    t_ab[mode].append(e0.elapsed_time(e1) * 1e-3)
+        pool.set_gather_copy(hs.GATHER_COPY_LOADS)
+        ab_bytes = L * R * P * Kk * (2 * B + 4)
+        gather_ab = {"rows": L * R * P * Kk, "algorithmic_bytes": ab_bytes, "repeats": reps,
+                     "loads_us_median": 1e6 * statistics.median(t_ab[hs.GATHER_COPY_LOADS]),
+                     "bulk_us_median": 1e6 * statistics.median(t_ab[hs.GATHER_COPY_BULK]),
+                     "loads_gbs": ab_bytes / statistics.median(t_ab[hs.GATHER_COPY_LOADS]) / 1e9,
+                     "bulk_gbs": ab_bytes / statistics.median(t_ab[hs.GATHER_COPY_BULK]) / 1e9,
+                     "how": "hs_gather_rows of the last timed step's rows, one call per layer, the two copy "
+                            "modes alternating behind L2 flushes; medians"}
     h2d_gbs, d2h_gbs = link_peaks()
 
     sum_t = max_over_ranks(dist, float(sum(t_step)), dev)
@@ -873,7 +905,7 @@ def run_ours(args, ws, rank, local):
                            settle_step_us_medians=[round(1e3 * m, 1) for m in settle_medians]),
             "gathered_gbs": value * B / 1e9, "roofline": roofline, "step_roofline": step_roof,
             "cpu_baseline": cpu, "cpu_baseline_1thread": cpu1, "e2e": e2e, "gpu_launches": int(launches),
-            "graph_replay": graph,
+            "graph_replay": graph, "gather_copy_ab": gather_ab,
             "clocks": clocks,
             "wall_s_timed_region": wall, "timed_counts": {"resident": int(hits_misses[0]),
                                                           "hits": int(hits_misses[1]),

@@ -58,7 +58,7 @@ typedef enum {
   HS_ERR_CAPACITY = 4,     /* more misses than evictable hot slots this step                      */
   HS_ERR_STEP_ORDER = 5,   /* step is older than a stamp already in the hot state                 */
   HS_ERR_CUDA = 6,         /* a CUDA runtime call or launch failed                                */
-  HS_ERR_TIMEOUT = 7,      /* reserved: a bounded device wait gave up (no call waits today)       */
+  HS_ERR_TIMEOUT = 7,      /* a bounded device wait gave up (the bulk-copy gather's loads)        */
   HS_ERR_TABLE_RANGE = 8   /* a block-table, host-block-table or hot-block entry that the step
                               dereferences lies outside the pool; offload: a pair out of range    */
 } hs_status;
@@ -164,6 +164,22 @@ size_t hs_resolve_workspace_bytes_min(int32_t nl, int32_t R, int32_t P, int32_t 
 #define HS_MISS_ORDER_OFF 1
 #define HS_MISS_ORDER_ON 2
 hs_status hs_pool_set_miss_order(hs_pool* pool, int32_t mode);
+
+/* How hs_gather_rows moves its HBM rows.  Results are identical in both modes; only the speed
+ * differs.
+ *   HS_GATHER_COPY_LOADS (default)  every lane moves 16-byte chunks with ordinary loads and stores,
+ *                                   eight chunks in flight per thread;
+ *   HS_GATHER_COPY_BULK             one-dimensional bulk copies (cp.async.bulk) of whole rows, global
+ *                                   -> shared -> global, issued by one lane per warp through a ring of
+ *                                   16 row-sized shared-memory stages (12 loads in flight per warp);
+ *                                   falls back to loads when the stages do not fit the device's
+ *                                   shared memory.  Its waits are bounded: a load that never completes
+ *                                   sets HS_ERR_TIMEOUT in the gather's status word.
+ * The pages say only that the rows are gathered with one stride ([JA] "仕組み"); the copy mechanism
+ * is this library's choice.  HS_ERR_INVALID_ARG for an unknown mode. */
+#define HS_GATHER_COPY_LOADS 0
+#define HS_GATHER_COPY_BULK 1
+hs_status hs_pool_set_gather_copy(hs_pool* pool, int32_t mode);
 
 /* 1 if a resolve call on layers [layer_begin, layer_begin + nl) with this shape, hot state and
  * workspace size uses the address-ordered miss layout, 0 if it uses per-unit lists, -1 on bad

@@ -69,6 +69,127 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const LayerPtrs 
   if (bad && status) *status = HS_ERR_ID_RANGE;
 }
 
+// ---- the plain gather with one-dimensional bulk copies (cp.async.bulk), selected per pool by
+// hs_pool_set_gather_copy.  Each warp owns kBulkStages row-sized stages of shared memory and one
+// mbarrier per stage; lane 0 moves the warp's rows i = w, w + warps, ... from HBM into the stages
+// (global -> shared, completing on the stage's mbarrier) kBulkAhead rows ahead, and from each
+// completed stage into its output row (shared -> global, one bulk group per row).  A stage is
+// reloaded only after the bulk store that read it has finished reading (wait_group.read).  Rows -1
+// (and rows outside the pool) are zero-filled by the warp's lanes with ordinary stores.  Every wait
+// is bounded: a load that has not completed after kBulkSpinLimit polls sets HS_ERR_TIMEOUT in the
+// status word (when given), and the warp stops issuing, waits (bounded again) for the copies it
+// has in flight and returns.
+constexpr int kBulkThreads = 256;
+constexpr int kBulkWarps = kBulkThreads / 32;
+constexpr int kBulkStages = 16;
+constexpr int kBulkAhead = 12;  // loads in flight per warp; the stores of the other stages drain meanwhile
+constexpr uint32_t kBulkSpinLimit = 1u << 22;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+// Polls a stage's mbarrier for the phase `parity`; false after kBulkSpinLimit polls.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  for (uint32_t it = 0; it < kBulkSpinLimit; ++it)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+__global__ void __launch_bounds__(kBulkThreads) gather_bulk_kernel(const LayerPtrs ptrs, int32_t layer_begin,
+                                                                   const int32_t* __restrict__ rows, int64_t n,
+                                                                   uint8_t* __restrict__ out, int32_t row_bytes,
+                                                                   int64_t num_rows, int32_t* status) {
+  extern __shared__ __align__(128) unsigned char bulk_smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lr = blockIdx.y;
+  const uint8_t* __restrict__ pool = ptrs.gpu[layer_begin + lr];
+  const int32_t* __restrict__ lrows = rows + (int64_t)lr * n;
+  uint8_t* __restrict__ lout = out + (int64_t)lr * n * row_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(bulk_smem) + warp * kBulkStages;
+  unsigned char* stages =
+      bulk_smem + sizeof(uint64_t) * kBulkStages * kBulkWarps + (size_t)warp * kBulkStages * row_bytes;
+  const int64_t gw = (int64_t)blockIdx.x * kBulkWarps + warp;
+  const int64_t nw = (int64_t)gridDim.x * kBulkWarps;
+  const int64_t cnt = gw < n ? (n - gw + nw - 1) / nw : 0;  // rows of this warp: gw + k * nw, k < cnt
+  if (lane == 0) {
+    for (int st = 0; st < kBulkStages; ++st)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bars + st)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  uint32_t phase = 0u;     // lane 0: parity bit per stage of the next completion to wait for
+  uint32_t loaded = 0u;    // lane 0: stages with a load in flight
+  bool bad = false, timed_out = false;
+  auto row_of = [&](int64_t k) { return __ldg(lrows + gw + k * nw); };
+  auto issue = [&](int64_t k) {  // lane 0: the load of the warp's k-th row into its stage
+    const int row = row_of(k);
+    if (row < 0 || row >= num_rows) return;
+    const int st = (int)(k % kBulkStages);
+    const uint32_t bar = smem_u32(bars + st);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(row_bytes) : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(stages + (size_t)st * row_bytes)),
+                 "l"(pool + (int64_t)row * row_bytes), "r"(row_bytes), "r"(bar)
+                 : "memory");
+    loaded |= 1u << st;
+  };
+  if (lane == 0)
+    for (int64_t k = 0; k < cnt && k < kBulkAhead; ++k) issue(k);
+  for (int64_t k = 0; k < cnt; ++k) {
+    const int row = row_of(k);
+    const int64_t i = gw + k * nw;
+    if (row >= 0 && row < num_rows) {
+      if (lane == 0 && !timed_out) {
+        const int st = (int)(k % kBulkStages);
+        if (mbar_wait_bounded(smem_u32(bars + st), (phase >> st) & 1u)) {
+          phase ^= 1u << st;
+          loaded &= ~(1u << st);
+          asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(lout + i * row_bytes),
+                       "r"(smem_u32(stages + (size_t)st * row_bytes)), "r"(row_bytes)
+                       : "memory");
+        } else {
+          timed_out = true;
+        }
+      }
+    } else {
+      if (row != -1) bad = true;
+      uint4* dst = reinterpret_cast<uint4*>(lout + i * row_bytes);
+      for (int c = lane; c < (row_bytes >> 4); c += 32) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (lane == 0 && !timed_out) {
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");  // one group per row (empty for zero rows)
+      const int64_t kk = k + kBulkAhead;
+      if (kk < cnt) {
+        // the stage of row kk last served row kk - kBulkStages, whose store group was committed
+        // kBulkStages - kBulkAhead groups ago: it must have finished reading the stage
+        asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kBulkStages - kBulkAhead) : "memory");
+        issue(kk);
+      }
+    }
+    if (__shfl_sync(0xffffffffu, (int)timed_out, 0)) break;
+  }
+  timed_out = __shfl_sync(0xffffffffu, (int)timed_out, 0) != 0;
+  if (lane == 0) {
+    if (timed_out) {
+      // bounded drain of the loads still in flight, so that no copy lands in shared memory after exit
+      for (int st = 0; st < kBulkStages; ++st)
+        if (loaded & (1u << st)) mbar_wait_bounded(smem_u32(bars + st), (phase >> st) & 1u);
+      if (status) *status = HS_ERR_TIMEOUT;
+    }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  }
+  if (bad && status && !timed_out) *status = HS_ERR_ID_RANGE;
+}
+
 constexpr int kRepeatRegs = 3;  // repeat positions per entry followed before the stores (P - 1 for MTP3)
 
 // Copies the rows of up to kMissRowsPerItem miss entries (lane j < nrows holds entry j) from the
@@ -256,6 +377,12 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
 
 int g_occ_plain[2] = {0, 0};
 int g_occ_fused[2] = {0, 0};
+int g_occ_bulk = 0;          // resident bulk-gather CTAs per SM for the 656-byte rows' footprint
+size_t g_bulk_smem_max = 0;  // dynamic shared memory the bulk gather may use (the opt-in maximum)
+
+size_t bulk_smem_bytes(int32_t row_bytes) {
+  return sizeof(uint64_t) * kBulkStages * kBulkWarps + (size_t)kBulkStages * kBulkWarps * (size_t)row_bytes;
+}
 
 template <typename Kern>
 int resident_blocks(Kern kern, int* cache) {
@@ -293,11 +420,36 @@ void warm_gather_launch_configs() {
   resident_blocks(gather_kernel<0>, &g_occ_plain[1]);
   resident_blocks(gather_fused_kernel<41>, &g_occ_fused[0]);
   resident_blocks(gather_fused_kernel<0>, &g_occ_fused[1]);
+  if (g_bulk_smem_max == 0) {
+    int dev = 0, optin = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess && optin > 0 &&
+        cudaFuncSetAttribute(gather_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) == cudaSuccess) {
+      g_bulk_smem_max = (size_t)optin;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_occ_bulk, gather_bulk_kernel, kBulkThreads,
+                                                        bulk_smem_bytes(656)) != cudaSuccess || g_occ_bulk < 1)
+        g_occ_bulk = 1;
+    }
+    cudaGetLastError();
+  }
+}
+
+bool gather_bulk_fits(int32_t row_bytes) {
+  return g_bulk_smem_max > 0 && bulk_smem_bytes(row_bytes) <= g_bulk_smem_max;
 }
 
 cudaError_t launch_gather(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, const int32_t* rows, int64_t n,
                           uint8_t* out, int32_t row_bytes, int64_t num_rows, int32_t* status, int sms,
-                          cudaStream_t s) {
+                          cudaStream_t s, bool bulk) {
+  if (bulk && gather_bulk_fits(row_bytes)) {
+    const size_t smem = bulk_smem_bytes(row_bytes);
+    const int occ = row_bytes == 656 ? g_occ_bulk : 1;
+    const int64_t want = (n + kBulkWarps * kBulkStages - 1) / (kBulkWarps * kBulkStages);
+    const dim3 grid = wave_grid(sms, occ, want, nl);
+    gather_bulk_kernel<<<grid, kBulkThreads, smem, s>>>(ptrs, layer_begin, rows, n, out, row_bytes, num_rows, status);
+    count_launch();
+    return cudaGetLastError();
+  }
   int* occ = g_occ_plain;
   const bool k41 = row_bytes == 656;
   auto kern = k41 ? gather_kernel<41> : gather_kernel<0>;

@@ -11,7 +11,8 @@ struct hs_pool {
   hs::PoolGeom g;
   hs::LayerPtrs ptrs;
   int device;
-  int32_t miss_order;  // HS_MISS_ORDER_*
+  int32_t miss_order;   // HS_MISS_ORDER_*
+  int32_t gather_copy;  // HS_GATHER_COPY_*
 };
 
 namespace hs {
@@ -164,6 +165,12 @@ void hs_pool_destroy(hs_pool* p) { delete p; }
 hs_status hs_pool_set_miss_order(hs_pool* pool, int32_t mode) {
   if (!pool || mode < HS_MISS_ORDER_AUTO || mode > HS_MISS_ORDER_ON) return HS_ERR_INVALID_ARG;
   pool->miss_order = mode;
+  return HS_OK;
+}
+
+hs_status hs_pool_set_gather_copy(hs_pool* pool, int32_t mode) {
+  if (!pool || mode < HS_GATHER_COPY_LOADS || mode > HS_GATHER_COPY_BULK) return HS_ERR_INVALID_ARG;
+  pool->gather_copy = mode;
   return HS_OK;
 }
 
@@ -396,7 +403,7 @@ hs_status hs_gather_rows(const hs_pool* pool, int32_t layer_begin, int32_t nl, c
   if (sms <= 0) return HS_ERR_CUDA;
   return hs::cuda_status(hs::launch_gather(pool->ptrs, layer_begin, nl, rows, n, static_cast<uint8_t*>(out),
                                            g.row_bytes, (int64_t)g.num_gpu_blocks * g.page_size, out_status, sms,
-                                           stream));
+                                           stream, pool->gather_copy == HS_GATHER_COPY_BULK));
 }
 
 hs_status hs_offload_pages(const hs_pool* pool, const int32_t* gpu_blocks, const int32_t* host_blocks, int32_t n,

@@ -205,9 +205,12 @@ int resolve_threads(const ResolveSmem& sm, int64_t units, int64_t n, int sms, in
 cudaError_t launch_resolve(const ResolveParams& p, const ResolveSmem& sm, cudaStream_t s);
 cudaError_t launch_miss_copy(const ResolveParams& p, const LayerPtrs& ptrs, int32_t row_bytes, int sms,
                              cudaStream_t s);
+// bulk: move the rows with one-dimensional bulk copies through shared memory (HS_GATHER_COPY_BULK)
+// when the stages fit the device's shared memory, else with 16-byte loads and stores.
 cudaError_t launch_gather(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, const int32_t* rows, int64_t n,
                           uint8_t* out, int32_t row_bytes, int64_t num_rows, int32_t* status, int sms,
-                          cudaStream_t s);
+                          cudaStream_t s, bool bulk = false);
+bool gather_bulk_fits(int32_t row_bytes);
 // The fused gather: rows of layers [layer_begin, layer_begin+nl), R requests x n positions each; miss
 // rows come from the pinned host pool through the resolver's miss lists (dedicated warps) and are
 // also stored into their hot slots; msrc marks positions the miss warps own.  Layer layer_begin + l

@@ -528,6 +528,41 @@ def test_gather_standalone_multilayer_and_status():
     pool.close()
 
 
+@pytest.mark.parametrize("B", [656, 32])
+def test_gather_bulk_copies_equal_the_oracle(B):
+    """hs_pool_set_gather_copy(BULK): whole rows through shared-memory stages with bulk copies.  The
+    same bytes as the oracle's gather for ragged sizes (fewer rows than warps, rows not a multiple of
+    the stages), padding rows, rows outside the pool (zero-filled, ID_RANGE status), several layers
+    and a layer window; repeated calls reuse the stages."""
+    dev = torch.device("cuda")
+    L, S, ngb = 3, 8, 40
+    gpu = [torch.randint(0, 256, (ngb, S, B), dtype=torch.uint8, device=dev) for _ in range(L)]
+    pool = hs.Pool(gpu, None)
+    pool.set_gather_copy(hs.GATHER_COPY_BULK)
+    pools_np = [g.cpu().numpy().reshape(-1) for g in gpu]
+    rng = np.random.default_rng(B)
+    for n in (1, 5, 127, 128, 129, 5003, 300001):
+        rows = rng.integers(-1, ngb * S, size=(L, n)).astype(np.int32)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        for _ in range(2):
+            out = hs.gather_rows(pool, torch.from_numpy(rows).to(dev), status=status)
+            o_out, st = oracle.gather(B=B, num_rows=ngb * S, pools=pools_np, rows=rows)
+            assert st == 0 and int(status.item()) == 0 and np.array_equal(out.cpu().numpy(), o_out), n
+    bad = rng.integers(-1, ngb * S, size=(L, 5003)).astype(np.int32)
+    bad[1, 17] = ngb * S
+    bad[2, 4000] = -9
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = hs.gather_rows(pool, torch.from_numpy(bad).to(dev), status=status)
+    o_out, st = oracle.gather(B=B, num_rows=ngb * S, pools=pools_np, rows=bad)
+    assert int(status.item()) == st == 2 and np.array_equal(out.cpu().numpy(), o_out)
+    out = hs.gather_rows(pool, torch.from_numpy(bad[:2]).to(dev), layer_begin=1)
+    o_out, _ = oracle.gather(B=B, num_rows=ngb * S, pools=pools_np, rows=bad[:2], layer_begin=1)
+    assert np.array_equal(out.cpu().numpy(), o_out)
+    with pytest.raises(hs.HSError):
+        pool.set_gather_copy(7)
+    pool.close()
+
+
 def test_offload_standalone_all_layers_one_launch():
     dev = torch.device("cuda")
     L, S, B, ngb, nhb = 4, 64, 656, 30, 50
