@@ -87,12 +87,21 @@ def parse():
                     help="after the timed passes, time the plain gather (hs_gather_rows) of the last step's "
                          "resolved rows with 16-byte loads and with bulk copies (hs_pool_set_gather_copy), "
                          "alternating, in this process")
+    ap.add_argument("--miss-warps-ab", action="store_true",
+                    help="after the timed passes, replay the last timed step's planned gather (hs_gather_planned) "
+                         "with 1 and 2 miss warps per CTA (hs_pool_set_miss_warps), alternating, in this process")
+    ap.add_argument("--miss-warps", type=int, default=0, choices=[0, 1, 2],
+                    help="miss warps per fused-gather CTA under the range schedule (0: the library's default)")
     ap.add_argument("--link-probe", action="store_true",
                     help="measure the miss path's host-link rate against the span of host memory it reads "
                          "(one layer, all-miss steps) instead of a workload")
     ap.add_argument("--probe-pool-gb", type=float, default=72.0, help="pinned host pool of the link probe")
     ap.add_argument("--probe-windows-gb", type=float, nargs="+", default=[1, 4, 10, 20, 40, 72],
                     help="spans of the host pool the link probe's misses read")
+    ap.add_argument("--probe-base-pages", action="store_true",
+                    help="link probe: register the host pool without huge pages (for comparison)")
+    ap.add_argument("--probe-cpu-fill", action="store_true",
+                    help="link probe: write the host pool with CPU stores instead of DMA (for comparison)")
     ap.add_argument("--miss-order", choices=["auto", "on", "off"], default="auto",
                     help="miss layout handed to the copy warps: auto (the library's default: host-address order "
                          "for host pools of 16 GiB or more), on (always address order), off (per-unit lists)")
@@ -459,6 +468,9 @@ def run_ours(args, ws, rank, local):
         sdev.fill_host_pool(w, l, host[l], dev)
     pool = hs.Pool(gpu, host)
     pool.set_miss_order({"auto": hs.MISS_ORDER_AUTO, "on": hs.MISS_ORDER_ON, "off": hs.MISS_ORDER_OFF}[args.miss_order])
+    pool.set_miss_warps(args.miss_warps)
+    from sparse_mla_kv_gb300.hostmem import huge_page_fraction
+    huge_frac = [round(huge_page_fraction(h), 4) for h in host]
     tb = Tables(w, steps)
     bt = torch.from_numpy(tb.bt).to(dev)
     hbt = torch.from_numpy(tb.hbt).to(dev)
@@ -701,6 +713,29 @@ def run_ours(args, ws, rank, local):
                  "timing": "each timed step captured as one CUDA graph, replayed once behind an L2 flush; "
                            "events around the replay"}
         del graphs
+    miss_warps_ab = None
+    if args.miss_warps_ab and fused:
+        # the last timed step's plan stays in the workspace: replaying hs_gather_planned rewrites the same
+        # bytes (hot slots and outputs), so each replay is the same gather with another miss-warp count
+        reps = max(5, K)
+        t_mw = {1: [], 2: []}
+        for rep in range(reps + 1):
+            for mwc in (1, 2):
+                pool.set_miss_warps(mwc)
+                flush.fill_(rep & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                phase2()
+                e1.record(stream)
+                e1.synchronize()
+                if rep:
+                    t_mw[mwc].append(e0.elapsed_time(e1) * 1e-3)
+        pool.set_miss_warps(args.miss_warps)
+        miss_warps_ab = {"repeats": reps, "miss_order": miss_order,
+                         "gather_us_median_1": 1e6 * statistics.median(t_mw[1]),
+                         "gather_us_median_2": 1e6 * statistics.median(t_mw[2]),
+                         "how": "hs_gather_planned of the last timed step replayed with 1 and 2 miss warps per CTA "
+                                "(hs_pool_set_miss_warps), alternating behind L2 flushes; medians"}
     gather_ab = None
     if args.gather_ab:
         # the plain gather of the last timed step's rows, every layer of each index group reading its
@@ -901,11 +936,12 @@ def run_ours(args, ws, rank, local):
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "u8", "data": "synthetic",
             "config": dict(config_dict(w, args), miss_order=miss_order, timing=headline_timing,
+                           host_pool_huge_page_fraction=huge_frac,
                            settle_passes=len(settle_medians),
                            settle_step_us_medians=[round(1e3 * m, 1) for m in settle_medians]),
             "gathered_gbs": value * B / 1e9, "roofline": roofline, "step_roofline": step_roof,
             "cpu_baseline": cpu, "cpu_baseline_1thread": cpu1, "e2e": e2e, "gpu_launches": int(launches),
-            "graph_replay": graph, "gather_copy_ab": gather_ab,
+            "graph_replay": graph, "gather_copy_ab": gather_ab, "miss_warps_ab": miss_warps_ab,
             "clocks": clocks,
             "wall_s_timed_region": wall, "timed_counts": {"resident": int(hits_misses[0]),
                                                           "hits": int(hits_misses[1]),
@@ -1018,15 +1054,20 @@ def run_link_probe(args):
     pool_bytes = int(args.probe_pool_gb * 1e9) // page * page
     nhb = pool_bytes // page
     windows = sorted({min(nhb, int(g * 1e9) // page) for g in args.probe_windows_gb})
-    host = pinned_host_pool((nhb, S, B))
-    # written by DMA from the device (host memory last written by CPU stores reads slowly through the GPU)
-    dbuf = torch.arange(1 << 30, dtype=torch.int64, device=dev).to(torch.uint8)
+    host = pinned_host_pool((nhb, S, B), huge=not args.probe_base_pages)
+    from sparse_mla_kv_gb300.hostmem import huge_page_fraction
     flat = host.view(-1)
-    for o in range(0, flat.numel(), dbuf.numel()):
-        n_ = min(dbuf.numel(), flat.numel() - o)
-        flat[o:o + n_].copy_(dbuf[:n_], non_blocking=True)
-    torch.cuda.synchronize()
-    del dbuf
+    if args.probe_cpu_fill:
+        # written by CPU stores (a served pool is written by DMA or GPU stores; this is the comparison)
+        flat.numpy()[:] = 7
+    else:
+        # written by DMA from the device
+        dbuf = torch.arange(1 << 30, dtype=torch.int64, device=dev).to(torch.uint8)
+        for o in range(0, flat.numel(), dbuf.numel()):
+            n_ = min(dbuf.numel(), flat.numel() - o)
+            flat[o:o + n_].copy_(dbuf[:n_], non_blocking=True)
+        torch.cuda.synchronize()
+        del dbuf
     ngb = R * (C // S) + R
     gpu = torch.zeros((ngb, S, B), dtype=torch.uint8, device=dev)
     pool = hs.Pool([gpu], [host])
@@ -1109,6 +1150,9 @@ def run_link_probe(args):
     pool.close()
     print(json.dumps({"metric": "miss-path host-link rate vs span of host memory read", "unit": "GB/s",
                       "pool_gb": round(pool_bytes / 1e9, 2), "requests": R, "K": K, "row_bytes": B,
+                      "host_pages": "base pages" if args.probe_base_pages else "huge pages (madvise)",
+                      "huge_page_fraction": round(huge_page_fraction(host), 4),
+                      "host_fill": "CPU stores" if args.probe_cpu_fill else "DMA from the device",
                       "steps": args.steps, "warmup": args.warmup, "table": table,
                       "how": run_link_probe.__doc__.split("\n\n")[1].replace("\n", " ").strip()}), flush=True)
     return 0

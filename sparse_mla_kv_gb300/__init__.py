@@ -25,7 +25,7 @@ LIB_VARIANT = os.environ.get("HS_LIB_VARIANT", "")
 LIB_PATH = os.path.join(_HERE, f"libhs_{LIB_VARIANT}.so" if LIB_VARIANT else "libhs.so")
 
 HS_OK = 0
-MISS_ORDER_AUTO, MISS_ORDER_OFF, MISS_ORDER_ON = 0, 1, 2
+MISS_ORDER_AUTO, MISS_ORDER_OFF, MISS_ORDER_ON, MISS_ORDER_RANGES = 0, 1, 2, 3
 GATHER_COPY_LOADS, GATHER_COPY_BULK = 0, 1
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "ID_RANGE", 3: "MISSING_ROW", 4: "CAPACITY", 5: "STEP_ORDER",
                 6: "CUDA", 7: "TIMEOUT", 8: "TABLE_RANGE"}
@@ -84,6 +84,8 @@ def lib():
         L.hs_pool_set_miss_order.argtypes = [p, i32]
         L.hs_pool_set_gather_copy.restype = i32
         L.hs_pool_set_gather_copy.argtypes = [p, i32]
+        L.hs_pool_set_miss_warps.restype = i32
+        L.hs_pool_set_miss_warps.argtypes = [p, i32]
         L.hs_resolve_miss_order.restype = i32
         L.hs_resolve_miss_order.argtypes = [p, i32, i32, i32, i32, i32, ctypes.POINTER(HotStateC), sz]
         L.hs_resolve_smem_bytes.restype = sz
@@ -185,12 +187,18 @@ class Pool:
         self.handle = h
 
     def set_miss_order(self, mode: int) -> None:
-        """MISS_ORDER_AUTO (default), MISS_ORDER_OFF or MISS_ORDER_ON: see hs_pool_set_miss_order."""
+        """MISS_ORDER_AUTO (default), MISS_ORDER_OFF, MISS_ORDER_ON or MISS_ORDER_RANGES: see
+        hs_pool_set_miss_order."""
         _check(lib().hs_pool_set_miss_order(self.handle, int(mode)), "hs_pool_set_miss_order")
 
     def set_gather_copy(self, mode: int) -> None:
         """GATHER_COPY_LOADS (default) or GATHER_COPY_BULK: see hs_pool_set_gather_copy."""
         _check(lib().hs_pool_set_gather_copy(self.handle, int(mode)), "hs_pool_set_gather_copy")
+
+    def set_miss_warps(self, warps: int) -> None:
+        """Miss warps per fused-gather CTA under the range schedule (0 = default, 1, 2): see
+        hs_pool_set_miss_warps."""
+        _check(lib().hs_pool_set_miss_warps(self.handle, int(warps)), "hs_pool_set_miss_warps")
 
     def close(self) -> None:
         if getattr(self, "handle", None) is not None and self.handle.value:

@@ -18,7 +18,8 @@
 //                      one launch, and HBM warps never wait on host latency.  Under IndexShare
 //                      the G layers of an index group read the same plan (rows, sources, miss
 //                      list); each layer's CTAs copy the misses into that layer's tensor.  With the
-//                      ordered miss layout the miss warps take the misses in host-row-range order.
+//                      ordered miss layout each miss warp takes whole host-row ranges (buckets) and
+//                      reads them in address order.
 #include "hs_internal.cuh"
 
 namespace hs {
@@ -29,7 +30,11 @@ HS_CHECK_WORD
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kGatherThreads = 256;
 constexpr int kGatherUnroll = 8;
-constexpr int kMissWarps = 1;  // per CTA of the fused gather (one is enough to keep the host link busy)
+// Miss warps per CTA of the fused gather: one keeps the host link busy on small pools (two were slower
+// on the mixed batch); with the range schedule of large pools the pool may ask for two
+// (hs_pool_set_miss_warps), so that more host ranges are read at once.
+constexpr int kMaxMissWarps = 2;
+constexpr int kSortChunk = 256;  // ordered layout: bucket entries one miss warp orders and copies at a time
 
 template <int CPR>
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const LayerPtrs ptrs, int32_t layer_begin,
@@ -273,82 +278,293 @@ __device__ __forceinline__ void copy_miss_item(const uint8_t* __restrict__ host,
   }
 }
 
+// ---- staged miss copies (ordered layout).  A warp copies its sorted bucket entries in batches of up
+// to kBatchRows rows: cp.async moves each row's 16-byte chunks from the pinned host pool into a
+// shared-memory stage (no registers hold the data), and while one batch is in flight the previous one
+// is stored from the other stage into its hot slots, its output positions and the positions of its
+// repeats.  Each warp thus keeps up to two batches of host reads in flight.
+constexpr int kBatchRows = 16;
+constexpr int kStageBudget = 24 * 1024;  // dynamic shared memory of a CTA's stages (all its miss warps), at most
+
+__device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Rows per batch for this row size with nmiss miss warps per CTA sharing the budget (0: the stages do
+// not fit, copy through registers instead).
+__host__ __device__ inline int staged_batch_rows(int row_bytes, int nmiss) {
+  const int r = kStageBudget / nmiss / (2 * row_bytes);
+  return r >= kBatchRows ? kBatchRows : (r >= 1 ? r : 0);
+}
+
+// A warp's entry is usable if its host row, pool row and output position lie in their buffers (always
+// true outside the bounds-checked build).
+__device__ __forceinline__ bool entry_ok(int4 e, int64_t per_layer, int64_t gpu_rows, int64_t host_rows) {
+  (void)per_layer;
+  (void)gpu_rows;
+  (void)host_rows;
+  return HS_CHECK(e.x >= 0 && e.x < host_rows, kChkHostRow) && HS_CHECK(e.y >= 0 && e.y < gpu_rows, kChkPoolRow) &&
+         HS_CHECK(e.z >= 0 && e.z < per_layer, kChkOutPos);
+}
+
+// Issues the cp.async copies of ents[0..nr) into stage (one commit group).
+template <int CPR>
+__device__ __forceinline__ void stage_batch(const uint8_t* __restrict__ host, const int4* ents, int nr, int row_bytes,
+                                            uint32_t stage, int64_t per_layer, int64_t gpu_rows, int64_t host_rows) {
+  const int cpr = CPR ? CPR : (row_bytes >> 4);
+  const int lane = threadIdx.x & 31;
+  for (int f = lane; f < nr * cpr; f += 32) {
+    const int rr = f / cpr;
+    const int4 e = ents[rr];
+    if (HS_CHECKED && !entry_ok(e, per_layer, gpu_rows, host_rows)) continue;
+    cp_async16(stage + 16u * (uint32_t)f, host + (int64_t)e.x * row_bytes + (int64_t)(f - rr * cpr) * 16);
+  }
+  cp_async_commit();
+}
+
+// Stores a landed batch: every row into its hot slot and its output position, then along the repeat
+// chains (one link per round for every entry at once).  chain: kBatchRows ints of the warp's shared
+// memory.  Ends with __syncwarp (the stage may be refilled).
+template <int CPR>
+__device__ __forceinline__ void store_batch(uint8_t* __restrict__ pool, uint8_t* __restrict__ lout,
+                                            const int32_t* __restrict__ lmsrc, int n, const int4* ents, int nr,
+                                            int row_bytes, const unsigned char* stage, int* chain, int64_t per_layer,
+                                            int64_t gpu_rows, int64_t host_rows) {
+  const int cpr = CPR ? CPR : (row_bytes >> 4);
+  const int lane = threadIdx.x & 31;
+  if (lane < nr) {
+    const int4 e = ents[lane];
+    int d = entry_ok(e, per_layer, gpu_rows, host_rows) ? e.w : -1;
+    if (d >= 0 && !HS_CHECK(d < n, kChkChain)) d = -1;
+    chain[lane] = d;
+  }
+  __syncwarp();
+  for (int f = lane; f < nr * cpr; f += 32) {
+    const int rr = f / cpr;
+    const int4 e = ents[rr];
+    if (HS_CHECKED && !entry_ok(e, per_layer, gpu_rows, host_rows)) continue;
+    const uint4 v = reinterpret_cast<const uint4*>(stage)[f];
+    const int64_t cc16 = (int64_t)(f - rr * cpr) * 16;
+    *reinterpret_cast<uint4*>(pool + (int64_t)e.y * row_bytes + cc16) = v;
+    *reinterpret_cast<uint4*>(lout + (int64_t)e.z * row_bytes + cc16) = v;
+  }
+  while (__any_sync(kFull, lane < nr && chain[lane] >= 0)) {
+    for (int f = lane; f < nr * cpr; f += 32) {
+      const int rr = f / cpr;
+      const int d = chain[rr];
+      if (d < 0) continue;
+      const int q = ents[rr].z / n;  // the entry's request
+      *reinterpret_cast<uint4*>(lout + ((int64_t)q * n + d) * row_bytes + (int64_t)(f - rr * cpr) * 16) =
+          reinterpret_cast<const uint4*>(stage)[f];
+    }
+    __syncwarp();
+    if (lane < nr) {
+      int d = chain[lane];
+      if (d >= 0) {
+        d = -3 - __ldcg(lmsrc + (int64_t)(ents[lane].z / n) * n + d);
+        if (d >= 0 && !HS_CHECK(d < n, kChkChain)) d = -1;
+        chain[lane] = d;
+      }
+    }
+    __syncwarp();
+  }
+  __syncwarp();
+}
+
+// The miss warps of the fused gather, one per CTA, outside the kernel body (not inlined) so that
+// their registers do not add to the HBM warps' streaming loop.
+// Ordered layout on large host pools (ranges): the layer's miss warps take its group's buckets whole
+// (warp w: buckets w, w + nmw, ...), each chunk ordered by sub-range in shared memory, so that every
+// warp reads its own host range upward; then one slice of the overflow list per warp.
+template <int CPR>
+__device__ __noinline__ void miss_warp_ordered(const MissOrder ord, int pu, int mw, int nmw,
+                                               const uint8_t* __restrict__ host, uint8_t* __restrict__ pool,
+                                               uint8_t* __restrict__ lout, const int32_t* __restrict__ lmsrc, int n,
+                                               int row_bytes, int64_t per_layer, int64_t num_rows,
+                                               int64_t num_host_rows, unsigned char* stages, int batch,
+                                               int4* s_sorted, int* s_sub, int* s_chain) {
+  const int wib = threadIdx.x >> 5;  // the CTA's miss warps are its first warps: each has its own buffers
+  const int32_t* cntg = ord.cnt + (int64_t)pu * (kMissBuckets + 1);  // counts read from L2 where needed
+  const int ovn = min(__ldcg(cntg + kMissBuckets), ord.per_group);
+  const int4* bk = ord.buckets + (int64_t)pu * kMissBuckets * ord.cap;
+  const size_t stage_bytes = (size_t)batch * row_bytes;
+  unsigned char* my_stages = stages + 2 * stage_bytes * wib;
+  const uint32_t st0 = static_cast<uint32_t>(__cvta_generic_to_shared(my_stages));
+  // the buckets whole (index b < kMissBuckets), then one contiguous slice of the overflow list per warp
+  // (index kMissBuckets + slice), in chunks of kSortChunk entries
+  const int ov_per = (ovn + nmw - 1) / nmw;
+  for (int b = mw; b < kMissBuckets + nmw; b += nmw) {
+    const bool ov = b >= kMissBuckets;
+    const int o0 = ov ? (b - kMissBuckets) * ov_per : 0;
+    const int nb = ov ? max(0, min(ov_per, ovn - o0)) : min(__ldcg(cntg + b), ord.cap);
+    const int4* src = ov ? ord.overflow + (int64_t)pu * ord.per_group + o0 : bk + (int64_t)b * ord.cap;
+    for (int c0 = 0; c0 < nb; c0 += kSortChunk) {
+      const int m = min(kSortChunk, nb - c0);
+      sort_by_subrange(src + c0, m, ord.shift, s_sorted, s_sub);
+      // two stages: batch k + 1 lands while batch k is stored
+      const int nbat = (m + batch - 1) / batch;
+      stage_batch<CPR>(host, s_sorted, min(batch, m), row_bytes, st0, per_layer, num_rows, num_host_rows);
+      for (int k = 0; k < nbat; ++k) {
+        if (k + 1 < nbat) {
+          stage_batch<CPR>(host, s_sorted + (k + 1) * batch, min(batch, m - (k + 1) * batch), row_bytes,
+                           st0 + (uint32_t)(((k + 1) & 1) * stage_bytes), per_layer, num_rows, num_host_rows);
+          cp_async_wait<1>();
+        } else {
+          cp_async_wait<0>();
+        }
+        __syncwarp();
+        store_batch<CPR>(pool, lout, lmsrc, n, s_sorted + k * batch, min(batch, m - k * batch), row_bytes,
+                         my_stages + (k & 1) * stage_bytes, s_chain, per_layer, num_rows, num_host_rows);
+      }
+      __syncwarp();
+    }
+  }
+}
+
+// The same without stages, for rows too large to stage (each item's rows held in registers).
+template <int CPR>
+__device__ __noinline__ void miss_warp_ordered_regs(const MissOrder ord, int pu, int mw, int nmw,
+                                                    const uint8_t* __restrict__ host, uint8_t* __restrict__ pool,
+                                                    uint8_t* __restrict__ lout, const int32_t* __restrict__ lmsrc,
+                                                    int n, int row_bytes, int64_t per_layer, int64_t num_rows,
+                                                    int64_t num_host_rows, int4* s_sorted, int* s_sub) {
+  const int lane = threadIdx.x & 31;
+  const int32_t* cntg = ord.cnt + (int64_t)pu * (kMissBuckets + 1);
+  const int ovn = min(__ldcg(cntg + kMissBuckets), ord.per_group);
+  const int4* bk = ord.buckets + (int64_t)pu * kMissBuckets * ord.cap;
+  const int ov_per = (ovn + nmw - 1) / nmw;
+  for (int b = mw; b < kMissBuckets + nmw; b += nmw) {
+    const bool ov = b >= kMissBuckets;
+    const int o0 = ov ? (b - kMissBuckets) * ov_per : 0;
+    const int nb = ov ? max(0, min(ov_per, ovn - o0)) : min(__ldcg(cntg + b), ord.cap);
+    const int4* src = ov ? ord.overflow + (int64_t)pu * ord.per_group + o0 : bk + (int64_t)b * ord.cap;
+    for (int c0 = 0; c0 < nb; c0 += kSortChunk) {
+      const int m = min(kSortChunk, nb - c0);
+      sort_by_subrange(src + c0, m, ord.shift, s_sorted, s_sub);
+      for (int i = 0; i < m; i += kMissRowsPerItem) {
+        const int nrows = min(kMissRowsPerItem, m - i);
+        const int4 ent = lane < nrows ? s_sorted[i + lane] : make_int4(0, 0, 0, 0);
+        copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
+      }
+      __syncwarp();
+    }
+  }
+}
+
+// Spread schedule (ordered layout on smaller host pools): the layer's miss warps take its group's
+// 4-entry items in bucket order (warp w: items w, w + nmw, ...), so that all copy warps work on
+// neighbouring host ranges at once and every warp has an item in flight.
+template <int CPR>
+__device__ __noinline__ void miss_warp_spread(const MissOrder ord, int pu, int mw, int nmw,
+                                              const uint8_t* __restrict__ host, uint8_t* __restrict__ pool,
+                                              uint8_t* __restrict__ lout, const int32_t* __restrict__ lmsrc, int n,
+                                              int row_bytes, int64_t per_layer, int64_t num_rows,
+                                              int64_t num_host_rows, MissItems& mi) {
+  const int lane = threadIdx.x & 31;
+  mi.load(ord, pu);
+  const int4* bk = ord.buckets + (int64_t)pu * kMissBuckets * ord.cap;
+  const int4* ovl = ord.overflow + (int64_t)pu * ord.per_group;
+  for (int32_t i = mw; i < mi.items; i += nmw) {
+    int64_t start;
+    bool in_ov;
+    int nrows;
+    mi.locate(ord, i, start, in_ov, nrows);
+    int4 ent = make_int4(0, 0, 0, 0);
+    if (lane < nrows) ent = (in_ov ? ovl : bk)[start + lane];
+    copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
+  }
+}
+
+// Per-unit lists: items (request, chunk of kMissRowsPerItem misses) of this layer, numbered chunk-major
+// so live items are the low numbers; lane j of miss-warp w tests item w + j * nmw.
+template <int CPR>
+__device__ __noinline__ void miss_warp_lists(const int32_t* __restrict__ miss_count, const int4* __restrict__ miss_list,
+                                             int pu, int R, int max_m, int64_t mw, int64_t nmw,
+                                             const uint8_t* __restrict__ host, uint8_t* __restrict__ pool,
+                                             uint8_t* __restrict__ lout, const int32_t* __restrict__ lmsrc, int n,
+                                             int row_bytes, int64_t per_layer, int64_t num_rows,
+                                             int64_t num_host_rows) {
+  const int lane = threadIdx.x & 31;
+  const int items_per_unit = (max_m + kMissRowsPerItem - 1) / kMissRowsPerItem;
+  const int64_t items = (int64_t)R * items_per_unit;
+  for (int64_t base = mw; base < items; base += nmw * 32) {
+    const int64_t item = base + (int64_t)lane * nmw;
+    int r = 0, chunk = 0, cnt = 0;
+    bool live = false;
+    if (item < items) {
+      chunk = (int)(item / R);
+      r = (int)(item - (int64_t)chunk * R);
+      cnt = miss_count[pu * R + r];
+      live = chunk * kMissRowsPerItem < cnt;
+    }
+    uint32_t todo = __ballot_sync(kFull, live);
+    while (todo) {
+      const int src_lane = __ffs(todo) - 1;
+      todo &= todo - 1u;
+      const int rq = __shfl_sync(kFull, r, src_lane);
+      const int ch = __shfl_sync(kFull, chunk, src_lane);
+      const int c = __shfl_sync(kFull, cnt, src_lane);
+      const int r0 = ch * kMissRowsPerItem;
+      const int nrows = min(kMissRowsPerItem, c - r0);
+      int4 ent = make_int4(0, 0, 0, 0);
+      if (lane < nrows) ent = miss_list[((int64_t)pu * R + rq) * max_m + r0 + lane];
+      copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
+    }
+  }
+}
+
 template <int CPR>
 __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
     const LayerPtrs ptrs, int32_t layer_begin, int32_t group, int32_t R, int32_t n, int32_t max_m,
     const int32_t* __restrict__ rows, const int32_t* __restrict__ miss_count, const int4* __restrict__ miss_list,
     const MissOrder ord, const int32_t* __restrict__ msrc, uint8_t* __restrict__ out, int32_t row_bytes,
-    int64_t num_rows, int64_t num_host_rows) {
+    int64_t num_rows, int64_t num_host_rows, int32_t batch, int32_t nmiss) {
+  extern __shared__ __align__(16) unsigned char fused_stages[];  // ordered layout: the miss warps' stages
   pdl_wait_prerequisites();   // the resolve plan (rows, sources, miss lists) must be complete and visible
   const int cpr = CPR ? CPR : (row_bytes >> 4);
   const int lr = blockIdx.y;
   const int pu = lr / group;  // the index group (plan) this layer reads
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   uint8_t* __restrict__ pool = ptrs.gpu[layer_begin + lr];
   const uint8_t* __restrict__ host = ptrs.host[layer_begin + lr];
   const int64_t per_layer = (int64_t)R * n;
   uint8_t* __restrict__ lout = out + (int64_t)lr * per_layer * row_bytes;
   const int32_t* __restrict__ lmsrc = msrc + (int64_t)pu * per_layer;
 
-  if (warp < kMissWarps) {
-    const int64_t mw = (int64_t)blockIdx.x * kMissWarps + warp;
-    const int64_t nmw = (int64_t)gridDim.x * kMissWarps;
-    if (ord.cnt) {
-      // ---- ordered layout: the layer's miss warps take its group's items in bucket order (warp w:
-      // items w, w + nmw, ...), so the host rows in flight lie in neighbouring ranges
-      __shared__ MissItems mi;
-      mi.load(ord, pu);
-      const int4* bk = ord.buckets + (int64_t)pu * kMissBuckets * ord.cap;
-      const int4* ovl = ord.overflow + (int64_t)pu * ord.per_group;
-      for (int32_t i = (int32_t)mw; i < mi.items; i += (int32_t)nmw) {
-        int64_t start;
-        bool in_ov;
-        int nrows;
-        mi.locate(ord, i, start, in_ov, nrows);
-        int4 ent = make_int4(0, 0, 0, 0);
-        if (lane < nrows) ent = (in_ov ? ovl : bk)[start + lane];
-        copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
-      }
-      return;
-    }
-    // ---- miss warps: items (request, chunk of kMissRowsPerItem misses) of this layer, numbered
-    // chunk-major so live items are the low numbers; lane j of miss-warp w tests item w + j * nmw.
-    const int items_per_unit = (max_m + kMissRowsPerItem - 1) / kMissRowsPerItem;
-    const int64_t items = (int64_t)R * items_per_unit;
-    for (int64_t base = mw; base < items; base += nmw * 32) {
-      const int64_t item = base + (int64_t)lane * nmw;
-      int r = 0, chunk = 0, cnt = 0;
-      bool live = false;
-      if (item < items) {
-        chunk = (int)(item / R);
-        r = (int)(item - (int64_t)chunk * R);
-        cnt = miss_count[pu * R + r];
-        live = chunk * kMissRowsPerItem < cnt;
-      }
-      uint32_t todo = __ballot_sync(kFull, live);
-      while (todo) {
-        const int src_lane = __ffs(todo) - 1;
-        todo &= todo - 1u;
-        const int rq = __shfl_sync(kFull, r, src_lane);
-        const int ch = __shfl_sync(kFull, chunk, src_lane);
-        const int c = __shfl_sync(kFull, cnt, src_lane);
-        const int r0 = ch * kMissRowsPerItem;
-        const int nrows = min(kMissRowsPerItem, c - r0);
-        int4 ent = make_int4(0, 0, 0, 0);
-        if (lane < nrows) ent = miss_list[((int64_t)pu * R + rq) * max_m + r0 + lane];
-        copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
-      }
-    }
+  if (warp < nmiss) {
+    // CTA-major numbering: consecutive buckets (or items) go to different CTAs, spread over the SMs
+    const int64_t mw = (int64_t)warp * gridDim.x + blockIdx.x;
+    const int64_t nmw = (int64_t)gridDim.x * nmiss;
+    // the ordered layout's per-miss-warp buffers: bucket counts, a sorted chunk, sub-range counters, chains
+    __shared__ MissItems s_mi;  // spread schedule (one miss warp)
+    __shared__ int4 s_sorted[kMaxMissWarps][kSortChunk];
+    __shared__ int s_sub[kMaxMissWarps][kSubRanges];
+    __shared__ int s_chain[kMaxMissWarps][kBatchRows];
+    if (ord.cnt && !ord.ranges)
+      miss_warp_spread<CPR>(ord, pu, (int)mw, (int)nmw, host, pool, lout, lmsrc, n, row_bytes, per_layer, num_rows,
+                            num_host_rows, s_mi);
+    else if (ord.cnt && batch)
+      miss_warp_ordered<CPR>(ord, pu, (int)mw, (int)nmw, host, pool, lout, lmsrc, n, row_bytes, per_layer, num_rows,
+                             num_host_rows, fused_stages, batch, s_sorted[warp], s_sub[warp], s_chain[warp]);
+    else if (ord.cnt)
+      miss_warp_ordered_regs<CPR>(ord, pu, (int)mw, (int)nmw, host, pool, lout, lmsrc, n, row_bytes, per_layer,
+                                  num_rows, num_host_rows, s_sorted[warp], s_sub[warp]);
+    else
+      miss_warp_lists<CPR>(miss_count, miss_list, pu, R, max_m, mw, nmw, host, pool, lout, lmsrc, n, row_bytes,
+                           per_layer, num_rows, num_host_rows);
     return;
   }
 
   // ---- HBM warps: every position the miss warps do not own (resident rows, hit rows, padding);
   // one source word per position
-  constexpr int kHbmThreads = kGatherThreads - kMissWarps * 32;
+  const int hbm_threads = kGatherThreads - nmiss * 32;
   uint4* __restrict__ lout4 = reinterpret_cast<uint4*>(lout);
   const int64_t total = per_layer * cpr;
-  const int64_t stride = (int64_t)gridDim.x * kHbmThreads;
-  for (int64_t c0 = (int64_t)blockIdx.x * kHbmThreads + (threadIdx.x - kMissWarps * 32); c0 < total;
+  const int64_t stride = (int64_t)gridDim.x * hbm_threads;
+  for (int64_t c0 = (int64_t)blockIdx.x * hbm_threads + (threadIdx.x - nmiss * 32); c0 < total;
        c0 += stride * kGatherUnroll) {
     uint4 v[kGatherUnroll];
     bool st[kGatherUnroll];
@@ -385,8 +601,8 @@ size_t bulk_smem_bytes(int32_t row_bytes) {
 }
 
 template <typename Kern>
-int resident_blocks(Kern kern, int* cache) {
-  if (*cache <= 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(cache, kern, kGatherThreads, 0) != cudaSuccess)
+int resident_blocks(Kern kern, int* cache, size_t smem = 0) {
+  if (*cache <= 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(cache, kern, kGatherThreads, smem) != cudaSuccess)
     *cache = 2;
   if (*cache <= 0) *cache = 1;
   return *cache;
@@ -418,8 +634,9 @@ uint32_t check_take_gather() {
 void warm_gather_launch_configs() {
   resident_blocks(gather_kernel<41>, &g_occ_plain[0]);
   resident_blocks(gather_kernel<0>, &g_occ_plain[1]);
-  resident_blocks(gather_fused_kernel<41>, &g_occ_fused[0]);
-  resident_blocks(gather_fused_kernel<0>, &g_occ_fused[1]);
+  // the fused gather's CTAs may carry up to kStageBudget bytes of stages (ordered layout, range schedule)
+  resident_blocks(gather_fused_kernel<41>, &g_occ_fused[0], kStageBudget);
+  resident_blocks(gather_fused_kernel<0>, &g_occ_fused[1], kStageBudget);
   if (g_bulk_smem_max == 0) {
     int dev = 0, optin = 0;
     if (cudaGetDevice(&dev) == cudaSuccess &&
@@ -464,30 +681,34 @@ cudaError_t launch_gather(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl
 cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, int32_t group, int32_t R,
                                 int32_t n, int32_t max_m, const int32_t* rows, const int32_t* miss_count,
                                 const int4* miss_list, const MissOrder& ord, const int32_t* msrc, uint8_t* out,
-                                int32_t row_bytes, int64_t num_rows, int64_t num_host_rows, int sms, cudaStream_t s) {
+                                int32_t row_bytes, int64_t num_rows, int64_t num_host_rows, int range_miss_warps,
+                                int sms, cudaStream_t s) {
   int* occ = g_occ_fused;
   const bool k41 = row_bytes == 656;
   auto kern = k41 ? gather_fused_kernel<41> : gather_fused_kernel<0>;
+  // miss warps per CTA: the pool's choice for the range schedule, one otherwise
+  const int nmiss = (ord.cnt && ord.ranges) ? (range_miss_warps >= 2 ? 2 : 1) : 1;
   const int64_t per_layer = (int64_t)R * n * (row_bytes >> 4);
   const int64_t want_hbm = (per_layer + (int64_t)kGatherThreads * kGatherUnroll - 1) /
                            ((int64_t)kGatherThreads * kGatherUnroll);
-  // one miss warp per CTA: enough CTAs that each can take one item (kMissRowsPerItem misses) of the most
-  // a layer can have, so a small batch does not queue its host round trips on a few warps
-  const int64_t want_miss = ((int64_t)R * ((max_m + kMissRowsPerItem - 1) / kMissRowsPerItem) + kMissWarps - 1) /
-                            kMissWarps;
-  const dim3 grid = wave_grid(sms, resident_blocks(kern, &occ[k41 ? 0 : 1]), want_hbm > want_miss ? want_hbm : want_miss,
-                              nl);
+  // enough CTAs that each miss warp can take one item (kMissRowsPerItem misses) of the most a layer can
+  // have, so a small batch does not queue its host round trips on a few warps
+  const int64_t want_miss = ((int64_t)R * ((max_m + kMissRowsPerItem - 1) / kMissRowsPerItem) + nmiss - 1) / nmiss;
+  const dim3 grid = wave_grid(sms, resident_blocks(kern, &occ[k41 ? 0 : 1], kStageBudget),
+                              want_hbm > want_miss ? want_hbm : want_miss, nl);
   // With the ordered layout (large host pools) the gather is not launched early: CTAs placed while
   // the resolver still runs made the whole gather's host reads slower there (measured: agentic
   // decode over a 29 GB pool, 684 us per step against 333 us with the launch held back).
   cudaError_t e;
   if (ord.cnt) {
-    kern<<<grid, kGatherThreads, 0, s>>>(ptrs, layer_begin, group, R, n, max_m, rows, miss_count, miss_list, ord, msrc,
-                                         out, row_bytes, num_rows, num_host_rows);
+    const int batch = ord.ranges ? staged_batch_rows(row_bytes, nmiss) : 0;
+    const size_t smem = (size_t)nmiss * 2 * batch * row_bytes;
+    kern<<<grid, kGatherThreads, smem, s>>>(ptrs, layer_begin, group, R, n, max_m, rows, miss_count, miss_list, ord,
+                                            msrc, out, row_bytes, num_rows, num_host_rows, batch, nmiss);
     e = cudaGetLastError();
   } else {
     e = launch_dependent(kern, grid, dim3(kGatherThreads), 0, s, ptrs, layer_begin, group, R, n, max_m, rows,
-                         miss_count, miss_list, ord, msrc, out, row_bytes, num_rows, num_host_rows);
+                         miss_count, miss_list, ord, msrc, out, row_bytes, num_rows, num_host_rows, 0, 1);
   }
   if (e != cudaSuccess) return e;
   count_launch();

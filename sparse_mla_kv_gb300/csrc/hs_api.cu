@@ -13,6 +13,7 @@ struct hs_pool {
   int device;
   int32_t miss_order;   // HS_MISS_ORDER_*
   int32_t gather_copy;  // HS_GATHER_COPY_*
+  int32_t miss_warps;   // fused gather, range schedule: miss warps per CTA (0 = the library's default)
 };
 
 namespace hs {
@@ -51,14 +52,18 @@ bool use_miss_order(const hs_pool* pool, int32_t nl, int64_t ng, int32_t R, int6
   if (2 * (int64_t)R * max_m > INT32_MAX) return false;
   if (workspace_bytes < resolve_workspace_bytes_ordered(ng, R, n, C)) return false;
   const int64_t host_bytes = (int64_t)g.num_host_blocks * g.page_size * g.row_bytes * nl;
-  return pool->miss_order == HS_MISS_ORDER_ON || host_bytes >= kMissOrderAutoBytes;
+  return pool->miss_order >= HS_MISS_ORDER_ON || host_bytes >= kMissOrderAutoBytes;
 }
 
 // The ordered layout's pointers within `workspace`, or cnt = nullptr for per-unit lists.
 MissOrder call_miss_order(const hs_pool* pool, int32_t nl, int64_t ng, int32_t R, int64_t n, int32_t C,
                           void* workspace, size_t workspace_bytes) {
   if (!use_miss_order(pool, nl, ng, R, n, C, workspace_bytes)) return MissOrder{};
-  return miss_order_layout(workspace, ng, R, n, C, (int64_t)pool->g.num_host_blocks * pool->g.page_size);
+  MissOrder o = miss_order_layout(workspace, ng, R, n, C, (int64_t)pool->g.num_host_blocks * pool->g.page_size);
+  const PoolGeom& g = pool->g;
+  o.ranges = (pool->miss_order == HS_MISS_ORDER_RANGES ||
+              (int64_t)g.num_host_blocks * g.page_size * g.row_bytes * nl >= kMissRangesBytes) ? 1 : 0;
+  return o;
 }
 
 }  // namespace
@@ -163,7 +168,7 @@ hs_status hs_pool_create(const hs_pool_desc* d, hs_pool** out) {
 void hs_pool_destroy(hs_pool* p) { delete p; }
 
 hs_status hs_pool_set_miss_order(hs_pool* pool, int32_t mode) {
-  if (!pool || mode < HS_MISS_ORDER_AUTO || mode > HS_MISS_ORDER_ON) return HS_ERR_INVALID_ARG;
+  if (!pool || mode < HS_MISS_ORDER_AUTO || mode > HS_MISS_ORDER_RANGES) return HS_ERR_INVALID_ARG;
   pool->miss_order = mode;
   return HS_OK;
 }
@@ -171,6 +176,12 @@ hs_status hs_pool_set_miss_order(hs_pool* pool, int32_t mode) {
 hs_status hs_pool_set_gather_copy(hs_pool* pool, int32_t mode) {
   if (!pool || mode < HS_GATHER_COPY_LOADS || mode > HS_GATHER_COPY_BULK) return HS_ERR_INVALID_ARG;
   pool->gather_copy = mode;
+  return HS_OK;
+}
+
+hs_status hs_pool_set_miss_warps(hs_pool* pool, int32_t warps) {
+  if (!pool || warps < 0 || warps > 2) return HS_ERR_INVALID_ARG;
+  pool->miss_warps = warps;
   return HS_OK;
 }
 
@@ -374,7 +385,8 @@ hs_status hs_gather_planned(const hs_pool* pool, int32_t layer_begin, int32_t nl
       pool->ptrs, layer_begin, nl, G, R, (int32_t)n, max_m, out_rows, reinterpret_cast<const int32_t*>(ws),
       reinterpret_cast<const int4*>(ws + hs::ws_counts_bytes(units)), ord,
       reinterpret_cast<const int32_t*>(ws + hs::ws_msrc_offset(units, n, capacity)), static_cast<uint8_t*>(out),
-      g.row_bytes, (int64_t)g.num_gpu_blocks * g.page_size, (int64_t)g.num_host_blocks * g.page_size, sms, stream));
+      g.row_bytes, (int64_t)g.num_gpu_blocks * g.page_size, (int64_t)g.num_host_blocks * g.page_size,
+      pool->miss_warps ? pool->miss_warps : hs::kDefaultRangeMissWarps, sms, stream));
 }
 
 hs_status hs_resolve_gather(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P, int32_t K,

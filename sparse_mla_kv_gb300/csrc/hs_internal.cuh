@@ -97,10 +97,10 @@ constexpr int kMissRowsPerItem = 4;
 // by the device's address translation for host memory, not by the link: a step whose in-flight
 // reads span the whole pool misses the translation caches on nearly every row.  In this layout the
 // resolver files each miss of an index group into one of kMissBuckets buckets by host row range
-// (bucket = host row >> shift), and the copy warps take consecutive items in bucket order, so the
-// rows in flight at any moment lie in a few neighbouring ranges.  Results do not depend on it: every
-// miss writes its own hot slot and output row.
-constexpr int kMissBuckets = 256;
+// (bucket = host row >> shift), and each copy warp takes whole buckets and reads them in address
+// order (see sort_by_subrange below).  Results do not depend on it: every miss writes its own hot
+// slot and output row.
+constexpr int kMissBuckets = 1024;  // enough host ranges that every copy warp of a large step owns some
 constexpr int kBucketsPerLane = kMissBuckets / 32;
 struct MissOrder {
   int32_t* cnt;       // [groups][kMissBuckets + 1]: entries filed per bucket, then the overflow count;
@@ -110,7 +110,18 @@ struct MissOrder {
   int32_t shift;      // bucket of host row h: h >> shift
   int32_t cap;        // entries per bucket
   int32_t per_group;  // misses an index group can have: R * max_m
+  int32_t ranges;     // 1: each copy warp takes whole buckets (ranges); 0: 4-entry items in bucket order,
+                      // spread over all copy warps
 };
+// Host pools at least this large (over the layers of a call) are copied bucket by bucket, each bucket by
+// one warp; smaller ones with the items of all buckets spread over every copy warp.  Measured with the
+// library's miss path (131K misses per step, one layer): over spans up to 20 GB the spread items keep
+// more rows in flight (185 against 145 GB/s at 4 GB); from 40 GB on, where the device's translation of
+// host addresses binds, whole buckets per warp are faster (118 against 50 GB/s at 40 GB, 54 against 39
+// at 72 GB).
+constexpr int64_t kMissRangesBytes = int64_t(40) << 30;
+// Miss warps per CTA of the fused gather with the range schedule, unless the pool sets another count.
+constexpr int kDefaultRangeMissWarps = 1;
 // Bucket capacity: twice the even share, so that only strongly skewed steps overflow.
 inline int32_t miss_bucket_cap(int64_t per_group) {
   return (int32_t)((2 * per_group + kMissBuckets - 1) / kMissBuckets);
@@ -218,7 +229,8 @@ bool gather_bulk_fits(int32_t row_bytes);
 cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, int32_t group, int32_t R,
                                 int32_t n, int32_t max_m, const int32_t* rows, const int32_t* miss_count,
                                 const int4* miss_list, const MissOrder& ord, const int32_t* msrc, uint8_t* out,
-                                int32_t row_bytes, int64_t num_rows, int64_t num_host_rows, int sms, cudaStream_t s);
+                                int32_t row_bytes, int64_t num_rows, int64_t num_host_rows, int range_miss_warps,
+                                int sms, cudaStream_t s);
 cudaError_t launch_offload(const LayerPtrs& ptrs, const PoolGeom& g, const int32_t* gpu_blocks,
                            const int32_t* host_blocks, int32_t n, int32_t* status, int sms, cudaStream_t s);
 cudaError_t launch_fill_i32(int32_t* a, int64_t count, int32_t value, int sms, cudaStream_t s);
@@ -229,25 +241,27 @@ void count_launch(int k = 1);
 // The device a pool was created on (its device pointers belong to it).
 int pool_device(const hs_pool* pool);
 
-// The item index of an index group's ordered misses, kept in shared memory (one per CTA): item i
-// (up to kMissRowsPerItem consecutive entries of one bucket, or of the overflow list) -> its first
-// entry and its row count.  load() is called by one whole warp; the others read after a barrier.
+// The index of an index group's ordered misses, kept in shared memory (one per copy warp or CTA):
+// entries filed in each bucket (at most cap) and in the overflow list, and the item numbering of the
+// spread schedule -- item i (up to kMissRowsPerItem consecutive entries of one bucket, or of the
+// overflow list) -> its first entry and its row count.  load() is called by one whole warp; other
+// warps read after a barrier.
 struct MissItems {
   int32_t cnt[kMissBuckets];       // entries in each bucket (at most cap)
   int32_t pref[kMissBuckets + 1];  // items before each bucket; pref[kMissBuckets]: all bucket items
-  int32_t overflow;                // overflow entries
+  int32_t overflow;                // overflow entries (at most per_group)
   int32_t items;                   // bucket items plus overflow items
 
   __device__ __forceinline__ void load(const MissOrder& o, int g) {
     const int lane = threadIdx.x & 31;
     const int32_t* c = o.cnt + (int64_t)g * (kMissBuckets + 1);
-    int32_t v[kBucketsPerLane];
     int32_t sum = 0;
-#pragma unroll
+#pragma unroll 4
     for (int k = 0; k < kBucketsPerLane; ++k) {
       const int32_t x = __ldcg(c + lane * kBucketsPerLane + k);
-      v[k] = x < o.cap ? x : o.cap;
-      sum += (v[k] + kMissRowsPerItem - 1) / kMissRowsPerItem;
+      const int32_t v = x < o.cap ? x : o.cap;
+      cnt[lane * kBucketsPerLane + k] = v;
+      sum += (v + kMissRowsPerItem - 1) / kMissRowsPerItem;
     }
     int32_t incl = sum;
 #pragma unroll
@@ -256,11 +270,9 @@ struct MissItems {
       if (lane >= d) incl += x;
     }
     int32_t base = incl - sum;
-#pragma unroll
     for (int k = 0; k < kBucketsPerLane; ++k) {
-      cnt[lane * kBucketsPerLane + k] = v[k];
       pref[lane * kBucketsPerLane + k] = base;
-      base += (v[k] + kMissRowsPerItem - 1) / kMissRowsPerItem;
+      base += (cnt[lane * kBucketsPerLane + k] + kMissRowsPerItem - 1) / kMissRowsPerItem;
     }
     if (lane == 31) {
       pref[kMissBuckets] = incl;
@@ -270,8 +282,8 @@ struct MissItems {
     }
     __syncwarp();
   }
-  // Item i < items: its first entry (relative to the group's buckets, or to its overflow list when
-  // in_overflow) and its row count.
+  // Spread schedule, item i < items: its first entry (relative to the group's buckets, or to its
+  // overflow list when in_overflow) and its row count.
   __device__ __forceinline__ void locate(const MissOrder& o, int32_t i, int64_t& start, bool& in_overflow,
                                          int& nrows) const {
     const int32_t nb = pref[kMissBuckets];
@@ -296,6 +308,43 @@ struct MissItems {
     nrows = count < kMissRowsPerItem ? count : kMissRowsPerItem;
   }
 };
+
+// Bucket-major copying of the ordered layout.  A copy warp takes whole buckets (a bucket is a range of
+// 2^shift host rows), in chunks of at most `cap` entries, and orders each chunk in shared memory by
+// the 64 sub-ranges of its bucket (a counting sort; order inside a sub-range is arbitrary) before
+// copying it.  Each warp then reads its own address range upward, so the host rows any warp has in
+// flight lie in one or two of the device's translation pages; warps interleaved over the same
+// buckets, or rows in random order within a bucket, made the reads over a 72 GB pool 1.3-4x slower.
+constexpr int kSubRanges = 64;
+// Warp-level: dst[0..m) = src[0..m) ordered by sub-range of the host row (field x).  cnt: 64 ints of
+// shared memory owned by the warp.  Contains __syncwarp.
+__device__ __forceinline__ void sort_by_subrange(const int4* __restrict__ src, int m, int shift, int4* dst, int* cnt) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t low = shift > 0 ? (1u << shift) - 1u : 0u;
+  const int sub_shift = shift > 6 ? shift - 6 : 0;
+  cnt[lane] = 0;
+  cnt[lane + 32] = 0;
+  __syncwarp();
+  for (int e = lane; e < m; e += 32) atomicAdd(&cnt[(((uint32_t)__ldcg(&src[e].x) & low) >> sub_shift) & 63], 1);
+  __syncwarp();
+  const int a = cnt[2 * lane], b = cnt[2 * lane + 1];
+  int incl = a + b;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += x;
+  }
+  const int excl = incl - a - b;
+  __syncwarp();
+  cnt[2 * lane] = excl;
+  cnt[2 * lane + 1] = excl + a;
+  __syncwarp();
+  for (int e = lane; e < m; e += 32) {
+    const int4 v = __ldcg(src + e);
+    dst[atomicAdd(&cnt[(((uint32_t)v.x & low) >> sub_shift) & 63], 1)] = v;
+  }
+  __syncwarp();
+}
 
 // Programmatic dependent launch.  A kernel that follows another of this library's kernels on the
 // same stream is launched with programmatic stream serialization: its CTAs may be placed as soon as

@@ -29,8 +29,8 @@
 //                    the rows as 16-byte zero-copy loads from the mapped pinned host pool, once for
 //                    each layer of the unit's index group.  Spreading keeps enough loads in flight on
 //                    the host link even when few units miss a lot.  With the ordered layout each
-//                    index group gets its own CTAs, whose warps take the group's 4-entry items in
-//                    bucket (host row range) order.
+//                    index group gets its own CTAs, whose warps take the group's buckets (host row
+//                    ranges) whole, each read in address order.
 //   order_clear_kernel zeroes the ordered layout's bucket counters before the resolver, which is its
 //                    programmatic dependent and waits for it only where it first needs them.
 //
@@ -695,6 +695,7 @@ __global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const
 }
 
 constexpr int kCopyThreads = 256;
+constexpr int kCopySortChunk = 128;  // ordered layout: bucket entries one copy warp orders and copies at a time
 
 // Copies the rows of up to kMissRowsPerItem entries (lane j < nrows holds entry j) from the host pool
 // into their hot slots, in every layer [l0, l0 + group), all of a layer's 16-byte loads before its
@@ -741,20 +742,21 @@ __device__ __forceinline__ void copy_miss_rows(const LayerPtrs& ptrs, int l0, in
 // Copies the misses of every unit.  Per-unit lists: items (unit, group of kMissRowsPerItem
 // consecutive misses) are numbered chunk-major (item = group * units + unit), so the live items are
 // the low numbers; lane j of warp w tests item w + j * nwarps, which spreads the live items over all
-// warps of the grid.  Ordered layout: blockIdx.y is the index group, and the warps of its CTAs take
-// its items in bucket order (warp w: items w, w + nwarps, ...), so the rows in flight lie in
-// neighbouring host ranges.  A live item's rows are copied with all its 16-byte loads issued before
-// any store.
+// warps of the grid.  Ordered layout: blockIdx.y is the index group, and each warp of its CTAs takes
+// whole buckets and reads them in address order, so every warp walks its own host range upward.  A
+// live item's rows are copied with all its 16-byte loads issued before any store.
 template <int CPR>
 __global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(const ResolveParams p, const LayerPtrs ptrs,
                                                                  int32_t row_bytes) {
   pdl_wait_prerequisites();   // the resolver's miss lists must be complete and visible
   const int lane = threadIdx.x & 31;
-  if (p.ord.cnt) {
+  __shared__ MissItems mi;  // the ordered layout's index of this CTA's index group
+  if (p.ord.cnt && !p.ord.ranges) {
+    // ordered layout, spread schedule: the group's warps take its 4-entry items in bucket order (warp w:
+    // items w, w + nwarps, ...)
     const int g = blockIdx.y;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    __shared__ MissItems mi;
     if (threadIdx.x < 32) mi.load(p.ord, g);
     __syncthreads();
     const int4* bk = p.ord.buckets + (int64_t)g * kMissBuckets * p.ord.cap;
@@ -768,6 +770,45 @@ __global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(const ResolvePa
       int4 ent = make_int4(0, 0, 0, 0);
       if (lane < nrows) ent = (in_ov ? ov : bk)[start + lane];
       copy_miss_rows<CPR>(ptrs, l0, p.group, ent, nrows, row_bytes, p.num_gpu_blocks * p.S, p.num_host_blocks * p.S);
+    }
+    return;
+  }
+  if (p.ord.cnt) {
+    // ordered layout on large host pools: the group's warps take its buckets whole (warp w: buckets w,
+    // w + nwarps, ...), each chunk ordered by sub-range in the warp's shared memory, then the overflow
+    // entries
+    const int g = blockIdx.y;
+    const int wib = threadIdx.x >> 5;
+    // CTA-major numbering: consecutive buckets go to different CTAs (different SMs), so the warps
+    // that have work are spread over the whole grid
+    const int warp = wib * (int)gridDim.x + (int)blockIdx.x;
+    const int nwarps = (int)(((int64_t)gridDim.x * blockDim.x) >> 5);
+    __shared__ int4 s_sorted[kCopyThreads / 32][kCopySortChunk];
+    __shared__ int s_sub[kCopyThreads / 32][kSubRanges];
+    if (threadIdx.x < 32) mi.load(p.ord, g);
+    __syncthreads();
+    const int4* bk = p.ord.buckets + (int64_t)g * kMissBuckets * p.ord.cap;
+    const int4* ov = p.ord.overflow + (int64_t)g * p.ord.per_group;
+    const int l0 = (p.layer_begin + g) * p.group;
+    const int gpu_rows = p.num_gpu_blocks * p.S, host_rows = p.num_host_blocks * p.S;
+    for (int b = warp; b < kMissBuckets; b += nwarps) {
+      const int nb = mi.cnt[b];
+      for (int c0 = 0; c0 < nb; c0 += kCopySortChunk) {
+        const int m = min(kCopySortChunk, nb - c0);
+        sort_by_subrange(bk + (int64_t)b * p.ord.cap + c0, m, p.ord.shift, s_sorted[wib], s_sub[wib]);
+        for (int i = 0; i < m; i += kMissRowsPerItem) {
+          const int nrows = min(kMissRowsPerItem, m - i);
+          const int4 ent = lane < nrows ? s_sorted[wib][i + lane] : make_int4(0, 0, 0, 0);
+          copy_miss_rows<CPR>(ptrs, l0, p.group, ent, nrows, row_bytes, gpu_rows, host_rows);
+        }
+        __syncwarp();
+      }
+    }
+    const int ov_items = (mi.overflow + kMissRowsPerItem - 1) / kMissRowsPerItem;
+    for (int i = warp; i < ov_items; i += nwarps) {
+      const int nrows = min(kMissRowsPerItem, mi.overflow - i * kMissRowsPerItem);
+      const int4 ent = lane < nrows ? ov[(int64_t)i * kMissRowsPerItem + lane] : make_int4(0, 0, 0, 0);
+      copy_miss_rows<CPR>(ptrs, l0, p.group, ent, nrows, row_bytes, gpu_rows, host_rows);
     }
     return;
   }

@@ -62,7 +62,7 @@ def huge_page_bytes() -> int:
 class _Mapping:
     """Owns one mapping, aligned to the huge page size; the tensor views keep it alive."""
 
-    def __init__(self, nbytes: int):
+    def __init__(self, nbytes: int, huge: bool = True):
         L = _c()
         hp = huge_page_bytes()
         span = nbytes + hp
@@ -70,7 +70,7 @@ class _Mapping:
         if base is None or base == ctypes.c_void_p(-1).value:
             raise MemoryError(f"mmap of {span} bytes failed")
         ptr = (base + hp - 1) // hp * hp
-        self.huge = L.madvise(ptr, nbytes, _MADV_HUGEPAGE) == 0
+        self.huge = huge and L.madvise(ptr, nbytes, _MADV_HUGEPAGE) == 0
         rc = int(torch.cuda.cudart().cudaHostRegister(ptr, nbytes, _CUDA_HOST_REGISTER_PORTABLE_MAPPED))
         if rc != 0:
             L.munmap(base, span)
@@ -87,10 +87,33 @@ def _array(m: _Mapping, nbytes: int) -> np.ndarray:
     return np.ctypeslib.as_array(buf)[:nbytes]
 
 
-def pinned_host_pool(shape, dtype=torch.uint8) -> torch.Tensor:
+def huge_page_fraction(t: torch.Tensor) -> float:
+    """The share of a host tensor's resident bytes that the kernel backs with transparent huge pages
+    (AnonHugePages / Rss of the mappings it spans, from /proc/self/smaps); -1.0 if it cannot be read."""
+    lo = t.data_ptr()
+    hi = lo + t.numel() * t.element_size()
+    rss = huge = 0
+    try:
+        cur = None
+        for line in open("/proc/self/smaps"):
+            f = line.split()
+            if "-" in f[0] and len(f) >= 5 and not f[0].endswith(":"):
+                a, b = (int(x, 16) for x in f[0].split("-"))
+                cur = a < hi and b > lo
+            elif cur and f[0] == "Rss:":
+                rss += int(f[1])
+            elif cur and f[0] == "AnonHugePages:":
+                huge += int(f[1])
+    except (OSError, ValueError, IndexError):
+        return -1.0
+    return huge / rss if rss else -1.0
+
+
+def pinned_host_pool(shape, dtype=torch.uint8, huge: bool = True) -> torch.Tensor:
     """A page-locked, device-mapped host tensor of exactly this size, backed by huge pages where the
-    system allows (see the module docstring).  Contents are unspecified."""
+    system allows (see the module docstring); huge=False keeps the base pages (for comparison).
+    Contents are unspecified."""
     itemsize = torch.empty((), dtype=dtype).element_size()
     nbytes = max(int(np.prod(shape)) * itemsize, 1 << 16)
-    m = _Mapping(nbytes)
+    m = _Mapping(nbytes, huge)
     return torch.from_numpy(_array(m, int(np.prod(shape)) * itemsize)).view(dtype).reshape(shape)

@@ -17,11 +17,16 @@ class Rig:
     def __init__(self, w, *, oracle_bytes: bool = False, device: str = "cuda", check_hot_bytes: bool = True,
                  mode: str = "split", graph: bool = False):
         # "split" / "fused": the library's default miss layout for the pool (ordered only for large host
-        # pools); a "+order" suffix forces the address-ordered layout on any pool
+        # pools); a "+order" suffix forces the address-ordered layout on any pool, "+ranges" its range
+        # schedule (whole host ranges per copy warp), "+ranges2" the same with two miss warps per
+        # fused-gather CTA
         base, _, opt = mode.partition("+")
-        assert base in ("split", "fused") and opt in ("", "order")
+        assert base in ("split", "fused") and opt in ("", "order", "ranges", "ranges2")
         self.mode = base
-        self.force_order = opt == "order"
+        self.force_order = opt != ""
+        self.order_mode = {"order": hs.MISS_ORDER_ON, "ranges": hs.MISS_ORDER_RANGES,
+                           "ranges2": hs.MISS_ORDER_RANGES}.get(opt)
+        self.miss_warps = 2 if opt == "ranges2" else 0
         self.graph = graph
         self.prep = None
         self.w = w
@@ -41,7 +46,8 @@ class Rig:
                 sdev.fill_host_pool(w, l, self.host[l], self.dev)
         self.pool = hs.Pool(self.gpu, self.host if w.num_host_blocks else None)
         if self.force_order:
-            self.pool.set_miss_order(hs.MISS_ORDER_ON)
+            self.pool.set_miss_order(self.order_mode)
+            self.pool.set_miss_warps(self.miss_warps)
         self.bt_np = w.block_table.copy()
         self.hbt_np = w.host_block_table.copy()
         self.bt = torch.from_numpy(self.bt_np).to(self.dev)

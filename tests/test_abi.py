@@ -57,12 +57,15 @@ def test_status_strings(lib):
     assert hs.status_str(99) == "unknown status"
 
 
+NB = 1024   # buckets per index group of the address-ordered miss layout
+
+
 def _ordered_extra(ng, R, P, K, C):
-    # bucket counters (256 + 1 per index group, 16-byte aligned) and 256 buckets per group of twice
+    # bucket counters (NB + 1 per index group, 16-byte aligned) and NB buckets per group of twice
     # the even share of the group's R * min(P*K, C) possible misses, 16 B per entry
     per_group = R * min(P * K, C)
-    cap = -(-2 * per_group // 256)
-    return -(-4 * ng * 257 // 16) * 16 + 16 * ng * 256 * cap
+    cap = -(-2 * per_group // NB)
+    return -(-4 * ng * (NB + 1) // 16) * 16 + 16 * ng * NB * cap
 
 
 def test_size_queries(lib):
@@ -118,6 +121,7 @@ def test_calls_on_null_handles_are_rejected(lib):
     assert L.hs_hot_reset(None, ctypes.byref(hot), 1, None) == 1
     assert L.hs_pool_set_miss_order(None, hs.MISS_ORDER_ON) == 1
     assert L.hs_pool_set_gather_copy(None, hs.GATHER_COPY_BULK) == 1
+    assert L.hs_pool_set_miss_warps(None, 1) == 1
     assert L.hs_resolve_miss_order(None, 0, 1, 1, 1, 1, ctypes.byref(hot), 1 << 30) == -1
     assert L.hs_resolve_workspace_bytes_min(1, 1, 0, 5, 4) == 0
     assert L.hs_resolve_workspace_bytes_min(1, 1, 1, 16385, 4) == 0   # plan beyond HS_MAX_PLAN

@@ -28,7 +28,7 @@ from tests.casekit import Case, host_only_case
 
 pytestmark = pytest.mark.gpu
 
-MODES_ORDER = ["split", "fused", "split+order", "fused+order"]
+MODES_ORDER = ["split", "fused", "split+order", "fused+order", "split+ranges", "fused+ranges", "fused+ranges2"]
 INT32_MAX = 2**31 - 1
 
 
@@ -121,8 +121,12 @@ def _to_gpu(case, dev, mode):
     gpu = [torch.from_numpy(case.pools[0].reshape(case.ngb, S, B).copy()).to(dev)]
     host = [torch.from_numpy(case.hosts[0].reshape(-1, S, B).copy()).pin_memory()]
     pool = hs.Pool(gpu, host)
-    if mode.endswith("+order"):
+    opt = mode.partition("+")[2]
+    if opt == "order":
         pool.set_miss_order(hs.MISS_ORDER_ON)
+    elif opt:
+        pool.set_miss_order(hs.MISS_ORDER_RANGES)
+        pool.set_miss_warps(2 if opt == "ranges2" else 0)
     hot = hs.HotState.allocate(1, torch.from_numpy(case.hot_blocks).to(dev), case.C)
     hot.slot_token.copy_(torch.from_numpy(case.tok))
     hot.slot_stamp.copy_(torch.from_numpy(case.stamp))

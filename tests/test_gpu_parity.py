@@ -33,7 +33,7 @@ def _rig(w, **kw):
 MODES = ["split", "fused"]
 # the same, plus both paths with the address-ordered miss layout forced on (small pools default to
 # per-unit lists)
-MODES_ORDER = MODES + ["split+order", "fused+order"]
+MODES_ORDER = MODES + ["split+order", "fused+order", "split+ranges", "fused+ranges", "fused+ranges2"]
 
 
 def _base(mode):
@@ -41,8 +41,15 @@ def _base(mode):
 
 
 def _set_order(pool, mode):
-    if mode.endswith("+order"):
+    """+order: the address-ordered miss layout on any pool (its spread schedule on small pools);
+    +ranges: its range schedule (whole host ranges per copy warp); +ranges2: with two miss warps per
+    fused-gather CTA."""
+    opt = mode.partition("+")[2]
+    if opt == "order":
         pool.set_miss_order(hs.MISS_ORDER_ON)
+    elif opt in ("ranges", "ranges2"):
+        pool.set_miss_order(hs.MISS_ORDER_RANGES)
+        pool.set_miss_warps(2 if opt == "ranges2" else 0)
 
 
 @pytest.mark.parametrize("mode", MODES_ORDER)
@@ -470,10 +477,15 @@ def test_miss_order_decision():
     assert hs.miss_order_used(pool, hot, 2, R, P, K, full)
     assert hs.miss_order_used(pool, hot, 1, R, P, K, full, layer_begin=1)
     assert not hs.miss_order_used(pool, hot, 2, R, P, K, small)
+    pool.set_miss_order(hs.MISS_ORDER_RANGES)
+    assert hs.miss_order_used(pool, hot, 2, R, P, K, full)
+    assert not hs.miss_order_used(pool, hot, 2, R, P, K, small)
     pool.set_miss_order(hs.MISS_ORDER_OFF)
     assert not hs.miss_order_used(pool, hot, 2, R, P, K, full)
     with pytest.raises(hs.HSError):
         pool.set_miss_order(7)
+    with pytest.raises(hs.HSError):
+        pool.set_miss_warps(3)
     no_host = hs.Pool(gpu)
     no_host.set_miss_order(hs.MISS_ORDER_ON)
     assert not hs.miss_order_used(no_host, hot, 2, R, P, K, full)
@@ -525,6 +537,59 @@ def test_gather_standalone_multilayer_and_status():
     out = hs.gather_rows(pool, torch.from_numpy(rows[:2]).to(dev), layer_begin=1)
     o_out, _ = oracle.gather(B=B, num_rows=ngb * S, pools=pools_np, rows=rows[:2], layer_begin=1)
     assert np.array_equal(out.cpu().numpy(), o_out)
+    pool.close()
+
+
+@pytest.mark.parametrize("mode", ["split+order", "fused+order", "split+ranges", "fused+ranges", "fused+ranges2"])
+@pytest.mark.parametrize("P", [1, 4])
+def test_ordered_misses_overflowing_their_bucket(mode, P):
+    """Every page's host copy lies in the first two host blocks (one host-row range), so with the
+    address-ordered layout forced on almost all misses overflow their bucket into the overflow list:
+    rows, stats, slot state, pool bytes and gathered bytes must still equal the oracle's, with repeats
+    of missed ids across positions (P = 4)."""
+    rng = np.random.default_rng(40 + P)
+    dev = torch.device("cuda")
+    R, S, B, pages, C = 8, 64, 656, 64, 1024
+    K = 256 if P == 1 else 128
+    nb = C // S
+    perm = rng.permutation(R + R * nb).astype(np.int32)
+    bt = np.full((R, pages), -1, np.int32)
+    bt[:, pages - 1] = perm[:R]
+    hot = perm[R:].reshape(R, nb)
+    hbt = (np.arange(pages, dtype=np.int32)[None, :] % 2).repeat(R, 0)
+    case = Case(R=R, S=S, B=B, C=C, max_pages=pages, ctx=[pages * S] * R, resident=True, host=True, hot_blocks=hot,
+                num_gpu_blocks=R + R * nb, num_host_blocks=512, bt=bt, hbt=hbt, seed=9)
+    pool, gpu, host, hot_t = _case_to_gpu(case, dev)
+    _set_order(pool, mode)
+    bt_d, hbt_d, ctx = torch.from_numpy(case.bt).to(dev), torch.from_numpy(case.hbt).to(dev), torch.from_numpy(case.ctx).to(dev)
+    prev = None
+    for t in range(3):
+        ids = np.empty((R, P, K), np.int32)
+        for r in range(R):
+            base = rng.choice(pages * S, size=K, replace=False) if prev is None else np.concatenate(
+                [rng.choice(prev[r, 0], size=K // 2, replace=False),
+                 rng.choice(np.setdiff1d(np.arange(pages * S), prev[r, 0]), size=K - K // 2, replace=False)])
+            ids[r, 0] = rng.permutation(base)
+            for q in range(1, P):
+                ids[r, q] = rng.permutation(np.concatenate([ids[r, 0][:int(0.9 * K)],
+                                                            rng.choice(pages * S, size=K - int(0.9 * K))]))
+        prev = ids
+        topk = torch.from_numpy(ids[None]).to(dev)
+        if _base(mode) == "fused":
+            rows, stats, g = hs.resolve_gather(pool, topk, bt_d, hbt_d, ctx, hot_t, t)
+        else:
+            rows, stats = hs.resolve_topk(pool, topk, bt_d, hbt_d, ctx, hot_t, t)
+            g = hs.gather_rows(pool, rows.reshape(1, -1))
+        o_rows, o_stats = case.step(ids, t)
+        torch.cuda.synchronize()
+        assert (o_stats[..., 0] == 0).all() and int(o_stats[..., 3].sum()) > 500
+        assert np.array_equal(stats.cpu().numpy(), o_stats), t
+        assert np.array_equal(rows.cpu().numpy(), o_rows), t
+        assert np.array_equal(hot_t.slot_token.cpu().numpy(), case.tok), t
+        assert np.array_equal(hot_t.slot_stamp.cpu().numpy(), case.stamp), t
+        assert np.array_equal(gpu[0].cpu().numpy().reshape(-1), case.pools[0]), t
+        o_out, _ = case.gather(o_rows.reshape(1, -1))
+        assert np.array_equal(g.cpu().numpy(), o_out), t
     pool.close()
 
 
