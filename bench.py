@@ -102,9 +102,10 @@ def parse():
                     help="link probe: register the host pool without huge pages (for comparison)")
     ap.add_argument("--probe-cpu-fill", action="store_true",
                     help="link probe: write the host pool with CPU stores instead of DMA (for comparison)")
-    ap.add_argument("--miss-order", choices=["auto", "on", "off"], default="auto",
+    ap.add_argument("--miss-order", choices=["auto", "on", "off", "ranges"], default="auto",
                     help="miss layout handed to the copy warps: auto (the library's default: host-address order "
-                         "for host pools of 16 GiB or more), on (always address order), off (per-unit lists)")
+                         "for host pools of 16 GiB or more), on (always address order), off (per-unit lists), "
+                         "ranges (address order with the range schedule on any pool)")
     ap.add_argument("--timing", choices=["auto", "eager", "graph", "both"], default="auto",
                     help="eager: the C-ABI calls of each timed step bracketed by events; graph: each timed step "
                          "captured as one CUDA graph and replayed once, the replay bracketed by events; both: "
@@ -467,7 +468,8 @@ def run_ours(args, ws, rank, local):
         sdev.fill_gpu_pool(w, l, gpu[l])
         sdev.fill_host_pool(w, l, host[l], dev)
     pool = hs.Pool(gpu, host)
-    pool.set_miss_order({"auto": hs.MISS_ORDER_AUTO, "on": hs.MISS_ORDER_ON, "off": hs.MISS_ORDER_OFF}[args.miss_order])
+    pool.set_miss_order({"auto": hs.MISS_ORDER_AUTO, "on": hs.MISS_ORDER_ON, "off": hs.MISS_ORDER_OFF,
+                         "ranges": hs.MISS_ORDER_RANGES}[args.miss_order])
     pool.set_miss_warps(args.miss_warps)
     from sparse_mla_kv_gb300.hostmem import huge_page_fraction
     huge_frac = [round(huge_page_fraction(h), 4) for h in host]
@@ -487,8 +489,10 @@ def run_ours(args, ws, rank, local):
     out_rows = res_dev[:n_rows_dev].view(NG, R, P, Kk)
     out_stats = res_dev[n_rows_dev:].view(NG, R, 4)
     ws_buf = hs.alloc_workspace(NG, R, P, Kk, C, dev)
-    miss_order = ("host-address buckets" if hs.miss_order_used(pool, hot, L, R, P, Kk, ws_buf.numel())
-                  else "per-unit lists")
+    host_total = L * max(1, w.num_host_blocks) * S * B
+    miss_order = ("per-unit lists" if not hs.miss_order_used(pool, hot, L, R, P, Kk, ws_buf.numel())
+                  else "host-address buckets, " + ("range schedule" if args.miss_order == "ranges" or
+                                                   host_total >= (40 << 30) else "spread schedule"))
     gout = torch.empty((L, R * P * Kk, B), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
