@@ -153,8 +153,8 @@ size_t hs_resolve_workspace_bytes_min(int32_t nl, int32_t R, int32_t P, int32_t 
  * Address-ordered: the resolver files each index group's misses into 1024 buckets by host row range.
  * The copy warps then take them in one of two schedules: on host pools under 40 GiB (over the call's
  * layers) the 4-entry items of all buckets in bucket order, spread over every copy warp; from 40 GiB
- * on (or with HS_MISS_ORDER_RANGES) whole buckets per warp, each read in address order, so that every
- * warp walks its own range of the pool.  The pages copy single rows from pinned host memory
+ * on (or with HS_MISS_ORDER_RANGES) one contiguous block of buckets per warp, so that every warp reads
+ * its own range of the pool.  The pages copy single rows from pinned host memory
  * ("vLLM GLM 5.3 Optimizations: Hybrid HiSparse Offloading", "Technical Implementation of Hybrid
  * HiSparse") and say nothing of their order; this is the library's choice.  Zero-copy reads spread
  * over tens of GB of host memory are bound by the device's address translation for host memory, not
@@ -187,7 +187,7 @@ hs_status hs_pool_set_gather_copy(hs_pool* pool, int32_t mode);
 
 /* Miss warps per CTA of the fused gather (hs_gather_planned, hs_resolve_gather) when the address-
  * ordered miss layout takes its range schedule (host pools of 40 GiB or more over the call's layers:
- * each copy warp reads whole host-row ranges): 1 or 2, or 0 for the library's default (1).  More warps
+ * each copy warp reads its own range of host rows): 1 or 2, or 0 for the library's default (1).  More warps
  * read more ranges at once and leave fewer warps per CTA for the HBM rows.  Results are identical.
  * Other layouts always use one miss warp per CTA.  HS_ERR_INVALID_ARG for another count. */
 hs_status hs_pool_set_miss_warps(hs_pool* pool, int32_t warps);

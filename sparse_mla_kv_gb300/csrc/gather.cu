@@ -34,7 +34,6 @@ constexpr int kGatherUnroll = 8;
 // on the mixed batch); with the range schedule of large pools the pool may ask for two
 // (hs_pool_set_miss_warps), so that more host ranges are read at once.
 constexpr int kMaxMissWarps = 2;
-constexpr int kSortChunk = 256;  // ordered layout: bucket entries one miss warp orders and copies at a time
 
 template <int CPR>
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const LayerPtrs ptrs, int32_t layer_begin,
@@ -278,179 +277,44 @@ __device__ __forceinline__ void copy_miss_item(const uint8_t* __restrict__ host,
   }
 }
 
-// ---- staged miss copies (ordered layout).  A warp copies its sorted bucket entries in batches of up
-// to kBatchRows rows: cp.async moves each row's 16-byte chunks from the pinned host pool into a
-// shared-memory stage (no registers hold the data), and while one batch is in flight the previous one
-// is stored from the other stage into its hot slots, its output positions and the positions of its
-// repeats.  Each warp thus keeps up to two batches of host reads in flight.
-constexpr int kBatchRows = 16;
-constexpr int kStageBudget = 24 * 1024;  // dynamic shared memory of a CTA's stages (all its miss warps), at most
-
-__device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* gsrc) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst), "l"(gsrc) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// Rows per batch for this row size with nmiss miss warps per CTA sharing the budget (0: the stages do
-// not fit, copy through registers instead).
-__host__ __device__ inline int staged_batch_rows(int row_bytes, int nmiss) {
-  const int r = kStageBudget / nmiss / (2 * row_bytes);
-  return r >= kBatchRows ? kBatchRows : (r >= 1 ? r : 0);
-}
-
-// A warp's entry is usable if its host row, pool row and output position lie in their buffers (always
-// true outside the bounds-checked build).
-__device__ __forceinline__ bool entry_ok(int4 e, int64_t per_layer, int64_t gpu_rows, int64_t host_rows) {
-  (void)per_layer;
-  (void)gpu_rows;
-  (void)host_rows;
-  return HS_CHECK(e.x >= 0 && e.x < host_rows, kChkHostRow) && HS_CHECK(e.y >= 0 && e.y < gpu_rows, kChkPoolRow) &&
-         HS_CHECK(e.z >= 0 && e.z < per_layer, kChkOutPos);
-}
-
-// Issues the cp.async copies of ents[0..nr) into stage (one commit group).
+// The miss warps of the fused gather (the CTA's first warps), outside the kernel body (not inlined) so
+// that their registers do not add to the HBM warps' streaming loop.
+//
+// Range schedule (ordered layout on large host pools): the layer's nmw miss warps split its group's
+// buckets into contiguous blocks -- warp w takes buckets [w * kMissBuckets / nmw, (w + 1) * kMissBuckets
+// / nmw), a range of the host pool -- and copies their entries in 4-entry items as filed, then one
+// slice of the overflow list.  Every warp thus reads its own range of the pool.  Measured on the
+// full-size MTP3 miss pattern (4 pools of 18 GB, 94.5K misses each) with a standalone read: 134 GB/s
+// with 304 warps per pool reading contiguous blocks of 17.6 MB buckets, against 113 GB/s with 152
+// warps, 85-120 GB/s fully address-sorted, and 39 GB/s in random order; rows staged in shared memory
+// with cp.async were no faster than rows held in registers.
 template <int CPR>
-__device__ __forceinline__ void stage_batch(const uint8_t* __restrict__ host, const int4* ents, int nr, int row_bytes,
-                                            uint32_t stage, int64_t per_layer, int64_t gpu_rows, int64_t host_rows) {
-  const int cpr = CPR ? CPR : (row_bytes >> 4);
+__device__ __noinline__ void miss_warp_ranges(const MissOrder ord, int pu, int mw, int nmw,
+                                              const uint8_t* __restrict__ host, uint8_t* __restrict__ pool,
+                                              uint8_t* __restrict__ lout, const int32_t* __restrict__ lmsrc, int n,
+                                              int row_bytes, int64_t per_layer, int64_t num_rows,
+                                              int64_t num_host_rows) {
   const int lane = threadIdx.x & 31;
-  for (int f = lane; f < nr * cpr; f += 32) {
-    const int rr = f / cpr;
-    const int4 e = ents[rr];
-    if (HS_CHECKED && !entry_ok(e, per_layer, gpu_rows, host_rows)) continue;
-    cp_async16(stage + 16u * (uint32_t)f, host + (int64_t)e.x * row_bytes + (int64_t)(f - rr * cpr) * 16);
-  }
-  cp_async_commit();
-}
-
-// Stores a landed batch: every row into its hot slot and its output position, then along the repeat
-// chains (one link per round for every entry at once).  chain: kBatchRows ints of the warp's shared
-// memory.  Ends with __syncwarp (the stage may be refilled).
-template <int CPR>
-__device__ __forceinline__ void store_batch(uint8_t* __restrict__ pool, uint8_t* __restrict__ lout,
-                                            const int32_t* __restrict__ lmsrc, int n, const int4* ents, int nr,
-                                            int row_bytes, const unsigned char* stage, int* chain, int64_t per_layer,
-                                            int64_t gpu_rows, int64_t host_rows) {
-  const int cpr = CPR ? CPR : (row_bytes >> 4);
-  const int lane = threadIdx.x & 31;
-  if (lane < nr) {
-    const int4 e = ents[lane];
-    int d = entry_ok(e, per_layer, gpu_rows, host_rows) ? e.w : -1;
-    if (d >= 0 && !HS_CHECK(d < n, kChkChain)) d = -1;
-    chain[lane] = d;
-  }
-  __syncwarp();
-  for (int f = lane; f < nr * cpr; f += 32) {
-    const int rr = f / cpr;
-    const int4 e = ents[rr];
-    if (HS_CHECKED && !entry_ok(e, per_layer, gpu_rows, host_rows)) continue;
-    const uint4 v = reinterpret_cast<const uint4*>(stage)[f];
-    const int64_t cc16 = (int64_t)(f - rr * cpr) * 16;
-    *reinterpret_cast<uint4*>(pool + (int64_t)e.y * row_bytes + cc16) = v;
-    *reinterpret_cast<uint4*>(lout + (int64_t)e.z * row_bytes + cc16) = v;
-  }
-  while (__any_sync(kFull, lane < nr && chain[lane] >= 0)) {
-    for (int f = lane; f < nr * cpr; f += 32) {
-      const int rr = f / cpr;
-      const int d = chain[rr];
-      if (d < 0) continue;
-      const int q = ents[rr].z / n;  // the entry's request
-      *reinterpret_cast<uint4*>(lout + ((int64_t)q * n + d) * row_bytes + (int64_t)(f - rr * cpr) * 16) =
-          reinterpret_cast<const uint4*>(stage)[f];
-    }
-    __syncwarp();
-    if (lane < nr) {
-      int d = chain[lane];
-      if (d >= 0) {
-        d = -3 - __ldcg(lmsrc + (int64_t)(ents[lane].z / n) * n + d);
-        if (d >= 0 && !HS_CHECK(d < n, kChkChain)) d = -1;
-        chain[lane] = d;
-      }
-    }
-    __syncwarp();
-  }
-  __syncwarp();
-}
-
-// The miss warps of the fused gather, one per CTA, outside the kernel body (not inlined) so that
-// their registers do not add to the HBM warps' streaming loop.
-// Ordered layout on large host pools (ranges): the layer's miss warps take its group's buckets whole
-// (warp w: buckets w, w + nmw, ...), each chunk ordered by sub-range in shared memory, so that every
-// warp reads its own host range upward; then one slice of the overflow list per warp.
-template <int CPR>
-__device__ __noinline__ void miss_warp_ordered(const MissOrder ord, int pu, int mw, int nmw,
-                                               const uint8_t* __restrict__ host, uint8_t* __restrict__ pool,
-                                               uint8_t* __restrict__ lout, const int32_t* __restrict__ lmsrc, int n,
-                                               int row_bytes, int64_t per_layer, int64_t num_rows,
-                                               int64_t num_host_rows, unsigned char* stages, int batch,
-                                               int4* s_sorted, int* s_sub, int* s_chain) {
-  const int wib = threadIdx.x >> 5;  // the CTA's miss warps are its first warps: each has its own buffers
   const int32_t* cntg = ord.cnt + (int64_t)pu * (kMissBuckets + 1);  // counts read from L2 where needed
-  const int ovn = min(__ldcg(cntg + kMissBuckets), ord.per_group);
   const int4* bk = ord.buckets + (int64_t)pu * kMissBuckets * ord.cap;
-  const size_t stage_bytes = (size_t)batch * row_bytes;
-  unsigned char* my_stages = stages + 2 * stage_bytes * wib;
-  const uint32_t st0 = static_cast<uint32_t>(__cvta_generic_to_shared(my_stages));
-  // the buckets whole (index b < kMissBuckets), then one contiguous slice of the overflow list per warp
-  // (index kMissBuckets + slice), in chunks of kSortChunk entries
-  const int ov_per = (ovn + nmw - 1) / nmw;
-  for (int b = mw; b < kMissBuckets + nmw; b += nmw) {
-    const bool ov = b >= kMissBuckets;
-    const int o0 = ov ? (b - kMissBuckets) * ov_per : 0;
-    const int nb = ov ? max(0, min(ov_per, ovn - o0)) : min(__ldcg(cntg + b), ord.cap);
-    const int4* src = ov ? ord.overflow + (int64_t)pu * ord.per_group + o0 : bk + (int64_t)b * ord.cap;
-    for (int c0 = 0; c0 < nb; c0 += kSortChunk) {
-      const int m = min(kSortChunk, nb - c0);
-      sort_by_subrange(src + c0, m, ord.shift, s_sorted, s_sub);
-      // two stages: batch k + 1 lands while batch k is stored
-      const int nbat = (m + batch - 1) / batch;
-      stage_batch<CPR>(host, s_sorted, min(batch, m), row_bytes, st0, per_layer, num_rows, num_host_rows);
-      for (int k = 0; k < nbat; ++k) {
-        if (k + 1 < nbat) {
-          stage_batch<CPR>(host, s_sorted + (k + 1) * batch, min(batch, m - (k + 1) * batch), row_bytes,
-                           st0 + (uint32_t)(((k + 1) & 1) * stage_bytes), per_layer, num_rows, num_host_rows);
-          cp_async_wait<1>();
-        } else {
-          cp_async_wait<0>();
-        }
-        __syncwarp();
-        store_batch<CPR>(pool, lout, lmsrc, n, s_sorted + k * batch, min(batch, m - k * batch), row_bytes,
-                         my_stages + (k & 1) * stage_bytes, s_chain, per_layer, num_rows, num_host_rows);
-      }
-      __syncwarp();
+  const int b0 = (int)((int64_t)mw * kMissBuckets / nmw), b1 = (int)((int64_t)(mw + 1) * kMissBuckets / nmw);
+  for (int b = b0; b < b1; ++b) {
+    const int nb = min(__ldcg(cntg + b), ord.cap);
+    const int4* src = bk + (int64_t)b * ord.cap;
+    for (int i = 0; i < nb; i += kMissRowsPerItem) {
+      const int nrows = min(kMissRowsPerItem, nb - i);
+      const int4 ent = lane < nrows ? src[i + lane] : make_int4(0, 0, 0, 0);
+      copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
     }
   }
-}
-
-// The same without stages, for rows too large to stage (each item's rows held in registers).
-template <int CPR>
-__device__ __noinline__ void miss_warp_ordered_regs(const MissOrder ord, int pu, int mw, int nmw,
-                                                    const uint8_t* __restrict__ host, uint8_t* __restrict__ pool,
-                                                    uint8_t* __restrict__ lout, const int32_t* __restrict__ lmsrc,
-                                                    int n, int row_bytes, int64_t per_layer, int64_t num_rows,
-                                                    int64_t num_host_rows, int4* s_sorted, int* s_sub) {
-  const int lane = threadIdx.x & 31;
-  const int32_t* cntg = ord.cnt + (int64_t)pu * (kMissBuckets + 1);
   const int ovn = min(__ldcg(cntg + kMissBuckets), ord.per_group);
-  const int4* bk = ord.buckets + (int64_t)pu * kMissBuckets * ord.cap;
   const int ov_per = (ovn + nmw - 1) / nmw;
-  for (int b = mw; b < kMissBuckets + nmw; b += nmw) {
-    const bool ov = b >= kMissBuckets;
-    const int o0 = ov ? (b - kMissBuckets) * ov_per : 0;
-    const int nb = ov ? max(0, min(ov_per, ovn - o0)) : min(__ldcg(cntg + b), ord.cap);
-    const int4* src = ov ? ord.overflow + (int64_t)pu * ord.per_group + o0 : bk + (int64_t)b * ord.cap;
-    for (int c0 = 0; c0 < nb; c0 += kSortChunk) {
-      const int m = min(kSortChunk, nb - c0);
-      sort_by_subrange(src + c0, m, ord.shift, s_sorted, s_sub);
-      for (int i = 0; i < m; i += kMissRowsPerItem) {
-        const int nrows = min(kMissRowsPerItem, m - i);
-        const int4 ent = lane < nrows ? s_sorted[i + lane] : make_int4(0, 0, 0, 0);
-        copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
-      }
-      __syncwarp();
-    }
+  const int o0 = mw * ov_per, o1 = min(ovn, o0 + ov_per);
+  const int4* ovl = ord.overflow + (int64_t)pu * ord.per_group;
+  for (int i = o0; i < o1; i += kMissRowsPerItem) {
+    const int nrows = min(kMissRowsPerItem, o1 - i);
+    const int4 ent = lane < nrows ? ovl[i + lane] : make_int4(0, 0, 0, 0);
+    copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
   }
 }
 
@@ -521,8 +385,7 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
     const LayerPtrs ptrs, int32_t layer_begin, int32_t group, int32_t R, int32_t n, int32_t max_m,
     const int32_t* __restrict__ rows, const int32_t* __restrict__ miss_count, const int4* __restrict__ miss_list,
     const MissOrder ord, const int32_t* __restrict__ msrc, uint8_t* __restrict__ out, int32_t row_bytes,
-    int64_t num_rows, int64_t num_host_rows, int32_t batch, int32_t nmiss) {
-  extern __shared__ __align__(16) unsigned char fused_stages[];  // ordered layout: the miss warps' stages
+    int64_t num_rows, int64_t num_host_rows, int32_t nmiss) {
   pdl_wait_prerequisites();   // the resolve plan (rows, sources, miss lists) must be complete and visible
   const int cpr = CPR ? CPR : (row_bytes >> 4);
   const int lr = blockIdx.y;
@@ -538,20 +401,13 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
     // CTA-major numbering: consecutive buckets (or items) go to different CTAs, spread over the SMs
     const int64_t mw = (int64_t)warp * gridDim.x + blockIdx.x;
     const int64_t nmw = (int64_t)gridDim.x * nmiss;
-    // the ordered layout's per-miss-warp buffers: bucket counts, a sorted chunk, sub-range counters, chains
     __shared__ MissItems s_mi;  // spread schedule (one miss warp)
-    __shared__ int4 s_sorted[kMaxMissWarps][kSortChunk];
-    __shared__ int s_sub[kMaxMissWarps][kSubRanges];
-    __shared__ int s_chain[kMaxMissWarps][kBatchRows];
     if (ord.cnt && !ord.ranges)
       miss_warp_spread<CPR>(ord, pu, (int)mw, (int)nmw, host, pool, lout, lmsrc, n, row_bytes, per_layer, num_rows,
                             num_host_rows, s_mi);
-    else if (ord.cnt && batch)
-      miss_warp_ordered<CPR>(ord, pu, (int)mw, (int)nmw, host, pool, lout, lmsrc, n, row_bytes, per_layer, num_rows,
-                             num_host_rows, fused_stages, batch, s_sorted[warp], s_sub[warp], s_chain[warp]);
     else if (ord.cnt)
-      miss_warp_ordered_regs<CPR>(ord, pu, (int)mw, (int)nmw, host, pool, lout, lmsrc, n, row_bytes, per_layer,
-                                  num_rows, num_host_rows, s_sorted[warp], s_sub[warp]);
+      miss_warp_ranges<CPR>(ord, pu, (int)mw, (int)nmw, host, pool, lout, lmsrc, n, row_bytes, per_layer, num_rows,
+                            num_host_rows);
     else
       miss_warp_lists<CPR>(miss_count, miss_list, pu, R, max_m, mw, nmw, host, pool, lout, lmsrc, n, row_bytes,
                            per_layer, num_rows, num_host_rows);
@@ -634,9 +490,8 @@ uint32_t check_take_gather() {
 void warm_gather_launch_configs() {
   resident_blocks(gather_kernel<41>, &g_occ_plain[0]);
   resident_blocks(gather_kernel<0>, &g_occ_plain[1]);
-  // the fused gather's CTAs may carry up to kStageBudget bytes of stages (ordered layout, range schedule)
-  resident_blocks(gather_fused_kernel<41>, &g_occ_fused[0], kStageBudget);
-  resident_blocks(gather_fused_kernel<0>, &g_occ_fused[1], kStageBudget);
+  resident_blocks(gather_fused_kernel<41>, &g_occ_fused[0]);
+  resident_blocks(gather_fused_kernel<0>, &g_occ_fused[1]);
   if (g_bulk_smem_max == 0) {
     int dev = 0, optin = 0;
     if (cudaGetDevice(&dev) == cudaSuccess &&
@@ -687,28 +542,26 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
   const bool k41 = row_bytes == 656;
   auto kern = k41 ? gather_fused_kernel<41> : gather_fused_kernel<0>;
   // miss warps per CTA: the pool's choice for the range schedule, one otherwise
-  const int nmiss = (ord.cnt && ord.ranges) ? (range_miss_warps >= 2 ? 2 : 1) : 1;
+  const int nmiss = (ord.cnt && ord.ranges) ? (range_miss_warps >= kMaxMissWarps ? kMaxMissWarps : 1) : 1;
   const int64_t per_layer = (int64_t)R * n * (row_bytes >> 4);
   const int64_t want_hbm = (per_layer + (int64_t)kGatherThreads * kGatherUnroll - 1) /
                            ((int64_t)kGatherThreads * kGatherUnroll);
   // enough CTAs that each miss warp can take one item (kMissRowsPerItem misses) of the most a layer can
   // have, so a small batch does not queue its host round trips on a few warps
   const int64_t want_miss = ((int64_t)R * ((max_m + kMissRowsPerItem - 1) / kMissRowsPerItem) + nmiss - 1) / nmiss;
-  const dim3 grid = wave_grid(sms, resident_blocks(kern, &occ[k41 ? 0 : 1], kStageBudget),
-                              want_hbm > want_miss ? want_hbm : want_miss, nl);
+  const dim3 grid = wave_grid(sms, resident_blocks(kern, &occ[k41 ? 0 : 1]), want_hbm > want_miss ? want_hbm : want_miss,
+                              nl);
   // With the ordered layout (large host pools) the gather is not launched early: CTAs placed while
   // the resolver still runs made the whole gather's host reads slower there (measured: agentic
   // decode over a 29 GB pool, 684 us per step against 333 us with the launch held back).
   cudaError_t e;
   if (ord.cnt) {
-    const int batch = ord.ranges ? staged_batch_rows(row_bytes, nmiss) : 0;
-    const size_t smem = (size_t)nmiss * 2 * batch * row_bytes;
-    kern<<<grid, kGatherThreads, smem, s>>>(ptrs, layer_begin, group, R, n, max_m, rows, miss_count, miss_list, ord,
-                                            msrc, out, row_bytes, num_rows, num_host_rows, batch, nmiss);
+    kern<<<grid, kGatherThreads, 0, s>>>(ptrs, layer_begin, group, R, n, max_m, rows, miss_count, miss_list, ord, msrc,
+                                         out, row_bytes, num_rows, num_host_rows, nmiss);
     e = cudaGetLastError();
   } else {
     e = launch_dependent(kern, grid, dim3(kGatherThreads), 0, s, ptrs, layer_begin, group, R, n, max_m, rows,
-                         miss_count, miss_list, ord, msrc, out, row_bytes, num_rows, num_host_rows, 0, 1);
+                         miss_count, miss_list, ord, msrc, out, row_bytes, num_rows, num_host_rows, 1);
   }
   if (e != cudaSuccess) return e;
   count_launch();

@@ -97,9 +97,8 @@ constexpr int kMissRowsPerItem = 4;
 // by the device's address translation for host memory, not by the link: a step whose in-flight
 // reads span the whole pool misses the translation caches on nearly every row.  In this layout the
 // resolver files each miss of an index group into one of kMissBuckets buckets by host row range
-// (bucket = host row >> shift), and each copy warp takes whole buckets and reads them in address
-// order (see sort_by_subrange below).  Results do not depend on it: every miss writes its own hot
-// slot and output row.
+// (bucket = host row >> shift), and the copy warps take the buckets in one of two schedules (below).
+// Results do not depend on it: every miss writes its own hot slot and output row.
 constexpr int kMissBuckets = 1024;  // enough host ranges that every copy warp of a large step owns some
 constexpr int kBucketsPerLane = kMissBuckets / 32;
 struct MissOrder {
@@ -308,43 +307,6 @@ struct MissItems {
     nrows = count < kMissRowsPerItem ? count : kMissRowsPerItem;
   }
 };
-
-// Bucket-major copying of the ordered layout.  A copy warp takes whole buckets (a bucket is a range of
-// 2^shift host rows), in chunks of at most `cap` entries, and orders each chunk in shared memory by
-// the 64 sub-ranges of its bucket (a counting sort; order inside a sub-range is arbitrary) before
-// copying it.  Each warp then reads its own address range upward, so the host rows any warp has in
-// flight lie in one or two of the device's translation pages; warps interleaved over the same
-// buckets, or rows in random order within a bucket, made the reads over a 72 GB pool 1.3-4x slower.
-constexpr int kSubRanges = 64;
-// Warp-level: dst[0..m) = src[0..m) ordered by sub-range of the host row (field x).  cnt: 64 ints of
-// shared memory owned by the warp.  Contains __syncwarp.
-__device__ __forceinline__ void sort_by_subrange(const int4* __restrict__ src, int m, int shift, int4* dst, int* cnt) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t low = shift > 0 ? (1u << shift) - 1u : 0u;
-  const int sub_shift = shift > 6 ? shift - 6 : 0;
-  cnt[lane] = 0;
-  cnt[lane + 32] = 0;
-  __syncwarp();
-  for (int e = lane; e < m; e += 32) atomicAdd(&cnt[(((uint32_t)__ldcg(&src[e].x) & low) >> sub_shift) & 63], 1);
-  __syncwarp();
-  const int a = cnt[2 * lane], b = cnt[2 * lane + 1];
-  int incl = a + b;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int x = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= d) incl += x;
-  }
-  const int excl = incl - a - b;
-  __syncwarp();
-  cnt[2 * lane] = excl;
-  cnt[2 * lane + 1] = excl + a;
-  __syncwarp();
-  for (int e = lane; e < m; e += 32) {
-    const int4 v = __ldcg(src + e);
-    dst[atomicAdd(&cnt[(((uint32_t)v.x & low) >> sub_shift) & 63], 1)] = v;
-  }
-  __syncwarp();
-}
 
 // Programmatic dependent launch.  A kernel that follows another of this library's kernels on the
 // same stream is launched with programmatic stream serialization: its CTAs may be placed as soon as

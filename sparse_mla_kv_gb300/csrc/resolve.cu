@@ -695,7 +695,6 @@ __global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const
 }
 
 constexpr int kCopyThreads = 256;
-constexpr int kCopySortChunk = 128;  // ordered layout: bucket entries one copy warp orders and copies at a time
 
 // Copies the rows of up to kMissRowsPerItem entries (lane j < nrows holds entry j) from the host pool
 // into their hot slots, in every layer [l0, l0 + group), all of a layer's 16-byte loads before its
@@ -774,40 +773,33 @@ __global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(const ResolvePa
     return;
   }
   if (p.ord.cnt) {
-    // ordered layout on large host pools: the group's warps take its buckets whole (warp w: buckets w,
-    // w + nwarps, ...), each chunk ordered by sub-range in the warp's shared memory, then the overflow
-    // entries
+    // ordered layout on large host pools (range schedule): the group's warps split its buckets into
+    // contiguous blocks (warp w: buckets [w * kMissBuckets / nwarps, (w + 1) * kMissBuckets / nwarps),
+    // numbered CTA-major so that neighbouring blocks run on different SMs), copy their entries as filed,
+    // then one slice of the overflow list each
     const int g = blockIdx.y;
-    const int wib = threadIdx.x >> 5;
-    // CTA-major numbering: consecutive buckets go to different CTAs (different SMs), so the warps
-    // that have work are spread over the whole grid
-    const int warp = wib * (int)gridDim.x + (int)blockIdx.x;
+    const int warp = (int)(threadIdx.x >> 5) * (int)gridDim.x + (int)blockIdx.x;
     const int nwarps = (int)(((int64_t)gridDim.x * blockDim.x) >> 5);
-    __shared__ int4 s_sorted[kCopyThreads / 32][kCopySortChunk];
-    __shared__ int s_sub[kCopyThreads / 32][kSubRanges];
-    if (threadIdx.x < 32) mi.load(p.ord, g);
-    __syncthreads();
     const int4* bk = p.ord.buckets + (int64_t)g * kMissBuckets * p.ord.cap;
-    const int4* ov = p.ord.overflow + (int64_t)g * p.ord.per_group;
+    const int32_t* cntg = p.ord.cnt + (int64_t)g * (kMissBuckets + 1);
     const int l0 = (p.layer_begin + g) * p.group;
     const int gpu_rows = p.num_gpu_blocks * p.S, host_rows = p.num_host_blocks * p.S;
-    for (int b = warp; b < kMissBuckets; b += nwarps) {
-      const int nb = mi.cnt[b];
-      for (int c0 = 0; c0 < nb; c0 += kCopySortChunk) {
-        const int m = min(kCopySortChunk, nb - c0);
-        sort_by_subrange(bk + (int64_t)b * p.ord.cap + c0, m, p.ord.shift, s_sorted[wib], s_sub[wib]);
-        for (int i = 0; i < m; i += kMissRowsPerItem) {
-          const int nrows = min(kMissRowsPerItem, m - i);
-          const int4 ent = lane < nrows ? s_sorted[wib][i + lane] : make_int4(0, 0, 0, 0);
-          copy_miss_rows<CPR>(ptrs, l0, p.group, ent, nrows, row_bytes, gpu_rows, host_rows);
-        }
-        __syncwarp();
+    const int b0 = (int)((int64_t)warp * kMissBuckets / nwarps), b1 = (int)((int64_t)(warp + 1) * kMissBuckets / nwarps);
+    for (int b = b0; b < b1; ++b) {
+      const int nb = min(__ldcg(cntg + b), p.ord.cap);
+      for (int i = 0; i < nb; i += kMissRowsPerItem) {
+        const int nrows = min(kMissRowsPerItem, nb - i);
+        const int4 ent = lane < nrows ? bk[(int64_t)b * p.ord.cap + i + lane] : make_int4(0, 0, 0, 0);
+        copy_miss_rows<CPR>(ptrs, l0, p.group, ent, nrows, row_bytes, gpu_rows, host_rows);
       }
     }
-    const int ov_items = (mi.overflow + kMissRowsPerItem - 1) / kMissRowsPerItem;
-    for (int i = warp; i < ov_items; i += nwarps) {
-      const int nrows = min(kMissRowsPerItem, mi.overflow - i * kMissRowsPerItem);
-      const int4 ent = lane < nrows ? ov[(int64_t)i * kMissRowsPerItem + lane] : make_int4(0, 0, 0, 0);
+    const int ovn = min(__ldcg(cntg + kMissBuckets), p.ord.per_group);
+    const int ov_per = (ovn + nwarps - 1) / nwarps;
+    const int o0 = warp * ov_per, o1 = min(ovn, o0 + ov_per);
+    const int4* ov = p.ord.overflow + (int64_t)g * p.ord.per_group;
+    for (int i = o0; i < o1; i += kMissRowsPerItem) {
+      const int nrows = min(kMissRowsPerItem, o1 - i);
+      const int4 ent = lane < nrows ? ov[i + lane] : make_int4(0, 0, 0, 0);
       copy_miss_rows<CPR>(ptrs, l0, p.group, ent, nrows, row_bytes, gpu_rows, host_rows);
     }
     return;
@@ -1028,7 +1020,11 @@ cudaError_t launch_miss_copy(const ResolveParams& p, const LayerPtrs& ptrs, int3
   // one warp per item at most, capped at a full resident grid (split over the index groups when
   // the ordered layout gives each group its own CTAs)
   int64_t blocks = (items + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
-  const int64_t cap = p.ord.cnt ? ((int64_t)sms * 8 + p.nl - 1) / p.nl : (int64_t)sms * 8;
+  // the range schedule: two CTAs per SM over all index groups (about 2,400 warps, each owning a block of
+  // buckets, spread over every SM); the others up to eight CTAs per SM
+  const int64_t cap = p.ord.cnt ? (p.ord.ranges ? ((int64_t)sms * 2 + p.nl - 1) / p.nl
+                                                : ((int64_t)sms * 8 + p.nl - 1) / p.nl)
+                                : (int64_t)sms * 8;
   if (p.ord.cnt) blocks = (blocks + p.nl - 1) / p.nl;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;

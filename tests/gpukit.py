@@ -18,15 +18,15 @@ class Rig:
                  mode: str = "split", graph: bool = False):
         # "split" / "fused": the library's default miss layout for the pool (ordered only for large host
         # pools); a "+order" suffix forces the address-ordered layout on any pool, "+ranges" its range
-        # schedule (whole host ranges per copy warp), "+ranges2" the same with two miss warps per
-        # fused-gather CTA
+        # schedule (a contiguous block of host ranges per copy warp) with one miss warp per fused-gather
+        # CTA, "+ranges2" with two
         base, _, opt = mode.partition("+")
         assert base in ("split", "fused") and opt in ("", "order", "ranges", "ranges2")
         self.mode = base
         self.force_order = opt != ""
         self.order_mode = {"order": hs.MISS_ORDER_ON, "ranges": hs.MISS_ORDER_RANGES,
                            "ranges2": hs.MISS_ORDER_RANGES}.get(opt)
-        self.miss_warps = 2 if opt == "ranges2" else 0
+        self.miss_warps = 2 if opt == "ranges2" else 1
         self.graph = graph
         self.prep = None
         self.w = w

@@ -126,7 +126,7 @@ def _to_gpu(case, dev, mode):
         pool.set_miss_order(hs.MISS_ORDER_ON)
     elif opt:
         pool.set_miss_order(hs.MISS_ORDER_RANGES)
-        pool.set_miss_warps(2 if opt == "ranges2" else 0)
+        pool.set_miss_warps(2 if opt == "ranges2" else 1)
     hot = hs.HotState.allocate(1, torch.from_numpy(case.hot_blocks).to(dev), case.C)
     hot.slot_token.copy_(torch.from_numpy(case.tok))
     hot.slot_stamp.copy_(torch.from_numpy(case.stamp))

@@ -42,14 +42,14 @@ def _base(mode):
 
 def _set_order(pool, mode):
     """+order: the address-ordered miss layout on any pool (its spread schedule on small pools);
-    +ranges: its range schedule (whole host ranges per copy warp); +ranges2: with two miss warps per
-    fused-gather CTA."""
+    +ranges: its range schedule (a contiguous block of host ranges per copy warp) with one miss warp per
+    fused-gather CTA; +ranges2: with two."""
     opt = mode.partition("+")[2]
     if opt == "order":
         pool.set_miss_order(hs.MISS_ORDER_ON)
     elif opt in ("ranges", "ranges2"):
         pool.set_miss_order(hs.MISS_ORDER_RANGES)
-        pool.set_miss_warps(2 if opt == "ranges2" else 0)
+        pool.set_miss_warps(2 if opt == "ranges2" else 1)
 
 
 @pytest.mark.parametrize("mode", MODES_ORDER)
