@@ -102,7 +102,11 @@ def parse():
                     help="link probe: register the host pool without huge pages (for comparison)")
     ap.add_argument("--probe-cpu-fill", action="store_true",
                     help="link probe: write the host pool with CPU stores instead of DMA (for comparison)")
-    ap.add_argument("--miss-order", choices=["auto", "on", "off", "ranges"], default="auto",
+    ap.add_argument("--schedule-ab", type=int, default=0, metavar="ROUNDS",
+                    help="after the timed passes, ROUNDS rounds of two more timed passes over the same steps, one "
+                         "with the range schedule and one with the spread schedule of the ordered miss layout "
+                         "(hs_pool_set_miss_order), in this process")
+    ap.add_argument("--miss-order", choices=["auto", "on", "off", "ranges", "spread"], default="auto",
                     help="miss layout handed to the copy warps: auto (the library's default: host-address order "
                          "for host pools of 16 GiB or more), on (always address order), off (per-unit lists), "
                          "ranges (address order with the range schedule on any pool)")
@@ -468,14 +472,19 @@ def run_ours(args, ws, rank, local):
         sdev.fill_gpu_pool(w, l, gpu[l])
         sdev.fill_host_pool(w, l, host[l], dev)
     pool = hs.Pool(gpu, host)
-    pool.set_miss_order({"auto": hs.MISS_ORDER_AUTO, "on": hs.MISS_ORDER_ON, "off": hs.MISS_ORDER_OFF,
-                         "ranges": hs.MISS_ORDER_RANGES}[args.miss_order])
+    order_modes = {"auto": hs.MISS_ORDER_AUTO, "on": hs.MISS_ORDER_ON, "off": hs.MISS_ORDER_OFF,
+                   "ranges": hs.MISS_ORDER_RANGES, "spread": hs.MISS_ORDER_SPREAD}
+    pool.set_miss_order(order_modes[args.miss_order])
     pool.set_miss_warps(args.miss_warps)
     from sparse_mla_kv_gb300.hostmem import huge_page_fraction
     huge_frac = [round(huge_page_fraction(h), 4) for h in host]
     tb = Tables(w, steps)
     bt = torch.from_numpy(tb.bt).to(dev)
     hbt = torch.from_numpy(tb.hbt).to(dev)
+    # pinned staging for the tables' per-step uploads (a copy from pageable memory can go through the
+    # device's translation of host memory, which the step's zero-copy misses depend on)
+    bt_stage = torch.empty(tuple(bt.shape), dtype=torch.int32, pin_memory=True)
+    hbt_stage = torch.empty(tuple(hbt.shape), dtype=torch.int32, pin_memory=True)
     ctx = torch.from_numpy(w.ctx_len.astype(np.int32)).to(dev)
     hot = hs.HotState.allocate(L, torch.from_numpy(w.hot_blocks).to(dev), C, layers_per_index=G)
     hs.hot_reset(pool, hot)
@@ -492,7 +501,8 @@ def run_ours(args, ws, rank, local):
     host_total = L * max(1, w.num_host_blocks) * S * B
     miss_order = ("per-unit lists" if not hs.miss_order_used(pool, hot, L, R, P, Kk, ws_buf.numel())
                   else "host-address buckets, " + ("range schedule" if args.miss_order == "ranges" or
-                                                   host_total >= (40 << 30) else "spread schedule"))
+                                                   (host_total >= (40 << 30) and args.miss_order != "spread")
+                                                   else "spread schedule"))
     gout = torch.empty((L, R * P * Kk, B), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -539,8 +549,11 @@ def run_ours(args, ws, rank, local):
     def restore():
         """Back to the state before the first step: tables, contexts and empty hot buffers."""
         tb.restore()
-        bt.copy_(torch.from_numpy(tb.bt))
-        hbt.copy_(torch.from_numpy(tb.hbt))
+        torch.cuda.current_stream().synchronize()
+        np.copyto(bt_stage.numpy(), tb.bt)
+        np.copyto(hbt_stage.numpy(), tb.hbt)
+        bt.copy_(bt_stage, non_blocking=True)
+        hbt.copy_(hbt_stage, non_blocking=True)
         hs.hot_reset(pool, hot)
 
     def before(i, upload_tables=True):
@@ -550,8 +563,11 @@ def run_ours(args, ws, rank, local):
         st = steps[i]
         changed = tb.edit(i)
         if changed and upload_tables:
-            bt.copy_(torch.from_numpy(tb.bt))
-            hbt.copy_(torch.from_numpy(tb.hbt))
+            torch.cuda.current_stream().synchronize()   # the staging buffers' previous upload has landed
+            np.copyto(bt_stage.numpy(), tb.bt)
+            np.copyto(hbt_stage.numpy(), tb.hbt)
+            bt.copy_(bt_stage, non_blocking=True)
+            hbt.copy_(hbt_stage, non_blocking=True)
         if len(st.fills):
             blocks = st.fills[:, 0].astype(np.int64)
             owners = st.fills[:, 1:].astype(np.int64)
@@ -717,6 +733,26 @@ def run_ours(args, ws, rank, local):
                  "timing": "each timed step captured as one CUDA graph, replayed once behind an L2 flush; "
                            "events around the replay"}
         del graphs
+    schedule_ab = None
+    if args.schedule_ab and hs.miss_order_used(pool, hot, L, R, P, Kk, ws_buf.numel()):
+        # whole timed passes over the same steps, alternating the two schedules of the ordered layout (each
+        # pass plans and gathers in one mode), so both see the same machine state
+        sums = {"ranges": [], "spread": []}
+        steps_med = {"ranges": [], "spread": []}
+        for rnd in range(args.schedule_ab):
+            for name, mode in (("ranges", hs.MISS_ORDER_RANGES), ("spread", hs.MISS_ORDER_SPREAD)):
+                pool.set_miss_order(mode)
+                replay_warmup()
+                ev_ab = timed_pass(split=False)
+                ts = [ev_ab[k][0].elapsed_time(ev_ab[k][2]) * 1e-3 for k in range(K)]
+                sums[name].append(1e3 * sum(ts) / K)
+                steps_med[name].append(1e6 * statistics.median(ts))
+        pool.set_miss_order(order_modes[args.miss_order])
+        schedule_ab = {"rounds": args.schedule_ab,
+                       "ms_per_step": {k: [round(x, 3) for x in v] for k, v in sums.items()},
+                       "step_us_median": {k: [round(x, 1) for x in v] for k, v in steps_med.items()},
+                       "how": "per round, one timed pass (the K timed steps after the warm-up replay) with each "
+                              "schedule of the ordered miss layout; mean step time of each pass"}
     miss_warps_ab = None
     if args.miss_warps_ab and fused:
         # the last timed step's plan stays in the workspace: replaying hs_gather_planned rewrites the same
@@ -946,6 +982,7 @@ def run_ours(args, ws, rank, local):
             "gathered_gbs": value * B / 1e9, "roofline": roofline, "step_roofline": step_roof,
             "cpu_baseline": cpu, "cpu_baseline_1thread": cpu1, "e2e": e2e, "gpu_launches": int(launches),
             "graph_replay": graph, "gather_copy_ab": gather_ab, "miss_warps_ab": miss_warps_ab,
+            "schedule_ab": schedule_ab,
             "clocks": clocks,
             "wall_s_timed_region": wall, "timed_counts": {"resident": int(hits_misses[0]),
                                                           "hits": int(hits_misses[1]),

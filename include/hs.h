@@ -149,12 +149,14 @@ size_t hs_resolve_workspace_bytes_min(int32_t nl, int32_t R, int32_t P, int32_t 
  *                                 least 16 GiB together and the workspace has room for it;
  *   HS_MISS_ORDER_OFF             per-unit lists, copied unit by unit;
  *   HS_MISS_ORDER_ON              address-ordered whenever the workspace has room for it;
- *   HS_MISS_ORDER_RANGES          address-ordered with the range schedule (below) whatever the pool size.
+ *   HS_MISS_ORDER_RANGES          address-ordered with the range schedule (below) whatever the pool size;
+ *   HS_MISS_ORDER_SPREAD          address-ordered with the spread schedule (below) whatever the pool size.
  * Address-ordered: the resolver files each index group's misses into 1024 buckets by host row range.
  * The copy warps then take them in one of two schedules: on host pools under 40 GiB (over the call's
  * layers) the 4-entry items of all buckets in bucket order, spread over every copy warp; from 40 GiB
- * on (or with HS_MISS_ORDER_RANGES) one contiguous block of buckets per warp, so that every warp reads
- * its own range of the pool.  The pages copy single rows from pinned host memory
+ * on (or with HS_MISS_ORDER_RANGES; HS_MISS_ORDER_SPREAD keeps the spread schedule on any pool) one
+ * contiguous block of buckets per warp, so that every warp reads its own range of the pool.  The pages
+ * copy single rows from pinned host memory
  * ("vLLM GLM 5.3 Optimizations: Hybrid HiSparse Offloading", "Technical Implementation of Hybrid
  * HiSparse") and say nothing of their order; this is the library's choice.  Zero-copy reads spread
  * over tens of GB of host memory are bound by the device's address translation for host memory, not
@@ -167,6 +169,7 @@ size_t hs_resolve_workspace_bytes_min(int32_t nl, int32_t R, int32_t P, int32_t 
 #define HS_MISS_ORDER_OFF 1
 #define HS_MISS_ORDER_ON 2
 #define HS_MISS_ORDER_RANGES 3
+#define HS_MISS_ORDER_SPREAD 4
 hs_status hs_pool_set_miss_order(hs_pool* pool, int32_t mode);
 
 /* How hs_gather_rows moves its HBM rows.  Results are identical in both modes; only the speed

@@ -25,7 +25,7 @@ LIB_VARIANT = os.environ.get("HS_LIB_VARIANT", "")
 LIB_PATH = os.path.join(_HERE, f"libhs_{LIB_VARIANT}.so" if LIB_VARIANT else "libhs.so")
 
 HS_OK = 0
-MISS_ORDER_AUTO, MISS_ORDER_OFF, MISS_ORDER_ON, MISS_ORDER_RANGES = 0, 1, 2, 3
+MISS_ORDER_AUTO, MISS_ORDER_OFF, MISS_ORDER_ON, MISS_ORDER_RANGES, MISS_ORDER_SPREAD = 0, 1, 2, 3, 4
 GATHER_COPY_LOADS, GATHER_COPY_BULK = 0, 1
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "ID_RANGE", 3: "MISSING_ROW", 4: "CAPACITY", 5: "STEP_ORDER",
                 6: "CUDA", 7: "TIMEOUT", 8: "TABLE_RANGE"}
@@ -187,8 +187,8 @@ class Pool:
         self.handle = h
 
     def set_miss_order(self, mode: int) -> None:
-        """MISS_ORDER_AUTO (default), MISS_ORDER_OFF, MISS_ORDER_ON or MISS_ORDER_RANGES: see
-        hs_pool_set_miss_order."""
+        """MISS_ORDER_AUTO (default), MISS_ORDER_OFF, MISS_ORDER_ON, MISS_ORDER_RANGES or MISS_ORDER_SPREAD:
+        see hs_pool_set_miss_order."""
         _check(lib().hs_pool_set_miss_order(self.handle, int(mode)), "hs_pool_set_miss_order")
 
     def set_gather_copy(self, mode: int) -> None:

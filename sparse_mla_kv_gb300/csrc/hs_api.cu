@@ -61,7 +61,8 @@ MissOrder call_miss_order(const hs_pool* pool, int32_t nl, int64_t ng, int32_t R
   if (!use_miss_order(pool, nl, ng, R, n, C, workspace_bytes)) return MissOrder{};
   MissOrder o = miss_order_layout(workspace, ng, R, n, C, (int64_t)pool->g.num_host_blocks * pool->g.page_size);
   const PoolGeom& g = pool->g;
-  o.ranges = (pool->miss_order == HS_MISS_ORDER_RANGES ||
+  o.ranges = pool->miss_order == HS_MISS_ORDER_RANGES ||
+             (pool->miss_order != HS_MISS_ORDER_SPREAD &&
               (int64_t)g.num_host_blocks * g.page_size * g.row_bytes * nl >= kMissRangesBytes) ? 1 : 0;
   return o;
 }
@@ -168,7 +169,7 @@ hs_status hs_pool_create(const hs_pool_desc* d, hs_pool** out) {
 void hs_pool_destroy(hs_pool* p) { delete p; }
 
 hs_status hs_pool_set_miss_order(hs_pool* pool, int32_t mode) {
-  if (!pool || mode < HS_MISS_ORDER_AUTO || mode > HS_MISS_ORDER_RANGES) return HS_ERR_INVALID_ARG;
+  if (!pool || mode < HS_MISS_ORDER_AUTO || mode > HS_MISS_ORDER_SPREAD) return HS_ERR_INVALID_ARG;
   pool->miss_order = mode;
   return HS_OK;
 }

@@ -477,13 +477,14 @@ def test_miss_order_decision():
     assert hs.miss_order_used(pool, hot, 2, R, P, K, full)
     assert hs.miss_order_used(pool, hot, 1, R, P, K, full, layer_begin=1)
     assert not hs.miss_order_used(pool, hot, 2, R, P, K, small)
-    pool.set_miss_order(hs.MISS_ORDER_RANGES)
-    assert hs.miss_order_used(pool, hot, 2, R, P, K, full)
-    assert not hs.miss_order_used(pool, hot, 2, R, P, K, small)
+    for mode in (hs.MISS_ORDER_RANGES, hs.MISS_ORDER_SPREAD):
+        pool.set_miss_order(mode)
+        assert hs.miss_order_used(pool, hot, 2, R, P, K, full)
+        assert not hs.miss_order_used(pool, hot, 2, R, P, K, small)
     pool.set_miss_order(hs.MISS_ORDER_OFF)
     assert not hs.miss_order_used(pool, hot, 2, R, P, K, full)
     with pytest.raises(hs.HSError):
-        pool.set_miss_order(7)
+        pool.set_miss_order(5)
     with pytest.raises(hs.HSError):
         pool.set_miss_warps(3)
     no_host = hs.Pool(gpu)
