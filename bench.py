@@ -89,9 +89,11 @@ def parse():
                          "alternating, in this process")
     ap.add_argument("--miss-warps-ab", action="store_true",
                     help="after the timed passes, replay the last timed step's planned gather (hs_gather_planned) "
-                         "with 1 and 2 miss warps per CTA (hs_pool_set_miss_warps), alternating, in this process")
+                         "with the SM partition and with 1 and 2 miss warps in every CTA (hs_pool_set_miss_warps), "
+                         "alternating, in this process")
     ap.add_argument("--miss-warps", type=int, default=0, choices=[0, 1, 2],
-                    help="miss warps per fused-gather CTA under the range schedule (0: the library's default)")
+                    help="fused gather under the range schedule: 0 = SM partition (the library's default), 1 or 2 = "
+                         "that many miss warps in every CTA")
     ap.add_argument("--link-probe", action="store_true",
                     help="measure the miss path's host-link rate against the span of host memory it reads "
                          "(one layer, all-miss steps) instead of a workload")
@@ -758,9 +760,9 @@ def run_ours(args, ws, rank, local):
         # the last timed step's plan stays in the workspace: replaying hs_gather_planned rewrites the same
         # bytes (hot slots and outputs), so each replay is the same gather with another miss-warp count
         reps = max(5, K)
-        t_mw = {1: [], 2: []}
+        t_mw = {0: [], 1: [], 2: []}
         for rep in range(reps + 1):
-            for mwc in (1, 2):
+            for mwc in (0, 1, 2):
                 pool.set_miss_warps(mwc)
                 flush.fill_(rep & 0xFF)
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -772,10 +774,12 @@ def run_ours(args, ws, rank, local):
                     t_mw[mwc].append(e0.elapsed_time(e1) * 1e-3)
         pool.set_miss_warps(args.miss_warps)
         miss_warps_ab = {"repeats": reps, "miss_order": miss_order,
+                         "gather_us_median_partition": 1e6 * statistics.median(t_mw[0]),
                          "gather_us_median_1": 1e6 * statistics.median(t_mw[1]),
                          "gather_us_median_2": 1e6 * statistics.median(t_mw[2]),
-                         "how": "hs_gather_planned of the last timed step replayed with 1 and 2 miss warps per CTA "
-                                "(hs_pool_set_miss_warps), alternating behind L2 flushes; medians"}
+                         "how": "hs_gather_planned of the last timed step replayed with the SM partition and with 1 "
+                                "and 2 miss warps in every CTA (hs_pool_set_miss_warps 0, 1, 2), alternating behind "
+                                "L2 flushes; medians"}
     gather_ab = None
     if args.gather_ab:
         # the plain gather of the last timed step's rows, every layer of each index group reading its

@@ -188,11 +188,13 @@ hs_status hs_pool_set_miss_order(hs_pool* pool, int32_t mode);
 #define HS_GATHER_COPY_BULK 1
 hs_status hs_pool_set_gather_copy(hs_pool* pool, int32_t mode);
 
-/* Miss warps per CTA of the fused gather (hs_gather_planned, hs_resolve_gather) when the address-
- * ordered miss layout takes its range schedule (host pools of 40 GiB or more over the call's layers:
- * each copy warp reads its own range of host rows): 1 or 2, or 0 for the library's default (1).  More warps
- * read more ranges at once and leave fewer warps per CTA for the HBM rows.  Results are identical.
- * Other layouts always use one miss warp per CTA.  HS_ERR_INVALID_ARG for another count. */
+/* How the fused gather (hs_gather_planned, hs_resolve_gather) places its miss copies when the
+ * address-ordered miss layout takes its range schedule (host pools of 40 GiB or more over the call's
+ * layers).  0 (the default): SM partition -- the CTAs on one SM in eight copy misses, a bucket of host
+ * rows per warp at a time, and the others stream the HBM rows; whichever finishes first takes the other
+ * kind of work.  1 or 2: that many miss warps in every CTA, each reading a contiguous block of buckets,
+ * beside the HBM warps.  Results are identical.  Other layouts always use one miss warp per CTA.
+ * HS_ERR_INVALID_ARG for another value. */
 hs_status hs_pool_set_miss_warps(hs_pool* pool, int32_t warps);
 
 /* 1 if a resolve call on layers [layer_begin, layer_begin + nl) with this shape, hot state and

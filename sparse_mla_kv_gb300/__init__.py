@@ -196,8 +196,8 @@ class Pool:
         _check(lib().hs_pool_set_gather_copy(self.handle, int(mode)), "hs_pool_set_gather_copy")
 
     def set_miss_warps(self, warps: int) -> None:
-        """Miss warps per fused-gather CTA under the range schedule (0 = default, 1, 2): see
-        hs_pool_set_miss_warps."""
+        """Fused gather under the range schedule: 0 = SM partition (default), 1 or 2 = that many miss warps
+        in every CTA; see hs_pool_set_miss_warps."""
         _check(lib().hs_pool_set_miss_warps(self.handle, int(warps)), "hs_pool_set_miss_warps")
 
     def close(self) -> None:

@@ -30,9 +30,9 @@ HS_CHECK_WORD
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kGatherThreads = 256;
 constexpr int kGatherUnroll = 8;
-// Miss warps per CTA of the fused gather: one keeps the host link busy on small pools (two were slower
-// on the mixed batch); with the range schedule of large pools the pool may ask for two
-// (hs_pool_set_miss_warps), so that more host ranges are read at once.
+// Miss warps per CTA of the fused gather when every CTA carries misses: one keeps the host link busy on
+// small pools (two were slower on the mixed batch); with the range schedule of large pools the pool may
+// ask for two (hs_pool_set_miss_warps) instead of the SM partition.
 constexpr int kMaxMissWarps = 2;
 
 template <int CPR>
@@ -318,6 +318,133 @@ __device__ __noinline__ void miss_warp_ranges(const MissOrder ord, int pu, int m
   }
 }
 
+// ---- range schedule, SM partition (the default on large host pools).  Host reads and HBM rows slow
+// each other down when warps of both kinds share an SM: measured on the full-size MTP3 pattern (4 x 18 GB
+// host pools, 378K misses, 8.4M HBM rows) with a standalone kernel, a miss warp in every CTA took 3.3-3.4
+// ms, the misses alone 2.1 ms and the HBM rows alone 1.9 ms, while giving every eighth SM to the misses
+// and the others to the HBM rows took 2.45 ms.  So the CTAs on every kMissSmDivisor-th SM (by %smid)
+// copy misses with all their warps and the others stream HBM rows; work comes from three counters shared
+// by every layer of the launch (miss buckets, overflow slices, HBM chunks), and a CTA that has drained
+// its own kind of work takes the other kind, so every unit is done whichever SMs the CTAs land on.
+constexpr int kMissSmDivisor = 8;
+constexpr int kStripes = 64;         // miss buckets are handed out across 64 stripes of the pool at once
+constexpr int kOvUnit = 64;          // overflow entries per work unit
+constexpr int kHbmChunk = 8192;      // 16-byte output chunks per HBM work unit (128 KB)
+
+__device__ __forceinline__ unsigned sm_id() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+
+// Miss work units of one launch: for each of its nl layers, kMissBuckets bucket units and as many
+// overflow slices of kOvUnit entries as the fullest group's overflow list needs.  Unit u belongs to
+// layer u % nl; i = u / nl < kMissBuckets is a bucket (taken in stripe order, so the warps working at
+// one time read kStripes ranges spread over the pool), i >= kMissBuckets an overflow slice.
+__device__ __forceinline__ int partition_miss_units(const MissOrder& ord, int nl, int group) {
+  int ov_units = 0;
+  for (int pu = 0; pu * group < nl; ++pu) {
+    const int ovn = min(__ldcg(ord.cnt + (int64_t)pu * (kMissBuckets + 1) + kMissBuckets), ord.per_group);
+    ov_units = max(ov_units, (ovn + kOvUnit - 1) / kOvUnit);
+  }
+  return nl * (kMissBuckets + ov_units);
+}
+
+// One warp copies the entries of miss unit i (bucket or overflow slice) of group pu.
+template <int CPR>
+__device__ __forceinline__ void partition_miss_unit(const MissOrder ord, int i, int pu,
+                                                 const uint8_t* __restrict__ host, uint8_t* __restrict__ pool,
+                                                 uint8_t* __restrict__ lout, const int32_t* __restrict__ lmsrc, int n,
+                                                 int row_bytes, int64_t per_layer, int64_t num_rows,
+                                                 int64_t num_host_rows) {
+  const int lane = threadIdx.x & 31;
+  const int32_t* cntg = ord.cnt + (int64_t)pu * (kMissBuckets + 1);
+  const int4* src;
+  int nb;
+  if (i < kMissBuckets) {
+    const int b = (i % kStripes) * (kMissBuckets / kStripes) + i / kStripes;
+    nb = min(__ldcg(cntg + b), ord.cap);
+    src = ord.buckets + ((int64_t)pu * kMissBuckets + b) * ord.cap;
+  } else {
+    const int o0 = (i - kMissBuckets) * kOvUnit;
+    nb = max(0, min(kOvUnit, min(__ldcg(cntg + kMissBuckets), ord.per_group) - o0));
+    src = ord.overflow + (int64_t)pu * ord.per_group + o0;
+  }
+  for (int j = 0; j < nb; j += kMissRowsPerItem) {
+    const int nrows = min(kMissRowsPerItem, nb - j);
+    const int4 ent = lane < nrows ? src[j + lane] : make_int4(0, 0, 0, 0);
+    copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
+  }
+}
+
+// The whole CTA: HBM chunks until the queue is empty.  Chunk unit c covers 16-byte output chunks
+// [(c / nl) * kHbmChunk, ...) of layer c % nl; every position the miss warps do not own is written.
+template <int CPR>
+__device__ __forceinline__ void partition_hbm(const LayerPtrs& ptrs, int32_t layer_begin, int32_t group, int nl,
+                                              const MissOrder& ord, const int32_t* __restrict__ msrc,
+                                              uint8_t* __restrict__ out, int64_t per_layer, int row_bytes,
+                                              int64_t num_rows) {
+  const int cpr = CPR ? CPR : (row_bytes >> 4);
+  const int64_t total = per_layer * cpr;  // 16-byte chunks per layer
+  const int64_t units = (total + kHbmChunk - 1) / kHbmChunk * nl;
+  __shared__ int64_t s_unit;
+  for (;;) {
+    __syncthreads();  // every thread has read the previous unit
+    if (threadIdx.x == 0) s_unit = (int64_t)atomicAdd(reinterpret_cast<unsigned int*>(ord.queues + 2), 1u);
+    __syncthreads();
+    const int64_t c = s_unit;
+    if (c >= units) break;
+    const int l = (int)(c % nl);
+    const int64_t c0 = (c / nl) * kHbmChunk, c1 = min(total, c0 + kHbmChunk);
+    const uint8_t* __restrict__ pool = ptrs.gpu[layer_begin + l];
+    uint4* __restrict__ lout4 = reinterpret_cast<uint4*>(out + (int64_t)l * per_layer * row_bytes);
+    const int32_t* __restrict__ lmsrc = msrc + (int64_t)(l / group) * per_layer;
+    for (int64_t cb = c0 + threadIdx.x; cb < c1; cb += (int64_t)kGatherThreads * kGatherUnroll) {
+      uint4 v[kGatherUnroll];
+      bool st[kGatherUnroll];
+#pragma unroll
+      for (int k = 0; k < kGatherUnroll; ++k) {
+        const int64_t cc = cb + (int64_t)k * kGatherThreads;
+        v[k] = make_uint4(0u, 0u, 0u, 0u);
+        st[k] = false;
+        if (cc < c1) {
+          const int64_t i = cc / cpr;
+          const int j = (int)(cc - i * cpr);
+          const int ms = __ldg(lmsrc + i);
+          if (ms >= 0) {
+            if (ms < num_rows) v[k] = __ldg(reinterpret_cast<const uint4*>(pool + (int64_t)ms * row_bytes) + j);
+            st[k] = true;
+          } else if (ms == -1) {
+            st[k] = true;
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kGatherUnroll; ++k)
+        if (st[k]) lout4[cb + (int64_t)k * kGatherThreads] = v[k];
+    }
+  }
+}
+
+// A warp's share of the miss units: it takes units until the counter passes the end.
+template <int CPR>
+__device__ __forceinline__ void partition_misses(const LayerPtrs& ptrs, int32_t layer_begin, int32_t group, int nl,
+                                                 const MissOrder& ord, const int32_t* __restrict__ msrc,
+                                                 uint8_t* __restrict__ out, int n, int64_t per_layer, int row_bytes,
+                                                 int64_t num_rows, int64_t num_host_rows) {
+  const int units = partition_miss_units(ord, nl, group);
+  for (;;) {
+    int u = 0;
+    if ((threadIdx.x & 31) == 0) u = atomicAdd(ord.queues, 1);
+    u = __shfl_sync(kFull, u, 0);
+    if (u >= units) break;
+    const int l = u % nl, pu = l / group;
+    partition_miss_unit<CPR>(ord, u / nl, pu, ptrs.host[layer_begin + l], ptrs.gpu[layer_begin + l],
+                             out + (int64_t)l * per_layer * row_bytes, msrc + (int64_t)pu * per_layer, n, row_bytes,
+                             per_layer, num_rows, num_host_rows);
+  }
+}
+
 // Spread schedule (ordered layout on smaller host pools): the layer's miss warps take its group's
 // 4-entry items in bucket order (warp w: items w, w + nmw, ...), so that all copy warps work on
 // neighbouring host ranges at once and every warp has an item in flight.
@@ -378,6 +505,26 @@ __device__ __noinline__ void miss_warp_lists(const int32_t* __restrict__ miss_co
       copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
     }
   }
+}
+
+// The fused gather with the range schedule's SM partition (see partition_misses): the same outputs as
+// gather_fused_kernel, in a kernel of its own so that neither layout's registers constrain the other's.
+template <int CPR>
+__global__ void __launch_bounds__(kGatherThreads, 4) gather_partition_kernel(
+    const LayerPtrs ptrs, int32_t layer_begin, int32_t group, int32_t R, int32_t n, const MissOrder ord,
+    const int32_t* __restrict__ msrc, uint8_t* __restrict__ out, int32_t row_bytes, int64_t num_rows,
+    int64_t num_host_rows) {
+  const int nl = gridDim.y;
+  const int64_t per_layer = (int64_t)R * n;
+  // CTAs on a miss SM copy misses first, then help with the HBM rows; the others the other way round
+  const bool miss_sm = sm_id() % kMissSmDivisor == 0;
+  if (miss_sm)
+    partition_misses<CPR>(ptrs, layer_begin, group, nl, ord, msrc, out, n, per_layer, row_bytes, num_rows,
+                          num_host_rows);
+  partition_hbm<CPR>(ptrs, layer_begin, group, nl, ord, msrc, out, per_layer, row_bytes, num_rows);
+  if (!miss_sm)
+    partition_misses<CPR>(ptrs, layer_begin, group, nl, ord, msrc, out, n, per_layer, row_bytes, num_rows,
+                          num_host_rows);
 }
 
 template <int CPR>
@@ -449,6 +596,7 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
 
 int g_occ_plain[2] = {0, 0};
 int g_occ_fused[2] = {0, 0};
+int g_occ_partition[2] = {0, 0};
 int g_occ_bulk = 0;          // resident bulk-gather CTAs per SM for the 656-byte rows' footprint
 size_t g_bulk_smem_max = 0;  // dynamic shared memory the bulk gather may use (the opt-in maximum)
 
@@ -492,6 +640,8 @@ void warm_gather_launch_configs() {
   resident_blocks(gather_kernel<0>, &g_occ_plain[1]);
   resident_blocks(gather_fused_kernel<41>, &g_occ_fused[0]);
   resident_blocks(gather_fused_kernel<0>, &g_occ_fused[1]);
+  resident_blocks(gather_partition_kernel<41>, &g_occ_partition[0]);
+  resident_blocks(gather_partition_kernel<0>, &g_occ_partition[1]);
   if (g_bulk_smem_max == 0) {
     int dev = 0, optin = 0;
     if (cudaGetDevice(&dev) == cudaSuccess &&
@@ -541,21 +691,33 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
   int* occ = g_occ_fused;
   const bool k41 = row_bytes == 656;
   auto kern = k41 ? gather_fused_kernel<41> : gather_fused_kernel<0>;
-  // miss warps per CTA: the pool's choice for the range schedule, one otherwise
-  const int nmiss = (ord.cnt && ord.ranges) ? (range_miss_warps >= kMaxMissWarps ? kMaxMissWarps : 1) : 1;
+  // range schedule: 0 = SM partition, else that many miss warps in every CTA; one otherwise
+  const int nmiss = (ord.cnt && ord.ranges)
+                        ? (range_miss_warps <= 0 ? 0 : (range_miss_warps >= kMaxMissWarps ? kMaxMissWarps : 1))
+                        : 1;
   const int64_t per_layer = (int64_t)R * n * (row_bytes >> 4);
   const int64_t want_hbm = (per_layer + (int64_t)kGatherThreads * kGatherUnroll - 1) /
                            ((int64_t)kGatherThreads * kGatherUnroll);
   // enough CTAs that each miss warp can take one item (kMissRowsPerItem misses) of the most a layer can
   // have, so a small batch does not queue its host round trips on a few warps
-  const int64_t want_miss = ((int64_t)R * ((max_m + kMissRowsPerItem - 1) / kMissRowsPerItem) + nmiss - 1) / nmiss;
+  const int64_t want_miss =
+      ((int64_t)R * ((max_m + kMissRowsPerItem - 1) / kMissRowsPerItem) + nmiss - 1) / (nmiss > 0 ? nmiss : 1);
   const dim3 grid = wave_grid(sms, resident_blocks(kern, &occ[k41 ? 0 : 1]), want_hbm > want_miss ? want_hbm : want_miss,
                               nl);
   // With the ordered layout (large host pools) the gather is not launched early: CTAs placed while
   // the resolver still runs made the whole gather's host reads slower there (measured: agentic
   // decode over a 29 GB pool, 684 us per step against 333 us with the launch held back).
   cudaError_t e;
-  if (ord.cnt) {
+  if (nmiss == 0) {
+    // SM partition: one full wave; its work counters start at zero in every launch
+    auto pkern = k41 ? gather_partition_kernel<41> : gather_partition_kernel<0>;
+    const dim3 pgrid = wave_grid(sms, resident_blocks(pkern, &g_occ_partition[k41 ? 0 : 1]), (int64_t)1 << 40, nl);
+    e = cudaMemsetAsync(ord.queues, 0, kQueueInts * sizeof(int32_t), s);
+    if (e != cudaSuccess) return e;
+    pkern<<<pgrid, kGatherThreads, 0, s>>>(ptrs, layer_begin, group, R, n, ord, msrc, out, row_bytes, num_rows,
+                                           num_host_rows);
+    e = cudaGetLastError();
+  } else if (ord.cnt) {
     kern<<<grid, kGatherThreads, 0, s>>>(ptrs, layer_begin, group, R, n, max_m, rows, miss_count, miss_list, ord, msrc,
                                          out, row_bytes, num_rows, num_host_rows, nmiss);
     e = cudaGetLastError();

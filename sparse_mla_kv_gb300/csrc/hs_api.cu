@@ -13,7 +13,7 @@ struct hs_pool {
   int device;
   int32_t miss_order;   // HS_MISS_ORDER_*
   int32_t gather_copy;  // HS_GATHER_COPY_*
-  int32_t miss_warps;   // fused gather, range schedule: miss warps per CTA (0 = the library's default)
+  int32_t miss_warps;   // fused gather, range schedule: 0 = SM partition, 1 or 2 = miss warps in every CTA
 };
 
 namespace hs {
@@ -387,7 +387,7 @@ hs_status hs_gather_planned(const hs_pool* pool, int32_t layer_begin, int32_t nl
       reinterpret_cast<const int4*>(ws + hs::ws_counts_bytes(units)), ord,
       reinterpret_cast<const int32_t*>(ws + hs::ws_msrc_offset(units, n, capacity)), static_cast<uint8_t*>(out),
       g.row_bytes, (int64_t)g.num_gpu_blocks * g.page_size, (int64_t)g.num_host_blocks * g.page_size,
-      pool->miss_warps ? pool->miss_warps : hs::kDefaultRangeMissWarps, sms, stream));
+      pool->miss_warps, sms, stream));
 }
 
 hs_status hs_resolve_gather(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P, int32_t K,

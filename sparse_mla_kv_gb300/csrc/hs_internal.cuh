@@ -111,7 +111,11 @@ struct MissOrder {
   int32_t per_group;  // misses an index group can have: R * max_m
   int32_t ranges;     // 1: each copy warp takes whole buckets (ranges); 0: 4-entry items in bucket order,
                       // spread over all copy warps
+  int32_t* queues;    // range schedule, SM partition: the fused gather's work counters (kQueueInts ints,
+                      // zeroed before each launch)
 };
+constexpr int kQueueInts = 4;            // miss buckets, overflow units, HBM chunks, spare
+constexpr size_t kQueueBytes = 256;      // their room at the end of the ordered layout
 // Host pools at least this large (over the layers of a call) are copied bucket by bucket, each bucket by
 // one warp; smaller ones with the items of all buckets spread over every copy warp.  Measured with the
 // library's miss path (131K misses per step, one layer): over spans up to 20 GB the spread items keep
@@ -119,8 +123,6 @@ struct MissOrder {
 // host addresses binds, whole buckets per warp are faster (118 against 50 GB/s at 40 GB, 54 against 39
 // at 72 GB).
 constexpr int64_t kMissRangesBytes = int64_t(40) << 30;
-// Miss warps per CTA of the fused gather with the range schedule, unless the pool sets another count.
-constexpr int kDefaultRangeMissWarps = 1;
 // Bucket capacity: twice the even share, so that only strongly skewed steps overflow.
 inline int32_t miss_bucket_cap(int64_t per_group) {
   return (int32_t)((2 * per_group + kMissBuckets - 1) / kMissBuckets);

@@ -915,7 +915,7 @@ size_t resolve_workspace_bytes(int64_t units, int64_t n, int64_t C) {
 size_t resolve_workspace_bytes_ordered(int64_t groups, int64_t R, int64_t n, int64_t C) {
   const int64_t max_m = n < C ? n : C;
   return resolve_workspace_bytes(groups * R, n, C) + ws_order_cnt_bytes(groups) +
-         16 * (size_t)groups * kMissBuckets * (size_t)miss_bucket_cap(R * max_m);
+         16 * (size_t)groups * kMissBuckets * (size_t)miss_bucket_cap(R * max_m) + kQueueBytes;
 }
 
 MissOrder miss_order_layout(void* workspace, int64_t groups, int64_t R, int64_t n, int64_t C, int64_t num_host_rows) {
@@ -931,6 +931,8 @@ MissOrder miss_order_layout(void* workspace, int64_t groups, int64_t R, int64_t 
   o.shift = miss_bucket_shift(num_host_rows);
   o.cap = miss_bucket_cap(per_group);
   o.per_group = (int32_t)per_group;
+  o.queues = reinterpret_cast<int32_t*>(ws + base + ws_order_cnt_bytes(groups) +
+                                        16 * (size_t)groups * kMissBuckets * (size_t)o.cap);
   return o;
 }
 

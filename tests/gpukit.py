@@ -18,15 +18,14 @@ class Rig:
                  mode: str = "split", graph: bool = False):
         # "split" / "fused": the library's default miss layout for the pool (ordered only for large host
         # pools); a "+order" suffix forces the address-ordered layout on any pool, "+ranges" its range
-        # schedule (a contiguous block of host ranges per copy warp) with one miss warp per fused-gather
-        # CTA, "+ranges2" with two
+        # schedule with the fused gather's default SM partition, "+ranges1" / "+ranges2" with one or two
+        # miss warps in every fused-gather CTA
         base, _, opt = mode.partition("+")
-        assert base in ("split", "fused") and opt in ("", "order", "ranges", "ranges2")
+        assert base in ("split", "fused") and opt in ("", "order", "ranges", "ranges1", "ranges2")
         self.mode = base
         self.force_order = opt != ""
-        self.order_mode = {"order": hs.MISS_ORDER_ON, "ranges": hs.MISS_ORDER_RANGES,
-                           "ranges2": hs.MISS_ORDER_RANGES}.get(opt)
-        self.miss_warps = 2 if opt == "ranges2" else 1
+        self.order_mode = hs.MISS_ORDER_ON if opt == "order" else (hs.MISS_ORDER_RANGES if opt else None)
+        self.miss_warps = {"ranges1": 1, "ranges2": 2}.get(opt, 0)
         self.graph = graph
         self.prep = None
         self.w = w

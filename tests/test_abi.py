@@ -65,7 +65,7 @@ def _ordered_extra(ng, R, P, K, C):
     # the even share of the group's R * min(P*K, C) possible misses, 16 B per entry
     per_group = R * min(P * K, C)
     cap = -(-2 * per_group // NB)
-    return -(-4 * ng * (NB + 1) // 16) * 16 + 16 * ng * NB * cap
+    return -(-4 * ng * (NB + 1) // 16) * 16 + 16 * ng * NB * cap + 256   # + the fused gather's work counters
 
 
 def test_size_queries(lib):

@@ -28,7 +28,8 @@ from tests.casekit import Case, host_only_case
 
 pytestmark = pytest.mark.gpu
 
-MODES_ORDER = ["split", "fused", "split+order", "fused+order", "split+ranges", "fused+ranges", "fused+ranges2"]
+MODES_ORDER = ["split", "fused", "split+order", "fused+order", "split+ranges", "fused+ranges", "fused+ranges1",
+               "fused+ranges2"]
 INT32_MAX = 2**31 - 1
 
 
@@ -126,7 +127,7 @@ def _to_gpu(case, dev, mode):
         pool.set_miss_order(hs.MISS_ORDER_ON)
     elif opt:
         pool.set_miss_order(hs.MISS_ORDER_RANGES)
-        pool.set_miss_warps(2 if opt == "ranges2" else 1)
+        pool.set_miss_warps({"ranges1": 1, "ranges2": 2}.get(opt, 0))
     hot = hs.HotState.allocate(1, torch.from_numpy(case.hot_blocks).to(dev), case.C)
     hot.slot_token.copy_(torch.from_numpy(case.tok))
     hot.slot_stamp.copy_(torch.from_numpy(case.stamp))

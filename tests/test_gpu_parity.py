@@ -33,7 +33,8 @@ def _rig(w, **kw):
 MODES = ["split", "fused"]
 # the same, plus both paths with the address-ordered miss layout forced on (small pools default to
 # per-unit lists)
-MODES_ORDER = MODES + ["split+order", "fused+order", "split+ranges", "fused+ranges", "fused+ranges2"]
+MODES_ORDER = MODES + ["split+order", "fused+order", "split+ranges", "fused+ranges", "fused+ranges1",
+                       "fused+ranges2"]
 
 
 def _base(mode):
@@ -42,14 +43,14 @@ def _base(mode):
 
 def _set_order(pool, mode):
     """+order: the address-ordered miss layout on any pool (its spread schedule on small pools);
-    +ranges: its range schedule (a contiguous block of host ranges per copy warp) with one miss warp per
-    fused-gather CTA; +ranges2: with two."""
+    +ranges: its range schedule with the fused gather's default SM partition; +ranges1 / +ranges2: with one
+    or two miss warps in every fused-gather CTA."""
     opt = mode.partition("+")[2]
     if opt == "order":
         pool.set_miss_order(hs.MISS_ORDER_ON)
-    elif opt in ("ranges", "ranges2"):
+    elif opt.startswith("ranges"):
         pool.set_miss_order(hs.MISS_ORDER_RANGES)
-        pool.set_miss_warps(2 if opt == "ranges2" else 1)
+        pool.set_miss_warps({"ranges1": 1, "ranges2": 2}.get(opt, 0))
 
 
 @pytest.mark.parametrize("mode", MODES_ORDER)
@@ -541,7 +542,8 @@ def test_gather_standalone_multilayer_and_status():
     pool.close()
 
 
-@pytest.mark.parametrize("mode", ["split+order", "fused+order", "split+ranges", "fused+ranges", "fused+ranges2"])
+@pytest.mark.parametrize("mode", ["split+order", "fused+order", "split+ranges", "fused+ranges", "fused+ranges1",
+                                  "fused+ranges2"])
 @pytest.mark.parametrize("P", [1, 4])
 def test_ordered_misses_overflowing_their_bucket(mode, P):
     """Every page's host copy lies in the first two host blocks (one host-row range), so with the
