@@ -835,7 +835,11 @@ def run_ours(args, ws, rank, local):
     m_mean = float(counts[:, 2].mean())
     gather_bytes = n_rows * (2 * B + (8 if fused else 4))
     t_g = statistics.fmean(t_gat)
-    tr = traffic_record("gather_kernel_fused" if fused else "gather_kernel", "gather.cu", n_rows)
+    # the fused gather's kernel: with the range schedule and the SM partition (the default for it) the
+    # partition kernel, else the mixed kernel
+    partition = fused and miss_order.endswith("range schedule") and args.miss_warps == 0
+    gkernel = "gather_partition_kernel" if partition else ("gather_fused_kernel" if fused else "gather_kernel")
+    tr = traffic_record(gkernel, "gather.cu", n_rows)
     # The fused gather moves its miss rows over the host link while it streams the other rows from HBM:
     # its roof is the slower of the two, each against its own peak -- HBM against the measured copy
     # peak, the host link against this run's bulk pinned host-to-device copy rate (MEASURED_PEAKS
@@ -850,7 +854,7 @@ def run_ours(args, ws, rank, local):
                  "algorithmic_bytes_per_launch": link_bytes}
     bound = "host_link" if t_link_roof > t_hbm_roof else "hbm"
     main = link_part if bound == "host_link" else hbm_part
-    roofline = {"bound": bound, "kernel": "gather_kernel<fused>" if fused else "gather_kernel",
+    roofline = {"bound": bound, "kernel": gkernel,
                 "achieved": main["achieved"], "peak": main["peak"], "unit": "GB/s", "frac": main["frac"],
                 "peak_kind": main["peak_kind"], "algorithmic_bytes_per_launch": main["algorithmic_bytes_per_launch"],
                 "timing": "mean launch time from the split pass (events between the calls)",

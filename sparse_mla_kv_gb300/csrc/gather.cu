@@ -319,15 +319,22 @@ __device__ __noinline__ void miss_warp_ranges(const MissOrder ord, int pu, int m
 }
 
 // ---- range schedule, SM partition (the default on large host pools).  Host reads and HBM rows slow
-// each other down when warps of both kinds share an SM: measured on the full-size MTP3 pattern (4 x 18 GB
-// host pools, 378K misses, 8.4M HBM rows) with a standalone kernel, a miss warp in every CTA took 3.3-3.4
-// ms, the misses alone 2.1 ms and the HBM rows alone 1.9 ms, while giving every eighth SM to the misses
-// and the others to the HBM rows took 2.45 ms.  So the CTAs on every kMissSmDivisor-th SM (by %smid)
-// copy misses with all their warps and the others stream HBM rows; work comes from three counters shared
-// by every layer of the launch (miss buckets, overflow slices, HBM chunks), and a CTA that has drained
-// its own kind of work takes the other kind, so every unit is done whichever SMs the CTAs land on.
-constexpr int kMissSmDivisor = 8;
-constexpr int kStripes = 64;         // miss buckets are handed out across 64 stripes of the pool at once
+// each other down when warps of both kinds share an SM, and the host reads are bound by the device's
+// translation of host addresses, which favours fewer host ranges in flight at a time.  So the CTAs on
+// every kMissSmDivisor-th SM (by %smid) copy misses with all their warps, one bucket per warp at a time,
+// layer after layer and in address order within a layer, while the CTAs on the other SMs stream the HBM
+// rows.  Work comes from counters shared by every layer of the launch: one of miss units (each layer's
+// buckets, then its overflow slices) and one of HBM chunks.  A miss CTA that finds no miss work left
+// joins the HBM rows; an HBM CTA joins the misses only if no CTA has registered as a miss CTA, so the
+// misses are always drained, whichever SMs the CTAs land on.
+//
+// Measured on the full-size MTP3 batch (4 layers over 18 GB host pools each, 378K misses and 8.4M HBM
+// rows per step; medians of 20 replays of one planned gather in one process): one miss warp in every CTA
+// 3.30-3.36 ms; this layout 2.68 ms.  Variants of it: an eighth, seventh or fifth of the SMs for the
+// misses 2.89, 2.80 and 2.84 ms; buckets handed out over all layers at once 2.83 ms, and across 64
+// stripes of every pool 3.0-3.9 ms; a bucket split between 4 or 8 warps 3.8-4.0 ms; the HBM CTAs' first
+// warp joining the misses 2.82 ms.  The misses end last: the HBM rows are done after about 2.0 ms.
+constexpr int kMissSmDivisor = 6;
 constexpr int kOvUnit = 64;          // overflow entries per work unit
 constexpr int kHbmChunk = 8192;      // 16-byte output chunks per HBM work unit (128 KB)
 
@@ -337,17 +344,15 @@ __device__ __forceinline__ unsigned sm_id() {
   return r;
 }
 
-// Miss work units of one launch: for each of its nl layers, kMissBuckets bucket units and as many
-// overflow slices of kOvUnit entries as the fullest group's overflow list needs.  Unit u belongs to
-// layer u % nl; i = u / nl < kMissBuckets is a bucket (taken in stripe order, so the warps working at
-// one time read kStripes ranges spread over the pool), i >= kMissBuckets an overflow slice.
-__device__ __forceinline__ int partition_miss_units(const MissOrder& ord, int nl, int group) {
+// Miss work units per layer: kMissBuckets buckets, then as many overflow slices of kOvUnit entries as
+// the fullest group's overflow list needs.
+__device__ __forceinline__ int partition_layer_units(const MissOrder& ord, int nl, int group) {
   int ov_units = 0;
   for (int pu = 0; pu * group < nl; ++pu) {
     const int ovn = min(__ldcg(ord.cnt + (int64_t)pu * (kMissBuckets + 1) + kMissBuckets), ord.per_group);
     ov_units = max(ov_units, (ovn + kOvUnit - 1) / kOvUnit);
   }
-  return nl * (kMissBuckets + ov_units);
+  return kMissBuckets + ov_units;
 }
 
 // One warp copies the entries of miss unit i (bucket or overflow slice) of group pu.
@@ -362,9 +367,8 @@ __device__ __forceinline__ void partition_miss_unit(const MissOrder ord, int i, 
   const int4* src;
   int nb;
   if (i < kMissBuckets) {
-    const int b = (i % kStripes) * (kMissBuckets / kStripes) + i / kStripes;
-    nb = min(__ldcg(cntg + b), ord.cap);
-    src = ord.buckets + ((int64_t)pu * kMissBuckets + b) * ord.cap;
+    nb = min(__ldcg(cntg + i), ord.cap);
+    src = ord.buckets + ((int64_t)pu * kMissBuckets + i) * ord.cap;
   } else {
     const int o0 = (i - kMissBuckets) * kOvUnit;
     nb = max(0, min(kOvUnit, min(__ldcg(cntg + kMissBuckets), ord.per_group) - o0));
@@ -426,20 +430,21 @@ __device__ __forceinline__ void partition_hbm(const LayerPtrs& ptrs, int32_t lay
   }
 }
 
-// A warp's share of the miss units: it takes units until the counter passes the end.
+// A warp's share of the miss units: it takes units until the counter passes the end.  Unit u is unit
+// u % upl of layer u / upl (layer after layer).
 template <int CPR>
 __device__ __forceinline__ void partition_misses(const LayerPtrs& ptrs, int32_t layer_begin, int32_t group, int nl,
                                                  const MissOrder& ord, const int32_t* __restrict__ msrc,
                                                  uint8_t* __restrict__ out, int n, int64_t per_layer, int row_bytes,
                                                  int64_t num_rows, int64_t num_host_rows) {
-  const int units = partition_miss_units(ord, nl, group);
+  const int upl = partition_layer_units(ord, nl, group), units = nl * upl;
   for (;;) {
     int u = 0;
     if ((threadIdx.x & 31) == 0) u = atomicAdd(ord.queues, 1);
     u = __shfl_sync(kFull, u, 0);
     if (u >= units) break;
-    const int l = u % nl, pu = l / group;
-    partition_miss_unit<CPR>(ord, u / nl, pu, ptrs.host[layer_begin + l], ptrs.gpu[layer_begin + l],
+    const int l = u / upl, pu = l / group;
+    partition_miss_unit<CPR>(ord, u - l * upl, pu, ptrs.host[layer_begin + l], ptrs.gpu[layer_begin + l],
                              out + (int64_t)l * per_layer * row_bytes, msrc + (int64_t)pu * per_layer, n, row_bytes,
                              per_layer, num_rows, num_host_rows);
   }
@@ -516,13 +521,19 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_partition_kernel(
     int64_t num_host_rows) {
   const int nl = gridDim.y;
   const int64_t per_layer = (int64_t)R * n;
-  // CTAs on a miss SM copy misses first, then help with the HBM rows; the others the other way round
+  // CTAs on a miss SM register, copy misses, then help with the HBM rows; the others stream HBM rows and
+  // take misses only when no miss CTA has registered (queues[3] counts them)
   const bool miss_sm = sm_id() % kMissSmDivisor == 0;
-  if (miss_sm)
+  if (miss_sm) {
+    if (threadIdx.x == 0) atomicAdd(ord.queues + 3, 1);
     partition_misses<CPR>(ptrs, layer_begin, group, nl, ord, msrc, out, n, per_layer, row_bytes, num_rows,
                           num_host_rows);
+  }
   partition_hbm<CPR>(ptrs, layer_begin, group, nl, ord, msrc, out, per_layer, row_bytes, num_rows);
-  if (!miss_sm)
+  if (miss_sm) return;
+  int no_miss_cta = 0;  // decided once per warp: the miss loop below is warp-synchronous
+  if ((threadIdx.x & 31) == 0) no_miss_cta = *reinterpret_cast<volatile int32_t*>(ord.queues + 3) == 0;
+  if (__shfl_sync(kFull, no_miss_cta, 0))
     partition_misses<CPR>(ptrs, layer_begin, group, nl, ord, msrc, out, n, per_layer, row_bytes, num_rows,
                           num_host_rows);
 }
