@@ -91,6 +91,10 @@ def parse():
                     help="after the timed passes, replay the last timed step's planned gather (hs_gather_planned) "
                          "with the SM partition and with 1 and 2 miss warps in every CTA (hs_pool_set_miss_warps), "
                          "alternating, in this process")
+    ap.add_argument("--miss-sm-ab", type=str, default="",
+                    help="comma-separated SM divisors (e.g. 4,5,6,8): after the timed passes, replay the last timed "
+                         "step's planned gather with the SM partition at each divisor (hs_pool_set_miss_sm_divisor), "
+                         "alternating, in this process")
     ap.add_argument("--miss-warps", type=int, default=0, choices=[0, 1, 2],
                     help="fused gather under the range schedule: 0 = SM partition (the library's default), 1 or 2 = "
                          "that many miss warps in every CTA")
@@ -780,6 +784,30 @@ def run_ours(args, ws, rank, local):
                          "how": "hs_gather_planned of the last timed step replayed with the SM partition and with 1 "
                                 "and 2 miss warps in every CTA (hs_pool_set_miss_warps 0, 1, 2), alternating behind "
                                 "L2 flushes; medians"}
+    miss_sm_ab = None
+    if args.miss_sm_ab and fused:
+        # the same replay as the miss-warp A/B, with the SM partition at each divisor
+        divs = [int(x) for x in args.miss_sm_ab.split(",") if x.strip()]
+        reps = max(5, K)
+        t_div = {d: [] for d in divs}
+        pool.set_miss_warps(0)
+        for rep in range(reps + 1):
+            for dv in divs:
+                pool.set_miss_sm_divisor(dv)
+                flush.fill_(rep & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                phase2()
+                e1.record(stream)
+                e1.synchronize()
+                if rep:
+                    t_div[dv].append(e0.elapsed_time(e1) * 1e-3)
+        pool.set_miss_sm_divisor(0)
+        pool.set_miss_warps(args.miss_warps)
+        miss_sm_ab = {"repeats": reps, "miss_order": miss_order,
+                      "gather_us_median": {str(d): round(1e6 * statistics.median(t_div[d]), 1) for d in divs},
+                      "how": "hs_gather_planned of the last timed step replayed with the SM partition, every divisor-th "
+                             "SM copying misses (hs_pool_set_miss_sm_divisor), alternating behind L2 flushes; medians"}
     gather_ab = None
     if args.gather_ab:
         # the plain gather of the last timed step's rows, every layer of each index group reading its
@@ -989,7 +1017,7 @@ def run_ours(args, ws, rank, local):
                            settle_step_us_medians=[round(1e3 * m, 1) for m in settle_medians]),
             "gathered_gbs": value * B / 1e9, "roofline": roofline, "step_roofline": step_roof,
             "cpu_baseline": cpu, "cpu_baseline_1thread": cpu1, "e2e": e2e, "gpu_launches": int(launches),
-            "graph_replay": graph, "gather_copy_ab": gather_ab, "miss_warps_ab": miss_warps_ab,
+            "graph_replay": graph, "gather_copy_ab": gather_ab, "miss_warps_ab": miss_warps_ab, "miss_sm_ab": miss_sm_ab,
             "schedule_ab": schedule_ab,
             "clocks": clocks,
             "wall_s_timed_region": wall, "timed_counts": {"resident": int(hits_misses[0]),

@@ -86,6 +86,8 @@ def lib():
         L.hs_pool_set_gather_copy.argtypes = [p, i32]
         L.hs_pool_set_miss_warps.restype = i32
         L.hs_pool_set_miss_warps.argtypes = [p, i32]
+        L.hs_pool_set_miss_sm_divisor.restype = i32
+        L.hs_pool_set_miss_sm_divisor.argtypes = [p, i32]
         L.hs_resolve_miss_order.restype = i32
         L.hs_resolve_miss_order.argtypes = [p, i32, i32, i32, i32, i32, ctypes.POINTER(HotStateC), sz]
         L.hs_resolve_smem_bytes.restype = sz
@@ -199,6 +201,11 @@ class Pool:
         """Fused gather under the range schedule: 0 = SM partition (default), 1 or 2 = that many miss warps
         in every CTA; see hs_pool_set_miss_warps."""
         _check(lib().hs_pool_set_miss_warps(self.handle, int(warps)), "hs_pool_set_miss_warps")
+
+    def set_miss_sm_divisor(self, divisor: int) -> None:
+        """SM partition: every divisor-th SM copies the misses (2..32, 0 = default); see
+        hs_pool_set_miss_sm_divisor."""
+        _check(lib().hs_pool_set_miss_sm_divisor(self.handle, int(divisor)), "hs_pool_set_miss_sm_divisor")
 
     def close(self) -> None:
         if getattr(self, "handle", None) is not None and self.handle.value:

@@ -14,6 +14,7 @@ struct hs_pool {
   int32_t miss_order;   // HS_MISS_ORDER_*
   int32_t gather_copy;  // HS_GATHER_COPY_*
   int32_t miss_warps;   // fused gather, range schedule: 0 = SM partition, 1 or 2 = miss warps in every CTA
+  int32_t miss_sm_div;  // SM partition: every miss_sm_div-th SM copies misses (0 = the library's default)
 };
 
 namespace hs {
@@ -183,6 +184,12 @@ hs_status hs_pool_set_gather_copy(hs_pool* pool, int32_t mode) {
 hs_status hs_pool_set_miss_warps(hs_pool* pool, int32_t warps) {
   if (!pool || warps < 0 || warps > 2) return HS_ERR_INVALID_ARG;
   pool->miss_warps = warps;
+  return HS_OK;
+}
+
+hs_status hs_pool_set_miss_sm_divisor(hs_pool* pool, int32_t divisor) {
+  if (!pool || divisor < 0 || divisor == 1 || divisor > 32) return HS_ERR_INVALID_ARG;
+  pool->miss_sm_div = divisor;
   return HS_OK;
 }
 
@@ -387,7 +394,7 @@ hs_status hs_gather_planned(const hs_pool* pool, int32_t layer_begin, int32_t nl
       reinterpret_cast<const int4*>(ws + hs::ws_counts_bytes(units)), ord,
       reinterpret_cast<const int32_t*>(ws + hs::ws_msrc_offset(units, n, capacity)), static_cast<uint8_t*>(out),
       g.row_bytes, (int64_t)g.num_gpu_blocks * g.page_size, (int64_t)g.num_host_blocks * g.page_size,
-      pool->miss_warps, sms, stream));
+      pool->miss_warps, pool->miss_sm_div, sms, stream));
 }
 
 hs_status hs_resolve_gather(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P, int32_t K,

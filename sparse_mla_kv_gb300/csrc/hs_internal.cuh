@@ -101,6 +101,8 @@ constexpr int kMissRowsPerItem = 4;
 // Results do not depend on it: every miss writes its own hot slot and output row.
 constexpr int kMissBuckets = 1024;  // enough host ranges that every copy warp of a large step owns some
 constexpr int kBucketsPerLane = kMissBuckets / 32;
+// the resolver counts a unit's misses per bucket in the victim sort's histogram memory
+static_assert(kMissBuckets <= kRadixBins * kSortWarps, "bucket counters must fit the sort histograms");
 struct MissOrder {
   int32_t* cnt;       // [groups][kMissBuckets + 1]: entries filed per bucket, then the overflow count;
                       // zeroed before the resolver runs.  nullptr: per-unit lists instead.
@@ -231,7 +233,7 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
                                 int32_t n, int32_t max_m, const int32_t* rows, const int32_t* miss_count,
                                 const int4* miss_list, const MissOrder& ord, const int32_t* msrc, uint8_t* out,
                                 int32_t row_bytes, int64_t num_rows, int64_t num_host_rows, int range_miss_warps,
-                                int sms, cudaStream_t s);
+                                int miss_sm_div, int sms, cudaStream_t s);
 cudaError_t launch_offload(const LayerPtrs& ptrs, const PoolGeom& g, const int32_t* gpu_blocks,
                            const int32_t* host_blocks, int32_t n, int32_t* status, int sms, cudaStream_t s);
 cudaError_t launch_fill_i32(int32_t* a, int64_t count, int32_t value, int sms, cudaStream_t s);

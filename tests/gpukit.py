@@ -15,7 +15,7 @@ from synth import content, device as sdev
 
 class Rig:
     def __init__(self, w, *, oracle_bytes: bool = False, device: str = "cuda", check_hot_bytes: bool = True,
-                 mode: str = "split", graph: bool = False):
+                 mode: str = "split", graph: bool = False, miss_sm_div: int = 0):
         # "split" / "fused": the library's default miss layout for the pool (ordered only for large host
         # pools); a "+order" suffix forces the address-ordered layout on any pool, "+ranges" its range
         # schedule with the fused gather's default SM partition, "+ranges1" / "+ranges2" with one or two
@@ -47,6 +47,7 @@ class Rig:
         if self.force_order:
             self.pool.set_miss_order(self.order_mode)
             self.pool.set_miss_warps(self.miss_warps)
+            self.pool.set_miss_sm_divisor(miss_sm_div)
         self.bt_np = w.block_table.copy()
         self.hbt_np = w.host_block_table.copy()
         self.bt = torch.from_numpy(self.bt_np).to(self.dev)

@@ -64,6 +64,23 @@ def test_tiny_decode_all_bytes(mode):
     assert misses > 0
 
 
+@pytest.mark.parametrize("div", [2, 3, 32])
+def test_sm_partition_divisors(div):
+    """The fused gather's SM partition gives the oracle's bytes whatever share of the SMs copies the
+    misses (every second, third or 32nd SM), on the tiny decode and on a small MTP3 batch."""
+    w = workloads.config1(seed=4, steps=6)
+    rig = _rig(w, oracle_bytes=True, mode="fused+ranges", miss_sm_div=div)
+    misses = 0
+    for st in w.iter_steps():
+        _, stats, _, _, _ = rig.step(st)
+        misses += int(stats[..., 3].sum())
+    assert misses > 0
+    w = workloads.config5(seed=5, R=6, L=2, steps=4)
+    rig = _rig(w, mode="fused+ranges", miss_sm_div=div)
+    for st in w.iter_steps():
+        rig.step(st)
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_tiny_decode_other_seeds_and_replay(mode):
     for seed in (1, 2):
@@ -488,6 +505,11 @@ def test_miss_order_decision():
         pool.set_miss_order(5)
     with pytest.raises(hs.HSError):
         pool.set_miss_warps(3)
+    for bad in (-1, 1, 33):
+        with pytest.raises(hs.HSError):
+            pool.set_miss_sm_divisor(bad)
+    for ok in (0, 2, 32):
+        pool.set_miss_sm_divisor(ok)
     no_host = hs.Pool(gpu)
     no_host.set_miss_order(hs.MISS_ORDER_ON)
     assert not hs.miss_order_used(no_host, hot, 2, R, P, K, full)
