@@ -95,6 +95,11 @@ def parse():
                     help="comma-separated SM divisors (e.g. 4,5,6,8): after the timed passes, replay the last timed "
                          "step's planned gather with the SM partition at each divisor (hs_pool_set_miss_sm_divisor), "
                          "alternating, in this process")
+    ap.add_argument("--prefetch-ab", type=int, default=0, metavar="ROUNDS",
+                    help="after the timed passes, ROUNDS rounds of whole timed passes alternating the resolver's miss "
+                         "prefetch off and on (hs_pool_set_miss_prefetch), in this process")
+    ap.add_argument("--miss-prefetch", choices=["off", "on"], default="off",
+                    help="the resolver's miss prefetch for the timed passes (hs_pool_set_miss_prefetch)")
     ap.add_argument("--miss-warps", type=int, default=0, choices=[0, 1, 2],
                     help="fused gather under the range schedule: 0 = SM partition (the library's default), 1 or 2 = "
                          "that many miss warps in every CTA")
@@ -482,6 +487,8 @@ def run_ours(args, ws, rank, local):
                    "ranges": hs.MISS_ORDER_RANGES, "spread": hs.MISS_ORDER_SPREAD}
     pool.set_miss_order(order_modes[args.miss_order])
     pool.set_miss_warps(args.miss_warps)
+    prefetch_mode = hs.MISS_PREFETCH_ON if args.miss_prefetch == "on" else hs.MISS_PREFETCH_OFF
+    pool.set_miss_prefetch(prefetch_mode)
     from sparse_mla_kv_gb300.hostmem import huge_page_fraction
     huge_frac = [round(huge_page_fraction(h), 4) for h in host]
     tb = Tables(w, steps)
@@ -759,6 +766,25 @@ def run_ours(args, ws, rank, local):
                        "step_us_median": {k: [round(x, 1) for x in v] for k, v in steps_med.items()},
                        "how": "per round, one timed pass (the K timed steps after the warm-up replay) with each "
                               "schedule of the ordered miss layout; mean step time of each pass"}
+    prefetch_ab = None
+    if args.prefetch_ab:
+        # whole timed passes over the same steps, alternating the resolver's miss prefetch off and on
+        sums = {"off": [], "on": []}
+        steps_med = {"off": [], "on": []}
+        for rnd in range(args.prefetch_ab):
+            for name, mode in (("off", hs.MISS_PREFETCH_OFF), ("on", hs.MISS_PREFETCH_ON)):
+                pool.set_miss_prefetch(mode)
+                replay_warmup()
+                ev_ab = timed_pass(split=False)
+                ts = [ev_ab[k][0].elapsed_time(ev_ab[k][2]) * 1e-3 for k in range(K)]
+                sums[name].append(1e3 * sum(ts) / K)
+                steps_med[name].append(1e6 * statistics.median(ts))
+        pool.set_miss_prefetch(prefetch_mode)
+        prefetch_ab = {"rounds": args.prefetch_ab, "miss_order": miss_order,
+                       "ms_per_step": {k: [round(x, 4) for x in v] for k, v in sums.items()},
+                       "step_us_median": {k: [round(x, 1) for x in v] for k, v in steps_med.items()},
+                       "how": "per round, one timed pass (the K timed steps after the warm-up replay) with the "
+                              "miss prefetch off, then on; mean and median step time of each pass"}
     miss_warps_ab = None
     if args.miss_warps_ab and fused:
         # the last timed step's plan stays in the workspace: replaying hs_gather_planned rewrites the same
@@ -1011,14 +1037,15 @@ def run_ours(args, ws, rank, local):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": W,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "u8", "data": "synthetic",
-            "config": dict(config_dict(w, args), miss_order=miss_order, timing=headline_timing,
+            "config": dict(config_dict(w, args), miss_order=miss_order, miss_prefetch=args.miss_prefetch,
+                           timing=headline_timing,
                            host_pool_huge_page_fraction=huge_frac,
                            settle_passes=len(settle_medians),
                            settle_step_us_medians=[round(1e3 * m, 1) for m in settle_medians]),
             "gathered_gbs": value * B / 1e9, "roofline": roofline, "step_roofline": step_roof,
             "cpu_baseline": cpu, "cpu_baseline_1thread": cpu1, "e2e": e2e, "gpu_launches": int(launches),
             "graph_replay": graph, "gather_copy_ab": gather_ab, "miss_warps_ab": miss_warps_ab, "miss_sm_ab": miss_sm_ab,
-            "schedule_ab": schedule_ab,
+            "schedule_ab": schedule_ab, "prefetch_ab": prefetch_ab,
             "clocks": clocks,
             "wall_s_timed_region": wall, "timed_counts": {"resident": int(hits_misses[0]),
                                                           "hits": int(hits_misses[1]),

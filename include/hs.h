@@ -172,6 +172,17 @@ size_t hs_resolve_workspace_bytes_min(int32_t nl, int32_t R, int32_t P, int32_t 
 #define HS_MISS_ORDER_SPREAD 4
 hs_status hs_pool_set_miss_order(hs_pool* pool, int32_t mode);
 
+/* Miss prefetch: with HS_MISS_PREFETCH_ON the resolver starts moving each miss's host row into L2
+ * (one bulk L2 prefetch per row and layer of its index group) as soon as it classifies the id, before
+ * it picks the victims; the copy that follows (the miss-copy kernel, or the fused gather's miss warps)
+ * then finds the row in L2.  HS_MISS_PREFETCH_OFF (default): no prefetch.  Results are identical.
+ * The pages copy single rows from pinned host memory ("vLLM GLM 5.3 Optimizations: Hybrid HiSparse
+ * Offloading", "Technical Implementation of Hybrid HiSparse"); when the read starts is this library's
+ * choice.  HS_ERR_INVALID_ARG for an unknown mode. */
+#define HS_MISS_PREFETCH_OFF 0
+#define HS_MISS_PREFETCH_ON 1
+hs_status hs_pool_set_miss_prefetch(hs_pool* pool, int32_t mode);
+
 /* How hs_gather_rows moves its HBM rows.  Results are identical in both modes; only the speed
  * differs.
  *   HS_GATHER_COPY_LOADS (default)  every lane moves 16-byte chunks with ordinary loads and stores,

@@ -27,6 +27,7 @@ LIB_PATH = os.path.join(_HERE, f"libhs_{LIB_VARIANT}.so" if LIB_VARIANT else "li
 HS_OK = 0
 MISS_ORDER_AUTO, MISS_ORDER_OFF, MISS_ORDER_ON, MISS_ORDER_RANGES, MISS_ORDER_SPREAD = 0, 1, 2, 3, 4
 GATHER_COPY_LOADS, GATHER_COPY_BULK = 0, 1
+MISS_PREFETCH_OFF, MISS_PREFETCH_ON = 0, 1
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "ID_RANGE", 3: "MISSING_ROW", 4: "CAPACITY", 5: "STEP_ORDER",
                 6: "CUDA", 7: "TIMEOUT", 8: "TABLE_RANGE"}
 MAX_LAYERS = 128
@@ -88,6 +89,8 @@ def lib():
         L.hs_pool_set_miss_warps.argtypes = [p, i32]
         L.hs_pool_set_miss_sm_divisor.restype = i32
         L.hs_pool_set_miss_sm_divisor.argtypes = [p, i32]
+        L.hs_pool_set_miss_prefetch.restype = i32
+        L.hs_pool_set_miss_prefetch.argtypes = [p, i32]
         L.hs_resolve_miss_order.restype = i32
         L.hs_resolve_miss_order.argtypes = [p, i32, i32, i32, i32, i32, ctypes.POINTER(HotStateC), sz]
         L.hs_resolve_smem_bytes.restype = sz
@@ -201,6 +204,11 @@ class Pool:
         """Fused gather under the range schedule: 0 = SM partition (default), 1 or 2 = that many miss warps
         in every CTA; see hs_pool_set_miss_warps."""
         _check(lib().hs_pool_set_miss_warps(self.handle, int(warps)), "hs_pool_set_miss_warps")
+
+    def set_miss_prefetch(self, mode: int) -> None:
+        """MISS_PREFETCH_ON: the resolver prefetches each miss's host row into L2 when it classifies it;
+        see hs_pool_set_miss_prefetch."""
+        _check(lib().hs_pool_set_miss_prefetch(self.handle, int(mode)), "hs_pool_set_miss_prefetch")
 
     def set_miss_sm_divisor(self, divisor: int) -> None:
         """SM partition: every divisor-th SM copies the misses (2..32, 0 = default); see

@@ -15,6 +15,7 @@ struct hs_pool {
   int32_t gather_copy;  // HS_GATHER_COPY_*
   int32_t miss_warps;   // fused gather, range schedule: 0 = SM partition, 1 or 2 = miss warps in every CTA
   int32_t miss_sm_div;  // SM partition: every miss_sm_div-th SM copies misses (0 = the library's default)
+  int32_t miss_prefetch;  // HS_MISS_PREFETCH_*
 };
 
 namespace hs {
@@ -187,6 +188,12 @@ hs_status hs_pool_set_miss_warps(hs_pool* pool, int32_t warps) {
   return HS_OK;
 }
 
+hs_status hs_pool_set_miss_prefetch(hs_pool* pool, int32_t mode) {
+  if (!pool || mode < HS_MISS_PREFETCH_OFF || mode > HS_MISS_PREFETCH_ON) return HS_ERR_INVALID_ARG;
+  pool->miss_prefetch = mode;
+  return HS_OK;
+}
+
 hs_status hs_pool_set_miss_sm_divisor(hs_pool* pool, int32_t divisor) {
   if (!pool || divisor < 0 || divisor == 1 || divisor > 32) return HS_ERR_INVALID_ARG;
   pool->miss_sm_div = divisor;
@@ -319,6 +326,10 @@ hs_status prepare_resolve(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
   p.miss_list = reinterpret_cast<int4*>(static_cast<uint8_t*>(workspace) + hs::ws_counts_bytes((int64_t)ng * R));
   p.ord = hs::call_miss_order(pool, nl, ng, R, n, C, workspace, workspace_bytes);
   p.msrc = nullptr;
+  if (pool->miss_prefetch == HS_MISS_PREFETCH_ON && g.num_host_blocks > 0) {
+    p.row_bytes = g.row_bytes;
+    for (int l = 0; l < g.num_layers; ++l) p.host[l] = pool->ptrs.host[l];
+  }
   return HS_OK;
 }
 

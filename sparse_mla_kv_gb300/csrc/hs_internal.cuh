@@ -187,6 +187,10 @@ struct ResolveParams {
   //   position of the following repeat, -1 after the last).  A miss entry's fourth field is its first
   //   repeat (-1: none), so the repeats form a chain that starts at the entry.
   int32_t* msrc;
+  // Miss prefetch (row_bytes > 0): each miss's host row is prefetched into L2, in every layer of its
+  // index group, as soon as the resolver classifies it (host[l] is layer l's host pool).
+  int32_t row_bytes;
+  const uint8_t* host[HS_MAX_LAYERS];
 };
 
 struct ResolveSmem {

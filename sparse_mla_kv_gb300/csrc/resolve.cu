@@ -236,6 +236,17 @@ __device__ unsigned short* radix_sort_slots(unsigned short* a, unsigned short* b
 // kS: the page size when it is a compile-time constant (64 in the pages' FP8 MLA setup), else 0.
 // kWide: the id table's entry width (see IdHash).  kT: threads per CTA -- 1024, or 512 so that two
 // units share an SM when there are more units than SMs or a unit is small.  Results do not depend on it.
+// Starts moving a missed row into L2 in every layer of the unit's index group (lr: the group within
+// the call), so that the copy that follows finds it there: one bulk prefetch per layer, with no
+// completion to wait for.  The row is inside the host pool (its block was checked) and 16-byte aligned.
+__device__ __forceinline__ void prefetch_host_row(const ResolveParams& p, int lr, int row) {
+  const int l0 = (p.layer_begin + lr) * p.group;
+  for (int g = 0; g < p.group; ++g) {
+    const uint8_t* a = p.host[l0 + g] + (int64_t)row * p.row_bytes;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(p.row_bytes) : "memory");
+  }
+}
+
 template <int kS, bool kWide, int kT>
 __global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const ResolveParams p, const ResolveSmem sm) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -495,7 +506,10 @@ __global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const
           } else {
             if (e == -1) err |= kErrMissing;
             else if (e == kBadHost) err |= kErrTable;
-            else val = (-2 - e) * S + off;
+            else {
+              val = (-2 - e) * S + off;
+              if (p.row_bytes) prefetch_host_row(p, lr, val);
+            }
             cls = kMiss;
             ++c_miss;
           }

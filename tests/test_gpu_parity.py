@@ -64,6 +64,24 @@ def test_tiny_decode_all_bytes(mode):
     assert misses > 0
 
 
+@pytest.mark.parametrize("mode", ["split", "fused", "split+order", "fused+order", "fused+ranges"])
+def test_miss_prefetch_same_results(mode):
+    """With the resolver's miss prefetch on, every path and miss layout gives the oracle's rows, stats,
+    hot state and bytes (tiny decode, all bytes compared) and the closed-form bytes on an IndexShare MTP3
+    batch (two layers per index group: each miss is prefetched in both layers)."""
+    w = workloads.config1(seed=6, steps=6)
+    rig = _rig(w, oracle_bytes=True, mode=mode, prefetch=True)
+    misses = 0
+    for st in w.iter_steps():
+        _, stats, _, _, _ = rig.step(st)
+        misses += int(stats[..., 3].sum())
+    assert misses > 0
+    w = workloads.config5(seed=7, R=6, L=4, layers_per_index=2, steps=4)
+    rig = _rig(w, mode=mode, prefetch=True)
+    for st in w.iter_steps():
+        rig.step(st)
+
+
 @pytest.mark.parametrize("div", [2, 3, 32])
 def test_sm_partition_divisors(div):
     """The fused gather's SM partition gives the oracle's bytes whatever share of the SMs copies the
@@ -510,6 +528,11 @@ def test_miss_order_decision():
             pool.set_miss_sm_divisor(bad)
     for ok in (0, 2, 32):
         pool.set_miss_sm_divisor(ok)
+    for bad in (-1, 2):
+        with pytest.raises(hs.HSError):
+            pool.set_miss_prefetch(bad)
+    pool.set_miss_prefetch(hs.MISS_PREFETCH_ON)
+    pool.set_miss_prefetch(hs.MISS_PREFETCH_OFF)
     no_host = hs.Pool(gpu)
     no_host.set_miss_order(hs.MISS_ORDER_ON)
     assert not hs.miss_order_used(no_host, hot, 2, R, P, K, full)
