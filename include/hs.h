@@ -174,8 +174,11 @@ hs_status hs_pool_set_miss_order(hs_pool* pool, int32_t mode);
 
 /* Miss prefetch: with HS_MISS_PREFETCH_ON the resolver starts moving each miss's host row into L2
  * (one bulk L2 prefetch per row and layer of its index group) as soon as it classifies the id, before
- * it picks the victims; the copy that follows (the miss-copy kernel, or the fused gather's miss warps)
- * then finds the row in L2.  HS_MISS_PREFETCH_OFF (default): no prefetch.  Results are identical.
+ * it picks the victims, so that the copy that follows (the miss-copy kernel, or the fused gather's miss
+ * warps) may find the row in L2.  HS_MISS_PREFETCH_OFF (default): no prefetch.  Results are identical.
+ * Measured on one GB300, whole timed passes alternating in one process: no gain on the mixed-residency
+ * batch (83 against 82.6 us per step) and slower on the agentic batch (0.75 against 0.34 ms), so it
+ * stays off.
  * The pages copy single rows from pinned host memory ("vLLM GLM 5.3 Optimizations: Hybrid HiSparse
  * Offloading", "Technical Implementation of Hybrid HiSparse"); when the read starts is this library's
  * choice.  HS_ERR_INVALID_ARG for an unknown mode. */

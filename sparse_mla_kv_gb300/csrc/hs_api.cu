@@ -326,7 +326,7 @@ hs_status prepare_resolve(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
   p.miss_list = reinterpret_cast<int4*>(static_cast<uint8_t*>(workspace) + hs::ws_counts_bytes((int64_t)ng * R));
   p.ord = hs::call_miss_order(pool, nl, ng, R, n, C, workspace, workspace_bytes);
   p.msrc = nullptr;
-  if (pool->miss_prefetch == HS_MISS_PREFETCH_ON && g.num_host_blocks > 0) {
+  if (pool->miss_prefetch != HS_MISS_PREFETCH_OFF && g.num_host_blocks > 0) {
     p.row_bytes = g.row_bytes;
     for (int l = 0; l < g.num_layers; ++l) p.host[l] = pool->ptrs.host[l];
   }

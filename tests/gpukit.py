@@ -15,7 +15,7 @@ from synth import content, device as sdev
 
 class Rig:
     def __init__(self, w, *, oracle_bytes: bool = False, device: str = "cuda", check_hot_bytes: bool = True,
-                 mode: str = "split", graph: bool = False, miss_sm_div: int = 0, prefetch: bool = False):
+                 mode: str = "split", graph: bool = False, miss_sm_div: int = 0, prefetch: int = 0):
         # "split" / "fused": the library's default miss layout for the pool (ordered only for large host
         # pools); a "+order" suffix forces the address-ordered layout on any pool, "+ranges" its range
         # schedule with the fused gather's default SM partition, "+ranges1" / "+ranges2" with one or two
@@ -45,7 +45,7 @@ class Rig:
                 sdev.fill_host_pool(w, l, self.host[l], self.dev)
         self.pool = hs.Pool(self.gpu, self.host if w.num_host_blocks else None)
         if prefetch:
-            self.pool.set_miss_prefetch(hs.MISS_PREFETCH_ON)
+            self.pool.set_miss_prefetch(prefetch)
         if self.force_order:
             self.pool.set_miss_order(self.order_mode)
             self.pool.set_miss_warps(self.miss_warps)

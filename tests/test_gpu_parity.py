@@ -70,14 +70,14 @@ def test_miss_prefetch_same_results(mode):
     hot state and bytes (tiny decode, all bytes compared) and the closed-form bytes on an IndexShare MTP3
     batch (two layers per index group: each miss is prefetched in both layers)."""
     w = workloads.config1(seed=6, steps=6)
-    rig = _rig(w, oracle_bytes=True, mode=mode, prefetch=True)
+    rig = _rig(w, oracle_bytes=True, mode=mode, prefetch=hs.MISS_PREFETCH_ON)
     misses = 0
     for st in w.iter_steps():
         _, stats, _, _, _ = rig.step(st)
         misses += int(stats[..., 3].sum())
     assert misses > 0
     w = workloads.config5(seed=7, R=6, L=4, layers_per_index=2, steps=4)
-    rig = _rig(w, mode=mode, prefetch=True)
+    rig = _rig(w, mode=mode, prefetch=hs.MISS_PREFETCH_ON)
     for st in w.iter_steps():
         rig.step(st)
 
