@@ -100,6 +100,9 @@ def parse():
                          "prefetch off and on (hs_pool_set_miss_prefetch), in this process")
     ap.add_argument("--miss-prefetch", choices=["off", "on"], default="off",
                     help="the resolver's miss prefetch for the timed passes (hs_pool_set_miss_prefetch)")
+    ap.add_argument("--planes-ab", action="store_true",
+                    help="after the timed passes, replay the last timed step's gather with the output in rows and in "
+                         "the planes {512, 16, 128} (hs_pool_set_gather_planes), alternating, in this process")
     ap.add_argument("--miss-warps", type=int, default=0, choices=[0, 1, 2],
                     help="fused gather under the range schedule: 0 = SM partition (the library's default), 1 or 2 = "
                          "that many miss warps in every CTA")
@@ -834,6 +837,33 @@ def run_ours(args, ws, rank, local):
                       "gather_us_median": {str(d): round(1e6 * statistics.median(t_div[d]), 1) for d in divs},
                       "how": "hs_gather_planned of the last timed step replayed with the SM partition, every divisor-th "
                              "SM copying misses (hs_pool_set_miss_sm_divisor), alternating behind L2 flushes; medians"}
+    planes_ab = None
+    if args.planes_ab and B == 656:
+        # the last timed step's gather (planned gather when fused, plain gather of its rows otherwise)
+        # replayed with each output layout; the bytes differ only in their order
+        rows_p = out_rows.reshape(NG, -1)
+        reps = max(5, K)
+        t_pl = {"rows": [], "planes": []}
+        for rep in range(reps + 1):
+            for name, pl in (("rows", ()), ("planes", (512, 16, 128))):
+                pool.set_gather_planes(pl)
+                flush.fill_(rep & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                if fused:
+                    phase2()
+                else:
+                    for l in range(L):
+                        hs.gather_rows(pool, rows_p[l // G], layer_begin=l, out=gout[l])
+                e1.record(stream)
+                e1.synchronize()
+                if rep:
+                    t_pl[name].append(e0.elapsed_time(e1) * 1e-3)
+        pool.set_gather_planes(())
+        planes_ab = {"repeats": reps, "path": args.path,
+                     "gather_us_median": {k: round(1e6 * statistics.median(v), 1) for k, v in t_pl.items()},
+                     "how": "the last timed step's gather replayed with the output in rows and in planes "
+                            "{512, 16, 128} (hs_pool_set_gather_planes), alternating behind L2 flushes; medians"}
     gather_ab = None
     if args.gather_ab:
         # the plain gather of the last timed step's rows, every layer of each index group reading its
@@ -1044,7 +1074,7 @@ def run_ours(args, ws, rank, local):
                            settle_step_us_medians=[round(1e3 * m, 1) for m in settle_medians]),
             "gathered_gbs": value * B / 1e9, "roofline": roofline, "step_roofline": step_roof,
             "cpu_baseline": cpu, "cpu_baseline_1thread": cpu1, "e2e": e2e, "gpu_launches": int(launches),
-            "graph_replay": graph, "gather_copy_ab": gather_ab, "miss_warps_ab": miss_warps_ab, "miss_sm_ab": miss_sm_ab,
+            "graph_replay": graph, "gather_copy_ab": gather_ab, "miss_warps_ab": miss_warps_ab, "miss_sm_ab": miss_sm_ab, "planes_ab": planes_ab,
             "schedule_ab": schedule_ab, "prefetch_ab": prefetch_ab,
             "clocks": clocks,
             "wall_s_timed_region": wall, "timed_counts": {"resident": int(hits_misses[0]),

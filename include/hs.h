@@ -186,6 +186,21 @@ hs_status hs_pool_set_miss_order(hs_pool* pool, int32_t mode);
 #define HS_MISS_PREFETCH_ON 1
 hs_status hs_pool_set_miss_prefetch(hs_pool* pool, int32_t mode);
 
+/* Output layout of the gathers (hs_gather_rows, hs_gather_planned, hs_resolve_gather).  nplanes = 0
+ * (the default): rows, out[layer][position][row_bytes].  nplanes = 1..HS_MAX_PLANES: each row is cut
+ * into planes of plane_bytes[p] bytes (each > 0 and a multiple of 16, summing to row_bytes), and each
+ * layer's output holds the planes one after the other: plane p of position i at
+ *   out + layer_bytes * layer + positions * (plane_bytes[0] + ... + plane_bytes[p-1]) + i * plane_bytes[p],
+ * layer_bytes = positions * row_bytes (the same buffer size as rows).  The FP8 MLA row of the pages'
+ * benchmark configs is 512 B of latent, 16 B of scales and 128 B of rope: {512, 16, 128} gives a
+ * sparse-MLA consumer each part as its own dense array.  The pages gather whole rows with one stride
+ * ("vLLM GLM 5.3 Optimizations: Hybrid HiSparse Offloading", "Technical Implementation of Hybrid
+ * HiSparse"); the split is this library's option.  The bulk copy mode writes rows only: with planes
+ * set, hs_gather_rows uses loads.  Results are the same bytes in either layout.  HS_ERR_INVALID_ARG
+ * for a bad count or plane size (plane_bytes is read during the call only). */
+#define HS_MAX_PLANES 4
+hs_status hs_pool_set_gather_planes(hs_pool* pool, int32_t nplanes, const int32_t* plane_bytes);
+
 /* How hs_gather_rows moves its HBM rows.  Results are identical in both modes; only the speed
  * differs.
  *   HS_GATHER_COPY_LOADS (default)  every lane moves 16-byte chunks with ordinary loads and stores,

@@ -28,6 +28,7 @@ HS_OK = 0
 MISS_ORDER_AUTO, MISS_ORDER_OFF, MISS_ORDER_ON, MISS_ORDER_RANGES, MISS_ORDER_SPREAD = 0, 1, 2, 3, 4
 GATHER_COPY_LOADS, GATHER_COPY_BULK = 0, 1
 MISS_PREFETCH_OFF, MISS_PREFETCH_ON = 0, 1
+MAX_PLANES = 4
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "ID_RANGE", 3: "MISSING_ROW", 4: "CAPACITY", 5: "STEP_ORDER",
                 6: "CUDA", 7: "TIMEOUT", 8: "TABLE_RANGE"}
 MAX_LAYERS = 128
@@ -91,6 +92,8 @@ def lib():
         L.hs_pool_set_miss_sm_divisor.argtypes = [p, i32]
         L.hs_pool_set_miss_prefetch.restype = i32
         L.hs_pool_set_miss_prefetch.argtypes = [p, i32]
+        L.hs_pool_set_gather_planes.restype = i32
+        L.hs_pool_set_gather_planes.argtypes = [p, i32, ctypes.POINTER(i32)]
         L.hs_resolve_miss_order.restype = i32
         L.hs_resolve_miss_order.argtypes = [p, i32, i32, i32, i32, i32, ctypes.POINTER(HotStateC), sz]
         L.hs_resolve_smem_bytes.restype = sz
@@ -190,6 +193,7 @@ class Pool:
         with torch.cuda.device(g0.device):
             _check(lib().hs_pool_create(ctypes.byref(desc), ctypes.byref(h)), "hs_pool_create")
         self.handle = h
+        self.planes = ()
 
     def set_miss_order(self, mode: int) -> None:
         """MISS_ORDER_AUTO (default), MISS_ORDER_OFF, MISS_ORDER_ON, MISS_ORDER_RANGES or MISS_ORDER_SPREAD:
@@ -204,6 +208,15 @@ class Pool:
         """Fused gather under the range schedule: 0 = SM partition (default), 1 or 2 = that many miss warps
         in every CTA; see hs_pool_set_miss_warps."""
         _check(lib().hs_pool_set_miss_warps(self.handle, int(warps)), "hs_pool_set_miss_warps")
+
+    def set_gather_planes(self, plane_bytes=()) -> None:
+        """Output layout of the gathers: () = rows; else the row cut into planes of these byte sizes
+        (multiples of 16 summing to row_bytes, at most MAX_PLANES), each layer's output holding the planes
+        one after the other; see hs_pool_set_gather_planes and plane_views."""
+        pb = [int(x) for x in plane_bytes]
+        arr = (ctypes.c_int32 * max(1, len(pb)))(*pb)
+        _check(lib().hs_pool_set_gather_planes(self.handle, len(pb), arr), "hs_pool_set_gather_planes")
+        self.planes = tuple(pb)
 
     def set_miss_prefetch(self, mode: int) -> None:
         """MISS_PREFETCH_ON: the resolver prefetches each miss's host row into L2 when it classifies it;
@@ -365,7 +378,8 @@ def resolve_gather(pool: Pool, topk: torch.Tensor, block_table: torch.Tensor, ho
 
 def gather_rows(pool: Pool, rows: torch.Tensor, *, layer_begin: int = 0, out: Optional[torch.Tensor] = None,
                 status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """rows int32 [nl][n] (or [n] for one layer) -> uint8 [nl][n][row_bytes] (or [n][row_bytes])."""
+    """rows int32 [nl][n] (or [n] for one layer) -> uint8 [nl][n][row_bytes] (or [n][row_bytes]), each
+    layer's bytes in the pool's output layout (rows, or planes: see plane_views)."""
     squeeze = rows.dim() == 1
     r2 = rows.reshape(1, -1) if squeeze else rows.reshape(rows.shape[0], -1)
     nl, n = int(r2.shape[0]), int(r2.shape[1])
@@ -377,6 +391,24 @@ def gather_rows(pool: Pool, rows: torch.Tensor, *, layer_begin: int = 0, out: Op
                                 _opt(status, "status"), _stream(stream))
     _check(code, "hs_gather_rows")
     return out.reshape(n, pool.row_bytes) if squeeze else out
+
+
+def plane_views(out: torch.Tensor, plane_bytes) -> list:
+    """Views of a gather output written in a plane layout (Pool.set_gather_planes): out uint8
+    [nl][n][row_bytes] (or [n][row_bytes]) -> one uint8 tensor per plane, [nl][n][plane_bytes[p]] (or
+    [n][plane_bytes[p]]).  No copy."""
+    squeeze = out.dim() == 2
+    o = out.reshape(1, out.shape[0], out.shape[1]) if squeeze else out
+    nl, n, rb = int(o.shape[0]), int(o.shape[1]), int(o.shape[2])
+    if sum(plane_bytes) != rb:
+        raise ValueError("plane sizes must sum to the row size")
+    flat = o.reshape(nl, n * rb)
+    views, off = [], 0
+    for w in plane_bytes:
+        v = flat[:, off:off + n * w].reshape(nl, n, w)
+        views.append(v[0] if squeeze else v)
+        off += n * w
+    return views
 
 
 def offload_pages(pool: Pool, gpu_blocks: torch.Tensor, host_blocks: torch.Tensor, *,

@@ -35,11 +35,12 @@ constexpr int kGatherUnroll = 8;
 // ask for two (hs_pool_set_miss_warps) instead of the SM partition.
 constexpr int kMaxMissWarps = 2;
 
-template <int CPR>
+template <int CPR, bool kPlanes>
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const LayerPtrs ptrs, int32_t layer_begin,
                                                                 const int32_t* __restrict__ rows, int64_t n,
                                                                 uint8_t* __restrict__ out, int32_t row_bytes,
-                                                                int64_t num_rows, int32_t* status) {
+                                                                int64_t num_rows, int32_t* status,
+                                                                const OutPlanes pl) {
   const int cpr = CPR ? CPR : (row_bytes >> 4);
   const int lr = blockIdx.y;
   const uint8_t* __restrict__ pool = ptrs.gpu[layer_begin + lr];
@@ -67,7 +68,14 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const LayerPtrs 
 #pragma unroll
     for (int k = 0; k < kGatherUnroll; ++k) {
       const int64_t c = c0 + k * stride;
-      if (c < total) lout[c] = v[k];
+      if (c < total) {
+        if constexpr (kPlanes) {
+          const int64_t i = c / cpr;
+          *plane_chunk(reinterpret_cast<uint8_t*>(lout), pl, n, i, (int)(c - i * cpr)) = v[k];
+        } else {
+          lout[c] = v[k];
+        }
+      }
     }
   }
   if (bad && status) *status = HS_ERR_ID_RANGE;
@@ -196,6 +204,28 @@ __global__ void __launch_bounds__(kBulkThreads) gather_bulk_kernel(const LayerPt
 
 constexpr int kRepeatRegs = 3;  // repeat positions per entry followed before the stores (P - 1 for MTP3)
 
+// Where the miss copies write a layer's output.  The row-size-specialised kernels (CPR > 0) write rows
+// only and carry just the base; the generic kernels (CPR = 0) carry the layout, rows or planes (the
+// launchers send plane layouts to the generic kernels).
+// at(i, b, row_bytes): the 16 bytes at byte b (a multiple of 16) of position i's row.
+template <int CPR>
+struct MissOut {
+  uint8_t* base;
+  __device__ __forceinline__ uint4* at(int64_t i, int64_t b, int row_bytes) const {
+    return reinterpret_cast<uint4*>(base + i * row_bytes + b);
+  }
+};
+template <>
+struct MissOut<0> {
+  OutMap om;
+  __device__ __forceinline__ uint4* at(int64_t i, int64_t b, int) const { return out_chunk(om, i, (int)(b >> 4)); }
+};
+template <int CPR>
+__device__ __forceinline__ MissOut<CPR> miss_out(uint8_t* base, int64_t rows, int row_bytes, const OutPlanes& pl) {
+  if constexpr (CPR > 0) return MissOut<CPR>{base};
+  else return MissOut<0>{OutMap{base, rows, row_bytes, pl}};
+}
+
 // Copies the rows of up to kMissRowsPerItem miss entries (lane j < nrows holds entry j) from the
 // host pool into their hot slots, their output positions and the output positions of their repeats
 // (the chain that starts at the entry's fourth field and continues through lmsrc, the plan's
@@ -203,7 +233,7 @@ constexpr int kRepeatRegs = 3;  // repeat positions per entry followed before th
 // are read while they are in flight, then everything is stored.  n: positions per request.
 template <int CPR>
 __device__ __forceinline__ void copy_miss_item(const uint8_t* __restrict__ host, uint8_t* __restrict__ pool,
-                                               uint8_t* __restrict__ lout, const int32_t* __restrict__ lmsrc,
+                                               const MissOut<CPR>& om, const int32_t* __restrict__ lmsrc,
                                                int n, int4 ent, int nrows, int row_bytes, int64_t per_layer,
                                                int64_t gpu_rows, int64_t host_rows) {
   constexpr int kU = CPR ? (kMissRowsPerItem * CPR + 31) / 32 : 4;
@@ -254,10 +284,10 @@ __device__ __forceinline__ void copy_miss_item(const uint8_t* __restrict__ host,
       const bool row_ok = HS_CHECKED ? __shfl_sync(kFull, ok, rr) != 0 : true;
       if (in && row_ok) {
         *reinterpret_cast<uint4*>(pool + (int64_t)dst * row_bytes + cc16) = v[k];
-        *reinterpret_cast<uint4*>(lout + (int64_t)pos * row_bytes + cc16) = v[k];
+        *om.at(pos, cc16, row_bytes) = v[k];
 #pragma unroll
         for (int t = 0; t < kRepeatRegs; ++t)
-          if (rp[t] >= 0) *reinterpret_cast<uint4*>(lout + ((int64_t)q * n + rp[t]) * row_bytes + cc16) = v[k];
+          if (rp[t] >= 0) *om.at((int64_t)q * n + rp[t], cc16, row_bytes) = v[k];
       }
     }
     if (d >= 0 && !HS_CHECK(d < n, kChkChain)) d = -1;
@@ -269,7 +299,7 @@ __device__ __forceinline__ void copy_miss_item(const uint8_t* __restrict__ host,
         const int q = __shfl_sync(kFull, rq, rr);
         const int dd = __shfl_sync(kFull, d, rr);
         if (f < total && dd >= 0)
-          *reinterpret_cast<uint4*>(lout + ((int64_t)q * n + dd) * row_bytes + (int64_t)(f - rr * cpr) * 16) = v[k];
+          *om.at((int64_t)q * n + dd, (int64_t)(f - rr * cpr) * 16, row_bytes) = v[k];
       }
       if (d >= 0) d = -3 - __ldcg(lmsrc + (int64_t)rq * n + d);
       if (d >= 0 && !HS_CHECK(d < n, kChkChain)) d = -1;
@@ -291,7 +321,7 @@ __device__ __forceinline__ void copy_miss_item(const uint8_t* __restrict__ host,
 template <int CPR>
 __device__ __noinline__ void miss_warp_ranges(const MissOrder ord, int pu, int mw, int nmw,
                                               const uint8_t* __restrict__ host, uint8_t* __restrict__ pool,
-                                              uint8_t* __restrict__ lout, const int32_t* __restrict__ lmsrc, int n,
+                                              const MissOut<CPR> om, const int32_t* __restrict__ lmsrc, int n,
                                               int row_bytes, int64_t per_layer, int64_t num_rows,
                                               int64_t num_host_rows) {
   const int lane = threadIdx.x & 31;
@@ -304,7 +334,7 @@ __device__ __noinline__ void miss_warp_ranges(const MissOrder ord, int pu, int m
     for (int i = 0; i < nb; i += kMissRowsPerItem) {
       const int nrows = min(kMissRowsPerItem, nb - i);
       const int4 ent = lane < nrows ? src[i + lane] : make_int4(0, 0, 0, 0);
-      copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
+      copy_miss_item<CPR>(host, pool, om, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
     }
   }
   const int ovn = min(__ldcg(cntg + kMissBuckets), ord.per_group);
@@ -314,7 +344,7 @@ __device__ __noinline__ void miss_warp_ranges(const MissOrder ord, int pu, int m
   for (int i = o0; i < o1; i += kMissRowsPerItem) {
     const int nrows = min(kMissRowsPerItem, o1 - i);
     const int4 ent = lane < nrows ? ovl[i + lane] : make_int4(0, 0, 0, 0);
-    copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
+    copy_miss_item<CPR>(host, pool, om, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
   }
 }
 
@@ -359,7 +389,7 @@ __device__ __forceinline__ int partition_layer_units(const MissOrder& ord, int n
 template <int CPR>
 __device__ __forceinline__ void partition_miss_unit(const MissOrder ord, int i, int pu,
                                                  const uint8_t* __restrict__ host, uint8_t* __restrict__ pool,
-                                                 uint8_t* __restrict__ lout, const int32_t* __restrict__ lmsrc, int n,
+                                                 const MissOut<CPR> om, const int32_t* __restrict__ lmsrc, int n,
                                                  int row_bytes, int64_t per_layer, int64_t num_rows,
                                                  int64_t num_host_rows) {
   const int lane = threadIdx.x & 31;
@@ -377,17 +407,17 @@ __device__ __forceinline__ void partition_miss_unit(const MissOrder ord, int i, 
   for (int j = 0; j < nb; j += kMissRowsPerItem) {
     const int nrows = min(kMissRowsPerItem, nb - j);
     const int4 ent = lane < nrows ? src[j + lane] : make_int4(0, 0, 0, 0);
-    copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
+    copy_miss_item<CPR>(host, pool, om, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
   }
 }
 
 // The whole CTA: HBM chunks until the queue is empty.  Chunk unit c covers 16-byte output chunks
 // [(c / nl) * kHbmChunk, ...) of layer c % nl; every position the miss warps do not own is written.
-template <int CPR>
+template <int CPR, bool kPlanes>
 __device__ __forceinline__ void partition_hbm(const LayerPtrs& ptrs, int32_t layer_begin, int32_t group, int nl,
                                               const MissOrder& ord, const int32_t* __restrict__ msrc,
                                               uint8_t* __restrict__ out, int64_t per_layer, int row_bytes,
-                                              int64_t num_rows) {
+                                              int64_t num_rows, const OutPlanes& pl) {
   const int cpr = CPR ? CPR : (row_bytes >> 4);
   const int64_t total = per_layer * cpr;  // 16-byte chunks per layer
   const int64_t units = (total + kHbmChunk - 1) / kHbmChunk * nl;
@@ -424,8 +454,16 @@ __device__ __forceinline__ void partition_hbm(const LayerPtrs& ptrs, int32_t lay
         }
       }
 #pragma unroll
-      for (int k = 0; k < kGatherUnroll; ++k)
-        if (st[k]) lout4[cb + (int64_t)k * kGatherThreads] = v[k];
+      for (int k = 0; k < kGatherUnroll; ++k) {
+        if (!st[k]) continue;
+        const int64_t cc = cb + (int64_t)k * kGatherThreads;
+        if constexpr (kPlanes) {
+          const int64_t i = cc / cpr;
+          *plane_chunk(reinterpret_cast<uint8_t*>(lout4), pl, per_layer, i, (int)(cc - i * cpr)) = v[k];
+        } else {
+          lout4[cc] = v[k];
+        }
+      }
     }
   }
 }
@@ -436,7 +474,7 @@ template <int CPR>
 __device__ __forceinline__ void partition_misses(const LayerPtrs& ptrs, int32_t layer_begin, int32_t group, int nl,
                                                  const MissOrder& ord, const int32_t* __restrict__ msrc,
                                                  uint8_t* __restrict__ out, int n, int64_t per_layer, int row_bytes,
-                                                 int64_t num_rows, int64_t num_host_rows) {
+                                                 int64_t num_rows, int64_t num_host_rows, const OutPlanes& pl) {
   const int upl = partition_layer_units(ord, nl, group), units = nl * upl;
   for (;;) {
     int u = 0;
@@ -444,9 +482,9 @@ __device__ __forceinline__ void partition_misses(const LayerPtrs& ptrs, int32_t 
     u = __shfl_sync(kFull, u, 0);
     if (u >= units) break;
     const int l = u / upl, pu = l / group;
-    partition_miss_unit<CPR>(ord, u - l * upl, pu, ptrs.host[layer_begin + l], ptrs.gpu[layer_begin + l],
-                             out + (int64_t)l * per_layer * row_bytes, msrc + (int64_t)pu * per_layer, n, row_bytes,
-                             per_layer, num_rows, num_host_rows);
+    const MissOut<CPR> om = miss_out<CPR>(out + (int64_t)l * per_layer * row_bytes, per_layer, row_bytes, pl);
+    partition_miss_unit<CPR>(ord, u - l * upl, pu, ptrs.host[layer_begin + l], ptrs.gpu[layer_begin + l], om,
+                             msrc + (int64_t)pu * per_layer, n, row_bytes, per_layer, num_rows, num_host_rows);
   }
 }
 
@@ -456,7 +494,7 @@ __device__ __forceinline__ void partition_misses(const LayerPtrs& ptrs, int32_t 
 template <int CPR>
 __device__ __noinline__ void miss_warp_spread(const MissOrder ord, int pu, int mw, int nmw,
                                               const uint8_t* __restrict__ host, uint8_t* __restrict__ pool,
-                                              uint8_t* __restrict__ lout, const int32_t* __restrict__ lmsrc, int n,
+                                              const MissOut<CPR> om, const int32_t* __restrict__ lmsrc, int n,
                                               int row_bytes, int64_t per_layer, int64_t num_rows,
                                               int64_t num_host_rows, MissItems& mi) {
   const int lane = threadIdx.x & 31;
@@ -470,7 +508,7 @@ __device__ __noinline__ void miss_warp_spread(const MissOrder ord, int pu, int m
     mi.locate(ord, i, start, in_ov, nrows);
     int4 ent = make_int4(0, 0, 0, 0);
     if (lane < nrows) ent = (in_ov ? ovl : bk)[start + lane];
-    copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
+    copy_miss_item<CPR>(host, pool, om, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
   }
 }
 
@@ -480,7 +518,7 @@ template <int CPR>
 __device__ __noinline__ void miss_warp_lists(const int32_t* __restrict__ miss_count, const int4* __restrict__ miss_list,
                                              int pu, int R, int max_m, int64_t mw, int64_t nmw,
                                              const uint8_t* __restrict__ host, uint8_t* __restrict__ pool,
-                                             uint8_t* __restrict__ lout, const int32_t* __restrict__ lmsrc, int n,
+                                             const MissOut<CPR> om, const int32_t* __restrict__ lmsrc, int n,
                                              int row_bytes, int64_t per_layer, int64_t num_rows,
                                              int64_t num_host_rows) {
   const int lane = threadIdx.x & 31;
@@ -507,7 +545,7 @@ __device__ __noinline__ void miss_warp_lists(const int32_t* __restrict__ miss_co
       const int nrows = min(kMissRowsPerItem, c - r0);
       int4 ent = make_int4(0, 0, 0, 0);
       if (lane < nrows) ent = miss_list[((int64_t)pu * R + rq) * max_m + r0 + lane];
-      copy_miss_item<CPR>(host, pool, lout, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
+      copy_miss_item<CPR>(host, pool, om, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
     }
   }
 }
@@ -516,11 +554,11 @@ __device__ __noinline__ void miss_warp_lists(const int32_t* __restrict__ miss_co
 // gather_fused_kernel, in a kernel of its own so that neither layout's registers constrain the other's.
 // The CTAs on SMs whose %smid is a multiple of miss_sm_div (kMissSmDivisor unless the pool sets another)
 // copy the misses.
-template <int CPR>
+template <int CPR, bool kPlanes>
 __global__ void __launch_bounds__(kGatherThreads, 4) gather_partition_kernel(
     const LayerPtrs ptrs, int32_t layer_begin, int32_t group, int32_t R, int32_t n, const MissOrder ord,
     const int32_t* __restrict__ msrc, uint8_t* __restrict__ out, int32_t row_bytes, int64_t num_rows,
-    int64_t num_host_rows, int miss_sm_div) {
+    int64_t num_host_rows, int miss_sm_div, const OutPlanes pl) {
   const int nl = gridDim.y;
   const int64_t per_layer = (int64_t)R * n;
   // CTAs on a miss SM register, copy misses, then help with the HBM rows; the others stream HBM rows and
@@ -529,23 +567,23 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_partition_kernel(
   if (miss_sm) {
     if (threadIdx.x == 0) atomicAdd(ord.queues + 3, 1);
     partition_misses<CPR>(ptrs, layer_begin, group, nl, ord, msrc, out, n, per_layer, row_bytes, num_rows,
-                          num_host_rows);
+                          num_host_rows, pl);
   }
-  partition_hbm<CPR>(ptrs, layer_begin, group, nl, ord, msrc, out, per_layer, row_bytes, num_rows);
+  partition_hbm<CPR, kPlanes>(ptrs, layer_begin, group, nl, ord, msrc, out, per_layer, row_bytes, num_rows, pl);
   if (miss_sm) return;
   int no_miss_cta = 0;  // decided once per warp: the miss loop below is warp-synchronous
   if ((threadIdx.x & 31) == 0) no_miss_cta = *reinterpret_cast<volatile int32_t*>(ord.queues + 3) == 0;
   if (__shfl_sync(kFull, no_miss_cta, 0))
     partition_misses<CPR>(ptrs, layer_begin, group, nl, ord, msrc, out, n, per_layer, row_bytes, num_rows,
-                          num_host_rows);
+                          num_host_rows, pl);
 }
 
-template <int CPR>
+template <int CPR, bool kPlanes>
 __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
     const LayerPtrs ptrs, int32_t layer_begin, int32_t group, int32_t R, int32_t n, int32_t max_m,
     const int32_t* __restrict__ rows, const int32_t* __restrict__ miss_count, const int4* __restrict__ miss_list,
     const MissOrder ord, const int32_t* __restrict__ msrc, uint8_t* __restrict__ out, int32_t row_bytes,
-    int64_t num_rows, int64_t num_host_rows, int32_t nmiss) {
+    int64_t num_rows, int64_t num_host_rows, int32_t nmiss, const OutPlanes pl) {
   pdl_wait_prerequisites();   // the resolve plan (rows, sources, miss lists) must be complete and visible
   const int cpr = CPR ? CPR : (row_bytes >> 4);
   const int lr = blockIdx.y;
@@ -555,6 +593,7 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
   const uint8_t* __restrict__ host = ptrs.host[layer_begin + lr];
   const int64_t per_layer = (int64_t)R * n;
   uint8_t* __restrict__ lout = out + (int64_t)lr * per_layer * row_bytes;
+  const MissOut<CPR> om = miss_out<CPR>(lout, per_layer, row_bytes, pl);
   const int32_t* __restrict__ lmsrc = msrc + (int64_t)pu * per_layer;
 
   if (warp < nmiss) {
@@ -563,13 +602,13 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
     const int64_t nmw = (int64_t)gridDim.x * nmiss;
     __shared__ MissItems s_mi;  // spread schedule (one miss warp)
     if (ord.cnt && !ord.ranges)
-      miss_warp_spread<CPR>(ord, pu, (int)mw, (int)nmw, host, pool, lout, lmsrc, n, row_bytes, per_layer, num_rows,
+      miss_warp_spread<CPR>(ord, pu, (int)mw, (int)nmw, host, pool, om, lmsrc, n, row_bytes, per_layer, num_rows,
                             num_host_rows, s_mi);
     else if (ord.cnt)
-      miss_warp_ranges<CPR>(ord, pu, (int)mw, (int)nmw, host, pool, lout, lmsrc, n, row_bytes, per_layer, num_rows,
+      miss_warp_ranges<CPR>(ord, pu, (int)mw, (int)nmw, host, pool, om, lmsrc, n, row_bytes, per_layer, num_rows,
                             num_host_rows);
     else
-      miss_warp_lists<CPR>(miss_count, miss_list, pu, R, max_m, mw, nmw, host, pool, lout, lmsrc, n, row_bytes,
+      miss_warp_lists<CPR>(miss_count, miss_list, pu, R, max_m, mw, nmw, host, pool, om, lmsrc, n, row_bytes,
                            per_layer, num_rows, num_host_rows);
     return;
   }
@@ -602,14 +641,23 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_fused_kernel(
       }
     }
 #pragma unroll
-    for (int k = 0; k < kGatherUnroll; ++k)
-      if (st[k]) lout4[c0 + k * stride] = v[k];
+    for (int k = 0; k < kGatherUnroll; ++k) {
+      if (!st[k]) continue;
+      const int64_t c = c0 + k * stride;
+      if constexpr (kPlanes) {
+        const int64_t i = c / cpr;
+        *plane_chunk(lout, pl, per_layer, i, (int)(c - i * cpr)) = v[k];
+      } else {
+        lout4[c] = v[k];
+      }
+    }
   }
 }
 
-int g_occ_plain[2] = {0, 0};
-int g_occ_fused[2] = {0, 0};
-int g_occ_partition[2] = {0, 0};
+// resident CTAs per SM of each kernel: [0] 656-byte rows, [1] any row size, [2] any row size in planes
+int g_occ_plain[3] = {0, 0, 0};
+int g_occ_fused[3] = {0, 0, 0};
+int g_occ_partition[3] = {0, 0, 0};
 int g_occ_bulk = 0;          // resident bulk-gather CTAs per SM for the 656-byte rows' footprint
 size_t g_bulk_smem_max = 0;  // dynamic shared memory the bulk gather may use (the opt-in maximum)
 
@@ -649,12 +697,15 @@ uint32_t check_take_gather() {
 }
 
 void warm_gather_launch_configs() {
-  resident_blocks(gather_kernel<41>, &g_occ_plain[0]);
-  resident_blocks(gather_kernel<0>, &g_occ_plain[1]);
-  resident_blocks(gather_fused_kernel<41>, &g_occ_fused[0]);
-  resident_blocks(gather_fused_kernel<0>, &g_occ_fused[1]);
-  resident_blocks(gather_partition_kernel<41>, &g_occ_partition[0]);
-  resident_blocks(gather_partition_kernel<0>, &g_occ_partition[1]);
+  resident_blocks(gather_kernel<41, false>, &g_occ_plain[0]);
+  resident_blocks(gather_kernel<0, false>, &g_occ_plain[1]);
+  resident_blocks(gather_kernel<0, true>, &g_occ_plain[2]);
+  resident_blocks(gather_fused_kernel<41, false>, &g_occ_fused[0]);
+  resident_blocks(gather_fused_kernel<0, false>, &g_occ_fused[1]);
+  resident_blocks(gather_fused_kernel<0, true>, &g_occ_fused[2]);
+  resident_blocks(gather_partition_kernel<41, false>, &g_occ_partition[0]);
+  resident_blocks(gather_partition_kernel<0, false>, &g_occ_partition[1]);
+  resident_blocks(gather_partition_kernel<0, true>, &g_occ_partition[2]);
   if (g_bulk_smem_max == 0) {
     int dev = 0, optin = 0;
     if (cudaGetDevice(&dev) == cudaSuccess &&
@@ -675,8 +726,8 @@ bool gather_bulk_fits(int32_t row_bytes) {
 
 cudaError_t launch_gather(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, const int32_t* rows, int64_t n,
                           uint8_t* out, int32_t row_bytes, int64_t num_rows, int32_t* status, int sms,
-                          cudaStream_t s, bool bulk) {
-  if (bulk && gather_bulk_fits(row_bytes)) {
+                          cudaStream_t s, bool bulk, const OutPlanes& planes) {
+  if (bulk && planes.n == 0 && gather_bulk_fits(row_bytes)) {
     const size_t smem = bulk_smem_bytes(row_bytes);
     const int occ = row_bytes == 656 ? g_occ_bulk : 1;
     const int64_t want = (n + kBulkWarps * kBulkStages - 1) / (kBulkWarps * kBulkStages);
@@ -685,13 +736,13 @@ cudaError_t launch_gather(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl
     count_launch();
     return cudaGetLastError();
   }
-  int* occ = g_occ_plain;
-  const bool k41 = row_bytes == 656;
-  auto kern = k41 ? gather_kernel<41> : gather_kernel<0>;
+  // kernel variant: 656-byte rows, any row size, any row size in planes
+  const int var = planes.n ? 2 : (row_bytes == 656 ? 0 : 1);
+  auto kern = var == 0 ? gather_kernel<41, false> : (var == 1 ? gather_kernel<0, false> : gather_kernel<0, true>);
   const int64_t want = (n * (row_bytes >> 4) + (int64_t)kGatherThreads * kGatherUnroll - 1) /
                        ((int64_t)kGatherThreads * kGatherUnroll);
-  const dim3 grid = wave_grid(sms, resident_blocks(kern, &occ[k41 ? 0 : 1]), want, nl);
-  kern<<<grid, kGatherThreads, 0, s>>>(ptrs, layer_begin, rows, n, out, row_bytes, num_rows, status);
+  const dim3 grid = wave_grid(sms, resident_blocks(kern, &g_occ_plain[var]), want, nl);
+  kern<<<grid, kGatherThreads, 0, s>>>(ptrs, layer_begin, rows, n, out, row_bytes, num_rows, status, planes);
   count_launch();
   return cudaGetLastError();
 }
@@ -700,10 +751,11 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
                                 int32_t n, int32_t max_m, const int32_t* rows, const int32_t* miss_count,
                                 const int4* miss_list, const MissOrder& ord, const int32_t* msrc, uint8_t* out,
                                 int32_t row_bytes, int64_t num_rows, int64_t num_host_rows, int range_miss_warps,
-                                int miss_sm_div, int sms, cudaStream_t s) {
-  int* occ = g_occ_fused;
-  const bool k41 = row_bytes == 656;
-  auto kern = k41 ? gather_fused_kernel<41> : gather_fused_kernel<0>;
+                                int miss_sm_div, const OutPlanes& planes, int sms, cudaStream_t s) {
+  // kernel variant: 656-byte rows, any row size, any row size in planes
+  const int var = planes.n ? 2 : (row_bytes == 656 ? 0 : 1);
+  auto kern = var == 0 ? gather_fused_kernel<41, false>
+                       : (var == 1 ? gather_fused_kernel<0, false> : gather_fused_kernel<0, true>);
   // range schedule: 0 = SM partition, else that many miss warps in every CTA; one otherwise
   const int nmiss = (ord.cnt && ord.ranges)
                         ? (range_miss_warps <= 0 ? 0 : (range_miss_warps >= kMaxMissWarps ? kMaxMissWarps : 1))
@@ -715,7 +767,7 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
   // have, so a small batch does not queue its host round trips on a few warps
   const int64_t want_miss =
       ((int64_t)R * ((max_m + kMissRowsPerItem - 1) / kMissRowsPerItem) + nmiss - 1) / (nmiss > 0 ? nmiss : 1);
-  const dim3 grid = wave_grid(sms, resident_blocks(kern, &occ[k41 ? 0 : 1]), want_hbm > want_miss ? want_hbm : want_miss,
+  const dim3 grid = wave_grid(sms, resident_blocks(kern, &g_occ_fused[var]), want_hbm > want_miss ? want_hbm : want_miss,
                               nl);
   // With the ordered layout (large host pools) the gather is not launched early: CTAs placed while
   // the resolver still runs made the whole gather's host reads slower there (measured: agentic
@@ -723,20 +775,21 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
   cudaError_t e;
   if (nmiss == 0) {
     // SM partition: one full wave; its work counters start at zero in every launch
-    auto pkern = k41 ? gather_partition_kernel<41> : gather_partition_kernel<0>;
-    const dim3 pgrid = wave_grid(sms, resident_blocks(pkern, &g_occ_partition[k41 ? 0 : 1]), (int64_t)1 << 40, nl);
+    auto pkern = var == 0 ? gather_partition_kernel<41, false>
+                          : (var == 1 ? gather_partition_kernel<0, false> : gather_partition_kernel<0, true>);
+    const dim3 pgrid = wave_grid(sms, resident_blocks(pkern, &g_occ_partition[var]), (int64_t)1 << 40, nl);
     e = cudaMemsetAsync(ord.queues, 0, kQueueInts * sizeof(int32_t), s);
     if (e != cudaSuccess) return e;
     pkern<<<pgrid, kGatherThreads, 0, s>>>(ptrs, layer_begin, group, R, n, ord, msrc, out, row_bytes, num_rows,
-                                           num_host_rows, miss_sm_div >= 2 ? miss_sm_div : kMissSmDivisor);
+                                           num_host_rows, miss_sm_div >= 2 ? miss_sm_div : kMissSmDivisor, planes);
     e = cudaGetLastError();
   } else if (ord.cnt) {
     kern<<<grid, kGatherThreads, 0, s>>>(ptrs, layer_begin, group, R, n, max_m, rows, miss_count, miss_list, ord, msrc,
-                                         out, row_bytes, num_rows, num_host_rows, nmiss);
+                                         out, row_bytes, num_rows, num_host_rows, nmiss, planes);
     e = cudaGetLastError();
   } else {
     e = launch_dependent(kern, grid, dim3(kGatherThreads), 0, s, ptrs, layer_begin, group, R, n, max_m, rows,
-                         miss_count, miss_list, ord, msrc, out, row_bytes, num_rows, num_host_rows, 1);
+                         miss_count, miss_list, ord, msrc, out, row_bytes, num_rows, num_host_rows, 1, planes);
   }
   if (e != cudaSuccess) return e;
   count_launch();

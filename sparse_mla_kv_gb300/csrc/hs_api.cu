@@ -16,6 +16,7 @@ struct hs_pool {
   int32_t miss_warps;   // fused gather, range schedule: 0 = SM partition, 1 or 2 = miss warps in every CTA
   int32_t miss_sm_div;  // SM partition: every miss_sm_div-th SM copies misses (0 = the library's default)
   int32_t miss_prefetch;  // HS_MISS_PREFETCH_*
+  hs::OutPlanes planes;   // output layout of the gathers (planes.n = 0: rows)
 };
 
 namespace hs {
@@ -185,6 +186,24 @@ hs_status hs_pool_set_gather_copy(hs_pool* pool, int32_t mode) {
 hs_status hs_pool_set_miss_warps(hs_pool* pool, int32_t warps) {
   if (!pool || warps < 0 || warps > 2) return HS_ERR_INVALID_ARG;
   pool->miss_warps = warps;
+  return HS_OK;
+}
+
+hs_status hs_pool_set_gather_planes(hs_pool* pool, int32_t nplanes, const int32_t* plane_bytes) {
+  if (!pool || nplanes < 0 || nplanes > HS_MAX_PLANES || (nplanes > 0 && !plane_bytes)) return HS_ERR_INVALID_ARG;
+  hs::OutPlanes pl{};
+  int64_t sum = 0;
+  for (int p = 0; p < nplanes; ++p) {
+    if (plane_bytes[p] <= 0 || plane_bytes[p] % 16) return HS_ERR_INVALID_ARG;
+    pl.start[p] = (int32_t)(sum >> 4);
+    pl.width[p] = plane_bytes[p] >> 4;
+    sum += plane_bytes[p];
+  }
+  if (nplanes > 0 && sum != pool->g.row_bytes) return HS_ERR_INVALID_ARG;
+  for (int p = nplanes; p < HS_MAX_PLANES; ++p) pl.start[p] = INT32_MAX;  // no chunk reaches a missing plane
+  pl.start[0] = 0;
+  pl.n = nplanes;
+  pool->planes = pl;
   return HS_OK;
 }
 
@@ -405,7 +424,7 @@ hs_status hs_gather_planned(const hs_pool* pool, int32_t layer_begin, int32_t nl
       reinterpret_cast<const int4*>(ws + hs::ws_counts_bytes(units)), ord,
       reinterpret_cast<const int32_t*>(ws + hs::ws_msrc_offset(units, n, capacity)), static_cast<uint8_t*>(out),
       g.row_bytes, (int64_t)g.num_gpu_blocks * g.page_size, (int64_t)g.num_host_blocks * g.page_size,
-      pool->miss_warps, pool->miss_sm_div, sms, stream));
+      pool->miss_warps, pool->miss_sm_div, pool->planes, sms, stream));
 }
 
 hs_status hs_resolve_gather(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P, int32_t K,
@@ -434,7 +453,7 @@ hs_status hs_gather_rows(const hs_pool* pool, int32_t layer_begin, int32_t nl, c
   if (sms <= 0) return HS_ERR_CUDA;
   return hs::cuda_status(hs::launch_gather(pool->ptrs, layer_begin, nl, rows, n, static_cast<uint8_t*>(out),
                                            g.row_bytes, (int64_t)g.num_gpu_blocks * g.page_size, out_status, sms,
-                                           stream, pool->gather_copy == HS_GATHER_COPY_BULK));
+                                           stream, pool->gather_copy == HS_GATHER_COPY_BULK, pool->planes));
 }
 
 hs_status hs_offload_pages(const hs_pool* pool, const int32_t* gpu_blocks, const int32_t* host_blocks, int32_t n,

@@ -103,6 +103,32 @@ constexpr int kMissBuckets = 1024;  // enough host ranges that every copy warp o
 constexpr int kBucketsPerLane = kMissBuckets / 32;
 // the resolver counts a unit's misses per bucket in the victim sort's histogram memory
 static_assert(kMissBuckets <= kRadixBins * kSortWarps, "bucket counters must fit the sort histograms");
+// Output layout of gathered rows.  n = 0: rows, [positions][row_bytes].  n = 1..4: the row is cut into
+// n planes of width[p] 16-byte chunks (start[p] = the plane's first chunk within the row; start[q] for
+// q >= n lies past any chunk), stored one after the other: [plane 0 of every position][plane 1 ...].
+struct OutPlanes {
+  int32_t n;
+  int32_t start[4];
+  int32_t width[4];
+};
+// One layer's output: `rows` positions from `base`, in the pool's layout.
+struct OutMap {
+  uint8_t* base;
+  int64_t rows;
+  int32_t row_bytes;
+  OutPlanes pl;
+};
+// Address of 16-byte chunk j of output position i in the plane layout.
+__device__ __forceinline__ uint4* plane_chunk(uint8_t* base, const OutPlanes& pl, int64_t rows, int64_t i, int j) {
+  const int p = (j >= pl.start[1]) + (j >= pl.start[2]) + (j >= pl.start[3]);
+  return reinterpret_cast<uint4*>(base) + rows * pl.start[p] + i * pl.width[p] + (j - pl.start[p]);
+}
+// Address of 16-byte chunk j of output position i in either layout.
+__device__ __forceinline__ uint4* out_chunk(const OutMap& om, int64_t i, int j) {
+  return om.pl.n ? plane_chunk(om.base, om.pl, om.rows, i, j)
+                 : reinterpret_cast<uint4*>(om.base + i * om.row_bytes) + j;
+}
+
 struct MissOrder {
   int32_t* cnt;       // [groups][kMissBuckets + 1]: entries filed per bucket, then the overflow count;
                       // zeroed before the resolver runs.  nullptr: per-unit lists instead.
@@ -225,9 +251,11 @@ cudaError_t launch_miss_copy(const ResolveParams& p, const LayerPtrs& ptrs, int3
                              cudaStream_t s);
 // bulk: move the rows with one-dimensional bulk copies through shared memory (HS_GATHER_COPY_BULK)
 // when the stages fit the device's shared memory, else with 16-byte loads and stores.
+// planes: the output layout (rows when planes.n = 0; the bulk mode writes rows only and falls back to
+// loads for planes).
 cudaError_t launch_gather(const LayerPtrs& ptrs, int32_t layer_begin, int32_t nl, const int32_t* rows, int64_t n,
                           uint8_t* out, int32_t row_bytes, int64_t num_rows, int32_t* status, int sms,
-                          cudaStream_t s, bool bulk = false);
+                          cudaStream_t s, bool bulk, const OutPlanes& planes);
 bool gather_bulk_fits(int32_t row_bytes);
 // The fused gather: rows of layers [layer_begin, layer_begin+nl), R requests x n positions each; miss
 // rows come from the pinned host pool through the resolver's miss lists (dedicated warps) and are
@@ -237,7 +265,7 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
                                 int32_t n, int32_t max_m, const int32_t* rows, const int32_t* miss_count,
                                 const int4* miss_list, const MissOrder& ord, const int32_t* msrc, uint8_t* out,
                                 int32_t row_bytes, int64_t num_rows, int64_t num_host_rows, int range_miss_warps,
-                                int miss_sm_div, int sms, cudaStream_t s);
+                                int miss_sm_div, const OutPlanes& planes, int sms, cudaStream_t s);
 cudaError_t launch_offload(const LayerPtrs& ptrs, const PoolGeom& g, const int32_t* gpu_blocks,
                            const int32_t* host_blocks, int32_t n, int32_t* status, int sms, cudaStream_t s);
 cudaError_t launch_fill_i32(int32_t* a, int64_t count, int32_t value, int sms, cudaStream_t s);

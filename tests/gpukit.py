@@ -15,7 +15,8 @@ from synth import content, device as sdev
 
 class Rig:
     def __init__(self, w, *, oracle_bytes: bool = False, device: str = "cuda", check_hot_bytes: bool = True,
-                 mode: str = "split", graph: bool = False, miss_sm_div: int = 0, prefetch: int = 0):
+                 mode: str = "split", graph: bool = False, miss_sm_div: int = 0, prefetch: int = 0,
+                 planes: tuple = ()):
         # "split" / "fused": the library's default miss layout for the pool (ordered only for large host
         # pools); a "+order" suffix forces the address-ordered layout on any pool, "+ranges" its range
         # schedule with the fused gather's default SM partition, "+ranges1" / "+ranges2" with one or two
@@ -46,6 +47,9 @@ class Rig:
         self.pool = hs.Pool(self.gpu, self.host if w.num_host_blocks else None)
         if prefetch:
             self.pool.set_miss_prefetch(prefetch)
+        self.planes = tuple(planes)
+        if self.planes:
+            self.pool.set_gather_planes(self.planes)
         if self.force_order:
             self.pool.set_miss_order(self.order_mode)
             self.pool.set_miss_warps(self.miss_warps)
@@ -174,6 +178,9 @@ class Rig:
 
     def compare(self, st, rows, stats, out, o_rows, o_stats) -> None:
         w = self.w
+        if self.planes:   # back to rows: each plane is a column range of the rows
+            views = hs.plane_views(out, self.planes)
+            out = torch.cat(views, dim=-1)
         g_rows = rows.cpu().numpy()
         g_stats = stats.cpu().numpy()
         assert np.array_equal(g_stats, o_stats), f"stats differ at step {st.index}"

@@ -587,6 +587,57 @@ def test_gather_standalone_multilayer_and_status():
     pool.close()
 
 
+@pytest.mark.parametrize("planes", [(512, 16, 128), (656,), (16, 640), (128, 128, 128, 272)])
+def test_gather_planes_standalone(planes):
+    """hs_gather_rows with the plane layout: each plane holds, for every position, its column range of
+    the oracle's gathered rows (ragged tail, -1 rows, several layers); the bulk copy mode falls back to
+    loads with planes set."""
+    dev = torch.device("cuda")
+    L, S, B, ngb = 3, 8, 656, 40
+    gpu = [torch.randint(0, 256, (ngb, S, B), dtype=torch.uint8, device=dev) for _ in range(L)]
+    pool = hs.Pool(gpu, None)
+    pool.set_gather_planes(planes)
+    rng = np.random.default_rng(2)
+    n = 4099
+    rows = rng.integers(-1, ngb * S, size=(L, n)).astype(np.int32)
+    pools_np = [g.cpu().numpy().reshape(-1) for g in gpu]
+    o_out, st = oracle.gather(B=B, num_rows=ngb * S, pools=pools_np, rows=rows)
+    assert st == 0
+    # the layout written out: per layer, plane p = every position's bytes [c_p, c_p + planes[p]) in turn
+    cuts = np.cumsum((0,) + tuple(planes))
+    expect = np.stack([np.concatenate([o_out[l][:, cuts[p]:cuts[p + 1]].reshape(-1) for p in range(len(planes))])
+                       for l in range(L)])
+    for copy in (hs.GATHER_COPY_LOADS, hs.GATHER_COPY_BULK):
+        pool.set_gather_copy(copy)
+        out = hs.gather_rows(pool, torch.from_numpy(rows).to(dev))
+        assert np.array_equal(out.cpu().numpy().reshape(L, -1), expect), f"planes {planes} copy mode {copy}"
+        back = torch.cat(hs.plane_views(out, planes), dim=-1)
+        assert np.array_equal(back.cpu().numpy(), o_out)
+    # back to rows
+    pool.set_gather_planes(())
+    out = hs.gather_rows(pool, torch.from_numpy(rows).to(dev))
+    assert np.array_equal(out.cpu().numpy(), o_out)
+    for bad in ((512, 16), (512, 16, 120, 8), (0, 656), (16,) * 5):
+        with pytest.raises(hs.HSError):
+            pool.set_gather_planes(bad)
+    pool.close()
+
+
+@pytest.mark.parametrize("mode", ["split", "fused", "fused+order", "fused+ranges", "fused+ranges1"])
+def test_planes_through_the_resolver(mode):
+    """The fused gathers (per-unit lists, spread schedule, SM partition, mixed range layout) and the
+    split path write the plane layout {512, 16, 128}: converted back to rows, every gathered byte, pool
+    byte and slot equals the oracle's (tiny decode) and the closed form (small MTP3 batch with IndexShare)."""
+    w = workloads.config1(seed=8, steps=6)
+    rig = _rig(w, oracle_bytes=True, mode=mode, planes=(512, 16, 128))
+    for st in w.iter_steps():
+        rig.step(st)
+    w = workloads.config5(seed=9, R=6, L=4, layers_per_index=2, steps=4)
+    rig = _rig(w, mode=mode, planes=(512, 16, 128))
+    for st in w.iter_steps():
+        rig.step(st)
+
+
 @pytest.mark.parametrize("mode", ["split+order", "fused+order", "split+ranges", "fused+ranges", "fused+ranges1",
                                   "fused+ranges2"])
 @pytest.mark.parametrize("P", [1, 4])
