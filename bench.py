@@ -816,7 +816,7 @@ def run_ours(args, ws, rank, local):
     miss_sm_ab = None
     if args.miss_sm_ab and fused:
         # the same replay as the miss-warp A/B, with the SM partition at each divisor
-        divs = [int(x) for x in args.miss_sm_ab.split(",") if x.strip()]
+        divs = [int(x) for x in args.miss_sm_ab.split(",") if x.strip()]   # -1: no miss SM
         reps = max(5, K)
         t_div = {d: [] for d in divs}
         pool.set_miss_warps(0)

@@ -229,7 +229,8 @@ hs_status hs_pool_set_miss_warps(hs_pool* pool, int32_t warps);
 /* The SM partition's share of miss SMs: the CTAs on every divisor-th SM (by SM id) copy the misses, the
  * others stream the HBM rows.  divisor 2..32, or 0 for the library's default (6: on the full-size MTP3
  * batch the misses, read over the host link, end last; fewer miss SMs leave them slower, more slow the
- * HBM rows).  Results are identical for every divisor.  HS_ERR_INVALID_ARG for another value. */
+ * HBM rows), or -1 for no miss SM: every CTA streams HBM rows, then copies misses.  Results are identical
+ * for every divisor.  HS_ERR_INVALID_ARG for another value. */
 hs_status hs_pool_set_miss_sm_divisor(hs_pool* pool, int32_t divisor);
 
 /* 1 if a resolve call on layers [layer_begin, layer_begin + nl) with this shape, hot state and

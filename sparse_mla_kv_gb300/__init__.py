@@ -224,8 +224,8 @@ class Pool:
         _check(lib().hs_pool_set_miss_prefetch(self.handle, int(mode)), "hs_pool_set_miss_prefetch")
 
     def set_miss_sm_divisor(self, divisor: int) -> None:
-        """SM partition: every divisor-th SM copies the misses (2..32, 0 = default); see
-        hs_pool_set_miss_sm_divisor."""
+        """SM partition: every divisor-th SM copies the misses (2..32, 0 = default, -1 = none: HBM rows
+        first, then misses on every SM); see hs_pool_set_miss_sm_divisor."""
         _check(lib().hs_pool_set_miss_sm_divisor(self.handle, int(divisor)), "hs_pool_set_miss_sm_divisor")
 
     def close(self) -> None:

@@ -553,7 +553,8 @@ __device__ __noinline__ void miss_warp_lists(const int32_t* __restrict__ miss_co
 // The fused gather with the range schedule's SM partition (see partition_misses): the same outputs as
 // gather_fused_kernel, in a kernel of its own so that neither layout's registers constrain the other's.
 // The CTAs on SMs whose %smid is a multiple of miss_sm_div (kMissSmDivisor unless the pool sets another)
-// copy the misses.
+// copy the misses; miss_sm_div = 0 names no miss SM, so every CTA streams HBM rows first and then takes
+// misses (the path a launch whose CTAs miss every miss SM takes).
 template <int CPR, bool kPlanes>
 __global__ void __launch_bounds__(kGatherThreads, 4) gather_partition_kernel(
     const LayerPtrs ptrs, int32_t layer_begin, int32_t group, int32_t R, int32_t n, const MissOrder ord,
@@ -563,7 +564,7 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_partition_kernel(
   const int64_t per_layer = (int64_t)R * n;
   // CTAs on a miss SM register, copy misses, then help with the HBM rows; the others stream HBM rows and
   // take misses only when no miss CTA has registered (queues[3] counts them)
-  const bool miss_sm = sm_id() % (unsigned)miss_sm_div == 0;
+  const bool miss_sm = miss_sm_div > 0 && sm_id() % (unsigned)miss_sm_div == 0;
   if (miss_sm) {
     if (threadIdx.x == 0) atomicAdd(ord.queues + 3, 1);
     partition_misses<CPR>(ptrs, layer_begin, group, nl, ord, msrc, out, n, per_layer, row_bytes, num_rows,
@@ -781,7 +782,8 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
     e = cudaMemsetAsync(ord.queues, 0, kQueueInts * sizeof(int32_t), s);
     if (e != cudaSuccess) return e;
     pkern<<<pgrid, kGatherThreads, 0, s>>>(ptrs, layer_begin, group, R, n, ord, msrc, out, row_bytes, num_rows,
-                                           num_host_rows, miss_sm_div >= 2 ? miss_sm_div : kMissSmDivisor, planes);
+                                           num_host_rows, miss_sm_div >= 2 ? miss_sm_div : (miss_sm_div < 0 ? 0 : kMissSmDivisor),
+                                           planes);
     e = cudaGetLastError();
   } else if (ord.cnt) {
     kern<<<grid, kGatherThreads, 0, s>>>(ptrs, layer_begin, group, R, n, max_m, rows, miss_count, miss_list, ord, msrc,

@@ -14,7 +14,7 @@ struct hs_pool {
   int32_t miss_order;   // HS_MISS_ORDER_*
   int32_t gather_copy;  // HS_GATHER_COPY_*
   int32_t miss_warps;   // fused gather, range schedule: 0 = SM partition, 1 or 2 = miss warps in every CTA
-  int32_t miss_sm_div;  // SM partition: every miss_sm_div-th SM copies misses (0 = the library's default)
+  int32_t miss_sm_div;  // SM partition: every miss_sm_div-th SM copies misses (0 = the library's default, -1 none)
   int32_t miss_prefetch;  // HS_MISS_PREFETCH_*
   hs::OutPlanes planes;   // output layout of the gathers (planes.n = 0: rows)
 };
@@ -214,7 +214,7 @@ hs_status hs_pool_set_miss_prefetch(hs_pool* pool, int32_t mode) {
 }
 
 hs_status hs_pool_set_miss_sm_divisor(hs_pool* pool, int32_t divisor) {
-  if (!pool || divisor < 0 || divisor == 1 || divisor > 32) return HS_ERR_INVALID_ARG;
+  if (!pool || divisor < -1 || divisor == 1 || divisor > 32) return HS_ERR_INVALID_ARG;
   pool->miss_sm_div = divisor;
   return HS_OK;
 }

@@ -82,10 +82,12 @@ def test_miss_prefetch_same_results(mode):
         rig.step(st)
 
 
-@pytest.mark.parametrize("div", [2, 3, 32])
+@pytest.mark.parametrize("div", [2, 3, 32, -1])
 def test_sm_partition_divisors(div):
     """The fused gather's SM partition gives the oracle's bytes whatever share of the SMs copies the
-    misses (every second, third or 32nd SM), on the tiny decode and on a small MTP3 batch."""
+    misses (every second, third or 32nd SM), and with no miss SM at all (-1: every CTA streams its HBM
+    rows, then drains the misses -- the path of a launch whose CTAs land on no miss SM), on the tiny
+    decode and on a small MTP3 batch."""
     w = workloads.config1(seed=4, steps=6)
     rig = _rig(w, oracle_bytes=True, mode="fused+ranges", miss_sm_div=div)
     misses = 0
@@ -523,10 +525,10 @@ def test_miss_order_decision():
         pool.set_miss_order(5)
     with pytest.raises(hs.HSError):
         pool.set_miss_warps(3)
-    for bad in (-1, 1, 33):
+    for bad in (-2, 1, 33):
         with pytest.raises(hs.HSError):
             pool.set_miss_sm_divisor(bad)
-    for ok in (0, 2, 32):
+    for ok in (0, 2, 32, -1):
         pool.set_miss_sm_divisor(ok)
     for bad in (-1, 2):
         with pytest.raises(hs.HSError):
