@@ -103,9 +103,10 @@ def parse():
     ap.add_argument("--planes-ab", action="store_true",
                     help="after the timed passes, replay the last timed step's gather with the output in rows and in "
                          "the planes {512, 16, 128} (hs_pool_set_gather_planes), alternating, in this process")
-    ap.add_argument("--miss-warps", type=int, default=0, choices=[0, 1, 2],
-                    help="fused gather under the range schedule: 0 = SM partition (the library's default), 1 or 2 = "
-                         "that many miss warps in every CTA")
+    ap.add_argument("--miss-warps", type=int, default=-1, choices=[-1, 0, 1, 2],
+                    help="fused gather: -1 = the library's default (SM partition with the range schedule, one miss "
+                         "warp per CTA with per-unit lists), 0 = SM partition, 1 or 2 = that many miss warps in every "
+                         "CTA (hs_pool_set_miss_warps)")
     ap.add_argument("--link-probe", action="store_true",
                     help="measure the miss path's host-link rate against the span of host memory it reads "
                          "(one layer, all-miss steps) instead of a workload")
@@ -921,7 +922,8 @@ def run_ours(args, ws, rank, local):
     t_g = statistics.fmean(t_gat)
     # the fused gather's kernel: with the range schedule and the SM partition (the default for it) the
     # partition kernel, else the mixed kernel
-    partition = fused and miss_order.endswith("range schedule") and args.miss_warps == 0
+    partition = fused and ((miss_order.endswith("range schedule") and args.miss_warps <= 0) or
+                           (miss_order == "per-unit lists" and args.miss_warps == 0))
     gkernel = "gather_partition_kernel" if partition else ("gather_fused_kernel" if fused else "gather_kernel")
     tr = traffic_record(gkernel, "gather.cu", n_rows)
     # The fused gather moves its miss rows over the host link while it streams the other rows from HBM:

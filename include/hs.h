@@ -217,12 +217,15 @@ hs_status hs_pool_set_gather_planes(hs_pool* pool, int32_t nplanes, const int32_
 #define HS_GATHER_COPY_BULK 1
 hs_status hs_pool_set_gather_copy(hs_pool* pool, int32_t mode);
 
-/* How the fused gather (hs_gather_planned, hs_resolve_gather) places its miss copies when the
- * address-ordered miss layout takes its range schedule (host pools of 40 GiB or more over the call's
- * layers).  0 (the default): SM partition -- the CTAs on one SM in eight copy misses, a bucket of host
- * rows per warp at a time, and the others stream the HBM rows; whichever finishes first takes the other
- * kind of work.  1 or 2: that many miss warps in every CTA, each reading a contiguous block of buckets,
- * beside the HBM warps.  Results are identical.  Other layouts always use one miss warp per CTA.
+/* How the fused gather (hs_gather_planned, hs_resolve_gather) places its miss copies.
+ *   0   SM partition: the CTAs on one SM in six (hs_pool_set_miss_sm_divisor) copy misses, a bucket of
+ *       host rows (range schedule) or a chunk of a unit's miss list (per-unit lists) per warp at a time,
+ *       and the others stream the HBM rows; a CTA that runs out of its own kind of work takes the other.
+ *   1, 2  that many miss warps in every CTA beside the HBM warps (the range schedule's warps each read a
+ *       contiguous block of buckets).
+ *   -1  the default: the SM partition with the range schedule (host pools from 40 GiB), one miss warp in
+ *       every CTA with per-unit lists.
+ * The spread schedule always uses one miss warp in every CTA.  Results are identical.
  * HS_ERR_INVALID_ARG for another value. */
 hs_status hs_pool_set_miss_warps(hs_pool* pool, int32_t warps);
 

@@ -205,8 +205,8 @@ class Pool:
         _check(lib().hs_pool_set_gather_copy(self.handle, int(mode)), "hs_pool_set_gather_copy")
 
     def set_miss_warps(self, warps: int) -> None:
-        """Fused gather under the range schedule: 0 = SM partition (default), 1 or 2 = that many miss warps
-        in every CTA; see hs_pool_set_miss_warps."""
+        """Fused gather: -1 = default, 0 = SM partition, 1 or 2 = that many miss warps in every CTA; see
+        hs_pool_set_miss_warps."""
         _check(lib().hs_pool_set_miss_warps(self.handle, int(warps)), "hs_pool_set_miss_warps")
 
     def set_gather_planes(self, plane_bytes=()) -> None:

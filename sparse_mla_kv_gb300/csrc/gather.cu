@@ -366,7 +366,18 @@ __device__ __noinline__ void miss_warp_ranges(const MissOrder ord, int pu, int m
 // warp joining the misses 2.82 ms.  The misses end last: the HBM rows are done after about 2.0 ms.
 constexpr int kMissSmDivisor = 6;
 constexpr int kOvUnit = 64;          // overflow entries per work unit
+constexpr int kListChunk = 16;       // per-unit lists: misses per work unit
 constexpr int kHbmChunk = 8192;      // 16-byte output chunks per HBM work unit (128 KB)
+
+// What the partition's miss warps copy: the range schedule's buckets (ord.cnt set), else the resolver's
+// per-unit miss lists; and the work counters.
+struct PartitionWork {
+  MissOrder ord;
+  const int32_t* miss_count;  // per-unit lists: misses of each (index group, request) unit
+  const int4* miss_list;      // [units][max_m] entries
+  int32_t max_m;
+  int32_t* queues;            // kQueueInts counters: miss units, finished CTAs, HBM chunks, miss CTAs
+};
 
 __device__ __forceinline__ unsigned sm_id() {
   unsigned r;
@@ -385,17 +396,10 @@ __device__ __forceinline__ int partition_layer_units(const MissOrder& ord, int n
   return kMissBuckets + ov_units;
 }
 
-// One warp copies the entries of miss unit i (bucket or overflow slice) of group pu.
-template <int CPR>
-__device__ __forceinline__ void partition_miss_unit(const MissOrder ord, int i, int pu,
-                                                 const uint8_t* __restrict__ host, uint8_t* __restrict__ pool,
-                                                 const MissOut<CPR> om, const int32_t* __restrict__ lmsrc, int n,
-                                                 int row_bytes, int64_t per_layer, int64_t num_rows,
-                                                 int64_t num_host_rows) {
-  const int lane = threadIdx.x & 31;
+// The entries of range-schedule unit i of group pu: bucket i (address order), or overflow slice
+// i - kMissBuckets, as src[0, nb).
+__device__ __forceinline__ void partition_unit_range(const MissOrder& ord, int i, int pu, const int4*& src, int& nb) {
   const int32_t* cntg = ord.cnt + (int64_t)pu * (kMissBuckets + 1);
-  const int4* src;
-  int nb;
   if (i < kMissBuckets) {
     nb = min(__ldcg(cntg + i), ord.cap);
     src = ord.buckets + ((int64_t)pu * kMissBuckets + i) * ord.cap;
@@ -404,18 +408,13 @@ __device__ __forceinline__ void partition_miss_unit(const MissOrder ord, int i, 
     nb = max(0, min(kOvUnit, min(__ldcg(cntg + kMissBuckets), ord.per_group) - o0));
     src = ord.overflow + (int64_t)pu * ord.per_group + o0;
   }
-  for (int j = 0; j < nb; j += kMissRowsPerItem) {
-    const int nrows = min(kMissRowsPerItem, nb - j);
-    const int4 ent = lane < nrows ? src[j + lane] : make_int4(0, 0, 0, 0);
-    copy_miss_item<CPR>(host, pool, om, lmsrc, n, ent, nrows, row_bytes, per_layer, num_rows, num_host_rows);
-  }
 }
 
 // The whole CTA: HBM chunks until the queue is empty.  Chunk unit c covers 16-byte output chunks
 // [(c / nl) * kHbmChunk, ...) of layer c % nl; every position the miss warps do not own is written.
 template <int CPR, bool kPlanes>
 __device__ __forceinline__ void partition_hbm(const LayerPtrs& ptrs, int32_t layer_begin, int32_t group, int nl,
-                                              const MissOrder& ord, const int32_t* __restrict__ msrc,
+                                              int32_t* queues, const int32_t* __restrict__ msrc,
                                               uint8_t* __restrict__ out, int64_t per_layer, int row_bytes,
                                               int64_t num_rows, const OutPlanes& pl) {
   const int cpr = CPR ? CPR : (row_bytes >> 4);
@@ -424,7 +423,7 @@ __device__ __forceinline__ void partition_hbm(const LayerPtrs& ptrs, int32_t lay
   __shared__ int64_t s_unit;
   for (;;) {
     __syncthreads();  // every thread has read the previous unit
-    if (threadIdx.x == 0) s_unit = (int64_t)atomicAdd(reinterpret_cast<unsigned int*>(ord.queues + 2), 1u);
+    if (threadIdx.x == 0) s_unit = (int64_t)atomicAdd(reinterpret_cast<unsigned int*>(queues + 2), 1u);
     __syncthreads();
     const int64_t c = s_unit;
     if (c >= units) break;
@@ -468,23 +467,54 @@ __device__ __forceinline__ void partition_hbm(const LayerPtrs& ptrs, int32_t lay
   }
 }
 
-// A warp's share of the miss units: it takes units until the counter passes the end.  Unit u is unit
-// u % upl of layer u / upl (layer after layer).
+// A warp's share of the miss units: it takes units until the counter passes the end, layer after layer.
+// Range schedule: unit u is unit u % upl (a bucket, then an overflow slice) of layer u / upl.  Per-unit
+// lists: the units of a layer are chunks of kListChunk misses of its group's lists, chunk-major (chunk
+// c of request r is unit c * R + r), up to the most misses any list of the call holds.
 template <int CPR>
 __device__ __forceinline__ void partition_misses(const LayerPtrs& ptrs, int32_t layer_begin, int32_t group, int nl,
-                                                 const MissOrder& ord, const int32_t* __restrict__ msrc,
+                                                 int R, const PartitionWork& pw, const int32_t* __restrict__ msrc,
                                                  uint8_t* __restrict__ out, int n, int64_t per_layer, int row_bytes,
                                                  int64_t num_rows, int64_t num_host_rows, const OutPlanes& pl) {
-  const int upl = partition_layer_units(ord, nl, group), units = nl * upl;
+  const int lane = threadIdx.x & 31;
+  const bool lists = pw.ord.cnt == nullptr;
+  int upl;
+  if (lists) {
+    int m = 0;
+    const int ngroups = (nl + group - 1) / group;
+    for (int k = lane; k < ngroups * R; k += 32) m = max(m, __ldcg(pw.miss_count + k));
+    m = min(__reduce_max_sync(kFull, m), pw.max_m);
+    upl = R * ((m + kListChunk - 1) / kListChunk);
+  } else {
+    upl = partition_layer_units(pw.ord, nl, group);
+  }
+  const int units = nl * upl;
   for (;;) {
     int u = 0;
-    if ((threadIdx.x & 31) == 0) u = atomicAdd(ord.queues, 1);
+    if (lane == 0) u = atomicAdd(pw.queues, 1);
     u = __shfl_sync(kFull, u, 0);
     if (u >= units) break;
-    const int l = u / upl, pu = l / group;
+    const int l = u / upl, pu = l / group, i = u - l * upl;
+    // the unit's entries: src[0, nb)
+    const int4* src;
+    int nb;
+    if (lists) {
+      const int c = i / R, r = i - c * R;
+      const int cnt = min(__ldcg(pw.miss_count + (int64_t)pu * R + r), pw.max_m);
+      const int j0 = c * kListChunk;
+      nb = max(0, min(kListChunk, cnt - j0));
+      src = pw.miss_list + ((int64_t)pu * R + r) * pw.max_m + j0;
+    } else {
+      partition_unit_range(pw.ord, i, pu, src, nb);
+    }
     const MissOut<CPR> om = miss_out<CPR>(out + (int64_t)l * per_layer * row_bytes, per_layer, row_bytes, pl);
-    partition_miss_unit<CPR>(ord, u - l * upl, pu, ptrs.host[layer_begin + l], ptrs.gpu[layer_begin + l], om,
-                             msrc + (int64_t)pu * per_layer, n, row_bytes, per_layer, num_rows, num_host_rows);
+    const int32_t* lmsrc = msrc + (int64_t)pu * per_layer;
+    for (int j = 0; j < nb; j += kMissRowsPerItem) {
+      const int nrows = min(kMissRowsPerItem, nb - j);
+      const int4 ent = lane < nrows ? src[j + lane] : make_int4(0, 0, 0, 0);
+      copy_miss_item<CPR>(ptrs.host[layer_begin + l], ptrs.gpu[layer_begin + l], om, lmsrc, n, ent, nrows, row_bytes,
+                          per_layer, num_rows, num_host_rows);
+    }
   }
 }
 
@@ -557,26 +587,41 @@ __device__ __noinline__ void miss_warp_lists(const int32_t* __restrict__ miss_co
 // misses (the path a launch whose CTAs miss every miss SM takes).
 template <int CPR, bool kPlanes>
 __global__ void __launch_bounds__(kGatherThreads, 4) gather_partition_kernel(
-    const LayerPtrs ptrs, int32_t layer_begin, int32_t group, int32_t R, int32_t n, const MissOrder ord,
+    const LayerPtrs ptrs, int32_t layer_begin, int32_t group, int32_t R, int32_t n, const PartitionWork pw,
     const int32_t* __restrict__ msrc, uint8_t* __restrict__ out, int32_t row_bytes, int64_t num_rows,
     int64_t num_host_rows, int miss_sm_div, const OutPlanes pl) {
+  pdl_wait_prerequisites();   // per-unit lists: launched early, the plan must be complete and visible
   const int nl = gridDim.y;
   const int64_t per_layer = (int64_t)R * n;
   // CTAs on a miss SM register, copy misses, then help with the HBM rows; the others stream HBM rows and
   // take misses only when no miss CTA has registered (queues[3] counts them)
   const bool miss_sm = miss_sm_div > 0 && sm_id() % (unsigned)miss_sm_div == 0;
   if (miss_sm) {
-    if (threadIdx.x == 0) atomicAdd(ord.queues + 3, 1);
-    partition_misses<CPR>(ptrs, layer_begin, group, nl, ord, msrc, out, n, per_layer, row_bytes, num_rows,
+    if (threadIdx.x == 0) atomicAdd(pw.queues + 3, 1);
+    partition_misses<CPR>(ptrs, layer_begin, group, nl, R, pw, msrc, out, n, per_layer, row_bytes, num_rows,
                           num_host_rows, pl);
   }
-  partition_hbm<CPR, kPlanes>(ptrs, layer_begin, group, nl, ord, msrc, out, per_layer, row_bytes, num_rows, pl);
-  if (miss_sm) return;
-  int no_miss_cta = 0;  // decided once per warp: the miss loop below is warp-synchronous
-  if ((threadIdx.x & 31) == 0) no_miss_cta = *reinterpret_cast<volatile int32_t*>(ord.queues + 3) == 0;
-  if (__shfl_sync(kFull, no_miss_cta, 0))
-    partition_misses<CPR>(ptrs, layer_begin, group, nl, ord, msrc, out, n, per_layer, row_bytes, num_rows,
-                          num_host_rows, pl);
+  partition_hbm<CPR, kPlanes>(ptrs, layer_begin, group, nl, pw.queues, msrc, out, per_layer, row_bytes, num_rows, pl);
+  if (!miss_sm) {
+    int no_miss_cta = 0;  // decided once per warp: the miss loop below is warp-synchronous
+    if ((threadIdx.x & 31) == 0) no_miss_cta = *reinterpret_cast<volatile int32_t*>(pw.queues + 3) == 0;
+    if (__shfl_sync(kFull, no_miss_cta, 0))
+      partition_misses<CPR>(ptrs, layer_begin, group, nl, R, pw, msrc, out, n, per_layer, row_bytes, num_rows,
+                            num_host_rows, pl);
+  }
+  // the last CTA to finish zeroes the counters, so that the next launch on this workspace (a replay of
+  // the same plan) starts from zero; every other CTA is done with them when it counts itself finished
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(pw.queues + 1, 1) == (int)(gridDim.x * gridDim.y) - 1) {
+      pw.queues[0] = 0;
+      pw.queues[2] = 0;
+      pw.queues[3] = 0;
+      __threadfence();
+      pw.queues[1] = 0;
+    }
+  }
 }
 
 template <int CPR, bool kPlanes>
@@ -752,15 +797,18 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
                                 int32_t n, int32_t max_m, const int32_t* rows, const int32_t* miss_count,
                                 const int4* miss_list, const MissOrder& ord, const int32_t* msrc, uint8_t* out,
                                 int32_t row_bytes, int64_t num_rows, int64_t num_host_rows, int range_miss_warps,
-                                int miss_sm_div, const OutPlanes& planes, int sms, cudaStream_t s) {
+                                int miss_sm_div, const OutPlanes& planes, int32_t* queues, int sms, cudaStream_t s) {
   // kernel variant: 656-byte rows, any row size, any row size in planes
   const int var = planes.n ? 2 : (row_bytes == 656 ? 0 : 1);
   auto kern = var == 0 ? gather_fused_kernel<41, false>
                        : (var == 1 ? gather_fused_kernel<0, false> : gather_fused_kernel<0, true>);
-  // range schedule: 0 = SM partition, else that many miss warps in every CTA; one otherwise
-  const int nmiss = (ord.cnt && ord.ranges)
-                        ? (range_miss_warps <= 0 ? 0 : (range_miss_warps >= kMaxMissWarps ? kMaxMissWarps : 1))
-                        : 1;
+  // the pool's choice (range_miss_warps): -1 (default) the SM partition with the range schedule and one miss
+  // warp in every CTA otherwise; 0 the SM partition with the range schedule or per-unit lists; 1 or 2
+  // miss warps in every CTA.  The spread schedule keeps one miss warp in every CTA.
+  const bool ranges = ord.cnt && ord.ranges, lists = !ord.cnt;
+  const int mw = range_miss_warps;
+  const int nmiss = ((ranges && mw <= 0) || (lists && mw == 0)) ? 0
+                    : ((ranges || lists) && mw >= kMaxMissWarps ? kMaxMissWarps : 1);
   const int64_t per_layer = (int64_t)R * n * (row_bytes >> 4);
   const int64_t want_hbm = (per_layer + (int64_t)kGatherThreads * kGatherUnroll - 1) /
                            ((int64_t)kGatherThreads * kGatherUnroll);
@@ -775,16 +823,21 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
   // decode over a 29 GB pool, 684 us per step against 333 us with the launch held back).
   cudaError_t e;
   if (nmiss == 0) {
-    // SM partition: one full wave; its work counters start at zero in every launch
+    // SM partition: one full wave; its work counters were zeroed by the resolver (and again by the last
+    // CTA of the previous launch on this workspace).  Launched early only with per-unit lists.
     auto pkern = var == 0 ? gather_partition_kernel<41, false>
                           : (var == 1 ? gather_partition_kernel<0, false> : gather_partition_kernel<0, true>);
     const dim3 pgrid = wave_grid(sms, resident_blocks(pkern, &g_occ_partition[var]), (int64_t)1 << 40, nl);
-    e = cudaMemsetAsync(ord.queues, 0, kQueueInts * sizeof(int32_t), s);
-    if (e != cudaSuccess) return e;
-    pkern<<<pgrid, kGatherThreads, 0, s>>>(ptrs, layer_begin, group, R, n, ord, msrc, out, row_bytes, num_rows,
-                                           num_host_rows, miss_sm_div >= 2 ? miss_sm_div : (miss_sm_div < 0 ? 0 : kMissSmDivisor),
-                                           planes);
-    e = cudaGetLastError();
+    const PartitionWork pw{ord, miss_count, miss_list, max_m, queues};
+    const int div = miss_sm_div >= 2 ? miss_sm_div : (miss_sm_div < 0 ? 0 : kMissSmDivisor);
+    if (lists) {
+      e = launch_dependent(pkern, pgrid, dim3(kGatherThreads), 0, s, ptrs, layer_begin, group, R, n, pw, msrc, out,
+                           row_bytes, num_rows, num_host_rows, div, planes);
+    } else {
+      pkern<<<pgrid, kGatherThreads, 0, s>>>(ptrs, layer_begin, group, R, n, pw, msrc, out, row_bytes, num_rows,
+                                             num_host_rows, div, planes);
+      e = cudaGetLastError();
+    }
   } else if (ord.cnt) {
     kern<<<grid, kGatherThreads, 0, s>>>(ptrs, layer_begin, group, R, n, max_m, rows, miss_count, miss_list, ord, msrc,
                                          out, row_bytes, num_rows, num_host_rows, nmiss, planes);

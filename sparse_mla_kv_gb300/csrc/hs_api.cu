@@ -13,7 +13,7 @@ struct hs_pool {
   int device;
   int32_t miss_order;   // HS_MISS_ORDER_*
   int32_t gather_copy;  // HS_GATHER_COPY_*
-  int32_t miss_warps;   // fused gather, range schedule: 0 = SM partition, 1 or 2 = miss warps in every CTA
+  int32_t miss_warps;   // fused gather: -1 default, 0 SM partition, 1 or 2 miss warps in every CTA
   int32_t miss_sm_div;  // SM partition: every miss_sm_div-th SM copies misses (0 = the library's default, -1 none)
   int32_t miss_prefetch;  // HS_MISS_PREFETCH_*
   hs::OutPlanes planes;   // output layout of the gathers (planes.n = 0: rows)
@@ -133,6 +133,7 @@ hs_status hs_pool_create(const hs_pool_desc* d, hs_pool** out) {
   hs_pool* p = new (std::nothrow) hs_pool;
   if (!p) return HS_ERR_INVALID_ARG;
   std::memset(p, 0, sizeof(*p));
+  p->miss_warps = -1;
   p->g = {d->num_layers, d->page_size, d->row_bytes, d->num_gpu_blocks, d->num_host_blocks};
   if (cudaGetDevice(&p->device) != cudaSuccess) {
     cudaGetLastError();
@@ -184,7 +185,7 @@ hs_status hs_pool_set_gather_copy(hs_pool* pool, int32_t mode) {
 }
 
 hs_status hs_pool_set_miss_warps(hs_pool* pool, int32_t warps) {
-  if (!pool || warps < 0 || warps > 2) return HS_ERR_INVALID_ARG;
+  if (!pool || warps < -1 || warps > 2) return HS_ERR_INVALID_ARG;
   pool->miss_warps = warps;
   return HS_OK;
 }
@@ -345,6 +346,7 @@ hs_status prepare_resolve(const hs_pool* pool, int32_t layer_begin, int32_t nl, 
   p.miss_list = reinterpret_cast<int4*>(static_cast<uint8_t*>(workspace) + hs::ws_counts_bytes((int64_t)ng * R));
   p.ord = hs::call_miss_order(pool, nl, ng, R, n, C, workspace, workspace_bytes);
   p.msrc = nullptr;
+  p.queues = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + hs::ws_queue_offset((int64_t)ng * R, n, C));
   if (pool->miss_prefetch != HS_MISS_PREFETCH_OFF && g.num_host_blocks > 0) {
     p.row_bytes = g.row_bytes;
     for (int l = 0; l < g.num_layers; ++l) p.host[l] = pool->ptrs.host[l];
@@ -424,7 +426,8 @@ hs_status hs_gather_planned(const hs_pool* pool, int32_t layer_begin, int32_t nl
       reinterpret_cast<const int4*>(ws + hs::ws_counts_bytes(units)), ord,
       reinterpret_cast<const int32_t*>(ws + hs::ws_msrc_offset(units, n, capacity)), static_cast<uint8_t*>(out),
       g.row_bytes, (int64_t)g.num_gpu_blocks * g.page_size, (int64_t)g.num_host_blocks * g.page_size,
-      pool->miss_warps, pool->miss_sm_div, pool->planes, sms, stream));
+      pool->miss_warps, pool->miss_sm_div, pool->planes,
+      reinterpret_cast<int32_t*>(const_cast<uint8_t*>(ws) + hs::ws_queue_offset(units, n, capacity)), sms, stream));
 }
 
 hs_status hs_resolve_gather(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P, int32_t K,

@@ -139,11 +139,12 @@ struct MissOrder {
   int32_t per_group;  // misses an index group can have: R * max_m
   int32_t ranges;     // 1: each copy warp takes whole buckets (ranges); 0: 4-entry items in bucket order,
                       // spread over all copy warps
-  int32_t* queues;    // range schedule, SM partition: the fused gather's work counters (kQueueInts ints,
-                      // zeroed before each launch)
 };
-constexpr int kQueueInts = 4;            // miss buckets, overflow units, HBM chunks, spare
-constexpr size_t kQueueBytes = 256;      // their room at the end of the ordered layout
+// The SM partition's work counters (miss units, finished CTAs, HBM chunks, registered miss CTAs), at the
+// end of the per-unit workspace layout.  The resolver zeroes them; the partition gather's last CTA
+// zeroes them again, so that the plan's gather can be replayed.
+constexpr int kQueueInts = 4;
+constexpr size_t kQueueBytes = 256;
 // Host pools at least this large (over the layers of a call) are copied bucket by bucket, each bucket by
 // one warp; smaller ones with the items of all buckets spread over every copy warp.  Measured with the
 // library's miss path (131K misses per step, one layer): over spans up to 20 GB the spread items keep
@@ -168,6 +169,10 @@ inline size_t ws_counts_bytes(int64_t units) { return (4 * (size_t)units + 15) &
 inline size_t ws_msrc_offset(int64_t units, int64_t n, int64_t C) {
   const int64_t max_m = n < C ? n : C;
   return ws_counts_bytes(units) + 16 * (size_t)units * (size_t)max_m;
+}
+// [miss counts][miss lists][per-position sources][work counters]: the counters' offset.
+inline size_t ws_queue_offset(int64_t units, int64_t n, int64_t C) {
+  return ws_msrc_offset(units, n, C) + ((4 * (size_t)units * (size_t)n + 15) & ~size_t(15));
 }
 // The ordered layout's extra areas follow the per-unit layout (resolve_workspace_bytes): bucket
 // counters, then the buckets; its overflow lists reuse the per-unit miss lists (group g's at unit
@@ -213,6 +218,7 @@ struct ResolveParams {
   //   position of the following repeat, -1 after the last).  A miss entry's fourth field is its first
   //   repeat (-1: none), so the repeats form a chain that starts at the entry.
   int32_t* msrc;
+  int32_t* queues;  // the SM partition's work counters, zeroed by the resolver (kQueueInts ints)
   // Miss prefetch (row_bytes > 0): each miss's host row is prefetched into L2, in every layer of its
   // index group, as soon as the resolver classifies it (host[l] is layer l's host pool).
   int32_t row_bytes;
@@ -265,7 +271,7 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
                                 int32_t n, int32_t max_m, const int32_t* rows, const int32_t* miss_count,
                                 const int4* miss_list, const MissOrder& ord, const int32_t* msrc, uint8_t* out,
                                 int32_t row_bytes, int64_t num_rows, int64_t num_host_rows, int range_miss_warps,
-                                int miss_sm_div, const OutPlanes& planes, int sms, cudaStream_t s);
+                                int miss_sm_div, const OutPlanes& planes, int32_t* queues, int sms, cudaStream_t s);
 cudaError_t launch_offload(const LayerPtrs& ptrs, const PoolGeom& g, const int32_t* gpu_blocks,
                            const int32_t* host_blocks, int32_t n, int32_t* status, int sms, cudaStream_t s);
 cudaError_t launch_fill_i32(int32_t* a, int64_t count, int32_t value, int sms, cudaStream_t s);

@@ -271,6 +271,7 @@ __global__ void __launch_bounds__(kT, kResolveThreads / kT) resolve_kernel(const
   pdl_allow_dependents();   // the following gather / miss-copy kernel may place its CTAs now
   const int unit = blockIdx.x;
   const int lr = unit / p.R, r = unit - lr * p.R;
+  if (unit == 0 && tid < kQueueInts && p.queues) p.queues[tid] = 0;  // the fused gather's work counters
   const int grp = p.layer_begin + lr;  // index group (a layer when no layers share an indexer)
   const int n = p.n, C = p.C, step = p.step;
   const int S = kS ? kS : p.S;
@@ -922,14 +923,14 @@ ResolveSmem resolve_smem_plan_staged(int64_t n, int64_t C, int64_t S, int64_t ma
 
 size_t resolve_workspace_bytes(int64_t units, int64_t n, int64_t C) {
   // [miss counts, 16-byte aligned] [miss lists: units x min(n, C) int4] [per-position sources: units x n]
-  const int64_t max_m = n < C ? n : C;
-  return align16(4 * (size_t)units) + 16 * (size_t)units * (size_t)max_m + align16(4 * (size_t)units * (size_t)n);
+  // [the fused gather's work counters]
+  return ws_queue_offset(units, n, C) + kQueueBytes;
 }
 
 size_t resolve_workspace_bytes_ordered(int64_t groups, int64_t R, int64_t n, int64_t C) {
   const int64_t max_m = n < C ? n : C;
   return resolve_workspace_bytes(groups * R, n, C) + ws_order_cnt_bytes(groups) +
-         16 * (size_t)groups * kMissBuckets * (size_t)miss_bucket_cap(R * max_m) + kQueueBytes;
+         16 * (size_t)groups * kMissBuckets * (size_t)miss_bucket_cap(R * max_m);
 }
 
 MissOrder miss_order_layout(void* workspace, int64_t groups, int64_t R, int64_t n, int64_t C, int64_t num_host_rows) {
@@ -945,8 +946,6 @@ MissOrder miss_order_layout(void* workspace, int64_t groups, int64_t R, int64_t 
   o.shift = miss_bucket_shift(num_host_rows);
   o.cap = miss_bucket_cap(per_group);
   o.per_group = (int32_t)per_group;
-  o.queues = reinterpret_cast<int32_t*>(ws + base + ws_order_cnt_bytes(groups) +
-                                        16 * (size_t)groups * kMissBuckets * (size_t)o.cap);
   return o;
 }
 

@@ -20,13 +20,14 @@ class Rig:
         # "split" / "fused": the library's default miss layout for the pool (ordered only for large host
         # pools); a "+order" suffix forces the address-ordered layout on any pool, "+ranges" its range
         # schedule with the fused gather's default SM partition, "+ranges1" / "+ranges2" with one or two
-        # miss warps in every fused-gather CTA
+        # miss warps in every fused-gather CTA; "+part" keeps the default layout and asks for the SM
+        # partition (per-unit lists on small pools)
         base, _, opt = mode.partition("+")
-        assert base in ("split", "fused") and opt in ("", "order", "ranges", "ranges1", "ranges2")
+        assert base in ("split", "fused") and opt in ("", "order", "ranges", "ranges1", "ranges2", "part")
         self.mode = base
-        self.force_order = opt != ""
-        self.order_mode = hs.MISS_ORDER_ON if opt == "order" else (hs.MISS_ORDER_RANGES if opt else None)
-        self.miss_warps = {"ranges1": 1, "ranges2": 2}.get(opt, 0)
+        self.force_order = opt not in ("", "part")
+        self.order_mode = hs.MISS_ORDER_ON if opt == "order" else (hs.MISS_ORDER_RANGES if self.force_order else None)
+        self.miss_warps = {"ranges1": 1, "ranges2": 2, "ranges": 0, "part": 0}.get(opt, -1)
         self.graph = graph
         self.prep = None
         self.w = w
@@ -52,7 +53,7 @@ class Rig:
             self.pool.set_gather_planes(self.planes)
         if self.force_order:
             self.pool.set_miss_order(self.order_mode)
-            self.pool.set_miss_warps(self.miss_warps)
+        self.pool.set_miss_warps(self.miss_warps)
             self.pool.set_miss_sm_divisor(miss_sm_div)
         self.bt_np = w.block_table.copy()
         self.hbt_np = w.host_block_table.copy()

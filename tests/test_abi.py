@@ -65,15 +65,16 @@ def _ordered_extra(ng, R, P, K, C):
     # the even share of the group's R * min(P*K, C) possible misses, 16 B per entry
     per_group = R * min(P * K, C)
     cap = -(-2 * per_group // NB)
-    return -(-4 * ng * (NB + 1) // 16) * 16 + 16 * ng * NB * cap + 256   # + the fused gather's work counters
+    return -(-4 * ng * (NB + 1) // 16) * 16 + 16 * ng * NB * cap
 
 
 def test_size_queries(lib):
     # workspace: 16-byte-aligned miss counts + (host row, pool row, position) per possible miss
-    # (min(P*K, C) per unit, 16 B each) + one host source per position (16-byte aligned)
-    assert hs.resolve_workspace_bytes_min(1, 64, 1, 2048, 4096) == 256 + 16 * 64 * 2048 + 4 * 64 * 2048
-    assert hs.resolve_workspace_bytes_min(4, 256, 4, 2048, 4096) == 4096 + 16 * 1024 * 4096 + 4 * 1024 * 8192
-    assert hs.resolve_workspace_bytes_min(1, 3, 1, 5, 4) == 16 + 16 * 3 * 4 + 64
+    # (min(P*K, C) per unit, 16 B each) + one host source per position (16-byte aligned) + 256 B of
+    # the fused gather's work counters
+    assert hs.resolve_workspace_bytes_min(1, 64, 1, 2048, 4096) == 256 + 16 * 64 * 2048 + 4 * 64 * 2048 + 256
+    assert hs.resolve_workspace_bytes_min(4, 256, 4, 2048, 4096) == 4096 + 16 * 1024 * 4096 + 4 * 1024 * 8192 + 256
+    assert hs.resolve_workspace_bytes_min(1, 3, 1, 5, 4) == 16 + 16 * 3 * 4 + 64 + 256
     assert hs.resolve_workspace_bytes_min(1, 1, 0, 5, 4) == 0
     # the full size adds the address-ordered miss layout's room
     for shape in ((1, 64, 1, 2048, 4096), (4, 256, 4, 2048, 4096), (1, 3, 1, 5, 4), (16, 32, 1, 2048, 4096)):

@@ -29,7 +29,7 @@ from tests.casekit import Case, host_only_case
 pytestmark = pytest.mark.gpu
 
 MODES_ORDER = ["split", "fused", "split+order", "fused+order", "split+ranges", "fused+ranges", "fused+ranges1",
-               "fused+ranges2"]
+               "fused+ranges2", "fused+part"]
 INT32_MAX = 2**31 - 1
 
 
@@ -123,7 +123,9 @@ def _to_gpu(case, dev, mode):
     host = [torch.from_numpy(case.hosts[0].reshape(-1, S, B).copy()).pin_memory()]
     pool = hs.Pool(gpu, host)
     opt = mode.partition("+")[2]
-    if opt == "order":
+    if opt == "part":
+        pool.set_miss_warps(0)
+    elif opt == "order":
         pool.set_miss_order(hs.MISS_ORDER_ON)
     elif opt:
         pool.set_miss_order(hs.MISS_ORDER_RANGES)

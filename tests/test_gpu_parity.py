@@ -34,7 +34,7 @@ MODES = ["split", "fused"]
 # the same, plus both paths with the address-ordered miss layout forced on (small pools default to
 # per-unit lists)
 MODES_ORDER = MODES + ["split+order", "fused+order", "split+ranges", "fused+ranges", "fused+ranges1",
-                       "fused+ranges2"]
+                       "fused+ranges2", "fused+part"]
 
 
 def _base(mode):
@@ -44,9 +44,11 @@ def _base(mode):
 def _set_order(pool, mode):
     """+order: the address-ordered miss layout on any pool (its spread schedule on small pools);
     +ranges: its range schedule with the fused gather's default SM partition; +ranges1 / +ranges2: with one
-    or two miss warps in every fused-gather CTA."""
+    or two miss warps in every fused-gather CTA; +part: the default layout with the SM partition."""
     opt = mode.partition("+")[2]
-    if opt == "order":
+    if opt == "part":
+        pool.set_miss_warps(0)
+    elif opt == "order":
         pool.set_miss_order(hs.MISS_ORDER_ON)
     elif opt.startswith("ranges"):
         pool.set_miss_order(hs.MISS_ORDER_RANGES)
@@ -525,6 +527,9 @@ def test_miss_order_decision():
         pool.set_miss_order(5)
     with pytest.raises(hs.HSError):
         pool.set_miss_warps(3)
+    with pytest.raises(hs.HSError):
+        pool.set_miss_warps(-2)
+    pool.set_miss_warps(-1)
     for bad in (-2, 1, 33):
         with pytest.raises(hs.HSError):
             pool.set_miss_sm_divisor(bad)
@@ -625,7 +630,7 @@ def test_gather_planes_standalone(planes):
     pool.close()
 
 
-@pytest.mark.parametrize("mode", ["split", "fused", "fused+order", "fused+ranges", "fused+ranges1"])
+@pytest.mark.parametrize("mode", ["split", "fused", "fused+order", "fused+ranges", "fused+ranges1", "fused+part"])
 def test_planes_through_the_resolver(mode):
     """The fused gathers (per-unit lists, spread schedule, SM partition, mixed range layout) and the
     split path write the plane layout {512, 16, 128}: converted back to rows, every gathered byte, pool
