@@ -54,7 +54,7 @@ class Rig:
         if self.force_order:
             self.pool.set_miss_order(self.order_mode)
         self.pool.set_miss_warps(self.miss_warps)
-            self.pool.set_miss_sm_divisor(miss_sm_div)
+        self.pool.set_miss_sm_divisor(miss_sm_div)
         self.bt_np = w.block_table.copy()
         self.hbt_np = w.host_block_table.copy()
         self.bt = torch.from_numpy(self.bt_np).to(self.dev)
