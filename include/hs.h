@@ -221,10 +221,12 @@ hs_status hs_pool_set_gather_copy(hs_pool* pool, int32_t mode);
  *   0   SM partition: the CTAs on one SM in six (hs_pool_set_miss_sm_divisor) copy misses, a bucket of
  *       host rows (range schedule) or a chunk of a unit's miss list (per-unit lists) per warp at a time,
  *       and the others stream the HBM rows; a CTA that runs out of its own kind of work takes the other.
- *   1, 2  that many miss warps in every CTA beside the HBM warps (the range schedule's warps each read a
- *       contiguous block of buckets).
+ *   1, 2  with the range schedule, that many miss warps in every CTA beside the HBM warps, each reading a
+ *       contiguous block of buckets; with per-unit lists, one miss warp in every CTA.
  *   -1  the default: the SM partition with the range schedule (host pools from 40 GiB), one miss warp in
- *       every CTA with per-unit lists.
+ *       every CTA with per-unit lists.  Measured in one process (the planned gather replayed): full-size
+ *       MTP3 batch 2.62 ms partitioned against 3.32 ms with one miss warp per CTA; mixed-residency batch
+ *       63.1 against 61.1 us, cold start 127.7 against 126.6 us, tiny decode 21.1 against 10.9 us.
  * The spread schedule always uses one miss warp in every CTA.  Results are identical.
  * HS_ERR_INVALID_ARG for another value. */
 hs_status hs_pool_set_miss_warps(hs_pool* pool, int32_t warps);

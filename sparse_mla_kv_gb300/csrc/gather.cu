@@ -804,11 +804,11 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
                        : (var == 1 ? gather_fused_kernel<0, false> : gather_fused_kernel<0, true>);
   // the pool's choice (range_miss_warps): -1 (default) the SM partition with the range schedule and one miss
   // warp in every CTA otherwise; 0 the SM partition with the range schedule or per-unit lists; 1 or 2
-  // miss warps in every CTA.  The spread schedule keeps one miss warp in every CTA.
+  // miss warps in every CTA with the range schedule (one with lists: two were slower on the mixed batch).
+  // The spread schedule keeps one miss warp in every CTA.
   const bool ranges = ord.cnt && ord.ranges, lists = !ord.cnt;
   const int mw = range_miss_warps;
-  const int nmiss = ((ranges && mw <= 0) || (lists && mw == 0)) ? 0
-                    : ((ranges || lists) && mw >= kMaxMissWarps ? kMaxMissWarps : 1);
+  const int nmiss = ((ranges && mw <= 0) || (lists && mw == 0)) ? 0 : (ranges && mw >= kMaxMissWarps ? kMaxMissWarps : 1);
   const int64_t per_layer = (int64_t)R * n * (row_bytes >> 4);
   const int64_t want_hbm = (per_layer + (int64_t)kGatherThreads * kGatherUnroll - 1) /
                            ((int64_t)kGatherThreads * kGatherUnroll);
