@@ -100,6 +100,9 @@ def parse():
                          "prefetch off and on (hs_pool_set_miss_prefetch), in this process")
     ap.add_argument("--miss-prefetch", choices=["off", "on"], default="off",
                     help="the resolver's miss prefetch for the timed passes (hs_pool_set_miss_prefetch)")
+    ap.add_argument("--gather-phases", action="store_true",
+                    help="after the timed passes, replay the last timed step's planned gather with the SM partition's "
+                         "device timestamps on (hs_pool_set_phase_timestamps): when its HBM rows and its misses end")
     ap.add_argument("--planes-ab", action="store_true",
                     help="after the timed passes, replay the last timed step's gather with the output in rows and in "
                          "the planes {512, 16, 128} (hs_pool_set_gather_planes), alternating, in this process")
@@ -838,6 +841,39 @@ def run_ours(args, ws, rank, local):
                       "gather_us_median": {str(d): round(1e6 * statistics.median(t_div[d]), 1) for d in divs},
                       "how": "hs_gather_planned of the last timed step replayed with the SM partition, every divisor-th "
                              "SM copying misses (hs_pool_set_miss_sm_divisor), alternating behind L2 flushes; medians"}
+    gather_phases = None
+    if args.gather_phases and fused:
+        # the last timed step's planned gather replayed in the SM partition with device timestamps: start,
+        # the last HBM-row CTA's end, the last miss warp's end and the last CTA's end (globaltimer, ns)
+        ts = torch.zeros(4, dtype=torch.int64, device=dev)
+        pool.set_phase_timestamps(ts)
+        pool.set_miss_warps(0)
+        reps = max(5, K)
+        rec = []
+        for rep in range(reps + 1):
+            ts.zero_()
+            ts[0] = -1   # all ones: the atomic minimum of the CTAs' starts
+            flush.fill_(rep & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            phase2()
+            e1.record(stream)
+            e1.synchronize()
+            t = ts.cpu().tolist()
+            if rep and t[3] > 0:
+                rec.append((e0.elapsed_time(e1) * 1e3, (t[1] - t[0]) / 1e3 if t[1] else None,
+                            (t[2] - t[0]) / 1e3 if t[2] else None, (t[3] - t[0]) / 1e3))
+        pool.set_phase_timestamps(None)
+        pool.set_miss_warps(args.miss_warps)
+
+        def med(j):
+            v = [r[j] for r in rec if r[j] is not None]
+            return round(statistics.median(v), 1) if v else None
+        gather_phases = {"repeats": len(rec), "miss_order": miss_order, "event_us": med(0), "hbm_rows_done_us": med(1),
+                         "misses_done_us": med(2), "kernel_us": med(3),
+                         "how": "hs_gather_planned of the last timed step replayed in the SM partition with "
+                                "hs_pool_set_phase_timestamps; medians of the device timestamps relative to the first "
+                                "CTA's start, and of the events around the launch"}
     planes_ab = None
     if args.planes_ab and B == 656:
         # the last timed step's gather (planned gather when fused, plain gather of its rows otherwise)
@@ -1077,6 +1113,7 @@ def run_ours(args, ws, rank, local):
             "gathered_gbs": value * B / 1e9, "roofline": roofline, "step_roofline": step_roof,
             "cpu_baseline": cpu, "cpu_baseline_1thread": cpu1, "e2e": e2e, "gpu_launches": int(launches),
             "graph_replay": graph, "gather_copy_ab": gather_ab, "miss_warps_ab": miss_warps_ab, "miss_sm_ab": miss_sm_ab, "planes_ab": planes_ab,
+            "gather_phases": gather_phases,
             "schedule_ab": schedule_ab, "prefetch_ab": prefetch_ab,
             "clocks": clocks,
             "wall_s_timed_region": wall, "timed_counts": {"resident": int(hits_misses[0]),

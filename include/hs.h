@@ -172,6 +172,15 @@ size_t hs_resolve_workspace_bytes_min(int32_t nl, int32_t R, int32_t P, int32_t 
 #define HS_MISS_ORDER_SPREAD 4
 hs_status hs_pool_set_miss_order(hs_pool* pool, int32_t mode);
 
+/* Diagnostics of the fused gather's SM partition.  With device_ts set (device memory, 4 x uint64,
+ * 16-byte aligned; NULL turns it off, the default) every partition launch records %globaltimer
+ * nanoseconds there: [0] the earliest CTA start (atomic min), [1] the latest end of a CTA that streamed HBM
+ * rows, [2] the latest end of a miss warp's misses, [3] the latest CTA end (atomic max).  The caller sets
+ * [0] to all ones and [1..3] to zero before a launch and reads them after it; [2] - [0] against [1] - [0]
+ * shows which kind of traffic sets the gather's time.  The pages have no counterpart; results are
+ * unchanged.  HS_ERR_INVALID_ARG for a misaligned pointer. */
+hs_status hs_pool_set_phase_timestamps(hs_pool* pool, unsigned long long* device_ts);
+
 /* Miss prefetch: with HS_MISS_PREFETCH_ON the resolver starts moving each miss's host row into L2
  * (one bulk L2 prefetch per row and layer of its index group) as soon as it classifies the id, before
  * it picks the victims, so that the copy that follows (the miss-copy kernel, or the fused gather's miss

@@ -92,6 +92,8 @@ def lib():
         L.hs_pool_set_miss_sm_divisor.argtypes = [p, i32]
         L.hs_pool_set_miss_prefetch.restype = i32
         L.hs_pool_set_miss_prefetch.argtypes = [p, i32]
+        L.hs_pool_set_phase_timestamps.restype = i32
+        L.hs_pool_set_phase_timestamps.argtypes = [p, ctypes.c_void_p]
         L.hs_pool_set_gather_planes.restype = i32
         L.hs_pool_set_gather_planes.argtypes = [p, i32, ctypes.POINTER(i32)]
         L.hs_resolve_miss_order.restype = i32
@@ -208,6 +210,15 @@ class Pool:
         """Fused gather: -1 = default, 0 = SM partition, 1 or 2 = that many miss warps in every CTA; see
         hs_pool_set_miss_warps."""
         _check(lib().hs_pool_set_miss_warps(self.handle, int(warps)), "hs_pool_set_miss_warps")
+
+    def set_phase_timestamps(self, ts: Optional[torch.Tensor]) -> None:
+        """ts: int64 CUDA tensor of 4 (or None to stop): the SM-partition gather's device timestamps; see
+        hs_pool_set_phase_timestamps."""
+        if ts is not None and (ts.dtype != torch.int64 or not ts.is_cuda or ts.numel() < 4 or not ts.is_contiguous()):
+            raise TypeError("ts must be a contiguous int64 CUDA tensor of at least 4 elements")
+        _check(lib().hs_pool_set_phase_timestamps(self.handle, ctypes.c_void_p(ts.data_ptr()) if ts is not None else None),
+               "hs_pool_set_phase_timestamps")
+        self._phase_ts = ts
 
     def set_gather_planes(self, plane_bytes=()) -> None:
         """Output layout of the gathers: () = rows; else the row cut into planes of these byte sizes

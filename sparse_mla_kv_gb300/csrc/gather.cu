@@ -377,7 +377,14 @@ struct PartitionWork {
   const int4* miss_list;      // [units][max_m] entries
   int32_t max_m;
   int32_t* queues;            // kQueueInts counters: miss units, finished CTAs, HBM chunks, miss CTAs
+  unsigned long long* phase_ts;  // optional (hs_pool_set_phase_timestamps): start, HBM rows done, misses done, end
 };
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ unsigned sm_id() {
   unsigned r;
@@ -413,7 +420,7 @@ __device__ __forceinline__ void partition_unit_range(const MissOrder& ord, int i
 // The whole CTA: HBM chunks until the queue is empty.  Chunk unit c covers 16-byte output chunks
 // [(c / nl) * kHbmChunk, ...) of layer c % nl; every position the miss warps do not own is written.
 template <int CPR, bool kPlanes>
-__device__ __forceinline__ void partition_hbm(const LayerPtrs& ptrs, int32_t layer_begin, int32_t group, int nl,
+__device__ __forceinline__ bool partition_hbm(const LayerPtrs& ptrs, int32_t layer_begin, int32_t group, int nl,
                                               int32_t* queues, const int32_t* __restrict__ msrc,
                                               uint8_t* __restrict__ out, int64_t per_layer, int row_bytes,
                                               int64_t num_rows, const OutPlanes& pl) {
@@ -421,12 +428,14 @@ __device__ __forceinline__ void partition_hbm(const LayerPtrs& ptrs, int32_t lay
   const int64_t total = per_layer * cpr;  // 16-byte chunks per layer
   const int64_t units = (total + kHbmChunk - 1) / kHbmChunk * nl;
   __shared__ int64_t s_unit;
+  bool worked = false;
   for (;;) {
     __syncthreads();  // every thread has read the previous unit
     if (threadIdx.x == 0) s_unit = (int64_t)atomicAdd(reinterpret_cast<unsigned int*>(queues + 2), 1u);
     __syncthreads();
     const int64_t c = s_unit;
     if (c >= units) break;
+    worked = true;
     const int l = (int)(c % nl);
     const int64_t c0 = (c / nl) * kHbmChunk, c1 = min(total, c0 + kHbmChunk);
     const uint8_t* __restrict__ pool = ptrs.gpu[layer_begin + l];
@@ -465,6 +474,7 @@ __device__ __forceinline__ void partition_hbm(const LayerPtrs& ptrs, int32_t lay
       }
     }
   }
+  return worked;
 }
 
 // A warp's share of the miss units: it takes units until the counter passes the end, layer after layer.
@@ -596,23 +606,30 @@ __global__ void __launch_bounds__(kGatherThreads, 4) gather_partition_kernel(
   // CTAs on a miss SM register, copy misses, then help with the HBM rows; the others stream HBM rows and
   // take misses only when no miss CTA has registered (queues[3] counts them)
   const bool miss_sm = miss_sm_div > 0 && sm_id() % (unsigned)miss_sm_div == 0;
+  if (pw.phase_ts && threadIdx.x == 0) atomicMin(pw.phase_ts, global_ns());
   if (miss_sm) {
     if (threadIdx.x == 0) atomicAdd(pw.queues + 3, 1);
     partition_misses<CPR>(ptrs, layer_begin, group, nl, R, pw, msrc, out, n, per_layer, row_bytes, num_rows,
                           num_host_rows, pl);
+    if (pw.phase_ts && (threadIdx.x & 31) == 0) atomicMax(pw.phase_ts + 2, global_ns());
   }
-  partition_hbm<CPR, kPlanes>(ptrs, layer_begin, group, nl, pw.queues, msrc, out, per_layer, row_bytes, num_rows, pl);
+  const bool hbm = partition_hbm<CPR, kPlanes>(ptrs, layer_begin, group, nl, pw.queues, msrc, out, per_layer,
+                                               row_bytes, num_rows, pl);
+  if (pw.phase_ts && hbm && threadIdx.x == 0) atomicMax(pw.phase_ts + 1, global_ns());
   if (!miss_sm) {
     int no_miss_cta = 0;  // decided once per warp: the miss loop below is warp-synchronous
     if ((threadIdx.x & 31) == 0) no_miss_cta = *reinterpret_cast<volatile int32_t*>(pw.queues + 3) == 0;
-    if (__shfl_sync(kFull, no_miss_cta, 0))
+    if (__shfl_sync(kFull, no_miss_cta, 0)) {
       partition_misses<CPR>(ptrs, layer_begin, group, nl, R, pw, msrc, out, n, per_layer, row_bytes, num_rows,
                             num_host_rows, pl);
+      if (pw.phase_ts && (threadIdx.x & 31) == 0) atomicMax(pw.phase_ts + 2, global_ns());
+    }
   }
   // the last CTA to finish zeroes the counters, so that the next launch on this workspace (a replay of
   // the same plan) starts from zero; every other CTA is done with them when it counts itself finished
   __syncthreads();
   if (threadIdx.x == 0) {
+    if (pw.phase_ts) atomicMax(pw.phase_ts + 3, global_ns());
     __threadfence();
     if (atomicAdd(pw.queues + 1, 1) == (int)(gridDim.x * gridDim.y) - 1) {
       pw.queues[0] = 0;
@@ -797,7 +814,8 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
                                 int32_t n, int32_t max_m, const int32_t* rows, const int32_t* miss_count,
                                 const int4* miss_list, const MissOrder& ord, const int32_t* msrc, uint8_t* out,
                                 int32_t row_bytes, int64_t num_rows, int64_t num_host_rows, int range_miss_warps,
-                                int miss_sm_div, const OutPlanes& planes, int32_t* queues, int sms, cudaStream_t s) {
+                                int miss_sm_div, const OutPlanes& planes, int32_t* queues,
+                                unsigned long long* phase_ts, int sms, cudaStream_t s) {
   // kernel variant: 656-byte rows, any row size, any row size in planes
   const int var = planes.n ? 2 : (row_bytes == 656 ? 0 : 1);
   auto kern = var == 0 ? gather_fused_kernel<41, false>
@@ -828,7 +846,7 @@ cudaError_t launch_gather_fused(const LayerPtrs& ptrs, int32_t layer_begin, int3
     auto pkern = var == 0 ? gather_partition_kernel<41, false>
                           : (var == 1 ? gather_partition_kernel<0, false> : gather_partition_kernel<0, true>);
     const dim3 pgrid = wave_grid(sms, resident_blocks(pkern, &g_occ_partition[var]), (int64_t)1 << 40, nl);
-    const PartitionWork pw{ord, miss_count, miss_list, max_m, queues};
+    const PartitionWork pw{ord, miss_count, miss_list, max_m, queues, phase_ts};
     const int div = miss_sm_div >= 2 ? miss_sm_div : (miss_sm_div < 0 ? 0 : kMissSmDivisor);
     if (lists) {
       e = launch_dependent(pkern, pgrid, dim3(kGatherThreads), 0, s, ptrs, layer_begin, group, R, n, pw, msrc, out,

@@ -17,6 +17,7 @@ struct hs_pool {
   int32_t miss_sm_div;  // SM partition: every miss_sm_div-th SM copies misses (0 = the library's default, -1 none)
   int32_t miss_prefetch;  // HS_MISS_PREFETCH_*
   hs::OutPlanes planes;   // output layout of the gathers (planes.n = 0: rows)
+  unsigned long long* phase_ts;  // optional device timestamps of the SM-partition gather
 };
 
 namespace hs {
@@ -205,6 +206,12 @@ hs_status hs_pool_set_gather_planes(hs_pool* pool, int32_t nplanes, const int32_
   pl.start[0] = 0;
   pl.n = nplanes;
   pool->planes = pl;
+  return HS_OK;
+}
+
+hs_status hs_pool_set_phase_timestamps(hs_pool* pool, unsigned long long* device_ts) {
+  if (!pool || (device_ts && !hs::aligned16(device_ts))) return HS_ERR_INVALID_ARG;
+  pool->phase_ts = device_ts;
   return HS_OK;
 }
 
@@ -427,7 +434,8 @@ hs_status hs_gather_planned(const hs_pool* pool, int32_t layer_begin, int32_t nl
       reinterpret_cast<const int32_t*>(ws + hs::ws_msrc_offset(units, n, capacity)), static_cast<uint8_t*>(out),
       g.row_bytes, (int64_t)g.num_gpu_blocks * g.page_size, (int64_t)g.num_host_blocks * g.page_size,
       pool->miss_warps, pool->miss_sm_div, pool->planes,
-      reinterpret_cast<int32_t*>(const_cast<uint8_t*>(ws) + hs::ws_queue_offset(units, n, capacity)), sms, stream));
+      reinterpret_cast<int32_t*>(const_cast<uint8_t*>(ws) + hs::ws_queue_offset(units, n, capacity)), pool->phase_ts,
+      sms, stream));
 }
 
 hs_status hs_resolve_gather(const hs_pool* pool, int32_t layer_begin, int32_t nl, int32_t R, int32_t P, int32_t K,

@@ -126,6 +126,7 @@ def test_calls_on_null_handles_are_rejected(lib):
     assert L.hs_pool_set_miss_sm_divisor(None, 6) == 1
     assert L.hs_pool_set_miss_prefetch(None, 1) == 1
     assert L.hs_pool_set_gather_planes(None, 0, None) == 1
+    assert L.hs_pool_set_phase_timestamps(None, None) == 1
     assert L.hs_resolve_miss_order(None, 0, 1, 1, 1, 1, ctypes.byref(hot), 1 << 30) == -1
     assert L.hs_resolve_workspace_bytes_min(1, 1, 0, 5, 4) == 0
     assert L.hs_resolve_workspace_bytes_min(1, 1, 1, 16385, 4) == 0   # plan beyond HS_MAX_PLAN

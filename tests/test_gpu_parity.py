@@ -3,6 +3,8 @@
 Compared on every step: out_rows, out_stats, slot_token, slot_stamp (oracle), gathered bytes
 (closed-form row contents), and pool bytes (oracle with byte pools) or hot-slot bytes (closed form).
 Tolerance is zero everywhere: this is integer and byte work."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -101,6 +103,27 @@ def test_sm_partition_divisors(div):
     rig = _rig(w, mode="fused+ranges", miss_sm_div=div)
     for st in w.iter_steps():
         rig.step(st)
+
+
+@pytest.mark.parametrize("div", [0, -1])
+def test_partition_phase_timestamps(div):
+    """hs_pool_set_phase_timestamps: every SM-partition launch records its start, the end of its HBM rows,
+    the end of its misses and its own end, in order, without changing any result (small MTP3 batch with
+    the range schedule; the default share of miss SMs and no miss SM)."""
+    w = workloads.config5(seed=11, R=6, L=2, steps=4)
+    rig = _rig(w, mode="fused+ranges", miss_sm_div=div)
+    ts = torch.zeros(4, dtype=torch.int64, device="cuda")
+    rig.pool.set_phase_timestamps(ts)
+    for st in w.iter_steps():
+        ts.zero_()
+        ts[0] = -1
+        _, stats, *_ = rig.step(st)
+        t = ts.cpu().tolist()
+        assert t[0] > 0 and t[3] >= t[1] >= t[0] and t[1] > 0, t
+        if int(stats[..., 3].sum()):
+            assert t[3] >= t[2] >= t[0] and t[2] > 0, t
+    rig.pool.set_phase_timestamps(None)
+    assert hs.lib().hs_pool_set_phase_timestamps(rig.pool.handle, ctypes.c_void_p(ts.data_ptr() + 8)) == 1
 
 
 @pytest.mark.parametrize("mode", MODES)
