@@ -133,7 +133,8 @@ hs_status hs_hot_reset_requests(const hs_pool* pool, const hs_hot_state* hot, in
 
 /* Bytes of caller-owned device workspace for hs_resolve_topk and hs_resolve_gather with this shape
  * (per-unit miss lists handed from the resolver kernel to the miss-copy kernel, per-position host
- * sources handed to the fused gather), including the room the address-ordered miss layout needs
+ * sources handed to the fused gather, 256 bytes of the fused gather's work counters, which the
+ * resolver zeroes), including the room the address-ordered miss layout needs
  * (hs_pool_set_miss_order).  nl counts resolver units per request: layers when G = 1, index groups
  * (layers / G) under IndexShare; passing the layer count there over-sizes the workspace, which is
  * harmless.  0 on a bad shape. */

@@ -143,3 +143,25 @@ def test_checked_build_exports_every_declared_symbol(lib):
         pytest.skip("no nm")
     out = subprocess.run([nm, "-D", "--defined-only", path], capture_output=True, text=True).stdout
     assert set(declared_functions()) <= set(re.findall(r"\b(hs_[a-z0-9_]+)\b", out))
+
+
+def test_plane_views_split_rows_without_copying():
+    """plane_views cuts a gather output written in planes into per-plane views: plane p of layer l is
+    the positions' bytes [c_p, c_p + w_p) laid out one plane after the other (CPU tensors here)."""
+    import torch
+    nl, n, planes = 2, 5, (512, 16, 128)
+    rows = torch.randint(0, 256, (nl, n, sum(planes)), dtype=torch.uint8)
+    cuts = [0, 512, 528, 656]
+    written = torch.cat([torch.cat([rows[l, :, cuts[p]:cuts[p + 1]].reshape(-1) for p in range(3)])
+                         for l in range(nl)]).reshape(nl, n, sum(planes))
+    views = hs.plane_views(written, planes)
+    assert [tuple(v.shape) for v in views] == [(nl, n, 512), (nl, n, 16), (nl, n, 128)]
+    assert torch.equal(torch.cat(views, dim=-1), rows)
+    assert all(v.data_ptr() >= written.data_ptr() for v in views)   # views into the same storage
+    one = hs.plane_views(written[0], planes)                         # a single layer
+    assert torch.equal(torch.cat(one, dim=-1), rows[0])
+    try:
+        hs.plane_views(written, (512, 16))
+        raise AssertionError("sizes that do not sum to the row were accepted")
+    except ValueError:
+        pass
