@@ -348,22 +348,23 @@ __device__ __noinline__ void miss_warp_ranges(const MissOrder ord, int pu, int m
   }
 }
 
-// ---- range schedule, SM partition (the default on large host pools).  Host reads and HBM rows slow
-// each other down when warps of both kinds share an SM, and the host reads are bound by the device's
-// translation of host addresses, which favours fewer host ranges in flight at a time.  So the CTAs on
-// every kMissSmDivisor-th SM (by %smid) copy misses with all their warps, one bucket per warp at a time,
-// layer after layer and in address order within a layer, while the CTAs on the other SMs stream the HBM
-// rows.  Work comes from counters shared by every layer of the launch: one of miss units (each layer's
-// buckets, then its overflow slices) and one of HBM chunks.  A miss CTA that finds no miss work left
-// joins the HBM rows; an HBM CTA joins the misses only if no CTA has registered as a miss CTA, so the
-// misses are always drained, whichever SMs the CTAs land on.
+// ---- SM partition (the default with the range schedule, on large host pools; optional with per-unit
+// lists).  Host reads and HBM rows slow each other down when warps of both kinds share an SM, and the host
+// reads are bound by the device's translation of host addresses, which favours fewer host ranges in flight
+// at a time.  So the CTAs on every kMissSmDivisor-th SM (by %smid) copy misses with all their warps, one
+// work unit per warp at a time (a bucket of the range schedule, in address order, or a chunk of a unit's
+// miss list), layer after layer, while the CTAs on the other SMs stream the HBM rows.  Work comes from
+// counters shared by every layer of the launch: one of miss units and one of HBM chunks.  A miss CTA
+// that finds no miss work left joins the HBM rows; an HBM CTA joins the misses only if no CTA has
+// registered as a miss CTA, so the misses are always drained, whichever SMs the CTAs land on.
 //
 // Measured on the full-size MTP3 batch (4 layers over 18 GB host pools each, 378K misses and 8.4M HBM
 // rows per step; medians of 20 replays of one planned gather in one process): one miss warp in every CTA
-// 3.30-3.36 ms; this layout 2.68 ms.  Variants of it: an eighth, seventh or fifth of the SMs for the
-// misses 2.89, 2.80 and 2.84 ms; buckets handed out over all layers at once 2.83 ms, and across 64
-// stripes of every pool 3.0-3.9 ms; a bucket split between 4 or 8 warps 3.8-4.0 ms; the HBM CTAs' first
-// warp joining the misses 2.82 ms.  The misses end last: the HBM rows are done after about 2.0 ms.
+// 3.20-3.32 ms, this layout 2.60-2.66 ms; every fifth, sixth, seventh or eighth SM for the misses 2.83,
+// 2.77, 2.79 and 2.86 ms.  In instrumented copies: buckets handed out over all layers at once 2.83 ms
+// (against 2.68), across 64 stripes of every pool 2.9-3.9 ms, a bucket split between 4 or 8 warps 3.8-4.0
+// ms, the HBM CTAs' first warp joining the misses 2.82 ms.  Its own timestamps put the end of the HBM rows
+// at 2.04 ms and the end of the misses at 2.76 ms: the misses set the time.
 constexpr int kMissSmDivisor = 6;
 constexpr int kOvUnit = 64;          // overflow entries per work unit
 constexpr int kListChunk = 16;       // per-unit lists: misses per work unit
