@@ -20,6 +20,10 @@
 //                      list); each layer's CTAs copy the misses into that layer's tensor.  With the
 //                      ordered miss layout each miss warp takes whole host-row ranges (buckets) and
 //                      reads them in address order.
+// gather_partition_kernel  the fused gather's SM partition: the CTAs on every sixth SM copy the misses,
+//                      the others stream the HBM rows (the default with the range schedule).
+// gather_bulk_kernel   the plain gather with one-dimensional bulk copies through shared memory.
+// Every gather writes rows, or the planes the pool asks for (hs_pool_set_gather_planes).
 #include "hs_internal.cuh"
 
 namespace hs {
