@@ -670,20 +670,16 @@ def run_ours(args, ws, rank, local):
             phase3(i)
         torch.cuda.synchronize()
 
-    # settle: untimed passes over the timed steps until two in a row agree within 5% and the last one
-    # has no stalled step (none over 1.5x its median), at most --settle-seconds.  On host pools of tens
-    # of GB the first seconds after pinning read unevenly on some machines, and reads of host memory stall
-    # for a while now and then; a long-running server sees the settled rate.
+    # settle: untimed passes over the timed steps until two in a row agree within 5% (at most
+    # --settle-seconds).  On host pools of tens of GB the first seconds after pinning read unevenly
+    # on some machines; a long-running server sees the settled rate.
     settle_medians = []
     t_settle = time.time()
     while True:
         replay_warmup()
         ev_u = timed_pass(split=False)
-        ts_u = [ev_u[k][0].elapsed_time(ev_u[k][2]) for k in range(K)]
-        settle_medians.append(statistics.median(ts_u))
-        calm = max(ts_u) <= 1.5 * settle_medians[-1]
-        if (len(settle_medians) >= 2 and abs(settle_medians[-1] - settle_medians[-2]) <= 0.05 * settle_medians[-2]
-                and calm):
+        settle_medians.append(statistics.median(ev_u[k][0].elapsed_time(ev_u[k][2]) for k in range(K)))
+        if len(settle_medians) >= 2 and abs(settle_medians[-1] - settle_medians[-2]) <= 0.05 * settle_medians[-2]:
             break
         if time.time() - t_settle > args.settle_seconds:
             break
