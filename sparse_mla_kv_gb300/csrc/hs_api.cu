@@ -428,12 +428,18 @@ hs_status hs_gather_planned(const hs_pool* pool, int32_t layer_begin, int32_t nl
   const int32_t max_m = (int32_t)(n < capacity ? n : capacity);
   const hs::MissOrder ord =
       hs::call_miss_order(pool, nl, nl / G, R, n, capacity, const_cast<void*>(workspace), workspace_bytes);
+  // The SM partition numbers its miss units with 32-bit counters: shapes whose unit count could come near
+  // 2^31 (per layer: 1024 buckets and 64-miss overflow slices, or 16-miss chunks of every unit's list) take
+  // one miss warp per CTA instead.
+  const int64_t miss_units =
+      (int64_t)nl * (ord.cnt ? 1024 + ((int64_t)R * max_m + 63) / 64 : (int64_t)R * ((max_m + 15) / 16));
+  const int32_t miss_warps = miss_units > (int64_t(1) << 30) && pool->miss_warps <= 0 ? 1 : pool->miss_warps;
   return hs::cuda_status(hs::launch_gather_fused(
       pool->ptrs, layer_begin, nl, G, R, (int32_t)n, max_m, out_rows, reinterpret_cast<const int32_t*>(ws),
       reinterpret_cast<const int4*>(ws + hs::ws_counts_bytes(units)), ord,
       reinterpret_cast<const int32_t*>(ws + hs::ws_msrc_offset(units, n, capacity)), static_cast<uint8_t*>(out),
       g.row_bytes, (int64_t)g.num_gpu_blocks * g.page_size, (int64_t)g.num_host_blocks * g.page_size,
-      pool->miss_warps, pool->miss_sm_div, pool->planes,
+      miss_warps, pool->miss_sm_div, pool->planes,
       reinterpret_cast<int32_t*>(const_cast<uint8_t*>(ws) + hs::ws_queue_offset(units, n, capacity)), pool->phase_ts,
       sms, stream));
 }
