@@ -447,6 +447,36 @@ def test_empty_and_degenerate_shapes():
     pool.close()
 
 
+@pytest.mark.parametrize("mode", ["fused", "fused+part", "fused+ranges", "fused+ranges1", "fused+order"])
+def test_degenerate_shapes_through_the_fused_layouts(mode):
+    """The fused gathers on degenerate steps: an empty plan (K = 0), an all-padding step (rows -1, zero
+    bytes), and a step that uses every hot slot (capacity exactly C): rows, stats and every gathered byte
+    equal the oracle's, in every miss layout (per-unit lists, SM partition, mixed range layout, spread)."""
+    dev = torch.device("cuda")
+    case = Case(R=2, S=4, B=16, C=8, max_pages=4, ctx=[16, 16], resident=True, host=True,
+                hot_blocks=[[0, 1], [2, 3]], num_gpu_blocks=6, num_host_blocks=8, bt=[[-1, -1, -1, 4], [-1, -1, -1, 5]],
+                hbt=[[0, 1, 2, 3], [4, 5, 6, 7]])
+    pool, gpu, host, hot = _case_to_gpu(case, dev)
+    _set_order(pool, mode)
+    bt, hbt = torch.from_numpy(case.bt).to(dev), torch.from_numpy(case.hbt).to(dev)
+    ctx = torch.from_numpy(case.ctx).to(dev)
+    rows, stats, out = hs.resolve_gather(pool, torch.zeros((1, 2, 1, 0), dtype=torch.int32, device=dev), bt, hbt,
+                                         ctx, hot, 0)
+    assert stats.cpu().tolist() == [[[0, 0, 0, 0], [0, 0, 0, 0]]] and out.numel() == 0
+    ids = torch.full((1, 2, 2, 3), -1, dtype=torch.int32, device=dev)
+    rows, stats, out = hs.resolve_gather(pool, ids, bt, hbt, ctx, hot, 1)
+    assert (rows == -1).all() and stats.cpu().tolist() == [[[0, 0, 0, 0], [0, 0, 0, 0]]]
+    assert int(out.count_nonzero()) == 0
+    ids = torch.tensor([[[[0, 1, 2, 3, 4, 5, 6, 7]], [[8, 9, 10, 11, 0, 1, 2, 3]]]], dtype=torch.int32, device=dev)
+    rows, stats, out = hs.resolve_gather(pool, ids, bt, hbt, ctx, hot, 2)
+    o_rows, o_stats = case.step(ids.cpu().numpy()[0], 2)
+    assert np.array_equal(stats.cpu().numpy(), o_stats) and np.array_equal(rows.cpu().numpy(), o_rows)
+    assert o_stats[0, :, 3].tolist() == [8, 8]
+    o_out, _ = case.gather(o_rows.reshape(1, -1))
+    assert np.array_equal(out.cpu().numpy().reshape(o_out.shape), o_out)
+    pool.close()
+
+
 def test_largest_shapes_and_shape_limits():
     """P*K = 8192 ids with C = 4096 (the MTP3 shape) and with C = 10240 (the pages' MTP sizing
     (num_spec + 2) * K), C = 8192 and the largest capacity C = 16384: parity over three steps; a shape
